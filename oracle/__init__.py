@@ -1,0 +1,16 @@
+"""CPU oracle for top-k sparse attention over a two-level KV cache.
+
+TEST INFRASTRUCTURE: imported only by the tests, the smoke check and the
+benchmark's CPU-baseline leg.  It shares no code with the CUDA library.
+"""
+from .hisparse_oracle import (  # noqa: F401
+    bf16_to_f64,
+    indexer_scores,
+    indexer_scores_many,
+    topk_select,
+    LRUHotCache,
+    belady_misses,
+    sparse_attention,
+    hot_over_full,
+    hot_cache_bytes,
+)

@@ -1,0 +1,251 @@
+"""Plain CPU oracle for one decode layer-step of top-k sparse attention over a
+two-level KV cache (HiSparse).
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the benchmark's
+CPU-baseline leg may import or run this module.  The CUDA library never calls
+it and shares no code with it; the two meet only at the seeded input generators
+in the ``workload`` package.
+
+What is computed, and where it is stated:
+
+* "KV卸载上主机:HiSparse、PDD与DDR4回收" (yeyulingfeng.com), section
+  "二、论文分析 / 论文1：HiSparse": an indexer tells every step which KV
+  positions it needs; the authoritative full KV lives in pinned host DRAM, the GPU
+  keeps B slots per request per layer, a page table plus LRU metadata drive
+  replacement, and only placement changes, so the result is exactly top-k sparse
+  attention over the full KV.
+* "10月14日学习笔记" (zgchen.com), section "HiSparse / 动机": the indexer picks
+  the top-k tokens; "方法" item 1: adjacent decode steps overlap, LRU fits best.
+* "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory for
+  Retrieval-Based Sparse Attention" (vsvnakers.github.io), section
+  "核心公式与算法", formula 2: Attention = softmax(QK^T / sqrt(d_k) (masked)) V.
+  The mask is printed as an elementwise product; read here as an additive
+  -inf mask, i.e. softmax over the selected positions only.
+
+Steps the pages leave open are fixed as follows (each is one plain reading):
+indexer = one int8 query dot int8 index key, exact integer sum, no scale;
+candidates = every position < N including the token just appended;
+k_eff = min(k, N); ties broken by lower position; selection reported in
+ascending position order; LRU victims = unpinned slots with the smallest
+(last-use stamp, slot); misses filled in ascending position order; appends do
+not enter the hot cache; q head h reads kv head floor(h * H_kv / H_q);
+softmax scale 1/sqrt(d_qk) unless given.
+
+Floating point is fp64 throughout; integer work is exact int64.
+"""
+from __future__ import annotations
+
+import heapq
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# bf16 inputs
+# ---------------------------------------------------------------------------
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact float64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# a1: indexer scores (HiSparse summary: the sparse selector states which
+# positions each step needs; the score is fixed here as int8 . int8 -> integer)
+# ---------------------------------------------------------------------------
+
+
+def indexer_scores(idx_keys: np.ndarray, q_idx: np.ndarray) -> np.ndarray:
+    """s[p] = sum_j q_idx[j] * K_idx[p, j] for every stored position p, exact int64."""
+    k = np.asarray(idx_keys, dtype=np.int8).astype(np.int64)
+    q = np.asarray(q_idx, dtype=np.int8).astype(np.int64)
+    return k @ q
+
+
+def indexer_scores_many(idx_keys: np.ndarray, q_idx: np.ndarray) -> np.ndarray:
+    """Scores of every position for several queries at once: int64 [N, T].
+
+    Uses a float32 matrix product.  Each product term is at most 128*128 = 2^14
+    in magnitude and d_idx <= 1023 terms are summed, so every partial sum is an
+    integer below 2^24 and is represented exactly in float32 whatever order the
+    library sums in; the result is the exact integer score."""
+    k = np.asarray(idx_keys, dtype=np.int8)
+    q = np.asarray(q_idx, dtype=np.int8)
+    if q.ndim == 1:
+        q = q[:, None]
+    elif q.shape[0] != k.shape[1]:
+        q = q.T
+    assert k.shape[1] * 128 * 128 < (1 << 24), "float32 path is exact only for d_idx < 1024"
+    s = k.astype(np.float32) @ q.astype(np.float32)
+    return s.astype(np.int64)
+
+
+# ---------------------------------------------------------------------------
+# a2: top-k selection ("10月14日学习笔记", HiSparse / 动机: the indexer keeps
+# the top-k tokens).  Ties go to the lower position; output ascending.
+# ---------------------------------------------------------------------------
+
+
+def topk_select(scores: np.ndarray, k: int) -> np.ndarray:
+    """Positions of the k_eff = min(k, N) highest scores, ascending (int64)."""
+    s = np.asarray(scores, dtype=np.int64)
+    n = s.shape[0]
+    k_eff = min(k, n)
+    pos = np.arange(n, dtype=np.int64)
+    order = np.lexsort((pos, -s))          # primary: score desc; secondary: position asc
+    return np.sort(order[:k_eff])
+
+
+# ---------------------------------------------------------------------------
+# a3/a4: the hot cache with LRU replacement (HiSparse summary: fixed B slots per
+# request per layer, page table + LRU metadata; study notes "方法" item 1: LRU).
+# ---------------------------------------------------------------------------
+
+
+class LRUHotCache:
+    """B-slot hot cache of one (request, layer), kept as plain Python lists.
+
+    State, as the pages name it: a page table position -> slot, the reverse map
+    slot -> position, and a last-use stamp per slot (the step counter of the
+    decode call that last used it; -1 for a slot never filled).  The step
+    counter starts at 0 and grows by one per decode call.
+
+    One decode call with selection ``sel`` (ascending positions):
+      1. a selected position with a page-table entry is a hit; its slot is pinned;
+      2. the other selected positions are misses, taken in ascending position order;
+      3. the victims are the m unpinned slots with the smallest (stamp, slot),
+         taken in that order; miss j goes to victim j;
+      4. a victim's old position (if any) leaves the page table; the page table and
+         reverse map record the new position;
+      5. every slot used by the call (hits and fills) gets stamp = step; step += 1.
+    Empty slots carry stamp -1, so they fill first, lowest slot first.
+    """
+
+    def __init__(self, n_slots: int):
+        self.B = int(n_slots)
+        self.slot_pos = [-1] * self.B
+        self.slot_stamp = [-1] * self.B
+        self.page: dict[int, int] = {}
+        self.step_no = 0
+
+    def step(self, sel) -> dict:
+        sel = [int(p) for p in sel]
+        assert len(sel) <= self.B, "every selected row must fit in the hot cache"
+        assert all(a < b for a, b in zip(sel, sel[1:])), "selection must be ascending and unique"
+        t = self.step_no
+        hit_slots = {self.page[p] for p in sel if p in self.page}
+        misses = [p for p in sel if p not in self.page]
+        candidates = sorted((self.slot_stamp[s], s) for s in range(self.B) if s not in hit_slots)
+        victims = [s for _, s in candidates[:len(misses)]]
+        fills = []
+        for p, v in zip(misses, victims):
+            old = self.slot_pos[v]
+            if old >= 0:
+                del self.page[old]
+            self.slot_pos[v] = p
+            self.page[p] = v
+            fills.append((p, v))
+        slot_of_sel = [self.page[p] for p in sel]
+        for s in slot_of_sel:
+            self.slot_stamp[s] = t
+        self.step_no = t + 1
+        return {
+            "slot_of_sel": np.asarray(slot_of_sel, dtype=np.int64),
+            "hits": len(sel) - len(misses),
+            "misses": len(misses),
+            "fills": fills,
+        }
+
+    def snapshot(self, n_positions: int):
+        """(page[n_positions], reverse[B], stamp[B], step) as int64 arrays / int."""
+        page = np.full(n_positions, -1, dtype=np.int64)
+        for p, s in self.page.items():
+            if p < n_positions:
+                page[p] = s
+        return (page, np.asarray(self.slot_pos, dtype=np.int64),
+                np.asarray(self.slot_stamp, dtype=np.int64), self.step_no)
+
+
+# ---------------------------------------------------------------------------
+# Belady's MIN (HiSparse summary quotes the offline optimum as the floor of the
+# LRU miss rate).  A per-step set trace is serialised step by step, ascending
+# inside a step; any batched schedule is also a serial one, so MIN of the
+# serial trace is a lower bound on every replacement policy's misses.
+# ---------------------------------------------------------------------------
+
+
+def belady_misses(trace, n_slots: int) -> int:
+    """Misses of the offline optimum (evict the resident position whose next use
+    is farthest; never-used-again counts as infinitely far) on the serialised trace."""
+    assert n_slots >= 1
+    seq = [int(p) for step in trace for p in sorted(step)]
+    n = len(seq)
+    nxt = [n] * n
+    last: dict[int, int] = {}
+    for i in range(n - 1, -1, -1):
+        nxt[i] = last.get(seq[i], n + 1 + i)   # distinct "never" values keep the heap total
+        last[seq[i]] = i
+    resident: dict[int, int] = {}              # position -> its next use
+    heap: list = []                            # (-next_use, position), lazily invalidated
+    misses = 0
+    for i, p in enumerate(seq):
+        if p not in resident:
+            misses += 1
+            if len(resident) >= n_slots:
+                while True:
+                    negnu, q = heapq.heappop(heap)
+                    if resident.get(q) == -negnu:
+                        del resident[q]
+                        break
+        resident[p] = nxt[i]
+        heapq.heappush(heap, (-nxt[i], p))
+    return misses
+
+
+# ---------------------------------------------------------------------------
+# a5: sparse attention over the selected rows (KARAT digest, formula 2, with
+# the mask read as "selected positions only"; HiSparse summary: exact).
+# ---------------------------------------------------------------------------
+
+
+def sparse_attention(q_bits: np.ndarray, rows_bits: np.ndarray, *, h_kv: int, d_qk: int,
+                     d_v: int, v_offset: int, scale: float | None = None) -> np.ndarray:
+    """o[h] = sum_i softmax_i(scale * q[h] . K_i) V_i over the given rows, fp64.
+
+    q_bits: bf16 bits [H_q, d_qk]; rows_bits: bf16 bits [n, row_elems] in the order
+    selected.  K of kv head g = row[g*d_qk : (g+1)*d_qk]; V of kv head g =
+    row[v_offset + g*d_v : v_offset + (g+1)*d_v].  q head h reads kv head
+    floor(h * h_kv / H_q).  Returns float64 [H_q, d_v]; zeros when n == 0."""
+    q = bf16_to_f64(q_bits)
+    rows = bf16_to_f64(rows_bits)
+    h_q = q.shape[0]
+    if scale is None or scale == 0.0:
+        scale = 1.0 / math.sqrt(d_qk)
+    out = np.zeros((h_q, d_v), dtype=np.float64)
+    if rows.shape[0] == 0:
+        return out
+    for h in range(h_q):
+        g = (h * h_kv) // h_q
+        K = rows[:, g * d_qk:(g + 1) * d_qk]
+        V = rows[:, v_offset + g * d_v: v_offset + (g + 1) * d_v]
+        logits = scale * (K @ q[h])
+        w = np.exp(logits - logits.max())
+        out[h] = (w / w.sum()) @ V
+    return out
+
+
+# ---------------------------------------------------------------------------
+# capacity (HiSparse summary: 128K GLM-5.1 request, 13.09 GB BF16 KV, ~0.4 GB
+# at B = 4096, about 30x)
+# ---------------------------------------------------------------------------
+
+
+def hot_over_full(n_slots: int, n_positions: int) -> float:
+    """Fraction of a request-layer's KV bytes that the hot cache holds: B / N."""
+    return n_slots / n_positions
+
+
+def hot_cache_bytes(full_kv_bytes: float, n_positions: int, n_slots: int) -> float:
+    return full_kv_bytes * hot_over_full(n_slots, n_positions)
