@@ -1,0 +1,221 @@
+/*
+ * hs.h — C ABI of a two-level KV cache for top-k sparse-attention decode
+ * (HiSparse), written for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What the library does, and where the method is stated:
+ *   "KV卸载上主机:HiSparse、PDD与DDR4回收" (yeyulingfeng.com), section
+ *   "二、论文分析 / 论文1：HiSparse": the authoritative full KV of every active
+ *   request lives in pinned host DRAM; the GPU keeps a fixed hot cache of B slots
+ *   per request per layer; a page table plus LRU metadata drive replacement; hit
+ *   detection, LRU replacement, metadata update and the host fetch are fused into
+ *   one RESOLVE kernel launched once per layer; only placement changes, so the
+ *   attention result is exactly top-k sparse attention over the full KV.
+ *   "10月14日学习笔记" (zgchen.com), section "HiSparse": the indexer picks the
+ *   top-k tokens ("动机"); adjacent steps overlap and LRU fits them ("方法" 1);
+ *   the whole flow runs without host involvement inside a CUDA graph ("方法" 2).
+ *
+ * Conventions for every call below:
+ *   - Return value: HS_OK (0) or a negative HS_ERR_* status.  On error nothing
+ *     was enqueued unless stated; hs_last_error() gives a message.
+ *   - "dev" pointers are CUDA device pointers (or any address the GPU can
+ *     dereference, e.g. pinned host memory under unified addressing); they stay
+ *     owned by the caller and must stay valid until the enqueued work finishes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls on one handle must be ordered on one stream (they share scratch).
+ *   - bf16 tensors are raw bf16 bit patterns, row-major, densely packed.
+ *   - Errors that only the GPU can see (a request id out of range, an append past
+ *     max_context, a decode of an empty request, a bounded wait that gave up)
+ *     do not fail the call: the kernel skips the affected request, sets a bit in
+ *     the handle's device error word (HS_DEVERR_*), and hs_stats() reports it.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define HS_OK 0
+#define HS_ERR_INVALID (-1)  /* bad argument (null pointer, range, layer, count) */
+#define HS_ERR_CONFIG (-2)   /* configuration outside what the kernels support */
+#define HS_ERR_OOM (-3)      /* host or device allocation failed (all freed again) */
+#define HS_ERR_CAPACITY (-4) /* request/position capacity exceeded (host-side check) */
+#define HS_ERR_CUDA (-5)     /* a CUDA runtime call failed (message has the name) */
+#define HS_ERR_DEVICE (-6)   /* hs_stats: the device error word is non-zero */
+
+/* ---- bits of the device error word -------------------------------------- */
+#define HS_DEVERR_REQ_RANGE 0x1u  /* a request id outside [0, max_requests) */
+#define HS_DEVERR_CAPACITY 0x2u   /* append past max_context: request skipped, nothing written */
+#define HS_DEVERR_EMPTY 0x4u      /* decode of a request with no positions: output set to 0 */
+#define HS_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel gave up */
+#define HS_DEVERR_METADATA 0x10u  /* page table / reverse map found inconsistent */
+
+/*
+ * Configuration.  Positions and rows:
+ *   A "row" is one position's K and V for all kv heads of one layer, bf16:
+ *     GQA (shared_kv = 0): [K: h_kv x d_qk][V: h_kv x d_v], row_elems = h_kv*(d_qk+d_v)
+ *     latent (shared_kv = 1, h_kv = 1): one row of d_qk elements read as K; its
+ *       first d_v elements are V (DeepSeek-style MLA latent), row_elems = d_qk.
+ *   q head h reads kv head floor(h * h_kv / h_q).
+ * Supported by the kernels (else HS_ERR_CONFIG):
+ *   GQA: d_qk = d_v = 128, h_q % h_kv == 0, h_kv in {1,2,4,8}, h_q/h_kv <= 16.
+ *   latent: h_kv = 1, d_qk = 576, d_v = 512, h_q in {16, 32, 64, 128}.
+ *   d_idx in {16, 32, 64, 128, 256}; 1 <= top_k <= hot_slots <= 16384;
+ *   top_k <= 8192; 1 <= max_context <= HS_MAX_CONTEXT; n_layers, max_requests >= 1.
+ */
+#define HS_MAX_CONTEXT (1 << 20)
+
+typedef struct hs_config {
+  int32_t n_layers;
+  int32_t max_requests;  /* request ids are 0 .. max_requests-1 */
+  int32_t max_context;   /* positions per (request, layer) */
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t d_qk;
+  int32_t d_v;
+  int32_t shared_kv;     /* 0: GQA rows, 1: latent rows (see above) */
+  int32_t d_idx;         /* int8 index-key width */
+  int32_t top_k;         /* k: positions attended per step */
+  int32_t hot_slots;     /* B: HBM slots per (request, layer) */
+  float softmax_scale;   /* 0 => 1/sqrt(d_qk) */
+  int32_t device;        /* CUDA device ordinal */
+} hs_config_t;
+
+typedef struct hs_handle hs_handle_t;
+
+typedef struct hs_stats {
+  uint64_t hits;          /* selected positions found in the hot cache, all calls */
+  uint64_t misses;        /* selected positions pulled from host memory */
+  uint64_t h2d_bytes;     /* bytes pulled host -> HBM by RESOLVE */
+  uint64_t d2h_bytes;     /* K/V bytes written to the host copy by appends */
+  uint64_t decode_calls;  /* hs_decode_layer calls enqueued */
+  uint64_t append_calls;  /* hs_append calls enqueued */
+  uint64_t host_bytes;    /* size of the pinned host K/V store */
+  uint64_t hot_bytes;     /* size of the HBM hot cache */
+  uint64_t index_bytes;   /* size of the HBM index-key store */
+  uint64_t meta_bytes;    /* page table, reverse map, stamps, LRU order, counters */
+  uint32_t device_error;  /* HS_DEVERR_* bits seen so far (sticky) */
+  uint32_t _pad;
+} hs_stats_t;
+
+/*
+ * hs_create — validate `cfg` and allocate every store (synchronous).
+ *   host store  D1: [max_requests][n_layers][max_context][row] bf16, pinned and
+ *                   mapped host memory (cudaHostAllocMapped): the authoritative copy;
+ *   hot cache   D2: [max_requests][n_layers][hot_slots][row] bf16 in HBM;
+ *   index keys  D3: [max_requests][n_layers][max_context][d_idx] int8 in HBM;
+ *   page table  D4: [max_requests][n_layers][max_context] int32, -1 = not resident;
+ *   reverse map, last-use stamps, LRU order: [max_requests][n_layers][hot_slots]
+ *   int32; per-(request, layer) length, step counter, hit and miss counters.
+ *   All requests start empty (length 0, every slot empty, step 0).
+ * Returns HS_ERR_INVALID (null), HS_ERR_CONFIG (unsupported shape), HS_ERR_OOM
+ * (allocation failed; nothing stays allocated) or HS_ERR_CUDA.  On success
+ * *out owns everything until hs_destroy.  The environment variable
+ * HS_FAULT_INJECT=hostalloc|devalloc makes the first host / device allocation
+ * fail (to test the clean-up path).
+ */
+int hs_create(const hs_config_t* cfg, hs_handle_t** out);
+
+/* hs_destroy — synchronise the device and free everything; NULL is a no-op. */
+void hs_destroy(hs_handle_t* h);
+
+/*
+ * hs_append — append n_tok tokens to each of n_req requests of one layer
+ * (stream-ordered, no host synchronisation).
+ *   req_ids : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
+ *   kv_rows : dev bf16 [n_req][n_tok][row_elems]   (device or pinned host memory)
+ *   idx_keys: dev int8 [n_req][n_tok][d_idx]
+ * For request r with current length L the tokens take positions L..L+n_tok-1:
+ * their index keys go to the HBM key store, their K/V rows to the pinned host
+ * copy (not to the hot cache: a new token enters the cache only when a later
+ * step selects it), and the length becomes L+n_tok.  A request whose append
+ * would pass max_context is skipped whole (HS_DEVERR_CAPACITY).
+ * n_req = 0 or n_tok = 0 is a no-op.  HS_ERR_INVALID for layer out of range,
+ * n_req > max_requests, n_tok > max_context or a null buffer.
+ */
+int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_ids,
+              int32_t n_tok, const void* kv_rows, const int8_t* idx_keys, void* stream);
+
+/*
+ * hs_decode_layer — one decode layer-step for n_req requests (stream-ordered,
+ * no host synchronisation, capturable in a CUDA graph).
+ *   req_ids : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
+ *   q_idx   : dev int8 [n_req][d_idx]       indexer query
+ *   q       : dev bf16 [n_req][h_q][d_qk]   attention query
+ *   out     : dev bf16 [n_req][h_q][d_v]    attention output (written)
+ *   sel_out : dev int32 [n_req][top_k] or NULL: selected positions, ascending;
+ *             entries past k_eff = min(top_k, length) are -1
+ * Per request with N positions: (1) score every position p < N as
+ * sum_j q_idx[j] * K_idx[p][j] (exact int32); (2) keep the k_eff highest, ties
+ * to the lower position; (3) RESOLVE: hits via the page table, misses pulled from
+ * the host copy into LRU victim slots, metadata and stamps updated, step += 1;
+ * (4) o_h = sum_i softmax_i(scale * q_h . K_i) V_i over the selected rows in
+ * ascending position order, fp32 accumulation, bf16 output.  The output does
+ * not depend on hot_slots or on the cache state (bit-identical across B).
+ * HS_ERR_INVALID for layer out of range, n_req > max_requests or null buffers.
+ */
+int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_ids,
+                    const int8_t* q_idx, const void* q, void* out, int32_t* sel_out,
+                    void* stream);
+
+/*
+ * hs_stats — synchronise the device and fill *out with cumulative counters and
+ * sizes.  Returns HS_ERR_DEVICE (with *out filled) when the device error word is
+ * non-zero, HS_ERR_INVALID for null arguments.
+ */
+int hs_stats(hs_handle_t* h, hs_stats_t* out);
+
+/*
+ * hs_snapshot — synchronise and copy the cache state of one (request, layer)
+ * to host buffers (test and debugging introspection).  Any output may be NULL.
+ *   page    : int32 [n_page]   page-table entries of positions 0..n_page-1
+ *   reverse : int32 [hot_slots] position held by each slot, -1 = empty
+ *   stamp   : int32 [hot_slots] step of last use of each slot, -1 = never
+ *   order   : int32 [hot_slots] slots from least to most recently used
+ *             (sorted by (stamp, slot))
+ *   scalars : int64 [4] = {length, step, hits, misses} of this (request, layer)
+ * HS_ERR_INVALID for out-of-range req/layer or n_page > max_context.
+ */
+int hs_snapshot(hs_handle_t* h, int32_t req, int32_t layer, int32_t* page, int32_t n_page,
+                int32_t* reverse, int32_t* stamp, int32_t* order, int64_t* scalars);
+
+/*
+ * hs_reset_request — forget request `req` on every layer (stream-ordered):
+ * length 0, page table cleared, every slot empty, step 0, counters 0.  Used to
+ * recycle a request id.  HS_ERR_INVALID when req is out of range.
+ */
+int hs_reset_request(hs_handle_t* h, int32_t req, void* stream);
+
+/*
+ * hs_set_timing / hs_kernel_times — per-kernel device timing.  With timing on,
+ * every launch is bracketed by CUDA events on the caller's stream; hs_kernel_times
+ * synchronises and returns, per kernel kind (HS_K_*), the summed milliseconds and
+ * the number of launches since the last hs_set_timing(h, 1).
+ */
+#define HS_K_APPEND 0
+#define HS_K_INDEXER_TOPK 1
+#define HS_K_RESOLVE 2
+#define HS_K_ATTENTION 3
+#define HS_K_COUNT 4
+int hs_set_timing(hs_handle_t* h, int32_t enable);
+int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launches /*[HS_K_COUNT]*/);
+
+/* hs_last_error — message of the handle's last failed call ("" if none); with
+ * h == NULL, the message of the last failed hs_create in this thread. */
+const char* hs_last_error(const hs_handle_t* h);
+
+/* hs_status_string — static name of a status code. */
+const char* hs_status_string(int32_t status);
+
+/* hs_row_elems — bf16 elements of one K/V row under cfg (0 if cfg is invalid). */
+int32_t hs_row_elems(const hs_config_t* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports every symbol include/hs.h
+declares; host-side argument and configuration checks (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tiered_kv_cache_int8_gb300.build import build
+    build()
+    from tiered_kv_cache_int8_gb300 import hs
+    return hs.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "hs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hs_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/hs.h but not exported"
+    from tiered_kv_cache_int8_gb300 import hs
+    assert sorted(hs.EXPORTED) == names
+
+
+def cfg(**over):
+    from tiered_kv_cache_int8_gb300.hs import HsConfig
+    base = dict(n_layers=1, max_requests=2, max_context=4096, h_q=32, h_kv=8, d_qk=128, d_v=128,
+                shared_kv=0, d_idx=128, top_k=256, hot_slots=512, softmax_scale=0.0, device=0)
+    base.update(over)
+    return HsConfig(**base)
+
+
+@pytest.mark.parametrize("over", [
+    dict(top_k=600),                 # k > B
+    dict(hot_slots=20000, top_k=16),  # B too large
+    dict(d_idx=48),                  # not a power of two
+    dict(d_idx=512),
+    dict(d_qk=64, d_v=64),           # GQA head dim
+    dict(h_q=24, h_kv=8),            # group of 3
+    dict(h_kv=16, h_q=32),
+    dict(n_layers=0),
+    dict(max_context=0),
+    dict(max_context=(1 << 20) + 1),
+    dict(top_k=0),
+    dict(shared_kv=2),
+    dict(softmax_scale=-1.0),
+])
+def test_unsupported_configs_are_rejected_before_touching_the_gpu(L, over):
+    from tiered_kv_cache_int8_gb300 import hs
+    h = ctypes.c_void_p()
+    rc = L.hs_create(ctypes.byref(cfg(**over)), ctypes.byref(h))
+    assert rc == hs.HS_ERR_CONFIG and not h
+    assert L.hs_last_error(None).decode().startswith("hs_create:")
+
+
+def test_row_elems_and_status_strings(L):
+    assert L.hs_row_elems(ctypes.byref(cfg())) == 8 * 256
+    assert L.hs_row_elems(ctypes.byref(cfg(h_kv=1, h_q=8))) == 256
+    assert L.hs_row_elems(ctypes.byref(cfg(top_k=9999))) == 0
+    assert L.hs_status_string(0) == b"HS_OK"
+    assert L.hs_status_string(-4) == b"HS_ERR_CAPACITY"
+    assert L.hs_status_string(-99) == b"HS_ERR_UNKNOWN"
+
+
+def test_null_arguments(L):
+    from tiered_kv_cache_int8_gb300 import hs
+    h = ctypes.c_void_p()
+    assert L.hs_create(None, ctypes.byref(h)) == hs.HS_ERR_INVALID
+    assert L.hs_append(None, 0, 1, None, 1, None, None, None) == hs.HS_ERR_INVALID
+    assert L.hs_decode_layer(None, 0, 1, None, None, None, None, None, None) == hs.HS_ERR_INVALID
+    assert L.hs_stats(None, None) == hs.HS_ERR_INVALID
+    assert L.hs_snapshot(None, 0, 0, None, 0, None, None, None, None) == hs.HS_ERR_INVALID
+    L.hs_destroy(None)
+
+
+def test_no_gpu_means_a_cuda_error_not_a_fallback(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from tiered_kv_cache_int8_gb300 import hs
+    h = ctypes.c_void_p()
+    rc = L.hs_create(ctypes.byref(cfg()), ctypes.byref(h))
+    assert rc == hs.HS_ERR_CUDA and not h
+    with pytest.raises(hs.HsError):
+        hs.HiSparseCache(n_layers=1, max_requests=1, max_context=64, h_q=8, h_kv=1, d_qk=128, d_v=128,
+                         d_idx=16, top_k=8, hot_slots=8)

@@ -1,0 +1,298 @@
+"""CUDA path against the CPU oracle, through the C ABI (binding in
+tiered_kv_cache_int8_gb300.hs).
+
+Bit-exact: selected positions, per-step hits and misses, page table, reverse
+map, last-use stamps, step counters.  Attention: max-abs <= 2e-2 and relative
+L2 <= 5e-3 against fp64.  Sizes span several tiles and ragged tails; the edge
+cases (k >= N, empty request, ties, request subsets, bad ids, capacity) are
+covered below; full-size workloads are in test_gpu_full.py.
+"""
+import numpy as np
+import pytest
+
+import workload as wl
+from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+from tests.harness import MAX_ABS, REL_L2, StepInputs, attention_error, make_cache, prefill, run_steps
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from tiered_kv_cache_int8_gb300.build import build
+    build()
+    yield
+
+
+def oracle_steps(w, r, l, steps, n_slots=None):
+    """Per step: (sel, step result, snapshot) from the oracle."""
+    keys = wl.idx_keys_upto(w, r, l, steps)
+    walk = wl.query_walk(w, r, l, steps)
+    scores = indexer_scores_many(keys, walk)
+    cache = LRUHotCache(n_slots or w.hot_slots)
+    n0 = int(w.contexts()[r])
+    out = []
+    for t in range(steps):
+        n = n0 + t + 1
+        sel = topk_select(scores[:n, t], w.top_k)
+        st = cache.step(sel)
+        out.append((sel, st, cache.snapshot(n)))
+    return out
+
+
+def oracle_attention(w, r, l, t, sel):
+    rows = wl.kv_rows_at(w, r, l, sel)
+    return sparse_attention(wl.step_query(w, r, l, t), rows, h_kv=w.h_kv, d_qk=w.d_qk, d_v=w.d_v,
+                            v_offset=w.v_offset)
+
+
+def check_order(order, stamp):
+    keys = sorted(range(len(stamp)), key=lambda s: (stamp[s], s))
+    assert order.tolist() == keys
+
+
+def full_parity(w, steps, hot_slots=None):
+    cache = make_cache(w, steps, hot_slots)
+    prefill(cache, w)
+    inp = StepInputs(w, steps)
+    got = run_steps(cache, w, inp, steps, collect_meta=True)
+    B = hot_slots or w.hot_slots
+    worst = (0.0, 0.0)
+    for l in range(w.n_layers):
+        for r in range(w.n_requests):
+            prev_h = prev_m = 0
+            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B)):
+                k_eff = sel.size
+                g_sel = got["sel"][l, t][r]
+                assert np.array_equal(g_sel[:k_eff], sel), f"selection r{r} l{l} t{t}"
+                assert (g_sel[k_eff:] == -1).all()
+                page, rev, stamp, order, (length, step, hits, misses) = got["meta"][l, t][r]
+                assert length == int(w.contexts()[r]) + t + 1 and step == t + 1
+                assert (hits - prev_h, misses - prev_m) == (st["hits"], st["misses"]), f"hit/miss r{r} l{l} t{t}"
+                prev_h, prev_m = hits, misses
+                o_page, o_rev, o_stamp, _ = snap
+                assert np.array_equal(page, o_page), f"page table r{r} l{l} t{t}"
+                assert np.array_equal(rev, o_rev), f"reverse map r{r} l{l} t{t}"
+                assert np.array_equal(stamp, o_stamp), f"stamps r{r} l{l} t{t}"
+                check_order(order, stamp)
+                ref = oracle_attention(w, r, l, t, sel)
+                ma, rel = attention_error(got["out"][l, t][r], ref)
+                assert ma <= MAX_ABS and rel <= REL_L2, f"attention r{r} l{l} t{t}: {ma} {rel}"
+                worst = (max(worst[0], ma), max(worst[1], rel))
+    st = cache.stats()
+    assert st["device_error"] == 0
+    cache.close()
+    return got, worst
+
+
+def test_tiny_workload_every_step():
+    # 1 request x 1 layer, context 4096 (+32), d_idx 64, k 256, B 512, 32 steps
+    full_parity(wl.WORKLOADS["tiny"], 32)
+
+
+def test_gqa_batch_ragged_small():
+    # several requests and layers, contexts not multiples of any tile, GQA 32/8
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=5003, top_k=256,
+                         hot_slots=512, steps=6)
+    full_parity(w, 6)
+
+
+def test_mixed_lengths_small():
+    w = wl.make_workload("mixed_8k_200k", n_requests=5, context_range=(300, 9000), top_k=256,
+                         hot_slots=384, steps=5)
+    full_parity(w, 5)
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(8, 8), (16, 2), (64, 4), (16, 1)])
+def test_gqa_head_groupings(h_q, h_kv):
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=1500, h_q=h_q, h_kv=h_kv,
+                         top_k=200, hot_slots=300, steps=3, d_idx=32)
+    full_parity(w, 3)
+
+
+def test_k_equals_B_and_high_sigma():
+    # every unhit slot is a victim each step; low locality
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=3000, top_k=256,
+                         hot_slots=256, steps=5, sigma=0.3)
+    full_parity(w, 5)
+
+
+def test_output_bit_identical_across_B():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=4000, top_k=256,
+                         hot_slots=256, steps=4)
+    outs = []
+    for B in (256, 512, 1024):
+        cache = make_cache(w, 4, B)
+        prefill(cache, w)
+        outs.append(run_steps(cache, w, StepInputs(w, 4), 4))
+        cache.close()
+    for t in range(4):
+        assert np.array_equal(outs[0]["out"][0, t], outs[1]["out"][0, t])
+        assert np.array_equal(outs[0]["out"][0, t], outs[2]["out"][0, t])
+        assert np.array_equal(outs[0]["sel"][0, t], outs[2]["sel"][0, t])
+
+
+def test_repeated_runs_are_bit_identical():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=2500, top_k=256,
+                         hot_slots=512, steps=3)
+    runs = []
+    for _ in range(2):
+        cache = make_cache(w, 3)
+        prefill(cache, w)
+        runs.append(run_steps(cache, w, StepInputs(w, 3), 3))
+        cache.close()
+    for key in runs[0]["out"]:
+        assert np.array_equal(runs[0]["out"][key], runs[1]["out"][key])
+
+
+def test_context_shorter_than_k_is_dense():
+    # k >= N: every position is selected (k_eff = N); the tail of sel_out is -1
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=100, top_k=256,
+                         hot_slots=256, steps=3)
+    full_parity(w, 3)
+
+
+def test_ties_take_the_lowest_positions():
+    import torch
+    from tiered_kv_cache_int8_gb300 import HiSparseCache
+    dev = torch.device("cuda", 0)
+    R, N, d, k = 2, 3000, 64, 128
+    cache = HiSparseCache(n_layers=1, max_requests=R, max_context=N + 4, h_q=4, h_kv=1, d_qk=128, d_v=128,
+                          d_idx=d, top_k=k, hot_slots=k)
+    kv = torch.randn(R, N, 256, device=dev).to(torch.bfloat16)
+    keys = torch.full((R, N, d), 3, dtype=torch.int8, device=dev)
+    keys[1, 2000:2010] = 4            # ten strictly higher scores, then ties
+    cache.append(0, kv, keys)
+    q_idx = torch.ones(R, d, dtype=torch.int8, device=dev)
+    q = torch.randn(R, 4, 128, device=dev).to(torch.bfloat16)
+    sel = torch.empty(R, k, dtype=torch.int32, device=dev)
+    cache.decode_layer(0, q_idx, q, sel_out=sel)
+    s = sel.cpu().numpy()
+    assert s[0].tolist() == list(range(k))
+    assert s[1].tolist() == sorted(list(range(k - 10)) + list(range(2000, 2010)))
+    assert cache.stats()["device_error"] == 0
+    cache.close()
+
+
+def test_request_subset_and_order():
+    import torch
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=1, context=2000, top_k=128,
+                         hot_slots=256, steps=2)
+    cache = make_cache(w, 2)
+    prefill(cache, w)
+    dev = torch.device("cuda", 0)
+    ids = torch.tensor([2, 0], dtype=torch.int32, device=dev)
+    kv = torch.from_numpy(np.stack([wl.step_kv_row(w, r, 0, 0) for r in (2, 0)])[:, None].view(np.int16)).to(dev)
+    keys = torch.from_numpy(np.stack([wl.step_idx_key(w, r, 0, 0) for r in (2, 0)])[:, None]).to(dev)
+    cache.append(0, kv, keys, req_ids=ids)
+    q_idx = torch.from_numpy(np.stack([wl.query_walk(w, r, 0, 1)[0] for r in (2, 0)])).to(dev)
+    q = torch.from_numpy(np.stack([wl.step_query(w, r, 0, 0) for r in (2, 0)]).view(np.int16)).to(dev)
+    sel = torch.empty(2, w.top_k, dtype=torch.int32, device=dev)
+    out = cache.decode_layer(0, q_idx, q, sel_out=sel, req_ids=ids)
+    for i, r in enumerate((2, 0)):
+        o_sel, o_st, _ = oracle_steps(w, r, 0, 1)[0]
+        assert np.array_equal(sel[i].cpu().numpy(), o_sel)
+        ref = oracle_attention(w, r, 0, 0, o_sel)
+        ma, rel = attention_error(out[i].view(torch.int16).cpu().numpy().view(np.uint16), ref)
+        assert ma <= MAX_ABS and rel <= REL_L2
+    assert cache.snapshot(1, 0, 1)[4][:2] == (2000, 0)     # request 1 untouched
+    assert cache.snapshot(2, 0, 1)[4][:2] == (2001, 1)
+    cache.close()
+
+
+def test_empty_request_and_bad_ids_set_error_bits():
+    import torch
+    from tiered_kv_cache_int8_gb300 import HiSparseCache, hs
+    dev = torch.device("cuda", 0)
+    cache = HiSparseCache(n_layers=1, max_requests=2, max_context=64, h_q=4, h_kv=1, d_qk=128, d_v=128,
+                          d_idx=16, top_k=8, hot_slots=8)
+    q_idx = torch.ones(1, 16, dtype=torch.int8, device=dev)
+    q = torch.ones(1, 4, 128, device=dev).to(torch.bfloat16)
+    out = torch.full((1, 4, 128), 7.0, device=dev).to(torch.bfloat16)
+    cache.decode_layer(0, q_idx, q, out=out)                 # request 0 has no positions
+    assert (out.float() == 0).all()
+    assert cache.stats()["device_error"] == hs.HS_DEVERR_EMPTY
+    cache.close()
+    cache = HiSparseCache(n_layers=1, max_requests=2, max_context=64, h_q=4, h_kv=1, d_qk=128, d_v=128,
+                          d_idx=16, top_k=8, hot_slots=8)
+    bad = torch.tensor([5], dtype=torch.int32, device=dev)
+    cache.append(0, torch.zeros(1, 1, 256, dtype=torch.bfloat16, device=dev),
+                 torch.zeros(1, 1, 16, dtype=torch.int8, device=dev), req_ids=bad)
+    cache.decode_layer(0, q_idx, q, req_ids=bad)
+    assert cache.stats()["device_error"] & hs.HS_DEVERR_REQ_RANGE
+    cache.close()
+
+
+def test_append_past_capacity_is_rejected_whole():
+    import torch
+    from tiered_kv_cache_int8_gb300 import HiSparseCache, hs
+    dev = torch.device("cuda", 0)
+    cache = HiSparseCache(n_layers=1, max_requests=2, max_context=40, h_q=4, h_kv=1, d_qk=128, d_v=128,
+                          d_idx=16, top_k=8, hot_slots=8)
+    cache.append(0, torch.zeros(2, 30, 256, dtype=torch.bfloat16, device=dev),
+                 torch.zeros(2, 30, 16, dtype=torch.int8, device=dev))
+    cache.append(0, torch.zeros(1, 20, 256, dtype=torch.bfloat16, device=dev),
+                 torch.zeros(1, 20, 16, dtype=torch.int8, device=dev))
+    assert cache.stats()["device_error"] == hs.HS_DEVERR_CAPACITY
+    assert cache.snapshot(0, 0, 1)[4][0] == 30 and cache.snapshot(1, 0, 1)[4][0] == 30
+    with pytest.raises(hs.HsError):
+        cache.append(0, torch.zeros(1, 41, 256, dtype=torch.bfloat16, device=dev),
+                     torch.zeros(1, 41, 16, dtype=torch.int8, device=dev))
+    cache.close()
+
+
+def test_reset_request_recycles_the_id():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=2, context=1800, top_k=128,
+                         hot_slots=256, steps=2)
+    cache = make_cache(w, 2)
+    prefill(cache, w)
+    run_steps(cache, w, StepInputs(w, 2), 2, collect_out=False)
+    cache.reset_request(1)
+    page, rev, stamp, order, sc = cache.snapshot(1, 1, 1800)
+    assert sc == (0, 0, 0, 0) and (page == -1).all() and (rev == -1).all() and (stamp == -1).all()
+    assert order.tolist() == list(range(256))
+    assert cache.snapshot(0, 1, 1)[4][1] == 2
+    cache.close()
+
+
+def test_graph_capture_replays_the_same_step():
+    import torch
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=3000, top_k=256,
+                         hot_slots=512, steps=3)
+    inp = StepInputs(w, 3)
+    eager = make_cache(w, 3)
+    prefill(eager, w)
+    ref = run_steps(eager, w, inp, 3)
+    eager.close()
+
+    cache = make_cache(w, 3)
+    prefill(cache, w)
+    dev = torch.device("cuda", 0)
+    q_idx = inp.q_idx[0, 0].clone()
+    q = inp.q[0, 0].clone()
+    kv = inp.kv[0, 0].clone()
+    keys = inp.keys[0, 0].clone()
+    out = torch.empty(2, w.h_q, w.d_v, dtype=torch.bfloat16, device=dev)
+    sel = torch.empty(2, w.top_k, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            cache.append(0, kv, keys, stream=s)
+            cache.decode_layer(0, q_idx, q, out=out, sel_out=sel, stream=s)
+    torch.cuda.synchronize()
+    # capture enqueues nothing: the cache is still at step 0
+    assert cache.snapshot(0, 0, 1)[4][:2] == (3000, 0)
+    for t in range(3):
+        q_idx.copy_(inp.q_idx[0, t])
+        q.copy_(inp.q[0, t])
+        kv.copy_(inp.kv[0, t])
+        keys.copy_(inp.keys[0, t])
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(sel.cpu().numpy(), ref["sel"][0, t])
+        assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"][0, t])
+    assert cache.stats()["device_error"] == 0
+    cache.close()

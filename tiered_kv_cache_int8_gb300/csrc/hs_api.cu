@@ -1,0 +1,492 @@
+// Host side of the C ABI declared in include/hs.h: configuration checks,
+// allocation of the two memory tiers and the cache metadata, argument checks
+// and kernel launches, counters, snapshots and optional per-kernel timing.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "hs_internal.cuh"
+
+namespace {
+
+thread_local std::string g_create_error;
+
+int set_err(hs_handle* h, int code, const std::string& msg) {
+  if (h) h->last_error = msg;
+  else g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(hs_handle* h, cudaError_t e, const char* what) {
+  std::string msg = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  (void)cudaGetLastError();
+  return set_err(h, HS_ERR_CUDA, msg);
+}
+
+bool is_pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+// Returns "" when the configuration is one the kernels support, else the reason.
+std::string check_config(const hs_config_t& c) {
+  if (c.n_layers < 1) return "n_layers must be >= 1";
+  if (c.max_requests < 1 || c.max_requests > 65535) return "max_requests must be in [1, 65535]";
+  if (c.max_context < 1 || c.max_context > HS_MAX_CONTEXT) return "max_context must be in [1, HS_MAX_CONTEXT]";
+  if (!is_pow2_in(c.d_idx, 16, 256)) return "d_idx must be one of 16, 32, 64, 128, 256";
+  if (c.top_k < 1 || c.top_k > 8192) return "top_k must be in [1, 8192]";
+  if (c.hot_slots < c.top_k || c.hot_slots > 16384) return "hot_slots must be in [top_k, 16384]";
+  if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return "softmax_scale must be finite and >= 0";
+  if (c.shared_kv == 0) {
+    if (c.d_qk != 128 || c.d_v != 128) return "GQA rows: d_qk = d_v = 128 required";
+    if (!is_pow2_in(c.h_kv, 1, 8)) return "GQA rows: h_kv must be one of 1, 2, 4, 8";
+    if (c.h_q < c.h_kv || c.h_q % c.h_kv != 0) return "GQA rows: h_q must be a multiple of h_kv";
+    if (!is_pow2_in(c.h_q / c.h_kv, 1, 16)) return "GQA rows: h_q / h_kv must be one of 1, 2, 4, 8, 16";
+  } else if (c.shared_kv == 1) {
+    return "latent (shared K/V) rows are not supported by this build";
+  } else {
+    return "shared_kv must be 0 or 1";
+  }
+  return "";
+}
+
+void free_all(hs_handle* h) {
+  for (void* p : h->dev_allocs) cudaFree(p);
+  h->dev_allocs.clear();
+  if (h->host_kv_host) cudaFreeHost(h->host_kv_host);
+  h->host_kv_host = nullptr;
+  for (auto& t : h->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  h->timed.clear();
+  for (cudaEvent_t e : h->event_pool) cudaEventDestroy(e);
+  h->event_pool.clear();
+}
+
+struct FaultInject {
+  bool host = false, dev = false;
+  FaultInject() {
+    const char* v = std::getenv("HS_FAULT_INJECT");
+    if (v) {
+      host = std::strcmp(v, "hostalloc") == 0;
+      dev = std::strcmp(v, "devalloc") == 0;
+    }
+  }
+};
+
+template <typename T>
+cudaError_t dev_alloc(hs_handle* h, T** p, size_t bytes, FaultInject& fi) {
+  if (fi.dev) {
+    fi.dev = false;
+    return cudaErrorMemoryAllocation;
+  }
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+  if (e == cudaSuccess) {
+    h->dev_allocs.push_back(q);
+    *p = static_cast<T*>(q);
+  }
+  return e;
+}
+
+cudaEvent_t take_event(hs_handle* h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one launch with events when timing is on.
+template <typename F>
+cudaError_t timed_launch(hs_handle* h, int kind, cudaStream_t st, F&& launch) {
+  if (!h->timing) return launch();
+  cudaEvent_t a = take_event(h), b = take_event(h);
+  if (!a || !b) return launch();
+  cudaEventRecord(a, st);
+  cudaError_t e = launch();
+  cudaEventRecord(b, st);
+  h->timed.push_back({kind, a, b});
+  return e;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Makes the handle's device current without a call when it already is (keeps
+// the enqueue path free of anything but launches, e.g. under stream capture).
+void use_device(const hs_handle* h) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->cfg.device) cudaSetDevice(h->cfg.device);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hs_status_string(int32_t s) {
+  switch (s) {
+    case HS_OK: return "HS_OK";
+    case HS_ERR_INVALID: return "HS_ERR_INVALID";
+    case HS_ERR_CONFIG: return "HS_ERR_CONFIG";
+    case HS_ERR_OOM: return "HS_ERR_OOM";
+    case HS_ERR_CAPACITY: return "HS_ERR_CAPACITY";
+    case HS_ERR_CUDA: return "HS_ERR_CUDA";
+    case HS_ERR_DEVICE: return "HS_ERR_DEVICE";
+    default: return "HS_ERR_UNKNOWN";
+  }
+}
+
+const char* hs_last_error(const hs_handle_t* h) { return h ? h->last_error.c_str() : g_create_error.c_str(); }
+
+int32_t hs_row_elems(const hs_config_t* c) {
+  if (!c || !check_config(*c).empty()) return 0;
+  return c->shared_kv ? c->d_qk : c->h_kv * (c->d_qk + c->d_v);
+}
+
+int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
+  g_create_error.clear();
+  if (!cfg || !out) return set_err(nullptr, HS_ERR_INVALID, "hs_create: null argument");
+  *out = nullptr;
+  const std::string why = check_config(*cfg);
+  if (!why.empty()) return set_err(nullptr, HS_ERR_CONFIG, "hs_create: " + why);
+
+  hs_handle* h = new (std::nothrow) hs_handle();
+  if (!h) return set_err(nullptr, HS_ERR_OOM, "hs_create: out of host memory");
+  h->cfg = *cfg;
+  hs::Geometry& g = h->g;
+  g.n_layers = cfg->n_layers;
+  g.max_requests = cfg->max_requests;
+  g.max_context = cfg->max_context;
+  g.h_q = cfg->h_q;
+  g.h_kv = cfg->h_kv;
+  g.d_qk = cfg->d_qk;
+  g.d_v = cfg->d_v;
+  g.shared_kv = cfg->shared_kv;
+  g.d_idx = cfg->d_idx;
+  g.top_k = cfg->top_k;
+  g.hot_slots = cfg->hot_slots;
+  g.row_elems = hs_row_elems(cfg);
+  g.row_bytes = 2 * g.row_elems;
+  g.v_off = cfg->shared_kv ? 0 : cfg->h_kv * cfg->d_qk;
+  const float scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / std::sqrt((float)cfg->d_qk);
+  h->scale_log2 = scale * 1.4426950408889634f;
+
+  auto fail_free = [&](int code, const std::string& msg) {
+    free_all(h);
+    delete h;
+    return set_err(nullptr, code, msg);
+  };
+
+  cudaError_t e = cudaSetDevice(cfg->device);
+  if (e != cudaSuccess) {
+    std::string msg = std::string("hs_create: cudaSetDevice: ") + cudaGetErrorName(e);
+    (void)cudaGetLastError();
+    delete h;
+    return set_err(nullptr, HS_ERR_CUDA, msg);
+  }
+  int smem_optin = 0, cluster_ok = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, cfg->device);
+  cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, cfg->device);
+  if (!cluster_ok) return fail_free(HS_ERR_CONFIG, "hs_create: device has no thread-block cluster launch");
+
+  int chunk = (cfg->max_context + hs::IDX_CLUSTER - 1) / hs::IDX_CLUSTER;
+  h->idx_chunk_max = (chunk + 31) & ~31;
+  h->idx_smem = hs::indexer_smem_bytes(g, h->idx_chunk_max);
+  h->res_smem = hs::resolve_smem_bytes(g);
+  h->att_smem = hs::attention_smem_bytes(g);
+  h->att_parts = hs::attention_parts(g);
+  if (h->idx_smem > (size_t)smem_optin)
+    return fail_free(HS_ERR_CONFIG, "hs_create: max_context too large for the indexer's shared memory (" +
+                                        std::to_string(h->idx_smem) + " > " + std::to_string(smem_optin) + " bytes)");
+  if (h->res_smem > (size_t)smem_optin)
+    return fail_free(HS_ERR_CONFIG, "hs_create: top_k / hot_slots too large for RESOLVE's shared memory");
+  if (h->att_smem > (size_t)smem_optin)
+    return fail_free(HS_ERR_CONFIG, "hs_create: row too wide for the attention kernel's shared memory");
+
+  const size_t R = cfg->max_requests, Lr = cfg->n_layers, N = cfg->max_context, B = cfg->hot_slots;
+  const size_t K = cfg->top_k;
+  h->host_bytes = R * Lr * N * (size_t)g.row_bytes;
+  h->hot_bytes = R * Lr * B * (size_t)g.row_bytes;
+  h->index_bytes = R * Lr * N * (size_t)g.d_idx;
+
+  FaultInject fi;
+  // D1: authoritative copy in pinned, mapped host memory
+  if (fi.host) return fail_free(HS_ERR_OOM, "hs_create: pinned host allocation failed (injected)");
+  void* hp = nullptr;
+  e = cudaHostAlloc(&hp, h->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail_free(HS_ERR_OOM, std::string("hs_create: cudaHostAlloc of ") + std::to_string(h->host_bytes) +
+                                     " bytes failed: " + cudaGetErrorName(e));
+  }
+  h->host_kv_host = static_cast<uint16_t*>(hp);
+  void* dp = nullptr;
+  e = cudaHostGetDevicePointer(&dp, hp, 0);
+  if (e != cudaSuccess) return fail_free(HS_ERR_CUDA, "hs_create: cudaHostGetDevicePointer failed");
+  h->s.host_kv = static_cast<uint16_t*>(dp);
+
+  hs::DeviceState& s = h->s;
+  size_t meta = 0;
+  struct A {
+    void** p;
+    size_t bytes;
+    bool meta;
+  };
+  const A allocs[] = {
+      {(void**)&s.hot, h->hot_bytes, false},
+      {(void**)&s.idx_keys, h->index_bytes, false},
+      {(void**)&s.page, R * Lr * N * 4, true},
+      {(void**)&s.reverse, R * Lr * B * 4, true},
+      {(void**)&s.stamp, R * Lr * B * 4, true},
+      {(void**)&s.order, R * Lr * B * 4, true},
+      {(void**)&s.length, R * Lr * 4, true},
+      {(void**)&s.step, R * Lr * 4, true},
+      {(void**)&s.hits, R * Lr * 8, true},
+      {(void**)&s.misses, R * Lr * 8, true},
+      {(void**)&s.glob, 4 * 8, true},
+      {(void**)&s.dev_error, 16, true},
+      {(void**)&s.sel, R * K * 4, false},
+      {(void**)&s.slot_of_sel, R * K * 4, false},
+      {(void**)&s.part_o, R * (size_t)h->att_parts * g.h_q * g.d_v * 4, false},
+      {(void**)&s.part_ml, R * (size_t)h->att_parts * g.h_q * 2 * 4, false},
+      {(void**)&s.att_counter, R * 4, false},
+      {(void**)&s.app_counter, R * 4, false},
+  };
+  for (const A& a : allocs) {
+    e = dev_alloc(h, a.p, a.bytes, fi);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail_free(HS_ERR_OOM, std::string("hs_create: device allocation of ") + std::to_string(a.bytes) +
+                                       " bytes failed: " + cudaGetErrorName(e));
+    }
+    if (a.meta) meta += a.bytes;
+  }
+  h->meta_bytes = meta;
+
+  // initial state: empty cache everywhere
+  bool ok = cudaMemset(s.page, 0xff, R * Lr * N * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.reverse, 0xff, R * Lr * B * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.stamp, 0xff, R * Lr * B * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.length, 0, R * Lr * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.step, 0, R * Lr * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.hits, 0, R * Lr * 8) == cudaSuccess;
+  ok = ok && cudaMemset(s.misses, 0, R * Lr * 8) == cudaSuccess;
+  ok = ok && cudaMemset(s.glob, 0, 32) == cudaSuccess;
+  ok = ok && cudaMemset(s.dev_error, 0, 16) == cudaSuccess;
+  ok = ok && cudaMemset(s.slot_of_sel, 0, R * K * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.att_counter, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
+  ok = ok && hs::launch_init_order(s.order, (long long)(R * Lr), (int)B, 0) == cudaSuccess;
+  if (!ok) return fail_free(HS_ERR_CUDA, "hs_create: initialising the metadata failed");
+  if ((e = hs::prepare_indexer(h->idx_smem)) != cudaSuccess ||
+      (e = hs::prepare_resolve(h->res_smem)) != cudaSuccess ||
+      (e = hs::prepare_attention(g, h->att_smem)) != cudaSuccess)
+    return fail_free(HS_ERR_CUDA, std::string("hs_create: kernel set-up failed: ") + cudaGetErrorName(e));
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_free(HS_ERR_CUDA, std::string("hs_create: ") + cudaGetErrorName(e));
+  *out = h;
+  return HS_OK;
+}
+
+void hs_destroy(hs_handle_t* h) {
+  if (!h) return;
+  cudaSetDevice(h->cfg.device);
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+}
+
+int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_ids, int32_t n_tok,
+              const void* kv_rows, const int8_t* idx_keys, void* stream) {
+  if (!h) return HS_ERR_INVALID;
+  if (layer < 0 || layer >= h->cfg.n_layers) return set_err(h, HS_ERR_INVALID, "hs_append: layer out of range");
+  if (n_req < 0 || n_req > h->cfg.max_requests) return set_err(h, HS_ERR_INVALID, "hs_append: n_req out of range");
+  if (n_tok < 0) return set_err(h, HS_ERR_INVALID, "hs_append: n_tok < 0");
+  if (n_tok > h->cfg.max_context)
+    return set_err(h, HS_ERR_CAPACITY, "hs_append: n_tok exceeds max_context");
+  if (n_req == 0 || n_tok == 0) return HS_OK;
+  if (!kv_rows || !idx_keys) return set_err(h, HS_ERR_INVALID, "hs_append: null buffer");
+  if (!aligned16(kv_rows) || !aligned16(idx_keys))
+    return set_err(h, HS_ERR_INVALID, "hs_append: kv_rows and idx_keys must be 16-byte aligned");
+  use_device(h);
+  hs::AppendParams p;
+  p.g = h->g;
+  p.s = h->s;
+  p.layer = layer;
+  p.n_req = n_req;
+  p.n_tok = n_tok;
+  p.req_ids = req_ids;
+  p.kv_rows = static_cast<const uint16_t*>(kv_rows);
+  p.keys = idx_keys;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed_launch(h, HS_K_APPEND, st, [&] { return hs::launch_append(p, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_append: launch");
+  ++h->append_calls;
+  return HS_OK;
+}
+
+int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_ids, const int8_t* q_idx,
+                    const void* q, void* out, int32_t* sel_out, void* stream) {
+  if (!h) return HS_ERR_INVALID;
+  if (layer < 0 || layer >= h->cfg.n_layers)
+    return set_err(h, HS_ERR_INVALID, "hs_decode_layer: layer out of range");
+  if (n_req < 0 || n_req > h->cfg.max_requests)
+    return set_err(h, HS_ERR_INVALID, "hs_decode_layer: n_req out of range");
+  if (n_req == 0) return HS_OK;
+  if (!q_idx || !q || !out) return set_err(h, HS_ERR_INVALID, "hs_decode_layer: null buffer");
+  if (!aligned16(q_idx)) return set_err(h, HS_ERR_INVALID, "hs_decode_layer: q_idx must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(out) & 1u) ||
+      (reinterpret_cast<uintptr_t>(sel_out) & 3u))
+    return set_err(h, HS_ERR_INVALID, "hs_decode_layer: misaligned q / out / sel_out");
+  use_device(h);
+  hs::DecodeParams p;
+  p.g = h->g;
+  p.s = h->s;
+  p.layer = layer;
+  p.n_req = n_req;
+  p.req_ids = req_ids;
+  p.q_idx = q_idx;
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = static_cast<uint16_t*>(out);
+  p.sel_out = sel_out;
+  p.scale_log2 = h->scale_log2;
+  p.idx_chunk_max = h->idx_chunk_max;
+  p.att_parts = h->att_parts;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed_launch(h, HS_K_INDEXER_TOPK, st, [&] { return hs::launch_indexer_topk(p, h->idx_smem, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: indexer/top-k launch");
+  e = timed_launch(h, HS_K_RESOLVE, st, [&] { return hs::launch_resolve(p, h->res_smem, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: RESOLVE launch");
+  e = timed_launch(h, HS_K_ATTENTION, st, [&] { return hs::launch_attention(p, h->att_smem, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: attention launch");
+  ++h->decode_calls;
+  return HS_OK;
+}
+
+int hs_stats(hs_handle_t* h, hs_stats_t* out) {
+  if (!h || !out) return HS_ERR_INVALID;
+  cudaSetDevice(h->cfg.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_stats: synchronize");
+  const size_t RL = (size_t)h->cfg.max_requests * h->cfg.n_layers;
+  std::vector<unsigned long long> hits(RL), misses(RL), glob(4);
+  unsigned int err = 0;
+  if ((e = cudaMemcpy(hits.data(), h->s.hits, RL * 8, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(misses.data(), h->s.misses, RL * 8, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(glob.data(), h->s.glob, 32, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(&err, h->s.dev_error, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(h, e, "hs_stats: copy");
+  std::memset(out, 0, sizeof(*out));
+  for (size_t i = 0; i < RL; ++i) {
+    out->hits += hits[i];
+    out->misses += misses[i];
+  }
+  out->h2d_bytes = glob[0];
+  out->d2h_bytes = glob[1];
+  out->decode_calls = h->decode_calls;
+  out->append_calls = h->append_calls;
+  out->host_bytes = h->host_bytes;
+  out->hot_bytes = h->hot_bytes;
+  out->index_bytes = h->index_bytes;
+  out->meta_bytes = h->meta_bytes;
+  out->device_error = err;
+  if (err) return set_err(h, HS_ERR_DEVICE, "hs_stats: device error word " + std::to_string(err));
+  return HS_OK;
+}
+
+int hs_snapshot(hs_handle_t* h, int32_t req, int32_t layer, int32_t* page, int32_t n_page, int32_t* reverse,
+                int32_t* stamp, int32_t* order, int64_t* scalars) {
+  if (!h) return HS_ERR_INVALID;
+  if (req < 0 || req >= h->cfg.max_requests || layer < 0 || layer >= h->cfg.n_layers)
+    return set_err(h, HS_ERR_INVALID, "hs_snapshot: request or layer out of range");
+  if (page && (n_page < 0 || n_page > h->cfg.max_context))
+    return set_err(h, HS_ERR_INVALID, "hs_snapshot: n_page out of range");
+  cudaSetDevice(h->cfg.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_snapshot: synchronize");
+  const size_t rl = (size_t)req * h->cfg.n_layers + layer;
+  const size_t B = h->cfg.hot_slots;
+  if (page && n_page > 0 &&
+      (e = cudaMemcpy(page, h->s.page + rl * h->cfg.max_context, (size_t)n_page * 4, cudaMemcpyDeviceToHost)) !=
+          cudaSuccess)
+    return cuda_fail(h, e, "hs_snapshot: page");
+  if (reverse && (e = cudaMemcpy(reverse, h->s.reverse + rl * B, B * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(h, e, "hs_snapshot: reverse");
+  if (stamp && (e = cudaMemcpy(stamp, h->s.stamp + rl * B, B * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(h, e, "hs_snapshot: stamp");
+  if (order && (e = cudaMemcpy(order, h->s.order + rl * B, B * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(h, e, "hs_snapshot: order");
+  if (scalars) {
+    int32_t len = 0, step = 0;
+    unsigned long long hi = 0, mi = 0;
+    if ((e = cudaMemcpy(&len, h->s.length + rl, 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(&step, h->s.step + rl, 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(&hi, h->s.hits + rl, 8, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(&mi, h->s.misses + rl, 8, cudaMemcpyDeviceToHost)) != cudaSuccess)
+      return cuda_fail(h, e, "hs_snapshot: scalars");
+    scalars[0] = len;
+    scalars[1] = step;
+    scalars[2] = (int64_t)hi;
+    scalars[3] = (int64_t)mi;
+  }
+  return HS_OK;
+}
+
+int hs_reset_request(hs_handle_t* h, int32_t req, void* stream) {
+  if (!h) return HS_ERR_INVALID;
+  if (req < 0 || req >= h->cfg.max_requests)
+    return set_err(h, HS_ERR_INVALID, "hs_reset_request: request out of range");
+  use_device(h);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t L = h->cfg.n_layers, N = h->cfg.max_context, B = h->cfg.hot_slots;
+  const size_t r = req;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(h->s.page + r * L * N, 0xff, L * N * 4, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.reverse + r * L * B, 0xff, L * B * 4, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.stamp + r * L * B, 0xff, L * B * 4, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.length + r * L, 0, L * 4, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.step + r * L, 0, L * 4, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.hits + r * L, 0, L * 8, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.misses + r * L, 0, L * 8, st)) != cudaSuccess ||
+      (e = hs::launch_init_order(h->s.order + r * L * B, (long long)L, (int)B, st)) != cudaSuccess)
+    return cuda_fail(h, e, "hs_reset_request");
+  return HS_OK;
+}
+
+int hs_set_timing(hs_handle_t* h, int32_t enable) {
+  if (!h) return HS_ERR_INVALID;
+  cudaSetDevice(h->cfg.device);
+  cudaDeviceSynchronize();
+  for (auto& t : h->timed) {
+    h->event_pool.push_back(t.a);
+    h->event_pool.push_back(t.b);
+  }
+  h->timed.clear();
+  h->timing = enable != 0;
+  return HS_OK;
+}
+
+int hs_kernel_times(hs_handle_t* h, double* ms, int64_t* launches) {
+  if (!h || !ms || !launches) return HS_ERR_INVALID;
+  cudaSetDevice(h->cfg.device);
+  for (int k = 0; k < HS_K_COUNT; ++k) {
+    ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_kernel_times: synchronize");
+  for (auto& t : h->timed) {
+    float x = 0.f;
+    if (cudaEventElapsedTime(&x, t.a, t.b) == cudaSuccess) {
+      ms[t.kind] += x;
+      launches[t.kind] += 1;
+    }
+  }
+  (void)cudaGetLastError();
+  return HS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Append path (one new token per step, or a bulk prefill): index keys to the
+// HBM key store, K/V rows to the authoritative copy in pinned host memory, and
+// the request's length advanced once every CTA of the request has read it.
+//
+// Method: "KV卸载上主机:HiSparse、PDD与DDR4回收", section "论文1：HiSparse" —
+// host DRAM holds the complete, authoritative KV of every active request, so
+// each new token's K/V goes there; the hot cache is only filled by RESOLVE.
+#include "hs_internal.cuh"
+
+namespace hs {
+
+// grid (ceil(n_tok / APP_TOKENS_PER_CTA), n_req); block APP_THREADS
+__global__ void __launch_bounds__(APP_THREADS) append_kernel(AppendParams p) {
+  const Geometry& g = p.g;
+  const int ri = blockIdx.y;
+  const int req = p.req_ids ? p.req_ids[ri] : ri;
+  if (req < 0 || req >= g.max_requests) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(p.s.dev_error, HS_DEVERR_REQ_RANGE);
+    return;
+  }
+  const long long rl = (long long)req * g.n_layers + p.layer;
+  __shared__ int s_len;
+  if (threadIdx.x == 0) s_len = p.s.length[rl];
+  __syncthreads();
+  const int len = s_len;
+  const bool fits = (long long)len + p.n_tok <= g.max_context;
+
+  if (fits) {
+    const int t0 = blockIdx.x * APP_TOKENS_PER_CTA;
+    const int nt = min(APP_TOKENS_PER_CTA, p.n_tok - t0);
+    // index keys: d_idx bytes per token, 16-byte vectors
+    const int kvec = g.d_idx / 16;
+    const int4* ksrc = reinterpret_cast<const int4*>(p.keys + ((long long)ri * p.n_tok + t0) * g.d_idx);
+    int4* kdst = reinterpret_cast<int4*>(p.s.idx_keys + (rl * g.max_context + len + t0) * g.d_idx);
+    for (int e = threadIdx.x; e < nt * kvec; e += APP_THREADS) kdst[e] = ksrc[e];
+    // K/V rows -> pinned host store (writes cross the host link)
+    const int rvec = g.row_bytes / 16;
+    const int4* rsrc = reinterpret_cast<const int4*>(p.kv_rows + ((long long)ri * p.n_tok + t0) * g.row_elems);
+    int4* rdst = reinterpret_cast<int4*>(p.s.host_kv + (rl * g.max_context + len + t0) * g.row_elems);
+    const int total = nt * rvec;
+    for (int e = threadIdx.x; e < total; e += 4 * APP_THREADS) {
+      int4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (e + u * APP_THREADS < total) v[u] = rsrc[e + u * APP_THREADS];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (e + u * APP_THREADS < total) rdst[e + u * APP_THREADS] = v[u];
+    }
+  }
+
+  // The last CTA of this request (all others have read `len` by then) advances
+  // the length and resets the arrival counter for the next call.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&p.s.app_counter[req], 1u);
+    if (prev == gridDim.x - 1) {
+      p.s.app_counter[req] = 0;
+      if (fits) {
+        p.s.length[rl] = len + p.n_tok;
+        atomicAdd(&p.s.glob[1], (unsigned long long)p.n_tok * g.row_bytes);
+      } else {
+        set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
+      }
+    }
+  }
+}
+
+__global__ void init_order_kernel(int32_t* order, long long n_lists, int B) {
+  const long long total = n_lists * B;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x)
+    order[i] = (int32_t)(i % B);
+}
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st) {
+  dim3 grid((p.n_tok + APP_TOKENS_PER_CTA - 1) / APP_TOKENS_PER_CTA, p.n_req);
+  append_kernel<<<grid, APP_THREADS, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_init_order(int32_t* order, long long n_lists, int B, cudaStream_t st) {
+  const long long total = n_lists * B;
+  int blocks = (int)std::min<long long>((total + 255) / 256, 4096);
+  if (blocks < 1) blocks = 1;
+  init_order_kernel<<<blocks, 256, 0, st>>>(order, n_lists, B);
+  return cudaGetLastError();
+}
+
+}  // namespace hs

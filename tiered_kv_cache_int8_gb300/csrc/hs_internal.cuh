@@ -1,0 +1,255 @@
+// Internal declarations shared by the CUDA translation units of the library:
+// the handle, the per-kernel parameter blocks, launch helpers and small
+// device-side primitives (PTX wrappers for mbarriers and bulk copies, block scans).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/hs.h"
+
+namespace hs {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// ---- geometry fixed by the kernels ------------------------------------------
+constexpr int IDX_THREADS = 512;     // indexer + top-k CTA
+constexpr int IDX_CLUSTER = 8;       // CTAs (one cluster) per request
+constexpr int IDX_TILE_BYTES = 16384;
+constexpr int IDX_STAGES = 3;
+constexpr int IDX_BINS = 4096;       // radix digit: 12 bits, two levels cover 24-bit keys
+constexpr int IDX_KEY_BIAS = 1 << 22;  // |score| <= 128*128*256 = 2^22 for d_idx <= 256
+
+constexpr int RES_THREADS = 512;     // RESOLVE CTA
+constexpr int RES_CLUSTER = 8;       // CTAs per request: rank 0 updates metadata, all copy
+
+constexpr int ATT_THREADS = 256;     // attention CTA: 8 warps
+constexpr int ATT_WARPS = 8;
+constexpr int ATT_SUBTILE = 16;      // rows per warp per tile
+constexpr int ATT_SPLIT = 128;       // selection ordinals per CTA (fixed: output independent of B)
+constexpr int ATT_STAGES = 2;
+constexpr int ATT_ROW_PAD = 16;      // bytes of padding per row in shared memory (bank spread)
+
+constexpr int APP_THREADS = 256;
+constexpr int APP_TOKENS_PER_CTA = 16;
+
+// one bounded wait gives up after this many nanoseconds of wall time
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+
+// ---- parameter blocks -------------------------------------------------------
+struct Geometry {
+  int n_layers, max_requests, max_context;
+  int h_q, h_kv, d_qk, d_v, shared_kv, d_idx, top_k, hot_slots;
+  int row_elems, row_bytes, v_off;
+};
+
+struct DeviceState {
+  uint16_t* host_kv;       // device alias of the pinned host store [R][L][Nmax][row]
+  uint16_t* hot;           // [R][L][B][row]
+  int8_t* idx_keys;        // [R][L][Nmax][d_idx]
+  int32_t* page;           // [R][L][Nmax]
+  int32_t* reverse;        // [R][L][B]
+  int32_t* stamp;          // [R][L][B]
+  int32_t* order;          // [R][L][B]  slots by (stamp, slot) ascending
+  int32_t* length;         // [R][L]
+  int32_t* step;           // [R][L]
+  unsigned long long* hits;    // [R][L]
+  unsigned long long* misses;  // [R][L]
+  unsigned long long* glob;    // [0] h2d bytes, [1] d2h bytes
+  unsigned int* dev_error;     // sticky HS_DEVERR_* bits
+  // scratch (one call in flight per handle)
+  int32_t* sel;            // [R][k]
+  int32_t* slot_of_sel;    // [R][k]
+  float* part_o;           // [R][parts][h_q][d_v]
+  float* part_ml;          // [R][parts][h_q][2]
+  unsigned int* att_counter;   // [R]
+  unsigned int* app_counter;   // [R]
+};
+
+struct AppendParams {
+  Geometry g;
+  DeviceState s;
+  int layer, n_req, n_tok;
+  const int32_t* req_ids;
+  const uint16_t* kv_rows;
+  const int8_t* keys;
+};
+
+struct DecodeParams {
+  Geometry g;
+  DeviceState s;
+  int layer, n_req;
+  const int32_t* req_ids;
+  const int8_t* q_idx;
+  const uint16_t* q;
+  uint16_t* out;
+  int32_t* sel_out;
+  float scale_log2;        // softmax scale * log2(e)
+  int idx_chunk_max;       // positions per indexer CTA the shared memory holds
+  int att_parts;           // partial results per request (splits x slices)
+};
+
+}  // namespace hs
+
+// ---- the handle -----------------------------------------------------------------
+struct hs_handle {
+  hs_config_t cfg;
+  hs::Geometry g;
+  hs::DeviceState s;
+  uint16_t* host_kv_host = nullptr;   // host view of the pinned store
+  float scale_log2 = 0.f;
+  int idx_chunk_max = 0;
+  size_t idx_smem = 0, res_smem = 0, att_smem = 0;
+  int att_parts = 0;
+  size_t host_bytes = 0, hot_bytes = 0, index_bytes = 0, meta_bytes = 0;
+  uint64_t decode_calls = 0, append_calls = 0;
+  std::vector<void*> dev_allocs;
+  // timing
+  bool timing = false;
+  struct Timed { int kind; cudaEvent_t a, b; };
+  std::vector<Timed> timed;
+  std::vector<cudaEvent_t> event_pool;
+  std::string last_error;
+};
+
+namespace hs {
+
+// launchers (one per kernel translation unit); return a CUDA error code
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+cudaError_t launch_indexer_topk(const DecodeParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_attention(const DecodeParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_init_order(int32_t* order, long long n_lists, int B, cudaStream_t st);
+
+// shared-memory needs, checked against the device limit at create time
+size_t indexer_smem_bytes(const Geometry& g, int chunk_max);
+size_t resolve_smem_bytes(const Geometry& g);
+size_t attention_smem_bytes(const Geometry& g);
+int attention_parts(const Geometry& g);
+cudaError_t prepare_indexer(size_t smem);
+cudaError_t prepare_resolve(size_t smem);
+cudaError_t prepare_attention(const Geometry& g, size_t smem);
+
+// ---- device helpers -------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity; gives up after WAIT_LIMIT_NS and
+// returns false (the caller records HS_DEVERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
+// Bulk (non-tensor) asynchronous copy global -> this CTA's shared memory,
+// completing `bytes` transaction bytes on `bar`.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ int4 ld_nc_v4(const void* p) {
+  int4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void set_error(unsigned int* word, unsigned int bit) { atomicOr(word, bit); }
+
+// bf16 pair (low half = element 0) -> two floats
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Exclusive prefix sum of one value per thread over the block.  `scratch` holds
+// NT/32 + 1 ints; every thread of the block must call it.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int x = lane < NW ? scratch[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(FULL_MASK, xi, o);
+      if (lane >= o) xi += n;
+    }
+    if (lane < NW) scratch[lane] = xi - x;
+    if (lane == NW - 1) scratch[NW] = xi;
+  }
+  __syncthreads();
+  const int excl = incl - v + scratch[warp];
+  if (total) *total = scratch[NW];
+  __syncthreads();
+  return excl;
+}
+
+template <int NT>
+__device__ __forceinline__ int block_sum(int v, int* scratch) {
+  int total;
+  block_exclusive_scan<NT>(v, scratch, &total);
+  return total;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace hs
