@@ -1,0 +1,580 @@
+#!/usr/bin/env python3
+"""Benchmark: decode layer-steps/s of top-k sparse attention over a two-level
+KV cache, on the batch-16 / 4-layer / 32K-context workload by default.
+
+One step = one decode step of every request over every layer: for each layer,
+append the new token (index key to HBM, K/V row to the pinned host copy) and
+run hs_decode_layer (indexer + top-k, RESOLVE, attention).  value = layer-steps
+per second (one layer-step = one layer of all R requests); tokens/s = R * steps
+per second.  The timed steps are captured once into a CUDA graph and replayed,
+as a serving engine's decode graph would be; every kernel still runs every
+step.  e2e repeats the measurement through the Python API with the step's
+inputs copied host -> device and the outputs device -> host inside the loop.
+
+--impl reference times the CPU oracle on the same workload (a bounded sample
+of requests per step, scaled to the whole batch).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workload as wl  # noqa: E402
+
+METRIC = "sparse-decode layer-steps/s"
+UNIT = "layer-steps/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def rank_workload(w: wl.Workload, rank: int, world: int) -> wl.Workload:
+    """Weak scaling: each rank serves its own batch of requests (its own seed)."""
+    if world <= 1:
+        return w
+    import dataclasses
+    return dataclasses.replace(w, seed=w.base_seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's time (torch.distributed, timing only: no data-path collective)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "tiered_kv_cache_int8_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+KERNEL_FILES = {"append": "hs_append.cu", "indexer": "hs_score.cu",
+                "topk_resolve": "hs_resolve.cu", "attention": "hs_attention.cu"}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this kernel source and workload (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha") != kernel_source_hash(KERNEL_FILES[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic traffic of one layer of all R requests (per kernel)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float) -> dict:
+    """HBM and host-link bytes the method itself moves for one layer-step of all
+    requests.  n_ctx: context length of each request at this step; misses: rows
+    pulled from host memory in this layer-step (all requests)."""
+    k_eff = np.minimum(w.top_k, n_ctx)
+    R = w.n_requests
+    row = w.row_bytes
+    hbm = {
+        "append": R * (row + 2 * w.d_idx) + R * 4,
+        "indexer": float((n_ctx * w.d_idx).sum()) + R * w.d_idx,
+        "topk_resolve": float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12,
+        "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2 + misses * row,
+    }
+    link = {"append": R * row, "indexer": 0.0, "topk_resolve": 0.0, "attention": misses * row}
+    return {"hbm": hbm, "link": link}
+
+
+def link_peak_gbs(dev, nbytes=1 << 30, reps=5) -> float:
+    """Pinned host -> device cudaMemcpyAsync bandwidth (best of reps)."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w: wl.Workload, requests, layers, steps: int) -> tuple[float, int]:
+    """Times the oracle over decode steps 0..steps-1 of the given (request, layer)
+    pairs; returns (seconds, request-layer-steps).  Input generation is not timed."""
+    from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+    total = 0.0
+    units = 0
+    for l in layers:
+        for r in requests:
+            keys = wl.idx_keys_upto(w, r, l, steps)
+            walk = wl.query_walk(w, r, l, steps)
+            kv = wl.prefill_kv(w, r, l)
+            n0 = int(w.contexts()[r])
+            qs = [wl.step_query(w, r, l, t) for t in range(steps)]
+            app = [wl.step_kv_row(w, r, l, t) for t in range(steps)]
+            cache = LRUHotCache(w.hot_slots)
+            t0 = time.perf_counter()
+            for t in range(steps):
+                n = n0 + t + 1
+                s = indexer_scores_many(keys[:n], walk[t])[:, 0]
+                sel = topk_select(s, w.top_k)
+                cache.step(sel)
+                rows = np.empty((sel.size, w.row_elems), np.uint16)
+                pre = sel < n0
+                rows[pre] = kv[sel[pre]]
+                for i in np.nonzero(~pre)[0]:
+                    rows[i] = app[int(sel[i] - n0)]
+                sparse_attention(qs[t], rows, h_kv=w.h_kv, d_qk=w.d_qk, d_v=w.d_v, v_offset=w.v_offset)
+            total += time.perf_counter() - t0
+            units += steps
+    return total, units
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) -> dict | None:
+    import torch
+
+    from tiered_kv_cache_int8_gb300 import HiSparseCache
+    from tiered_kv_cache_int8_gb300.build import build
+
+    build()
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    W, K = args.warmup, args.steps
+    T = W + 2 * K + args.e2e_steps
+    R, L = w.n_requests, w.n_layers
+    cache = HiSparseCache(n_layers=L, max_requests=R, max_context=w.max_context(T), h_q=w.h_q, h_kv=w.h_kv,
+                          d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k, hot_slots=w.hot_slots,
+                          shared_kv=w.shared_kv, device=dev_index)
+
+    # ---- prefill: generate each (request, layer) context and append it -----------
+    t_pre = time.time()
+    n0 = w.contexts()
+    stage_kv = torch.empty((int(n0.max()), w.row_elems), dtype=torch.int16, pin_memory=True)
+    stage_keys = torch.empty((int(n0.max()), w.d_idx), dtype=torch.int8, pin_memory=True)
+    for l in range(L):
+        for r in range(R):
+            n = int(n0[r])
+            wl.prefill_kv(w, r, l, out=stage_kv[:n].numpy().view(np.uint16))
+            stage_keys[:n].numpy()[:] = wl.prefill_idx_keys(w, r, l)
+            rid = torch.tensor([r], dtype=torch.int32, device=dev)
+            cache.append(l, stage_kv[:n].view(1, n, w.row_elems), stage_keys[:n].view(1, n, w.d_idx), req_ids=rid)
+            torch.cuda.synchronize(dev)   # the staging buffer is reused
+    del stage_kv, stage_keys
+    t_pre = time.time() - t_pre
+
+    # ---- per-step inputs, resident in HBM -----------------------------------------
+    walks = np.stack([np.stack([wl.query_walk(w, r, l, T) for r in range(R)]) for l in range(L)])  # [L,R,T,d]
+    q_idx = torch.from_numpy(np.ascontiguousarray(walks.transpose(2, 0, 1, 3))).to(dev)             # [T,L,R,d]
+    q_host = np.empty((T, L, R, w.h_q, w.d_qk), np.uint16)
+    kv_host = np.empty((T, L, R, 1, w.row_elems), np.uint16)
+    key_host = np.empty((T, L, R, 1, w.d_idx), np.int8)
+    for t in range(T):
+        for l in range(L):
+            for r in range(R):
+                q_host[t, l, r] = wl.step_query(w, r, l, t)
+                kv_host[t, l, r, 0] = wl.step_kv_row(w, r, l, t)
+                key_host[t, l, r, 0] = wl.step_idx_key(w, r, l, t)
+    q_dev = torch.from_numpy(q_host.view(np.int16)).to(dev)
+    kv_dev = torch.from_numpy(kv_host.view(np.int16)).to(dev)
+    key_dev = torch.from_numpy(key_host).to(dev)
+    out_dev = torch.empty((L, R, w.h_q, w.d_v), dtype=torch.bfloat16, device=dev)
+
+    stream = torch.cuda.Stream(dev)
+
+    def enqueue_step(t):
+        for l in range(L):
+            cache.append(l, kv_dev[t, l], key_dev[t, l], stream=stream)
+            cache.decode_layer(l, q_idx[t, l], q_dev[t, l], out=out_dev[l], stream=stream)
+
+    # ---- warm-up (eager) ------------------------------------------------------------
+    with torch.cuda.stream(stream):
+        for t in range(W):
+            enqueue_step(t)
+    torch.cuda.synchronize(dev)
+    st0 = cache.stats()
+
+    def capture(t_begin, t_end):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for t in range(t_begin, t_end):
+                    enqueue_step(t)
+        torch.cuda.synchronize(dev)
+        return g
+
+    def replay_timed(g):
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(e0.elapsed_time(e1), world)
+
+    # ---- timed region A: the K steps as one CUDA graph (the headline value) ----------
+    graph = capture(W, W + K)
+    clocks = ClockSampler(dev_index)
+    clocks.start()
+    ms_total = replay_timed(graph)
+    clk = clocks.stop()
+    del graph
+    st1 = cache.stats()
+    misses = st1["misses"] - st0["misses"]
+    hits = st1["hits"] - st0["hits"]
+
+    # ---- timed region B: the next K steps with every kernel bracketed by events -------
+    cache.set_timing(True)
+    graph_b = capture(W + K, W + 2 * K)
+    ms_total_b = replay_timed(graph_b)
+    ktimes = cache.kernel_times()
+    timing_mode = "events in the CUDA graph"
+    if sum(n for _, n in ktimes.values()) == 0:   # event nodes not timeable: time eagerly
+        cache.set_timing(True)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for t in range(W + K, W + 2 * K):
+                enqueue_step(t)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_total_b = e0.elapsed_time(e1)
+        ktimes = cache.kernel_times()
+        timing_mode = "events around eager launches"
+    cache.set_timing(False)
+    del graph_b
+    st2 = cache.stats()
+    misses_b = st2["misses"] - st1["misses"]
+    n_launch_per_step = L * 4
+
+    # ---- e2e through the API: host inputs in, host outputs out, every step ------------
+    E = args.e2e_steps
+    q_pin = torch.from_numpy(q_host.view(np.int16)).pin_memory()
+    kv_pin = torch.from_numpy(kv_host.view(np.int16)).pin_memory()
+    key_pin = torch.from_numpy(key_host).pin_memory()
+    qi_pin = torch.from_numpy(np.ascontiguousarray(walks.transpose(2, 0, 1, 3))).pin_memory()
+    out_pin = torch.empty((L, R, w.h_q, w.d_v), dtype=torch.bfloat16).pin_memory()
+    qi_d = torch.empty((L, R, w.d_idx), dtype=torch.int8, device=dev)
+    q_d = torch.empty((L, R, w.h_q, w.d_qk), dtype=torch.int16, device=dev)
+    kv_d = torch.empty((L, R, 1, w.row_elems), dtype=torch.int16, device=dev)
+    key_d = torch.empty((L, R, 1, w.d_idx), dtype=torch.int8, device=dev)
+    h2d = qi_d.numel() + 2 * q_d.numel() + 2 * kv_d.numel() + key_d.numel()
+    d2h = 2 * out_pin.numel()
+    e2e_val = None
+    if E > 0:
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for t in range(W + 2 * K, W + 2 * K + E):
+                qi_d.copy_(qi_pin[t], non_blocking=True)
+                q_d.copy_(q_pin[t], non_blocking=True)
+                kv_d.copy_(kv_pin[t], non_blocking=True)
+                key_d.copy_(key_pin[t], non_blocking=True)
+                for l in range(L):
+                    cache.append(l, kv_d[l], key_d[l], stream=stream)
+                    cache.decode_layer(l, qi_d[l], q_d[l], out=out_dev[l], stream=stream)
+                out_pin.copy_(out_dev, non_blocking=True)
+                stream.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        e2e_val = world * E * L / e2e_s
+    final = cache.stats()
+    dev_err = final["device_error"]
+
+    # ---- numbers -------------------------------------------------------------------
+    ms_step = ms_total / K
+    value = world * K * L / (ms_total * 1e-3)
+    tokens = world * K * R / (ms_total * 1e-3)
+    # algorithmic traffic of a timed region (contexts grow by one per step)
+    def region_bytes(t_begin, n_miss):
+        hb = {k: 0.0 for k in KERNEL_FILES}
+        lb = {k: 0.0 for k in KERNEL_FILES}
+        for t in range(t_begin, t_begin + K):
+            ab = algorithmic_bytes(w, n0 + t + 1, n_miss / (K * L))
+            for k in KERNEL_FILES:
+                hb[k] += ab["hbm"][k] * L
+                lb[k] += ab["link"][k] * L
+        return hb, lb
+
+    hb_a, lb_a = region_bytes(W, misses)
+    hbm_total = sum(hb_a.values())
+    link_total = sum(lb_a.values())
+    per_kernel_bytes, per_kernel_link = region_bytes(W + K, misses_b)
+    peak_hbm, peak_src = measured_peaks()
+    peak_link = link_peak_gbs(dev)
+    t_roof = max(hbm_total / (peak_hbm * 1e9), link_total / (peak_link * 1e9))
+    step_frac = t_roof / (ms_total * 1e-3)
+    kernels = {}
+    for k, (ms, n) in ktimes.items():
+        if n == 0:
+            continue
+        avg = ms / n
+        kernels[k] = {"launches": n, "avg_us": round(avg * 1e3, 3), "share": None,
+                      "hbm_gbs": round(per_kernel_bytes[k] / n / (avg * 1e-3) / 1e9, 1),
+                      "link_gbs": round(per_kernel_link[k] / n / (avg * 1e-3) / 1e9, 1),
+                      "hbm_bytes_per_launch": int(per_kernel_bytes[k] / n),
+                      "link_bytes_per_launch": int(per_kernel_link[k] / n)}
+    tot_k = sum(v["avg_us"] * v["launches"] for v in kernels.values()) or 1.0
+    for v in kernels.values():
+        v["share"] = round(v["avg_us"] * v["launches"] / tot_k, 4)
+    dom = max(kernels, key=lambda k: kernels[k]["share"]) if kernels else None
+    roof = None
+    if dom:
+        ach = kernels[dom]["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
+                "frac": round(ach / peak_hbm, 4), "peak_source": peak_src,
+                "traffic": ncu_traffic(dom, w.name), "bytes_per_launch": kernels[dom]["hbm_bytes_per_launch"]}
+    gpu_launches = sum(v["launches"] for v in kernels.values())
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "dtype_detail": "int8 indexer (int32 accumulate); bf16 K/V and q, fp32 softmax/accumulate",
+        "data": "synthetic (seeded; N(0,1) bf16 K/V, uniform int8 index keys, random-walk int8 queries)",
+        "config": {"workload": w.name, "requests": R, "layers": L, "context": int(n0[0]) if w.context_range is None
+                   else [int(n0.min()), int(n0.max())], "h_q": w.h_q, "h_kv": w.h_kv, "d_qk": w.d_qk,
+                   "d_v": w.d_v, "d_idx": w.d_idx, "top_k": w.top_k, "hot_slots": w.hot_slots,
+                   "sigma": w.sigma, "parallelism": f"requests sharded, {world} independent cache(s)",
+                   "l2": f"inputs larger than L2: {hbm_total / K / 2**20:.0f} MiB read per step > 129 MiB",
+                   "timed": "one CUDA graph of the timed steps, replayed once"},
+        "kernel_timing": {"mode": timing_mode, "steps": K, "ms_per_step": round(ms_total_b / K, 4)},
+        "tokens_per_s": round(tokens, 1),
+        "hbm_gbs": round(hbm_total / (ms_total * 1e-3) / 1e9, 1),
+        "link_gbs": round(link_total / (ms_total * 1e-3) / 1e9, 2),
+        "link_peak_gbs": round(peak_link, 1),
+        "miss_rate": round(misses / max(1, hits + misses), 5),
+        "misses_per_layer_step": round(misses / (K * L), 1),
+        "step_roofline": {"t_roof_ms": round(t_roof * 1e3 / K, 4), "t_meas_ms": round(ms_step, 4),
+                          "frac": round(step_frac, 4), "hbm_bytes_per_step": int(hbm_total / K),
+                          "link_bytes_per_step": int(link_total / K),
+                          "bound": "hbm" if hbm_total / peak_hbm >= link_total / peak_link else "link"},
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": gpu_launches if gpu_launches else n_launch_per_step * K,
+        "e2e": {"value": round(e2e_val, 2) if e2e_val else None, "unit": UNIT, "steps": E,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "clocks": clk,
+        "prefill_s": round(t_pre, 1),
+        "device_error": dev_err,
+    }
+    cache.close()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=61)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="hisparse", choices=["hisparse", "reference"])
+    ap.add_argument("--workload", default="batch16_32k", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--hot-slots", type=int, default=None)
+    ap.add_argument("--sigma", type=float, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "hisparse" else "gloo"
+        dist.init_process_group(backend=backend)
+
+    w = wl.WORKLOADS[args.workload]
+    if args.hot_slots or args.sigma is not None:
+        w = wl.stress_point(args.hot_slots or w.hot_slots, args.sigma if args.sigma is not None else w.sigma) \
+            if args.workload == "stress_128k" else wl.make_workload(
+                args.workload, **({"hot_slots": args.hot_slots} if args.hot_slots else {}),
+                **({"sigma": args.sigma} if args.sigma is not None else {}))
+    w = rank_workload(w, rank, world)
+
+    sr, sl, ss = (int(x) for x in args.cpu_sample.split("x"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, w, sr, sl, ss)
+        print(json.dumps(res), flush=True)
+        return
+
+    res = run_hisparse(args, w, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            secs, units = oracle_sample(w, range(sr), range(sl), ss)
+            per_unit = secs / units
+            res["cpu_baseline"] = {"value": round(1.0 / (per_unit * w.n_requests), 4), "unit": UNIT,
+                                   "cores": cpu_threads(), "kind": "oracle",
+                                   "sample": f"{sr} request(s) x {sl} layer(s) x {ss} decode steps of {w.name} "
+                                             f"({units} request-layer-steps, {secs:.1f} s), scaled by "
+                                             f"{w.n_requests} requests per layer-step"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
+    """The CPU oracle as the reference arm: each step runs the oracle on a
+    bounded sample (sr requests x sl layers, one decode step each) and the rate
+    is scaled to the whole batch."""
+    W, K = args.warmup, args.steps
+    steps = W + K
+    # the oracle replays steps 0..steps-1 of each sampled (request, layer); the
+    # first W are the warm-up
+    from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+    per_step = []
+    for l in range(sl):
+        for r in range(sr):
+            keys = wl.idx_keys_upto(w, r, l, steps)
+            walk = wl.query_walk(w, r, l, steps)
+            kv = wl.prefill_kv(w, r, l)
+            n0 = int(w.contexts()[r])
+            cache = LRUHotCache(w.hot_slots)
+            for t in range(steps):
+                q = wl.step_query(w, r, l, t)
+                app = [wl.step_kv_row(w, r, l, u) for u in range(t + 1)]
+                t0 = time.perf_counter()
+                n = n0 + t + 1
+                s = indexer_scores_many(keys[:n], walk[t])[:, 0]
+                sel = topk_select(s, w.top_k)
+                cache.step(sel)
+                rows = np.empty((sel.size, w.row_elems), np.uint16)
+                pre = sel < n0
+                rows[pre] = kv[sel[pre]]
+                for i in np.nonzero(~pre)[0]:
+                    rows[i] = app[int(sel[i] - n0)]
+                sparse_attention(q, rows, h_kv=w.h_kv, d_qk=w.d_qk, d_v=w.d_v, v_offset=w.v_offset)
+                if t >= W:
+                    per_step.append(time.perf_counter() - t0)
+    per_unit = float(np.mean(per_step))
+    value = 1.0 / (per_unit * w.n_requests)
+    sample = (f"{sr} request(s) x {sl} layer(s) per step, steps {W}..{steps - 1} of {w.name}, "
+              f"scaled by {w.n_requests} requests per layer-step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 0,
+            "steps": K, "warmup": W, "ms_per_step": round(per_unit * w.n_requests * w.n_layers * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": w.name},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+if __name__ == "__main__":
+    main()

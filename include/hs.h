@@ -65,7 +65,9 @@ extern "C" {
  *   GQA: d_qk = d_v = 128, h_q % h_kv == 0, h_kv in {1,2,4,8}, h_q/h_kv <= 16.
  *   latent: h_kv = 1, d_qk = 576, d_v = 512, h_q in {16, 32, 64, 128}.
  *   d_idx in {16, 32, 64, 128, 256}; 1 <= top_k <= hot_slots <= 16384;
- *   top_k <= 8192; 1 <= max_context <= HS_MAX_CONTEXT; n_layers, max_requests >= 1.
+ *   top_k <= 8192; 1 <= max_context <= HS_MAX_CONTEXT (and the indexer's shared
+ *   memory must hold max_context / cluster scores); n_layers >= 1;
+ *   1 <= max_requests <= 4096.
  */
 #define HS_MAX_CONTEXT (1 << 20)
 
@@ -83,6 +85,10 @@ typedef struct hs_config {
   int32_t hot_slots;     /* B: HBM slots per (request, layer) */
   float softmax_scale;   /* 0 => 1/sqrt(d_qk) */
   int32_t device;        /* CUDA device ordinal */
+  int32_t fetch_mode;    /* where missed rows are copied host -> HBM (results identical):
+                            0 = by loader warps of the attention kernel, overlapping the
+                                HBM reads of the hit rows (default);
+                            1 = inside the RESOLVE kernel, before attention starts */
 } hs_config_t;
 
 typedef struct hs_handle hs_handle_t;
@@ -196,10 +202,10 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream);
  * synchronises and returns, per kernel kind (HS_K_*), the summed milliseconds and
  * the number of launches since the last hs_set_timing(h, 1).
  */
-#define HS_K_APPEND 0
-#define HS_K_INDEXER_TOPK 1
-#define HS_K_RESOLVE 2
-#define HS_K_ATTENTION 3
+#define HS_K_APPEND 0        /* append kernel */
+#define HS_K_INDEXER 1       /* scores of every position + first-digit histogram */
+#define HS_K_TOPK_RESOLVE 2  /* exact top-k + RESOLVE (and the host fetch when fetch_mode = 1) */
+#define HS_K_ATTENTION 3     /* attention (and the host fetch when fetch_mode = 0) */
 #define HS_K_COUNT 4
 int hs_set_timing(hs_handle_t* h, int32_t enable);
 int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launches /*[HS_K_COUNT]*/);

@@ -53,8 +53,8 @@ def check_order(order, stamp):
     assert order.tolist() == keys
 
 
-def full_parity(w, steps, hot_slots=None):
-    cache = make_cache(w, steps, hot_slots)
+def full_parity(w, steps, hot_slots=None, fetch_mode=0):
+    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode)
     prefill(cache, w)
     inp = StepInputs(w, steps)
     got = run_steps(cache, w, inp, steps, collect_meta=True)
@@ -117,6 +117,31 @@ def test_k_equals_B_and_high_sigma():
     w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=3000, top_k=256,
                          hot_slots=256, steps=5, sigma=0.3)
     full_parity(w, 5)
+
+
+def test_fetch_in_resolve_matches_the_oracle():
+    # fetch_mode 1: RESOLVE itself copies the missed rows (the pages' placement)
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=4100, top_k=256,
+                         hot_slots=512, steps=4)
+    full_parity(w, 4, fetch_mode=1)
+
+
+def test_fetch_modes_are_bit_identical():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=6000, top_k=512,
+                         hot_slots=768, steps=4, sigma=0.3)
+    runs = []
+    for mode in (0, 1):
+        cache = make_cache(w, 4, fetch_mode=mode)
+        prefill(cache, w)
+        runs.append(run_steps(cache, w, StepInputs(w, 4), 4, collect_meta=True))
+        cache.close()
+    for key in runs[0]["out"]:
+        assert np.array_equal(runs[0]["out"][key], runs[1]["out"][key])
+        assert np.array_equal(runs[0]["sel"][key], runs[1]["sel"][key])
+        for a, b in zip(runs[0]["meta"][key], runs[1]["meta"][key]):
+            for x, y in zip(a[:4], b[:4]):
+                assert np.array_equal(x, y)
+            assert a[4] == b[4]
 
 
 def test_output_bit_identical_across_B():

@@ -30,12 +30,13 @@ bool is_pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 
 // Returns "" when the configuration is one the kernels support, else the reason.
 std::string check_config(const hs_config_t& c) {
   if (c.n_layers < 1) return "n_layers must be >= 1";
-  if (c.max_requests < 1 || c.max_requests > 65535) return "max_requests must be in [1, 65535]";
+  if (c.max_requests < 1 || c.max_requests > 4096) return "max_requests must be in [1, 4096]";
   if (c.max_context < 1 || c.max_context > HS_MAX_CONTEXT) return "max_context must be in [1, HS_MAX_CONTEXT]";
   if (!is_pow2_in(c.d_idx, 16, 256)) return "d_idx must be one of 16, 32, 64, 128, 256";
   if (c.top_k < 1 || c.top_k > 8192) return "top_k must be in [1, 8192]";
   if (c.hot_slots < c.top_k || c.hot_slots > 16384) return "hot_slots must be in [top_k, 16384]";
   if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return "softmax_scale must be finite and >= 0";
+  if (c.fetch_mode != 0 && c.fetch_mode != 1) return "fetch_mode must be 0 or 1";
   if (c.shared_kv == 0) {
     if (c.d_qk != 128 || c.d_v != 128) return "GQA rows: d_qk = d_v = 128 required";
     if (!is_pow2_in(c.h_kv, 1, 8)) return "GQA rows: h_kv must be one of 1, 2, 4, 8";
@@ -106,9 +107,14 @@ cudaError_t timed_launch(hs_handle* h, int kind, cudaStream_t st, F&& launch) {
   if (!h->timing) return launch();
   cudaEvent_t a = take_event(h), b = take_event(h);
   if (!a || !b) return launch();
-  cudaEventRecord(a, st);
+  // Under stream capture the events become external event-record nodes, so
+  // they can still be timed after the graph is replayed.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  cudaEventRecordWithFlags(a, st, flags);
   cudaError_t e = launch();
-  cudaEventRecord(b, st);
+  cudaEventRecordWithFlags(b, st, flags);
   h->timed.push_back({kind, a, b});
   return e;
 }
@@ -192,19 +198,19 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, cfg->device);
   if (!cluster_ok) return fail_free(HS_ERR_CONFIG, "hs_create: device has no thread-block cluster launch");
 
-  int chunk = (cfg->max_context + hs::IDX_CLUSTER - 1) / hs::IDX_CLUSTER;
-  h->idx_chunk_max = (chunk + 31) & ~31;
-  h->idx_smem = hs::indexer_smem_bytes(g, h->idx_chunk_max);
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
+  h->score_stride = ((long long)cfg->max_context + 3) & ~3LL;
+  h->idx_smem = hs::score_smem_bytes(g);
   h->res_smem = hs::resolve_smem_bytes(g);
   h->att_smem = hs::attention_smem_bytes(g);
   h->att_parts = hs::attention_parts(g);
   if (h->idx_smem > (size_t)smem_optin)
-    return fail_free(HS_ERR_CONFIG, "hs_create: max_context too large for the indexer's shared memory (" +
-                                        std::to_string(h->idx_smem) + " > " + std::to_string(smem_optin) + " bytes)");
+    return fail_free(HS_ERR_CONFIG, "hs_create: max_requests too large for the score kernel's shared memory");
   if (h->res_smem > (size_t)smem_optin)
     return fail_free(HS_ERR_CONFIG, "hs_create: top_k / hot_slots too large for RESOLVE's shared memory");
   if (h->att_smem > (size_t)smem_optin)
-    return fail_free(HS_ERR_CONFIG, "hs_create: row too wide for the attention kernel's shared memory");
+    return fail_free(HS_ERR_CONFIG,
+                     "hs_create: rows or max_requests too large for the attention kernel's shared memory");
 
   const size_t R = cfg->max_requests, Lr = cfg->n_layers, N = cfg->max_context, B = cfg->hot_slots;
   const size_t K = cfg->top_k;
@@ -248,6 +254,8 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.misses, R * Lr * 8, true},
       {(void**)&s.glob, 4 * 8, true},
       {(void**)&s.dev_error, 16, true},
+      {(void**)&s.scores, R * (size_t)h->score_stride * 4, false},
+      {(void**)&s.hist, R * (size_t)hs::IDX_BINS * 4, false},
       {(void**)&s.sel, R * K * 4, false},
       {(void**)&s.slot_of_sel, R * K * 4, false},
       {(void**)&s.part_o, R * (size_t)h->att_parts * g.h_q * g.d_v * 4, false},
@@ -278,10 +286,11 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.dev_error, 0, 16) == cudaSuccess;
   ok = ok && cudaMemset(s.slot_of_sel, 0, R * K * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.att_counter, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.hist, 0, R * (size_t)hs::IDX_BINS * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
   ok = ok && hs::launch_init_order(s.order, (long long)(R * Lr), (int)B, 0) == cudaSuccess;
   if (!ok) return fail_free(HS_ERR_CUDA, "hs_create: initialising the metadata failed");
-  if ((e = hs::prepare_indexer(h->idx_smem)) != cudaSuccess ||
+  if ((e = hs::prepare_score(g, h->idx_smem)) != cudaSuccess ||
       (e = hs::prepare_resolve(h->res_smem)) != cudaSuccess ||
       (e = hs::prepare_attention(g, h->att_smem)) != cudaSuccess)
     return fail_free(HS_ERR_CUDA, std::string("hs_create: kernel set-up failed: ") + cudaGetErrorName(e));
@@ -353,13 +362,16 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.out = static_cast<uint16_t*>(out);
   p.sel_out = sel_out;
   p.scale_log2 = h->scale_log2;
-  p.idx_chunk_max = h->idx_chunk_max;
+  p.score_stride = h->score_stride;
+  p.score_grid = h->num_sms;
   p.att_parts = h->att_parts;
+  p.att_grid = h->num_sms;
+  p.fetch_mode = h->cfg.fetch_mode;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = timed_launch(h, HS_K_INDEXER_TOPK, st, [&] { return hs::launch_indexer_topk(p, h->idx_smem, st); });
-  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: indexer/top-k launch");
-  e = timed_launch(h, HS_K_RESOLVE, st, [&] { return hs::launch_resolve(p, h->res_smem, st); });
-  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: RESOLVE launch");
+  cudaError_t e = timed_launch(h, HS_K_INDEXER, st, [&] { return hs::launch_score(p, h->idx_smem, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: indexer launch");
+  e = timed_launch(h, HS_K_TOPK_RESOLVE, st, [&] { return hs::launch_resolve(p, h->res_smem, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: top-k/RESOLVE launch");
   e = timed_launch(h, HS_K_ATTENTION, st, [&] { return hs::launch_attention(p, h->att_smem, st); });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: attention launch");
   ++h->decode_calls;

@@ -49,6 +49,18 @@ __global__ void __launch_bounds__(APP_THREADS) append_kernel(AppendParams p) {
     }
   }
 
+  if (gridDim.x == 1) {   // one CTA per request (decode-time appends): no arrival counter
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (fits) {
+        p.s.length[rl] = len + p.n_tok;
+        atomicAdd(&p.s.glob[1], (unsigned long long)p.n_tok * g.row_bytes);
+      } else {
+        set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
+      }
+    }
+    return;
+  }
   // The last CTA of this request (all others have read `len` by then) advances
   // the length and resets the arrival counter for the next call.
   __threadfence();

@@ -16,21 +16,18 @@ namespace hs {
 constexpr unsigned FULL_MASK = 0xffffffffu;
 
 // ---- geometry fixed by the kernels ------------------------------------------
-constexpr int IDX_THREADS = 512;     // indexer + top-k CTA
-constexpr int IDX_CLUSTER = 8;       // CTAs (one cluster) per request
-constexpr int IDX_TILE_BYTES = 16384;
-constexpr int IDX_STAGES = 3;
+constexpr int SC_THREADS = 256;      // score kernel CTA
+constexpr int IDX_TILE_BYTES = 32768;  // index keys per bulk copy (one tile)
+constexpr int IDX_STAGES = 4;
 constexpr int IDX_BINS = 4096;       // radix digit: 12 bits, two levels cover 24-bit keys
 constexpr int IDX_KEY_BIAS = 1 << 22;  // |score| <= 128*128*256 = 2^22 for d_idx <= 256
 
-constexpr int RES_THREADS = 512;     // RESOLVE CTA
-constexpr int RES_CLUSTER = 8;       // CTAs per request: rank 0 updates metadata, all copy
+constexpr int RES_THREADS = 1024;    // top-k + RESOLVE CTA (one per request)
 
-constexpr int ATT_THREADS = 256;     // attention CTA: 8 warps
-constexpr int ATT_WARPS = 8;
+// slot_of_sel entries of rows RESOLVE left for the attention kernel to fetch
+constexpr int HS_SLOT_MISS_FLAG = 0x40000000;
+
 constexpr int ATT_SUBTILE = 16;      // rows per warp per tile
-constexpr int ATT_SPLIT = 128;       // selection ordinals per CTA (fixed: output independent of B)
-constexpr int ATT_STAGES = 2;
 constexpr int ATT_ROW_PAD = 16;      // bytes of padding per row in shared memory (bank spread)
 
 constexpr int APP_THREADS = 256;
@@ -61,6 +58,8 @@ struct DeviceState {
   unsigned long long* glob;    // [0] h2d bytes, [1] d2h bytes
   unsigned int* dev_error;     // sticky HS_DEVERR_* bits
   // scratch (one call in flight per handle)
+  uint32_t* scores;        // [R][score_stride] 24-bit keys of the current call
+  uint32_t* hist;          // [R][4096] high-digit histogram of the current call (zero between calls)
   int32_t* sel;            // [R][k]
   int32_t* slot_of_sel;    // [R][k]
   float* part_o;           // [R][parts][h_q][d_v]
@@ -88,8 +87,11 @@ struct DecodeParams {
   uint16_t* out;
   int32_t* sel_out;
   float scale_log2;        // softmax scale * log2(e)
-  int idx_chunk_max;       // positions per indexer CTA the shared memory holds
-  int att_parts;           // partial results per request (splits x slices)
+  long long score_stride;  // scores row stride (positions, multiple of 4)
+  int score_grid;          // score kernel CTAs
+  int att_parts;           // partial results per request (CTAs x slices)
+  int att_grid;            // attention CTAs (one per SM)
+  int fetch_mode;          // 0: attention kernel fetches misses, 1: RESOLVE does
 };
 
 }  // namespace hs
@@ -101,7 +103,8 @@ struct hs_handle {
   hs::DeviceState s;
   uint16_t* host_kv_host = nullptr;   // host view of the pinned store
   float scale_log2 = 0.f;
-  int idx_chunk_max = 0;
+  int num_sms = 0;
+  long long score_stride = 0;
   size_t idx_smem = 0, res_smem = 0, att_smem = 0;
   int att_parts = 0;
   size_t host_bytes = 0, hot_bytes = 0, index_bytes = 0, meta_bytes = 0;
@@ -119,17 +122,17 @@ namespace hs {
 
 // launchers (one per kernel translation unit); return a CUDA error code
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
-cudaError_t launch_indexer_topk(const DecodeParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_attention(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_init_order(int32_t* order, long long n_lists, int B, cudaStream_t st);
 
 // shared-memory needs, checked against the device limit at create time
-size_t indexer_smem_bytes(const Geometry& g, int chunk_max);
+size_t score_smem_bytes(const Geometry& g);
 size_t resolve_smem_bytes(const Geometry& g);
 size_t attention_smem_bytes(const Geometry& g);
 int attention_parts(const Geometry& g);
-cudaError_t prepare_indexer(size_t smem);
+cudaError_t prepare_score(const Geometry& g, size_t smem);
 cudaError_t prepare_resolve(size_t smem);
 cudaError_t prepare_attention(const Geometry& g, size_t smem);
 

@@ -27,8 +27,8 @@ HS_DEVERR_EMPTY = 0x4
 HS_DEVERR_TIMEOUT = 0x8
 HS_DEVERR_METADATA = 0x10
 
-HS_K_APPEND, HS_K_INDEXER_TOPK, HS_K_RESOLVE, HS_K_ATTENTION, HS_K_COUNT = 0, 1, 2, 3, 4
-KERNEL_NAMES = ("append", "indexer_topk", "resolve", "attention")
+HS_K_APPEND, HS_K_INDEXER, HS_K_TOPK_RESOLVE, HS_K_ATTENTION, HS_K_COUNT = 0, 1, 2, 3, 4
+KERNEL_NAMES = ("append", "indexer", "topk_resolve", "attention")
 
 # the symbols include/hs.h declares
 EXPORTED = ("hs_create", "hs_destroy", "hs_append", "hs_decode_layer", "hs_stats", "hs_snapshot",
@@ -41,7 +41,8 @@ class HsConfig(ctypes.Structure):
                 ("max_context", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
                 ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32), ("shared_kv", ctypes.c_int32),
                 ("d_idx", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hot_slots", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float), ("device", ctypes.c_int32)]
+                ("softmax_scale", ctypes.c_float), ("device", ctypes.c_int32),
+                ("fetch_mode", ctypes.c_int32)]
 
 
 class HsStats(ctypes.Structure):
@@ -122,9 +123,9 @@ class HiSparseCache:
 
     def __init__(self, *, n_layers: int, max_requests: int, max_context: int, h_q: int, h_kv: int,
                  d_qk: int, d_v: int, d_idx: int, top_k: int, hot_slots: int, shared_kv: bool = False,
-                 softmax_scale: float = 0.0, device: int = 0):
+                 softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 0):
         self.cfg = HsConfig(n_layers, max_requests, max_context, h_q, h_kv, d_qk, d_v, int(shared_kv),
-                            d_idx, top_k, hot_slots, softmax_scale, device)
+                            d_idx, top_k, hot_slots, softmax_scale, device, fetch_mode)
         self._h = ctypes.c_void_p()
         rc = lib().hs_create(ctypes.byref(self.cfg), ctypes.byref(self._h))
         if rc != HS_OK:
