@@ -168,13 +168,16 @@ def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float) -> dict:
     k_eff = np.minimum(w.top_k, n_ctx)
     R = w.n_requests
     row = w.row_bytes
+    # the new token's append rides on the decode call (top-k/RESOLVE kernel):
+    # its row is read from HBM and written to the host copy, its key to HBM
     hbm = {
-        "append": R * (row + 2 * w.d_idx) + R * 4,
+        "append": 0.0,
         "indexer": float((n_ctx * w.d_idx).sum()) + R * w.d_idx,
-        "topk_resolve": float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12,
+        "topk_resolve": float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12
+        + R * (w.row_bytes + 2 * w.d_idx + 4),
         "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2 + misses * row,
     }
-    link = {"append": R * row, "indexer": 0.0, "topk_resolve": 0.0, "attention": misses * row}
+    link = {"append": 0.0, "indexer": 0.0, "topk_resolve": R * row, "attention": misses * row}
     return {"hbm": hbm, "link": link}
 
 
@@ -258,7 +261,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     R, L = w.n_requests, w.n_layers
     cache = HiSparseCache(n_layers=L, max_requests=R, max_context=w.max_context(T), h_q=w.h_q, h_kv=w.h_kv,
                           d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k, hot_slots=w.hot_slots,
-                          shared_kv=w.shared_kv, device=dev_index)
+                          shared_kv=w.shared_kv, device=dev_index, fetch_mode=args.fetch_mode)
 
     # ---- prefill: generate each (request, layer) context and append it -----------
     t_pre = time.time()
@@ -296,9 +299,9 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     stream = torch.cuda.Stream(dev)
 
     def enqueue_step(t):
-        for l in range(L):
-            cache.append(l, kv_dev[t, l], key_dev[t, l], stream=stream)
-            cache.decode_layer(l, q_idx[t, l], q_dev[t, l], out=out_dev[l], stream=stream)
+        for l in range(L):   # the new token's append rides on the decode call
+            cache.decode_layer(l, q_idx[t, l], q_dev[t, l], out=out_dev[l], stream=stream,
+                               new_kv=kv_dev[t, l], new_keys=key_dev[t, l])
 
     # ---- warm-up (eager) ------------------------------------------------------------
     with torch.cuda.stream(stream):
@@ -363,7 +366,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     del graph_b
     st2 = cache.stats()
     misses_b = st2["misses"] - st1["misses"]
-    n_launch_per_step = L * 4
+    n_launch_per_step = L * 3
 
     # ---- e2e through the API: host inputs in, host outputs out, every step ------------
     E = args.e2e_steps
@@ -389,8 +392,8 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                 kv_d.copy_(kv_pin[t], non_blocking=True)
                 key_d.copy_(key_pin[t], non_blocking=True)
                 for l in range(L):
-                    cache.append(l, kv_d[l], key_d[l], stream=stream)
-                    cache.decode_layer(l, qi_d[l], q_d[l], out=out_dev[l], stream=stream)
+                    cache.decode_layer(l, qi_d[l], q_d[l], out=out_dev[l], stream=stream,
+                                       new_kv=kv_d[l], new_keys=key_d[l])
                 out_pin.copy_(out_dev, non_blocking=True)
                 stream.synchronize()
         e2e_s = max_over_ranks(time.perf_counter() - t0, world)
@@ -452,7 +455,8 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                    "d_v": w.d_v, "d_idx": w.d_idx, "top_k": w.top_k, "hot_slots": w.hot_slots,
                    "sigma": w.sigma, "parallelism": f"requests sharded, {world} independent cache(s)",
                    "l2": f"inputs larger than L2: {hbm_total / K / 2**20:.0f} MiB read per step > 129 MiB",
-                   "timed": "one CUDA graph of the timed steps, replayed once"},
+                   "timed": "one CUDA graph of the timed steps, replayed once",
+                   "fetch_mode": args.fetch_mode},
         "kernel_timing": {"mode": timing_mode, "steps": K, "ms_per_step": round(ms_total_b / K, 4)},
         "tokens_per_s": round(tokens, 1),
         "hbm_gbs": round(hbm_total / (ms_total * 1e-3) / 1e9, 1),
@@ -487,6 +491,8 @@ def main():
     ap.add_argument("--hot-slots", type=int, default=None)
     ap.add_argument("--sigma", type=float, default=None)
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--fetch-mode", type=int, default=0, choices=[0, 1],
+                    help="0: attention kernel fetches missed rows (overlapped); 1: RESOLVE does")
     ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -64,7 +64,7 @@ extern "C" {
  * Supported by the kernels (else HS_ERR_CONFIG):
  *   GQA: d_qk = d_v = 128, h_q % h_kv == 0, h_kv in {1,2,4,8}, h_q/h_kv <= 16.
  *   latent: h_kv = 1, d_qk = 576, d_v = 512, h_q in {16, 32, 64, 128}.
- *   d_idx in {16, 32, 64, 128, 256}; 1 <= top_k <= hot_slots <= 16384;
+ *   d_idx in {16, 32, 64, 128, 256}; 1 <= top_k <= hot_slots <= 16384, hot_slots % 4 == 0;
  *   top_k <= 8192; 1 <= max_context <= HS_MAX_CONTEXT (and the indexer's shared
  *   memory must hold max_context / cluster scores); n_layers >= 1;
  *   1 <= max_requests <= 4096.
@@ -149,24 +149,32 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
 /*
  * hs_decode_layer — one decode layer-step for n_req requests (stream-ordered,
  * no host synchronisation, capturable in a CUDA graph).
- *   req_ids : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
- *   q_idx   : dev int8 [n_req][d_idx]       indexer query
- *   q       : dev bf16 [n_req][h_q][d_qk]   attention query
- *   out     : dev bf16 [n_req][h_q][d_v]    attention output (written)
- *   sel_out : dev int32 [n_req][top_k] or NULL: selected positions, ascending;
- *             entries past k_eff = min(top_k, length) are -1
+ *   req_ids     : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
+ *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned)
+ *   q           : dev bf16 [n_req][h_q][d_qk]   attention query
+ *   out         : dev bf16 [n_req][h_q][d_v]    attention output (written)
+ *   sel_out     : dev int32 [n_req][top_k] or NULL: selected positions, ascending;
+ *                 entries past k_eff = min(top_k, length) are -1
+ *   new_kv_rows : dev bf16 [n_req][row_elems] or NULL (16-byte aligned)
+ *   new_idx_keys: dev int8 [n_req][d_idx] or NULL (both or neither)
+ * With new_kv_rows / new_idx_keys the call first appends one token per request,
+ * exactly as hs_append with n_tok = 1 would (same positions, stores and length
+ * update; a request at max_context gets HS_DEVERR_CAPACITY and no append), but
+ * inside the decode kernels instead of a launch of its own.
  * Per request with N positions: (1) score every position p < N as
  * sum_j q_idx[j] * K_idx[p][j] (exact int32); (2) keep the k_eff highest, ties
- * to the lower position; (3) RESOLVE: hits via the page table, misses pulled from
- * the host copy into LRU victim slots, metadata and stamps updated, step += 1;
- * (4) o_h = sum_i softmax_i(scale * q_h . K_i) V_i over the selected rows in
- * ascending position order, fp32 accumulation, bf16 output.  The output does
- * not depend on hot_slots or on the cache state (bit-identical across B).
- * HS_ERR_INVALID for layer out of range, n_req > max_requests or null buffers.
+ * to the lower position; (3) RESOLVE: hits via the page table, misses assigned to
+ * LRU victim slots, metadata and stamps updated, step += 1, missed rows copied
+ * from the host copy into their slots (by RESOLVE or by the attention kernel,
+ * see fetch_mode); (4) o_h = sum_i softmax_i(scale * q_h . K_i) V_i over the
+ * selected rows in ascending position order, fp32 accumulation, bf16 output.
+ * The output does not depend on hot_slots or on the cache state (bit-identical
+ * across B).  HS_ERR_INVALID for layer out of range, n_req > max_requests, null or
+ * misaligned buffers.
  */
 int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_ids,
                     const int8_t* q_idx, const void* q, void* out, int32_t* sel_out,
-                    void* stream);
+                    const void* new_kv_rows, const int8_t* new_idx_keys, void* stream);
 
 /*
  * hs_stats — synchronise the device and fill *out with cumulative counters and

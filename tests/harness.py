@@ -68,9 +68,10 @@ class StepInputs:
 
 
 def run_steps(cache, w: wl.Workload, inp: StepInputs, steps: int, layers=None, *, collect_sel=True,
-              collect_out=True, collect_meta=False, t0: int = 0):
-    """Runs decode steps t0..t0+steps-1 (append then decode per layer); returns
-    per-(layer, step) selections, outputs and (optionally) metadata snapshots."""
+              collect_out=True, collect_meta=False, t0: int = 0, fused: bool = False):
+    """Runs decode steps t0..t0+steps-1 (append then decode per layer; with
+    fused=True the append rides on the decode call); returns per-(layer, step)
+    selections, outputs and (optionally) metadata snapshots."""
     torch = torch_mod()
     dev = torch.device("cuda", cache.device)
     layers = range(w.n_layers) if layers is None else layers
@@ -78,9 +79,13 @@ def run_steps(cache, w: wl.Workload, inp: StepInputs, steps: int, layers=None, *
     res = {"sel": {}, "out": {}, "meta": {}}
     for t in range(t0, t0 + steps):
         for l in layers:
-            cache.append(l, inp.kv[l, t], inp.keys[l, t])
             sel = torch.full((R, w.top_k), -7, dtype=torch.int32, device=dev)
-            out = cache.decode_layer(l, inp.q_idx[l, t], inp.q[l, t], sel_out=sel)
+            if fused:
+                out = cache.decode_layer(l, inp.q_idx[l, t], inp.q[l, t], sel_out=sel, new_kv=inp.kv[l, t],
+                                         new_keys=inp.keys[l, t])
+            else:
+                cache.append(l, inp.kv[l, t], inp.keys[l, t])
+                out = cache.decode_layer(l, inp.q_idx[l, t], inp.q[l, t], sel_out=sel)
             if collect_sel:
                 res["sel"][l, t] = sel.cpu().numpy()
             if collect_out:

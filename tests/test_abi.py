@@ -77,7 +77,7 @@ def test_null_arguments(L):
     h = ctypes.c_void_p()
     assert L.hs_create(None, ctypes.byref(h)) == hs.HS_ERR_INVALID
     assert L.hs_append(None, 0, 1, None, 1, None, None, None) == hs.HS_ERR_INVALID
-    assert L.hs_decode_layer(None, 0, 1, None, None, None, None, None, None) == hs.HS_ERR_INVALID
+    assert L.hs_decode_layer(None, 0, 1, None, None, None, None, None, None, None, None) == hs.HS_ERR_INVALID
     assert L.hs_stats(None, None) == hs.HS_ERR_INVALID
     assert L.hs_snapshot(None, 0, 0, None, 0, None, None, None, None) == hs.HS_ERR_INVALID
     L.hs_destroy(None)

@@ -53,11 +53,11 @@ def check_order(order, stamp):
     assert order.tolist() == keys
 
 
-def full_parity(w, steps, hot_slots=None, fetch_mode=0):
+def full_parity(w, steps, hot_slots=None, fetch_mode=0, fused=False):
     cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode)
     prefill(cache, w)
     inp = StepInputs(w, steps)
-    got = run_steps(cache, w, inp, steps, collect_meta=True)
+    got = run_steps(cache, w, inp, steps, collect_meta=True, fused=fused)
     B = hot_slots or w.hot_slots
     worst = (0.0, 0.0)
     for l in range(w.n_layers):
@@ -124,6 +124,32 @@ def test_fetch_in_resolve_matches_the_oracle():
     w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=4100, top_k=256,
                          hot_slots=512, steps=4)
     full_parity(w, 4, fetch_mode=1)
+
+
+@pytest.mark.parametrize("fetch_mode", [0, 1])
+def test_append_fused_into_decode_matches_the_oracle(fetch_mode):
+    # the new token rides on hs_decode_layer; it is selectable in the same step
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=2900, top_k=256,
+                         hot_slots=512, steps=5)
+    full_parity(w, 5, fetch_mode=fetch_mode, fused=True)
+
+
+def test_fused_and_separate_append_are_bit_identical():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=5000, top_k=384,
+                         hot_slots=512, steps=4, sigma=0.3)
+    runs = []
+    for fused in (False, True):
+        cache = make_cache(w, 4)
+        prefill(cache, w)
+        runs.append(run_steps(cache, w, StepInputs(w, 4), 4, collect_meta=True, fused=fused))
+        cache.close()
+    for key in runs[0]["out"]:
+        assert np.array_equal(runs[0]["out"][key], runs[1]["out"][key])
+        assert np.array_equal(runs[0]["sel"][key], runs[1]["sel"][key])
+        for a, b in zip(runs[0]["meta"][key], runs[1]["meta"][key]):
+            for x, y in zip(a[:4], b[:4]):
+                assert np.array_equal(x, y)
+            assert a[4] == b[4]
 
 
 def test_fetch_modes_are_bit_identical():

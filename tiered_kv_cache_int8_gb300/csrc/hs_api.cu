@@ -35,6 +35,7 @@ std::string check_config(const hs_config_t& c) {
   if (!is_pow2_in(c.d_idx, 16, 256)) return "d_idx must be one of 16, 32, 64, 128, 256";
   if (c.top_k < 1 || c.top_k > 8192) return "top_k must be in [1, 8192]";
   if (c.hot_slots < c.top_k || c.hot_slots > 16384) return "hot_slots must be in [top_k, 16384]";
+  if (c.hot_slots % 4 != 0) return "hot_slots must be a multiple of 4";
   if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return "softmax_scale must be finite and >= 0";
   if (c.fetch_mode != 0 && c.fetch_mode != 1) return "fetch_mode must be 0 or 1";
   if (c.shared_kv == 0) {
@@ -338,7 +339,8 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
 }
 
 int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_ids, const int8_t* q_idx,
-                    const void* q, void* out, int32_t* sel_out, void* stream) {
+                    const void* q, void* out, int32_t* sel_out, const void* new_kv_rows,
+                    const int8_t* new_idx_keys, void* stream) {
   if (!h) return HS_ERR_INVALID;
   if (layer < 0 || layer >= h->cfg.n_layers)
     return set_err(h, HS_ERR_INVALID, "hs_decode_layer: layer out of range");
@@ -350,6 +352,10 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   if ((reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(out) & 1u) ||
       (reinterpret_cast<uintptr_t>(sel_out) & 3u))
     return set_err(h, HS_ERR_INVALID, "hs_decode_layer: misaligned q / out / sel_out");
+  if ((new_kv_rows == nullptr) != (new_idx_keys == nullptr))
+    return set_err(h, HS_ERR_INVALID, "hs_decode_layer: new_kv_rows and new_idx_keys go together");
+  if (new_kv_rows && (!aligned16(new_kv_rows) || !aligned16(new_idx_keys)))
+    return set_err(h, HS_ERR_INVALID, "hs_decode_layer: new_kv_rows and new_idx_keys must be 16-byte aligned");
   use_device(h);
   hs::DecodeParams p;
   p.g = h->g;
@@ -361,6 +367,8 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   p.sel_out = sel_out;
+  p.new_kv = static_cast<const uint16_t*>(new_kv_rows);
+  p.new_keys = new_idx_keys;
   p.scale_log2 = h->scale_log2;
   p.score_stride = h->score_stride;
   p.score_grid = h->num_sms;
@@ -375,6 +383,7 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   e = timed_launch(h, HS_K_ATTENTION, st, [&] { return hs::launch_attention(p, h->att_smem, st); });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: attention launch");
   ++h->decode_calls;
+  if (new_kv_rows) ++h->append_calls;
   return HS_OK;
 }
 

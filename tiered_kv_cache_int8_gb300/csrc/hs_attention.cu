@@ -1,33 +1,43 @@
-// Sparse attention over the selected rows (GQA, head dim 128): a persistent,
-// warp-specialised flash-decode kernel whose per-request partial results are
-// merged in a fixed order by the last CTA that touched the request.
+// Sparse attention over the selected rows (GQA, head dim 128), fused with the
+// host fetch of the rows RESOLVE found missing: a persistent, warp-specialised
+// flash-decode kernel whose per-request partial results are merged in a fixed
+// order by the last CTA that touched the request.
 //
 // Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
 // for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
 // formula 2: softmax(Q K^T / sqrt(d_k), masked to the retrieved entries) V —
 // read as a softmax over the selected positions only.  "KV卸载上主机:
 // HiSparse、PDD与DDR4回收", "论文1：HiSparse": the attention math is unchanged
-// by the cache, so the result must not depend on where the rows sit.
+// by the cache, so the result must not depend on where the rows sit; missed rows
+// come from the authoritative copy in pinned host memory.
 //
 // Design (sm_103a).  The kernel is HBM-bound (each K/V byte is used by the
 // h_q / h_kv query heads of its group only), so the goal is to keep enough
-// bytes in flight on every SM with as few instructions per byte as possible:
+// bytes in flight on every SM with as few instructions per byte as possible,
+// and to keep the host-link latency of missed rows off the critical path:
 //  * Persistent grid, one CTA per SM.  The selected rows of all requests are
 //    flattened into units of TILE rows (16 rows per warp slice); CTA c takes
 //    units [c*U/G, (c+1)*U/G).  The split depends only on the k_eff of each
 //    request and on the grid size, never on B or on slot placement.
-//  * Warp specialisation: warp 8 is the producer.  For each unit it copies every
-//    selected row (all kv heads: one contiguous hot slot) HBM -> shared memory
-//    with one 1-D bulk async copy (cp.async.bulk, mbarrier completion) into a
-//    row-padded layout (16 extra bytes per row put the 8 rows of an ldmatrix
-//    phase in 8 different bank groups); up to 4 stages with full/empty mbarriers.
+//  * Warp 8 (stager) copies every hit row of a unit (all kv heads: one
+//    contiguous hot slot) HBM -> shared memory with one 1-D bulk async copy
+//    (cp.async.bulk, mbarrier completion) into a row-padded layout (16 extra bytes
+//    per row put the 8 rows of an ldmatrix phase in 8 different bank groups);
+//    up to 4 stages with full/empty mbarriers.
+//  * Warp 9 (fetcher) walks the same units, independently and ahead of the
+//    stager, and copies each missed row from the mapped pinned host copy into a
+//    ring of shared-memory row slots with 16-byte cp.async; every ring slot has
+//    its own full/empty mbarriers.  With few misses per CTA every host fetch is in
+//    flight from the start of the kernel; the ring bounds how far ahead it runs.
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
+//    Each row is read from its stage row or, for a missed row, its ring slot.
 //    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
-//    with the group's query heads as the 16 M rows (zero-padded).  The tensor
-//    cores are used to cut the instruction count per byte, not for throughput;
-//    K and V fragments come straight from shared memory with ldmatrix (.trans
-//    for V).  Online softmax in fp32 (exp2, scale * log2(e) applied to the fp32
-//    scores); P enters the second product as bf16.
+//    with the group's query heads as the 16 M rows (zero-padded): the tensor
+//    cores cut the instruction count per byte; K and V fragments come straight
+//    from shared memory with ldmatrix (.trans for V).  Online softmax in fp32
+//    (exp2, scale * log2(e) applied to the fp32 scores); P enters the second
+//    product as bf16.  Consumer warp 0 also writes each fetched row into its hot
+//    slot (bulk shared -> global copy), so later steps hit.
 //  * Every (CTA, request, slice) writes a partial (m, l, o) to scratch; the last
 //    CTA to finish a request (arrival counter) merges its partials in CTA order
 //    and writes bf16.  Rows are visited in ascending selection order and the
@@ -42,33 +52,43 @@ namespace {
 
 constexpr int D = 128;
 constexpr int NCONS = 8;                   // consumer warps
-constexpr int NLOAD = 2;                   // loader warps (host fetch of missed rows)
-constexpr int PRODUCER = NCONS;            // warp index of the producer
-constexpr int THREADS = (NCONS + 1 + NLOAD) * 32;
+constexpr int STAGER = NCONS;              // warp index of the stager
+constexpr int FETCHER = NCONS + 1;         // warp index of the host fetcher
+constexpr int THREADS = (NCONS + 2) * 32;
 constexpr int MAX_STAGES = 4;
+constexpr int MAX_RING = 32;    // preferred ring entries
+constexpr int RING_CAP = 128;   // most ring entries (a unit has at most 128 rows)
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct AttLayout {
-  size_t bar, mlist, prefix, stage, stage_bytes, total;
+  size_t bar, meta, prefix, rowc, stage, stage_bytes, ring, total;
 };
 
-// Shared memory: barriers and flags | unit prefix of every request | stages.
-__host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage) {
+constexpr int ROWCACHE = 2048;   // (slot, position) pairs of the CTA's rows kept in shared memory
+
+// Shared memory: barriers | per-stage miss masks | per-request tables | stages | ring.
+__host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage, int nring) {
   AttLayout L;
   const int nslice = NCONS / g.h_kv;
   const int tile = ATT_SUBTILE * nslice;
+  const size_t row_stride = (size_t)g.row_bytes + ATT_ROW_PAD;
   size_t off = 0;
   L.bar = off;
-  off += 256;   // full[4], empty[4], abort flag, loaded-unit count, miss-list count
-  L.mlist = off;
-  off += align_up((size_t)tile * 4, 128);   // the loader's miss list of one unit
+  off += 8 * (2 * MAX_STAGES + 2 * RING_CAP) + 16 + 4 * RING_CAP;   // barriers, abort flag, ring hot slots
+  off = align_up(off, 128);
+  L.meta = off;
+  off += align_up((size_t)MAX_STAGES * 4 * 4, 128);   // miss mask of each stage (up to 128 rows)
   L.prefix = off;
-  off += align_up((size_t)(g.max_requests + 1) * 4, 128);
+  off += align_up((size_t)(g.max_requests + 1) * 4 * 3, 128);   // unit prefix, k_eff, request id
+  L.rowc = off;
+  off += (size_t)ROWCACHE * 8;
   L.stage = off;
-  L.stage_bytes = align_up((size_t)tile * (g.row_bytes + ATT_ROW_PAD), 128);
+  L.stage_bytes = align_up((size_t)tile * row_stride, 128);
   off += (size_t)nstage * L.stage_bytes;
-  L.total = off;
+  L.ring = off;
+  off += (size_t)nring * row_stride;
+  L.total = align_up(off, 128);
   return L;
 }
 
@@ -101,6 +121,24 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// The mbarrier receives one arrival once all of this thread's earlier cp.async
+// copies have landed (its pending count is raised first, so the phase cannot
+// complete before then).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bulk copy shared -> global (hot slot), tracked per thread by bulk async-groups.
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Bounded wait that also gives up once another warp has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned int* err) {
@@ -119,32 +157,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-__device__ __forceinline__ void st_release(volatile int* p, int v) {
-  asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_addr((const void*)p)), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire(volatile int* p) {
-  int v;
-  asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr((const void*)p)) : "memory");
-  return v;
-}
-
-// Barrier 1 over the loader warps, returning the OR of `pred` over them.
-__device__ __forceinline__ bool loader_bar_or(bool pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, %2, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((int)pred), "n"(NLOAD * 32)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // CTA owning flattened unit u when U units are split over G CTAs as [c*U/G, (c+1)*U/G).
 __device__ __forceinline__ int owner_of(long long u, long long U, int G) {
   return (int)(((u + 1) * G + U - 1) / U) - 1;
@@ -159,18 +171,36 @@ int attention_parts(const Geometry& g) {
   return (units + 1) * nslice;
 }
 
-static int attention_stages(const Geometry& g, size_t limit) {
-  for (int ns = MAX_STAGES; ns >= 2; --ns)
-    if (att_layout(g, ns).total <= limit) return ns;
-  return 2;
+// Stages and ring entries that fit.  The ring must hold every missed row of one
+// unit (TILE rows): the consumers wait for all of a unit's rows before computing,
+// so a smaller ring could never be filled.  Three stages where that still fits.
+static void attention_shape(const Geometry& g, size_t limit, int* nstage, int* nring) {
+  const int tile = ATT_SUBTILE * (NCONS / g.h_kv);
+  const int min_ring = tile;
+  for (int ns = 3; ns >= 2; --ns) {
+    int nr = tile > MAX_RING ? tile : MAX_RING;
+    while (nr > min_ring && att_layout(g, ns, nr).total > limit) --nr;
+    if (att_layout(g, ns, nr).total <= limit) {
+      *nstage = ns;
+      *nring = nr;
+      return;
+    }
+  }
+  *nstage = 2;
+  *nring = min_ring;
 }
 
-size_t attention_smem_bytes(const Geometry& g) { return att_layout(g, attention_stages(g, 227 * 1024)).total; }
+size_t attention_smem_bytes(const Geometry& g) {
+  int ns, nr;
+  attention_shape(g, 227 * 1024, &ns, &nr);
+  return att_layout(g, ns, nr).total;
+}
 
 template <int G, int HKV>
-__global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, int nstage) {
+__global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, int nstage, int nring) {
   constexpr int NSLICE = NCONS / HKV;
   constexpr int TILE = ATT_SUBTILE * NSLICE;
+  constexpr int NJ = (TILE + 31) / 32;   // 32-row words of a unit
   constexpr int HQ = HKV * G;
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -178,16 +208,22 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   const int c = blockIdx.x;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  const AttLayout L = att_layout(g, nstage);
+  const AttLayout L = att_layout(g, nstage, nring);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
   uint64_t* empty = full + MAX_STAGES;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L.bar + 128);
-  volatile int* loaded = reinterpret_cast<volatile int*>(smem_raw + L.bar + 132);   // units fetched
-  volatile int* mcount = reinterpret_cast<volatile int*>(smem_raw + L.bar + 136);   // [2], per unit parity
-  int* mlist = reinterpret_cast<int*>(smem_raw + L.mlist);
+  uint64_t* rfull = empty + MAX_STAGES;
+  uint64_t* rempty = rfull + RING_CAP;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(rempty + RING_CAP);
+  int* ring_slot = const_cast<int*>(abort_flag) + 4;   // hot slot of the row in each ring entry
+  unsigned* stage_miss = reinterpret_cast<unsigned*>(smem_raw + L.meta);   // [stage][4] miss mask
   int* prefix = reinterpret_cast<int*>(smem_raw + L.prefix);   // prefix[i] = first unit of request i
+  int* kk_s = prefix + (g.max_requests + 1);                    // k_eff of request i
+  int* req_s = kk_s + (g.max_requests + 1);                     // request id of request i
+  int2* rowc = reinterpret_cast<int2*>(smem_raw + L.rowc);   // [unit k][row i] -> (slot_of_sel, position)
   unsigned char* stage = smem_raw + L.stage;
+  unsigned char* ring = smem_raw + L.ring;
   const int row_stride = g.row_bytes + ATT_ROW_PAD;
+  const int rvec = g.row_bytes / 16;
   __shared__ int scan_tmp[THREADS / 32 + 1];
   __shared__ int s_last[2];
 
@@ -201,6 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       int kk = 0;
       if (req >= 0 && req < g.max_requests) kk = min(K, p.s.length[(long long)req * g.n_layers + p.layer]);
       units = (kk + TILE - 1) / TILE;
+      kk_s[i] = kk;
+      req_s[i] = req;
       if (kk == 0 && i % (int)gridDim.x == c) {   // nothing selected: the output is defined as 0
         uint16_t* out = p.out + (long long)i * HQ * D;
         for (int e = 0; e < HQ * D; ++e) out[e] = 0;
@@ -218,25 +256,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NCONS);
     }
+    for (int k = 0; k < nring; ++k) {
+      mbar_init(&rfull[k], 1);
+      mbar_init(&rempty[k], NCONS);
+    }
     *abort_flag = 0;
-    *loaded = 0;
-    mcount[0] = 0;
-    mcount[1] = 0;
     fence_mbar_init();
   }
-  // Zero the stages once: rows past the end of a request are never copied, and
-  // their (masked, weight-0) values must be finite.
-  for (size_t e = (size_t)tid * 16; e < (size_t)nstage * L.stage_bytes; e += (size_t)THREADS * 16)
-    *reinterpret_cast<int4*>(stage + e) = make_int4(0, 0, 0, 0);
   __syncthreads();
   const long long U = carry;
-  // Only the first min(grid, U) CTAs take part, so every taking part owns at
+  if (U == 0) return;
+  // Only the first min(grid, U) CTAs take part, so every one taking part owns at
   // least one unit (the arrival counts below rely on that).
   const int Gc = (int)min((long long)gridDim.x, U);
   if (c >= Gc) return;
   const long long u0 = (long long)c * U / Gc, u1 = (long long)(c + 1) * U / Gc;
 
-  // first request with units at or after u0: the last i with prefix[i] <= u0 < prefix[i+1]
+  // first request with units at or after u0
   int ri = 0;
   {
     int lo = 0, hi = p.n_req - 1;
@@ -249,129 +285,167 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     while (prefix[ri + 1] <= u0) ++ri;
   }
 
-  if (warp == PRODUCER) {
-    // ============================ producer warp ============================
+  // Slot ids and positions of this CTA's rows, read once: in the loop below the
+  // stager and the fetcher then issue no global loads, which would otherwise
+  // queue behind the fetcher's slow host-memory requests.
+  const int ncache = (int)min((long long)ROWCACHE / TILE, u1 - u0);   // units whose rows are cached
+  for (int e0 = tid; e0 < ncache * TILE; e0 += 4 * THREADS) {   // all loads in flight together
+    int2 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + q * THREADS;
+      v[q] = make_int2(0, 0);
+      if (e < ncache * TILE) {
+        const long long u = u0 + e / TILE;
+        int lo = ri, hi = p.n_req - 1;   // request of unit u: last r with prefix[r] <= u
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= u) lo = mid;
+          else hi = mid - 1;
+        }
+        const int row = (int)(u - prefix[lo]) * TILE + e % TILE;
+        if (row < kk_s[lo]) {
+          const long long gi = (long long)lo * K + row;
+          v[q] = make_int2(p.s.slot_of_sel[gi], p.s.sel[gi]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (e0 + q * THREADS < ncache * TILE) rowc[e0 + q * THREADS] = v[q];
+  }
+  __syncthreads();
+  // (slot_of_sel, position) of row i of unit u (request r, first row row0)
+  auto row_info = [&](long long u, int r, int row0, int i) -> int2 {
+    const long long k = u - u0;
+    if (k < ncache) return rowc[k * TILE + i];
+    const long long gi = (long long)r * K + row0 + i;
+    return make_int2(p.s.slot_of_sel[gi], p.s.sel[gi]);
+  };
+
+  if (warp == STAGER) {
+    // ============================ stager warp ============================
+    // Unit u's slots are loaded one unit ahead, so the global loads overlap the
+    // wait for a free stage.
     int r = ri;
+    int slots[NJ];
+    int cur_r = -1, cur_nr = 0;
+    auto load_unit = [&](long long u, int (&sl)[NJ], int& ur, int& unr) {
+      while (prefix[r + 1] <= u) ++r;
+      ur = r;
+      const int urow0 = (int)(u - prefix[r]) * TILE;
+      unr = min(TILE, kk_s[r] - urow0);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int i = lane + 32 * j;
+        sl[j] = i < unr ? row_info(u, r, urow0, i).x : 0;
+      }
+    };
+    load_unit(u0, slots, cur_r, cur_nr);
     int s = 0;
     long long it = 0;
     for (long long u = u0; u < u1; ++u, ++it) {
-      while (prefix[r + 1] <= u) ++r;
-      const int req = p.req_ids ? p.req_ids[r] : r;
-      const long long rl = (long long)req * g.n_layers + p.layer;
-      const int kk = min(K, p.s.length[rl]);
-      const int row0 = (int)(u - prefix[r]) * TILE;
-      const int nr = min(TILE, kk - row0);
-      if (it >= nstage) {
-        if (!wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag, p.s.dev_error)) break;
-      }
-      const int32_t* sos = p.s.slot_of_sel + (long long)r * K + row0;
-      int slots[TILE / 32 > 0 ? TILE / 32 : 1];
-      bool miss = false;
-#pragma unroll
-      for (int j = 0; j < (TILE + 31) / 32; ++j) {
-        const int i = lane + 32 * j;
-        slots[j] = i < nr ? sos[i] : 0;
-        miss |= (slots[j] & HS_SLOT_MISS_FLAG) != 0;
-      }
-      if (__any_sync(FULL_MASK, miss)) {
-        // the loader warps copy this unit's missed rows into their slots first
-        const unsigned long long t_start = global_timer_ns();
-        bool ok = true;
-        for (uint32_t spin = 0; ld_acquire(loaded) < it + 1; ++spin) {
-          if ((spin & 255u) == 0 && (*abort_flag || global_timer_ns() - t_start > WAIT_LIMIT_NS)) {
-            if (!*abort_flag && lane == 0) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-        }
-        if (!__all_sync(FULL_MASK, ok)) break;
-        fence_proxy_async_global();
-      }
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * g.row_bytes));
-      }
-      __syncwarp();
+      int nslots[NJ];
+      int n_r = cur_r, n_nr = 0;
+      if (u + 1 < u1) load_unit(u + 1, nslots, n_r, n_nr);
+      if (it >= nstage &&
+          !__all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
+                                               p.s.dev_error)))
+        break;
+      const int nr = cur_nr;
+      const long long rl = (long long)req_s[cur_r] * g.n_layers + p.layer;
+      unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
       const unsigned char* hot =
           reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
+      unsigned miss_bits[NJ];
+      int hit_rows = nr;
 #pragma unroll
-      for (int j = 0; j < (TILE + 31) / 32; ++j) {
+      for (int j = 0; j < NJ; ++j) {
         const int i = lane + 32 * j;
-        if (i < nr) {
-          int slot = slots[j] & ~HS_SLOT_MISS_FLAG;
+        miss_bits[j] = __ballot_sync(FULL_MASK, i < nr && (slots[j] & HS_SLOT_MISS_FLAG) != 0);
+        hit_rows -= __popc(miss_bits[j]);
+        if (lane == j) stage_miss[s * 4 + j] = miss_bits[j];
+      }
+      if (lane >= NJ && lane < 4) stage_miss[s * 4 + lane] = 0u;
+      // rows past the end of a request: zero them so their masked (weight-0)
+      // values stay finite
+      if (nr < TILE) {
+        for (int e = lane; e < (TILE - nr) * rvec; e += 32) {
+          const int i = nr + e / rvec;
+          *reinterpret_cast<int4*>(st_s + (size_t)i * row_stride + (e % rvec) * 16) = make_int4(0, 0, 0, 0);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(hit_rows * g.row_bytes));
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int i = lane + 32 * j;
+        if (i < nr && !((miss_bits[j] >> lane) & 1u)) {
+          int slot = slots[j];
           if (slot < 0 || slot >= g.hot_slots) {   // never expected: keep the copy in bounds
             set_error(p.s.dev_error, HS_DEVERR_METADATA);
             slot = 0;
           }
-          bulk_g2s(stage + (size_t)s * L.stage_bytes + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes,
-                   (uint32_t)g.row_bytes, &full[s]);
+          bulk_g2s(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
+                   &full[s]);
         }
       }
       s = (s + 1 == nstage) ? 0 : s + 1;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) slots[j] = nslots[j];
+      cur_r = n_r;
+      cur_nr = n_nr;
     }
-  } else if (warp > PRODUCER) {
-    // ===================== loader warps: host fetch of missed rows =====================
-    // For each unit in order: list the rows RESOLVE flagged as misses, copy them
-    // from the mapped pinned host copy into their hot slots (16-byte loads, 8 in
-    // flight per thread), make the writes visible to the bulk-copy proxy, then
-    // publish the unit count the producer waits on.
-    const int lt = (warp - PRODUCER - 1) * 32 + lane;
-    constexpr int NLT = NLOAD * 32;
-    const int rvec = g.row_bytes / 16;
+  } else if (warp == FETCHER) {
+    // ============================ fetcher warp ============================
+    // Missed rows of every unit, in unit and row order, each into the next ring
+    // entry (FIFO); the consumers release entries in the same order.
     int r = ri;
-    long long it = 0;
-    for (long long u = u0; u < u1; ++u, ++it) {
+    long long k = 0;   // ring entries handed out so far
+    bool stop = false;
+    for (long long u = u0; u < u1 && !stop; ++u) {
       while (prefix[r + 1] <= u) ++r;
-      const int req = p.req_ids ? p.req_ids[r] : r;
-      const long long rl = (long long)req * g.n_layers + p.layer;
-      const int kk = min(K, p.s.length[rl]);
       const int row0 = (int)(u - prefix[r]) * TILE;
-      const int nr = min(TILE, kk - row0);
-      const int32_t* sos = p.s.slot_of_sel + (long long)r * K + row0;
-      const int32_t* selp = p.s.sel + (long long)r * K + row0;
-      volatile int* cnt = mcount + (it & 1);
-      for (int i = lt; i < nr; i += NLT)
-        if (sos[i] & HS_SLOT_MISS_FLAG) mlist[atomicAdd((int*)cnt, 1)] = i;
-      asm volatile("bar.sync 1, %0;" ::"n"(NLT) : "memory");
-      const int nm = *cnt;
-      // the other counter was last read before the barrier above and is next
-      // written after the barrier below
-      if (lt == 0) mcount[(it + 1) & 1] = 0;
-      if (nm > 0) {
-        const unsigned char* src = reinterpret_cast<const unsigned char*>(p.s.host_kv) +
-                                   (size_t)rl * g.max_context * g.row_bytes;
-        unsigned char* dst = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
-        const int total = nm * rvec;
-        constexpr int U = 8;
-        for (int e0 = lt; e0 < total; e0 += U * NLT) {
-          int4 v[U];
+      const int nr = min(TILE, kk_s[r] - row0);
+      const long long rl = (long long)req_s[r] * g.n_layers + p.layer;
+      const unsigned char* host =
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
 #pragma unroll
-          for (int q = 0; q < U; ++q) {
-            const int e = e0 + q * NLT;
-            if (e < total) {
-              const int row = mlist[e / rvec];
-              v[q] = ld_nc_v4(src + (size_t)selp[row] * g.row_bytes + (e % rvec) * 16);
-            }
+      for (int j = 0; j < NJ; ++j) {
+        const int i = lane + 32 * j;
+        const int2 info = i < nr ? row_info(u, r, row0, i) : make_int2(0, 0);
+        const int sl = info.x;
+        const int ps = info.y;
+        unsigned bits = __ballot_sync(FULL_MASK, i < nr && (sl & HS_SLOT_MISS_FLAG) != 0);
+        while (bits) {
+          const int b0 = __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int e = (int)(k % nring);
+          if (k >= nring &&
+              !__all_sync(FULL_MASK, wait_or_abort(&rempty[e], (uint32_t)(((k / nring) + 1) & 1), abort_flag,
+                                                   p.s.dev_error))) {
+            stop = true;
+            break;
           }
-#pragma unroll
-          for (int q = 0; q < U; ++q) {
-            const int e = e0 + q * NLT;
-            if (e < total) {
-              const int row = mlist[e / rvec];
-              const int slot = sos[row] & ~HS_SLOT_MISS_FLAG;
-              if (slot >= 0 && slot < g.hot_slots)
-                *reinterpret_cast<int4*>(dst + (size_t)slot * g.row_bytes + (e % rvec) * 16) = v[q];
-            }
-          }
+          const int pos = __shfl_sync(FULL_MASK, ps, b0);
+          const int slot = __shfl_sync(FULL_MASK, sl, b0) & ~HS_SLOT_MISS_FLAG;
+          if (lane == 0) ring_slot[e] = slot;
+          const unsigned char* src = host + (size_t)pos * g.row_bytes;
+          unsigned char* dst = ring + (size_t)e * row_stride;
+          for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+          cp_async_mbar_arrive(&rfull[e]);   // balanced: completes when this lane's copies land
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&rfull[e]);
+          ++k;
         }
-        fence_proxy_async_global();
+        if (stop) break;
       }
-      // every loader thread's copies of this unit are done: publish (and agree on abort)
-      const bool stop = loader_bar_or(*abort_flag != 0);
-      if (lt == 0) st_release(loaded, (int)(it + 1));
-      if (stop) break;
     }
+    cp_async_wait_all();
   } else {
     // ============================ consumer warps ============================
     const int kvh = warp % HKV;
@@ -383,6 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
     int r = -1;
     int s = 0;
+    long long rk = 0;   // ring entries consumed so far
 
     auto flush = [&](int req_i) {   // partial (m, l, o) of this (CTA, request, slice)
       float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
@@ -436,27 +511,58 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         m_lo = m_hi = -INFINITY;
         l_lo = l_hi = 0.f;
       }
-      const int req = p.req_ids ? p.req_ids[r] : r;
-      const int kk = min(K, p.s.length[(long long)req * g.n_layers + p.layer]);
+      const int kk = kk_s[r];
       const int row0 = (int)(u - prefix[r]) * TILE;
       const int nv = max(0, min(ATT_SUBTILE, kk - row0 - slice * ATT_SUBTILE));
 
-      if (!wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error)) break;
+      if (!__all_sync(FULL_MASK, wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag,
+                                               p.s.dev_error)))
+        break;
+      // missed rows of this unit: ring entries rk, rk+1, ... in row order
+      unsigned mm[NJ];
+      int nmiss = 0;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        mm[j] = stage_miss[s * 4 + j];
+        nmiss += __popc(mm[j]);
+      }
+      bool ok = true;
+      for (int q = 0; q < nmiss && ok; ++q) {
+        const long long kq = rk + q;
+        ok = __all_sync(FULL_MASK,
+                        wait_or_abort(&rfull[kq % nring], (uint32_t)((kq / nring) & 1), abort_flag, p.s.dev_error));
+      }
+      if (!ok) break;
+      const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+      // shared-memory address of row i of the unit (stage row, or its ring entry)
+      auto row_addr = [&](int i) -> uint32_t {
+        const int j = i >> 5, b = i & 31;
+        unsigned word = 0u;
+        int before = 0;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) {   // static indices only: mm stays in registers
+          if (jj == j) word = mm[jj];
+          if (jj < j) before += __popc(mm[jj]);
+        }
+        if ((word >> b) & 1u) {
+          before += __popc(word & ((1u << b) - 1u));
+          return smem_addr(ring + (size_t)((rk + before) % nring) * row_stride);
+        }
+        return smem_addr(st_s + (size_t)i * row_stride);
+      };
       if (nv > 0) {
-        const uint32_t sbase =
-            smem_addr(stage + (size_t)s * L.stage_bytes) + (uint32_t)(slice * ATT_SUBTILE * row_stride);
+        const int rbase = slice * ATT_SUBTILE;
         // ---- S = Q K^T over the 16 rows (two n-tiles of 8 rows) ----
         float sc[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+          const uint32_t rowa = row_addr(rbase + 8 * j + (lane & 7));
 #pragma unroll
           for (int kp = 0; kp < 4; ++kp) {
             // four 8x8 matrices: K rows 8j..8j+7, dims 32kp + 8*(lane/8) .. +7
             uint32_t b[4];
-            const uint32_t addr = sbase + (uint32_t)((8 * j + (lane & 7)) * row_stride) +
-                                  (uint32_t)((kvh * D + 32 * kp + 8 * (lane >> 3)) * 2);
-            ldsm_x4(b, addr);
+            ldsm_x4(b, rowa + (uint32_t)((kvh * D + 32 * kp + 8 * (lane >> 3)) * 2));
             mma_bf16(sc[j], qa[2 * kp], b[0], b[1]);
             mma_bf16(sc[j], qa[2 * kp + 1], b[2], b[3]);
           }
@@ -467,9 +573,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const bool ok = 8 * j + 2 * tq + e < nv;
-            sc[j][e] = ok ? sc[j][e] * sl2 : -INFINITY;
-            sc[j][2 + e] = ok ? sc[j][2 + e] * sl2 : -INFINITY;
+            const bool okr = 8 * j + 2 * tq + e < nv;
+            sc[j][e] = okr ? sc[j][e] * sl2 : -INFINITY;
+            sc[j][2 + e] = okr ? sc[j][2 + e] * sl2 : -INFINITY;
             mx_lo = fmaxf(mx_lo, sc[j][e]);
             mx_hi = fmaxf(mx_hi, sc[j][2 + e]);
           }
@@ -506,19 +612,38 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         }
         // ---- O += P V: 16 n-tiles of 8 dims, k = the 16 rows ----
         const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
+        const uint32_t rowv = row_addr(rbase + (lane & 7) + 8 * ((lane >> 3) & 1));
 #pragma unroll
         for (int tp = 0; tp < 8; ++tp) {
           // four 8x8 matrices: (rows 0-7 | 8-15) x (dims 16tp..+7 | 16tp+8..+15), transposed
           uint32_t b[4];
-          const uint32_t addr = sbase + (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * row_stride) +
-                                (uint32_t)((g.v_off + kvh * D + 16 * tp + 8 * (lane >> 4)) * 2);
-          ldsm_x4_t(b, addr);
+          ldsm_x4_t(b, rowv + (uint32_t)((g.v_off + kvh * D + 16 * tp + 8 * (lane >> 4)) * 2));
           mma_bf16(o[2 * tp], pfrag, b[0], b[1]);
           mma_bf16(o[2 * tp + 1], pfrag, b[2], b[3]);
         }
       }
+      // consumer warp 0 writes the rows fetched for this unit into their hot slots
+      bool stored = false;
+      if (warp == 0 && nmiss > 0) {
+        fence_proxy_async_smem();   // cp.async writes -> async-proxy reads
+        const long long rl = (long long)req_s[r] * g.n_layers + p.layer;
+        unsigned char* hotw = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
+        for (int q = lane; q < nmiss; q += 32) {
+          const int e = (int)((rk + q) % nring);
+          const int slot = ring_slot[e];
+          if (slot >= 0 && slot < g.hot_slots)
+            bulk_s2g(hotw + (size_t)slot * g.row_bytes, ring + (size_t)e * row_stride, (uint32_t)g.row_bytes);
+        }
+        bulk_commit();
+        stored = true;
+      }
+      if (stored) bulk_wait_read_all();   // ring entries may be refilled only after these reads
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) {
+        for (int q = 0; q < nmiss; ++q) mbar_arrive(&rempty[(rk + q) % nring]);
+        mbar_arrive(&empty[s]);
+      }
+      rk += nmiss;
       s = (s + 1 == nstage) ? 0 : s + 1;
     }
     if (r >= 0 && !*abort_flag) flush(r);
@@ -526,12 +651,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
 
   __syncthreads();
   if (*abort_flag) {
-    // drain copies that may still be in flight (bounded) before the stages go away
-    if (tid == 0)
+    // drain copies that may still be in flight (bounded) before the buffers go away
+    if (tid == 0) {
       for (int s2 = 0; s2 < nstage; ++s2) {
         (void)mbar_wait_bounded(&full[s2], 0);
         (void)mbar_wait_bounded(&full[s2], 1);
       }
+    }
     __syncthreads();
     return;
   }
@@ -557,18 +683,62 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       const float* po = p.s.part_o + (long long)rr * p.att_parts * HQ * D;
       const float* pml = p.s.part_ml + (long long)rr * p.att_parts * HQ * 2;
       uint16_t* out = p.out + (long long)rr * HQ * D;
-      for (int e = tid; e < HQ * D; e += THREADS) {
-        const int h = e / D;
+      // per-head merge weights w[q][h] = 2^(m_q - M_h) / L_h: the (m, l) pairs are
+      // read in one parallel step, then combined per head from shared memory
+      float* wsm = reinterpret_cast<float*>(stage);   // stages and ring are idle now
+      float2* mls = reinterpret_cast<float2*>(wsm + nparts * HQ);
+      // (m, l) pairs in shared memory when they fit beside the weights (always at
+      // the shapes this library accepts on GB300), else read from L2
+      const bool ml_smem = (size_t)nparts * HQ * 12 <= L.total - L.stage;
+      if (ml_smem)
+        for (int e = tid; e < nparts * HQ; e += THREADS) mls[e] = __ldcg(reinterpret_cast<const float2*>(pml) + e);
+      __syncthreads();
+      auto ml = [&](int e) -> float2 { return ml_smem ? mls[e] : __ldcg(reinterpret_cast<const float2*>(pml) + e); };
+      for (int h = tid; h < HQ; h += THREADS) {
         float M = -INFINITY;
-        for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(pml + ((long long)q * HQ + h) * 2));
-        float Ls = 0.f, O = 0.f;
+        for (int q = 0; q < nparts; ++q) M = fmaxf(M, ml(q * HQ + h).x);
+        float Ls = 0.f;
         for (int q = 0; q < nparts; ++q) {
-          const float mq = __ldcg(pml + ((long long)q * HQ + h) * 2);
-          const float w = exp2f(mq - M);
-          Ls = fmaf(__ldcg(pml + ((long long)q * HQ + h) * 2 + 1), w, Ls);
-          O = fmaf(__ldcg(po + (long long)q * HQ * D + e), w, O);
+          const float2 v = ml(q * HQ + h);
+          const float w = exp2f(v.x - M);
+          wsm[q * HQ + h] = w;
+          Ls = fmaf(v.y, w, Ls);
         }
-        out[e] = __bfloat16_as_ushort(__float2bfloat16_rn(O / Ls));
+        const float inv = 1.f / Ls;
+        for (int q = 0; q < nparts; ++q) wsm[q * HQ + h] *= inv;
+      }
+      __syncthreads();
+      // out = sum_q w[q][h] * o_q, four dims per thread, the parts' loads issued together
+      for (int e4 = tid; e4 < HQ * D / 4; e4 += THREADS) {
+        const int h = (e4 * 4) / D;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int q = 0;
+        for (; q + 4 <= nparts; q += 4) {
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            v[u] = __ldcg(reinterpret_cast<const float4*>(po + (long long)(q + u) * HQ * D) + e4);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w = wsm[(q + u) * HQ + h];
+            acc.x = fmaf(v[u].x, w, acc.x);
+            acc.y = fmaf(v[u].y, w, acc.y);
+            acc.z = fmaf(v[u].z, w, acc.z);
+            acc.w = fmaf(v[u].w, w, acc.w);
+          }
+        }
+        for (; q < nparts; ++q) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(po + (long long)q * HQ * D) + e4);
+          const float w = wsm[q * HQ + h];
+          acc.x = fmaf(v.x, w, acc.x);
+          acc.y = fmaf(v.y, w, acc.y);
+          acc.z = fmaf(v.z, w, acc.z);
+          acc.w = fmaf(v.w, w, acc.w);
+        }
+        uint2 pk;
+        pk.x = pack_bf16(acc.x, acc.y);
+        pk.y = pack_bf16(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(out + (long long)e4 * 4) = pk;
       }
       if (tid == 0) p.s.att_counter[rr] = 0;
     }
@@ -581,7 +751,9 @@ static cudaError_t run_gqa(const DecodeParams* p, size_t smem, cudaStream_t st) 
   auto kern = attn_gqa_kernel<G, HKV>;
   if (p == nullptr)   // prepare: allow the shared memory this shape needs
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<p->att_grid, THREADS, smem, st>>>(*p, attention_stages(p->g, smem));
+  int ns, nr;
+  attention_shape(p->g, 227 * 1024, &ns, &nr);
+  kern<<<p->att_grid, THREADS, smem, st>>>(*p, ns, nr);
   return cudaGetLastError();
 }
 

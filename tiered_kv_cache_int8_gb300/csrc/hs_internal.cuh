@@ -9,7 +9,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/hs.h"
+#include "hs.h"
 
 namespace hs {
 
@@ -86,6 +86,8 @@ struct DecodeParams {
   const uint16_t* q;
   uint16_t* out;
   int32_t* sel_out;
+  const uint16_t* new_kv;  // [n_req][row] token appended by this call, or null
+  const int8_t* new_keys;  // [n_req][d_idx]
   float scale_log2;        // softmax scale * log2(e)
   long long score_stride;  // scores row stride (positions, multiple of 4)
   int score_grid;          // score kernel CTAs
@@ -200,6 +202,12 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
       : "memory");
 }
 
+// 16-byte LSU async copy global (device or mapped host memory) -> shared.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ int4 ld_nc_v4(const void* p) {
   int4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
@@ -244,6 +252,57 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   if (total) *total = scratch[NW];
   __syncthreads();
   return excl;
+}
+
+// Two exclusive prefix sums at once (one set of barriers).  `scratch` holds
+// 2 * (NT/32 + 1) ints.
+template <int NT>
+__device__ __forceinline__ int2 block_exclusive_scan2(int a, int b, int* scratch, int* tot_a, int* tot_b) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int na = __shfl_up_sync(FULL_MASK, ia, o);
+    const int nb = __shfl_up_sync(FULL_MASK, ib, o);
+    if (lane >= o) {
+      ia += na;
+      ib += nb;
+    }
+  }
+  if (lane == 31) {
+    scratch[warp] = ia;
+    scratch[NW + 1 + warp] = ib;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int xa = lane < NW ? scratch[lane] : 0;
+    const int xb = lane < NW ? scratch[NW + 1 + lane] : 0;
+    int sa = xa, sb = xb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int na = __shfl_up_sync(FULL_MASK, sa, o);
+      const int nb = __shfl_up_sync(FULL_MASK, sb, o);
+      if (lane >= o) {
+        sa += na;
+        sb += nb;
+      }
+    }
+    if (lane < NW) {
+      scratch[lane] = sa - xa;
+      scratch[NW + 1 + lane] = sb - xb;
+    }
+    if (lane == NW - 1) {
+      scratch[NW] = sa;
+      scratch[2 * NW + 1] = sb;
+    }
+  }
+  __syncthreads();
+  const int2 r = make_int2(ia - a + scratch[warp], ib - b + scratch[NW + 1 + warp]);
+  if (tot_a) *tot_a = scratch[NW];
+  if (tot_b) *tot_b = scratch[2 * NW + 1];
+  __syncthreads();
+  return r;
 }
 
 template <int NT>

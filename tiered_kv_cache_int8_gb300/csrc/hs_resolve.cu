@@ -26,8 +26,9 @@
 //  3. the host fetch of the missed rows.  With fetch_mode 1 this CTA copies them
 //     from the mapped pinned host copy into their slots (serial, as the pages
 //     describe).  With fetch_mode 0 it marks them in slot_of_sel and the attention
-//     kernel's loader warps copy them while the rest of the rows stream from HBM,
-//     so host-link time overlaps HBM time.  Both give identical results.
+//     kernel's producer copies them from host memory into its stage (and from
+//     there into the slot) while the rest of the rows stream from HBM, so
+//     host-link time overlaps HBM time.  Both give identical results.
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -62,7 +63,7 @@ __host__ __device__ inline ResLayout res_layout(int B, int K) {
 }
 
 struct ResShared {
-  int scan[RES_THREADS / 32 + 1];
+  int scan[2 * (RES_THREADS / 32 + 1)];
   int b1, above1, b2, above2;
 };
 
@@ -113,8 +114,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     return;
   }
   const long long rl = (long long)req * g.n_layers + p.layer;
-  const int N = p.s.length[rl];
-  const int kk = min(K, N);
+  const int len = p.s.length[rl];
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const ResLayout L = res_layout(B, K);
@@ -127,30 +127,67 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   int32_t* ord = reinterpret_cast<int32_t*>(smem_raw + L.ord);
   uint8_t* used = smem_raw + L.used;
 
+  // The LRU order list is needed only after the selection: start copying it
+  // into shared memory now (async), so the copy overlaps the top-k passes.
+  const int32_t* order_g = p.s.order + rl * B;
+  for (int c4 = tid; c4 < B / 4; c4 += RES_THREADS) cp_async_16(ord + 4 * c4, order_g + 4 * c4);
+  const int t_step = p.s.step[rl];
+
+  // ---- the token appended by this call (its score was taken from the input) ----
+  int N = len;
+  if (p.new_kv) {
+    if (len + 1 <= g.max_context) {
+      N = len + 1;
+      const int kvec = g.d_idx / 16;
+      if (tid < kvec)
+        reinterpret_cast<int4*>(p.s.idx_keys + (rl * g.max_context + len) * g.d_idx)[tid] =
+            reinterpret_cast<const int4*>(p.new_keys + (long long)ri * g.d_idx)[tid];
+      const int rvec = g.row_bytes / 16;
+      const int4* src = reinterpret_cast<const int4*>(p.new_kv + (long long)ri * g.row_elems);
+      int4* dst = reinterpret_cast<int4*>(p.s.host_kv + (rl * g.max_context + len) * g.row_elems);
+      for (int v = tid; v < rvec; v += RES_THREADS) dst[v] = src[v];
+      if (tid == 0) {
+        p.s.length[rl] = N;
+        atomicAdd(&p.s.glob[1], (unsigned long long)g.row_bytes);
+      }
+    } else if (tid == 0) {
+      set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
+    }
+  }
+  const int kk = min(K, N);
+
   // ======================= 1. top-k, ascending =======================
   if (N <= K) {
     for (int i = tid; i < N; i += RES_THREADS) sel[i] = i;
   } else {
     const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
-    uint32_t* gh = p.s.hist + (long long)ri * IDX_BINS;
-    for (int b = tid; b < IDX_BINS; b += RES_THREADS) {
-      h[b] = gh[b];
-      gh[b] = 0;   // ready for the next call
-    }
+    uint4* gh4 = reinterpret_cast<uint4*>(p.s.hist + (long long)ri * IDX_BINS);
+    static_assert(IDX_BINS == 4 * RES_THREADS, "one 16-byte histogram chunk per thread");
+    reinterpret_cast<uint4*>(h)[tid] = gh4[tid];
+    gh4[tid] = make_uint4(0, 0, 0, 0);   // ready for the next call
     __syncthreads();
     select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
     const int b1 = sh.b1, above1 = sh.above1;
-    for (int b = tid; b < IDX_BINS; b += RES_THREADS) h[b] = 0;
+    reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     // second digit: histogram of the low 12 bits of the keys inside digit b1
     const int n4 = N >> 2;
     const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-    for (int i = tid; i < n4; i += RES_THREADS) {
-      const uint4 v = k4[i];
-      if ((int)(v.x >> 12) == b1) atomicAdd(&h[v.x & 4095u], 1u);
-      if ((int)(v.y >> 12) == b1) atomicAdd(&h[v.y & 4095u], 1u);
-      if ((int)(v.z >> 12) == b1) atomicAdd(&h[v.z & 4095u], 1u);
-      if ((int)(v.w >> 12) == b1) atomicAdd(&h[v.w & 4095u], 1u);
+    constexpr int UA = 8;   // loads in flight per thread
+    for (int i0 = tid; i0 < n4; i0 += UA * RES_THREADS) {
+      uint4 v[UA];
+#pragma unroll
+      for (int u = 0; u < UA; ++u) {
+        const int i = i0 + u * RES_THREADS;
+        v[u] = i < n4 ? k4[i] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < UA; ++u) {
+        if ((int)(v[u].x >> 12) == b1) atomicAdd(&h[v[u].x & 4095u], 1u);
+        if ((int)(v[u].y >> 12) == b1) atomicAdd(&h[v[u].y & 4095u], 1u);
+        if ((int)(v[u].z >> 12) == b1) atomicAdd(&h[v[u].z & 4095u], 1u);
+        if ((int)(v[u].w >> 12) == b1) atomicAdd(&h[v[u].w & 4095u], 1u);
+      }
     }
     for (int i = 4 * n4 + tid; i < N; i += RES_THREADS) {
       const uint32_t v = keys[i];
@@ -160,27 +197,69 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
     const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)sh.b2;
     const int need_eq = K - (above1 + sh.above2);   // >= 1
-    // ordered compaction over per-thread contiguous ranges
-    const int per = (N + RES_THREADS - 1) / RES_THREADS;
+    // ordered compaction over per-thread contiguous ranges (multiples of 4 keys,
+    // read as 16-byte vectors, 8 in flight; the second read hits L1)
+    const int per = (((N + RES_THREADS - 1) / RES_THREADS) + 3) & ~3;
     const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
+    const int jv = j0 + ((j1 - j0) & ~3);
     int n_gt = 0, n_eq = 0;
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t v = keys[j];
-      n_gt += v > vstar;
-      n_eq += v == vstar;
+    {
+      int j = j0;
+      for (; j + 32 <= jv; j += 32) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(keys + j + 4 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          n_gt += (v[u].x > vstar) + (v[u].y > vstar) + (v[u].z > vstar) + (v[u].w > vstar);
+          n_eq += (v[u].x == vstar) + (v[u].y == vstar) + (v[u].z == vstar) + (v[u].w == vstar);
+        }
+      }
+      for (; j + 4 <= jv; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
+        n_gt += (v.x > vstar) + (v.y > vstar) + (v.z > vstar) + (v.w > vstar);
+        n_eq += (v.x == vstar) + (v.y == vstar) + (v.z == vstar) + (v.w == vstar);
+      }
+      for (; j < j1; ++j) {
+        const uint32_t v = keys[j];
+        n_gt += v > vstar;
+        n_eq += v == vstar;
+      }
     }
-    const int gt_before = block_exclusive_scan<RES_THREADS>(n_gt, sh.scan, nullptr);
-    const int eq_before = block_exclusive_scan<RES_THREADS>(n_eq, sh.scan, nullptr);
-    int o = gt_before + min(eq_before, need_eq);
-    int eq_rank = eq_before;
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t v = keys[j];
+    const int2 before = block_exclusive_scan2<RES_THREADS>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+    int o = before.x + min(before.y, need_eq);
+    int eq_rank = before.y;
+    auto emit = [&](int j, uint32_t v) {
       bool take = v > vstar;
       if (v == vstar) {
         take = eq_rank < need_eq;
         ++eq_rank;
       }
       if (take && o < K) sel[o++] = j;
+    };
+    {
+      int j = j0;
+      for (; j + 32 <= jv; j += 32) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(keys + j + 4 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (max(max(v[u].x, v[u].y), max(v[u].z, v[u].w)) < vstar) continue;   // nothing taken
+          emit(j + 4 * u, v[u].x);
+          emit(j + 4 * u + 1, v[u].y);
+          emit(j + 4 * u + 2, v[u].z);
+          emit(j + 4 * u + 3, v[u].w);
+        }
+      }
+      for (; j + 4 <= jv; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
+        emit(j, v.x);
+        emit(j + 1, v.y);
+        emit(j + 2, v.z);
+        emit(j + 3, v.w);
+      }
+      for (; j < j1; ++j) emit(j, keys[j]);
     }
   }
   __syncthreads();
@@ -189,67 +268,68 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     if (i < kk) sel_g[i] = v;
     if (sel_out) sel_out[i] = v;
   }
-  if (kk == 0) return;   // nothing selected: the attention kernel writes zeros
+  if (kk == 0) {   // nothing selected: the attention kernel writes zeros
+    cp_async_wait_all();
+    return;
+  }
 
   // ======================= 2. RESOLVE metadata =======================
   int32_t* page = p.s.page + rl * g.max_context;
   int32_t* reverse = p.s.reverse + rl * B;
   int32_t* stamp = p.s.stamp + rl * B;
   int32_t* order = p.s.order + rl * B;
-  const int t = p.s.step[rl];
-  for (int j = tid; j < B; j += RES_THREADS) {
-    used[j] = 0;
-    ord[j] = order[j];
-  }
+  const int t = t_step;
+  for (int j = tid; j < B; j += RES_THREADS) used[j] = 0;
+  cp_async_wait_all();   // this thread's part of the LRU list has landed
   // hit test: independent page-table gathers, four in flight per thread
   bool bad = false;
   for (int i0 = tid; i0 < kk; i0 += 4 * RES_THREADS) {
-    int pos[4], s[4];
+    int pos[4], s4[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * RES_THREADS;
       pos[u] = i < kk ? sel[i] : -1;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) s[u] = (pos[u] >= 0 && pos[u] < N) ? page[pos[u]] : -1;
+    for (int u = 0; u < 4; ++u) s4[u] = (pos[u] >= 0 && pos[u] < N) ? page[pos[u]] : -1;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * RES_THREADS;
       if (i < kk) {
-        if (pos[u] < 0 || pos[u] >= N || s[u] >= B) bad = true;
-        slot_sel[i] = s[u];
+        if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
+        slot_sel[i] = s4[u];
       }
     }
   }
   __syncthreads();   // `used` is cleared before it is marked
   for (int i = tid; i < kk; i += RES_THREADS) {
-    const int s = slot_sel[i];
-    if (s >= 0 && s < B) used[s] = 1;
+    const int sl = slot_sel[i];
+    if (sl >= 0 && sl < B) used[sl] = 1;
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
     return;   // slot_of_sel keeps in-range values from before: the attention stays in bounds
   }
-  // misses in ascending selection order
+  // misses in ascending selection order, and the unpinned entries of the LRU list
   const int per_i = (kk + RES_THREADS - 1) / RES_THREADS;
   const int i0 = min(kk, tid * per_i), i1 = min(kk, i0 + per_i);
-  int nm = 0;
+  const int per_j = (B + RES_THREADS - 1) / RES_THREADS;
+  const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
+  int nm = 0, nc = 0;
   for (int i = i0; i < i1; ++i) nm += slot_sel[i] < 0;
+  for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
   int m;
-  int mb = block_exclusive_scan<RES_THREADS>(nm, sh.scan, &m);
+  const int2 mc = block_exclusive_scan2<RES_THREADS>(nm, nc, sh.scan, &m, nullptr);
+  int mb = mc.x;
   for (int i = i0; i < i1; ++i)
     if (slot_sel[i] < 0) miss_i[mb++] = i;
   // victims: the first m unpinned entries of the LRU list
-  const int per_j = (B + RES_THREADS - 1) / RES_THREADS;
-  const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
-  int nc = 0;
-  for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
-  int cb = block_exclusive_scan<RES_THREADS>(nc, sh.scan, nullptr);
+  int cb = mc.y;
   for (int j = j0; j < j1 && cb < m; ++j) {
-    const int s = ord[j];
-    if (used[s] == 0) {
-      victim[cb++] = s;
-      used[s] = 2;
+    const int sl = ord[j];
+    if (used[sl] == 0) {
+      victim[cb++] = sl;
+      used[sl] = 2;
     }
   }
   __syncthreads();
@@ -270,31 +350,31 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   }
   if (incons) set_error(p.s.dev_error, HS_DEVERR_METADATA);
   __syncthreads();
-  // slot of every selected position (misses flagged for the attention kernel's
-  // loader when it does the fetch); stamp every used slot
+  // slot of every selected position (misses flagged for the attention kernel
+  // when it does the fetch); stamp every used slot
   const int miss_flag = p.fetch_mode == 0 ? HS_SLOT_MISS_FLAG : 0;
   int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
   for (int i = tid; i < kk; i += RES_THREADS) {
-    const int s = slot_sel[i];
-    stamp[s] = t;
-    sos[i] = s;
+    const int sl = slot_sel[i];
+    stamp[sl] = t;
+    sos[i] = sl;
   }
   __syncthreads();
   for (int r = tid; r < m; r += RES_THREADS) sos[miss_i[r]] = victim[r] | miss_flag;
   // new LRU list: unused slots keep their order, used slots go last by slot
-  int n_unused;
-  int nu = 0;
+  int nu = 0, nus = 0;
   for (int j = j0; j < j1; ++j) nu += used[ord[j]] == 0;
-  int ub = block_exclusive_scan<RES_THREADS>(nu, sh.scan, &n_unused);
+  for (int sl = j0; sl < j1; ++sl) nus += used[sl] != 0;
+  int n_unused;
+  const int2 un = block_exclusive_scan2<RES_THREADS>(nu, nus, sh.scan, &n_unused, nullptr);
+  int ub = un.x;
   for (int j = j0; j < j1; ++j) {
-    const int s = ord[j];
-    if (used[s] == 0) order[ub++] = s;
+    const int sl = ord[j];
+    if (used[sl] == 0) order[ub++] = sl;
   }
-  int nus = 0;
-  for (int s = j0; s < j1; ++s) nus += used[s] != 0;
-  int sb = n_unused + block_exclusive_scan<RES_THREADS>(nus, sh.scan, nullptr);
-  for (int s = j0; s < j1; ++s)
-    if (used[s] != 0) order[sb++] = s;
+  int sb = n_unused + un.y;
+  for (int sl = j0; sl < j1; ++sl)
+    if (used[sl] != 0) order[sb++] = sl;
   if (tid == 0) {
     p.s.step[rl] = t + 1;
     p.s.hits[rl] += (unsigned long long)(kk - m);
@@ -310,6 +390,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
         reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
     unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * B * g.row_bytes;
     constexpr int U = 4;
+    // plain (coherent) loads: the row appended above may be among the misses
     for (long long e0 = tid; e0 < total; e0 += (long long)U * RES_THREADS) {
       int4 v[U];
 #pragma unroll
@@ -317,7 +398,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
         const long long e = e0 + (long long)u * RES_THREADS;
         if (e < total) {
           const int q = (int)(e / rvec), cidx = (int)(e - (long long)q * rvec);
-          v[u] = ld_nc_v4(src_base + (size_t)sel[miss_i[q]] * g.row_bytes + cidx * 16);
+          v[u] = *reinterpret_cast<const int4*>(src_base + (size_t)sel[miss_i[q]] * g.row_bytes + cidx * 16);
         }
       }
 #pragma unroll

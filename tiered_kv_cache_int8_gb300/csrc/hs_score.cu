@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     if (i < p.n_req) {
       const int req = p.req_ids ? p.req_ids[i] : i;
       if (req >= 0 && req < g.max_requests) {
-        const int N = p.s.length[(long long)req * g.n_layers + p.layer];
+        int N = p.s.length[(long long)req * g.n_layers + p.layer];
+        if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
         if (N > K) tiles = (N + TP - 1) / TP;
       }
     }
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
 
   // where tile t of this CTA lives
   struct TileRef {
-    int r, npos;
+    int r, npos, newpos;   // newpos: position of the appended token (its key comes from the input), or -1
     long long pos0, rl;
   };
   auto tile_ref = [&](int t, int& rc) -> TileRef {
@@ -121,7 +122,9 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     tr.r = rc;
     const int req = p.req_ids ? p.req_ids[rc] : rc;
     tr.rl = (long long)req * g.n_layers + p.layer;
-    const int N = p.s.length[tr.rl];
+    int N = p.s.length[tr.rl];
+    tr.newpos = -1;
+    if (p.new_kv && N + 1 <= g.max_context) tr.newpos = N++;
     tr.pos0 = (long long)(t - prefix[rc]) * TP;
     tr.npos = (int)min((long long)TP, N - tr.pos0);
     return tr;
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
   const int rot = NCH >= 8 ? (lane & (NCH - 1)) : ((lane & 7) / (8 / NCH));
   int4 qrot[NCH];
   int q_r = -1;
+  __shared__ __align__(16) unsigned char new_key[256];
 
   int r_cur = r0;
   bool timed_out = false;
@@ -157,6 +161,9 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) qrot[cc] = qsrc[(cc + rot) & (NCH - 1)];
     }
+    const int jnew = (tr.newpos >= tr.pos0 && tr.newpos < tr.pos0 + tr.npos) ? (int)(tr.newpos - tr.pos0) : -1;
+    if (jnew >= 0 && tid < NCH)   // the appended token's key is not in the store yet
+      reinterpret_cast<int4*>(new_key)[tid] = reinterpret_cast<const int4*>(p.new_keys + (long long)tr.r * d)[tid];
     const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((k / IDX_STAGES) & 1));
     if (__syncthreads_or(!ok)) {
       timed_out = true;
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     const unsigned char* tile = stage + (size_t)s * IDX_TILE_BYTES;
     uint32_t* keys_out = p.s.scores + (long long)tr.r * p.score_stride + tr.pos0;
     for (int j = tid; j < tr.npos; j += SC_THREADS) {
-      const unsigned char* rowp = tile + j * d;
+      const unsigned char* rowp = j == jnew ? new_key : tile + j * d;
       int acc = 0;
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {

@@ -78,7 +78,7 @@ def lib():
         L.hs_destroy.restype = None
         L.hs_append.argtypes = [VP, I32, I32, VP, I32, VP, VP, VP]
         L.hs_append.restype = ctypes.c_int
-        L.hs_decode_layer.argtypes = [VP, I32, I32, VP, VP, VP, VP, VP, VP]
+        L.hs_decode_layer.argtypes = [VP, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP]
         L.hs_decode_layer.restype = ctypes.c_int
         L.hs_stats.argtypes = [VP, P(HsStats)]
         L.hs_stats.restype = ctypes.c_int
@@ -165,8 +165,12 @@ class HiSparseCache:
         self._check(lib().hs_append(self._h, layer, n_req, _ptr(req_ids), n_tok, _ptr(kv_rows),
                                     _ptr(idx_keys), _stream(stream)))
 
-    def decode_layer(self, layer: int, q_idx, q, out=None, sel_out=None, req_ids=None, stream=None):
-        """q_idx: int8 [n_req, d_idx]; q: bf16 [n_req, h_q, d_qk] -> out bf16 [n_req, h_q, d_v]."""
+    def decode_layer(self, layer: int, q_idx, q, out=None, sel_out=None, req_ids=None, stream=None,
+                     new_kv=None, new_keys=None):
+        """q_idx: int8 [n_req, d_idx]; q: bf16 [n_req, h_q, d_qk] -> out bf16 [n_req, h_q, d_v].
+
+        new_kv (bf16 [n_req, row_elems]) / new_keys (int8 [n_req, d_idx]): append one
+        token per request first, inside the decode kernels."""
         import torch
         n_req = int(q_idx.shape[0])
         assert q_idx.is_cuda and q.is_cuda and q_idx.is_contiguous() and q.is_contiguous()
@@ -176,8 +180,13 @@ class HiSparseCache:
         assert out.is_contiguous() and out.element_size() == 2
         if sel_out is not None:
             assert sel_out.dtype == torch.int32 and tuple(sel_out.shape) == (n_req, self.cfg.top_k)
+        if new_kv is not None:
+            assert new_keys is not None and new_kv.is_contiguous() and new_keys.is_contiguous()
+            assert new_kv.numel() == n_req * self.row_elems and new_kv.element_size() == 2
+            assert new_keys.numel() == n_req * self.cfg.d_idx and new_keys.element_size() == 1
         self._check(lib().hs_decode_layer(self._h, layer, n_req, _ptr(req_ids), _ptr(q_idx), _ptr(q),
-                                          _ptr(out), _ptr(sel_out), _stream(stream)))
+                                          _ptr(out), _ptr(sel_out), _ptr(new_kv), _ptr(new_keys),
+                                          _stream(stream)))
         return out
 
     # -- introspection ---------------------------------------------------------------
