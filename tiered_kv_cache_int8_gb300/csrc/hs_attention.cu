@@ -750,7 +750,7 @@ template <int G, int HKV>
 static cudaError_t run_gqa(const DecodeParams* p, size_t smem, cudaStream_t st) {
   auto kern = attn_gqa_kernel<G, HKV>;
   if (p == nullptr)   // prepare: allow the shared memory this shape needs
-    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return allow_smem(kern, smem);
   int ns, nr;
   attention_shape(p->g, 227 * 1024, &ns, &nr);
   kern<<<p->att_grid, THREADS, smem, st>>>(*p, ns, nr);

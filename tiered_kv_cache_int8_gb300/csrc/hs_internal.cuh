@@ -138,6 +138,17 @@ cudaError_t prepare_score(const Geometry& g, size_t smem);
 cudaError_t prepare_resolve(size_t smem);
 cudaError_t prepare_attention(const Geometry& g, size_t smem);
 
+// Raises a kernel's dynamic shared-memory allowance to at least `smem`, never
+// lowers it: several handles (of different shapes) share the kernels.
+template <typename F>
+inline cudaError_t allow_smem(F* kern, size_t smem) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
 // ---- device helpers -------------------------------------------------------------
 #if defined(__CUDACC__)
 

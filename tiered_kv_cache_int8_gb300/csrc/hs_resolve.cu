@@ -419,7 +419,7 @@ cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st) 
 }
 
 cudaError_t prepare_resolve(size_t smem) {
-  return cudaFuncSetAttribute(topk_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return allow_smem(topk_resolve_kernel, smem);
 }
 
 }  // namespace hs

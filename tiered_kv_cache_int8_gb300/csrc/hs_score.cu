@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
 template <int NCH>
 static cudaError_t run_score(const DecodeParams* p, size_t smem, cudaStream_t st) {
   auto kern = score_kernel<NCH>;
-  if (p == nullptr) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (p == nullptr) return allow_smem(kern, smem);
   kern<<<p->score_grid, SC_THREADS, smem, st>>>(*p);
   return cudaGetLastError();
 }
