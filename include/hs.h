@@ -218,6 +218,39 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream);
 int hs_set_timing(hs_handle_t* h, int32_t enable);
 int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launches /*[HS_K_COUNT]*/);
 
+/*
+ * hs_indexer_topk_static — the indexer scores and exact top-k selection of
+ * hs_decode_layer (its steps 1 and 2, without the cache update) for callers
+ * that cannot allocate device memory: code that runs where cudaMalloc is not
+ * available or not allowed, such as inside another allocator's critical section,
+ * under a memory pool that forbids side allocations, or in a plugin that is only
+ * handed raw buffers.  The pages have no counterpart to this entry point.
+ * It allocates nothing (no cudaMalloc, cudaFree or allocating library call).  Its
+ * scratch — 64 histograms of 4096 bins and up to 2^21 32-bit keys, about 9 MiB —
+ * is one file-scope device array, which every GPU that loads the library holds
+ * until the process exits.
+ *   n_req    : requests, 0..64 (more: HS_ERR_CAPACITY)
+ *   n_max    : positions stride of idx_keys; n_req * round_up(n_max, 4) <= 2^21
+ *              (more: HS_ERR_CAPACITY)
+ *   d_idx    : 16, 32, 64, 128 or 256;   top_k : k >= 1
+ *   idx_keys : dev int8 [n_req][n_max][d_idx], 16-byte aligned
+ *   lengths  : HOST int32 [n_req], each in [0, n_max]: positions of each request
+ *   q_idx    : dev int8 [n_req][d_idx], 16-byte aligned
+ *   sel_out  : dev int32 [n_req][top_k]: the k_eff = min(top_k, length) highest
+ *              scores' positions, ascending, ties to the lower position, then -1
+ *              (the same values hs_decode_layer writes to its sel_out)
+ *   device   : CUDA device to run on (made current);  stream : cudaStream_t as void*
+ * The first call on a device does a one-time set-up with that device current (it
+ * looks up the device address of the array); make that first call before any
+ * stream capture.  All calls on a device share the array, which keeps the last
+ * call's contents: calls that overlap on the GPU (different streams, concurrent
+ * replays) race and must be ordered by the caller.  A non-zero status comes with
+ * a message in hs_last_error(NULL).
+ */
+int hs_indexer_topk_static(int32_t n_req, int32_t n_max, int32_t d_idx, int32_t top_k,
+                           const int8_t* idx_keys, const int32_t* lengths, const int8_t* q_idx,
+                           int32_t* sel_out, int32_t device, void* stream);
+
 /* hs_last_error — message of the handle's last failed call ("" if none); with
  * h == NULL, the message of the last failed hs_create in this thread. */
 const char* hs_last_error(const hs_handle_t* h);

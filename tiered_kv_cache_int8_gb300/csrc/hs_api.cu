@@ -131,6 +131,11 @@ void use_device(const hs_handle* h) {
 
 }  // namespace
 
+int hs::set_static_error(int code, const char* msg) {
+  g_create_error = msg;
+  return code;
+}
+
 extern "C" {
 
 const char* hs_status_string(int32_t s) {

@@ -128,6 +128,8 @@ cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_attention(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_init_order(int32_t* order, long long n_lists, int B, cudaStream_t st);
+// records a message for hs_last_error(NULL) and returns `code`
+int set_static_error(int code, const char* msg);
 
 // shared-memory needs, checked against the device limit at create time
 size_t score_smem_bytes(const Geometry& g);

@@ -33,7 +33,7 @@ KERNEL_NAMES = ("append", "indexer", "topk_resolve", "attention")
 # the symbols include/hs.h declares
 EXPORTED = ("hs_create", "hs_destroy", "hs_append", "hs_decode_layer", "hs_stats", "hs_snapshot",
             "hs_reset_request", "hs_set_timing", "hs_kernel_times", "hs_last_error",
-            "hs_status_string", "hs_row_elems")
+            "hs_status_string", "hs_row_elems", "hs_indexer_topk_static")
 
 
 class HsConfig(ctypes.Structure):
@@ -96,6 +96,8 @@ def lib():
         L.hs_status_string.restype = ctypes.c_char_p
         L.hs_row_elems.argtypes = [P(HsConfig)]
         L.hs_row_elems.restype = I32
+        L.hs_indexer_topk_static.argtypes = [I32, I32, I32, I32, VP, P(I32), VP, VP, I32, VP]
+        L.hs_indexer_topk_static.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -116,6 +118,22 @@ def _stream(stream) -> int | None:
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def indexer_topk_static(idx_keys, lengths, q_idx, top_k: int, sel_out=None, stream=None):
+    """Top-k selection with no device allocation inside the library (see
+    hs_indexer_topk_static in include/hs.h).  idx_keys: int8 cuda [n_req, n_max,
+    d_idx]; lengths: host ints [n_req]; q_idx: int8 cuda [n_req, d_idx]."""
+    import torch
+    n_req, n_max, d_idx = (int(x) for x in idx_keys.shape)
+    if sel_out is None:
+        sel_out = torch.empty((n_req, top_k), dtype=torch.int32, device=idx_keys.device)
+    lens = (ctypes.c_int32 * max(1, n_req))(*[int(x) for x in lengths])
+    rc = lib().hs_indexer_topk_static(n_req, n_max, d_idx, top_k, _ptr(idx_keys), lens, _ptr(q_idx),
+                                      _ptr(sel_out), idx_keys.device.index or 0, _stream(stream))
+    if rc != HS_OK:
+        raise HsError(rc, lib().hs_last_error(None).decode())
+    return sel_out
 
 
 class HiSparseCache:
