@@ -35,13 +35,24 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link if anything changed; returns the library path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, trace: bool | None = None) -> str:
+    """Compile and link if anything changed; returns the library path.  trace=True
+    (default: environment variable HS_WITH_TRACE=1) compiles the per-CTA phase
+    timeline in, for performance work; the library then writes it to the file
+    named by HS_TRACE_OUT when a handle is destroyed."""
+    if trace is None:
+        trace = os.environ.get("HS_WITH_TRACE") == "1"
+    flags_file = os.path.join(BUILD, "flags.txt")
+    flags = "trace" if trace else "release"
+    built_flags = open(flags_file).read() if os.path.exists(flags_file) else ""
+    if (not force and built_flags == flags and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= _deps_mtime()):
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if trace:
+        extra.append("-DHS_WITH_TRACE")
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
@@ -63,9 +74,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(flags_file, "w") as f:
+        f.write(flags)
     return LIB
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv)
+    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv, trace=True if "--trace" in sys.argv else None)
     print(LIB)

@@ -2,6 +2,7 @@
 // allocation of the two memory tiers and the cache metadata, argument checks
 // and kernel launches, counters, snapshots and optional per-kernel timing.
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -268,6 +269,9 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.part_ml, R * (size_t)h->att_parts * g.h_q * 2 * 4, false},
       {(void**)&s.att_counter, R * 4, false},
       {(void**)&s.app_counter, R * 4, false},
+#ifdef HS_WITH_TRACE
+      {(void**)&h->trace, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8, false},
+#endif
   };
   for (const A& a : allocs) {
     e = dev_alloc(h, a.p, a.bytes, fi);
@@ -294,6 +298,10 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.att_counter, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.hist, 0, R * (size_t)hs::IDX_BINS * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
+#ifdef HS_WITH_TRACE
+  ok = ok && cudaMemset(h->trace, 0, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8) ==
+                 cudaSuccess;
+#endif
   ok = ok && hs::launch_init_order(s.order, (long long)(R * Lr), (int)B, 0) == cudaSuccess;
   if (!ok) return fail_free(HS_ERR_CUDA, "hs_create: initialising the metadata failed");
   if ((e = hs::prepare_score(g, h->idx_smem)) != cudaSuccess ||
@@ -310,6 +318,16 @@ void hs_destroy(hs_handle_t* h) {
   if (!h) return;
   cudaSetDevice(h->cfg.device);
   cudaDeviceSynchronize();
+#ifdef HS_WITH_TRACE
+  if (const char* path = std::getenv("HS_TRACE_OUT")) {
+    std::vector<unsigned long long> t(2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS);
+    if (cudaMemcpy(t.data(), h->trace, t.size() * 8, cudaMemcpyDeviceToHost) == cudaSuccess)
+      if (FILE* f = std::fopen(path, "wb")) {
+        std::fwrite(t.data(), 8, t.size(), f);
+        std::fclose(f);
+      }
+  }
+#endif
   free_all(h);
   delete h;
 }
@@ -380,6 +398,9 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.att_parts = h->att_parts;
   p.att_grid = h->num_sms;
   p.fetch_mode = h->cfg.fetch_mode;
+#ifdef HS_WITH_TRACE
+  p.trace = h->trace;
+#endif
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = timed_launch(h, HS_K_INDEXER, st, [&] { return hs::launch_score(p, h->idx_smem, st); });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: indexer launch");

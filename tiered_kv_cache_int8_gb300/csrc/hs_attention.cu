@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   const int rvec = g.row_bytes / 16;
   __shared__ int scan_tmp[THREADS / 32 + 1];
   __shared__ int s_last[2];
+  HS_TRACE(p, 2, 0);
 
   // ---- flattened work list: units of every request (k_eff / TILE, rounded up) ----
   int carry = 0;
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     fence_mbar_init();
   }
   __syncthreads();
+  HS_TRACE(p, 2, 1);
   const long long U = carry;
   if (U == 0) return;
   // Only the first min(grid, U) CTAs take part, so every one taking part owns at
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       if (e0 + q * THREADS < ncache * TILE) rowc[e0 + q * THREADS] = v[q];
   }
   __syncthreads();
+  HS_TRACE(p, 2, 2);
   // (slot_of_sel, position) of row i of unit u (request r, first row row0)
   auto row_info = [&](long long u, int r, int row0, int i) -> int2 {
     const long long k = u - u0;
@@ -394,12 +397,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
                    &full[s]);
         }
       }
+      HS_TRACE_IF(p, 2, 3, lane == 0 && it == 0);
       s = (s + 1 == nstage) ? 0 : s + 1;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) slots[j] = nslots[j];
       cur_r = n_r;
       cur_nr = n_nr;
     }
+    HS_TRACE_IF(p, 2, 4, lane == 0);
   } else if (warp == FETCHER) {
     // ============================ fetcher warp ============================
     // Missed rows of every unit, in unit and row order, each into the next ring
@@ -437,6 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
           const unsigned char* src = host + (size_t)pos * g.row_bytes;
           unsigned char* dst = ring + (size_t)e * row_stride;
           for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+          HS_TRACE_IF(p, 2, 5, lane == 0 && k == 0);
           cp_async_mbar_arrive(&rfull[e]);   // balanced: completes when this lane's copies land
           __syncwarp();
           if (lane == 0) mbar_arrive(&rfull[e]);
@@ -445,7 +451,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         if (stop) break;
       }
     }
+    HS_TRACE_IF(p, 2, 6, lane == 0);
     cp_async_wait_all();
+    HS_TRACE_IF(p, 2, 7, lane == 0);
   } else {
     // ============================ consumer warps ============================
     const int kvh = warp % HKV;
@@ -533,6 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
                         wait_or_abort(&rfull[kq % nring], (uint32_t)((kq / nring) & 1), abort_flag, p.s.dev_error));
       }
       if (!ok) break;
+      HS_TRACE_IF(p, 2, 8, tid == 0 && it == 0);
       const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
       // shared-memory address of row i of the unit (stage row, or its ring entry)
       auto row_addr = [&](int i) -> uint32_t {
@@ -646,6 +655,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       rk += nmiss;
       s = (s + 1 == nstage) ? 0 : s + 1;
     }
+    HS_TRACE_IF(p, 2, 9, tid == 0);
+    HS_TRACE_IF(p, 2, 10, tid == 32 * (NCONS - 1));
     if (r >= 0 && !*abort_flag) flush(r);
   }
 
@@ -665,6 +676,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   // ---- arrival counters: the last CTA of a request merges its partials ------------
   __threadfence();
   __syncthreads();
+  HS_TRACE(p, 2, 11);
   int r_last = ri;
   while (prefix[r_last + 1] <= u1 - 1) ++r_last;
   for (int rr = ri; rr <= r_last; ++rr) {
@@ -678,6 +690,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     }
     __syncthreads();
     if (s_last[0]) {
+      HS_TRACE(p, 2, 12);
       __threadfence();
       const int nparts = s_last[1] * NSLICE;
       const float* po = p.s.part_o + (long long)rr * p.att_parts * HQ * D;
@@ -741,9 +754,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         *reinterpret_cast<uint2*>(out + (long long)e4 * 4) = pk;
       }
       if (tid == 0) p.s.att_counter[rr] = 0;
+      HS_TRACE(p, 2, 13);
     }
     __syncthreads();
   }
+  HS_TRACE(p, 2, 14);
 }
 
 template <int G, int HKV>

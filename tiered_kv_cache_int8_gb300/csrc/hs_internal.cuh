@@ -94,6 +94,9 @@ struct DecodeParams {
   int att_parts;           // partial results per request (CTAs x slices)
   int att_grid;            // attention CTAs (one per SM)
   int fetch_mode;          // 0: attention kernel fetches misses, 1: RESOLVE does
+#ifdef HS_WITH_TRACE
+  unsigned long long* trace;   // [2][3][1024][64]: clock64 and %globaltimer per (kernel, CTA, point)
+#endif
 };
 
 }  // namespace hs
@@ -118,6 +121,9 @@ struct hs_handle {
   std::vector<Timed> timed;
   std::vector<cudaEvent_t> event_pool;
   std::string last_error;
+#ifdef HS_WITH_TRACE
+  unsigned long long* trace = nullptr;
+#endif
 };
 
 namespace hs {
@@ -163,6 +169,26 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Phase timeline for performance work (builds with -DHS_WITH_TRACE only): the SM
+// cycle counter and the global timer at point `pt` of kernel `k`, per CTA, for
+// the latest launch.  Compiled out otherwise.
+constexpr int TRACE_KERNELS = 3, TRACE_CTAS = 1024, TRACE_POINTS = 64;
+#ifdef HS_WITH_TRACE
+#define HS_TRACE_IF(p, k, pt, cond)                                                               \
+  do {                                                                                            \
+    if ((cond) && (p).trace && blockIdx.x < TRACE_CTAS) {                                         \
+      const size_t i_ = ((size_t)(k) * TRACE_CTAS + blockIdx.x) * TRACE_POINTS + (pt);            \
+      (p).trace[i_] = clock64();                                                                  \
+      (p).trace[(size_t)TRACE_KERNELS * TRACE_CTAS * TRACE_POINTS + i_] = global_timer_ns();     \
+    }                                                                                             \
+  } while (0)
+#else
+#define HS_TRACE_IF(p, k, pt, cond) \
+  do {                              \
+  } while (0)
+#endif
+#define HS_TRACE(p, k, pt) HS_TRACE_IF(p, k, pt, threadIdx.x == 0)
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");

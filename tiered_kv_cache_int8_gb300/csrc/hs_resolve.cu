@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
       for (int i = tid; i < K; i += RES_THREADS) sel_out[i] = -1;
     return;
   }
+  HS_TRACE(p, 1, 0);
   const long long rl = (long long)req * g.n_layers + p.layer;
   const int len = p.s.length[rl];
 
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     }
   }
   const int kk = min(K, N);
+  HS_TRACE(p, 1, 1);
 
   // ======================= 1. top-k, ascending =======================
   if (N <= K) {
@@ -168,6 +170,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     __syncthreads();
     select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
     const int b1 = sh.b1, above1 = sh.above1;
+    HS_TRACE(p, 1, 2);
     reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     // second digit: histogram of the low 12 bits of the keys inside digit b1
@@ -194,7 +197,9 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
       if ((int)(v >> 12) == b1) atomicAdd(&h[v & 4095u], 1u);
     }
     __syncthreads();
+    HS_TRACE(p, 1, 3);
     select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
+    HS_TRACE(p, 1, 4);
     const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)sh.b2;
     const int need_eq = K - (above1 + sh.above2);   // >= 1
     // ordered compaction over per-thread contiguous ranges (multiples of 4 keys,
@@ -227,6 +232,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
       }
     }
     const int2 before = block_exclusive_scan2<RES_THREADS>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+    HS_TRACE(p, 1, 5);
     int o = before.x + min(before.y, need_eq);
     int eq_rank = before.y;
     auto emit = [&](int j, uint32_t v) {
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     }
   }
   __syncthreads();
+  HS_TRACE(p, 1, 6);
   for (int i = tid; i < K; i += RES_THREADS) {
     const int v = i < kk ? sel[i] : -1;
     if (i < kk) sel_g[i] = v;
@@ -306,10 +313,12 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     const int sl = slot_sel[i];
     if (sl >= 0 && sl < B) used[sl] = 1;
   }
+  HS_TRACE(p, 1, 7);
   if (__syncthreads_or(bad)) {
     if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
     return;   // slot_of_sel keeps in-range values from before: the attention stays in bounds
   }
+  HS_TRACE(p, 1, 8);
   // misses in ascending selection order, and the unpinned entries of the LRU list
   const int per_i = (kk + RES_THREADS - 1) / RES_THREADS;
   const int i0 = min(kk, tid * per_i), i1 = min(kk, i0 + per_i);
@@ -333,6 +342,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     }
   }
   __syncthreads();
+  HS_TRACE(p, 1, 9);
   // evict, then record the new residents
   bool incons = false;
   for (int r = tid; r < m; r += RES_THREADS) {
@@ -350,6 +360,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   }
   if (incons) set_error(p.s.dev_error, HS_DEVERR_METADATA);
   __syncthreads();
+  HS_TRACE(p, 1, 10);
   // slot of every selected position (misses flagged for the attention kernel
   // when it does the fetch); stamp every used slot
   const int miss_flag = p.fetch_mode == 0 ? HS_SLOT_MISS_FLAG : 0;
@@ -361,6 +372,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   }
   __syncthreads();
   for (int r = tid; r < m; r += RES_THREADS) sos[miss_i[r]] = victim[r] | miss_flag;
+  HS_TRACE(p, 1, 11);
   // new LRU list: unused slots keep their order, used slots go last by slot
   int nu = 0, nus = 0;
   for (int j = j0; j < j1; ++j) nu += used[ord[j]] == 0;
@@ -382,6 +394,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     atomicAdd(&p.s.glob[0], (unsigned long long)m * g.row_bytes);
   }
 
+  HS_TRACE(p, 1, 12);
   // ======================= 3. host fetch (fetch_mode 1) =======================
   if (p.fetch_mode == 1 && m > 0) {
     const int rvec = g.row_bytes / 16;
@@ -411,6 +424,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
       }
     }
   }
+  HS_TRACE(p, 1, 13);
 }
 
 cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st) {

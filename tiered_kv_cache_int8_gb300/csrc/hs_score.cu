@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
   unsigned char* stage = smem_raw + L.stage;
   __shared__ int scan_tmp[SC_THREADS / 32 + 1];
+  HS_TRACE(p, 0, 0);
 
   // ---- tiles of every request that needs a selection (N > k) ------------------
   int carry = 0;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     fence_mbar_init();
   }
   __syncthreads();
+  HS_TRACE(p, 0, 1);
   const long long T = carry;
   if (T == 0) return;
   const int Gc = (int)min((long long)gridDim.x, T);
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
       break;
     }
     consumed = k + 1;
+    HS_TRACE_IF(p, 0, 2, tid == 0 && k == 0);
     const unsigned char* tile = stage + (size_t)s * IDX_TILE_BYTES;
     uint32_t* keys_out = p.s.scores + (long long)tr.r * p.score_stride + tr.pos0;
     for (int j = tid; j < tr.npos; j += SC_THREADS) {
@@ -204,6 +207,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
       __syncthreads();
     }
   }
+  HS_TRACE(p, 0, 3);
   if (timed_out) {
     if (tid == 0) {
       const int issued = min(ntile, consumed + IDX_STAGES);
