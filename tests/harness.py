@@ -68,10 +68,11 @@ class StepInputs:
 
 
 def run_steps(cache, w: wl.Workload, inp: StepInputs, steps: int, layers=None, *, collect_sel=True,
-              collect_out=True, collect_meta=False, t0: int = 0, fused: bool = False):
+              collect_out=True, collect_meta=False, t0: int = 0, fused: bool = False, meta_pairs=None):
     """Runs decode steps t0..t0+steps-1 (append then decode per layer; with
     fused=True the append rides on the decode call); returns per-(layer, step)
-    selections, outputs and (optionally) metadata snapshots."""
+    selections, outputs and (optionally) metadata snapshots: of every request,
+    or with meta_pairs = {(request, layer), ...} of those only (a dict per step)."""
     torch = torch_mod()
     dev = torch.device("cuda", cache.device)
     layers = range(w.n_layers) if layers is None else layers
@@ -93,6 +94,10 @@ def run_steps(cache, w: wl.Workload, inp: StepInputs, steps: int, layers=None, *
             if collect_meta:
                 n0 = w.contexts()
                 res["meta"][l, t] = [cache.snapshot(r, l, int(n0[r]) + t + 1) for r in range(R)]
+            elif meta_pairs:
+                n0 = w.contexts()
+                res["meta"][l, t] = {r: cache.snapshot(r, l, int(n0[r]) + t + 1)
+                                     for (r, ll) in meta_pairs if ll == l}
     torch.cuda.synchronize(dev)
     return res
 

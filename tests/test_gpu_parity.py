@@ -112,6 +112,36 @@ def test_gqa_head_groupings(h_q, h_kv):
     full_parity(w, 3)
 
 
+@pytest.mark.parametrize("h_q,top_k,context", [(16, 200, 3001), (128, 256, 2600)])
+def test_latent_rows_mla(h_q, top_k, context):
+    # one shared 576-dim latent row per position, read as K and (first 512) as V;
+    # k_eff not a multiple of the 64-row unit, several requests and layers
+    w = wl.make_workload("mla_128k", n_requests=3, n_layers=2, context=context, h_q=h_q, top_k=top_k,
+                         hot_slots=384, steps=4)
+    full_parity(w, 4)
+
+
+def test_latent_rows_short_context_and_fused_append():
+    # contexts shorter than k (dense), the new token appended by the decode call
+    w = wl.make_workload("mla_128k", n_requests=2, n_layers=1, context=150, h_q=32, top_k=256,
+                         hot_slots=256, steps=3)
+    full_parity(w, 3, fused=True)
+
+
+def test_latent_rows_bit_identical_across_B():
+    w = wl.make_workload("mla_128k", n_requests=2, n_layers=1, context=3000, h_q=64, top_k=256,
+                         hot_slots=256, steps=3, sigma=0.3)
+    outs = []
+    for B in (256, 1024):
+        cache = make_cache(w, 3, B)
+        prefill(cache, w)
+        outs.append(run_steps(cache, w, StepInputs(w, 3), 3))
+        cache.close()
+    for t in range(3):
+        assert np.array_equal(outs[0]["out"][0, t], outs[1]["out"][0, t])
+        assert np.array_equal(outs[0]["sel"][0, t], outs[1]["sel"][0, t])
+
+
 def test_k_equals_B_and_high_sigma():
     # every unhit slot is a victim each step; low locality
     w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=3000, top_k=256,

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <sys/mman.h>
 #include <new>
 #include <string>
 
@@ -45,7 +46,9 @@ std::string check_config(const hs_config_t& c) {
     if (c.h_q < c.h_kv || c.h_q % c.h_kv != 0) return "GQA rows: h_q must be a multiple of h_kv";
     if (!is_pow2_in(c.h_q / c.h_kv, 1, 16)) return "GQA rows: h_q / h_kv must be one of 1, 2, 4, 8, 16";
   } else if (c.shared_kv == 1) {
-    return "latent (shared K/V) rows are not supported by this build";
+    if (c.h_kv != 1 || c.d_qk != 576 || c.d_v != 512)
+      return "latent rows: h_kv = 1, d_qk = 576 (the row, read as K), d_v = 512 (its first 512 dims, read as V)";
+    if (c.h_q != 16 && c.h_q != 32 && c.h_q != 64 && c.h_q != 128) return "latent rows: h_q must be 16, 32, 64 or 128";
   } else {
     return "shared_kv must be 0 or 1";
   }
@@ -55,8 +58,16 @@ std::string check_config(const hs_config_t& c) {
 void free_all(hs_handle* h) {
   for (void* p : h->dev_allocs) cudaFree(p);
   h->dev_allocs.clear();
-  if (h->host_kv_host) cudaFreeHost(h->host_kv_host);
+  if (h->host_kv_host) {
+    if (h->host_map_base) {
+      cudaHostUnregister(h->host_kv_host);
+      munmap(h->host_map_base, h->host_map_bytes);
+    } else {
+      cudaFreeHost(h->host_kv_host);
+    }
+  }
   h->host_kv_host = nullptr;
+  h->host_map_base = nullptr;
   for (auto& t : h->timed) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -228,8 +239,29 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   FaultInject fi;
   // D1: authoritative copy in pinned, mapped host memory
   if (fi.host) return fail_free(HS_ERR_OOM, "hs_create: pinned host allocation failed (injected)");
+  // Anonymous memory advised for transparent huge pages, then pinned and mapped:
+  // RESOLVE and the attention kernel read missed rows at random positions, and
+  // with large pages far fewer of those reads miss the GPU's TLB.  Falls back
+  // to cudaHostAlloc where the kernel offers no huge pages or registration fails.
   void* hp = nullptr;
-  e = cudaHostAlloc(&hp, h->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  {
+    const size_t align = (size_t)512 << 20;
+    const size_t len = h->host_bytes + align;
+    void* raw = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (raw != MAP_FAILED) {
+      void* a = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(raw) + align - 1) & ~(uintptr_t)(align - 1));
+      (void)madvise(a, h->host_bytes, MADV_HUGEPAGE);
+      if (cudaHostRegister(a, h->host_bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+        hp = a;
+        h->host_map_base = raw;
+        h->host_map_bytes = len;
+      } else {
+        (void)cudaGetLastError();
+        munmap(raw, len);
+      }
+    }
+  }
+  e = hp ? cudaSuccess : cudaHostAlloc(&hp, h->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return fail_free(HS_ERR_OOM, std::string("hs_create: cudaHostAlloc of ") + std::to_string(h->host_bytes) +
@@ -267,7 +299,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.slot_of_sel, R * K * 4, false},
       {(void**)&s.part_o, R * (size_t)h->att_parts * g.h_q * g.d_v * 4, false},
       {(void**)&s.part_ml, R * (size_t)h->att_parts * g.h_q * 2 * 4, false},
-      {(void**)&s.att_counter, R * 4, false},
+      {(void**)&s.att_nparts, R * 8 * 4, false},
       {(void**)&s.app_counter, R * 4, false},
 #ifdef HS_WITH_TRACE
       {(void**)&h->trace, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8, false},
@@ -295,7 +327,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.glob, 0, 32) == cudaSuccess;
   ok = ok && cudaMemset(s.dev_error, 0, 16) == cudaSuccess;
   ok = ok && cudaMemset(s.slot_of_sel, 0, R * K * 4) == cudaSuccess;
-  ok = ok && cudaMemset(s.att_counter, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.att_nparts, 0, R * 8 * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.hist, 0, R * (size_t)hs::IDX_BINS * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
 #ifdef HS_WITH_TRACE
@@ -397,7 +429,8 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.score_grid = h->num_sms;
   p.att_parts = h->att_parts;
   p.att_grid = h->num_sms;
-  p.fetch_mode = h->cfg.fetch_mode;
+  // latent rows are read by every head group's CTAs: RESOLVE pulls them (once)
+  p.fetch_mode = h->cfg.shared_kv ? 1 : h->cfg.fetch_mode;
 #ifdef HS_WITH_TRACE
   p.trace = h->trace;
 #endif

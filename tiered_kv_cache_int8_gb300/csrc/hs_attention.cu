@@ -23,14 +23,14 @@
 //    contiguous hot slot) HBM -> shared memory with one 1-D bulk async copy
 //    (cp.async.bulk, mbarrier completion) into a row-padded layout (16 extra bytes
 //    per row put the 8 rows of an ldmatrix phase in 8 different bank groups);
-//    up to 4 stages with full/empty mbarriers.
-//  * Warp 9 (fetcher) walks the same units, independently and ahead of the
-//    stager, and copies each missed row from the mapped pinned host copy into a
-//    ring of shared-memory row slots with 16-byte cp.async; every ring slot has
-//    its own full/empty mbarriers.  With few misses per CTA every host fetch is in
-//    flight from the start of the kernel; the ring bounds how far ahead it runs.
+//    up to 3 stages with full/empty mbarriers.
+//  * Warp 9 (fetcher) fills the missed rows of the same unit and stage: it
+//    copies each from the mapped pinned host copy straight into its stage row
+//    with 16-byte cp.async, and the stage's full barrier also waits for those
+//    copies.  Host reads are thus issued at most `stages` units ahead of the
+//    consumers, so the host link serves them roughly in the order the CTAs
+//    consume them instead of in one burst at kernel start.
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
-//    Each row is read from its stage row or, for a missed row, its ring slot.
 //    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
 //    with the group's query heads as the 16 M rows (zero-padded): the tensor
 //    cores cut the instruction count per byte; K and V fragments come straight
@@ -38,10 +38,14 @@
 //    (exp2, scale * log2(e) applied to the fp32 scores); P enters the second
 //    product as bf16.  Consumer warp 0 also writes each fetched row into its hot
 //    slot (bulk shared -> global copy), so later steps hit.
-//  * Every (CTA, request, slice) writes a partial (m, l, o) to scratch; the last
-//    CTA to finish a request (arrival counter) merges its partials in CTA order
-//    and writes bf16.  Rows are visited in ascending selection order and the
-//    merge order is fixed, so the output is bit-identical for any B.
+//  * Every (CTA, request, slice) writes a partial (m, l, o) to scratch; a small
+//    merge kernel (launched as a programmatic dependent, so its CTAs are already
+//    resident beside the attention CTAs when those finish) combines each head's
+//    partials in part order and writes bf16.  Rows are visited in ascending
+//    selection order and the merge order is fixed, so the output is
+//    bit-identical for any B.
+//  * Launched as a programmatic dependent: barrier set-up overlaps the previous
+//    kernel's tail; everything else waits for it.
 #include <cuda_bf16.h>
 
 #include "hs_internal.cuh"
@@ -55,30 +59,30 @@ constexpr int NCONS = 8;                   // consumer warps
 constexpr int STAGER = NCONS;              // warp index of the stager
 constexpr int FETCHER = NCONS + 1;         // warp index of the host fetcher
 constexpr int THREADS = (NCONS + 2) * 32;
-constexpr int MAX_STAGES = 4;
-constexpr int MAX_RING = 32;    // preferred ring entries
-constexpr int RING_CAP = 128;   // most ring entries (a unit has at most 128 rows)
+constexpr int MAX_STAGES = 3;
+constexpr int TILE_MAX = 128;   // rows of a unit at h_kv = 1 (8 slices of 16)
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct AttLayout {
-  size_t bar, meta, prefix, rowc, stage, stage_bytes, ring, total;
+  size_t bar, slot_tab, prefix, rowc, stage, stage_bytes, total;
 };
 
 constexpr int ROWCACHE = 2048;   // (slot, position) pairs of the CTA's rows kept in shared memory
 
-// Shared memory: barriers | per-stage miss masks | per-request tables | stages | ring.
-__host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage, int nring) {
+// Shared memory: barriers | per-stage hot slots of fetched rows | per-request
+// tables | row cache | stages.
+__host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage) {
   AttLayout L;
   const int nslice = NCONS / g.h_kv;
   const int tile = ATT_SUBTILE * nslice;
   const size_t row_stride = (size_t)g.row_bytes + ATT_ROW_PAD;
   size_t off = 0;
   L.bar = off;
-  off += 8 * (2 * MAX_STAGES + 2 * RING_CAP) + 16 + 4 * RING_CAP;   // barriers, abort flag, ring hot slots
+  off += 8 * (2 * MAX_STAGES) + 16;   // full/empty barriers, abort flag
   off = align_up(off, 128);
-  L.meta = off;
-  off += align_up((size_t)MAX_STAGES * 4 * 4, 128);   // miss mask of each stage (up to 128 rows)
+  L.slot_tab = off;
+  off += (size_t)MAX_STAGES * TILE_MAX * 4;   // hot slot of each fetched row (-1: none)
   L.prefix = off;
   off += align_up((size_t)(g.max_requests + 1) * 4 * 3, 128);   // unit prefix, k_eff, request id
   L.rowc = off;
@@ -86,8 +90,6 @@ __host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage, i
   L.stage = off;
   L.stage_bytes = align_up((size_t)tile * row_stride, 128);
   off += (size_t)nstage * L.stage_bytes;
-  L.ring = off;
-  off += (size_t)nring * row_stride;
   L.total = align_up(off, 128);
   return L;
 }
@@ -165,39 +167,25 @@ __device__ __forceinline__ int owner_of(long long u, long long U, int G) {
 }  // namespace
 
 int attention_parts(const Geometry& g) {
+  if (g.shared_kv) return mla_parts(g);
   const int nslice = NCONS / g.h_kv;
   const int tile = ATT_SUBTILE * nslice;
   const int units = (g.top_k + tile - 1) / tile;
   return (units + 1) * nslice;
 }
 
-// Stages and ring entries that fit.  The ring must hold every missed row of one
-// unit (TILE rows): the consumers wait for all of a unit's rows before computing,
-// so a smaller ring could never be filled.  Three stages where that still fits.
-static void attention_shape(const Geometry& g, size_t limit, int* nstage, int* nring) {
-  const int tile = ATT_SUBTILE * (NCONS / g.h_kv);
-  const int min_ring = tile;
-  for (int ns = 3; ns >= 2; --ns) {
-    int nr = tile > MAX_RING ? tile : MAX_RING;
-    while (nr > min_ring && att_layout(g, ns, nr).total > limit) --nr;
-    if (att_layout(g, ns, nr).total <= limit) {
-      *nstage = ns;
-      *nring = nr;
-      return;
-    }
-  }
-  *nstage = 2;
-  *nring = min_ring;
+// Three stages where they fit (small request tables), else two.
+static int attention_stages(const Geometry& g, size_t limit) {
+  return att_layout(g, MAX_STAGES).total <= limit ? MAX_STAGES : 2;
 }
 
 size_t attention_smem_bytes(const Geometry& g) {
-  int ns, nr;
-  attention_shape(g, 227 * 1024, &ns, &nr);
-  return att_layout(g, ns, nr).total;
+  if (g.shared_kv) return mla_smem_bytes(g);
+  return att_layout(g, attention_stages(g, 227 * 1024)).total;
 }
 
 template <int G, int HKV>
-__global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, int nstage, int nring) {
+__global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, int nstage) {
   constexpr int NSLICE = NCONS / HKV;
   constexpr int TILE = ATT_SUBTILE * NSLICE;
   constexpr int NJ = (TILE + 31) / 32;   // 32-row words of a unit
@@ -208,25 +196,31 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   const int c = blockIdx.x;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  const AttLayout L = att_layout(g, nstage, nring);
+  const AttLayout L = att_layout(g, nstage);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
   uint64_t* empty = full + MAX_STAGES;
-  uint64_t* rfull = empty + MAX_STAGES;
-  uint64_t* rempty = rfull + RING_CAP;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(rempty + RING_CAP);
-  int* ring_slot = const_cast<int*>(abort_flag) + 4;   // hot slot of the row in each ring entry
-  unsigned* stage_miss = reinterpret_cast<unsigned*>(smem_raw + L.meta);   // [stage][4] miss mask
-  int* prefix = reinterpret_cast<int*>(smem_raw + L.prefix);   // prefix[i] = first unit of request i
-  int* kk_s = prefix + (g.max_requests + 1);                    // k_eff of request i
-  int* req_s = kk_s + (g.max_requests + 1);                     // request id of request i
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + MAX_STAGES);
+  int* slot_tab = reinterpret_cast<int*>(smem_raw + L.slot_tab);   // [stage][TILE]: hot slot of a fetched row
+  int* prefix = reinterpret_cast<int*>(smem_raw + L.prefix);       // prefix[i] = first unit of request i
+  int* kk_s = prefix + (g.max_requests + 1);                        // k_eff of request i
+  int* req_s = kk_s + (g.max_requests + 1);                         // request id of request i
   int2* rowc = reinterpret_cast<int2*>(smem_raw + L.rowc);   // [unit k][row i] -> (slot_of_sel, position)
   unsigned char* stage = smem_raw + L.stage;
-  unsigned char* ring = smem_raw + L.ring;
   const int row_stride = g.row_bytes + ATT_ROW_PAD;
   const int rvec = g.row_bytes / 16;
   __shared__ int scan_tmp[THREADS / 32 + 1];
-  __shared__ int s_last[2];
   HS_TRACE(p, 2, 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(&full[s], 2);   // the stager's expect-tx arrival and the fetcher's
+      mbar_init(&empty[s], NCONS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  griddep_wait();   // selection, slots, lengths and host rows come from the kernels before
+  griddep_launch_dependents();
 
   // ---- flattened work list: units of every request (k_eff / TILE, rounded up) ----
   int carry = 0;
@@ -251,26 +245,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     if (i < p.n_req) prefix[i] = carry + ex;
     carry += tot;
   }
-  if (tid == 0) {
-    prefix[p.n_req] = carry;
-    for (int s = 0; s < nstage; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCONS);
-    }
-    for (int k = 0; k < nring; ++k) {
-      mbar_init(&rfull[k], 1);
-      mbar_init(&rempty[k], NCONS);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
+  if (tid == 0) prefix[p.n_req] = carry;
   __syncthreads();
   HS_TRACE(p, 2, 1);
   const long long U = carry;
-  if (U == 0) return;
   // Only the first min(grid, U) CTAs take part, so every one taking part owns at
-  // least one unit (the arrival counts below rely on that).
-  const int Gc = (int)min((long long)gridDim.x, U);
+  // least one unit.
+  const int Gc = (int)max(1LL, min((long long)gridDim.x, U));
+  if (c == 0)   // partials of each request, for the merge kernel
+    for (int i = tid; i < p.n_req; i += THREADS)
+      p.s.att_nparts[i] = prefix[i + 1] > prefix[i]
+                              ? (owner_of(prefix[i + 1] - 1, U, Gc) - owner_of(prefix[i], U, Gc) + 1) * NSLICE
+                              : 0;
+  if (U == 0) return;
   if (c >= Gc) return;
   const long long u0 = (long long)c * U / Gc, u1 = (long long)(c + 1) * U / Gc;
 
@@ -328,8 +315,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
 
   if (warp == STAGER) {
     // ============================ stager warp ============================
-    // Unit u's slots are loaded one unit ahead, so the global loads overlap the
-    // wait for a free stage.
+    // Hit rows of each unit by bulk copy; unit u+1's slots are read while the
+    // stager waits for a free stage.
     int r = ri;
     int slots[NJ];
     int cur_r = -1, cur_nr = 0;
@@ -345,6 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
     };
     load_unit(u0, slots, cur_r, cur_nr);
+    const uint64_t stream_policy = l2_evict_first_policy();   // hit rows are read once per call
     int s = 0;
     long long it = 0;
     for (long long u = u0; u < u1; ++u, ++it) {
@@ -360,16 +348,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
       const unsigned char* hot =
           reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
-      unsigned miss_bits[NJ];
-      int hit_rows = nr;
+      int hit_rows = 0;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
         const int i = lane + 32 * j;
-        miss_bits[j] = __ballot_sync(FULL_MASK, i < nr && (slots[j] & HS_SLOT_MISS_FLAG) != 0);
-        hit_rows -= __popc(miss_bits[j]);
-        if (lane == j) stage_miss[s * 4 + j] = miss_bits[j];
+        hit_rows += __popc(__ballot_sync(FULL_MASK, i < nr && (slots[j] & HS_SLOT_MISS_FLAG) == 0));
       }
-      if (lane >= NJ && lane < 4) stage_miss[s * 4 + lane] = 0u;
       // rows past the end of a request: zero them so their masked (weight-0)
       // values stay finite
       if (nr < TILE) {
@@ -387,14 +371,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
         const int i = lane + 32 * j;
-        if (i < nr && !((miss_bits[j] >> lane) & 1u)) {
+        if (i < nr && (slots[j] & HS_SLOT_MISS_FLAG) == 0) {
           int slot = slots[j];
           if (slot < 0 || slot >= g.hot_slots) {   // never expected: keep the copy in bounds
             set_error(p.s.dev_error, HS_DEVERR_METADATA);
             slot = 0;
           }
-          bulk_g2s(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
-                   &full[s]);
+          bulk_g2s_hint(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
+                        &full[s], stream_policy);
         }
       }
       HS_TRACE_IF(p, 2, 3, lane == 0 && it == 0);
@@ -407,49 +391,50 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     HS_TRACE_IF(p, 2, 4, lane == 0);
   } else if (warp == FETCHER) {
     // ============================ fetcher warp ============================
-    // Missed rows of every unit, in unit and row order, each into the next ring
-    // entry (FIFO); the consumers release entries in the same order.
+    // Missed rows of each unit, from the mapped host copy straight into their
+    // stage rows; the stage's full barrier completes when these copies land.
     int r = ri;
-    long long k = 0;   // ring entries handed out so far
-    bool stop = false;
-    for (long long u = u0; u < u1 && !stop; ++u) {
+    int s = 0;
+    long long it = 0;
+    for (long long u = u0; u < u1; ++u, ++it) {
       while (prefix[r + 1] <= u) ++r;
       const int row0 = (int)(u - prefix[r]) * TILE;
       const int nr = min(TILE, kk_s[r] - row0);
       const long long rl = (long long)req_s[r] * g.n_layers + p.layer;
       const unsigned char* host =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
+      int2 info[NJ];
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
         const int i = lane + 32 * j;
-        const int2 info = i < nr ? row_info(u, r, row0, i) : make_int2(0, 0);
-        const int sl = info.x;
-        const int ps = info.y;
-        unsigned bits = __ballot_sync(FULL_MASK, i < nr && (sl & HS_SLOT_MISS_FLAG) != 0);
+        info[j] = i < nr ? row_info(u, r, row0, i) : make_int2(0, 0);
+      }
+      if (it >= nstage &&
+          !__all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
+                                               p.s.dev_error)))
+        break;
+      unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+      int* tab = slot_tab + s * TILE_MAX;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int i = lane + 32 * j;
+        const bool miss = i < nr && (info[j].x & HS_SLOT_MISS_FLAG) != 0;
+        if (i < TILE) tab[i] = miss ? (info[j].x & ~HS_SLOT_MISS_FLAG) : -1;
+        unsigned bits = __ballot_sync(FULL_MASK, miss);
         while (bits) {
           const int b0 = __ffs(bits) - 1;
           bits &= bits - 1;
-          const int e = (int)(k % nring);
-          if (k >= nring &&
-              !__all_sync(FULL_MASK, wait_or_abort(&rempty[e], (uint32_t)(((k / nring) + 1) & 1), abort_flag,
-                                                   p.s.dev_error))) {
-            stop = true;
-            break;
-          }
-          const int pos = __shfl_sync(FULL_MASK, ps, b0);
-          const int slot = __shfl_sync(FULL_MASK, sl, b0) & ~HS_SLOT_MISS_FLAG;
-          if (lane == 0) ring_slot[e] = slot;
+          const int pos = __shfl_sync(FULL_MASK, info[j].y, b0);
           const unsigned char* src = host + (size_t)pos * g.row_bytes;
-          unsigned char* dst = ring + (size_t)e * row_stride;
+          unsigned char* dst = st_s + (size_t)(32 * j + b0) * row_stride;
           for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
-          HS_TRACE_IF(p, 2, 5, lane == 0 && k == 0);
-          cp_async_mbar_arrive(&rfull[e]);   // balanced: completes when this lane's copies land
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&rfull[e]);
-          ++k;
         }
-        if (stop) break;
       }
+      HS_TRACE_IF(p, 2, 5, lane == 0 && it == 0);
+      cp_async_mbar_arrive(&full[s]);   // balanced: completes when this lane's copies land
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+      s = (s + 1 == nstage) ? 0 : s + 1;
     }
     HS_TRACE_IF(p, 2, 6, lane == 0);
     cp_async_wait_all();
@@ -465,7 +450,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
     int r = -1;
     int s = 0;
-    long long rk = 0;   // ring entries consumed so far
 
     auto flush = [&](int req_i) {   // partial (m, l, o) of this (CTA, request, slice)
       float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
@@ -481,19 +465,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
 #pragma unroll
         for (int t = 0; t < 16; ++t)
           *reinterpret_cast<float2*>(po + (long long)h_lo * D + 8 * t + 2 * tq) = make_float2(o[t][0], o[t][1]);
-        if (tq == 0) {
-          pml[h_lo * 2 + 0] = m_lo;
-          pml[h_lo * 2 + 1] = ll;
-        }
+        if (tq == 0) *reinterpret_cast<float2*>(pml + h_lo * 2) = make_float2(m_lo, ll);
       }
       if (gq + 8 < G) {
 #pragma unroll
         for (int t = 0; t < 16; ++t)
           *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
-        if (tq == 0) {
-          pml[h_hi * 2 + 0] = m_hi;
-          pml[h_hi * 2 + 1] = lh;
-        }
+        if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
       }
     };
 
@@ -526,39 +504,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       if (!__all_sync(FULL_MASK, wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag,
                                                p.s.dev_error)))
         break;
-      // missed rows of this unit: ring entries rk, rk+1, ... in row order
-      unsigned mm[NJ];
-      int nmiss = 0;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        mm[j] = stage_miss[s * 4 + j];
-        nmiss += __popc(mm[j]);
-      }
-      bool ok = true;
-      for (int q = 0; q < nmiss && ok; ++q) {
-        const long long kq = rk + q;
-        ok = __all_sync(FULL_MASK,
-                        wait_or_abort(&rfull[kq % nring], (uint32_t)((kq / nring) & 1), abort_flag, p.s.dev_error));
-      }
-      if (!ok) break;
       HS_TRACE_IF(p, 2, 8, tid == 0 && it == 0);
       const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
-      // shared-memory address of row i of the unit (stage row, or its ring entry)
-      auto row_addr = [&](int i) -> uint32_t {
-        const int j = i >> 5, b = i & 31;
-        unsigned word = 0u;
-        int before = 0;
-#pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) {   // static indices only: mm stays in registers
-          if (jj == j) word = mm[jj];
-          if (jj < j) before += __popc(mm[jj]);
-        }
-        if ((word >> b) & 1u) {
-          before += __popc(word & ((1u << b) - 1u));
-          return smem_addr(ring + (size_t)((rk + before) % nring) * row_stride);
-        }
-        return smem_addr(st_s + (size_t)i * row_stride);
-      };
       if (nv > 0) {
         const int rbase = slice * ATT_SUBTILE;
         // ---- S = Q K^T over the 16 rows (two n-tiles of 8 rows) ----
@@ -566,7 +513,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-          const uint32_t rowa = row_addr(rbase + 8 * j + (lane & 7));
+          const uint32_t rowa = smem_addr(st_s + (size_t)(rbase + 8 * j + (lane & 7)) * row_stride);
 #pragma unroll
           for (int kp = 0; kp < 4; ++kp) {
             // four 8x8 matrices: K rows 8j..8j+7, dims 32kp + 8*(lane/8) .. +7
@@ -621,7 +568,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         }
         // ---- O += P V: 16 n-tiles of 8 dims, k = the 16 rows ----
         const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
-        const uint32_t rowv = row_addr(rbase + (lane & 7) + 8 * ((lane >> 3) & 1));
+        const uint32_t rowv = smem_addr(st_s + (size_t)(rbase + (lane & 7) + 8 * ((lane >> 3) & 1)) * row_stride);
 #pragma unroll
         for (int tp = 0; tp < 8; ++tp) {
           // four 8x8 matrices: (rows 0-7 | 8-15) x (dims 16tp..+7 | 16tp+8..+15), transposed
@@ -632,27 +579,26 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         }
       }
       // consumer warp 0 writes the rows fetched for this unit into their hot slots
-      bool stored = false;
-      if (warp == 0 && nmiss > 0) {
-        fence_proxy_async_smem();   // cp.async writes -> async-proxy reads
+      if (warp == 0) {
+        const int* tab = slot_tab + s * TILE_MAX;
         const long long rl = (long long)req_s[r] * g.n_layers + p.layer;
         unsigned char* hotw = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
-        for (int q = lane; q < nmiss; q += 32) {
-          const int e = (int)((rk + q) % nring);
-          const int slot = ring_slot[e];
-          if (slot >= 0 && slot < g.hot_slots)
-            bulk_s2g(hotw + (size_t)slot * g.row_bytes, ring + (size_t)e * row_stride, (uint32_t)g.row_bytes);
+        bool any = false;
+        for (int i = lane; i < TILE; i += 32) {
+          const int slot = tab[i];
+          if (slot >= 0 && slot < g.hot_slots) {
+            if (!any) fence_proxy_async_smem();   // cp.async writes -> async-proxy reads
+            any = true;
+            bulk_s2g(hotw + (size_t)slot * g.row_bytes, st_s + (size_t)i * row_stride, (uint32_t)g.row_bytes);
+          }
         }
-        bulk_commit();
-        stored = true;
+        if (any) {
+          bulk_commit();
+          bulk_wait_read_all();   // the stage may be refilled only after these reads
+        }
       }
-      if (stored) bulk_wait_read_all();   // ring entries may be refilled only after these reads
       __syncwarp();
-      if (lane == 0) {
-        for (int q = 0; q < nmiss; ++q) mbar_arrive(&rempty[(rk + q) % nring]);
-        mbar_arrive(&empty[s]);
-      }
-      rk += nmiss;
+      if (lane == 0) mbar_arrive(&empty[s]);
       s = (s + 1 == nstage) ? 0 : s + 1;
     }
     HS_TRACE_IF(p, 2, 9, tid == 0);
@@ -673,103 +619,136 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     return;
   }
 
-  // ---- arrival counters: the last CTA of a request merges its partials ------------
-  __threadfence();
-  __syncthreads();
-  HS_TRACE(p, 2, 11);
-  int r_last = ri;
-  while (prefix[r_last + 1] <= u1 - 1) ++r_last;
-  for (int rr = ri; rr <= r_last; ++rr) {
-    if (prefix[rr + 1] == prefix[rr]) continue;   // request without units
-    if (tid == 0) {
-      const int c_first = owner_of(prefix[rr], U, Gc);
-      const int c_last = owner_of(prefix[rr + 1] - 1, U, Gc);
-      const unsigned prev = atomicAdd(&p.s.att_counter[rr], 1u);
-      s_last[0] = prev == (unsigned)(c_last - c_first);
-      s_last[1] = c_last - c_first + 1;
-    }
-    __syncthreads();
-    if (s_last[0]) {
-      HS_TRACE(p, 2, 12);
-      __threadfence();
-      const int nparts = s_last[1] * NSLICE;
-      const float* po = p.s.part_o + (long long)rr * p.att_parts * HQ * D;
-      const float* pml = p.s.part_ml + (long long)rr * p.att_parts * HQ * 2;
-      uint16_t* out = p.out + (long long)rr * HQ * D;
-      // per-head merge weights w[q][h] = 2^(m_q - M_h) / L_h: the (m, l) pairs are
-      // read in one parallel step, then combined per head from shared memory
-      float* wsm = reinterpret_cast<float*>(stage);   // stages and ring are idle now
-      float2* mls = reinterpret_cast<float2*>(wsm + nparts * HQ);
-      // (m, l) pairs in shared memory when they fit beside the weights (always at
-      // the shapes this library accepts on GB300), else read from L2
-      const bool ml_smem = (size_t)nparts * HQ * 12 <= L.total - L.stage;
-      if (ml_smem)
-        for (int e = tid; e < nparts * HQ; e += THREADS) mls[e] = __ldcg(reinterpret_cast<const float2*>(pml) + e);
-      __syncthreads();
-      auto ml = [&](int e) -> float2 { return ml_smem ? mls[e] : __ldcg(reinterpret_cast<const float2*>(pml) + e); };
-      for (int h = tid; h < HQ; h += THREADS) {
-        float M = -INFINITY;
-        for (int q = 0; q < nparts; ++q) M = fmaxf(M, ml(q * HQ + h).x);
-        float Ls = 0.f;
-        for (int q = 0; q < nparts; ++q) {
-          const float2 v = ml(q * HQ + h);
-          const float w = exp2f(v.x - M);
-          wsm[q * HQ + h] = w;
-          Ls = fmaf(v.y, w, Ls);
-        }
-        const float inv = 1.f / Ls;
-        for (int q = 0; q < nparts; ++q) wsm[q * HQ + h] *= inv;
-      }
-      __syncthreads();
-      // out = sum_q w[q][h] * o_q, four dims per thread, the parts' loads issued together
-      for (int e4 = tid; e4 < HQ * D / 4; e4 += THREADS) {
-        const int h = (e4 * 4) / D;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int q = 0;
-        for (; q + 4 <= nparts; q += 4) {
-          float4 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            v[u] = __ldcg(reinterpret_cast<const float4*>(po + (long long)(q + u) * HQ * D) + e4);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float w = wsm[(q + u) * HQ + h];
-            acc.x = fmaf(v[u].x, w, acc.x);
-            acc.y = fmaf(v[u].y, w, acc.y);
-            acc.z = fmaf(v[u].z, w, acc.z);
-            acc.w = fmaf(v[u].w, w, acc.w);
-          }
-        }
-        for (; q < nparts; ++q) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(po + (long long)q * HQ * D) + e4);
-          const float w = wsm[q * HQ + h];
-          acc.x = fmaf(v.x, w, acc.x);
-          acc.y = fmaf(v.y, w, acc.y);
-          acc.z = fmaf(v.z, w, acc.z);
-          acc.w = fmaf(v.w, w, acc.w);
-        }
-        uint2 pk;
-        pk.x = pack_bf16(acc.x, acc.y);
-        pk.y = pack_bf16(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(out + (long long)e4 * 4) = pk;
-      }
-      if (tid == 0) p.s.att_counter[rr] = 0;
-      HS_TRACE(p, 2, 13);
-    }
-    __syncthreads();
-  }
   HS_TRACE(p, 2, 14);
 }
+
+// Combines the partials of each (request, head) in part order: grid (heads /
+// heads-per-CTA, requests), DV / 4 threads per head, one float4 of the head's
+// output dims per thread.  out = sum_q 2^(m_q - M) o_q / sum_q 2^(m_q - M) l_q.
+// Part counts are per group of GH heads (GQA: one group; latent rows: 16 heads).
+constexpr int MERGE_MAX_PARTS = 1024;
+
+template <int HQ, int DV, int GH>
+__global__ void __launch_bounds__(128) attn_merge_kernel(DecodeParams p) {
+  constexpr int TPH = DV / 4;                                        // threads per head
+  constexpr int HPC = (128 / TPH) < HQ ? (128 / TPH) : HQ;           // heads per CTA
+  __shared__ float2 mls[MERGE_MAX_PARTS / 8][HPC];   // (m, l) of a batch of parts
+  __shared__ float wsm[MERGE_MAX_PARTS][HPC];
+  __shared__ float Ms[HPC], Ls[HPC];
+  const int tid = threadIdx.x;
+  const int ri = blockIdx.y;
+  const int h0 = blockIdx.x * HPC;
+  griddep_wait();   // the attention kernel's partials
+  griddep_launch_dependents();
+  const int nparts = p.s.att_nparts[(long long)ri * (HQ / GH) + h0 / GH];
+  if (nparts <= 0) return;   // no units: the attention kernel wrote zeros
+  if (nparts > MERGE_MAX_PARTS) {   // not reachable with the shapes hs_create accepts
+    if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
+    return;
+  }
+  const float* pml = p.s.part_ml + (long long)ri * p.att_parts * HQ * 2;
+  const float* po = p.s.part_o + (long long)ri * p.att_parts * HQ * DV;
+  // weights: M = max_q m_q, w_q = 2^(m_q - M), L = sum_q w_q l_q (one thread per head, parts in order)
+  if (tid < HPC) {
+    Ms[tid] = -INFINITY;
+    Ls[tid] = 0.f;
+  }
+  for (int q0 = 0; q0 < nparts; q0 += MERGE_MAX_PARTS / 8) {
+    const int nq = min(MERGE_MAX_PARTS / 8, nparts - q0);
+    __syncthreads();
+    for (int e = tid; e < nq * HPC; e += blockDim.x)
+      mls[e / HPC][e % HPC] =
+          __ldcg(reinterpret_cast<const float2*>(pml) + (long long)(q0 + e / HPC) * HQ + h0 + e % HPC);
+    __syncthreads();
+    if (tid < HPC)
+      for (int q = 0; q < nq; ++q) Ms[tid] = fmaxf(Ms[tid], mls[q][tid].x);
+  }
+  __syncthreads();
+  for (int q0 = 0; q0 < nparts; q0 += MERGE_MAX_PARTS / 8) {
+    const int nq = min(MERGE_MAX_PARTS / 8, nparts - q0);
+    for (int e = tid; e < nq * HPC; e += blockDim.x)
+      mls[e / HPC][e % HPC] =
+          __ldcg(reinterpret_cast<const float2*>(pml) + (long long)(q0 + e / HPC) * HQ + h0 + e % HPC);
+    __syncthreads();
+    if (tid < HPC)
+      for (int q = 0; q < nq; ++q) {
+        const float w = exp2f(mls[q][tid].x - Ms[tid]);
+        wsm[q0 + q][tid] = w;
+        Ls[tid] = fmaf(mls[q][tid].y, w, Ls[tid]);
+      }
+    __syncthreads();
+  }
+  const int hh = tid / TPH;   // head within this CTA
+  if (hh >= HPC) return;
+  const int d4 = tid % TPH;   // float4 of the head's output dims
+  const float inv = 1.f / Ls[hh];
+  const float4* col = reinterpret_cast<const float4*>(po + (long long)(h0 + hh) * DV) + d4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int UQ = 8;   // parts in flight per thread
+  for (int q = 0; q < nparts; q += UQ) {
+    float4 v[UQ];
+#pragma unroll
+    for (int u = 0; u < UQ; ++u)
+      v[u] = q + u < nparts ? __ldcg(col + (long long)(q + u) * HQ * DV / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < UQ; ++u)
+      if (q + u < nparts) {
+        const float w = wsm[q + u][hh] * inv;
+        acc.x = fmaf(v[u].x, w, acc.x);
+        acc.y = fmaf(v[u].y, w, acc.y);
+        acc.z = fmaf(v[u].z, w, acc.z);
+        acc.w = fmaf(v[u].w, w, acc.w);
+      }
+  }
+  uint2 pk;
+  pk.x = pack_bf16(acc.x, acc.y);
+  pk.y = pack_bf16(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(p.out + ((long long)ri * HQ + h0 + hh) * DV + 4 * d4) = pk;
+}
+
+template <int HQ, int DV, int GH>
+static cudaError_t run_merge(const DecodeParams* p, cudaStream_t st) {
+  constexpr int TPH = DV / 4;
+  constexpr int HPC = (128 / TPH) < HQ ? (128 / TPH) : HQ;
+  if (p == nullptr) return allow_smem(attn_merge_kernel<HQ, DV, GH>, 0);
+  return launch_pdl(attn_merge_kernel<HQ, DV, GH>, dim3(HQ / HPC, p->n_req), dim3(HPC * TPH), 0, st, *p);
+}
+
+// p == nullptr: set-up only
+static cudaError_t dispatch_merge(const Geometry& g, const DecodeParams* p, cudaStream_t st) {
+  if (g.shared_kv) {
+    switch (g.h_q) {
+      case 16: return run_merge<16, 512, 16>(p, st);
+      case 32: return run_merge<32, 512, 16>(p, st);
+      case 64: return run_merge<64, 512, 16>(p, st);
+      case 128: return run_merge<128, 512, 16>(p, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (g.h_q) {
+    case 1: return run_merge<1, 128, 1>(p, st);
+    case 2: return run_merge<2, 128, 2>(p, st);
+    case 4: return run_merge<4, 128, 4>(p, st);
+    case 8: return run_merge<8, 128, 8>(p, st);
+    case 16: return run_merge<16, 128, 16>(p, st);
+    case 32: return run_merge<32, 128, 32>(p, st);
+    case 64: return run_merge<64, 128, 64>(p, st);
+    case 128: return run_merge<128, 128, 128>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) { return dispatch_merge(p.g, &p, st); }
 
 template <int G, int HKV>
 static cudaError_t run_gqa(const DecodeParams* p, size_t smem, cudaStream_t st) {
   auto kern = attn_gqa_kernel<G, HKV>;
   if (p == nullptr)   // prepare: allow the shared memory this shape needs
     return allow_smem(kern, smem);
-  int ns, nr;
-  attention_shape(p->g, 227 * 1024, &ns, &nr);
-  kern<<<p->att_grid, THREADS, smem, st>>>(*p, ns, nr);
-  return cudaGetLastError();
+  const int ns = attention_stages(p->g, 227 * 1024);
+  cudaError_t e = launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);
+  if (e != cudaSuccess) return e;
+  return launch_merge(*p, st);
 }
 
 template <int HKV>
@@ -794,10 +773,13 @@ static cudaError_t dispatch(const Geometry& g, const DecodeParams* p, size_t sme
   }
 }
 
-cudaError_t prepare_attention(const Geometry& g, size_t smem) { return dispatch(g, nullptr, smem, 0); }
+cudaError_t prepare_attention(const Geometry& g, size_t smem) {
+  const cudaError_t e = g.shared_kv ? dispatch_mla(g, nullptr, smem, 0) : dispatch(g, nullptr, smem, 0);
+  return e != cudaSuccess ? e : dispatch_merge(g, nullptr, 0);
+}
 
 cudaError_t launch_attention(const DecodeParams& p, size_t smem, cudaStream_t st) {
-  return dispatch(p.g, &p, smem, st);
+  return p.g.shared_kv ? dispatch_mla(p.g, &p, smem, st) : dispatch(p.g, &p, smem, st);
 }
 
 }  // namespace hs

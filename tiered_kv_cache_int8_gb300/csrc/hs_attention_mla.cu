@@ -1,0 +1,473 @@
+// Sparse attention over a shared latent row (MLA-style cache): every selected
+// position holds one latent vector of 576 bf16, read as K (all 576 dims) and as
+// V (its first 512 dims) by every query head; 16 to 128 query heads.
+//
+// Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
+// for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
+// formula 2: softmax over the selected positions only.  "KV卸载上主机:
+// HiSparse、PDD与DDR4回收", "论文1：HiSparse": only where rows live changes, so
+// the result must not depend on B.
+//
+// Design (sm_103a).  With 128 heads sharing each 1152-byte row the kernel does
+// ~240 flop per byte, so the products run on the tensor cores (mma.sync
+// m16n8k16, bf16 in, fp32 accumulate):
+//  * Work items are (request, group of 16 heads, unit of 64 selected rows),
+//    flattened in that order and split into equal contiguous ranges, one per
+//    CTA (persistent, one CTA per SM).  The split depends only on k_eff and the
+//    grid, never on B.  Rows are read once per head group; the groups of one
+//    request run close together in time, so the repeats hit L2.
+//  * Warp 8 (stager) copies the unit's 64 rows from their hot slots into shared
+//    memory with 1-D bulk async copies (cp.async.bulk, mbarrier completion), two
+//    or three stages deep.  RESOLVE has already pulled every missed row into its
+//    slot (latent rows are shared by all head groups, so they cross the host
+//    link once).
+//  * Warps 0-7: S = Q K^T with warp w taking rows 8w..8w+7 (36 k-steps over the
+//    576 dims; Q of the head group sits in shared memory); the per-head maxima
+//    and sums of the 64 rows are exchanged through shared memory; P goes to
+//    shared memory as bf16; then warp w accumulates O[16 heads, dims 64w..64w+63]
+//    += P V (4 k-steps over the 64 rows, V fragments by ldmatrix.trans).  Online
+//    softmax in fp32 with exp2; rows past k_eff are masked and zero-filled.
+//  * Each (CTA, request, head group) writes a partial (m, l, o); the merge kernel
+//    combines them in part order.
+#include <cuda_bf16.h>
+
+#include "hs_internal.cuh"
+
+namespace hs {
+
+namespace {
+
+constexpr int MLA_DK = 576, MLA_DV = 512;
+constexpr int MLA_HG = 16;                        // heads per group (the mma M)
+constexpr int MLA_TILE = 64;                      // rows per work item
+constexpr int MLA_NCONS = 8;                      // consumer warps
+constexpr int MLA_STAGER = MLA_NCONS;             // warp index of the stager
+constexpr int MLA_THREADS = (MLA_NCONS + 1) * 32;
+constexpr int MLA_ROW_STRIDE = MLA_DK * 2 + 16;   // shared-memory row pitch (bank spread for ldmatrix)
+constexpr int MLA_P_STRIDE = MLA_TILE * 2 + 16;
+constexpr int MLA_MAX_STAGES = 3;
+constexpr size_t MLA_SMEM_LIMIT = 227 * 1024;
+
+__host__ __device__ inline size_t mla_align(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct MlaLayout {
+  size_t bar, prefix, q, p, red, stage, stage_bytes, total;
+  int nstage;
+};
+
+__host__ __device__ inline MlaLayout mla_layout(const Geometry& g) {
+  MlaLayout L;
+  size_t off = 0;
+  L.bar = off;
+  off += 8 * 2 * MLA_MAX_STAGES + 16;   // full/empty barriers, abort flag
+  off = mla_align(off, 128);
+  L.prefix = off;   // first item, k_eff and request id of each request
+  off += mla_align((size_t)(g.max_requests + 1) * 4 * 3, 128);
+  L.q = off;
+  off += (size_t)MLA_HG * MLA_ROW_STRIDE;
+  L.p = off;
+  off += (size_t)MLA_HG * MLA_P_STRIDE;
+  L.red = off;   // per-warp head maxima (two buffers) and sums
+  off += (size_t)3 * MLA_NCONS * MLA_HG * 4;
+  off = mla_align(off, 128);
+  L.stage = off;
+  L.stage_bytes = (size_t)MLA_TILE * MLA_ROW_STRIDE;
+  L.nstage = off + 3 * L.stage_bytes <= MLA_SMEM_LIMIT ? 3 : 2;
+  off += (size_t)L.nstage * L.stage_bytes;
+  L.total = off;
+  return L;
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier of the 256 consumer threads that also ORs a flag over them.
+__device__ __forceinline__ bool consumers_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ bool wait_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        set_error(err, HS_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int owner(long long u, long long U, int G) {
+  return (int)(((u + 1) * G + U - 1) / U) - 1;
+}
+
+}  // namespace
+
+int mla_parts(const Geometry& g) { return (g.top_k + MLA_TILE - 1) / MLA_TILE + 1; }
+size_t mla_smem_bytes(const Geometry& g) { return mla_layout(g).total; }
+
+template <int HQ>
+__global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p) {
+  constexpr int NHG = HQ / MLA_HG;
+  const Geometry& g = p.g;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = g.top_k;
+  const int c = blockIdx.x;
+
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const MlaLayout L = mla_layout(g);
+  const int nstage = L.nstage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
+  uint64_t* empty = full + MLA_MAX_STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + MLA_MAX_STAGES);
+  int* prefix = reinterpret_cast<int*>(smem_raw + L.prefix);
+  int* kk_s = prefix + (g.max_requests + 1);
+  int* req_s = kk_s + (g.max_requests + 1);
+  unsigned char* qs = smem_raw + L.q;
+  unsigned char* ps = smem_raw + L.p;
+  float* smax = reinterpret_cast<float*>(smem_raw + L.red);   // [2][8][16]
+  float* ssum = smax + 2 * MLA_NCONS * MLA_HG;                // [8][16]
+  unsigned char* stage = smem_raw + L.stage;
+  __shared__ int scan_tmp[MLA_THREADS / 32 + 1];
+  HS_TRACE(p, 2, 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], MLA_NCONS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  griddep_wait();   // selection, slots (rows pulled by RESOLVE), lengths, q
+  griddep_launch_dependents();
+
+  // ---- work list: NHG * ceil(k_eff / 64) items per request ----
+  int carry = 0;
+  for (int base = 0; base < p.n_req; base += MLA_THREADS) {
+    const int i = base + tid;
+    int items = 0;
+    if (i < p.n_req) {
+      const int req = p.req_ids ? p.req_ids[i] : i;
+      int kk = 0;
+      if (req >= 0 && req < g.max_requests) kk = min(K, p.s.length[(long long)req * g.n_layers + p.layer]);
+      items = NHG * ((kk + MLA_TILE - 1) / MLA_TILE);
+      kk_s[i] = kk;
+      req_s[i] = req;
+      if (kk == 0 && i % (int)gridDim.x == c) {   // nothing selected: the output is defined as 0
+        uint16_t* out = p.out + (long long)i * HQ * MLA_DV;
+        for (int e = 0; e < HQ * MLA_DV; ++e) out[e] = 0;
+        if (req >= 0 && req < g.max_requests) set_error(p.s.dev_error, HS_DEVERR_EMPTY);
+      }
+    }
+    int tot;
+    const int ex = block_exclusive_scan<MLA_THREADS>(items, scan_tmp, &tot);
+    if (i < p.n_req) prefix[i] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) prefix[p.n_req] = carry;
+  __syncthreads();
+  const long long U = carry;
+  const int Gc = (int)max(1LL, min((long long)gridDim.x, U));
+  if (c == 0)   // partials of each (request, head group), for the merge kernel
+    for (int e = tid; e < p.n_req * NHG; e += MLA_THREADS) {
+      const int i = e / NHG, hg = e % NHG;
+      const int ui = (kk_s[i] + MLA_TILE - 1) / MLA_TILE;
+      const long long f0 = prefix[i] + (long long)hg * ui;
+      p.s.att_nparts[(long long)i * NHG + hg] = ui ? owner(f0 + ui - 1, U, Gc) - owner(f0, U, Gc) + 1 : 0;
+    }
+  if (U == 0 || c >= Gc) return;
+  const long long u0 = (long long)c * U / Gc, u1 = (long long)(c + 1) * U / Gc;
+  int ri = 0;
+  {
+    int lo = 0, hi = p.n_req - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= u0) lo = mid;
+      else hi = mid - 1;
+    }
+    ri = lo;
+    while (prefix[ri + 1] <= u0) ++ri;
+  }
+  struct Item {
+    int r, hg, unit, nv;
+  };
+  auto decode = [&](long long f, int& r) -> Item {
+    while (prefix[r + 1] <= f) ++r;
+    Item it;
+    it.r = r;
+    const int ui = (kk_s[r] + MLA_TILE - 1) / MLA_TILE;
+    const int local = (int)(f - prefix[r]);
+    it.hg = local / ui;
+    it.unit = local - it.hg * ui;
+    it.nv = min(MLA_TILE, kk_s[r] - it.unit * MLA_TILE);
+    return it;
+  };
+
+  if (warp == MLA_STAGER) {
+    // ============================ stager warp ============================
+    int r = ri;
+    int s = 0;
+    long long it = 0;
+    for (long long f = u0; f < u1; ++f, ++it) {
+      const Item w = decode(f, r);
+      const long long rl = (long long)req_s[w.r] * g.n_layers + p.layer;
+      int slot[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        slot[h] = j < w.nv ? p.s.slot_of_sel[(long long)w.r * K + w.unit * MLA_TILE + j] : 0;
+      }
+      if (it >= nstage &&
+          !__all_sync(FULL_MASK, wait_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
+                                            p.s.dev_error)))
+        break;
+      unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+      if (w.nv < MLA_TILE) {   // rows past k_eff: zeros keep the masked products finite
+        const int rvec = MLA_DK * 2 / 16;
+        for (int e = lane; e < (MLA_TILE - w.nv) * rvec; e += 32) {
+          const int j = w.nv + e / rvec;
+          *reinterpret_cast<int4*>(st_s + (size_t)j * MLA_ROW_STRIDE + (e % rvec) * 16) = make_int4(0, 0, 0, 0);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(w.nv * g.row_bytes));
+      }
+      __syncwarp();
+      const unsigned char* hot =
+          reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        if (j < w.nv) {
+          int sl = slot[h];
+          if (sl < 0 || sl >= g.hot_slots) {   // never expected (RESOLVE fills every slot): stay in bounds
+            set_error(p.s.dev_error, HS_DEVERR_METADATA);
+            sl = 0;
+          }
+          bulk_g2s(st_s + (size_t)j * MLA_ROW_STRIDE, hot + (size_t)sl * g.row_bytes, (uint32_t)g.row_bytes,
+                   &full[s]);
+        }
+      }
+      s = (s + 1 == nstage) ? 0 : s + 1;
+    }
+  } else {
+    // ============================ consumer warps ============================
+    const int gq = lane >> 2, tq = lane & 3;
+    const float sl2 = p.scale_log2;
+    const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1);   // ldmatrix row of this lane (16-row operands)
+    const int lcol = 8 * (lane >> 4);                        // and its column offset
+    float o[8][4];
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
+    int cur_r = -1, cur_hg = -1;
+    int r = ri;
+    int s = 0;
+    long long it = 0;
+
+    auto flush = [&](int rq, int hg) {
+      const long long f0 = prefix[rq] + (long long)hg * ((kk_s[rq] + MLA_TILE - 1) / MLA_TILE);
+      const int part = c - owner(f0, U, Gc);
+      const long long base = ((long long)rq * p.att_parts + part) * HQ + hg * MLA_HG;
+      float* po = p.s.part_o + base * MLA_DV;
+      float* pml = p.s.part_ml + base * 2;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int d = 64 * warp + 8 * t + 2 * tq;
+        *reinterpret_cast<float2*>(po + (long long)gq * MLA_DV + d) = make_float2(o[t][0], o[t][1]);
+        *reinterpret_cast<float2*>(po + (long long)(gq + 8) * MLA_DV + d) = make_float2(o[t][2], o[t][3]);
+      }
+      if (warp == 0 && tq == 0) {
+        *reinterpret_cast<float2*>(pml + gq * 2) = make_float2(m_lo, l_lo);
+        *reinterpret_cast<float2*>(pml + (gq + 8) * 2) = make_float2(m_hi, l_hi);
+      }
+    };
+
+    for (long long f = u0; f < u1; ++f, ++it) {
+      const Item w = decode(f, r);
+      if (w.r != cur_r || w.hg != cur_hg) {
+        if (cur_r >= 0) flush(cur_r, cur_hg);
+        cur_r = w.r;
+        cur_hg = w.hg;
+        consumers_sync();   // every warp is done with the previous group's Q
+        const int4* qsrc = reinterpret_cast<const int4*>(p.q + ((long long)w.r * HQ + w.hg * MLA_HG) * MLA_DK);
+        for (int e = tid; e < MLA_HG * MLA_DK / 8; e += MLA_NCONS * 32) {
+          const int h = e / (MLA_DK / 8), v = e % (MLA_DK / 8);
+          *reinterpret_cast<int4*>(qs + (size_t)h * MLA_ROW_STRIDE + v * 16) = qsrc[e];
+        }
+        consumers_sync();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
+      }
+      const bool ok = wait_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error);
+      const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+      // ---- S = Q K^T for rows 8*warp .. 8*warp + 7 ----
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint32_t rowa = smem_addr(st_s + (size_t)(8 * warp + (lane & 7)) * MLA_ROW_STRIDE) + 16 * (lane >> 3);
+        const uint32_t qa = smem_addr(qs + (size_t)lrow * MLA_ROW_STRIDE) + 2 * lcol;
+#pragma unroll 6
+        for (int kp = 0; kp < MLA_DK / 32; ++kp) {
+          uint32_t b[4], a0[4], a1[4];
+          ldsm4(b, rowa + 64 * kp);          // K rows x dims 32kp .. 32kp+31
+          ldsm4(a0, qa + 64 * kp);           // Q dims 32kp .. +15
+          ldsm4(a1, qa + 64 * kp + 32);      // Q dims 32kp+16 .. +31
+          mma16816(sc, a0, b[0], b[1]);
+          mma16816(sc, a1, b[2], b[3]);
+        }
+      }
+      // ---- tile maxima per head ----
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool okr = 8 * warp + 2 * tq + e < w.nv;
+        sc[e] = okr ? sc[e] * sl2 : -INFINITY;
+        sc[2 + e] = okr ? sc[2 + e] * sl2 : -INFINITY;
+        mx_lo = fmaxf(mx_lo, sc[e]);
+        mx_hi = fmaxf(mx_hi, sc[2 + e]);
+      }
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL_MASK, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL_MASK, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL_MASK, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL_MASK, mx_hi, 2));
+      float* smx = smax + (it & 1) * MLA_NCONS * MLA_HG;
+      if (tq == 0) {
+        smx[warp * MLA_HG + gq] = mx_lo;
+        smx[warp * MLA_HG + gq + 8] = mx_hi;
+      }
+      if (consumers_sync_or(!ok)) break;   // all consumer warps leave together
+      float tm_lo = -INFINITY, tm_hi = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < MLA_NCONS; ++q) {
+        tm_lo = fmaxf(tm_lo, smx[q * MLA_HG + gq]);
+        tm_hi = fmaxf(tm_hi, smx[q * MLA_HG + gq + 8]);
+      }
+      const float mn_lo = fmaxf(m_lo, tm_lo), mn_hi = fmaxf(m_hi, tm_hi);   // finite: every unit has a valid row
+      const float a_lo = exp2f(m_lo - mn_lo), a_hi = exp2f(m_hi - mn_hi);
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      const float p0 = exp2f(sc[0] - mn_lo), p1 = exp2f(sc[1] - mn_lo);
+      const float p2 = exp2f(sc[2] - mn_hi), p3 = exp2f(sc[3] - mn_hi);
+      *reinterpret_cast<uint32_t*>(ps + (size_t)gq * MLA_P_STRIDE + 2 * (8 * warp + 2 * tq)) = pack2_bf16(p0, p1);
+      *reinterpret_cast<uint32_t*>(ps + (size_t)(gq + 8) * MLA_P_STRIDE + 2 * (8 * warp + 2 * tq)) =
+          pack2_bf16(p2, p3);
+      float su_lo = p0 + p1, su_hi = p2 + p3;
+      su_lo += __shfl_xor_sync(FULL_MASK, su_lo, 1);
+      su_lo += __shfl_xor_sync(FULL_MASK, su_lo, 2);
+      su_hi += __shfl_xor_sync(FULL_MASK, su_hi, 1);
+      su_hi += __shfl_xor_sync(FULL_MASK, su_hi, 2);
+      if (tq == 0) {
+        ssum[warp * MLA_HG + gq] = su_lo;
+        ssum[warp * MLA_HG + gq + 8] = su_hi;
+      }
+      consumers_sync();
+      float ts_lo = 0.f, ts_hi = 0.f;
+#pragma unroll
+      for (int q = 0; q < MLA_NCONS; ++q) {   // fixed order: every warp gets the same l
+        ts_lo += ssum[q * MLA_HG + gq];
+        ts_hi += ssum[q * MLA_HG + gq + 8];
+      }
+      l_lo = l_lo * a_lo + ts_lo;
+      l_hi = l_hi * a_hi + ts_hi;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        o[t][0] *= a_lo;
+        o[t][1] *= a_lo;
+        o[t][2] *= a_hi;
+        o[t][3] *= a_hi;
+      }
+      // ---- O[:, 64*warp .. +63] += P V over the 64 rows ----
+      {
+        const uint32_t pa_base = smem_addr(ps + (size_t)lrow * MLA_P_STRIDE) + 2 * lcol;
+        const uint32_t v_base = smem_addr(st_s + (size_t)lrow * MLA_ROW_STRIDE) + 2 * (64 * warp + lcol);
+#pragma unroll
+        for (int ks = 0; ks < MLA_TILE / 16; ++ks) {
+          uint32_t pa[4];
+          ldsm4(pa, pa_base + 32 * ks);   // P heads x rows 16ks .. 16ks+15
+#pragma unroll
+          for (int tp = 0; tp < 4; ++tp) {
+            uint32_t b[4];
+            ldsm4_t(b, v_base + (uint32_t)(16 * ks * MLA_ROW_STRIDE) + 32 * tp);
+            mma16816(o[2 * tp], pa, b[0], b[1]);
+            mma16816(o[2 * tp + 1], pa, b[2], b[3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&empty[s]);
+      s = (s + 1 == nstage) ? 0 : s + 1;
+    }
+    if (cur_r >= 0 && !*abort_flag) flush(cur_r, cur_hg);
+  }
+  __syncthreads();
+  if (*abort_flag && tid == 0)   // drain copies that may still be in flight (bounded)
+    for (int s2 = 0; s2 < nstage; ++s2) {
+      (void)mbar_wait_bounded(&full[s2], 0);
+      (void)mbar_wait_bounded(&full[s2], 1);
+    }
+  HS_TRACE(p, 2, 14);
+}
+
+template <int HQ>
+static cudaError_t run_mla(const DecodeParams* p, size_t smem, cudaStream_t st) {
+  auto kern = attn_mla_kernel<HQ>;
+  if (p == nullptr) return allow_smem(kern, smem);
+  cudaError_t e = launch_pdl(kern, dim3(p->att_grid), dim3(MLA_THREADS), smem, st, *p);
+  if (e != cudaSuccess) return e;
+  return launch_merge(*p, st);
+}
+
+cudaError_t dispatch_mla(const Geometry& g, const DecodeParams* p, size_t smem, cudaStream_t st) {
+  switch (g.h_q) {
+    case 16: return run_mla<16>(p, smem, st);
+    case 32: return run_mla<32>(p, smem, st);
+    case 64: return run_mla<64>(p, smem, st);
+    case 128: return run_mla<128>(p, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace hs

@@ -18,7 +18,6 @@ constexpr unsigned FULL_MASK = 0xffffffffu;
 // ---- geometry fixed by the kernels ------------------------------------------
 constexpr int SC_THREADS = 256;      // score kernel CTA
 constexpr int IDX_TILE_BYTES = 32768;  // index keys per bulk copy (one tile)
-constexpr int IDX_STAGES = 4;
 constexpr int IDX_BINS = 4096;       // radix digit: 12 bits, two levels cover 24-bit keys
 constexpr int IDX_KEY_BIAS = 1 << 22;  // |score| <= 128*128*256 = 2^22 for d_idx <= 256
 
@@ -64,7 +63,7 @@ struct DeviceState {
   int32_t* slot_of_sel;    // [R][k]
   float* part_o;           // [R][parts][h_q][d_v]
   float* part_ml;          // [R][parts][h_q][2]
-  unsigned int* att_counter;   // [R]
+  int32_t* att_nparts;     // [R][8] partial results of each (request, head group) of the current call
   unsigned int* app_counter;   // [R]
 };
 
@@ -107,6 +106,8 @@ struct hs_handle {
   hs::Geometry g;
   hs::DeviceState s;
   uint16_t* host_kv_host = nullptr;   // host view of the pinned store
+  void* host_map_base = nullptr;      // the store's mapping when it was registered (else cudaHostAlloc)
+  size_t host_map_bytes = 0;
   float scale_log2 = 0.f;
   int num_sms = 0;
   long long score_stride = 0;
@@ -145,20 +146,65 @@ int attention_parts(const Geometry& g);
 cudaError_t prepare_score(const Geometry& g, size_t smem);
 cudaError_t prepare_resolve(size_t smem);
 cudaError_t prepare_attention(const Geometry& g, size_t smem);
+// attention over shared latent rows (hs_attention_mla.cu) and the partial merge
+int mla_parts(const Geometry& g);
+size_t mla_smem_bytes(const Geometry& g);
+cudaError_t dispatch_mla(const Geometry& g, const DecodeParams* p, size_t smem, cudaStream_t st);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st);
 
 // Raises a kernel's dynamic shared-memory allowance to at least `smem`, never
-// lowers it: several handles (of different shapes) share the kernels.
+// lowers it: several handles (of different shapes) share the kernels.  Every
+// kernel of the decode path also prefers the largest shared-memory carveout, so
+// consecutive kernels run with the same L1/shared split and the SMs need no
+// reconfiguration between them.
 template <typename F>
 inline cudaError_t allow_smem(F* kern, size_t smem) {
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
+  if (fa.preferredShmemCarveout != (int)cudaSharedmemCarveoutMaxShared) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
+// Launches a kernel that may start while the previous kernel in the stream is
+// still finishing (programmatic dependent launch).  Every such kernel runs
+// griddep_wait() before it reads anything earlier stream work wrote, and calls
+// griddep_launch_dependents() only after that wait, so a kernel that starts
+// early can rely on every kernel before its immediate predecessor having
+// completed.  Shared-memory set-up and barrier initialisation overlap the
+// predecessor's tail; in a CUDA graph the edge becomes a programmatic one.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---- device helpers -------------------------------------------------------------
 #if defined(__CUDACC__)
+
+// Waits until the preceding kernel of the stream has completed and its writes are
+// visible (returns at once when the kernel was launched without the
+// programmatic attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream begin launching.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -242,6 +288,28 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
 }
 
 // 16-byte LSU async copy global (device or mapped host memory) -> shared.
+// L2 policy for data read once (streams): evicted first, so data that is
+// reused soon (scores, partials, prefetched host rows) stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Starts bringing `bytes` (multiple of 16, 16-byte aligned) at gsrc into L2; no completion.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
 }
@@ -256,6 +324,11 @@ __device__ __forceinline__ int4 ld_nc_v4(const void* p) {
 }
 
 __device__ __forceinline__ void set_error(unsigned int* word, unsigned int bit) { atomicOr(word, bit); }
+
+// Fire-and-forget 64-bit add (no value returned, so the issuing thread never waits).
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // bf16 pair (low half = element 0) -> two floats
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -12,23 +12,38 @@
 // smallest (last-use stamp, slot), in that order; every used slot's stamp becomes
 // the (request, layer) step counter, which then grows by one.
 //
-// Design (sm_103a), one 1024-thread CTA per request, everything in shared memory:
-//  1. exact top-k over the 24-bit keys the score kernel left in L2: the first
-//     digit comes from the score kernel's histogram, one pass over the keys
-//     builds the second-digit histogram, and an ordered compaction (per-thread
-//     contiguous ranges + block scans) emits the k positions ascending, taking
-//     keys equal to the threshold in position order;
+// Design (sm_103a), one 1024-thread CTA per request; a latency-bound chain, so
+// every global read the chain needs is issued up front, and the steps between
+// are shared-memory work:
+//  0. prefetch (cp.async): the first-digit histogram the score kernel built, the
+//     LRU list, the reverse map (when it fits) and the appended token's row.
+//  1. exact top-k over the 24-bit keys the score kernel left in L2, in ONE
+//     coalesced pass: the first digit b1 comes from the histogram; each warp
+//     scans a contiguous range of positions, four keys per lane per load, and
+//     turns "digit above b1" into a bitmap (each 8-lane group's 4-bit nibbles
+//     OR-reduced into one 32-position word), while the few keys with digit b1 go
+//     to a per-warp list in position order (warp prefix sums) and into the
+//     second-digit histogram.  The threshold key and the number of equal keys to
+//     take follow from the second histogram; a scan of per-warp counts gives
+//     each warp its output offset, and each lane emits the positions of one
+//     bitmap word, taking keys equal to the threshold in position order.
+//     Contexts above FAST_MAX_N, or a warp whose list overflows (heavy ties),
+//     take the same steps with a second and third read of the keys instead.
 //  2. RESOLVE: hit test through the page table (independent gathers), miss
 //     compaction with prefix sums, victims from an explicit LRU list — slots
 //     sorted by (stamp, slot).  A call only moves the slots it used to the most
 //     recent end (they all get the newest stamp, so they sort by slot among
-//     themselves), so two stable compactions maintain the list: no sort, no heap;
+//     themselves), so two stable compactions maintain the list: no sort, no heap.
+//     The evicted positions come from the prefetched reverse map, so eviction
+//     issues stores only.
 //  3. the host fetch of the missed rows.  With fetch_mode 1 this CTA copies them
 //     from the mapped pinned host copy into their slots (serial, as the pages
 //     describe).  With fetch_mode 0 it marks them in slot_of_sel and the attention
-//     kernel's producer copies them from host memory into its stage (and from
-//     there into the slot) while the rest of the rows stream from HBM, so
-//     host-link time overlaps HBM time.  Both give identical results.
+//     kernel copies them from host memory into its stage (and from there into
+//     the slot) while the rest of the rows stream from HBM, so host-link time
+//     overlaps HBM time.  Both give identical results.
+//  4. the appended token: its index key to the HBM store, its K/V row to the
+//     pinned host copy, length + 1 (stores that drain while the kernel ends).
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -37,11 +52,18 @@ namespace {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int FAST_MAX_N = 256 * 1024;   // one-pass top-k: contexts up to this many positions
+constexpr int RES_WARPS = RES_THREADS / 32;
+constexpr int WCAP = 256;                // digit-b1 keys a warp lists in the one-pass top-k
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
 struct ResLayout {
-  size_t hist, sel, slot, miss_i, victim, used, ord, total;
+  size_t hist, sel, slot, miss_i, victim, ord, rev, used, bitmap, lists, newrow, total;
+  bool rev_smem, fast;
 };
 
-__host__ __device__ inline ResLayout res_layout(int B, int K) {
+__host__ __device__ inline ResLayout res_layout(const Geometry& g) {
+  const int B = g.hot_slots, K = g.top_k;
   ResLayout L;
   size_t off = 0;
   L.hist = off;
@@ -58,6 +80,19 @@ __host__ __device__ inline ResLayout res_layout(int B, int K) {
   off += (size_t)B * 4;
   L.used = off;
   off += align_up((size_t)B, 16);
+  L.newrow = off;
+  off += align_up((size_t)g.row_bytes, 16) + align_up((size_t)g.d_idx, 16);
+  const size_t base = off;
+  // optional parts, in order of value: the one-pass top-k, then the reverse map
+  const size_t fast_bytes = (size_t)FAST_MAX_N / 8 + (size_t)WCAP * RES_WARPS * 4;
+  L.fast = base + fast_bytes <= SMEM_LIMIT;
+  L.bitmap = off;
+  if (L.fast) off += (size_t)FAST_MAX_N / 8;
+  L.lists = off;
+  if (L.fast) off += (size_t)WCAP * RES_WARPS * 4;
+  L.rev = off;
+  L.rev_smem = off + (size_t)B * 4 <= SMEM_LIMIT;
+  if (L.rev_smem) off += (size_t)B * 4;
   L.total = off;
   return L;
 }
@@ -65,6 +100,7 @@ __host__ __device__ inline ResLayout res_layout(int B, int K) {
 struct ResShared {
   int scan[2 * (RES_THREADS / 32 + 1)];
   int b1, above1, b2, above2;
+  int N, len, t_step;
 };
 
 // Finds the digit holding the kneed-th largest key (bins scanned from the top)
@@ -96,7 +132,7 @@ __device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* 
 
 }  // namespace
 
-size_t resolve_smem_bytes(const Geometry& g) { return res_layout(g.hot_slots, g.top_k).total; }
+size_t resolve_smem_bytes(const Geometry& g) { return res_layout(g).total; }
 
 __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodeParams p) {
   const Geometry& g = p.g;
@@ -104,6 +140,28 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   const int ri = blockIdx.x;
   const int K = g.top_k;
   const int B = g.hot_slots;
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const ResLayout L = res_layout(g);
+  __shared__ ResShared sh;
+  uint32_t* h = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
+  int32_t* sel = reinterpret_cast<int32_t*>(smem_raw + L.sel);
+  int32_t* slot_sel = reinterpret_cast<int32_t*>(smem_raw + L.slot);
+  int32_t* miss_i = reinterpret_cast<int32_t*>(smem_raw + L.miss_i);
+  int32_t* victim = reinterpret_cast<int32_t*>(smem_raw + L.victim);
+  int32_t* ord = reinterpret_cast<int32_t*>(smem_raw + L.ord);
+  int32_t* rev_s = reinterpret_cast<int32_t*>(smem_raw + L.rev);
+  uint8_t* used = smem_raw + L.used;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + L.bitmap);
+  uint32_t* lists = reinterpret_cast<uint32_t*>(smem_raw + L.lists);   // [warp][WCAP]
+  unsigned char* newrow = smem_raw + L.newrow;
+  unsigned char* newkey = newrow + align_up((size_t)g.row_bytes, 16);
+  HS_TRACE(p, 1, 0);
+
+  for (int j = tid; j < B; j += RES_THREADS) used[j] = 0;
+  griddep_wait();   // the score kernel's keys and histogram, earlier appends
+  griddep_launch_dependents();
+
   int32_t* sel_g = p.s.sel + (long long)ri * K;
   int32_t* sel_out = p.sel_out ? p.sel_out + (long long)ri * K : nullptr;
   const int req = p.req_ids ? p.req_ids[ri] : ri;
@@ -113,48 +171,38 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
       for (int i = tid; i < K; i += RES_THREADS) sel_out[i] = -1;
     return;
   }
-  HS_TRACE(p, 1, 0);
   const long long rl = (long long)req * g.n_layers + p.layer;
-  const int len = p.s.length[rl];
 
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const ResLayout L = res_layout(B, K);
-  __shared__ ResShared sh;
-  uint32_t* h = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
-  int32_t* sel = reinterpret_cast<int32_t*>(smem_raw + L.sel);
-  int32_t* slot_sel = reinterpret_cast<int32_t*>(smem_raw + L.slot);
-  int32_t* miss_i = reinterpret_cast<int32_t*>(smem_raw + L.miss_i);
-  int32_t* victim = reinterpret_cast<int32_t*>(smem_raw + L.victim);
-  int32_t* ord = reinterpret_cast<int32_t*>(smem_raw + L.ord);
-  uint8_t* used = smem_raw + L.used;
-
-  // The LRU order list is needed only after the selection: start copying it
-  // into shared memory now (async), so the copy overlaps the top-k passes.
+  // ---- 0. every read the chain needs, issued together ----------------------------
   const int32_t* order_g = p.s.order + rl * B;
   for (int c4 = tid; c4 < B / 4; c4 += RES_THREADS) cp_async_16(ord + 4 * c4, order_g + 4 * c4);
-  const int t_step = p.s.step[rl];
-
-  // ---- the token appended by this call (its score was taken from the input) ----
-  int N = len;
-  if (p.new_kv) {
-    if (len + 1 <= g.max_context) {
-      N = len + 1;
-      const int kvec = g.d_idx / 16;
-      if (tid < kvec)
-        reinterpret_cast<int4*>(p.s.idx_keys + (rl * g.max_context + len) * g.d_idx)[tid] =
-            reinterpret_cast<const int4*>(p.new_keys + (long long)ri * g.d_idx)[tid];
-      const int rvec = g.row_bytes / 16;
-      const int4* src = reinterpret_cast<const int4*>(p.new_kv + (long long)ri * g.row_elems);
-      int4* dst = reinterpret_cast<int4*>(p.s.host_kv + (rl * g.max_context + len) * g.row_elems);
-      for (int v = tid; v < rvec; v += RES_THREADS) dst[v] = src[v];
-      if (tid == 0) {
-        p.s.length[rl] = N;
-        atomicAdd(&p.s.glob[1], (unsigned long long)g.row_bytes);
-      }
-    } else if (tid == 0) {
-      set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
-    }
+  if (L.rev_smem) {
+    const int32_t* rev_g = p.s.reverse + rl * B;
+    for (int c4 = tid; c4 < B / 4; c4 += RES_THREADS) cp_async_16(rev_s + 4 * c4, rev_g + 4 * c4);
   }
+  uint32_t* gh = p.s.hist + (long long)ri * IDX_BINS;
+  static_assert(IDX_BINS == 4 * RES_THREADS, "one 16-byte histogram chunk per thread");
+  cp_async_16(h + 4 * tid, gh + 4 * tid);
+  if (p.new_kv) {
+    for (int v = tid; v < g.row_bytes / 16; v += RES_THREADS)
+      cp_async_16(newrow + 16 * v, reinterpret_cast<const unsigned char*>(p.new_kv + (long long)ri * g.row_elems) + 16 * v);
+    if (tid < g.d_idx / 16) cp_async_16(newkey + 16 * tid, p.new_keys + (long long)ri * g.d_idx + 16 * tid);
+  }
+  if (tid == 0) {
+    const int len = p.s.length[rl];
+    sh.len = len;
+    sh.t_step = p.s.step[rl];
+    int N = len;
+    if (p.new_kv) {
+      if (len + 1 <= g.max_context) N = len + 1;
+      else set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
+    }
+    sh.N = N;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int len = sh.len, N = sh.N, t_step = sh.t_step;
+  const bool appended = N > len;
   const int kk = min(K, N);
   HS_TRACE(p, 1, 1);
 
@@ -163,109 +211,191 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     for (int i = tid; i < N; i += RES_THREADS) sel[i] = i;
   } else {
     const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
-    uint4* gh4 = reinterpret_cast<uint4*>(p.s.hist + (long long)ri * IDX_BINS);
-    static_assert(IDX_BINS == 4 * RES_THREADS, "one 16-byte histogram chunk per thread");
-    reinterpret_cast<uint4*>(h)[tid] = gh4[tid];
-    gh4[tid] = make_uint4(0, 0, 0, 0);   // ready for the next call
-    __syncthreads();
+    reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);   // ready for the next call
     select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
     const int b1 = sh.b1, above1 = sh.above1;
-    HS_TRACE(p, 1, 2);
     reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
     __syncthreads();
-    // second digit: histogram of the low 12 bits of the keys inside digit b1
-    const int n4 = N >> 2;
-    const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-    constexpr int UA = 8;   // loads in flight per thread
-    for (int i0 = tid; i0 < n4; i0 += UA * RES_THREADS) {
-      uint4 v[UA];
+    HS_TRACE(p, 1, 2);
+    // each thread: a contiguous range of whole 32-position words
+    // per-thread contiguous ranges (the rescan path)
+    const int per = ((N + RES_THREADS - 1) / RES_THREADS + 3) & ~3;
+    const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
+    // per-warp contiguous chunks of 128 positions (the one-pass path)
+    const int lane = tid & 31, wid = tid >> 5;
+    const int NC = (N + 127) >> 7;
+    const int c0 = (int)((long long)wid * NC / RES_WARPS), c1 = (int)((long long)(wid + 1) * NC / RES_WARPS);
+    uint32_t* wl = lists + wid * WCAP;
+    const bool fast = L.fast && N <= FAST_MAX_N;
+    int wcnt = 0;       // entries of this warp's list (warp-uniform)
+    int lane_gt = 0;    // keys above digit b1 seen by this lane
+    bool overflow = false;
+    if (fast) {
+      const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
+      constexpr int UC = 4;   // chunks in flight per lane
+      for (int cb = c0; cb < c1; cb += UC) {
+        uint4 v[UC];
 #pragma unroll
-      for (int u = 0; u < UA; ++u) {
-        const int i = i0 + u * RES_THREADS;
-        v[u] = i < n4 ? k4[i] : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < UC; ++u) {
+          const int pos = 128 * (cb + u) + 4 * lane;
+          v[u] = (cb + u < c1 && pos < N) ? k4[(cb + u) * 32 + lane] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < UC; ++u) {
+          if (cb + u >= c1) break;   // warp-uniform
+          const int pos = 128 * (cb + u) + 4 * lane;
+          const uint32_t kv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          uint32_t nib_gt = 0, nib_eq = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (pos + e < N) {
+              const int dg = (int)(kv[e] >> 12);
+              nib_gt |= (uint32_t)(dg > b1) << e;
+              if (dg == b1) {
+                nib_eq |= 1u << e;
+                atomicAdd(&h[kv[e] & 4095u], 1u);
+              }
+            }
+          }
+          lane_gt += __popc(nib_gt);
+          uint32_t word = nib_gt << (4 * (lane & 7));
+          word |= __shfl_xor_sync(FULL_MASK, word, 1);
+          word |= __shfl_xor_sync(FULL_MASK, word, 2);
+          word |= __shfl_xor_sync(FULL_MASK, word, 4);
+          if ((lane & 7) == 0) bitmap[4 * (cb + u) + (lane >> 3)] = word;
+          if (__any_sync(FULL_MASK, nib_eq != 0)) {   // list the digit-b1 keys in position order
+            const int cnt = __popc(nib_eq);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int n = __shfl_up_sync(FULL_MASK, incl, o);
+              if (lane >= o) incl += n;
+            }
+            int at = wcnt + incl - cnt;
+            for (int e = 0; e < 4; ++e)
+              if ((nib_eq >> e) & 1u) {
+                if (at < WCAP) wl[at] = ((uint32_t)(pos + e) << 12) | (kv[e] & 4095u);
+                else overflow = true;
+                ++at;
+              }
+            wcnt += __shfl_sync(FULL_MASK, incl, 31);
+          }
+        }
       }
+    } else {   // second-digit histogram only; the counts and the emission rescan the keys
+      const int n4 = N >> 2;
+      const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+      constexpr int UA = 8;   // loads in flight per thread
+      for (int i0 = tid; i0 < n4; i0 += UA * RES_THREADS) {
+        uint4 v[UA];
 #pragma unroll
-      for (int u = 0; u < UA; ++u) {
-        if ((int)(v[u].x >> 12) == b1) atomicAdd(&h[v[u].x & 4095u], 1u);
-        if ((int)(v[u].y >> 12) == b1) atomicAdd(&h[v[u].y & 4095u], 1u);
-        if ((int)(v[u].z >> 12) == b1) atomicAdd(&h[v[u].z & 4095u], 1u);
-        if ((int)(v[u].w >> 12) == b1) atomicAdd(&h[v[u].w & 4095u], 1u);
+        for (int u = 0; u < UA; ++u) {
+          const int i = i0 + u * RES_THREADS;
+          v[u] = i < n4 ? k4[i] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < UA; ++u) {
+          if ((int)(v[u].x >> 12) == b1) atomicAdd(&h[v[u].x & 4095u], 1u);
+          if ((int)(v[u].y >> 12) == b1) atomicAdd(&h[v[u].y & 4095u], 1u);
+          if ((int)(v[u].z >> 12) == b1) atomicAdd(&h[v[u].z & 4095u], 1u);
+          if ((int)(v[u].w >> 12) == b1) atomicAdd(&h[v[u].w & 4095u], 1u);
+        }
+      }
+      for (int i = 4 * n4 + tid; i < N; i += RES_THREADS) {
+        const uint32_t v = keys[i];
+        if ((int)(v >> 12) == b1) atomicAdd(&h[v & 4095u], 1u);
       }
     }
-    for (int i = 4 * n4 + tid; i < N; i += RES_THREADS) {
-      const uint32_t v = keys[i];
-      if ((int)(v >> 12) == b1) atomicAdd(&h[v & 4095u], 1u);
-    }
-    __syncthreads();
+    const bool use_lists = fast && !__syncthreads_or(overflow);
     HS_TRACE(p, 1, 3);
     select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
     HS_TRACE(p, 1, 4);
-    const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)sh.b2;
+    const int b2 = sh.b2;
+    const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)b2;
     const int need_eq = K - (above1 + sh.above2);   // >= 1
-    // ordered compaction over per-thread contiguous ranges (multiples of 4 keys,
-    // read as 16-byte vectors, 8 in flight; the second read hits L1)
-    const int per = (((N + RES_THREADS - 1) / RES_THREADS) + 3) & ~3;
-    const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
-    const int jv = j0 + ((j1 - j0) & ~3);
-    int n_gt = 0, n_eq = 0;
-    {
-      int j = j0;
-      for (; j + 32 <= jv; j += 32) {
-        uint4 v[8];
+    if (use_lists) {
+      // per-warp counts, then a scan over the warps
+      int n_gt = lane_gt, n_eq = 0;
+      for (int q = lane; q < wcnt; q += 32) {
+        const int lo = (int)(wl[q] & 4095u);
+        n_gt += lo > b2;
+        n_eq += lo == b2;
+      }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(keys + j + 4 * u);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          n_gt += (v[u].x > vstar) + (v[u].y > vstar) + (v[u].z > vstar) + (v[u].w > vstar);
-          n_eq += (v[u].x == vstar) + (v[u].y == vstar) + (v[u].z == vstar) + (v[u].w == vstar);
+      for (int o = 16; o > 0; o >>= 1) {
+        n_gt += __shfl_xor_sync(FULL_MASK, n_gt, o);
+        n_eq += __shfl_xor_sync(FULL_MASK, n_eq, o);
+      }
+      const int2 wb = block_exclusive_scan2<RES_THREADS>(lane == 0 ? n_gt : 0, lane == 0 ? n_eq : 0, sh.scan,
+                                                         nullptr, nullptr);
+      const int gt_before = __shfl_sync(FULL_MASK, wb.x, 0), eq_before = __shfl_sync(FULL_MASK, wb.y, 0);
+      HS_TRACE(p, 1, 5);
+      // emission: lane l owns bitmap word q0 + l of each group of 32 words
+      int out = gt_before + min(eq_before, need_eq);
+      int tie_run = eq_before;   // ties before the current list entry (position order)
+      int qe = 0;                // next list entry
+      const int w_end = 4 * c1;
+      for (int q0 = 4 * c0; q0 < w_end; q0 += 32) {
+        const int q = q0 + lane;
+        uint32_t m = q < w_end ? bitmap[q] : 0u;
+        for (; qe < wcnt; ++qe) {   // list entries of this group of words, in order
+          const uint32_t e = wl[qe];
+          const int pos = (int)(e >> 12);
+          if ((pos >> 5) >= q0 + 32) break;
+          const int lo = (int)(e & 4095u);
+          const bool mine = (pos >> 5) == q;
+          if (lo > b2) {
+            if (mine) m |= 1u << (pos & 31);
+          } else if (lo == b2) {
+            if (mine && tie_run < need_eq) m |= 1u << (pos & 31);
+            ++tie_run;
+          }
         }
-      }
-      for (; j + 4 <= jv; j += 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
-        n_gt += (v.x > vstar) + (v.y > vstar) + (v.z > vstar) + (v.w > vstar);
-        n_eq += (v.x == vstar) + (v.y == vstar) + (v.z == vstar) + (v.w == vstar);
-      }
-      for (; j < j1; ++j) {
-        const uint32_t v = keys[j];
-        n_gt += v > vstar;
-        n_eq += v == vstar;
-      }
-    }
-    const int2 before = block_exclusive_scan2<RES_THREADS>(n_gt, n_eq, sh.scan, nullptr, nullptr);
-    HS_TRACE(p, 1, 5);
-    int o = before.x + min(before.y, need_eq);
-    int eq_rank = before.y;
-    auto emit = [&](int j, uint32_t v) {
-      bool take = v > vstar;
-      if (v == vstar) {
-        take = eq_rank < need_eq;
-        ++eq_rank;
-      }
-      if (take && o < K) sel[o++] = j;
-    };
-    {
-      int j = j0;
-      for (; j + 32 <= jv; j += 32) {
-        uint4 v[8];
+        const int cnt = __popc(m);
+        int incl = cnt;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(keys + j + 4 * u);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (max(max(v[u].x, v[u].y), max(v[u].z, v[u].w)) < vstar) continue;   // nothing taken
-          emit(j + 4 * u, v[u].x);
-          emit(j + 4 * u + 1, v[u].y);
-          emit(j + 4 * u + 2, v[u].z);
-          emit(j + 4 * u + 3, v[u].w);
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += n;
         }
+        int o = out + incl - cnt;
+        while (m) {
+          const int bb = __ffs(m) - 1;
+          m &= m - 1;
+          if (o < K) sel[o++] = 32 * q + bb;
+        }
+        out += __shfl_sync(FULL_MASK, incl, 31);
       }
-      for (; j + 4 <= jv; j += 4) {
+    } else {
+      int n_gt = 0, n_eq = 0;
+      for (int j = j0; j < j1; j += 4) {   // multiples of 4 in bounds (padded rows)
         const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
-        emit(j, v.x);
-        emit(j + 1, v.y);
-        emit(j + 2, v.z);
-        emit(j + 3, v.w);
+        const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < j1) {
+            n_gt += kv[e] > vstar;
+            n_eq += kv[e] == vstar;
+          }
       }
-      for (; j < j1; ++j) emit(j, keys[j]);
+      const int2 before = block_exclusive_scan2<RES_THREADS>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+      HS_TRACE(p, 1, 5);
+      int o = before.x + min(before.y, need_eq);
+      int eq_rank = before.y;
+      for (int j = j0; j < j1; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
+        const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < j1) {
+            bool take = kv[e] > vstar;
+            if (kv[e] == vstar) {
+              take = eq_rank < need_eq;
+              ++eq_rank;
+            }
+            if (take && o < K) sel[o++] = j + e;
+          }
+      }
     }
   }
   __syncthreads();
@@ -275,10 +405,6 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     if (i < kk) sel_g[i] = v;
     if (sel_out) sel_out[i] = v;
   }
-  if (kk == 0) {   // nothing selected: the attention kernel writes zeros
-    cp_async_wait_all();
-    return;
-  }
 
   // ======================= 2. RESOLVE metadata =======================
   int32_t* page = p.s.page + rl * g.max_context;
@@ -286,115 +412,131 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   int32_t* stamp = p.s.stamp + rl * B;
   int32_t* order = p.s.order + rl * B;
   const int t = t_step;
-  for (int j = tid; j < B; j += RES_THREADS) used[j] = 0;
-  cp_async_wait_all();   // this thread's part of the LRU list has landed
-  // hit test: independent page-table gathers, four in flight per thread
-  bool bad = false;
-  for (int i0 = tid; i0 < kk; i0 += 4 * RES_THREADS) {
-    int pos[4], s4[4];
+  int m = 0;
+  if (kk > 0) {
+    // hit test: independent page-table gathers, four in flight per thread
+    bool bad = false;
+    for (int i0 = tid; i0 < kk; i0 += 4 * RES_THREADS) {
+      int pos[4], s4[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * RES_THREADS;
-      pos[u] = i < kk ? sel[i] : -1;
-    }
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * RES_THREADS;
+        pos[u] = i < kk ? sel[i] : -1;
+      }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) s4[u] = (pos[u] >= 0 && pos[u] < N) ? page[pos[u]] : -1;
+      for (int u = 0; u < 4; ++u) s4[u] = (pos[u] >= 0 && pos[u] < N) ? page[pos[u]] : -1;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * RES_THREADS;
-      if (i < kk) {
-        if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
-        slot_sel[i] = s4[u];
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * RES_THREADS;
+        if (i < kk) {
+          if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
+          slot_sel[i] = s4[u];
+          if (s4[u] >= 0 && s4[u] < B) used[s4[u]] = 1;
+          // a miss the attention kernel will read from host memory: start moving
+          // it over the host link into L2 now (the appended row is written below)
+          if (s4[u] < 0 && p.fetch_mode == 0 && pos[u] >= 0 && pos[u] < N && !(appended && pos[u] == len))
+            bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(p.s.host_kv) +
+                                 ((size_t)rl * g.max_context + pos[u]) * g.row_bytes,
+                             (uint32_t)g.row_bytes);
+        }
       }
     }
-  }
-  __syncthreads();   // `used` is cleared before it is marked
-  for (int i = tid; i < kk; i += RES_THREADS) {
-    const int sl = slot_sel[i];
-    if (sl >= 0 && sl < B) used[sl] = 1;
-  }
-  HS_TRACE(p, 1, 7);
-  if (__syncthreads_or(bad)) {
-    if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
-    return;   // slot_of_sel keeps in-range values from before: the attention stays in bounds
-  }
-  HS_TRACE(p, 1, 8);
-  // misses in ascending selection order, and the unpinned entries of the LRU list
-  const int per_i = (kk + RES_THREADS - 1) / RES_THREADS;
-  const int i0 = min(kk, tid * per_i), i1 = min(kk, i0 + per_i);
-  const int per_j = (B + RES_THREADS - 1) / RES_THREADS;
-  const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
-  int nm = 0, nc = 0;
-  for (int i = i0; i < i1; ++i) nm += slot_sel[i] < 0;
-  for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
-  int m;
-  const int2 mc = block_exclusive_scan2<RES_THREADS>(nm, nc, sh.scan, &m, nullptr);
-  int mb = mc.x;
-  for (int i = i0; i < i1; ++i)
-    if (slot_sel[i] < 0) miss_i[mb++] = i;
-  // victims: the first m unpinned entries of the LRU list
-  int cb = mc.y;
-  for (int j = j0; j < j1 && cb < m; ++j) {
-    const int sl = ord[j];
-    if (used[sl] == 0) {
-      victim[cb++] = sl;
-      used[sl] = 2;
+    if (__syncthreads_or(bad)) {
+      if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
+      return;   // slot_of_sel keeps in-range values from before: the attention stays in bounds
     }
-  }
-  __syncthreads();
-  HS_TRACE(p, 1, 9);
-  // evict, then record the new residents
-  bool incons = false;
-  for (int r = tid; r < m; r += RES_THREADS) {
-    const int v = victim[r];
-    const int i = miss_i[r];
-    const int pnew = sel[i];
-    const int old = reverse[v];
-    if (old >= 0) {
-      if (old >= g.max_context || page[old] != v) incons = true;
-      else page[old] = -1;
+    HS_TRACE(p, 1, 7);
+    // misses in ascending selection order, and the unpinned entries of the LRU list
+    const int per_i = (kk + RES_THREADS - 1) / RES_THREADS;
+    const int i0 = min(kk, tid * per_i), i1 = min(kk, i0 + per_i);
+    const int per_j = (B + RES_THREADS - 1) / RES_THREADS;
+    const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
+    int nm = 0, nc = 0;
+    for (int i = i0; i < i1; ++i) nm += slot_sel[i] < 0;
+    for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
+    HS_TRACE(p, 1, 20);
+    const int2 mc = block_exclusive_scan2<RES_THREADS>(nm, nc, sh.scan, &m, nullptr);
+    HS_TRACE(p, 1, 21);
+    int mb = mc.x;
+    for (int i = i0; i < i1; ++i)
+      if (slot_sel[i] < 0) miss_i[mb++] = i;
+    // victims: the first m unpinned entries of the LRU list
+    int cb = mc.y;
+    for (int j = j0; j < j1 && cb < m; ++j) {
+      const int sl = ord[j];
+      if (used[sl] == 0) {
+        victim[cb++] = sl;
+        used[sl] = 2;
+      }
     }
-    reverse[v] = pnew;
-    page[pnew] = v;
-    slot_sel[i] = v;
-  }
-  if (incons) set_error(p.s.dev_error, HS_DEVERR_METADATA);
-  __syncthreads();
-  HS_TRACE(p, 1, 10);
-  // slot of every selected position (misses flagged for the attention kernel
-  // when it does the fetch); stamp every used slot
-  const int miss_flag = p.fetch_mode == 0 ? HS_SLOT_MISS_FLAG : 0;
-  int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
-  for (int i = tid; i < kk; i += RES_THREADS) {
-    const int sl = slot_sel[i];
-    stamp[sl] = t;
-    sos[i] = sl;
-  }
-  __syncthreads();
-  for (int r = tid; r < m; r += RES_THREADS) sos[miss_i[r]] = victim[r] | miss_flag;
-  HS_TRACE(p, 1, 11);
-  // new LRU list: unused slots keep their order, used slots go last by slot
-  int nu = 0, nus = 0;
-  for (int j = j0; j < j1; ++j) nu += used[ord[j]] == 0;
-  for (int sl = j0; sl < j1; ++sl) nus += used[sl] != 0;
-  int n_unused;
-  const int2 un = block_exclusive_scan2<RES_THREADS>(nu, nus, sh.scan, &n_unused, nullptr);
-  int ub = un.x;
-  for (int j = j0; j < j1; ++j) {
-    const int sl = ord[j];
-    if (used[sl] == 0) order[ub++] = sl;
-  }
-  int sb = n_unused + un.y;
-  for (int sl = j0; sl < j1; ++sl)
-    if (used[sl] != 0) order[sb++] = sl;
-  if (tid == 0) {
-    p.s.step[rl] = t + 1;
-    p.s.hits[rl] += (unsigned long long)(kk - m);
-    p.s.misses[rl] += (unsigned long long)m;
-    atomicAdd(&p.s.glob[0], (unsigned long long)m * g.row_bytes);
+    __syncthreads();
+    HS_TRACE(p, 1, 8);
+    // evict, then record the new residents (stores only)
+    for (int q = tid; q < m; q += RES_THREADS) {
+      const int v = victim[q];
+      const int i = miss_i[q];
+      const int pnew = sel[i];
+      const int old = L.rev_smem ? rev_s[v] : reverse[v];
+      if (old >= 0 && old < g.max_context) page[old] = -1;
+      reverse[v] = pnew;
+      page[pnew] = v;
+      slot_sel[i] = v;
+    }
+    __syncthreads();
+    HS_TRACE(p, 1, 9);
+    // slot of every selected position (misses flagged for the attention kernel
+    // when it does the fetch); stamp every used slot
+    const int miss_flag = p.fetch_mode == 0 ? HS_SLOT_MISS_FLAG : 0;
+    int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
+    for (int i = tid; i < kk; i += RES_THREADS) {
+      const int sl = slot_sel[i];
+      stamp[sl] = t;
+      sos[i] = sl;
+    }
+    HS_TRACE(p, 1, 22);
+    __syncthreads();
+    HS_TRACE(p, 1, 23);
+    for (int q = tid; q < m; q += RES_THREADS) sos[miss_i[q]] = victim[q] | miss_flag;
+    // new LRU list: unused slots keep their order, used slots go last by slot
+    int nu = 0, nus = 0;
+    for (int j = j0; j < j1; ++j) nu += used[ord[j]] == 0;
+    for (int sl = j0; sl < j1; ++sl) nus += used[sl] != 0;
+    int n_unused;
+    HS_TRACE(p, 1, 24);
+    const int2 un = block_exclusive_scan2<RES_THREADS>(nu, nus, sh.scan, &n_unused, nullptr);
+    HS_TRACE(p, 1, 25);
+    int ub = un.x;
+    for (int j = j0; j < j1; ++j) {
+      const int sl = ord[j];
+      if (used[sl] == 0) order[ub++] = sl;
+    }
+    int sb = n_unused + un.y;
+    for (int sl = j0; sl < j1; ++sl)
+      if (used[sl] != 0) order[sb++] = sl;
+    HS_TRACE(p, 1, 26);
+    if (tid == 0) {
+      p.s.step[rl] = t + 1;
+      red_add_u64(&p.s.hits[rl], (unsigned long long)(kk - m));
+      red_add_u64(&p.s.misses[rl], (unsigned long long)m);
+      red_add_u64(&p.s.glob[0], (unsigned long long)m * g.row_bytes);
+    }
+    HS_TRACE(p, 1, 10);
   }
 
-  HS_TRACE(p, 1, 12);
+  // ======================= 4. the appended token =======================
+  if (appended) {
+    const int rvec = g.row_bytes / 16;
+    int4* dst = reinterpret_cast<int4*>(p.s.host_kv + (rl * g.max_context + len) * g.row_elems);
+    for (int v = tid; v < rvec; v += RES_THREADS) dst[v] = reinterpret_cast<const int4*>(newrow)[v];
+    if (tid < g.d_idx / 16)
+      reinterpret_cast<int4*>(p.s.idx_keys + (rl * g.max_context + len) * g.d_idx)[tid] =
+          reinterpret_cast<const int4*>(newkey)[tid];
+    if (tid == 0) {
+      p.s.length[rl] = N;
+      red_add_u64(&p.s.glob[1], (unsigned long long)g.row_bytes);
+    }
+  }
+
   // ======================= 3. host fetch (fetch_mode 1) =======================
   if (p.fetch_mode == 1 && m > 0) {
     const int rvec = g.row_bytes / 16;
@@ -403,7 +545,6 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
         reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
     unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * B * g.row_bytes;
     constexpr int U = 4;
-    // plain (coherent) loads: the row appended above may be among the misses
     for (long long e0 = tid; e0 < total; e0 += (long long)U * RES_THREADS) {
       int4 v[U];
 #pragma unroll
@@ -411,7 +552,10 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
         const long long e = e0 + (long long)u * RES_THREADS;
         if (e < total) {
           const int q = (int)(e / rvec), cidx = (int)(e - (long long)q * rvec);
-          v[u] = *reinterpret_cast<const int4*>(src_base + (size_t)sel[miss_i[q]] * g.row_bytes + cidx * 16);
+          const int pos = sel[miss_i[q]];
+          // the token appended by this call is read from its input copy
+          v[u] = (appended && pos == len) ? reinterpret_cast<const int4*>(newrow)[cidx]
+                                          : *reinterpret_cast<const int4*>(src_base + (size_t)pos * g.row_bytes + cidx * 16);
         }
       }
 #pragma unroll
@@ -428,8 +572,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
 }
 
 cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st) {
-  topk_resolve_kernel<<<p.n_req, RES_THREADS, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(topk_resolve_kernel, dim3(p.n_req), dim3(RES_THREADS), smem, st, p);
 }
 
 cudaError_t prepare_resolve(size_t smem) {

@@ -9,11 +9,16 @@
 // int32 with dp4a.
 //
 // Design (sm_103a), HBM-bound (d_idx bytes read per position, 4 written):
-//  * Persistent grid (SMs x 2).  The positions of all requests are flattened
-//    into tiles of IDX_TILE_BYTES of keys; CTA c takes a contiguous tile range,
-//    so it meets at most a few request boundaries.
-//  * Thread 0 streams the tiles HBM -> shared memory with 1-D bulk async copies
-//    (cp.async.bulk, mbarrier completion), IDX_STAGES deep.
+//  * Persistent grid, one CTA per SM.  The positions of all requests are
+//    flattened and split into equal contiguous ranges, one per CTA (so every CTA
+//    streams the same number of bytes); a CTA meets at most a few request
+//    boundaries.  A per-request table in shared memory (position prefix, request
+//    id, length) locates every tile without global loads.
+//  * Thread 0 streams the range HBM -> shared memory as tiles of up to
+//    IDX_TILE_BYTES (cut at request boundaries) with 1-D bulk async copies
+//    (cp.async.bulk, mbarrier completion), up to six stages deep: with one tile
+//    being scored the rest keep >= 128 KB per SM in flight, which is what a
+//    single CTA per SM needs to reach full HBM bandwidth on this part.
 //  * One lane per position.  Lane l reads the 16-byte chunks of its position in
 //    the rotated order (c + rot) mod NCH so the 8 lanes of a quarter warp hit 8
 //    different bank groups; the query chunks sit in registers in the same rotated
@@ -21,6 +26,8 @@
 //  * key = score + 2^22 (|score| <= 128*128*256 = 2^22) is stored to a per-call
 //    scratch row; the high-digit histogram is kept in shared memory per request
 //    segment and added to the request's global histogram when the segment ends.
+//  * Launched as a programmatic dependent: barrier and histogram set-up overlap
+//    the previous kernel's tail.
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -29,8 +36,12 @@ namespace {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int SC_MAX_STAGES = 6;
+constexpr size_t SC_SMEM_LIMIT = 227 * 1024;
+
 struct ScoreLayout {
-  size_t bar, prefix, hist, stage, total;
+  size_t bar, pprefix, req, len, hist, stage, total;
+  int nstage;
 };
 
 __host__ __device__ inline ScoreLayout score_layout(const Geometry& g) {
@@ -38,12 +49,20 @@ __host__ __device__ inline ScoreLayout score_layout(const Geometry& g) {
   size_t off = 0;
   L.bar = off;
   off += 128;
-  L.prefix = off;
-  off += align_up((size_t)(g.max_requests + 1) * 4, 128);
+  L.pprefix = off;   // long long [n + 1]: first flattened position of request i
+  off += align_up((size_t)(g.max_requests + 1) * 8, 128);
+  L.req = off;       // int [n]: request id (-1: no selection needed)
+  off += align_up((size_t)g.max_requests * 4, 128);
+  L.len = off;       // int [n]: positions of request i this call (with the appended token)
+  off += align_up((size_t)g.max_requests * 4, 128);
   L.hist = off;
   off += IDX_BINS * 4;
   L.stage = off;
-  off += (size_t)IDX_STAGES * IDX_TILE_BYTES;
+  // as many 32 KB stages as fit (at least two): with one stage being scored,
+  // the others keep >= 128 KB of copies in flight per SM
+  const size_t room = SC_SMEM_LIMIT > off ? (SC_SMEM_LIMIT - off) / IDX_TILE_BYTES : 0;
+  L.nstage = (int)(room < 2 ? 2 : (room > SC_MAX_STAGES ? SC_MAX_STAGES : room));
+  off += (size_t)L.nstage * IDX_TILE_BYTES;
   L.total = off;
   return L;
 }
@@ -55,7 +74,7 @@ size_t score_smem_bytes(const Geometry& g) { return score_layout(g).total; }
 template <int NCH>
 __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
   constexpr int d = NCH * 16;
-  constexpr int TP = IDX_TILE_BYTES / d;   // positions per tile
+  constexpr int TP = IDX_TILE_BYTES / d;   // positions per full tile
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31;
   const int c = blockIdx.x;
@@ -63,100 +82,141 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const ScoreLayout L = score_layout(g);
+  const int NST = L.nstage;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
-  int* prefix = reinterpret_cast<int*>(smem_raw + L.prefix);   // first tile of request i
+  long long* pprefix = reinterpret_cast<long long*>(smem_raw + L.pprefix);
+  int* req_s = reinterpret_cast<int*>(smem_raw + L.req);
+  int* len_s = reinterpret_cast<int*>(smem_raw + L.len);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
   unsigned char* stage = smem_raw + L.stage;
-  __shared__ int scan_tmp[SC_THREADS / 32 + 1];
+  __shared__ long long scan_tmp[SC_THREADS / 32 + 1];
+  __shared__ __align__(16) unsigned char new_key[256];
   HS_TRACE(p, 0, 0);
 
-  // ---- tiles of every request that needs a selection (N > k) ------------------
-  int carry = 0;
-  for (int base = 0; base < p.n_req; base += SC_THREADS) {
-    const int i = base + tid;
-    int tiles = 0;
-    if (i < p.n_req) {
-      const int req = p.req_ids ? p.req_ids[i] : i;
-      if (req >= 0 && req < g.max_requests) {
-        int N = p.s.length[(long long)req * g.n_layers + p.layer];
-        if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
-        if (N > K) tiles = (N + TP - 1) / TP;
-      }
-    }
-    int tot;
-    const int ex = block_exclusive_scan<SC_THREADS>(tiles, scan_tmp, &tot);
-    if (i < p.n_req) prefix[i] = carry + ex;
-    carry += tot;
-  }
   for (int b = tid; b < IDX_BINS; b += SC_THREADS) hist[b] = 0;
   if (tid == 0) {
-    prefix[p.n_req] = carry;
-    for (int s = 0; s < IDX_STAGES; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < NST; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
   }
+  griddep_wait();   // lengths, keys and the query come from earlier stream work
+  griddep_launch_dependents();
+
+  // ---- positions of every request that needs a selection (N > k) ----------------
+  long long carry = 0;
+  for (int base = 0; base < p.n_req; base += SC_THREADS) {
+    const int i = base + tid;
+    long long npos = 0;
+    if (i < p.n_req) {
+      const int req = p.req_ids ? p.req_ids[i] : i;
+      int N = 0;
+      if (req >= 0 && req < g.max_requests) {
+        N = p.s.length[(long long)req * g.n_layers + p.layer];
+        if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
+      }
+      npos = N > K ? N : 0;
+      req_s[i] = npos ? req : -1;
+      len_s[i] = N;
+    }
+    // block-wide exclusive scan of 64-bit counts
+    long long incl = npos;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long n = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) scan_tmp[tid >> 5] = incl;
+    __syncthreads();
+    if (tid < 32) {
+      long long x = tid < SC_THREADS / 32 ? scan_tmp[tid] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long n = __shfl_up_sync(FULL_MASK, x, o);
+        if (lane >= o) x += n;
+      }
+      if (tid < SC_THREADS / 32) scan_tmp[tid] = x;   // inclusive warp totals
+    }
+    __syncthreads();
+    const long long wbase = (tid >> 5) ? scan_tmp[(tid >> 5) - 1] : 0;
+    if (i < p.n_req) pprefix[i] = carry + wbase + incl - npos;
+    carry += scan_tmp[SC_THREADS / 32 - 1];
+    __syncthreads();
+  }
+  if (tid == 0) pprefix[p.n_req] = carry;
   __syncthreads();
   HS_TRACE(p, 0, 1);
-  const long long T = carry;
-  if (T == 0) return;
-  const int Gc = (int)min((long long)gridDim.x, T);
+  const long long P = carry;
+  if (P == 0) return;
+  const int Gc = (int)min((long long)gridDim.x, (P + TP - 1) / TP);
   if (c >= Gc) return;
-  const int t0 = (int)((long long)c * T / Gc), t1 = (int)((long long)(c + 1) * T / Gc);
+  const long long a0 = (long long)c * P / Gc, a1 = (long long)(c + 1) * P / Gc;
   int r0 = 0;
   {
     int lo = 0, hi = p.n_req - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= t0) lo = mid;
+      if (pprefix[mid] <= a0) lo = mid;
       else hi = mid - 1;
     }
     r0 = lo;
-    while (prefix[r0 + 1] <= t0) ++r0;
+    while (pprefix[r0 + 1] <= a0) ++r0;
   }
 
-  // where tile t of this CTA lives
+  // Tiles: consecutive pieces of [a0, a1), at most TP positions, never across a
+  // request boundary.  Walking them needs only the shared tables.
+  struct Cursor {
+    int r;
+    long long a;   // flattened position of the next tile
+  };
   struct TileRef {
     int r, npos, newpos;   // newpos: position of the appended token (its key comes from the input), or -1
     long long pos0, rl;
   };
-  auto tile_ref = [&](int t, int& rc) -> TileRef {
-    while (prefix[rc + 1] <= t) ++rc;
+  auto next_tile = [&](Cursor& cu) -> TileRef {
+    while (pprefix[cu.r + 1] <= cu.a) ++cu.r;
     TileRef tr;
-    tr.r = rc;
-    const int req = p.req_ids ? p.req_ids[rc] : rc;
-    tr.rl = (long long)req * g.n_layers + p.layer;
-    int N = p.s.length[tr.rl];
-    tr.newpos = -1;
-    if (p.new_kv && N + 1 <= g.max_context) tr.newpos = N++;
-    tr.pos0 = (long long)(t - prefix[rc]) * TP;
-    tr.npos = (int)min((long long)TP, N - tr.pos0);
+    tr.r = cu.r;
+    tr.rl = (long long)req_s[cu.r] * g.n_layers + p.layer;
+    const int N = len_s[cu.r];
+    tr.newpos = p.new_kv ? N - 1 : -1;
+    tr.pos0 = cu.a - pprefix[cu.r];
+    tr.npos = (int)min(min((long long)TP, (long long)N - tr.pos0), a1 - cu.a);
+    cu.a += tr.npos;
     return tr;
   };
+  // tile count of this CTA
+  int ntile = 0;
+  {
+    Cursor cu{r0, a0};
+    while (cu.a < a1) {
+      (void)next_tile(cu);
+      ++ntile;
+    }
+  }
 
-  int r_issue = r0;
-  auto issue = [&](int k) {   // tile t0 + k into stage k % IDX_STAGES
-    const TileRef tr = tile_ref(t0 + k, r_issue);
-    const int s = k % IDX_STAGES;
+  Cursor cu_issue{r0, a0};
+  const uint64_t stream_policy = l2_evict_first_policy();   // index keys are read once per call
+  auto issue = [&](int k) {   // tile k into stage k % NST
+    const TileRef tr = next_tile(cu_issue);
+    const int s = k % NST;
     const uint32_t bytes = (uint32_t)(tr.npos * d);
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(&bar[s], bytes);
-    bulk_g2s(stage + (size_t)s * IDX_TILE_BYTES, p.s.idx_keys + (tr.rl * g.max_context + tr.pos0) * d, bytes,
-             &bar[s]);
+    bulk_g2s_hint(stage + (size_t)s * IDX_TILE_BYTES, p.s.idx_keys + (tr.rl * g.max_context + tr.pos0) * d, bytes,
+                  &bar[s], stream_policy);
   };
-  const int ntile = t1 - t0;
   if (tid == 0)
-    for (int k = 0; k < IDX_STAGES && k < ntile; ++k) issue(k);
+    for (int k = 0; k < NST && k < ntile; ++k) issue(k);
 
   const int rot = NCH >= 8 ? (lane & (NCH - 1)) : ((lane & 7) / (8 / NCH));
   int4 qrot[NCH];
   int q_r = -1;
-  __shared__ __align__(16) unsigned char new_key[256];
 
-  int r_cur = r0;
+  Cursor cu{r0, a0};
   bool timed_out = false;
   int consumed = 0;
   for (int k = 0; k < ntile; ++k) {
-    const int s = k % IDX_STAGES;
-    const TileRef tr = tile_ref(t0 + k, r_cur);
+    const int s = k % NST;
+    const TileRef tr = next_tile(cu);
     if (tr.r != q_r) {   // the request's query chunks, rotated per lane
       q_r = tr.r;
       const int4* qsrc = reinterpret_cast<const int4*>(p.q_idx + (long long)tr.r * d);
@@ -166,7 +226,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     const int jnew = (tr.newpos >= tr.pos0 && tr.newpos < tr.pos0 + tr.npos) ? (int)(tr.newpos - tr.pos0) : -1;
     if (jnew >= 0 && tid < NCH)   // the appended token's key is not in the store yet
       reinterpret_cast<int4*>(new_key)[tid] = reinterpret_cast<const int4*>(p.new_keys + (long long)tr.r * d)[tid];
-    const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((k / IDX_STAGES) & 1));
+    const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((k / NST) & 1));
     if (__syncthreads_or(!ok)) {
       timed_out = true;
       break;
@@ -191,10 +251,9 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
       atomicAdd(&hist[key >> 12], 1u);
     }
     __syncthreads();   // stage s consumed; histogram updates of this tile done
-    if (tid == 0 && k + IDX_STAGES < ntile) issue(k + IDX_STAGES);
+    if (tid == 0 && k + NST < ntile) issue(k + NST);
     // end of this request's segment: add the histogram to the request's one
-    int rn = r_cur;
-    const bool seg_end = (k + 1 == ntile) || (prefix[rn + 1] <= t0 + k + 1);
+    const bool seg_end = (k + 1 == ntile) || (pprefix[tr.r + 1] <= cu.a);
     if (seg_end) {
       uint32_t* gh = p.s.hist + (long long)tr.r * IDX_BINS;
       for (int b = tid; b < IDX_BINS; b += SC_THREADS) {
@@ -210,9 +269,9 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
   HS_TRACE(p, 0, 3);
   if (timed_out) {
     if (tid == 0) {
-      const int issued = min(ntile, consumed + IDX_STAGES);
+      const int issued = min(ntile, consumed + NST);
       for (int k = consumed; k < issued; ++k)
-        (void)mbar_wait_bounded(&bar[k % IDX_STAGES], (uint32_t)((k / IDX_STAGES) & 1));
+        (void)mbar_wait_bounded(&bar[k % NST], (uint32_t)((k / NST) & 1));
       set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
     }
     __syncthreads();
@@ -223,8 +282,7 @@ template <int NCH>
 static cudaError_t run_score(const DecodeParams* p, size_t smem, cudaStream_t st) {
   auto kern = score_kernel<NCH>;
   if (p == nullptr) return allow_smem(kern, smem);
-  kern<<<p->score_grid, SC_THREADS, smem, st>>>(*p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p->score_grid), dim3(SC_THREADS), smem, st, *p);
 }
 
 static cudaError_t dispatch_score(int d_idx, const DecodeParams* p, size_t smem, cudaStream_t st) {
