@@ -65,9 +65,9 @@ extern "C" {
  *   GQA: d_qk = d_v = 128, h_q % h_kv == 0, h_kv in {1,2,4,8}, h_q/h_kv <= 16.
  *   latent: h_kv = 1, d_qk = 576, d_v = 512, h_q in {16, 32, 64, 128}.
  *   d_idx in {16, 32, 64, 128, 256}; 1 <= top_k <= hot_slots <= 16384, hot_slots % 4 == 0;
- *   top_k <= 8192; 1 <= max_context <= HS_MAX_CONTEXT (and the indexer's shared
- *   memory must hold max_context / cluster scores); n_layers >= 1;
- *   1 <= max_requests <= 4096.
+ *   top_k <= 8192; 1 <= max_context <= HS_MAX_CONTEXT; n_layers >= 1;
+ *   1 <= max_requests <= 4096 (and every kernel's shared-memory layout must fit,
+ *   else HS_ERR_CONFIG names the kernel).
  */
 #define HS_MAX_CONTEXT (1 << 20)
 
@@ -86,9 +86,12 @@ typedef struct hs_config {
   float softmax_scale;   /* 0 => 1/sqrt(d_qk) */
   int32_t device;        /* CUDA device ordinal */
   int32_t fetch_mode;    /* where missed rows are copied host -> HBM (results identical):
-                            0 = by loader warps of the attention kernel, overlapping the
-                                HBM reads of the hit rows (default);
-                            1 = inside the RESOLVE kernel, before attention starts */
+                            0 = by a loader warp of the attention kernel, overlapping the
+                                HBM reads of the hit rows; RESOLVE starts moving them
+                                into L2 as soon as it finds them (default);
+                            1 = inside the RESOLVE kernel, before attention starts.
+                            Latent rows (shared_kv = 1) always use 1: every head
+                            group reads them, so they cross the host link once. */
 } hs_config_t;
 
 typedef struct hs_handle hs_handle_t;
@@ -148,7 +151,10 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
 
 /*
  * hs_decode_layer — one decode layer-step for n_req requests (stream-ordered,
- * no host synchronisation, capturable in a CUDA graph).
+ * no host synchronisation, capturable in a CUDA graph).  Its kernels are
+ * launched as programmatic dependents: each waits for the previous kernel of the
+ * stream before it reads anything, so ordering against earlier stream work is
+ * the usual one.
  *   req_ids     : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
  *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned)
  *   q           : dev bf16 [n_req][h_q][d_qk]   attention query
@@ -213,7 +219,8 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream);
 #define HS_K_APPEND 0        /* append kernel */
 #define HS_K_INDEXER 1       /* scores of every position + first-digit histogram */
 #define HS_K_TOPK_RESOLVE 2  /* exact top-k + RESOLVE (and the host fetch when fetch_mode = 1) */
-#define HS_K_ATTENTION 3     /* attention (and the host fetch when fetch_mode = 0) */
+#define HS_K_ATTENTION 3     /* attention + merge of its split partials (and the host fetch
+                                when fetch_mode = 0) */
 #define HS_K_COUNT 4
 int hs_set_timing(hs_handle_t* h, int32_t enable);
 int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launches /*[HS_K_COUNT]*/);
