@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     bool overflow = false;
     if (fast) {
       const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
-      constexpr int UC = 4;   // chunks in flight per lane
+      constexpr int UC = 8;   // chunks in flight per lane (a 32K-position row in one round)
       for (int cb = c0; cb < c1; cb += UC) {
         uint4 v[UC];
 #pragma unroll
