@@ -96,7 +96,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
@@ -104,9 +104,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self) -> dict:
+    def stop(self, window=None) -> dict:
+        """Summary of the samples taken inside window = (t0, t1) (wall time), or of
+        all samples when none fell inside it."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -118,7 +120,8 @@ class ClockSampler:
         self.t.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        inside = [ln for t, ln in self.lines if window and window[0] <= t <= window[1]]
+        for ln in inside or [ln for _, ln in self.lines]:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -131,7 +134,8 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "timed region" if inside else "whole run (no sample fell inside the timed region)"}
 
 
 def kernel_source_hash(name: str) -> str:
@@ -336,8 +340,10 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     graph = capture(W, W + K)
     clocks = ClockSampler(dev_index)
     clocks.start()
+    time.sleep(0.5)   # the sampler's start-up (NVML initialisation) stays out of the timed region
+    t_wall0 = time.time()
     ms_total = replay_timed(graph)
-    clk = clocks.stop()
+    clk = clocks.stop(window=(t_wall0, time.time()))
     del graph
     st1 = cache.stats()
     misses = st1["misses"] - st0["misses"]
@@ -485,15 +491,16 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=61)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="hisparse", choices=["hisparse", "reference"])
     ap.add_argument("--workload", default="batch16_32k", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--hot-slots", type=int, default=None)
     ap.add_argument("--sigma", type=float, default=None)
     ap.add_argument("--e2e-steps", type=int, default=8)
-    ap.add_argument("--fetch-mode", type=int, default=0, choices=[0, 1],
-                    help="0: attention kernel fetches missed rows (overlapped); 1: RESOLVE does")
+    ap.add_argument("--fetch-mode", type=int, default=2, choices=[0, 1, 2],
+                    help="who copies missed rows: 0 the attention kernel (overlapped), 1 RESOLVE, "
+                         "2 chosen per request (default)")
     ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -87,9 +87,14 @@ typedef struct hs_config {
   int32_t device;        /* CUDA device ordinal */
   int32_t fetch_mode;    /* where missed rows are copied host -> HBM (results identical):
                             0 = by a loader warp of the attention kernel, overlapping the
-                                HBM reads of the hit rows; RESOLVE starts moving them
-                                into L2 as soon as it finds them (default);
-                            1 = inside the RESOLVE kernel, before attention starts.
+                                HBM reads of the hit rows (best with few misses per
+                                attention CTA);
+                            1 = inside the RESOLVE kernel, before attention starts;
+                            2 = chosen per request: RESOLVE pulls when the request's
+                                misses times n_req exceed 8 rows per attention CTA,
+                                else the attention kernel (the Python binding's default).
+                            RESOLVE starts every missed row moving into L2 as soon as
+                            it finds it, whichever copies it.
                             Latent rows (shared_kv = 1) always use 1: every head
                             group reads them, so they cross the host link once. */
 } hs_config_t;

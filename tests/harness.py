@@ -16,7 +16,7 @@ def torch_mod():
     return torch
 
 
-def make_cache(w: wl.Workload, steps: int, hot_slots: int | None = None, device: int = 0, fetch_mode: int = 0):
+def make_cache(w: wl.Workload, steps: int, hot_slots: int | None = None, device: int = 0, fetch_mode: int = 2):
     from tiered_kv_cache_int8_gb300 import HiSparseCache
     return HiSparseCache(n_layers=w.n_layers, max_requests=w.n_requests, max_context=w.max_context(steps),
                          h_q=w.h_q, h_kv=w.h_kv, d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k,

@@ -1,5 +1,6 @@
 """Full-size workloads through the decode path the benchmark times (fused
-append, fetch mode 0, the library's own launch shapes), against the CPU oracle.
+append, the default fetch placement, the library's own launch shapes), against
+the CPU oracle.
 
 Every selection of every (request, layer, step) and every (request, layer)'s
 hit and miss totals are compared bit-exactly; the page table, reverse map,

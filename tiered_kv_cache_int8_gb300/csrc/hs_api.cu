@@ -39,7 +39,7 @@ std::string check_config(const hs_config_t& c) {
   if (c.hot_slots < c.top_k || c.hot_slots > 16384) return "hot_slots must be in [top_k, 16384]";
   if (c.hot_slots % 4 != 0) return "hot_slots must be a multiple of 4";
   if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return "softmax_scale must be finite and >= 0";
-  if (c.fetch_mode != 0 && c.fetch_mode != 1) return "fetch_mode must be 0 or 1";
+  if (c.fetch_mode < 0 || c.fetch_mode > 2) return "fetch_mode must be 0, 1 or 2";
   if (c.shared_kv == 0) {
     if (c.d_qk != 128 || c.d_v != 128) return "GQA rows: d_qk = d_v = 128 required";
     if (!is_pow2_in(c.h_kv, 1, 8)) return "GQA rows: h_kv must be one of 1, 2, 4, 8";
@@ -295,6 +295,9 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.dev_error, 16, true},
       {(void**)&s.scores, R * (size_t)h->score_stride * 4, false},
       {(void**)&s.hist, R * (size_t)hs::IDX_BINS * 4, false},
+      {(void**)&s.cand_thr, R * Lr * 4, true},
+      {(void**)&s.cand_cnt, R * 4, false},
+      {(void**)&s.cand, R * 2 * K * 8, false},
       {(void**)&s.sel, R * K * 4, false},
       {(void**)&s.slot_of_sel, R * K * 4, false},
       {(void**)&s.part_o, R * (size_t)h->att_parts * g.h_q * g.d_v * 4, false},
@@ -329,6 +332,8 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.slot_of_sel, 0, R * K * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.att_nparts, 0, R * 8 * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.hist, 0, R * (size_t)hs::IDX_BINS * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.cand_thr, 0, R * Lr * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.cand_cnt, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
 #ifdef HS_WITH_TRACE
   ok = ok && cudaMemset(h->trace, 0, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8) ==
@@ -531,6 +536,7 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream) {
       (e = cudaMemsetAsync(h->s.step + r * L, 0, L * 4, st)) != cudaSuccess ||
       (e = cudaMemsetAsync(h->s.hits + r * L, 0, L * 8, st)) != cudaSuccess ||
       (e = cudaMemsetAsync(h->s.misses + r * L, 0, L * 8, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.cand_thr + r * L, 0, L * 4, st)) != cudaSuccess ||
       (e = hs::launch_init_order(h->s.order + r * L * B, (long long)L, (int)B, st)) != cudaSuccess)
     return cuda_fail(h, e, "hs_reset_request");
   return HS_OK;

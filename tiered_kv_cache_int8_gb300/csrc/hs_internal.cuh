@@ -59,6 +59,11 @@ struct DeviceState {
   // scratch (one call in flight per handle)
   uint32_t* scores;        // [R][score_stride] 24-bit keys of the current call
   uint32_t* hist;          // [R][4096] high-digit histogram of the current call (zero between calls)
+  // candidate pre-filter: keys at or above the (request, layer)'s threshold from
+  // the previous call, listed by the score kernel for the top-k
+  uint32_t* cand_thr;      // [R][L] threshold for the next call (0: none)
+  uint32_t* cand_cnt;      // [R] keys listed in the current call (zero between calls)
+  uint2* cand;             // [R][2k] (position, key), unordered
   int32_t* sel;            // [R][k]
   int32_t* slot_of_sel;    // [R][k]
   float* part_o;           // [R][parts][h_q][d_v]
@@ -303,11 +308,6 @@ __device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, 
           smem_addr(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
-}
-
-// Starts bringing `bytes` (multiple of 16, 16-byte aligned) at gsrc into L2; no completion.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {

@@ -41,7 +41,11 @@
 //     describe).  With fetch_mode 0 it marks them in slot_of_sel and the attention
 //     kernel copies them from host memory into its stage (and from there into
 //     the slot) while the rest of the rows stream from HBM, so host-link time
-//     overlaps HBM time.  Both give identical results.
+//     overlaps HBM time.  fetch_mode 2 chooses per request: this kernel pulls
+//     when the request's misses spread over the attention grid exceed a few rows
+//     per CTA.  All give identical results.  Either way every missed
+//     row is prefetched into L2 (per 128-byte line) the moment its page lookup
+//     misses, so the link starts working before the copies are issued.
 //  4. the appended token: its index key to the HBM store, its K/V row to the
 //     pinned host copy, length + 1 (stores that drain while the kernel ends).
 #include "hs_internal.cuh"
@@ -55,6 +59,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 constexpr int FAST_MAX_N = 256 * 1024;   // one-pass top-k: contexts up to this many positions
 constexpr int RES_WARPS = RES_THREADS / 32;
 constexpr int WCAP = 256;                // digit-b1 keys a warp lists in the one-pass top-k
+constexpr int AUTO_PULL_ROWS_PER_CTA = 8;  // fetch mode 2: pull here above this many misses per attention CTA
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 struct ResLayout {
@@ -99,8 +104,9 @@ __host__ __device__ inline ResLayout res_layout(const Geometry& g) {
 
 struct ResShared {
   int scan[2 * (RES_THREADS / 32 + 1)];
-  int b1, above1, b2, above2;
-  int N, len, t_step;
+  int b1, above1, b2, above2, bt, above_t;
+  int N, len, t_step, cnt;
+  uint32_t thr;
 };
 
 // Finds the digit holding the kneed-th largest key (bins scanned from the top)
@@ -192,6 +198,9 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     const int len = p.s.length[rl];
     sh.len = len;
     sh.t_step = p.s.step[rl];
+    sh.thr = p.s.cand_thr[rl];
+    sh.cnt = (int)min(p.s.cand_cnt[ri], 0x7fffffffu);
+    p.s.cand_cnt[ri] = 0;   // ready for the next call
     int N = len;
     if (p.new_kv) {
       if (len + 1 <= g.max_context) N = len + 1;
@@ -209,11 +218,17 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   // ======================= 1. top-k, ascending =======================
   if (N <= K) {
     for (int i = tid; i < N; i += RES_THREADS) sel[i] = i;
+    if (tid == 0) p.s.cand_thr[rl] = 0u;
   } else {
     const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
     reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);   // ready for the next call
+    // the digit of the k-th largest key, and the digit above which ~1.25 k keys lie:
+    // the next call lists keys from there on (exact whenever >= k of them clear it)
+    const int k_next = (int)min((long long)N, (long long)K + K / 4);
     select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
+    select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
     const int b1 = sh.b1, above1 = sh.above1;
+    if (tid == 0) p.s.cand_thr[rl] = (uint32_t)sh.bt << 12;
     reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     HS_TRACE(p, 1, 2);
@@ -226,11 +241,30 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     const int NC = (N + 127) >> 7;
     const int c0 = (int)((long long)wid * NC / RES_WARPS), c1 = (int)((long long)(wid + 1) * NC / RES_WARPS);
     uint32_t* wl = lists + wid * WCAP;
-    const bool fast = L.fast && N <= FAST_MAX_N;
+    const int cap = 2 * K;
+    const bool use_cand = L.fast && N <= FAST_MAX_N && sh.thr != 0u && sh.cnt >= K && sh.cnt <= cap;
+    const bool fast = !use_cand && L.fast && N <= FAST_MAX_N;
     int wcnt = 0;       // entries of this warp's list (warp-uniform)
     int lane_gt = 0;    // keys above digit b1 seen by this lane
     bool overflow = false;
-    if (fast) {
+    const uint2* cl = p.s.cand + (long long)ri * cap;   // this call's candidates
+    uint32_t* tiebm = lists;                            // the candidate path's second bitmap
+    const int NW = (N + 31) >> 5;
+    if (use_cand) {
+      // every key >= the threshold is listed and at least k are: the k largest
+      // (ties included) are all in the list.  Second digit from the list only.
+      for (int q = tid; q < NW; q += RES_THREADS) {
+        bitmap[q] = 0u;
+        tiebm[q] = 0u;
+      }
+      const int32_t* page_rl = p.s.page + rl * g.max_context;
+      for (int i = tid; i < sh.cnt; i += RES_THREADS) {
+        const uint2 c = __ldcg(&cl[i]);
+        if ((int)(c.y >> 12) == b1) atomicAdd(&h[c.y & 4095u], 1u);
+        // every selected position is a candidate: warm its page-table entry for the hit test
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(page_rl + c.x));
+      }
+    } else if (fast) {
       const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
       constexpr int UC = 8;   // chunks in flight per lane (a 32K-position row in one round)
       for (int cb = c0; cb < c1; cb += UC) {
@@ -306,14 +340,77 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
         if ((int)(v >> 12) == b1) atomicAdd(&h[v & 4095u], 1u);
       }
     }
-    const bool use_lists = fast && !__syncthreads_or(overflow);
+    // the barrier is taken on every path (it orders the histogram atomics above
+    // before the digit select below), then decides whether the lists are usable
+    const bool any_overflow = __syncthreads_or(overflow);
+    const bool use_lists = fast && !any_overflow;
     HS_TRACE(p, 1, 3);
     select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
     HS_TRACE(p, 1, 4);
     const int b2 = sh.b2;
     const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)b2;
     const int need_eq = K - (above1 + sh.above2);   // >= 1
-    if (use_lists) {
+    if (use_cand) {
+      // mark the taken keys (> threshold) and the threshold ties in two bitmaps
+      for (int i = tid; i < sh.cnt; i += RES_THREADS) {
+        const uint2 c = __ldcg(&cl[i]);
+        if (c.y > vstar) atomicOr(&bitmap[c.x >> 5], 1u << (c.x & 31));
+        else if (c.y == vstar) atomicOr(&tiebm[c.x >> 5], 1u << (c.x & 31));
+      }
+      __syncthreads();
+      // per-warp word ranges, counts, scan over the warps
+      const int q0w = (int)((long long)wid * NW / RES_WARPS), q1w = (int)((long long)(wid + 1) * NW / RES_WARPS);
+      int n_gt = 0, n_eq = 0;
+      for (int q = q0w + lane; q < q1w; q += 32) {
+        n_gt += __popc(bitmap[q]);
+        n_eq += __popc(tiebm[q]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        n_gt += __shfl_xor_sync(FULL_MASK, n_gt, o);
+        n_eq += __shfl_xor_sync(FULL_MASK, n_eq, o);
+      }
+      const int2 wb = block_exclusive_scan2<RES_THREADS>(lane == 0 ? n_gt : 0, lane == 0 ? n_eq : 0, sh.scan,
+                                                         nullptr, nullptr);
+      const int gt_before = __shfl_sync(FULL_MASK, wb.x, 0), eq_before = __shfl_sync(FULL_MASK, wb.y, 0);
+      HS_TRACE(p, 1, 5);
+      int out = gt_before + min(eq_before, need_eq);
+      int tie_run = eq_before;   // threshold ties before this group of words
+      for (int qg = q0w; qg < q1w; qg += 32) {
+        const int q = qg + lane;
+        uint32_t m = q < q1w ? bitmap[q] : 0u;
+        uint32_t tb = q < q1w ? tiebm[q] : 0u;
+        const int nt = __popc(tb);
+        int tincl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(FULL_MASK, tincl, o);
+          if (lane >= o) tincl += n;
+        }
+        int rank = tie_run + tincl - nt;   // ties take the lowest positions first
+        while (tb) {
+          const int bb = __ffs(tb) - 1;
+          tb &= tb - 1;
+          if (rank < need_eq) m |= 1u << bb;
+          ++rank;
+        }
+        tie_run += __shfl_sync(FULL_MASK, tincl, 31);
+        const int cnt = __popc(m);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += n;
+        }
+        int o = out + incl - cnt;
+        while (m) {
+          const int bb = __ffs(m) - 1;
+          m &= m - 1;
+          if (o < K) sel[o++] = 32 * q + bb;
+        }
+        out += __shfl_sync(FULL_MASK, incl, 31);
+      }
+    } else if (use_lists) {
       // per-warp counts, then a scan over the warps
       int n_gt = lane_gt, n_eq = 0;
       for (int q = lane; q < wcnt; q += 32) {
@@ -432,12 +529,14 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
           if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
           slot_sel[i] = s4[u];
           if (s4[u] >= 0 && s4[u] < B) used[s4[u]] = 1;
-          // a miss the attention kernel will read from host memory: start moving
-          // it over the host link into L2 now (the appended row is written below)
-          if (s4[u] < 0 && p.fetch_mode == 0 && pos[u] >= 0 && pos[u] < N && !(appended && pos[u] == len))
-            bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(p.s.host_kv) +
-                                 ((size_t)rl * g.max_context + pos[u]) * g.row_bytes,
-                             (uint32_t)g.row_bytes);
+          // a miss: start moving its host row over the link into L2 now, line by
+          // line (the pull below, or the attention kernel in fetch mode 0, then
+          // reads it from L2); the row appended by this call is written below
+          if (s4[u] < 0 && pos[u] >= 0 && pos[u] < N && !(appended && pos[u] == len)) {
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(p.s.host_kv) +
+                                       ((size_t)rl * g.max_context + pos[u]) * g.row_bytes;
+            for (int b = 0; b < g.row_bytes; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
+          }
         }
       }
     }
@@ -486,7 +585,12 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     HS_TRACE(p, 1, 9);
     // slot of every selected position (misses flagged for the attention kernel
     // when it does the fetch); stamp every used slot
-    const int miss_flag = p.fetch_mode == 0 ? HS_SLOT_MISS_FLAG : 0;
+    // who copies the missed rows: fetch mode 1 (or 2 with many misses per
+    // attention CTA) = this kernel below, else the attention kernel, which
+    // overlaps a few rows per CTA with its HBM reads but stalls on many
+    const bool pull = p.fetch_mode == 1 ||
+                      (p.fetch_mode == 2 && (long long)m * p.n_req > (long long)AUTO_PULL_ROWS_PER_CTA * p.att_grid);
+    const int miss_flag = pull ? 0 : HS_SLOT_MISS_FLAG;
     int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
     for (int i = tid; i < kk; i += RES_THREADS) {
       const int sl = slot_sel[i];
@@ -538,13 +642,14 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   }
 
   // ======================= 3. host fetch (fetch_mode 1) =======================
-  if (p.fetch_mode == 1 && m > 0) {
+  if (m > 0 && (p.fetch_mode == 1 ||
+                (p.fetch_mode == 2 && (long long)m * p.n_req > (long long)AUTO_PULL_ROWS_PER_CTA * p.att_grid))) {
     const int rvec = g.row_bytes / 16;
     const long long total = (long long)m * rvec;
     const unsigned char* src_base =
         reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
     unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * B * g.row_bytes;
-    constexpr int U = 4;
+    constexpr int U = 8;   // 128 KB of host reads in flight per CTA
     for (long long e0 = tid; e0 < total; e0 += (long long)U * RES_THREADS) {
       int4 v[U];
 #pragma unroll

@@ -26,6 +26,10 @@
 //  * key = score + 2^22 (|score| <= 128*128*256 = 2^22) is stored to a per-call
 //    scratch row; the high-digit histogram is kept in shared memory per request
 //    segment and added to the request's global histogram when the segment ends.
+//  * Keys at or above the request's candidate threshold (set by the previous
+//    call's top-k) are also appended, with their positions, to a short
+//    per-request list (warp-aggregated atomics), which lets the top-k skip the
+//    full scan when the selection moved little since the previous step.
 //  * Launched as a programmatic dependent: barrier and histogram set-up overlap
 //    the previous kernel's tail.
 #include "hs_internal.cuh"
@@ -39,8 +43,10 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 constexpr int SC_MAX_STAGES = 6;
 constexpr size_t SC_SMEM_LIMIT = 227 * 1024;
 
+constexpr int SC_CBUF = 1024;   // candidates buffered per CTA before a flush to the request's list
+
 struct ScoreLayout {
-  size_t bar, pprefix, req, len, hist, stage, total;
+  size_t bar, pprefix, req, len, thr, hist, cbuf, stage, total;
   int nstage;
 };
 
@@ -55,8 +61,12 @@ __host__ __device__ inline ScoreLayout score_layout(const Geometry& g) {
   off += align_up((size_t)g.max_requests * 4, 128);
   L.len = off;       // int [n]: positions of request i this call (with the appended token)
   off += align_up((size_t)g.max_requests * 4, 128);
+  L.thr = off;       // u32 [n]: candidate threshold of request i (0: list nothing)
+  off += align_up((size_t)g.max_requests * 4, 128);
   L.hist = off;
   off += IDX_BINS * 4;
+  L.cbuf = off;     // uint2 [SC_CBUF]: (position, key) listed since the last flush
+  off += (size_t)SC_CBUF * 8;
   L.stage = off;
   // as many 32 KB stages as fit (at least two): with one stage being scored,
   // the others keep >= 128 KB of copies in flight per SM
@@ -87,6 +97,9 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
   long long* pprefix = reinterpret_cast<long long*>(smem_raw + L.pprefix);
   int* req_s = reinterpret_cast<int*>(smem_raw + L.req);
   int* len_s = reinterpret_cast<int*>(smem_raw + L.len);
+  uint32_t* thr_s = reinterpret_cast<uint32_t*>(smem_raw + L.thr);
+  uint2* cbuf = reinterpret_cast<uint2*>(smem_raw + L.cbuf);
+  __shared__ int cb_n, cb_base;
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
   unsigned char* stage = smem_raw + L.stage;
   __shared__ long long scan_tmp[SC_THREADS / 32 + 1];
@@ -95,6 +108,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
 
   for (int b = tid; b < IDX_BINS; b += SC_THREADS) hist[b] = 0;
   if (tid == 0) {
+    cb_n = 0;
     for (int s = 0; s < NST; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
   }
@@ -116,6 +130,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
       npos = N > K ? N : 0;
       req_s[i] = npos ? req : -1;
       len_s[i] = N;
+      thr_s[i] = (npos && p.s.cand_thr) ? p.s.cand_thr[(long long)req * g.n_layers + p.layer] : 0u;
     }
     // block-wide exclusive scan of 64-bit counts
     long long incl = npos;
@@ -235,25 +250,58 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     HS_TRACE_IF(p, 0, 2, tid == 0 && k == 0);
     const unsigned char* tile = stage + (size_t)s * IDX_TILE_BYTES;
     uint32_t* keys_out = p.s.scores + (long long)tr.r * p.score_stride + tr.pos0;
-    for (int j = tid; j < tr.npos; j += SC_THREADS) {
-      const unsigned char* rowp = j == jnew ? new_key : tile + j * d;
-      int acc = 0;
+    const uint32_t thr = thr_s[tr.r];   // block-uniform
+    for (int j0 = 0; j0 < tr.npos; j0 += SC_THREADS) {
+      const int j = j0 + tid;
+      uint32_t key = 0;
+      if (j < tr.npos) {
+        const unsigned char* rowp = j == jnew ? new_key : tile + j * d;
+        int acc = 0;
 #pragma unroll
-      for (int cc = 0; cc < NCH; ++cc) {
-        const int4 kv = *reinterpret_cast<const int4*>(rowp + (((cc + rot) & (NCH - 1)) << 4));
-        acc = __dp4a(kv.x, qrot[cc].x, acc);
-        acc = __dp4a(kv.y, qrot[cc].y, acc);
-        acc = __dp4a(kv.z, qrot[cc].z, acc);
-        acc = __dp4a(kv.w, qrot[cc].w, acc);
+        for (int cc = 0; cc < NCH; ++cc) {
+          const int4 kv = *reinterpret_cast<const int4*>(rowp + (((cc + rot) & (NCH - 1)) << 4));
+          acc = __dp4a(kv.x, qrot[cc].x, acc);
+          acc = __dp4a(kv.y, qrot[cc].y, acc);
+          acc = __dp4a(kv.z, qrot[cc].z, acc);
+          acc = __dp4a(kv.w, qrot[cc].w, acc);
+        }
+        key = (uint32_t)(acc + IDX_KEY_BIAS);
+        keys_out[j] = key;
+        atomicAdd(&hist[key >> 12], 1u);
       }
-      const uint32_t key = (uint32_t)(acc + IDX_KEY_BIAS);
-      keys_out[j] = key;
-      atomicAdd(&hist[key >> 12], 1u);
+      if (thr != 0u) {   // buffer the keys at or above the threshold (warp-aggregated)
+        const bool c = j < tr.npos && key >= thr;
+        const unsigned m = __ballot_sync(FULL_MASK, c);
+        if (m) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&cb_n, __popc(m));
+          base = __shfl_sync(FULL_MASK, base, 0);
+          const int at = base + __popc(m & ((1u << lane) - 1u));
+          const uint2 v = make_uint2((uint32_t)(tr.pos0 + j), key);
+          if (c && at < SC_CBUF) {
+            cbuf[at] = v;
+          } else if (c) {   // buffer full within this tile (narrow keys): straight to the list
+            const unsigned g2 = atomicAdd(p.s.cand_cnt + tr.r, 1u);
+            if (g2 < 2u * (unsigned)K) p.s.cand[(long long)tr.r * 2 * K + g2] = v;
+          }
+        }
+      }
     }
-    __syncthreads();   // stage s consumed; histogram updates of this tile done
+    __syncthreads();   // stage s consumed; histogram updates and listed keys of this tile done
     if (tid == 0 && k + NST < ntile) issue(k + NST);
     // end of this request's segment: add the histogram to the request's one
     const bool seg_end = (k + 1 == ntile) || (pprefix[tr.r + 1] <= cu.a);
+    if (thr != 0u && (seg_end || cb_n + TP > SC_CBUF)) {   // flush the listed keys (one global atomic)
+      const int n = min(cb_n, SC_CBUF);
+      if (tid == 0) cb_base = n ? (int)atomicAdd(p.s.cand_cnt + tr.r, (unsigned)n) : 0;
+      __syncthreads();
+      const int base = cb_base;
+      uint2* dst = p.s.cand + (long long)tr.r * 2 * K;
+      for (int i = tid; i < n; i += SC_THREADS)
+        if (base + i < 2 * K) dst[base + i] = cbuf[i];
+      __syncthreads();
+      if (tid == 0) cb_n = 0;
+    }
     if (seg_end) {
       uint32_t* gh = p.s.hist + (long long)tr.r * IDX_BINS;
       for (int b = tid; b < IDX_BINS; b += SC_THREADS) {

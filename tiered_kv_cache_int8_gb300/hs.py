@@ -141,7 +141,7 @@ class HiSparseCache:
 
     def __init__(self, *, n_layers: int, max_requests: int, max_context: int, h_q: int, h_kv: int,
                  d_qk: int, d_v: int, d_idx: int, top_k: int, hot_slots: int, shared_kv: bool = False,
-                 softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 0):
+                 softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 2):
         self.cfg = HsConfig(n_layers, max_requests, max_context, h_q, h_kv, d_qk, d_v, int(shared_kv),
                             d_idx, top_k, hot_slots, softmax_scale, device, fetch_mode)
         self._h = ctypes.c_void_p()
