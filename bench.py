@@ -87,16 +87,19 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
 
     def start(self):
+        if self.interval_ms <= 0:
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
@@ -110,7 +113,8 @@ class ClockSampler:
         """Summary of the samples taken inside window = (t0, t1) (wall time), or of
         all samples when none fell inside it."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            why = "not sampled (--clock-interval-ms 0)" if self.interval_ms <= 0 else "nvidia-smi unavailable"
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [why]}
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -338,7 +342,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
 
     # ---- timed region A: the K steps as one CUDA graph (the headline value) ----------
     graph = capture(W, W + K)
-    clocks = ClockSampler(dev_index)
+    clocks = ClockSampler(dev_index, args.clock_interval_ms)
     clocks.start()
     time.sleep(0.5)   # the sampler's start-up (NVML initialisation) stays out of the timed region
     t_wall0 = time.time()
@@ -502,6 +506,8 @@ def main():
                     help="who copies missed rows: 0 the attention kernel (overlapped), 1 RESOLVE, "
                          "2 chosen per request (default)")
     ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
+    ap.add_argument("--clock-interval-ms", type=int, default=50,
+                    help="nvidia-smi clock sampling period during the timed region (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
