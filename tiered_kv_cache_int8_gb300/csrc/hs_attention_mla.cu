@@ -347,17 +347,26 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
       // ---- S = Q K^T for rows 8*warp .. 8*warp + 7 ----
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       {
+        // four independent accumulators over the 36 k-steps (a chain of 9 instead
+        // of 36 dependent mma), summed in a fixed order
+        float acc[4][4] = {};
         const uint32_t rowa = smem_addr(st_s + (size_t)(8 * warp + (lane & 7)) * MLA_ROW_STRIDE) + 16 * (lane >> 3);
         const uint32_t qa = smem_addr(qs + (size_t)lrow * MLA_ROW_STRIDE) + 2 * lcol;
-#pragma unroll 6
-        for (int kp = 0; kp < MLA_DK / 32; ++kp) {
-          uint32_t b[4], a0[4], a1[4];
-          ldsm4(b, rowa + 64 * kp);          // K rows x dims 32kp .. 32kp+31
-          ldsm4(a0, qa + 64 * kp);           // Q dims 32kp .. +15
-          ldsm4(a1, qa + 64 * kp + 32);      // Q dims 32kp+16 .. +31
-          mma16816(sc, a0, b[0], b[1]);
-          mma16816(sc, a1, b[2], b[3]);
+#pragma unroll
+        for (int kp2 = 0; kp2 < MLA_DK / 64; ++kp2) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int kp = 2 * kp2 + h2;
+            uint32_t b[4], a0[4], a1[4];
+            ldsm4(b, rowa + 64 * kp);          // K rows x dims 32kp .. 32kp+31
+            ldsm4(a0, qa + 64 * kp);           // Q dims 32kp .. +15
+            ldsm4(a1, qa + 64 * kp + 32);      // Q dims 32kp+16 .. +31
+            mma16816(acc[2 * h2], a0, b[0], b[1]);
+            mma16816(acc[2 * h2 + 1], a1, b[2], b[3]);
+          }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
       }
       // ---- tile maxima per head ----
       float mx_lo = -INFINITY, mx_hi = -INFINITY;
