@@ -303,6 +303,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.part_o, R * (size_t)h->att_parts * g.h_q * g.d_v * 4, false},
       {(void**)&s.part_ml, R * (size_t)h->att_parts * g.h_q * 2 * 4, false},
       {(void**)&s.att_nparts, R * 8 * 4, false},
+      {(void**)&s.call_n, R * 4, false},
       {(void**)&s.app_counter, R * 4, false},
 #ifdef HS_WITH_TRACE
       {(void**)&h->trace, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8, false},
@@ -331,6 +332,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.dev_error, 0, 16) == cudaSuccess;
   ok = ok && cudaMemset(s.slot_of_sel, 0, R * K * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.att_nparts, 0, R * 8 * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.call_n, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.hist, 0, R * (size_t)hs::IDX_BINS * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.cand_thr, 0, R * Lr * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.cand_cnt, 0, R * 4) == cudaSuccess;

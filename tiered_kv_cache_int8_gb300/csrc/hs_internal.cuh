@@ -69,6 +69,7 @@ struct DeviceState {
   float* part_o;           // [R][parts][h_q][d_v]
   float* part_ml;          // [R][parts][h_q][2]
   int32_t* att_nparts;     // [R][8] partial results of each (request, head group) of the current call
+  int32_t* call_n;         // [R] positions of request i in the current call (with its appended token)
   unsigned int* app_counter;   // [R]
 };
 

@@ -42,8 +42,10 @@
 //     kernel copies them from host memory into its stage (and from there into
 //     the slot) while the rest of the rows stream from HBM, so host-link time
 //     overlaps HBM time.  fetch_mode 2 chooses per request: this kernel pulls
-//     when the request's misses spread over the attention grid exceed a few rows
-//     per CTA.  All give identical results.  Either way every missed
+//     them all when the request's misses spread over the attention grid exceed a
+//     few rows per CTA; otherwise it pulls only those in each attention CTA's
+//     first units (needed at once) and leaves the rest, already moving into L2,
+//     to the attention kernel.  All give identical results.  Either way every missed
 //     row is prefetched into L2 (per 128-byte line) the moment its page lookup
 //     misses, so the link starts working before the copies are issued.
 //  4. the appended token: its index key to the HBM store, its K/V row to the
@@ -60,6 +62,8 @@ constexpr int FAST_MAX_N = 256 * 1024;   // one-pass top-k: contexts up to this 
 constexpr int RES_WARPS = RES_THREADS / 32;
 constexpr int WCAP = 256;                // digit-b1 keys a warp lists in the one-pass top-k
 constexpr int AUTO_PULL_ROWS_PER_CTA = 8;  // fetch mode 2: pull here above this many misses per attention CTA
+constexpr int FRONT_UNITS = 3;             // fetch mode 2: misses in an attention CTA's first units are pulled here
+constexpr int CAND_MAX_N_PER_K = 20;       // candidate listing only for contexts up to 20 k positions
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 struct ResLayout {
@@ -228,7 +232,9 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
     select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
     const int b1 = sh.b1, above1 = sh.above1;
-    if (tid == 0) p.s.cand_thr[rl] = (uint32_t)sh.bt << 12;
+    // listing costs the score kernel about as much per position as the full pass
+    // costs here, so it pays only while the context is short relative to k
+    if (tid == 0) p.s.cand_thr[rl] = N <= CAND_MAX_N_PER_K * K ? (uint32_t)sh.bt << 12 : 0u;
     reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     HS_TRACE(p, 1, 2);
@@ -510,6 +516,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   int32_t* order = p.s.order + rl * B;
   const int t = t_step;
   int m = 0;
+  bool pull = false, front_pull = false;   // who copies this request's missed rows (see below)
   if (kk > 0) {
     // hit test: independent page-table gathers, four in flight per thread
     bool bad = false;
@@ -588,8 +595,36 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     // who copies the missed rows: fetch mode 1 (or 2 with many misses per
     // attention CTA) = this kernel below, else the attention kernel, which
     // overlaps a few rows per CTA with its HBM reads but stalls on many
-    const bool pull = p.fetch_mode == 1 ||
-                      (p.fetch_mode == 2 && (long long)m * p.n_req > (long long)AUTO_PULL_ROWS_PER_CTA * p.att_grid);
+    pull = p.fetch_mode == 1 ||
+           (p.fetch_mode == 2 && (long long)m * p.n_req > (long long)AUTO_PULL_ROWS_PER_CTA * p.att_grid);
+    // fetch mode 2 with few misses: the attention kernel copies them, except those
+    // in the first FRONT_UNITS units of each attention CTA (needed before any
+    // prefetch could land), which are pulled here.  The attention kernel splits
+    // the flattened units of all requests into equal ranges over min(grid, U)
+    // CTAs; the same split is recomputed from every request's k_eff.
+    front_pull = p.fetch_mode == 2 && !pull && !g.shared_kv && p.s.call_n != nullptr;
+    if (front_pull) {
+      const int tile = ATT_SUBTILE * (8 / g.h_kv);
+      int before = 0, all = 0;
+      for (int j = tid; j < p.n_req; j += RES_THREADS) {
+        const int u = (min(K, p.s.call_n[j]) + tile - 1) / tile;
+        all += u;
+        if (j < ri) before += u;
+      }
+      int t_before, t_all;
+      (void)block_exclusive_scan2<RES_THREADS>(before, all, sh.scan, &t_before, &t_all);
+      const long long U = t_all;
+      const int Gc = (int)max(1LL, min((long long)p.att_grid, U));
+      for (int q = tid; q < m; q += RES_THREADS) {
+        const long long u = t_before + miss_i[q] / tile;
+        const long long c = ((u + 1) * Gc + U - 1) / U - 1;   // owning attention CTA
+        const bool front = u - c * U / Gc < FRONT_UNITS;
+        miss_i[q] = front ? (miss_i[q] | HS_SLOT_MISS_FLAG) : miss_i[q];   // mark: pulled here
+      }
+      __syncthreads();
+    }
+    auto pulled = [&](int q) { return pull || (front_pull && (miss_i[q] & HS_SLOT_MISS_FLAG)); };
+    auto miss_sel = [&](int q) { return miss_i[q] & ~HS_SLOT_MISS_FLAG; };
     const int miss_flag = pull ? 0 : HS_SLOT_MISS_FLAG;
     int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
     for (int i = tid; i < kk; i += RES_THREADS) {
@@ -600,7 +635,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     HS_TRACE(p, 1, 22);
     __syncthreads();
     HS_TRACE(p, 1, 23);
-    for (int q = tid; q < m; q += RES_THREADS) sos[miss_i[q]] = victim[q] | miss_flag;
+    for (int q = tid; q < m; q += RES_THREADS) sos[miss_sel(q)] = victim[q] | (pulled(q) ? 0 : miss_flag);
     // new LRU list: unused slots keep their order, used slots go last by slot
     int nu = 0, nus = 0;
     for (int j = j0; j < j1; ++j) nu += used[ord[j]] == 0;
@@ -642,8 +677,7 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
   }
 
   // ======================= 3. host fetch (fetch_mode 1) =======================
-  if (m > 0 && (p.fetch_mode == 1 ||
-                (p.fetch_mode == 2 && (long long)m * p.n_req > (long long)AUTO_PULL_ROWS_PER_CTA * p.att_grid))) {
+  if (m > 0 && (pull || front_pull)) {
     const int rvec = g.row_bytes / 16;
     const long long total = (long long)m * rvec;
     const unsigned char* src_base =
@@ -655,9 +689,10 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const long long e = e0 + (long long)u * RES_THREADS;
-        if (e < total) {
-          const int q = (int)(e / rvec), cidx = (int)(e - (long long)q * rvec);
-          const int pos = sel[miss_i[q]];
+        const int q = e < total ? (int)(e / rvec) : 0;
+        if (e < total && (pull || (miss_i[q] & HS_SLOT_MISS_FLAG))) {
+          const int cidx = (int)(e - (long long)q * rvec);
+          const int pos = sel[miss_i[q] & ~HS_SLOT_MISS_FLAG];
           // the token appended by this call is read from its input copy
           v[u] = (appended && pos == len) ? reinterpret_cast<const int4*>(newrow)[cidx]
                                           : *reinterpret_cast<const int4*>(src_base + (size_t)pos * g.row_bytes + cidx * 16);
@@ -666,8 +701,9 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const long long e = e0 + (long long)u * RES_THREADS;
-        if (e < total) {
-          const int q = (int)(e / rvec), cidx = (int)(e - (long long)q * rvec);
+        const int q = e < total ? (int)(e / rvec) : 0;
+        if (e < total && (pull || (miss_i[q] & HS_SLOT_MISS_FLAG))) {
+          const int cidx = (int)(e - (long long)q * rvec);
           *reinterpret_cast<int4*>(dst_base + (size_t)victim[q] * g.row_bytes + cidx * 16) = v[u];
         }
       }

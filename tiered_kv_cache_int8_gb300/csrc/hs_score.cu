@@ -44,6 +44,7 @@ constexpr int SC_MAX_STAGES = 6;
 constexpr size_t SC_SMEM_LIMIT = 227 * 1024;
 
 constexpr int SC_CBUF = 1024;   // candidates buffered per CTA before a flush to the request's list
+constexpr int SC_WBUF = SC_CBUF / (SC_THREADS / 32);   // per warp
 
 struct ScoreLayout {
   size_t bar, pprefix, req, len, thr, hist, cbuf, stage, total;
@@ -99,7 +100,10 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
   int* len_s = reinterpret_cast<int*>(smem_raw + L.len);
   uint32_t* thr_s = reinterpret_cast<uint32_t*>(smem_raw + L.thr);
   uint2* cbuf = reinterpret_cast<uint2*>(smem_raw + L.cbuf);
-  __shared__ int cb_n, cb_base;
+  __shared__ int cb_wn[SC_THREADS / 32], cb_base;
+  const int warp = tid >> 5;
+  uint2* wbuf = cbuf + warp * SC_WBUF;   // this warp's part of the buffer
+  int wn = 0;                            // entries in it (warp-uniform)
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
   unsigned char* stage = smem_raw + L.stage;
   __shared__ long long scan_tmp[SC_THREADS / 32 + 1];
@@ -108,7 +112,6 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
 
   for (int b = tid; b < IDX_BINS; b += SC_THREADS) hist[b] = 0;
   if (tid == 0) {
-    cb_n = 0;
     for (int s = 0; s < NST; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
   }
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
       req_s[i] = npos ? req : -1;
       len_s[i] = N;
       thr_s[i] = (npos && p.s.cand_thr) ? p.s.cand_thr[(long long)req * g.n_layers + p.layer] : 0u;
+      if (c == 0 && p.s.call_n) p.s.call_n[i] = N;   // for RESOLVE's view of the attention split
     }
     // block-wide exclusive scan of 64-bit counts
     long long incl = npos;
@@ -251,56 +255,76 @@ __global__ void __launch_bounds__(SC_THREADS) score_kernel(DecodeParams p) {
     const unsigned char* tile = stage + (size_t)s * IDX_TILE_BYTES;
     uint32_t* keys_out = p.s.scores + (long long)tr.r * p.score_stride + tr.pos0;
     const uint32_t thr = thr_s[tr.r];   // block-uniform
-    for (int j0 = 0; j0 < tr.npos; j0 += SC_THREADS) {
-      const int j = j0 + tid;
-      uint32_t key = 0;
-      if (j < tr.npos) {
-        const unsigned char* rowp = j == jnew ? new_key : tile + j * d;
-        int acc = 0;
+    // one position per thread and pass: dp4a over the 16-byte chunks in the
+    // lane's rotated order; key = score + 2^22
+    auto score_at = [&](int j) -> uint32_t {
+      const unsigned char* rowp = j == jnew ? new_key : tile + j * d;
+      int acc = 0;
 #pragma unroll
-        for (int cc = 0; cc < NCH; ++cc) {
-          const int4 kv = *reinterpret_cast<const int4*>(rowp + (((cc + rot) & (NCH - 1)) << 4));
-          acc = __dp4a(kv.x, qrot[cc].x, acc);
-          acc = __dp4a(kv.y, qrot[cc].y, acc);
-          acc = __dp4a(kv.z, qrot[cc].z, acc);
-          acc = __dp4a(kv.w, qrot[cc].w, acc);
-        }
-        key = (uint32_t)(acc + IDX_KEY_BIAS);
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int4 kv = *reinterpret_cast<const int4*>(rowp + (((cc + rot) & (NCH - 1)) << 4));
+        acc = __dp4a(kv.x, qrot[cc].x, acc);
+        acc = __dp4a(kv.y, qrot[cc].y, acc);
+        acc = __dp4a(kv.z, qrot[cc].z, acc);
+        acc = __dp4a(kv.w, qrot[cc].w, acc);
+      }
+      return (uint32_t)(acc + IDX_KEY_BIAS);
+    };
+    if (thr == 0u) {   // no listing for this request (kept as a separate, lean loop)
+      for (int j = tid; j < tr.npos; j += SC_THREADS) {
+        const uint32_t key = score_at(j);
         keys_out[j] = key;
         atomicAdd(&hist[key >> 12], 1u);
       }
-      if (thr != 0u) {   // buffer the keys at or above the threshold (warp-aggregated)
+    } else {
+      for (int j0 = 0; j0 < tr.npos; j0 += SC_THREADS) {
+        const int j = j0 + tid;
+        uint32_t key = 0;
+        if (j < tr.npos) {
+          key = score_at(j);
+          keys_out[j] = key;
+          atomicAdd(&hist[key >> 12], 1u);
+        }
+        // buffer the keys at or above the threshold (per warp, no atomics)
         const bool c = j < tr.npos && key >= thr;
         const unsigned m = __ballot_sync(FULL_MASK, c);
         if (m) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&cb_n, __popc(m));
-          base = __shfl_sync(FULL_MASK, base, 0);
-          const int at = base + __popc(m & ((1u << lane) - 1u));
+          const int at = wn + __popc(m & ((1u << lane) - 1u));
           const uint2 v = make_uint2((uint32_t)(tr.pos0 + j), key);
-          if (c && at < SC_CBUF) {
-            cbuf[at] = v;
-          } else if (c) {   // buffer full within this tile (narrow keys): straight to the list
+          if (wn + __popc(m) <= SC_WBUF) {
+            if (c) wbuf[at] = v;
+            wn += __popc(m);
+          } else if (c) {   // this warp's part is full (narrow keys): straight to the list
             const unsigned g2 = atomicAdd(p.s.cand_cnt + tr.r, 1u);
             if (g2 < 2u * (unsigned)K) p.s.cand[(long long)tr.r * 2 * K + g2] = v;
           }
         }
       }
     }
-    __syncthreads();   // stage s consumed; histogram updates and listed keys of this tile done
+    // stage s consumed; histogram updates of this tile done; is any warp's buffer
+    // too full for another tile?
+    bool near_full = false;
+    if (thr == 0u) __syncthreads();
+    else near_full = __syncthreads_or(wn + 32 * ((TP + SC_THREADS - 1) / SC_THREADS) > SC_WBUF);
     if (tid == 0 && k + NST < ntile) issue(k + NST);
     // end of this request's segment: add the histogram to the request's one
     const bool seg_end = (k + 1 == ntile) || (pprefix[tr.r + 1] <= cu.a);
-    if (thr != 0u && (seg_end || cb_n + TP > SC_CBUF)) {   // flush the listed keys (one global atomic)
-      const int n = min(cb_n, SC_CBUF);
-      if (tid == 0) cb_base = n ? (int)atomicAdd(p.s.cand_cnt + tr.r, (unsigned)n) : 0;
+    if (thr != 0u && (seg_end || near_full)) {   // flush the listed keys (one global atomic)
+      if (lane == 0) cb_wn[warp] = wn;
       __syncthreads();
-      const int base = cb_base;
+      if (tid == 0) {
+        int n = 0;
+        for (int w2 = 0; w2 < SC_THREADS / 32; ++w2) n += cb_wn[w2];
+        cb_base = n ? (int)atomicAdd(p.s.cand_cnt + tr.r, (unsigned)n) : 0;
+      }
+      __syncthreads();
+      int off = cb_base;
+      for (int w2 = 0; w2 < warp; ++w2) off += cb_wn[w2];
       uint2* dst = p.s.cand + (long long)tr.r * 2 * K;
-      for (int i = tid; i < n; i += SC_THREADS)
-        if (base + i < 2 * K) dst[base + i] = cbuf[i];
-      __syncthreads();
-      if (tid == 0) cb_n = 0;
+      for (int i = lane; i < wn; i += 32)
+        if (off + i < 2 * K) dst[off + i] = wbuf[i];
+      wn = 0;
+      __syncthreads();   // cb_wn and the buffer are reused
     }
     if (seg_end) {
       uint32_t* gh = p.s.hist + (long long)tr.r * IDX_BINS;
