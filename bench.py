@@ -151,16 +151,18 @@ KERNEL_FILES = {"append": "hs_append.cu", "indexer": "hs_score.cu",
                 "topk_resolve": "hs_resolve.cu", "attention": "hs_attention.cu"}
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, workload: str, latent: bool = False):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    this kernel source and workload (else None)."""
+    this kernel source and workload (else None).  Latent-row attention lives in
+    its own source file."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_sha") != kernel_source_hash(KERNEL_FILES[kernel]):
+    src = "hs_attention_mla.cu" if (latent and kernel == "attention") else KERNEL_FILES[kernel]
+    if not e or e.get("source_sha") != kernel_source_hash(src):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -453,7 +455,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         ach = kernels[dom]["hbm_gbs"]
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
                 "frac": round(ach / peak_hbm, 4), "peak_source": peak_src,
-                "traffic": ncu_traffic(dom, w.name), "bytes_per_launch": kernels[dom]["hbm_bytes_per_launch"]}
+                "traffic": ncu_traffic(dom, w.name, w.shared_kv), "bytes_per_launch": kernels[dom]["hbm_bytes_per_launch"]}
     # the attention entry also launches the partial-merge kernel
     gpu_launches = sum(v["launches"] for v in kernels.values()) + kernels.get("attention", {}).get("launches", 0)
     out = {

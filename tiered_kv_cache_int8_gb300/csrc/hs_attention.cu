@@ -716,12 +716,12 @@ static cudaError_t run_merge(const DecodeParams* p, cudaStream_t st) {
 
 // p == nullptr: set-up only
 static cudaError_t dispatch_merge(const Geometry& g, const DecodeParams* p, cudaStream_t st) {
-  if (g.shared_kv) {
+  if (g.shared_kv) {   // part counts per item head group: 16 heads at h_q = 16, else 32
     switch (g.h_q) {
       case 16: return run_merge<16, 512, 16>(p, st);
-      case 32: return run_merge<32, 512, 16>(p, st);
-      case 64: return run_merge<64, 512, 16>(p, st);
-      case 128: return run_merge<128, 512, 16>(p, st);
+      case 32: return run_merge<32, 512, 32>(p, st);
+      case 64: return run_merge<64, 512, 32>(p, st);
+      case 128: return run_merge<128, 512, 32>(p, st);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -11,22 +11,23 @@
 // Design (sm_103a).  With 128 heads sharing each 1152-byte row the kernel does
 // ~240 flop per byte, so the products run on the tensor cores (mma.sync
 // m16n8k16, bf16 in, fp32 accumulate):
-//  * Work items are (request, group of 16 heads, unit of 64 selected rows),
-//    flattened in that order and split into equal contiguous ranges, one per
-//    CTA (persistent, one CTA per SM).  The split depends only on k_eff and the
-//    grid, never on B.  Rows are read once per head group; the groups of one
-//    request run close together in time, so the repeats hit L2.
-//  * Warp 8 (stager) copies the unit's 64 rows from their hot slots into shared
-//    memory with 1-D bulk async copies (cp.async.bulk, mbarrier completion), two
-//    or three stages deep.  RESOLVE has already pulled every missed row into its
-//    slot (latent rows are shared by all head groups, so they cross the host
-//    link once).
-//  * Warps 0-7: S = Q K^T with warp w taking rows 8w..8w+7 (36 k-steps over the
-//    576 dims; Q of the head group sits in shared memory); the per-head maxima
-//    and sums of the 64 rows are exchanged through shared memory; P goes to
-//    shared memory as bf16; then warp w accumulates O[16 heads, dims 64w..64w+63]
-//    += P V (4 k-steps over the 64 rows, V fragments by ldmatrix.trans).  Online
-//    softmax in fp32 with exp2; rows past k_eff are masked and zero-filled.
+//  * Work items are (request, group of 16*NMT heads, unit of 64/NMT selected
+//    rows), flattened in that order and split into equal contiguous ranges, one
+//    per CTA (persistent, one CTA per SM).  The split depends only on k_eff and
+//    the grid, never on B.  With NMT = 2 (32 heads x 32 rows) an item moves half
+//    the bytes of a 64-row item for the same tensor work, so four stages fit in
+//    shared memory; rows are re-read once per head group, from L2.
+//  * Warp 8 (stager) copies an item's rows from their hot slots into shared
+//    memory with 1-D bulk async copies (cp.async.bulk, mbarrier completion).
+//    RESOLVE has already pulled every missed row into its slot (latent rows are
+//    shared by all head groups, so they cross the host link once).
+//  * Warps 0-7: S = Q K^T with warp w taking head tile w / (8/NMT) and row tile
+//    w % (8/NMT) (36 k-steps over the 576 dims in four independent accumulator
+//    chains; Q of the head group in shared memory); per-head maxima and sums of
+//    the item's rows are exchanged through shared memory; P goes to shared memory
+//    as bf16; then warp w accumulates O[all heads of the item, dims 64w..64w+63]
+//    += P V (V fragments by ldmatrix.trans).  Online softmax in fp32 with exp2;
+//    rows past k_eff are masked and zero-filled.
 //  * Each (CTA, request, head group) writes a partial (m, l, o); the merge kernel
 //    combines them in part order.
 #include <cuda_bf16.h>
@@ -38,15 +39,16 @@ namespace hs {
 namespace {
 
 constexpr int MLA_DK = 576, MLA_DV = 512;
-constexpr int MLA_HG = 16;                        // heads per group (the mma M)
-constexpr int MLA_TILE = 64;                      // rows per work item
 constexpr int MLA_NCONS = 8;                      // consumer warps
 constexpr int MLA_STAGER = MLA_NCONS;             // warp index of the stager
 constexpr int MLA_THREADS = (MLA_NCONS + 1) * 32;
 constexpr int MLA_ROW_STRIDE = MLA_DK * 2 + 16;   // shared-memory row pitch (bank spread for ldmatrix)
-constexpr int MLA_P_STRIDE = MLA_TILE * 2 + 16;
-constexpr int MLA_MAX_STAGES = 3;
+constexpr int MLA_MAX_STAGES = 4;
 constexpr size_t MLA_SMEM_LIMIT = 227 * 1024;
+
+// 16-head tiles per item: two (32 heads x 32 rows) when the heads allow it
+__host__ __device__ inline int mla_nmt(const Geometry& g) { return g.h_q >= 32 ? 2 : 1; }
+__host__ __device__ inline int mla_rows(const Geometry& g) { return 64 / mla_nmt(g); }
 
 __host__ __device__ inline size_t mla_align(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -56,6 +58,7 @@ struct MlaLayout {
 };
 
 __host__ __device__ inline MlaLayout mla_layout(const Geometry& g) {
+  const int nmt = mla_nmt(g), rows = mla_rows(g);
   MlaLayout L;
   size_t off = 0;
   L.bar = off;
@@ -63,17 +66,19 @@ __host__ __device__ inline MlaLayout mla_layout(const Geometry& g) {
   off = mla_align(off, 128);
   L.prefix = off;   // first item, k_eff and request id of each request
   off += mla_align((size_t)(g.max_requests + 1) * 4 * 3, 128);
-  L.q = off;
-  off += (size_t)MLA_HG * MLA_ROW_STRIDE;
-  L.p = off;
-  off += (size_t)MLA_HG * MLA_P_STRIDE;
-  L.red = off;   // per-warp head maxima (two buffers) and sums
-  off += (size_t)3 * MLA_NCONS * MLA_HG * 4;
+  L.q = off;        // Q of the item's heads
+  off += (size_t)16 * nmt * MLA_ROW_STRIDE;
+  L.p = off;        // P [heads][rows] bf16
+  off += (size_t)16 * nmt * (rows * 2 + 16);
+  L.red = off;      // per (head tile, row tile) head maxima (two buffers) and sums
+  off += (size_t)3 * 8 * 16 * 4;
   off = mla_align(off, 128);
   L.stage = off;
-  L.stage_bytes = (size_t)MLA_TILE * MLA_ROW_STRIDE;
-  L.nstage = off + 3 * L.stage_bytes <= MLA_SMEM_LIMIT ? 3 : 2;
-  off += (size_t)L.nstage * L.stage_bytes;
+  L.stage_bytes = (size_t)rows * MLA_ROW_STRIDE;
+  int ns = MLA_MAX_STAGES;
+  while (ns > 2 && off + ns * L.stage_bytes > MLA_SMEM_LIMIT) --ns;
+  L.nstage = ns;
+  off += (size_t)ns * L.stage_bytes;
   L.total = off;
   return L;
 }
@@ -143,12 +148,16 @@ __device__ __forceinline__ int owner(long long u, long long U, int G) {
 
 }  // namespace
 
-int mla_parts(const Geometry& g) { return (g.top_k + MLA_TILE - 1) / MLA_TILE + 1; }
+int mla_parts(const Geometry& g) { return (g.top_k + mla_rows(g) - 1) / mla_rows(g) + 1; }
 size_t mla_smem_bytes(const Geometry& g) { return mla_layout(g).total; }
 
-template <int HQ>
+template <int HQ, int NMT>
 __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p) {
-  constexpr int NHG = HQ / MLA_HG;
+  constexpr int GH = 16 * NMT;          // heads per item
+  constexpr int ROWS = 64 / NMT;        // rows per item
+  constexpr int NT = ROWS / 8;          // row tiles (mma N) per item
+  constexpr int NHG = HQ / GH;
+  constexpr int P_STRIDE = ROWS * 2 + 16;
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = g.top_k;
@@ -165,8 +174,8 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
   int* req_s = kk_s + (g.max_requests + 1);
   unsigned char* qs = smem_raw + L.q;
   unsigned char* ps = smem_raw + L.p;
-  float* smax = reinterpret_cast<float*>(smem_raw + L.red);   // [2][8][16]
-  float* ssum = smax + 2 * MLA_NCONS * MLA_HG;                // [8][16]
+  float* smax = reinterpret_cast<float*>(smem_raw + L.red);   // [2][8 blocks][16]
+  float* ssum = smax + 2 * 8 * 16;                            // [8 blocks][16]
   unsigned char* stage = smem_raw + L.stage;
   __shared__ int scan_tmp[MLA_THREADS / 32 + 1];
   HS_TRACE(p, 2, 0);
@@ -182,7 +191,7 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
   griddep_wait();   // selection, slots (rows pulled by RESOLVE), lengths, q
   griddep_launch_dependents();
 
-  // ---- work list: NHG * ceil(k_eff / 64) items per request ----
+  // ---- work list: NHG * ceil(k_eff / ROWS) items per request ----
   int carry = 0;
   for (int base = 0; base < p.n_req; base += MLA_THREADS) {
     const int i = base + tid;
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
       const int req = p.req_ids ? p.req_ids[i] : i;
       int kk = 0;
       if (req >= 0 && req < g.max_requests) kk = min(K, p.s.length[(long long)req * g.n_layers + p.layer]);
-      items = NHG * ((kk + MLA_TILE - 1) / MLA_TILE);
+      items = NHG * ((kk + ROWS - 1) / ROWS);
       kk_s[i] = kk;
       req_s[i] = req;
       if (kk == 0 && i % (int)gridDim.x == c) {   // nothing selected: the output is defined as 0
@@ -212,7 +221,7 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
   if (c == 0)   // partials of each (request, head group), for the merge kernel
     for (int e = tid; e < p.n_req * NHG; e += MLA_THREADS) {
       const int i = e / NHG, hg = e % NHG;
-      const int ui = (kk_s[i] + MLA_TILE - 1) / MLA_TILE;
+      const int ui = (kk_s[i] + ROWS - 1) / ROWS;
       const long long f0 = prefix[i] + (long long)hg * ui;
       p.s.att_nparts[(long long)i * NHG + hg] = ui ? owner(f0 + ui - 1, U, Gc) - owner(f0, U, Gc) + 1 : 0;
     }
@@ -236,11 +245,11 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
     while (prefix[r + 1] <= f) ++r;
     Item it;
     it.r = r;
-    const int ui = (kk_s[r] + MLA_TILE - 1) / MLA_TILE;
+    const int ui = (kk_s[r] + ROWS - 1) / ROWS;
     const int local = (int)(f - prefix[r]);
     it.hg = local / ui;
     it.unit = local - it.hg * ui;
-    it.nv = min(MLA_TILE, kk_s[r] - it.unit * MLA_TILE);
+    it.nv = min(ROWS, kk_s[r] - it.unit * ROWS);
     return it;
   };
 
@@ -252,20 +261,20 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
     for (long long f = u0; f < u1; ++f, ++it) {
       const Item w = decode(f, r);
       const long long rl = (long long)req_s[w.r] * g.n_layers + p.layer;
-      int slot[2];
+      int slot[(ROWS + 31) / 32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < (ROWS + 31) / 32; ++h) {
         const int j = lane + 32 * h;
-        slot[h] = j < w.nv ? p.s.slot_of_sel[(long long)w.r * K + w.unit * MLA_TILE + j] : 0;
+        slot[h] = j < w.nv ? p.s.slot_of_sel[(long long)w.r * K + w.unit * ROWS + j] : 0;
       }
       if (it >= nstage &&
           !__all_sync(FULL_MASK, wait_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
                                             p.s.dev_error)))
         break;
       unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
-      if (w.nv < MLA_TILE) {   // rows past k_eff: zeros keep the masked products finite
+      if (w.nv < ROWS) {   // rows past k_eff: zeros keep the masked products finite
         const int rvec = MLA_DK * 2 / 16;
-        for (int e = lane; e < (MLA_TILE - w.nv) * rvec; e += 32) {
+        for (int e = lane; e < (ROWS - w.nv) * rvec; e += 32) {
           const int j = w.nv + e / rvec;
           *reinterpret_cast<int4*>(st_s + (size_t)j * MLA_ROW_STRIDE + (e % rvec) * 16) = make_int4(0, 0, 0, 0);
         }
@@ -279,7 +288,7 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
       const unsigned char* hot =
           reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < (ROWS + 31) / 32; ++h) {
         const int j = lane + 32 * h;
         if (j < w.nv) {
           int sl = slot[h];
@@ -296,31 +305,36 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
   } else {
     // ============================ consumer warps ============================
     const int gq = lane >> 2, tq = lane & 3;
+    const int smt = warp / NT, snt = warp % NT;   // this warp's (head tile, row tile) of S
     const float sl2 = p.scale_log2;
     const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1);   // ldmatrix row of this lane (16-row operands)
     const int lcol = 8 * (lane >> 4);                        // and its column offset
-    float o[8][4];
-    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
+    float o[NMT][8][4];
+    float m[NMT][2], l[NMT][2];   // heads 16 mt + gq and 16 mt + gq + 8
     int cur_r = -1, cur_hg = -1;
     int r = ri;
     int s = 0;
     long long it = 0;
 
     auto flush = [&](int rq, int hg) {
-      const long long f0 = prefix[rq] + (long long)hg * ((kk_s[rq] + MLA_TILE - 1) / MLA_TILE);
+      const long long f0 = prefix[rq] + (long long)hg * ((kk_s[rq] + ROWS - 1) / ROWS);
       const int part = c - owner(f0, U, Gc);
-      const long long base = ((long long)rq * p.att_parts + part) * HQ + hg * MLA_HG;
+      const long long base = ((long long)rq * p.att_parts + part) * HQ + hg * GH;
       float* po = p.s.part_o + base * MLA_DV;
       float* pml = p.s.part_ml + base * 2;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int d = 64 * warp + 8 * t + 2 * tq;
-        *reinterpret_cast<float2*>(po + (long long)gq * MLA_DV + d) = make_float2(o[t][0], o[t][1]);
-        *reinterpret_cast<float2*>(po + (long long)(gq + 8) * MLA_DV + d) = make_float2(o[t][2], o[t][3]);
-      }
-      if (warp == 0 && tq == 0) {
-        *reinterpret_cast<float2*>(pml + gq * 2) = make_float2(m_lo, l_lo);
-        *reinterpret_cast<float2*>(pml + (gq + 8) * 2) = make_float2(m_hi, l_hi);
+      for (int mt = 0; mt < NMT; ++mt) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int d = 64 * warp + 8 * t + 2 * tq;
+          *reinterpret_cast<float2*>(po + (long long)(16 * mt + gq) * MLA_DV + d) = make_float2(o[mt][t][0], o[mt][t][1]);
+          *reinterpret_cast<float2*>(po + (long long)(16 * mt + gq + 8) * MLA_DV + d) =
+              make_float2(o[mt][t][2], o[mt][t][3]);
+        }
+        if (warp == 0 && tq == 0) {
+          *reinterpret_cast<float2*>(pml + (16 * mt + gq) * 2) = make_float2(m[mt][0], l[mt][0]);
+          *reinterpret_cast<float2*>(pml + (16 * mt + gq + 8) * 2) = make_float2(m[mt][1], l[mt][1]);
+        }
       }
     };
 
@@ -331,27 +345,28 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
         cur_r = w.r;
         cur_hg = w.hg;
         consumers_sync();   // every warp is done with the previous group's Q
-        const int4* qsrc = reinterpret_cast<const int4*>(p.q + ((long long)w.r * HQ + w.hg * MLA_HG) * MLA_DK);
-        for (int e = tid; e < MLA_HG * MLA_DK / 8; e += MLA_NCONS * 32) {
+        const int4* qsrc = reinterpret_cast<const int4*>(p.q + ((long long)w.r * HQ + w.hg * GH) * MLA_DK);
+        for (int e = tid; e < GH * MLA_DK / 8; e += MLA_NCONS * 32) {
           const int h = e / (MLA_DK / 8), v = e % (MLA_DK / 8);
           *reinterpret_cast<int4*>(qs + (size_t)h * MLA_ROW_STRIDE + v * 16) = qsrc[e];
         }
         consumers_sync();
 #pragma unroll
-        for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-        m_lo = m_hi = -INFINITY;
-        l_lo = l_hi = 0.f;
+        for (int mt = 0; mt < NMT; ++mt) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) o[mt][t][0] = o[mt][t][1] = o[mt][t][2] = o[mt][t][3] = 0.f;
+          m[mt][0] = m[mt][1] = -INFINITY;
+          l[mt][0] = l[mt][1] = 0.f;
+        }
       }
       const bool ok = wait_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error);
       const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
-      // ---- S = Q K^T for rows 8*warp .. 8*warp + 7 ----
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S = Q K^T for head tile smt x row tile snt ----
+      float sc[4];
       {
-        // four independent accumulators over the 36 k-steps (a chain of 9 instead
-        // of 36 dependent mma), summed in a fixed order
         float acc[4][4] = {};
-        const uint32_t rowa = smem_addr(st_s + (size_t)(8 * warp + (lane & 7)) * MLA_ROW_STRIDE) + 16 * (lane >> 3);
-        const uint32_t qa = smem_addr(qs + (size_t)lrow * MLA_ROW_STRIDE) + 2 * lcol;
+        const uint32_t rowa = smem_addr(st_s + (size_t)(8 * snt + (lane & 7)) * MLA_ROW_STRIDE) + 16 * (lane >> 3);
+        const uint32_t qa = smem_addr(qs + (size_t)(16 * smt + lrow) * MLA_ROW_STRIDE) + 2 * lcol;
 #pragma unroll
         for (int kp2 = 0; kp2 < MLA_DK / 64; ++kp2) {
 #pragma unroll
@@ -368,11 +383,11 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
       }
-      // ---- tile maxima per head ----
+      // ---- block maxima per head ----
       float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const bool okr = 8 * warp + 2 * tq + e < w.nv;
+        const bool okr = 8 * snt + 2 * tq + e < w.nv;
         sc[e] = okr ? sc[e] * sl2 : -INFINITY;
         sc[2 + e] = okr ? sc[2 + e] * sl2 : -INFINITY;
         mx_lo = fmaxf(mx_lo, sc[e]);
@@ -382,66 +397,87 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL_MASK, mx_lo, 2));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL_MASK, mx_hi, 1));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL_MASK, mx_hi, 2));
-      float* smx = smax + (it & 1) * MLA_NCONS * MLA_HG;
+      float* smx = smax + (it & 1) * 8 * 16;   // [block = warp][16 heads of its tile]
       if (tq == 0) {
-        smx[warp * MLA_HG + gq] = mx_lo;
-        smx[warp * MLA_HG + gq + 8] = mx_hi;
+        smx[warp * 16 + gq] = mx_lo;
+        smx[warp * 16 + gq + 8] = mx_hi;
       }
       if (consumers_sync_or(!ok)) break;   // all consumer warps leave together
-      float tm_lo = -INFINITY, tm_hi = -INFINITY;
+      // new running maxima of every head this lane covers (all head tiles), from
+      // the blocks of each head tile (same order in every warp)
+      float mnew[NMT][2], alpha[NMT][2];
 #pragma unroll
-      for (int q = 0; q < MLA_NCONS; ++q) {
-        tm_lo = fmaxf(tm_lo, smx[q * MLA_HG + gq]);
-        tm_hi = fmaxf(tm_hi, smx[q * MLA_HG + gq + 8]);
+      for (int mt = 0; mt < NMT; ++mt) {
+        float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+          t0 = fmaxf(t0, smx[(mt * NT + q) * 16 + gq]);
+          t1 = fmaxf(t1, smx[(mt * NT + q) * 16 + gq + 8]);
+        }
+        mnew[mt][0] = fmaxf(m[mt][0], t0);   // finite: every item has a valid row
+        mnew[mt][1] = fmaxf(m[mt][1], t1);
+        alpha[mt][0] = exp2f(m[mt][0] - mnew[mt][0]);
+        alpha[mt][1] = exp2f(m[mt][1] - mnew[mt][1]);
       }
-      const float mn_lo = fmaxf(m_lo, tm_lo), mn_hi = fmaxf(m_hi, tm_hi);   // finite: every unit has a valid row
-      const float a_lo = exp2f(m_lo - mn_lo), a_hi = exp2f(m_hi - mn_hi);
-      m_lo = mn_lo;
-      m_hi = mn_hi;
-      const float p0 = exp2f(sc[0] - mn_lo), p1 = exp2f(sc[1] - mn_lo);
-      const float p2 = exp2f(sc[2] - mn_hi), p3 = exp2f(sc[3] - mn_hi);
-      *reinterpret_cast<uint32_t*>(ps + (size_t)gq * MLA_P_STRIDE + 2 * (8 * warp + 2 * tq)) = pack2_bf16(p0, p1);
-      *reinterpret_cast<uint32_t*>(ps + (size_t)(gq + 8) * MLA_P_STRIDE + 2 * (8 * warp + 2 * tq)) =
-          pack2_bf16(p2, p3);
-      float su_lo = p0 + p1, su_hi = p2 + p3;
-      su_lo += __shfl_xor_sync(FULL_MASK, su_lo, 1);
-      su_lo += __shfl_xor_sync(FULL_MASK, su_lo, 2);
-      su_hi += __shfl_xor_sync(FULL_MASK, su_hi, 1);
-      su_hi += __shfl_xor_sync(FULL_MASK, su_hi, 2);
-      if (tq == 0) {
-        ssum[warp * MLA_HG + gq] = su_lo;
-        ssum[warp * MLA_HG + gq + 8] = su_hi;
+      // P of this warp's block, and its per-head sums
+      {
+        const float ml = mnew[smt][0], mh = mnew[smt][1];
+        const float p0 = exp2f(sc[0] - ml), p1 = exp2f(sc[1] - ml);
+        const float p2 = exp2f(sc[2] - mh), p3 = exp2f(sc[3] - mh);
+        *reinterpret_cast<uint32_t*>(ps + (size_t)(16 * smt + gq) * P_STRIDE + 2 * (8 * snt + 2 * tq)) =
+            pack2_bf16(p0, p1);
+        *reinterpret_cast<uint32_t*>(ps + (size_t)(16 * smt + gq + 8) * P_STRIDE + 2 * (8 * snt + 2 * tq)) =
+            pack2_bf16(p2, p3);
+        float su_lo = p0 + p1, su_hi = p2 + p3;
+        su_lo += __shfl_xor_sync(FULL_MASK, su_lo, 1);
+        su_lo += __shfl_xor_sync(FULL_MASK, su_lo, 2);
+        su_hi += __shfl_xor_sync(FULL_MASK, su_hi, 1);
+        su_hi += __shfl_xor_sync(FULL_MASK, su_hi, 2);
+        if (tq == 0) {
+          ssum[warp * 16 + gq] = su_lo;
+          ssum[warp * 16 + gq + 8] = su_hi;
+        }
       }
       consumers_sync();
-      float ts_lo = 0.f, ts_hi = 0.f;
 #pragma unroll
-      for (int q = 0; q < MLA_NCONS; ++q) {   // fixed order: every warp gets the same l
-        ts_lo += ssum[q * MLA_HG + gq];
-        ts_hi += ssum[q * MLA_HG + gq + 8];
-      }
-      l_lo = l_lo * a_lo + ts_lo;
-      l_hi = l_hi * a_hi + ts_hi;
+      for (int mt = 0; mt < NMT; ++mt) {
+        float ts0 = 0.f, ts1 = 0.f;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        o[t][0] *= a_lo;
-        o[t][1] *= a_lo;
-        o[t][2] *= a_hi;
-        o[t][3] *= a_hi;
+        for (int q = 0; q < NT; ++q) {   // fixed order: every warp gets the same l
+          ts0 += ssum[(mt * NT + q) * 16 + gq];
+          ts1 += ssum[(mt * NT + q) * 16 + gq + 8];
+        }
+        l[mt][0] = l[mt][0] * alpha[mt][0] + ts0;
+        l[mt][1] = l[mt][1] * alpha[mt][1] + ts1;
+        m[mt][0] = mnew[mt][0];
+        m[mt][1] = mnew[mt][1];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          o[mt][t][0] *= alpha[mt][0];
+          o[mt][t][1] *= alpha[mt][0];
+          o[mt][t][2] *= alpha[mt][1];
+          o[mt][t][3] *= alpha[mt][1];
+        }
       }
-      // ---- O[:, 64*warp .. +63] += P V over the 64 rows ----
+      // ---- O[:, 64*warp .. +63] += P V over the item's rows ----
       {
-        const uint32_t pa_base = smem_addr(ps + (size_t)lrow * MLA_P_STRIDE) + 2 * lcol;
+        const uint32_t pa_base = smem_addr(ps + (size_t)lrow * P_STRIDE) + 2 * lcol;
         const uint32_t v_base = smem_addr(st_s + (size_t)lrow * MLA_ROW_STRIDE) + 2 * (64 * warp + lcol);
 #pragma unroll
-        for (int ks = 0; ks < MLA_TILE / 16; ++ks) {
-          uint32_t pa[4];
-          ldsm4(pa, pa_base + 32 * ks);   // P heads x rows 16ks .. 16ks+15
+        for (int ks = 0; ks < ROWS / 16; ++ks) {
+          uint32_t pa[NMT][4];
+#pragma unroll
+          for (int mt = 0; mt < NMT; ++mt)
+            ldsm4(pa[mt], pa_base + (uint32_t)(16 * mt * P_STRIDE) + 32 * ks);   // P heads 16mt.. x rows 16ks..
 #pragma unroll
           for (int tp = 0; tp < 4; ++tp) {
             uint32_t b[4];
             ldsm4_t(b, v_base + (uint32_t)(16 * ks * MLA_ROW_STRIDE) + 32 * tp);
-            mma16816(o[2 * tp], pa, b[0], b[1]);
-            mma16816(o[2 * tp + 1], pa, b[2], b[3]);
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+              mma16816(o[mt][2 * tp], pa[mt], b[0], b[1]);
+              mma16816(o[mt][2 * tp + 1], pa[mt], b[2], b[3]);
+            }
           }
         }
       }
@@ -462,7 +498,8 @@ __global__ void __launch_bounds__(MLA_THREADS, 1) attn_mla_kernel(DecodeParams p
 
 template <int HQ>
 static cudaError_t run_mla(const DecodeParams* p, size_t smem, cudaStream_t st) {
-  auto kern = attn_mla_kernel<HQ>;
+  constexpr int NMT = HQ >= 32 ? 2 : 1;
+  auto kern = attn_mla_kernel<HQ, NMT>;
   if (p == nullptr) return allow_smem(kern, smem);
   cudaError_t e = launch_pdl(kern, dim3(p->att_grid), dim3(MLA_THREADS), smem, st, *p);
   if (e != cudaSuccess) return e;
