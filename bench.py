@@ -151,6 +151,32 @@ KERNEL_FILES = {"append": "hs_append.cu", "indexer": "hs_score.cu",
                 "topk_resolve": "hs_resolve.cu", "attention": "hs_attention.cu"}
 
 
+def host_store_pages(host_bytes: int) -> dict:
+    """How much of the pinned host K/V store the kernel backed with transparent
+    huge pages (the GPU's random row reads over the link miss its TLB far less on
+    them), read from /proc/self/smaps; plus the system's THP mode (read only)."""
+    out = {"thp_frac": None}
+    for name in ("enabled", "defrag"):
+        try:
+            with open(f"/sys/kernel/mm/transparent_hugepage/{name}") as f:
+                out[f"thp_{name}"] = f.read().strip()
+        except OSError:
+            out[f"thp_{name}"] = None
+    try:
+        with open("/proc/self/smaps") as f:
+            size = None
+            for line in f:
+                if line.startswith("Size:"):
+                    size = int(line.split()[1]) * 1024
+                elif line.startswith("AnonHugePages:") and size is not None:
+                    if host_bytes <= size <= host_bytes + (1 << 30):   # the store's own mapping
+                        out["thp_frac"] = round(int(line.split()[1]) * 1024 / host_bytes, 4)
+                        break
+    except OSError:
+        pass
+    return out
+
+
 def ncu_traffic(kernel: str, workload: str, latent: bool = False):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     this kernel source and workload (else None).  Latent-row attention lives in
@@ -288,6 +314,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
             torch.cuda.synchronize(dev)   # the staging buffer is reused
     del stage_kv, stage_keys
     t_pre = time.time() - t_pre
+    host_pages = host_store_pages(cache.stats()["host_bytes"])
 
     # ---- per-step inputs, resident in HBM -----------------------------------------
     walks = np.stack([np.stack([wl.query_walk(w, r, l, T) for r in range(R)]) for l in range(L)])  # [L,R,T,d]
@@ -488,6 +515,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "clocks": clk,
         "prefill_s": round(t_pre, 1),
+        "host_store": host_pages,
         "device_error": dev_err,
     }
     cache.close()

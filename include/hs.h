@@ -156,10 +156,10 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
 
 /*
  * hs_decode_layer — one decode layer-step for n_req requests (stream-ordered,
- * no host synchronisation, capturable in a CUDA graph).  Its kernels are
- * launched as programmatic dependents: each waits for the previous kernel of the
- * stream before it reads anything, so ordering against earlier stream work is
- * the usual one.
+ * no host synchronisation, capturable in a CUDA graph).  Its score, attention
+ * and merge kernels are launched as programmatic dependents: each waits for the
+ * previous kernel of the stream before it reads anything, so ordering against
+ * earlier stream work is the usual one.
  *   req_ids     : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
  *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned)
  *   q           : dev bf16 [n_req][h_q][d_qk]   attention query
