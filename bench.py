@@ -80,6 +80,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_tflops():
+    """Sustained dense bf16 tensor throughput (the kernels run inside a long step)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+    return 1700.0, "fallback (sustained)"
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -197,10 +208,12 @@ def ncu_traffic(kernel: str, workload: str, latent: bool = False):
 # algorithmic traffic of one layer of all R requests (per kernel)
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float) -> dict:
+def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_pulls: bool = False) -> dict:
     """HBM and host-link bytes the method itself moves for one layer-step of all
     requests.  n_ctx: context length of each request at this step; misses: rows
-    pulled from host memory in this layer-step (all requests)."""
+    pulled from host memory in this layer-step (all requests); resolve_pulls: the
+    missed rows are copied (host read, slot write) by the top-k + RESOLVE kernel
+    rather than by the attention kernel."""
     k_eff = np.minimum(w.top_k, n_ctx)
     R = w.n_requests
     row = w.row_bytes
@@ -211,10 +224,23 @@ def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float) -> dict:
         "indexer": float((n_ctx * w.d_idx).sum()) + R * w.d_idx,
         "topk_resolve": float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12
         + R * (w.row_bytes + 2 * w.d_idx + 4),
-        "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2 + misses * row,
+        "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2,
     }
-    link = {"append": 0.0, "indexer": 0.0, "topk_resolve": R * row, "attention": misses * row}
+    link = {"append": 0.0, "indexer": 0.0, "topk_resolve": R * row, "attention": 0.0}
+    puller = "topk_resolve" if resolve_pulls else "attention"
+    hbm[puller] += misses * row    # the slot writes
+    link[puller] += misses * row   # the host reads
     return {"hbm": hbm, "link": link}
+
+
+def resolve_pulls(fetch_mode: int, shared_kv: bool, misses_per_layer_step: float, n_sms: int) -> bool:
+    """Which kernel copies the missed rows: mode 1 and latent rows always RESOLVE;
+    mode 2 RESOLVE when the misses exceed 8 rows per attention CTA (the library's
+    per-request rule, applied to the average request), else mostly the attention
+    kernel; mode 0 the attention kernel."""
+    if shared_kv or fetch_mode == 1:
+        return True
+    return fetch_mode == 2 and misses_per_layer_step > 8 * n_sms
 
 
 def link_peak_gbs(dev, nbytes=1 << 30, reps=5) -> float:
@@ -445,11 +471,15 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     value = world * K * L / (ms_total * 1e-3)
     tokens = world * K * R / (ms_total * 1e-3)
     # algorithmic traffic of a timed region (contexts grow by one per step)
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
     def region_bytes(t_begin, n_miss):
         hb = {k: 0.0 for k in KERNEL_FILES}
         lb = {k: 0.0 for k in KERNEL_FILES}
+        m_ls = n_miss / (K * L)
+        rp = resolve_pulls(args.fetch_mode, w.shared_kv, m_ls, n_sms)
         for t in range(t_begin, t_begin + K):
-            ab = algorithmic_bytes(w, n0 + t + 1, n_miss / (K * L))
+            ab = algorithmic_bytes(w, n0 + t + 1, m_ls, rp)
             for k in KERNEL_FILES:
                 hb[k] += ab["hbm"][k] * L
                 lb[k] += ab["link"][k] * L
@@ -473,16 +503,36 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                       "link_gbs": round(per_kernel_link[k] / n / (avg * 1e-3) / 1e9, 1),
                       "hbm_bytes_per_launch": int(per_kernel_bytes[k] / n),
                       "link_bytes_per_launch": int(per_kernel_link[k] / n)}
+    if "attention" in kernels:
+        # the attention products on the tensor cores: 2 h_q (d_qk + d_v) flops per
+        # selected row (QK^T and PV).  Latent rows sit near the ridge point
+        # (~210 flop/byte against ~250 for these peaks); GQA rows far below it.
+        k_sum = float(np.minimum(w.top_k, n0 + W + K).sum())
+        fl = 2.0 * w.h_q * (w.d_qk + w.d_v) * k_sum
+        a = kernels["attention"]
+        tf_peak, tf_src = measured_bf16_tflops()
+        a["flops_per_launch"] = int(fl)
+        a["tflops"] = round(fl / (a["avg_us"] * 1e-6) / 1e12, 1)
+        a["tensor_frac"] = round(a["tflops"] / tf_peak, 4)
+        a["tensor_peak"] = {"tflops": tf_peak, "source": tf_src}
     tot_k = sum(v["avg_us"] * v["launches"] for v in kernels.values()) or 1.0
     for v in kernels.values():
         v["share"] = round(v["avg_us"] * v["launches"] / tot_k, 4)
     dom = max(kernels, key=lambda k: kernels[k]["share"]) if kernels else None
     roof = None
     if dom:
-        ach = kernels[dom]["hbm_gbs"]
-        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
-                "frac": round(ach / peak_hbm, 4), "peak_source": peak_src,
-                "traffic": ncu_traffic(dom, w.name, w.shared_kv), "bytes_per_launch": kernels[dom]["hbm_bytes_per_launch"]}
+        kd = kernels[dom]
+        if kd["link_bytes_per_launch"] / (peak_link * 1e9) > kd["hbm_bytes_per_launch"] / (peak_hbm * 1e9):
+            # the kernel's own bound is the host link (RESOLVE pulling many rows)
+            ach = kd["link_gbs"]
+            roof = {"kernel": dom, "bound": "link", "achieved": ach, "peak": round(peak_link, 1), "unit": "GB/s",
+                    "frac": round(ach / peak_link, 4), "peak_source": "pinned cudaMemcpyAsync H2D, measured in this run",
+                    "traffic": None, "bytes_per_launch": kd["link_bytes_per_launch"]}
+        else:
+            ach = kd["hbm_gbs"]
+            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
+                    "frac": round(ach / peak_hbm, 4), "peak_source": peak_src,
+                    "traffic": ncu_traffic(dom, w.name, w.shared_kv), "bytes_per_launch": kd["hbm_bytes_per_launch"]}
     # the attention entry also launches the partial-merge kernel
     gpu_launches = sum(v["launches"] for v in kernels.values()) + kernels.get("attention", {}).get("launches", 0)
     out = {

@@ -1,0 +1,34 @@
+"""bench.py's algorithmic-traffic model on CPU: the missed rows' host reads and
+slot writes are charged to the kernel that copies them, and totals do not depend
+on which one that is."""
+import numpy as np
+
+import workload as wl
+
+
+def test_pulled_rows_are_charged_to_the_copying_kernel():
+    import bench
+    w = wl.WORKLOADS["batch16_32k"]
+    n_ctx = w.contexts() + 5
+    a = bench.algorithmic_bytes(w, n_ctx, 700.0, resolve_pulls=False)
+    b = bench.algorithmic_bytes(w, n_ctx, 700.0, resolve_pulls=True)
+    moved = 700.0 * w.row_bytes
+    assert b["link"]["topk_resolve"] - a["link"]["topk_resolve"] == moved
+    assert a["link"]["attention"] - b["link"]["attention"] == moved
+    assert b["hbm"]["topk_resolve"] - a["hbm"]["topk_resolve"] == moved
+    for kind in ("hbm", "link"):
+        assert np.isclose(sum(a[kind].values()), sum(b[kind].values()))
+    # the index scan reads every key once; the attention every selected row once
+    # (with RESOLVE copying the misses, nothing else)
+    assert a["hbm"]["indexer"] == float((n_ctx * w.d_idx).sum()) + w.n_requests * w.d_idx
+    k_eff = np.minimum(w.top_k, n_ctx).sum()
+    assert b["hbm"]["attention"] == float(k_eff) * (w.row_bytes + 4) + w.n_requests * w.h_q * (w.d_qk + w.d_v) * 2
+
+
+def test_who_pulls_follows_the_library_rule():
+    import bench
+    assert bench.resolve_pulls(1, False, 0.0, 152)
+    assert bench.resolve_pulls(0, True, 0.0, 152)          # latent rows: always RESOLVE
+    assert not bench.resolve_pulls(0, False, 1e6, 152)
+    assert not bench.resolve_pulls(2, False, 8 * 152, 152)  # at the threshold: attention
+    assert bench.resolve_pulls(2, False, 8 * 152 + 1, 152)
