@@ -264,10 +264,11 @@ def link_peak_gbs(dev, nbytes=1 << 30, reps=5) -> float:
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w: wl.Workload, requests, layers, steps: int) -> tuple[float, int]:
+def oracle_sample(w: wl.Workload, requests, layers, steps: int, replacement: str = "lru") -> tuple[float, int]:
     """Times the oracle over decode steps 0..steps-1 of the given (request, layer)
     pairs; returns (seconds, request-layer-steps).  Input generation is not timed."""
-    from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+    from oracle import FIFOHotCache, LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+    policy = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement]
     total = 0.0
     units = 0
     for l in layers:
@@ -278,7 +279,7 @@ def oracle_sample(w: wl.Workload, requests, layers, steps: int) -> tuple[float, 
             n0 = int(w.contexts()[r])
             qs = [wl.step_query(w, r, l, t) for t in range(steps)]
             app = [wl.step_kv_row(w, r, l, t) for t in range(steps)]
-            cache = LRUHotCache(w.hot_slots)
+            cache = policy(w.hot_slots)
             t0 = time.perf_counter()
             for t in range(steps):
                 n = n0 + t + 1
@@ -323,7 +324,8 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     R, L = w.n_requests, w.n_layers
     cache = HiSparseCache(n_layers=L, max_requests=R, max_context=w.max_context(T), h_q=w.h_q, h_kv=w.h_kv,
                           d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k, hot_slots=w.hot_slots,
-                          shared_kv=w.shared_kv, device=dev_index, fetch_mode=args.fetch_mode)
+                          shared_kv=w.shared_kv, device=dev_index, fetch_mode=args.fetch_mode,
+                          replacement=args.replacement)
 
     # ---- prefill: generate each (request, layer) context and append it -----------
     t_pre = time.time()
@@ -546,7 +548,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                    "sigma": w.sigma, "parallelism": f"requests sharded, {world} independent cache(s)",
                    "l2": f"inputs larger than L2: {hbm_total / K / 2**20:.0f} MiB read per step > 129 MiB",
                    "timed": "one CUDA graph of the timed steps, replayed once",
-                   "fetch_mode": args.fetch_mode},
+                   "fetch_mode": args.fetch_mode, "replacement": args.replacement},
         "kernel_timing": {"mode": timing_mode, "steps": K, "ms_per_step": round(ms_total_b / K, 4)},
         "tokens_per_s": round(tokens, 1),
         "hbm_gbs": round(hbm_total / (ms_total * 1e-3) / 1e9, 1),
@@ -585,6 +587,8 @@ def main():
     ap.add_argument("--fetch-mode", type=int, default=2, choices=[0, 1, 2],
                     help="who copies missed rows: 0 the attention kernel (overlapped), 1 RESOLVE, "
                          "2 chosen per request (default)")
+    ap.add_argument("--replacement", default="lru", choices=["lru", "fifo"],
+                    help="hot-cache replacement: lru (the method's) or fifo (its comparison policy)")
     ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
     ap.add_argument("--clock-interval-ms", type=int, default=50,
                     help="nvidia-smi clock sampling period during the timed region (0: off)")
@@ -607,6 +611,7 @@ def main():
     w = rank_workload(w, rank, world)
 
     sr, sl, ss = (int(x) for x in args.cpu_sample.split("x"))
+    sr, sl = min(sr, w.n_requests), min(sl, w.n_layers)   # the sample stays inside the workload
     if args.impl == "reference":
         if rank != 0:
             return
@@ -617,7 +622,7 @@ def main():
     res = run_hisparse(args, w, rank, world, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            secs, units = oracle_sample(w, range(sr), range(sl), ss)
+            secs, units = oracle_sample(w, range(sr), range(sl), ss, args.replacement)
             per_unit = secs / units
             res["cpu_baseline"] = {"value": round(1.0 / (per_unit * w.n_requests), 4), "unit": UNIT,
                                    "cores": cpu_threads(), "kind": "oracle",
@@ -638,7 +643,8 @@ def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
     steps = W + K
     # the oracle replays steps 0..steps-1 of each sampled (request, layer); the
     # first W are the warm-up
-    from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+    from oracle import FIFOHotCache, LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+    policy = {"lru": LRUHotCache, "fifo": FIFOHotCache}[args.replacement]
     per_step = []
     for l in range(sl):
         for r in range(sr):
@@ -646,7 +652,7 @@ def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
             walk = wl.query_walk(w, r, l, steps)
             kv = wl.prefill_kv(w, r, l)
             n0 = int(w.contexts()[r])
-            cache = LRUHotCache(w.hot_slots)
+            cache = policy(w.hot_slots)
             for t in range(steps):
                 q = wl.step_query(w, r, l, t)
                 app = [wl.step_kv_row(w, r, l, u) for u in range(t + 1)]

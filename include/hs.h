@@ -97,7 +97,19 @@ typedef struct hs_config {
                             it finds it, whichever copies it.
                             Latent rows (shared_kv = 1) always use 1: every head
                             group reads them, so they cross the host link once. */
+  int32_t replacement;   /* which unpinned slots the misses replace (hits are always pinned;
+                            victims are the m unpinned slots with the smallest (stamp, slot)):
+                            HS_REPLACE_LRU  (0): every slot the call uses (hits and fills)
+                                gets stamp = step — least recently used first, the pages'
+                                policy;
+                            HS_REPLACE_FIFO (1): only filled slots get stamp = step, a hit
+                                keeps its fill stamp — first filled first, the comparison
+                                policy of the pages' miss-rate ablation.
+                            The attention result does not depend on it. */
 } hs_config_t;
+
+#define HS_REPLACE_LRU 0
+#define HS_REPLACE_FIFO 1
 
 typedef struct hs_handle hs_handle_t;
 
@@ -199,7 +211,8 @@ int hs_stats(hs_handle_t* h, hs_stats_t* out);
  * to host buffers (test and debugging introspection).  Any output may be NULL.
  *   page    : int32 [n_page]   page-table entries of positions 0..n_page-1
  *   reverse : int32 [hot_slots] position held by each slot, -1 = empty
- *   stamp   : int32 [hot_slots] step of last use of each slot, -1 = never
+ *   stamp   : int32 [hot_slots] step of last use of each slot (FIFO: of its last
+ *             fill), -1 = never
  *   order   : int32 [hot_slots] slots from least to most recently used
  *             (sorted by (stamp, slot))
  *   scalars : int64 [4] = {length, step, hits, misses} of this (request, layer)

@@ -9,6 +9,7 @@ from .hisparse_oracle import (  # noqa: F401
     indexer_scores_many,
     topk_select,
     LRUHotCache,
+    FIFOHotCache,
     belady_misses,
     sparse_attention,
     hot_over_full,

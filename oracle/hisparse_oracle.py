@@ -123,6 +123,8 @@ class LRUHotCache:
     Empty slots carry stamp -1, so they fill first, lowest slot first.
     """
 
+    refresh_hits = True   # LRU: a hit renews its slot's stamp
+
     def __init__(self, n_slots: int):
         self.B = int(n_slots)
         self.slot_pos = [-1] * self.B
@@ -148,8 +150,10 @@ class LRUHotCache:
             self.page[p] = v
             fills.append((p, v))
         slot_of_sel = [self.page[p] for p in sel]
+        filled = {v for _, v in fills}
         for s in slot_of_sel:
-            self.slot_stamp[s] = t
+            if self.refresh_hits or s in filled:
+                self.slot_stamp[s] = t
         self.step_no = t + 1
         return {
             "slot_of_sel": np.asarray(slot_of_sel, dtype=np.int64),
@@ -166,6 +170,19 @@ class LRUHotCache:
                 page[p] = s
         return (page, np.asarray(self.slot_pos, dtype=np.int64),
                 np.asarray(self.slot_stamp, dtype=np.int64), self.step_no)
+
+
+class FIFOHotCache(LRUHotCache):
+    """The same hot cache under first-in-first-out replacement, the comparison
+    policy of the HiSparse summary's miss-rate ablation ("论文1：HiSparse": LRU
+    13.4 % against FIFO 17.2 % at B = 4096).
+
+    Identical to the LRU rule except step 5: only the slots filled by the call
+    take stamp = step; a hit keeps the stamp of its fill, so the victims are the
+    unpinned slots filled longest ago (smallest (fill stamp, slot)).
+    """
+
+    refresh_hits = False
 
 
 # ---------------------------------------------------------------------------

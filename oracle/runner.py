@@ -16,23 +16,24 @@ import numpy as np
 
 import workload as wl
 
-from .hisparse_oracle import (LRUHotCache, belady_misses, indexer_scores_many,
+from .hisparse_oracle import (FIFOHotCache, LRUHotCache, belady_misses, indexer_scores_many,
                               sparse_attention, topk_select)
 
 
 def replay_request_layer(w: wl.Workload, req: int, layer: int, steps: int | None = None, *,
                          attention_steps=None, kv_prefill: np.ndarray | None = None,
-                         keep_trace: bool = True) -> dict:
+                         keep_trace: bool = True, replacement: str = "lru") -> dict:
     """Oracle results of decode steps 0..steps-1 of one (request, layer).
 
     attention_steps: None (no attention), "all", or an iterable of step numbers
-    whose attention outputs are wanted (float64 [H_q, d_v])."""
+    whose attention outputs are wanted (float64 [H_q, d_v]); replacement: "lru"
+    (the pages' policy) or "fifo" (their comparison policy)."""
     T = w.steps if steps is None else steps
     n0 = int(w.contexts()[req])
     keys = wl.idx_keys_upto(w, req, layer, T)
     walk = wl.query_walk(w, req, layer, T)
     scores = indexer_scores_many(keys, walk)           # [N0+T, T], exact integers
-    cache = LRUHotCache(w.hot_slots)
+    cache = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](w.hot_slots)
     if attention_steps == "all":
         att = set(range(T))
     elif attention_steps is None:

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import workload as wl
-from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+from oracle import FIFOHotCache, LRUHotCache, indexer_scores_many, sparse_attention, topk_select
 from tests.harness import MAX_ABS, REL_L2, StepInputs, attention_error, make_cache, prefill, run_steps
 
 pytestmark = pytest.mark.gpu
@@ -26,12 +26,12 @@ def _gpu():
     yield
 
 
-def oracle_steps(w, r, l, steps, n_slots=None):
+def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru"):
     """Per step: (sel, step result, snapshot) from the oracle."""
     keys = wl.idx_keys_upto(w, r, l, steps)
     walk = wl.query_walk(w, r, l, steps)
     scores = indexer_scores_many(keys, walk)
-    cache = LRUHotCache(n_slots or w.hot_slots)
+    cache = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](n_slots or w.hot_slots)
     n0 = int(w.contexts()[r])
     out = []
     for t in range(steps):
@@ -53,8 +53,8 @@ def check_order(order, stamp):
     assert order.tolist() == keys
 
 
-def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False):
-    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode)
+def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement="lru"):
+    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode, replacement=replacement)
     prefill(cache, w)
     inp = StepInputs(w, steps)
     got = run_steps(cache, w, inp, steps, collect_meta=True, fused=fused)
@@ -63,7 +63,7 @@ def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False):
     for l in range(w.n_layers):
         for r in range(w.n_requests):
             prev_h = prev_m = 0
-            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B)):
+            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B, replacement)):
                 k_eff = sel.size
                 g_sel = got["sel"][l, t][r]
                 assert np.array_equal(g_sel[:k_eff], sel), f"selection r{r} l{l} t{t}"
@@ -412,3 +412,38 @@ def test_graph_capture_replays_the_same_step():
         assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"][0, t])
     assert cache.stats()["device_error"] == 0
     cache.close()
+
+
+@pytest.mark.parametrize("fetch_mode", [0, 1, 2])
+def test_fifo_replacement_matches_the_oracle(fetch_mode):
+    # the pages' comparison policy: only fills renew a slot's stamp; B close to k
+    # and a fast-moving query so hits and evictions mix every step
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=4100, top_k=256,
+                         hot_slots=320, steps=6, sigma=0.3)
+    full_parity(w, 6, fetch_mode=fetch_mode, replacement="fifo")
+
+
+def test_fifo_latent_rows_and_fused_append():
+    w = wl.make_workload("mla_128k", n_requests=2, n_layers=1, context=2600, h_q=32, top_k=256,
+                         hot_slots=320, steps=4, sigma=0.3)
+    full_parity(w, 4, fused=True, replacement="fifo")
+
+
+def test_replacement_policy_changes_placement_not_the_result():
+    # LRU and FIFO put rows in different slots and miss differently; the
+    # selection and the attention output are bit-identical
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=6000, top_k=512,
+                         hot_slots=640, steps=6, sigma=0.3)
+    runs = []
+    for rep in ("lru", "fifo"):
+        cache = make_cache(w, 6, replacement=rep)
+        prefill(cache, w)
+        runs.append(run_steps(cache, w, StepInputs(w, 6), 6, collect_meta=True))
+        cache.close()
+    differ = False
+    for key in runs[0]["out"]:
+        assert np.array_equal(runs[0]["out"][key], runs[1]["out"][key])
+        assert np.array_equal(runs[0]["sel"][key], runs[1]["sel"][key])
+        for a, b in zip(runs[0]["meta"][key], runs[1]["meta"][key]):
+            differ |= not np.array_equal(a[2], b[2])   # stamps
+    assert differ, "the two policies should not leave identical stamps on this trace"

@@ -9,8 +9,9 @@
 //
 // Replacement rule: slots holding a selected position (hits) are pinned; the m
 // misses, in ascending position order, go to the m unpinned slots with the
-// smallest (last-use stamp, slot), in that order; every used slot's stamp becomes
-// the (request, layer) step counter, which then grows by one.
+// smallest (stamp, slot), in that order; every used slot's stamp (LRU), or only
+// every filled slot's (FIFO, the pages' comparison policy), becomes the (request,
+// layer) step counter, which then grows by one.
 //
 // Design (sm_103a), one 1024-thread CTA per request; a latency-bound chain, so
 // every global read the chain needs is issued up front, and the steps between
@@ -627,19 +628,23 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     auto miss_sel = [&](int q) { return miss_i[q] & ~HS_SLOT_MISS_FLAG; };
     const int miss_flag = pull ? 0 : HS_SLOT_MISS_FLAG;
     int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
+    // LRU: every used slot is refreshed; FIFO: only the filled ones (used == 2)
+    const bool fifo = p.fifo != 0;
+    auto refreshed = [&](uint8_t u) { return fifo ? u == 2 : u != 0; };
     for (int i = tid; i < kk; i += RES_THREADS) {
       const int sl = slot_sel[i];
-      stamp[sl] = t;
+      if (refreshed(used[sl])) stamp[sl] = t;
       sos[i] = sl;
     }
     HS_TRACE(p, 1, 22);
     __syncthreads();
     HS_TRACE(p, 1, 23);
     for (int q = tid; q < m; q += RES_THREADS) sos[miss_sel(q)] = victim[q] | (pulled(q) ? 0 : miss_flag);
-    // new LRU list: unused slots keep their order, used slots go last by slot
+    // new list: slots not refreshed keep their order, refreshed slots (all with
+    // the newest stamp) go last by slot
     int nu = 0, nus = 0;
-    for (int j = j0; j < j1; ++j) nu += used[ord[j]] == 0;
-    for (int sl = j0; sl < j1; ++sl) nus += used[sl] != 0;
+    for (int j = j0; j < j1; ++j) nu += !refreshed(used[ord[j]]);
+    for (int sl = j0; sl < j1; ++sl) nus += refreshed(used[sl]);
     int n_unused;
     HS_TRACE(p, 1, 24);
     const int2 un = block_exclusive_scan2<RES_THREADS>(nu, nus, sh.scan, &n_unused, nullptr);
@@ -647,11 +652,11 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     int ub = un.x;
     for (int j = j0; j < j1; ++j) {
       const int sl = ord[j];
-      if (used[sl] == 0) order[ub++] = sl;
+      if (!refreshed(used[sl])) order[ub++] = sl;
     }
     int sb = n_unused + un.y;
     for (int sl = j0; sl < j1; ++sl)
-      if (used[sl] != 0) order[sb++] = sl;
+      if (refreshed(used[sl])) order[sb++] = sl;
     HS_TRACE(p, 1, 26);
     if (tid == 0) {
       p.s.step[rl] = t + 1;
