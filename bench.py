@@ -264,11 +264,19 @@ def link_peak_gbs(dev, nbytes=1 << 30, reps=5) -> float:
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
+def oracle_cache(w: wl.Workload, r: int, l: int, replacement: str):
+    """The oracle's hot cache of one (request, layer) under the chosen policy
+    (the random policy's seed is the library default, 0)."""
+    from oracle import FIFOHotCache, LRUHotCache, RandomHotCache
+    if replacement == "random":
+        return RandomHotCache(w.hot_slots, seed=0, request=r, layer=l, n_layers=w.n_layers)
+    return {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](w.hot_slots)
+
+
 def oracle_sample(w: wl.Workload, requests, layers, steps: int, replacement: str = "lru") -> tuple[float, int]:
     """Times the oracle over decode steps 0..steps-1 of the given (request, layer)
     pairs; returns (seconds, request-layer-steps).  Input generation is not timed."""
-    from oracle import FIFOHotCache, LRUHotCache, indexer_scores_many, sparse_attention, topk_select
-    policy = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement]
+    from oracle import indexer_scores_many, sparse_attention, topk_select
     total = 0.0
     units = 0
     for l in layers:
@@ -279,7 +287,7 @@ def oracle_sample(w: wl.Workload, requests, layers, steps: int, replacement: str
             n0 = int(w.contexts()[r])
             qs = [wl.step_query(w, r, l, t) for t in range(steps)]
             app = [wl.step_kv_row(w, r, l, t) for t in range(steps)]
-            cache = policy(w.hot_slots)
+            cache = oracle_cache(w, r, l, replacement)
             t0 = time.perf_counter()
             for t in range(steps):
                 n = n0 + t + 1
@@ -587,8 +595,8 @@ def main():
     ap.add_argument("--fetch-mode", type=int, default=2, choices=[0, 1, 2],
                     help="who copies missed rows: 0 the attention kernel (overlapped), 1 RESOLVE, "
                          "2 chosen per request (default)")
-    ap.add_argument("--replacement", default="lru", choices=["lru", "fifo"],
-                    help="hot-cache replacement: lru (the method's) or fifo (its comparison policy)")
+    ap.add_argument("--replacement", default="lru", choices=["lru", "fifo", "random"],
+                    help="hot-cache replacement: lru (the method's), fifo or random (its comparison policies)")
     ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
     ap.add_argument("--clock-interval-ms", type=int, default=50,
                     help="nvidia-smi clock sampling period during the timed region (0: off)")
@@ -643,8 +651,7 @@ def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
     steps = W + K
     # the oracle replays steps 0..steps-1 of each sampled (request, layer); the
     # first W are the warm-up
-    from oracle import FIFOHotCache, LRUHotCache, indexer_scores_many, sparse_attention, topk_select
-    policy = {"lru": LRUHotCache, "fifo": FIFOHotCache}[args.replacement]
+    from oracle import indexer_scores_many, sparse_attention, topk_select
     per_step = []
     for l in range(sl):
         for r in range(sr):
@@ -652,7 +659,7 @@ def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
             walk = wl.query_walk(w, r, l, steps)
             kv = wl.prefill_kv(w, r, l)
             n0 = int(w.contexts()[r])
-            cache = policy(w.hot_slots)
+            cache = oracle_cache(w, r, l, args.replacement)
             for t in range(steps):
                 q = wl.step_query(w, r, l, t)
                 app = [wl.step_kv_row(w, r, l, u) for u in range(t + 1)]

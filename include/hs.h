@@ -104,12 +104,27 @@ typedef struct hs_config {
                                 policy;
                             HS_REPLACE_FIFO (1): only filled slots get stamp = step, a hit
                                 keeps its fill stamp — first filled first, the comparison
-                                policy of the pages' miss-rate ablation.
+                                policy of the pages' miss-rate ablation;
+                            HS_REPLACE_RANDOM (2): the other comparison policy: never-filled
+                                unpinned slots go first (lowest first), the rest of the
+                                victims are the unpinned filled slots with the smallest
+                                (key, slot), key = the top 23 bits of SplitMix64 (Steele,
+                                Lea and Flood 2014; Vigna's constants) at counter
+                                ((request * n_layers + layer) << 40 | (step mod 2^24) << 16
+                                | slot) + 1 from state replacement_seed, i.e.
+                                z = replacement_seed + (counter + 1) * 0x9E3779B97F4A7C15,
+                                z = (z ^ z >> 30) * 0xBF58476D1CE4E5B9,
+                                z = (z ^ z >> 27) * 0x94D049BB133111EB, z ^= z >> 31,
+                                key = z >> 41 (all mod 2^64): a uniformly random subset;
+                                the victims are filled in ascending slot order; stamps as
+                                for LRU.
                             The attention result does not depend on it. */
+  uint32_t replacement_seed;  /* seed of HS_REPLACE_RANDOM (ignored otherwise) */
 } hs_config_t;
 
 #define HS_REPLACE_LRU 0
 #define HS_REPLACE_FIFO 1
+#define HS_REPLACE_RANDOM 2
 
 typedef struct hs_handle hs_handle_t;
 

@@ -10,6 +10,8 @@ from .hisparse_oracle import (  # noqa: F401
     topk_select,
     LRUHotCache,
     FIFOHotCache,
+    RandomHotCache,
+    splitmix64,
     belady_misses,
     sparse_attention,
     hot_over_full,

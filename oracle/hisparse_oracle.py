@@ -139,8 +139,7 @@ class LRUHotCache:
         t = self.step_no
         hit_slots = {self.page[p] for p in sel if p in self.page}
         misses = [p for p in sel if p not in self.page]
-        candidates = sorted((self.slot_stamp[s], s) for s in range(self.B) if s not in hit_slots)
-        victims = [s for _, s in candidates[:len(misses)]]
+        victims = self._victims(t, hit_slots, len(misses))
         fills = []
         for p, v in zip(misses, victims):
             old = self.slot_pos[v]
@@ -161,6 +160,11 @@ class LRUHotCache:
             "misses": len(misses),
             "fills": fills,
         }
+
+    def _victims(self, t: int, hit_slots: set, m: int) -> list:
+        """The m unpinned slots with the smallest (stamp, slot), in that order."""
+        candidates = sorted((self.slot_stamp[s], s) for s in range(self.B) if s not in hit_slots)
+        return [s for _, s in candidates[:m]]
 
     def snapshot(self, n_positions: int):
         """(page[n_positions], reverse[B], stamp[B], step) as int64 arrays / int."""
@@ -183,6 +187,49 @@ class FIFOHotCache(LRUHotCache):
     """
 
     refresh_hits = False
+
+
+MASK64 = (1 << 64) - 1
+
+
+def splitmix64(state: int, draw: int) -> int:
+    """Output number ``draw`` (1, 2, ...) of SplitMix64 started from ``state``
+    (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+    OOPSLA 2014; increment and finaliser constants of Vigna's reference code):
+    z = state + draw * 0x9E3779B97F4A7C15, then two xor-shift-multiply rounds and a
+    final xor-shift, all modulo 2^64."""
+    z = (state + draw * 0x9E3779B97F4A7C15) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+class RandomHotCache(LRUHotCache):
+    """The same hot cache under random replacement, the other comparison policy of
+    the HiSparse summary's ablation ("论文1：HiSparse": random 16.1 % misses at
+    B = 4096).  The pages give no generator; this one is counter-based so that any
+    implementation reproduces it: at decode call t of (request, layer), slot s gets
+    key = the top 23 bits of splitmix64(seed, counter + 1) with counter =
+    ((request * n_layers + layer) << 40) | ((t mod 2^24) << 16) | s.  Never-filled
+    slots go first (lowest slot first), as under LRU and FIFO; the rest of the m
+    victims are the unpinned filled slots with the smallest (key, slot) — a
+    uniformly random subset of them.  Miss j (ascending position) goes to the j-th
+    victim in ascending slot order.  Stamps as for LRU (they do not steer this
+    policy)."""
+
+    def __init__(self, n_slots: int, *, seed: int, request: int, layer: int, n_layers: int):
+        super().__init__(n_slots)
+        self.seed = int(seed) & MASK64
+        self.rl = int(request) * int(n_layers) + int(layer)
+
+    def key(self, t: int, slot: int) -> int:
+        counter = (self.rl << 40) | ((t & 0xFFFFFF) << 16) | slot
+        return splitmix64(self.seed, counter + 1) >> 41
+
+    def _victims(self, t: int, hit_slots: set, m: int) -> list:
+        ranked = sorted(((0, 0, s) if self.slot_pos[s] < 0 else (1, self.key(t, s), s))
+                        for s in range(self.B) if s not in hit_slots)
+        return sorted(s for *_, s in ranked[:m])
 
 
 # ---------------------------------------------------------------------------

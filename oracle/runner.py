@@ -16,24 +16,28 @@ import numpy as np
 
 import workload as wl
 
-from .hisparse_oracle import (FIFOHotCache, LRUHotCache, belady_misses, indexer_scores_many,
-                              sparse_attention, topk_select)
+from .hisparse_oracle import (FIFOHotCache, LRUHotCache, RandomHotCache, belady_misses,
+                              indexer_scores_many, sparse_attention, topk_select)
 
 
 def replay_request_layer(w: wl.Workload, req: int, layer: int, steps: int | None = None, *,
                          attention_steps=None, kv_prefill: np.ndarray | None = None,
-                         keep_trace: bool = True, replacement: str = "lru") -> dict:
+                         keep_trace: bool = True, replacement: str = "lru", seed: int = 0) -> dict:
     """Oracle results of decode steps 0..steps-1 of one (request, layer).
 
     attention_steps: None (no attention), "all", or an iterable of step numbers
     whose attention outputs are wanted (float64 [H_q, d_v]); replacement: "lru"
-    (the pages' policy) or "fifo" (their comparison policy)."""
+    (the pages' policy), "fifo" or "random" (their comparison policies; seed for
+    the last)."""
     T = w.steps if steps is None else steps
     n0 = int(w.contexts()[req])
     keys = wl.idx_keys_upto(w, req, layer, T)
     walk = wl.query_walk(w, req, layer, T)
     scores = indexer_scores_many(keys, walk)           # [N0+T, T], exact integers
-    cache = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](w.hot_slots)
+    if replacement == "random":
+        cache = RandomHotCache(w.hot_slots, seed=seed, request=req, layer=layer, n_layers=w.n_layers)
+    else:
+        cache = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](w.hot_slots)
     if attention_steps == "all":
         att = set(range(T))
     elif attention_steps is None:

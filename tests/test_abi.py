@@ -55,7 +55,7 @@ def cfg(**over):
     dict(shared_kv=2),
     dict(softmax_scale=-1.0),
     dict(fetch_mode=3),
-    dict(replacement=2),             # neither LRU nor FIFO
+    dict(replacement=3),             # none of LRU, FIFO, random
 ])
 def test_unsupported_configs_are_rejected_before_touching_the_gpu(L, over):
     from tiered_kv_cache_int8_gb300 import hs

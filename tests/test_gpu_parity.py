@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import workload as wl
-from oracle import FIFOHotCache, LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+from oracle import FIFOHotCache, LRUHotCache, RandomHotCache, indexer_scores_many, sparse_attention, topk_select
 from tests.harness import MAX_ABS, REL_L2, StepInputs, attention_error, make_cache, prefill, run_steps
 
 pytestmark = pytest.mark.gpu
@@ -26,12 +26,18 @@ def _gpu():
     yield
 
 
-def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru"):
+def oracle_cache(w, r, l, n_slots, replacement="lru", seed=0):
+    if replacement == "random":
+        return RandomHotCache(n_slots, seed=seed, request=r, layer=l, n_layers=w.n_layers)
+    return {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](n_slots)
+
+
+def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru", seed=0):
     """Per step: (sel, step result, snapshot) from the oracle."""
     keys = wl.idx_keys_upto(w, r, l, steps)
     walk = wl.query_walk(w, r, l, steps)
     scores = indexer_scores_many(keys, walk)
-    cache = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](n_slots or w.hot_slots)
+    cache = oracle_cache(w, r, l, n_slots or w.hot_slots, replacement, seed)
     n0 = int(w.contexts()[r])
     out = []
     for t in range(steps):
@@ -53,8 +59,8 @@ def check_order(order, stamp):
     assert order.tolist() == keys
 
 
-def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement="lru"):
-    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode, replacement=replacement)
+def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement="lru", seed=0):
+    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode, replacement=replacement, replacement_seed=seed)
     prefill(cache, w)
     inp = StepInputs(w, steps)
     got = run_steps(cache, w, inp, steps, collect_meta=True, fused=fused)
@@ -63,7 +69,7 @@ def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement
     for l in range(w.n_layers):
         for r in range(w.n_requests):
             prev_h = prev_m = 0
-            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B, replacement)):
+            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B, replacement, seed)):
                 k_eff = sel.size
                 g_sel = got["sel"][l, t][r]
                 assert np.array_equal(g_sel[:k_eff], sel), f"selection r{r} l{l} t{t}"
@@ -430,20 +436,38 @@ def test_fifo_latent_rows_and_fused_append():
 
 
 def test_replacement_policy_changes_placement_not_the_result():
-    # LRU and FIFO put rows in different slots and miss differently; the
+    # LRU, FIFO and random put rows in different slots and miss differently; the
     # selection and the attention output are bit-identical
     w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=6000, top_k=512,
                          hot_slots=640, steps=6, sigma=0.3)
     runs = []
-    for rep in ("lru", "fifo"):
-        cache = make_cache(w, 6, replacement=rep)
+    for rep in ("lru", "fifo", "random"):
+        cache = make_cache(w, 6, replacement=rep, replacement_seed=99)
         prefill(cache, w)
         runs.append(run_steps(cache, w, StepInputs(w, 6), 6, collect_meta=True))
         cache.close()
-    differ = False
-    for key in runs[0]["out"]:
-        assert np.array_equal(runs[0]["out"][key], runs[1]["out"][key])
-        assert np.array_equal(runs[0]["sel"][key], runs[1]["sel"][key])
-        for a, b in zip(runs[0]["meta"][key], runs[1]["meta"][key]):
-            differ |= not np.array_equal(a[2], b[2])   # stamps
-    assert differ, "the two policies should not leave identical stamps on this trace"
+    for other in runs[1:]:
+        differ = False
+        for key in runs[0]["out"]:
+            assert np.array_equal(runs[0]["out"][key], other["out"][key])
+            assert np.array_equal(runs[0]["sel"][key], other["sel"][key])
+            for a, b in zip(runs[0]["meta"][key], other["meta"][key]):
+                differ |= not np.array_equal(a[1], b[1])   # reverse maps
+        assert differ, "another policy should place rows differently on this trace"
+
+
+@pytest.mark.parametrize("fetch_mode,seed", [(1, 0), (2, 0xC0FFEE)])
+def test_random_replacement_matches_the_oracle(fetch_mode, seed):
+    # the pages' other comparison policy: victims by a counter-based hash (same
+    # generator on both sides); several requests and layers, so the counter's
+    # request and layer fields matter
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=4100, top_k=256,
+                         hot_slots=320, steps=6, sigma=0.3)
+    full_parity(w, 6, fetch_mode=fetch_mode, replacement="random", seed=seed)
+
+
+def test_random_replacement_large_cache_and_latent_rows():
+    # B = 4 k (most victims are free slots at first, then random among filled ones)
+    w = wl.make_workload("mla_128k", n_requests=2, n_layers=1, context=2600, h_q=32, top_k=128,
+                         hot_slots=512, steps=6, sigma=0.3)
+    full_parity(w, 6, fused=True, replacement="random", seed=5)

@@ -40,8 +40,8 @@ std::string check_config(const hs_config_t& c) {
   if (c.hot_slots % 4 != 0) return "hot_slots must be a multiple of 4";
   if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return "softmax_scale must be finite and >= 0";
   if (c.fetch_mode < 0 || c.fetch_mode > 2) return "fetch_mode must be 0, 1 or 2";
-  if (c.replacement != HS_REPLACE_LRU && c.replacement != HS_REPLACE_FIFO)
-    return "replacement must be HS_REPLACE_LRU (0) or HS_REPLACE_FIFO (1)";
+  if (c.replacement != HS_REPLACE_LRU && c.replacement != HS_REPLACE_FIFO && c.replacement != HS_REPLACE_RANDOM)
+    return "replacement must be HS_REPLACE_LRU (0), HS_REPLACE_FIFO (1) or HS_REPLACE_RANDOM (2)";
   if (c.shared_kv == 0) {
     if (c.d_qk != 128 || c.d_v != 128) return "GQA rows: d_qk = d_v = 128 required";
     if (!is_pow2_in(c.h_kv, 1, 8)) return "GQA rows: h_kv must be one of 1, 2, 4, 8";
@@ -440,7 +440,8 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.att_grid = h->num_sms;
   // latent rows are read by every head group's CTAs: RESOLVE pulls them (once)
   p.fetch_mode = h->cfg.shared_kv ? 1 : h->cfg.fetch_mode;
-  p.fifo = h->cfg.replacement == HS_REPLACE_FIFO;
+  p.replacement = h->cfg.replacement;
+  p.replacement_seed = h->cfg.replacement_seed;
 #ifdef HS_WITH_TRACE
   p.trace = h->trace;
 #endif

@@ -99,7 +99,8 @@ struct DecodeParams {
   int att_parts;           // partial results per request (CTAs x slices)
   int att_grid;            // attention CTAs (one per SM)
   int fetch_mode;          // 0: attention kernel fetches misses, 1: RESOLVE does
-  int fifo;                // replacement: 0 LRU (hits refresh their stamp), 1 FIFO (only fills do)
+  int replacement;         // HS_REPLACE_LRU / _FIFO / _RANDOM
+  unsigned int replacement_seed;
 #ifdef HS_WITH_TRACE
   unsigned long long* trace;   // [2][3][1024][64]: clock64 and %globaltimer per (kernel, CTA, point)
 #endif

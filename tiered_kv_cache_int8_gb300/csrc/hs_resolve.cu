@@ -10,8 +10,10 @@
 // Replacement rule: slots holding a selected position (hits) are pinned; the m
 // misses, in ascending position order, go to the m unpinned slots with the
 // smallest (stamp, slot), in that order; every used slot's stamp (LRU), or only
-// every filled slot's (FIFO, the pages' comparison policy), becomes the (request,
-// layer) step counter, which then grows by one.
+// every filled slot's (FIFO, a comparison policy of the pages), becomes the
+// (request, layer) step counter, which then grows by one.  Random replacement (the
+// other comparison policy) takes the m unpinned slots with the smallest
+// counter-based hash keys instead, in ascending slot order, and stamps as LRU.
 //
 // Design (sm_103a), one 1024-thread CTA per request; a latency-bound chain, so
 // every global read the chain needs is issued up front, and the steps between
@@ -110,6 +112,7 @@ __host__ __device__ inline ResLayout res_layout(const Geometry& g) {
 struct ResShared {
   int scan[2 * (RES_THREADS / 32 + 1)];
   int b1, above1, b2, above2, bt, above_t;
+  int rb1, rabove1, rb2, rabove2;   // random replacement: digits of the m-th smallest key
   int N, len, t_step, cnt;
   uint32_t thr;
 };
@@ -139,6 +142,24 @@ __device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* 
     }
   }
   __syncthreads();
+}
+
+// Random replacement's rank of an unpinned slot as a 24-bit value, larger =
+// evicted first (the digit selection scans from the top): never-filled slots
+// 0xFFFFFF (they go first, lowest slot first, as under LRU); a filled slot
+// 0x7FFFFF minus the top 23 bits of SplitMix64 (Steele, Lea and Flood, "Fast
+// splittable pseudorandom number generators", 2014; the finaliser constants of
+// Vigna's reference code) for draw number counter + 1 from state seed, with
+// counter = ((request * n_layers + layer) << 40) | ((step mod 2^24) << 16) | slot.
+__device__ __forceinline__ uint32_t random_ikey(unsigned long long seed, unsigned long long rl, int step, int slot,
+                                                bool empty) {
+  if (empty) return 0xFFFFFFu;
+  const unsigned long long ctr = (rl << 40) | ((unsigned long long)(step & 0xFFFFFF) << 16) | (unsigned)slot;
+  unsigned long long z = seed + (ctr + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return 0x7FFFFFu - (uint32_t)(z >> 41);
 }
 
 }  // namespace
@@ -567,13 +588,66 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     int mb = mc.x;
     for (int i = i0; i < i1; ++i)
       if (slot_sel[i] < 0) miss_i[mb++] = i;
-    // victims: the first m unpinned entries of the LRU list
-    int cb = mc.y;
-    for (int j = j0; j < j1 && cb < m; ++j) {
-      const int sl = ord[j];
-      if (used[sl] == 0) {
-        victim[cb++] = sl;
-        used[sl] = 2;
+    if (p.replacement == HS_REPLACE_RANDOM) {
+      // victims: the m unpinned slots ranked first (never-filled, then smallest
+      // (key, slot)), in ascending slot order.  Two 12-bit digit selections over
+      // the 24-bit ranks (the same histogram scan as the top-k), then each thread
+      // takes its ranks above the threshold and, in slot order, the threshold ties
+      // still needed.  Slots are visited by index (this thread's range j0..j1);
+      // "never filled" is read from the reverse map as it was before this call.
+      if (m > 0) {
+        const unsigned long long seed = p.replacement_seed;
+        auto rank_of = [&](int j) {
+          const int old = L.rev_smem ? rev_s[j] : reverse[j];
+          return random_ikey(seed, rl, t, j, old < 0);
+        };
+        reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) atomicAdd(&h[rank_of(j) >> 12], 1u);
+        __syncthreads();
+        select_digit(h, m, sh.scan, &sh.rb1, &sh.rabove1);
+        const int rb1 = sh.rb1, rab1 = sh.rabove1;
+        reinterpret_cast<uint4*>(h)[tid] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) {
+            const uint32_t k = rank_of(j);
+            if ((int)(k >> 12) == rb1) atomicAdd(&h[k & 4095u], 1u);
+          }
+        __syncthreads();
+        select_digit(h, m - rab1, sh.scan, &sh.rb2, &sh.rabove2);
+        const uint32_t vstar = ((uint32_t)rb1 << 12) | (uint32_t)sh.rb2;
+        const int need_eq = m - rab1 - sh.rabove2;   // >= 1
+        int n_gt = 0, n_eq = 0;
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) {
+            const uint32_t k = rank_of(j);
+            n_gt += k > vstar;
+            n_eq += k == vstar;
+          }
+        const int2 ex = block_exclusive_scan2<RES_THREADS>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+        int eq_rank = ex.y;                        // threshold ties before this thread
+        int o = ex.x + min(ex.y, need_eq);         // victims before this thread
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) {
+            const uint32_t k = rank_of(j);
+            const bool take = k > vstar || (k == vstar && eq_rank++ < need_eq);
+            if (take) {
+              victim[o++] = j;
+              used[j] = 2;
+            }
+          }
+      }
+    } else {
+      // victims: the first m unpinned entries of the (stamp, slot)-sorted list
+      int cb = mc.y;
+      for (int j = j0; j < j1 && cb < m; ++j) {
+        const int sl = ord[j];
+        if (used[sl] == 0) {
+          victim[cb++] = sl;
+          used[sl] = 2;
+        }
       }
     }
     __syncthreads();
@@ -628,8 +702,8 @@ __global__ void __launch_bounds__(RES_THREADS, 1) topk_resolve_kernel(DecodePara
     auto miss_sel = [&](int q) { return miss_i[q] & ~HS_SLOT_MISS_FLAG; };
     const int miss_flag = pull ? 0 : HS_SLOT_MISS_FLAG;
     int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
-    // LRU: every used slot is refreshed; FIFO: only the filled ones (used == 2)
-    const bool fifo = p.fifo != 0;
+    // LRU and random: every used slot is refreshed; FIFO: only the filled ones (used == 2)
+    const bool fifo = p.replacement == HS_REPLACE_FIFO;
     auto refreshed = [&](uint8_t u) { return fifo ? u == 2 : u != 0; };
     for (int i = tid; i < kk; i += RES_THREADS) {
       const int sl = slot_sel[i];
