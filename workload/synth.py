@@ -46,7 +46,7 @@ IDX_CHUNK = 65536        # positions per prefill index-key stream
 @dataclass(frozen=True)
 class Workload:
     name: str
-    config_id: int
+    seed_index: int              # distinct per workload: the default seed is 20260000 + seed_index
     n_requests: int
     n_layers: int
     context: int                 # initial context per request (fixed-length workloads)
@@ -83,7 +83,7 @@ class Workload:
 
     @property
     def base_seed(self) -> int:
-        return self.seed if self.seed is not None else 20260000 + self.config_id
+        return self.seed if self.seed is not None else 20260000 + self.seed_index
 
     def contexts(self) -> np.ndarray:
         """Initial context length of every request (int64 [R])."""
