@@ -1,7 +1,7 @@
 // Sparse attention over the selected rows (GQA, head dim 128), fused with the
-// host fetch of the rows RESOLVE found missing: a persistent, warp-specialised
-// flash-decode kernel whose per-request partial results are merged in a fixed
-// order by the last CTA that touched the request.
+// host fetch of the missed rows RESOLVE left to it: a persistent,
+// warp-specialised flash-decode kernel whose partial results a separate merge
+// kernel (also here) combines in a fixed order.
 //
 // Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
 // for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
@@ -24,10 +24,11 @@
 //    (cp.async.bulk, mbarrier completion) into a row-padded layout (16 extra bytes
 //    per row put the 8 rows of an ldmatrix phase in 8 different bank groups);
 //    up to 3 stages with full/empty mbarriers.
-//  * Warp 9 (fetcher) fills the missed rows of the same unit and stage: it
-//    copies each from the mapped pinned host copy straight into its stage row
-//    with 16-byte cp.async, and the stage's full barrier also waits for those
-//    copies.  Host reads are thus issued at most `stages` units ahead of the
+//  * Warp 9 (fetcher) fills the missed rows of the same unit and stage that
+//    RESOLVE flagged for it (all misses in fetch mode 0; in mode 2 those RESOLVE
+//    did not pull itself): it copies each from the mapped pinned host copy
+//    straight into its stage row with 16-byte cp.async, and the stage's full
+//    barrier also waits for those copies.  Host reads are thus issued at most `stages` units ahead of the
 //    consumers, so the host link serves them roughly in the order the CTAs
 //    consume them instead of in one burst at kernel start.
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.

@@ -28,8 +28,10 @@
 //    segment and added to the request's global histogram when the segment ends.
 //  * Keys at or above the request's candidate threshold (set by the previous
 //    call's top-k) are also appended, with their positions, to a short
-//    per-request list (warp-aggregated atomics), which lets the top-k skip the
-//    full scan when the selection moved little since the previous step.
+//    per-request list (ballot + popcount into per-warp shared-memory buffers,
+//    one global atomic per flush), which lets the top-k skip the full scan when
+//    the selection moved little since the previous step; requests without a
+//    threshold take a separate loop that does none of this.
 //  * Launched as a programmatic dependent: barrier and histogram set-up overlap
 //    the previous kernel's tail.
 #include "hs_internal.cuh"
