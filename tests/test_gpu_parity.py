@@ -4,8 +4,9 @@ tiered_kv_cache_int8_gb300.hs).
 Bit-exact: selected positions, per-step hits and misses, page table, reverse
 map, last-use stamps, step counters.  Attention: max-abs <= 2e-2 and relative
 L2 <= 5e-3 against fp64.  Sizes span several tiles and ragged tails; the edge
-cases (k >= N, empty request, ties, request subsets, bad ids, capacity) are
-covered below; full-size workloads are in test_gpu_full.py.
+cases (k >= N, empty request, ties, request subsets, bad ids, capacity, the
+largest shapes: d_idx 256, k = B = 8192, B = 16384) are covered below; full-size
+workloads are in test_gpu_full.py.
 """
 import numpy as np
 import pytest
@@ -471,3 +472,20 @@ def test_random_replacement_large_cache_and_latent_rows():
     w = wl.make_workload("mla_128k", n_requests=2, n_layers=1, context=2600, h_q=32, top_k=128,
                          hot_slots=512, steps=6, sigma=0.3)
     full_parity(w, 6, fused=True, replacement="random", seed=5)
+
+
+def test_widest_index_keys_and_largest_selection():
+    # the largest shapes the kernels take: d_idx 256 (16 key chunks per position),
+    # top_k 8192 with k = B (every unhit slot a victim), fused append of a 256-byte key
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=20000, d_idx=256, top_k=8192,
+                         hot_slots=8192, steps=3, sigma=0.3)
+    full_parity(w, 3, fused=True)
+
+
+@pytest.mark.parametrize("replacement", ["lru", "random"])
+def test_largest_hot_cache_keeps_the_reverse_map_in_global_memory(replacement):
+    # B = 16384 leaves no room for the reverse map in RESOLVE's shared memory, so
+    # eviction (and the random policy's never-filled test) read it from HBM
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=40000, top_k=2048,
+                         hot_slots=16384, steps=4, sigma=0.3)
+    full_parity(w, 4, replacement=replacement, seed=3)
