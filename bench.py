@@ -153,9 +153,21 @@ class ClockSampler:
                 "window": "timed region" if inside else "whole run (no sample fell inside the timed region)"}
 
 
+def code_hash(path: str) -> str:
+    """First 16 hex digits of the SHA-256 of a source file's code lines: line
+    comments and blank lines are dropped, so an edit of comments alone keeps the
+    hash (and the ncu figures taken on that code)."""
+    code = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            line = line.split("//", 1)[0].strip()
+            if line:
+                code.append(line)
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
+
+
 def kernel_source_hash(name: str) -> str:
-    with open(os.path.join(ROOT, "tiered_kv_cache_int8_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    return code_hash(os.path.join(ROOT, "tiered_kv_cache_int8_gb300", "csrc", name))
 
 
 KERNEL_FILES = {"append": "hs_append.cu", "indexer": "hs_score.cu",

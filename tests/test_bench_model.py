@@ -32,3 +32,15 @@ def test_who_pulls_follows_the_library_rule():
     assert not bench.resolve_pulls(0, False, 1e6, 152)
     assert not bench.resolve_pulls(2, False, 8 * 152, 152)  # at the threshold: attention
     assert bench.resolve_pulls(2, False, 8 * 152 + 1, 152)
+
+
+def test_code_hash_ignores_comments_only(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;   // store\n}\n")
+    h = bench.code_hash(str(a))
+    a.write_text("// a different header\n\n__global__ void k(int* p) {\n  p[0] = 1;\n}\n// tail\n")
+    assert bench.code_hash(str(a)) == h
+    a.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
+    assert bench.code_hash(str(a)) != h
+
