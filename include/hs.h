@@ -146,11 +146,14 @@ typedef struct hs_stats {
 /*
  * hs_create — validate `cfg` and allocate every store (synchronous).
  *   host store  D1: [max_requests][n_layers][max_context][row] bf16, pinned and
- *                   mapped host memory (cudaHostAllocMapped): the authoritative copy;
+ *                   mapped host memory: anonymous memory advised for transparent
+ *                   huge pages and registered with cudaHostRegister (Mapped |
+ *                   Portable), else cudaHostAlloc(Mapped | Portable): the
+ *                   authoritative copy;
  *   hot cache   D2: [max_requests][n_layers][hot_slots][row] bf16 in HBM;
  *   index keys  D3: [max_requests][n_layers][max_context][d_idx] int8 in HBM;
  *   page table  D4: [max_requests][n_layers][max_context] int32, -1 = not resident;
- *   reverse map, last-use stamps, LRU order: [max_requests][n_layers][hot_slots]
+ *   reverse map, stamps, (stamp, slot) order: [max_requests][n_layers][hot_slots]
  *   int32; per-(request, layer) length, step counter, hit and miss counters.
  *   All requests start empty (length 0, every slot empty, step 0).
  * Returns HS_ERR_INVALID (null), HS_ERR_CONFIG (unsupported shape), HS_ERR_OOM
@@ -202,7 +205,8 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
  * Per request with N positions: (1) score every position p < N as
  * sum_j q_idx[j] * K_idx[p][j] (exact int32); (2) keep the k_eff highest, ties
  * to the lower position; (3) RESOLVE: hits via the page table, misses assigned to
- * LRU victim slots, metadata and stamps updated, step += 1, missed rows copied
+ * victim slots of the configured replacement policy (LRU unless set otherwise),
+ * metadata and stamps updated, step += 1, missed rows copied
  * from the host copy into their slots (by RESOLVE or by the attention kernel,
  * see fetch_mode); (4) o_h = sum_i softmax_i(scale * q_h . K_i) V_i over the
  * selected rows in ascending position order, fp32 accumulation, bf16 output.
