@@ -5,7 +5,8 @@ the CPU oracle.
 Every selection of every (request, layer, step) and every (request, layer)'s
 hit and miss totals are compared bit-exactly; the page table, reverse map,
 stamps, LRU order and counters after every step of sampled (request, layer)
-pairs; attention outputs of sampled steps within the fp tolerance.  The oracle
+pairs; attention outputs of sampled steps within the fp tolerance.  The
+comparison replacement policies (FIFO, random) run at full batch size too.  The oracle
 scores all positions in float32 BLAS, exact because every partial sum is an
 integer below 2^24.
 """
@@ -13,7 +14,7 @@ import numpy as np
 import pytest
 
 import workload as wl
-from oracle import LRUHotCache, indexer_scores_many, sparse_attention, topk_select
+from oracle import FIFOHotCache, LRUHotCache, RandomHotCache, indexer_scores_many, sparse_attention, topk_select
 from tests.harness import MAX_ABS, REL_L2, StepInputs, attention_error, make_cache, prefill, run_steps
 
 pytestmark = pytest.mark.gpu
@@ -28,8 +29,8 @@ def _gpu():
     yield
 
 
-def check_full(w, steps, meta_pairs, attn_pairs):
-    cache = make_cache(w, steps)
+def check_full(w, steps, meta_pairs, attn_pairs, replacement="lru", seed=0):
+    cache = make_cache(w, steps, replacement=replacement, replacement_seed=seed)
     prefill(cache, w)
     inp = StepInputs(w, steps)
     got = run_steps(cache, w, inp, steps, fused=True, meta_pairs=meta_pairs)
@@ -39,7 +40,10 @@ def check_full(w, steps, meta_pairs, attn_pairs):
         for r in range(w.n_requests):
             keys = wl.idx_keys_upto(w, r, l, steps)
             scores = indexer_scores_many(keys, wl.query_walk(w, r, l, steps))
-            lru = LRUHotCache(w.hot_slots)
+            if replacement == "random":
+                lru = RandomHotCache(w.hot_slots, seed=seed, request=r, layer=l, n_layers=w.n_layers)
+            else:
+                lru = {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](w.hot_slots)
             hits = misses = 0
             for t in range(steps):
                 n = int(n0[r]) + t + 1
@@ -91,3 +95,12 @@ def test_stress_128k_smallest_B_full():
 def test_mla_128k_full():
     w = wl.WORKLOADS["mla_128k"]   # 32 requests x 2 layers x 128K, latent 576 / 512, 128 heads
     check_full(w, 3, meta_pairs={(0, 0), (31, 1)}, attn_pairs={(0, 1), (17, 0), (31, 1)})
+
+
+@pytest.mark.parametrize("replacement", ["fifo", "random"])
+def test_comparison_policies_full(replacement):
+    # batch 16 x 4 layers x 32K with B a little above k and a fast-moving query, so
+    # every step evicts and the policies choose among several hundred free slots
+    w = wl.make_workload("batch16_32k", hot_slots=2304, sigma=0.3)
+    check_full(w, 4, meta_pairs={(0, 0), (8, 2), (15, 3)}, attn_pairs={(3, 1), (15, 3)},
+               replacement=replacement, seed=2026)
