@@ -330,6 +330,51 @@ def cpu_threads() -> int:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def policy_floor(args, w: wl.Workload, dev_index: int, n_pairs: int = 2, steps: int = 64) -> dict:
+    """Misses of the configured replacement policy against Belady's MIN on the same
+    GPU-selected trace (the floor the pages compare their policies with): a fresh
+    cache of the first n_pairs requests of layer 0 runs `steps` decode steps from
+    cold with the selections read back, outside every timed region."""
+    import torch
+    from tiered_kv_cache_int8_gb300 import HiSparseCache
+    from tiered_kv_cache_int8_gb300.analysis import belady_misses
+    dev = torch.device("cuda", dev_index)
+    R = min(n_pairs, w.n_requests)
+    n0 = w.contexts()[:R]
+    cache = HiSparseCache(n_layers=1, max_requests=R, max_context=int(n0.max()) + steps, h_q=w.h_q, h_kv=w.h_kv,
+                          d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k, hot_slots=w.hot_slots,
+                          shared_kv=w.shared_kv, device=dev_index, fetch_mode=args.fetch_mode,
+                          replacement=args.replacement)
+    try:
+        for r in range(R):
+            n = int(n0[r])
+            kv = torch.from_numpy(wl.prefill_kv(w, r, 0).view(np.int16)).to(dev)
+            keys = torch.from_numpy(wl.prefill_idx_keys(w, r, 0)).to(dev)
+            rid = torch.tensor([r], dtype=torch.int32, device=dev)
+            cache.append(0, kv.view(1, n, w.row_elems), keys.view(1, n, w.d_idx), req_ids=rid)
+            torch.cuda.synchronize(dev)
+        walks = [wl.query_walk(w, r, 0, steps) for r in range(R)]
+        sel = torch.empty((steps, R, w.top_k), dtype=torch.int32, device=dev)
+        for t in range(steps):
+            q_idx = torch.from_numpy(np.stack([walks[r][t] for r in range(R)])).to(dev)
+            q = torch.from_numpy(np.stack([wl.step_query(w, r, 0, t) for r in range(R)]).view(np.int16)).to(dev)
+            new_kv = torch.from_numpy(np.stack([wl.step_kv_row(w, r, 0, t) for r in range(R)]).view(np.int16)).to(dev)
+            new_keys = torch.from_numpy(np.stack([wl.step_idx_key(w, r, 0, t) for r in range(R)])).to(dev)
+            cache.decode_layer(0, q_idx, q, sel_out=sel[t], new_kv=new_kv, new_keys=new_keys)
+        st = cache.stats()
+        trace = sel.cpu().numpy()
+    finally:
+        cache.close()
+    accesses = st["hits"] + st["misses"]
+    floor = 0
+    for r in range(R):
+        floor += belady_misses([trace[t, r][trace[t, r] >= 0] for t in range(steps)], w.hot_slots)
+    return {"policy": args.replacement, "requests": R, "layer": 0, "steps": steps, "from": "cold",
+            "accesses": int(accesses), "misses": int(st["misses"]), "belady_misses": int(floor),
+            "miss_rate": round(st["misses"] / max(1, accesses), 5),
+            "belady_miss_rate": round(floor / max(1, accesses), 5)}
+
+
 def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) -> dict | None:
     import torch
 
@@ -591,6 +636,11 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         "device_error": dev_err,
     }
     cache.close()
+    if args.policy_floor and rank == 0:
+        try:   # a report beside the measurement: it must never cost the bench line
+            out["policy_floor"] = policy_floor(args, w, dev_index)
+        except Exception as e:   # noqa: BLE001
+            out["policy_floor"] = {"error": f"{type(e).__name__}: {e}"}
     return out
 
 
@@ -609,6 +659,9 @@ def main():
                          "2 chosen per request (default)")
     ap.add_argument("--replacement", default="lru", choices=["lru", "fifo", "random"],
                     help="hot-cache replacement: lru (the method's), fifo or random (its comparison policies)")
+    ap.add_argument("--policy-floor", type=int, default=1,
+                    help="1: also report the policy's misses against Belady's MIN on a cold 2-request trace "
+                         "(untimed, after the measurement); 0: skip")
     ap.add_argument("--cpu-sample", default="2x2x100", help="oracle sample: requests x layers x steps")
     ap.add_argument("--clock-interval-ms", type=int, default=50,
                     help="nvidia-smi clock sampling period during the timed region (0: off)")

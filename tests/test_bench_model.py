@@ -44,3 +44,17 @@ def test_code_hash_ignores_comments_only(tmp_path):
     a.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
     assert bench.code_hash(str(a)) != h
 
+
+
+def test_library_belady_equals_the_oracle():
+    # the package's host-side MIN (used by the benchmark's policy-floor leg) and
+    # the oracle's, written separately, agree on random set traces
+    from oracle import belady_misses as oracle_min
+    from tiered_kv_cache_int8_gb300.analysis import belady_misses as lib_min
+    rng = np.random.default_rng(31)
+    for _ in range(300):
+        k = int(rng.integers(1, 7))
+        B = k + int(rng.integers(0, 6))
+        n_pos = int(rng.integers(k, 40))
+        trace = [sorted(rng.choice(n_pos, size=k, replace=False).tolist()) for _ in range(int(rng.integers(1, 20)))]
+        assert lib_min(trace, B) == oracle_min(trace, B)
