@@ -4,8 +4,6 @@ rank's.  No GPU and no data-path collective is involved."""
 import os
 import socket
 
-import pytest
-
 
 def _free_port():
     s = socket.socket()

@@ -4,7 +4,6 @@ import math
 import os
 
 import numpy as np
-import pytest
 
 from oracle import bf16_to_f64, hot_cache_bytes, hot_over_full, sparse_attention
 from tests.conftest import GOLDEN
