@@ -1,6 +1,10 @@
-"""bench.py's algorithmic-traffic model on CPU: the missed rows' host reads and
-slot writes are charged to the kernel that copies them, and totals do not depend
-on which one that is."""
+"""bench.py's host logic on CPU: the algorithmic-traffic model (the missed rows'
+host reads and slot writes are charged to the kernel that copies them, totals do
+not depend on which one that is), the code hash that keys the committed ncu
+figures, the package's Belady MIN against the oracle's, and the reference arm's
+JSON line."""
+import os
+
 import numpy as np
 
 import workload as wl
@@ -58,3 +62,22 @@ def test_library_belady_equals_the_oracle():
         n_pos = int(rng.integers(k, 40))
         trace = [sorted(rng.choice(n_pos, size=k, replace=False).tolist()) for _ in range(int(rng.integers(1, 20)))]
         assert lib_min(trace, B) == oracle_min(trace, B)
+
+
+def test_reference_arm_line_on_cpu():
+    # the reference arm (the oracle, timed on host cores) prints one JSON line with
+    # the contract's keys; tiny workload, a few steps
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+                        "--steps", "2", "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["metric"] and d["unit"] == "layer-steps/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
