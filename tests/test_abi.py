@@ -96,3 +96,21 @@ def test_no_gpu_means_a_cuda_error_not_a_fallback(L):
     with pytest.raises(hs.HsError):
         hs.HiSparseCache(n_layers=1, max_requests=1, max_context=64, h_q=8, h_kv=1, d_qk=128, d_v=128,
                          d_idx=16, top_k=8, hot_slots=8)
+
+
+def test_plain_c_caller(L, tmp_path):
+    # the boundary is plain C: a C99 program compiled against include/hs.h and
+    # linked to libhs.so runs its host-side checks (tests/c/abi_from_c.c)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    lib_dir = os.path.join(ROOT, "tiered_kv_cache_int8_gb300")
+    exe = str(tmp_path / "abi_from_c")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-L", lib_dir, "-lhs",
+                    f"-Wl,-rpath,{lib_dir}", "-o", exe], check=True, capture_output=True, text=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "abi_from_c: ok" in r.stdout
