@@ -289,11 +289,23 @@ int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launch
  * stream capture.  All calls on a device share the array, which keeps the last
  * call's contents: calls that overlap on the GPU (different streams, concurrent
  * replays) race and must be ordered by the caller.  A non-zero status comes with
- * a message in hs_last_error(NULL).
+ * a message in hs_last_error(NULL).  Errors only the GPU can see (a bounded wait
+ * inside the score kernel that gave up) make the call write -1 to every entry
+ * of sel_out and set the device error word that hs_indexer_topk_static_error
+ * reads.
  */
 int hs_indexer_topk_static(int32_t n_req, int32_t n_max, int32_t d_idx, int32_t top_k,
                            const int8_t* idx_keys, const int32_t* lengths, const int8_t* q_idx,
                            int32_t* sel_out, int32_t device, void* stream);
+
+/*
+ * hs_indexer_topk_static_error — synchronise `device` and read the device error
+ * word (HS_DEVERR_* bits) left by the most recent hs_indexer_topk_static call on
+ * it (each call clears the word first).  *out = 0 and HS_OK when no call has run
+ * on the device; HS_ERR_DEVICE (with *out set) when the word is non-zero;
+ * HS_ERR_INVALID for a null `out` or a device out of range.  Allocates nothing.
+ */
+int hs_indexer_topk_static_error(int32_t device, uint32_t* out);
 
 /* hs_last_error — message of the handle's last failed call ("" if none); with
  * h == NULL, the message of the last failed hs_create in this thread. */

@@ -50,6 +50,7 @@ int main(void) {
   CHECK(strcmp(hs_status_string(HS_ERR_CONFIG), "HS_ERR_CONFIG") == 0);
   /* the entry point that allocates nothing rejects bad shapes on the host */
   CHECK(hs_indexer_topk_static(65, 16, 128, 8, NULL, NULL, NULL, NULL, 0, NULL) != HS_OK);
+  CHECK(hs_indexer_topk_static_error(0, NULL) == HS_ERR_INVALID);
   hs_destroy(NULL); /* a no-op */
   if (fails == 0) printf("abi_from_c: ok\n");
   return fails == 0 ? 0 : 1;

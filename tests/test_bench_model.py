@@ -64,6 +64,37 @@ def test_library_belady_equals_the_oracle():
         assert lib_min(trace, B) == oracle_min(trace, B)
 
 
+def _optimal_misses(refs, B):
+    """Fewest misses over every eviction choice (exhaustive; tiny traces only)."""
+    from functools import lru_cache
+
+    @lru_cache(maxsize=None)
+    def best(i, cached):
+        if i == len(refs):
+            return 0
+        p = refs[i]
+        if p in cached:
+            return best(i + 1, cached)
+        if len(cached) < B:
+            return 1 + best(i + 1, cached | {p})
+        return 1 + min(best(i + 1, (cached - {q}) | {p}) for q in cached)
+    return best(0, frozenset())
+
+
+def test_library_belady_equals_an_exhaustive_optimum():
+    # pinned on its own, not only against the oracle: on tiny step-serialised
+    # traces MIN's count equals the minimum over every possible eviction choice
+    from tiered_kv_cache_int8_gb300.analysis import belady_misses as lib_min
+    rng = np.random.default_rng(77)
+    for _ in range(150):
+        k = int(rng.integers(1, 4))
+        B = k + int(rng.integers(0, 3))
+        n_pos = int(rng.integers(k, 8))
+        trace = [sorted(rng.choice(n_pos, size=k, replace=False).tolist()) for _ in range(int(rng.integers(1, 7)))]
+        refs = tuple(p for s in trace for p in s)
+        assert lib_min(trace, B) == _optimal_misses(refs, B)
+
+
 def test_reference_arm_line_on_cpu():
     # the reference arm (the oracle, timed on host cores) prints one JSON line with
     # the contract's keys; tiny workload, a few steps

@@ -7,10 +7,15 @@ A decode step selects a set of positions; the trace is serialised step by step,
 ascending inside a step, and MIN evicts the resident position whose next use is
 farthest (never again = farthest of all).  Any batched schedule of the same
 trace is also a serial one, so this count is a lower bound for every policy.
+
+Formulation: a forward queue of use times per position gives each reference's
+next use as the queue's new head, and the resident positions are kept in a list
+sorted by (next use, position), so the victim is always the list's last entry.
 """
 from __future__ import annotations
 
-import heapq
+from bisect import bisect_left, insort
+from collections import deque
 
 
 def belady_misses(steps, n_slots: int) -> int:
@@ -19,31 +24,25 @@ def belady_misses(steps, n_slots: int) -> int:
     steps: iterable of iterables of positions (each step's selection)."""
     if n_slots < 1:
         raise ValueError("n_slots must be >= 1")
-    refs = []
-    for s in steps:
-        refs.extend(sorted(int(p) for p in s))
-    # next use of every reference, walking backwards
-    upcoming = [0] * len(refs)
-    seen: dict[int, int] = {}
-    never = len(refs)
-    for i in range(len(refs) - 1, -1, -1):
-        p = refs[i]
-        upcoming[i] = seen.get(p, never + i)   # distinct "never again" keys, all beyond the trace
-        seen[p] = i
-    cached: dict[int, int] = {}   # position -> index of its next use
-    farthest: list = []           # max-heap of (-next use, position); stale entries skipped
+    refs = [p for s in steps for p in sorted(int(x) for x in s)]
+    uses: dict[int, deque] = {}
+    for t, p in enumerate(refs):
+        uses.setdefault(p, deque()).append(t)
+    horizon = len(refs)
+    resident: list[tuple[int, int]] = []   # (next use, position), ascending
+    key_of: dict[int, int] = {}            # resident position -> its next use
     misses = 0
-    for i, p in enumerate(refs):
-        if p in cached:
-            cached[p] = upcoming[i]
+    for p in refs:
+        q = uses[p]
+        q.popleft()                                   # this reference
+        nxt = q[0] if q else horizon + p              # never again: beyond the trace, distinct
+        if p in key_of:
+            del resident[bisect_left(resident, (key_of[p], p))]
         else:
             misses += 1
-            if len(cached) == n_slots:
-                while True:
-                    nu, q = heapq.heappop(farthest)
-                    if cached.get(q) == -nu:
-                        del cached[q]
-                        break
-            cached[p] = upcoming[i]
-        heapq.heappush(farthest, (-upcoming[i], p))
+            if len(key_of) == n_slots:
+                _, victim = resident.pop()            # farthest next use
+                del key_of[victim]
+        insort(resident, (nxt, p))
+        key_of[p] = nxt
     return misses

@@ -61,10 +61,12 @@ __device__ __forceinline__ void digit_from_top(const uint32_t* h, int kneed, int
 
 // Exact top-k over the keys the score kernel left in the scratch array (the
 // selection step of the decode path, without the cache update).  One CTA per
-// request; output ascending, ties to the lower position, -1 past k_eff.
+// request; output ascending, ties to the lower position, -1 past k_eff.  When
+// the score kernel recorded an error (a bounded wait gave up, so some keys are
+// missing), every entry becomes -1: no partial selection passes as a result.
 __global__ void __launch_bounds__(RES_THREADS, 1)
     static_topk_kernel(const uint32_t* keys_all, const uint32_t* hist_all, const int32_t* lengths,
-                       long long stride, int top_k, int32_t* sel_out) {
+                       const unsigned int* err, long long stride, int top_k, int32_t* sel_out) {
   __shared__ uint32_t h[IDX_BINS];
   __shared__ TopkShared sh;
   const int tid = threadIdx.x;
@@ -72,6 +74,10 @@ __global__ void __launch_bounds__(RES_THREADS, 1)
   const int K = top_k;
   const int N = lengths[ri];
   int32_t* sel = sel_out + (long long)ri * K;
+  if (*reinterpret_cast<const volatile unsigned int*>(err) != 0u) {
+    for (int i = tid; i < K; i += RES_THREADS) sel[i] = -1;
+    return;
+  }
   if (N <= K) {
     for (int i = tid; i < K; i += RES_THREADS) sel[i] = i < N ? i : -1;
     return;
@@ -216,8 +222,34 @@ extern "C" int hs_indexer_topk_static(int32_t n_req, int32_t n_max, int32_t d_id
     (void)cudaGetLastError();
     return set_static_error(HS_ERR_CUDA, "hs_indexer_topk_static: score launch failed");
   }
-  static_topk_kernel<<<n_req, RES_THREADS, 0, st>>>(dkeys, dhist, dlen, stride, top_k, sel_out);
+  static_topk_kernel<<<n_req, RES_THREADS, 0, st>>>(dkeys, dhist, dlen, derr, stride, top_k, sel_out);
   if (cudaGetLastError() != cudaSuccess)
     return set_static_error(HS_ERR_CUDA, "hs_indexer_topk_static: top-k launch failed");
+  return HS_OK;
+}
+
+extern "C" int hs_indexer_topk_static_error(int32_t device, uint32_t* out) {
+  using namespace hs;
+  if (!out) return set_static_error(HS_ERR_INVALID, "hs_indexer_topk_static_error: null argument");
+  *out = 0;
+  if (device < 0 || device >= ST_MAX_DEVICES)
+    return set_static_error(HS_ERR_INVALID, "hs_indexer_topk_static_error: device out of range");
+  if (g_scratch[device] == nullptr) return HS_OK;   // no call has run on this device
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != device) {
+    if (cudaSetDevice(device) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return set_static_error(HS_ERR_CUDA, "hs_indexer_topk_static_error: cudaSetDevice failed");
+    }
+  }
+  unsigned int word = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(&word, hs_static_scratch, sizeof(word), ST_OFF_ERR, cudaMemcpyDeviceToHost) !=
+          cudaSuccess) {
+    (void)cudaGetLastError();
+    return set_static_error(HS_ERR_CUDA, "hs_indexer_topk_static_error: reading the error word failed");
+  }
+  *out = word;
+  if (word) return set_static_error(HS_ERR_DEVICE, "hs_indexer_topk_static: the last call's kernels set an error");
   return HS_OK;
 }

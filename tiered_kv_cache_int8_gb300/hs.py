@@ -38,7 +38,8 @@ KERNEL_NAMES = ("append", "indexer", "topk_resolve", "attention")
 # the symbols include/hs.h declares
 EXPORTED = ("hs_create", "hs_destroy", "hs_append", "hs_decode_layer", "hs_stats", "hs_snapshot",
             "hs_reset_request", "hs_set_timing", "hs_kernel_times", "hs_last_error",
-            "hs_status_string", "hs_row_elems", "hs_indexer_topk_static")
+            "hs_status_string", "hs_row_elems", "hs_indexer_topk_static",
+            "hs_indexer_topk_static_error")
 
 
 class HsConfig(ctypes.Structure):
@@ -104,6 +105,8 @@ def lib():
         L.hs_row_elems.restype = I32
         L.hs_indexer_topk_static.argtypes = [I32, I32, I32, I32, VP, P(I32), VP, VP, I32, VP]
         L.hs_indexer_topk_static.restype = ctypes.c_int
+        L.hs_indexer_topk_static_error.argtypes = [I32, P(ctypes.c_uint32)]
+        L.hs_indexer_topk_static_error.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -140,6 +143,16 @@ def indexer_topk_static(idx_keys, lengths, q_idx, top_k: int, sel_out=None, stre
     if rc != HS_OK:
         raise HsError(rc, lib().hs_last_error(None).decode())
     return sel_out
+
+
+def indexer_topk_static_error(device: int = 0) -> int:
+    """Device error word (HS_DEVERR_* bits) of the last indexer_topk_static call
+    on `device` (synchronises the device)."""
+    w = ctypes.c_uint32(0)
+    rc = lib().hs_indexer_topk_static_error(device, ctypes.byref(w))
+    if rc not in (HS_OK, HS_ERR_DEVICE):
+        raise HsError(rc, lib().hs_last_error(None).decode())
+    return int(w.value)
 
 
 class HiSparseCache:
