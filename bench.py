@@ -169,8 +169,7 @@ def kernel_source_hash(name: str) -> str:
     return code_hash(os.path.join(ROOT, "tiered_kv_cache_int8_gb300", "csrc", name))
 
 
-KERNEL_FILES = {"append": "hs_append.cu", "indexer": "hs_score.cu",
-                "topk_resolve": "hs_resolve.cu", "attention": "hs_attention.cu"}
+KERNEL_FILES = {"append": "hs_append.cu", "select": "hs_select.cu", "attention": "hs_attention.cu"}
 
 
 def host_store_pages(host_bytes: int) -> dict:
@@ -221,37 +220,37 @@ def ncu_traffic(kernel: str, workload: str, latent: bool = False):
 
 def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_pulls: bool = False) -> dict:
     """HBM and host-link bytes the method itself moves for one layer-step of all
-    requests.  n_ctx: context length of each request at this step; misses: rows
-    pulled from host memory in this layer-step (all requests); resolve_pulls: the
-    missed rows are copied (host read, slot write) by the top-k + RESOLVE kernel
-    rather than by the attention kernel."""
+    requests, per kernel.  n_ctx: context length of each request at this step;
+    misses: rows pulled from host memory in this layer-step (all requests);
+    resolve_pulls: the missed rows are copied (host read, slot write) by RESOLVE
+    inside the select kernel rather than by the attention kernel.
+
+    select: the index-key scan and query (the indexer), then per request the
+    selection, slot and page-table reads/writes (16 B per selected position), the
+    stamp/reverse scan (8 B per slot), 12 B of metadata per miss, and the appended
+    token (its row read from HBM and written to the host copy, its key).
+    attention: every selected row, its slot, the queries and the outputs."""
     k_eff = np.minimum(w.top_k, n_ctx)
     R = w.n_requests
     row = w.row_bytes
-    # the new token's append rides on the decode call (top-k/RESOLVE kernel):
-    # its row is read from HBM and written to the host copy, its key to HBM
     hbm = {
         "append": 0.0,
-        "indexer": float((n_ctx * w.d_idx).sum()) + R * w.d_idx,
-        "topk_resolve": float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12
+        "select": float((n_ctx * w.d_idx).sum()) + R * w.d_idx
+        + float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12
         + R * (w.row_bytes + 2 * w.d_idx + 4),
         "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2,
     }
-    link = {"append": 0.0, "indexer": 0.0, "topk_resolve": R * row, "attention": 0.0}
-    puller = "topk_resolve" if resolve_pulls else "attention"
+    link = {"append": 0.0, "select": R * row, "attention": 0.0}
+    puller = "select" if resolve_pulls else "attention"
     hbm[puller] += misses * row    # the slot writes
     link[puller] += misses * row   # the host reads
     return {"hbm": hbm, "link": link}
 
 
-def resolve_pulls(fetch_mode: int, shared_kv: bool, misses_per_layer_step: float, n_sms: int) -> bool:
-    """Which kernel copies the missed rows: mode 1 and latent rows always RESOLVE;
-    mode 2 RESOLVE when the misses exceed 8 rows per attention CTA (the library's
-    per-request rule, applied to the average request), else mostly the attention
-    kernel; mode 0 the attention kernel."""
-    if shared_kv or fetch_mode == 1:
-        return True
-    return fetch_mode == 2 and misses_per_layer_step > 8 * n_sms
+def resolve_pulls(fetch_mode: int, shared_kv: bool) -> bool:
+    """Which kernel copies the missed rows: RESOLVE (in the select kernel) for
+    fetch mode 1 and for latent rows, else the attention kernel's loader."""
+    return shared_kv or fetch_mode == 1
 
 
 def graph_upload(g, stream) -> bool:
@@ -516,7 +515,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     st2 = cache.stats()
     misses_b = st2["misses"] - st1["misses"]
     hits_b = st2["hits"] - st1["hits"]
-    n_launch_per_step = L * 4
+    n_launch_per_step = L * (3 if w.shared_kv else 2)   # select + attention (+ merge for latent rows)
 
     # ---- e2e through the API: host inputs in, host outputs out, every step ------------
     E = args.e2e_steps
@@ -562,7 +561,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         hb = {k: 0.0 for k in KERNEL_FILES}
         lb = {k: 0.0 for k in KERNEL_FILES}
         m_ls = n_miss / (K * L)
-        rp = resolve_pulls(args.fetch_mode, w.shared_kv, m_ls, n_sms)
+        rp = resolve_pulls(args.fetch_mode, w.shared_kv)
         for t in range(t_begin, t_begin + K):
             ab = algorithmic_bytes(w, n0 + t + 1, m_ls, rp)
             for k in KERNEL_FILES:
@@ -619,8 +618,9 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
             roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak_hbm, "unit": "GB/s",
                     "frac": round(ach / peak_hbm, 4), "peak_source": peak_src,
                     "traffic": ncu_traffic(dom, w.name, w.shared_kv), "bytes_per_launch": kd["hbm_bytes_per_launch"]}
-    # the attention entry also launches the partial-merge kernel
-    gpu_launches = sum(v["launches"] for v in kernels.values()) + kernels.get("attention", {}).get("launches", 0)
+    # latent rows: the attention entry also launches the partial-merge kernel
+    gpu_launches = sum(v["launches"] for v in kernels.values()) + (
+        kernels.get("attention", {}).get("launches", 0) if w.shared_kv else 0)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -86,13 +86,12 @@ typedef struct hs_config {
   float softmax_scale;   /* 0 => 1/sqrt(d_qk) */
   int32_t device;        /* CUDA device ordinal */
   int32_t fetch_mode;    /* where missed rows are copied host -> HBM (results identical):
-                            0 = by a loader warp of the attention kernel, overlapping the
-                                HBM reads of the hit rows (best with few misses per
-                                attention CTA);
-                            1 = inside the RESOLVE kernel, before attention starts;
-                            2 = chosen per request: RESOLVE pulls when the request's
-                                misses times n_req exceed 8 rows per attention CTA,
-                                else the attention kernel (the Python binding's default).
+                            0 = by the loader warp of the attention kernel, into its stage
+                                and from there into the slot, overlapping the HBM reads of
+                                the hit rows;
+                            1 = by RESOLVE (inside the select kernel), before the request
+                                is handed to the attention kernel;
+                            2 = the default: as 0.
                             RESOLVE starts every missed row moving into L2 as soon as
                             it finds it, whichever copies it.
                             Latent rows (shared_kv = 1) always use 1: every head
@@ -160,7 +159,11 @@ typedef struct hs_stats {
  * (allocation failed; nothing stays allocated) or HS_ERR_CUDA.  On success
  * *out owns everything until hs_destroy.  The environment variable
  * HS_FAULT_INJECT=hostalloc|devalloc makes the first host / device allocation
- * fail (to test the clean-up path).
+ * fail (to test the clean-up path); HS_FAULT_INJECT=noready (read here) makes
+ * every hs_decode_layer of the handle withhold the publication of its first
+ * request, so the attention kernel's bounded wait for it runs out (after about
+ * a second): the call sets HS_DEVERR_TIMEOUT, that request's output is
+ * undefined, and the handle must be destroyed (to test the timeout path).
  */
 int hs_create(const hs_config_t* cfg, hs_handle_t** out);
 
@@ -186,10 +189,13 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
 
 /*
  * hs_decode_layer — one decode layer-step for n_req requests (stream-ordered,
- * no host synchronisation, capturable in a CUDA graph).  Its score, attention
- * and merge kernels are launched as programmatic dependents: each waits for the
- * previous kernel of the stream before it reads anything, so ordering against
- * earlier stream work is the usual one.
+ * no host synchronisation, capturable in a CUDA graph).  Two kernels: the select
+ * kernel (scores, top-k, RESOLVE) waits for the previous kernel of the stream
+ * before it reads anything; the attention kernel is launched as its
+ * programmatic dependent and starts on each request as soon as that request is
+ * resolved, and completes only after the select kernel has.  So ordering against
+ * earlier and later stream work is the usual one.  At most 16 requests are
+ * resolved at a time (one resolver CTA each); the rest of the GPU scores.
  *   req_ids     : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
  *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned)
  *   q           : dev bf16 [n_req][h_q][d_qk]   attention query
@@ -249,16 +255,18 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream);
 
 /*
  * hs_set_timing / hs_kernel_times — per-kernel device timing.  With timing on,
- * every launch is bracketed by CUDA events on the caller's stream; hs_kernel_times
+ * every launch is bracketed by CUDA events on the caller's stream (so the
+ * attention kernel no longer starts while the select kernel still runs: the
+ * times are those of each kernel alone); hs_kernel_times
  * synchronises and returns, per kernel kind (HS_K_*), the summed milliseconds and
  * the number of launches since the last hs_set_timing(h, 1).
  */
-#define HS_K_APPEND 0        /* append kernel */
-#define HS_K_INDEXER 1       /* scores of every position + first-digit histogram */
-#define HS_K_TOPK_RESOLVE 2  /* exact top-k + RESOLVE (and the host fetch when fetch_mode = 1) */
-#define HS_K_ATTENTION 3     /* attention + merge of its split partials (and the host fetch
-                                when fetch_mode = 0) */
-#define HS_K_COUNT 4
+#define HS_K_APPEND 0     /* append kernel (hs_append) */
+#define HS_K_SELECT 1     /* the select kernel of hs_decode_layer: scores, exact top-k and RESOLVE
+                             (and the host fetch when fetch_mode = 1 or rows are latent) */
+#define HS_K_ATTENTION 2  /* attention with the merge of its partials (and the host fetch when
+                             fetch_mode = 0 or 2); latent rows: attention + merge kernels */
+#define HS_K_COUNT 3
 int hs_set_timing(hs_handle_t* h, int32_t enable);
 int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launches /*[HS_K_COUNT]*/);
 

@@ -17,25 +17,25 @@ def test_pulled_rows_are_charged_to_the_copying_kernel():
     a = bench.algorithmic_bytes(w, n_ctx, 700.0, resolve_pulls=False)
     b = bench.algorithmic_bytes(w, n_ctx, 700.0, resolve_pulls=True)
     moved = 700.0 * w.row_bytes
-    assert b["link"]["topk_resolve"] - a["link"]["topk_resolve"] == moved
+    assert b["link"]["select"] - a["link"]["select"] == moved
     assert a["link"]["attention"] - b["link"]["attention"] == moved
-    assert b["hbm"]["topk_resolve"] - a["hbm"]["topk_resolve"] == moved
+    assert b["hbm"]["select"] - a["hbm"]["select"] == moved
     for kind in ("hbm", "link"):
         assert np.isclose(sum(a[kind].values()), sum(b[kind].values()))
-    # the index scan reads every key once; the attention every selected row once
-    # (with RESOLVE copying the misses, nothing else)
-    assert a["hbm"]["indexer"] == float((n_ctx * w.d_idx).sum()) + w.n_requests * w.d_idx
+    # the index scan reads every key once (it dominates the select kernel's bytes);
+    # the attention every selected row once (with RESOLVE copying the misses,
+    # nothing else)
+    assert a["hbm"]["select"] >= float((n_ctx * w.d_idx).sum()) + w.n_requests * w.d_idx
     k_eff = np.minimum(w.top_k, n_ctx).sum()
     assert b["hbm"]["attention"] == float(k_eff) * (w.row_bytes + 4) + w.n_requests * w.h_q * (w.d_qk + w.d_v) * 2
 
 
 def test_who_pulls_follows_the_library_rule():
     import bench
-    assert bench.resolve_pulls(1, False, 0.0, 152)
-    assert bench.resolve_pulls(0, True, 0.0, 152)          # latent rows: always RESOLVE
-    assert not bench.resolve_pulls(0, False, 1e6, 152)
-    assert not bench.resolve_pulls(2, False, 8 * 152, 152)  # at the threshold: attention
-    assert bench.resolve_pulls(2, False, 8 * 152 + 1, 152)
+    assert bench.resolve_pulls(1, False)
+    assert bench.resolve_pulls(0, True)          # latent rows: always RESOLVE
+    assert not bench.resolve_pulls(0, False)
+    assert not bench.resolve_pulls(2, False)     # the default: the attention kernel
 
 
 def test_code_hash_ignores_comments_only(tmp_path):
@@ -112,3 +112,24 @@ def test_reference_arm_line_on_cpu():
     assert d["metric"] and d["unit"] == "layer-steps/s" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_bench_names_resolve():
+    # every module-level name bench.py uses is defined (catches a helper lost in an edit)
+    import ast
+    import builtins
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    tree = ast.parse(open(os.path.join(root, "bench.py")).read())
+    defined = {n.name for n in tree.body if isinstance(n, (ast.FunctionDef, ast.ClassDef))}
+    for n in tree.body:
+        if isinstance(n, ast.Assign):
+            defined |= {t.id for t in n.targets if isinstance(t, ast.Name)}
+    for n in ast.walk(tree):   # imports, also those inside functions
+        if isinstance(n, (ast.Import, ast.ImportFrom)):
+            defined |= {(a.asname or a.name).split(".")[0] for a in n.names}
+    called = {c.func.id for c in ast.walk(tree) if isinstance(c, ast.Call) and isinstance(c.func, ast.Name)}
+    local = {a.arg for f in ast.walk(tree) if isinstance(f, (ast.FunctionDef, ast.Lambda)) for a in f.args.args}
+    local |= {t.id for a in ast.walk(tree) if isinstance(a, ast.Assign) for t in a.targets if isinstance(t, ast.Name)}
+    local |= {f.name for f in ast.walk(tree) if isinstance(f, ast.FunctionDef)}
+    missing = sorted(c for c in called if c not in defined and c not in local and not hasattr(builtins, c))
+    assert not missing, missing

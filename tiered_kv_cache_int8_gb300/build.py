@@ -18,7 +18,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhs.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["hs_api.cu", "hs_append.cu", "hs_score.cu", "hs_resolve.cu", "hs_attention.cu", "hs_attention_mla.cu", "hs_static.cu"]
+SOURCES = ["hs_api.cu", "hs_append.cu", "hs_score.cu", "hs_select.cu", "hs_attention.cu", "hs_attention_mla.cu",
+           "hs_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/hs.h: configuration checks,
 // allocation of the two memory tiers and the cache metadata, argument checks
 // and kernel launches, counters, snapshots and optional per-kernel timing.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -80,12 +81,13 @@ void free_all(hs_handle* h) {
 }
 
 struct FaultInject {
-  bool host = false, dev = false;
+  bool host = false, dev = false, noready = false;
   FaultInject() {
     const char* v = std::getenv("HS_FAULT_INJECT");
     if (v) {
       host = std::strcmp(v, "hostalloc") == 0;
       dev = std::strcmp(v, "devalloc") == 0;
+      noready = std::strcmp(v, "noready") == 0;
     }
   }
 };
@@ -220,14 +222,14 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
 
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
   h->score_stride = ((long long)cfg->max_context + 3) & ~3LL;
-  h->idx_smem = hs::score_smem_bytes(g);
-  h->res_smem = hs::resolve_smem_bytes(g);
+  h->sel_smem = hs::select_smem_bytes(g);
   h->att_smem = hs::attention_smem_bytes(g);
   h->att_parts = hs::attention_parts(g);
-  if (h->idx_smem > (size_t)smem_optin)
-    return fail_free(HS_ERR_CONFIG, "hs_create: max_requests too large for the score kernel's shared memory");
-  if (h->res_smem > (size_t)smem_optin)
-    return fail_free(HS_ERR_CONFIG, "hs_create: top_k / hot_slots too large for RESOLVE's shared memory");
+  if (h->num_sms < 2)
+    return fail_free(HS_ERR_CONFIG, "hs_create: the select kernel needs at least two SMs");
+  if (h->sel_smem > (size_t)smem_optin)
+    return fail_free(HS_ERR_CONFIG,
+                     "hs_create: top_k / hot_slots / max_requests too large for the select kernel's shared memory");
   if (h->att_smem > (size_t)smem_optin)
     return fail_free(HS_ERR_CONFIG,
                      "hs_create: rows or max_requests too large for the attention kernel's shared memory");
@@ -239,6 +241,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   h->index_bytes = R * Lr * N * (size_t)g.d_idx;
 
   FaultInject fi;
+  h->fault = fi.noready ? 1 : 0;
   // D1: authoritative copy in pinned, mapped host memory
   if (fi.host) return fail_free(HS_ERR_OOM, "hs_create: pinned host allocation failed (injected)");
   // Anonymous memory advised for transparent huge pages, then pinned and mapped:
@@ -307,6 +310,12 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.att_nparts, R * 8 * 4, false},
       {(void**)&s.call_n, R * 4, false},
       {(void**)&s.app_counter, R * 4, false},
+      {(void**)&s.tiles_done, R * 4, false},
+      {(void**)&s.ready, R * 4, false},
+      {(void**)&s.kk_pub, R * 4, false},
+      {(void**)&s.chunk_done, R * 4, false},
+      {(void**)&s.merge_done, R * 4, false},
+      {(void**)&s.sync, 16, false},
 #ifdef HS_WITH_TRACE
       {(void**)&h->trace, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8, false},
 #endif
@@ -339,14 +348,19 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.cand_thr, 0, R * Lr * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.cand_cnt, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.tiles_done, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.ready, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.kk_pub, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.chunk_done, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.merge_done, 0, R * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.sync, 0, 16) == cudaSuccess;
 #ifdef HS_WITH_TRACE
   ok = ok && cudaMemset(h->trace, 0, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8) ==
                  cudaSuccess;
 #endif
   ok = ok && hs::launch_init_order(s.order, (long long)(R * Lr), (int)B, 0) == cudaSuccess;
   if (!ok) return fail_free(HS_ERR_CUDA, "hs_create: initialising the metadata failed");
-  if ((e = hs::prepare_score(g, h->idx_smem)) != cudaSuccess ||
-      (e = hs::prepare_resolve(h->res_smem)) != cudaSuccess ||
+  if ((e = hs::prepare_select(g, h->sel_smem)) != cudaSuccess ||
       (e = hs::prepare_attention(g, h->att_smem)) != cudaSuccess)
     return fail_free(HS_ERR_CUDA, std::string("hs_create: kernel set-up failed: ") + cudaGetErrorName(e));
   e = cudaDeviceSynchronize();
@@ -439,17 +453,19 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.att_parts = h->att_parts;
   p.att_grid = h->num_sms;
   // latent rows are read by every head group's CTAs: RESOLVE pulls them (once)
-  p.fetch_mode = h->cfg.shared_kv ? 1 : h->cfg.fetch_mode;
+  p.fetch_mode = h->cfg.shared_kv ? 1 : (h->cfg.fetch_mode == 1 ? 1 : 0);
   p.replacement = h->cfg.replacement;
   p.replacement_seed = h->cfg.replacement_seed;
+  p.sel_grid = h->num_sms;
+  p.n_resolvers = std::min(std::min(n_req, hs::SEL_MAX_RESOLVERS), h->num_sms - 1);
+  p.publish = h->cfg.shared_kv ? 0 : 1;   // the chunked GQA kernel starts on published requests
+  p.fault = h->fault;
 #ifdef HS_WITH_TRACE
   p.trace = h->trace;
 #endif
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = timed_launch(h, HS_K_INDEXER, st, [&] { return hs::launch_score(p, h->idx_smem, st); });
-  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: indexer launch");
-  e = timed_launch(h, HS_K_TOPK_RESOLVE, st, [&] { return hs::launch_resolve(p, h->res_smem, st); });
-  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: top-k/RESOLVE launch");
+  cudaError_t e = timed_launch(h, HS_K_SELECT, st, [&] { return hs::launch_select(p, h->sel_smem, st); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: select launch");
   e = timed_launch(h, HS_K_ATTENTION, st, [&] { return hs::launch_attention(p, h->att_smem, st); });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: attention launch");
   ++h->decode_calls;

@@ -1,7 +1,8 @@
 // Sparse attention over the selected rows (GQA, head dim 128), fused with the
-// host fetch of the missed rows RESOLVE left to it: a persistent,
-// warp-specialised flash-decode kernel whose partial results a separate merge
-// kernel (also here) combines in a fixed order.
+// host fetch of the missed rows RESOLVE left to it and with the merge of its
+// split partials: a persistent, warp-specialised flash-decode kernel that works
+// through a queue of chunks and merge tasks while the select kernel is still
+// resolving later requests.  (The merge kernel further down serves latent rows.)
 //
 // Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
 // for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
@@ -11,42 +12,39 @@
 // by the cache, so the result must not depend on where the rows sit; missed rows
 // come from the authoritative copy in pinned host memory.
 //
-// Design (sm_103a).  The kernel is HBM-bound (each K/V byte is used by the
-// h_q / h_kv query heads of its group only), so the goal is to keep enough
-// bytes in flight on every SM with as few instructions per byte as possible,
-// and to keep the host-link latency of missed rows off the critical path:
-//  * Persistent grid, one CTA per SM.  The selected rows of all requests are
-//    flattened into units of TILE rows (16 rows per warp slice); CTA c takes
-//    units [c*U/G, (c+1)*U/G).  The split depends only on the k_eff of each
-//    request and on the grid size, never on B or on slot placement.
-//  * Warp 8 (stager) copies every hit row of a unit (all kv heads: one
-//    contiguous hot slot) HBM -> shared memory with one 1-D bulk async copy
-//    (cp.async.bulk, mbarrier completion) into a row-padded layout (16 extra bytes
-//    per row put the 8 rows of an ldmatrix phase in 8 different bank groups);
-//    up to 3 stages with full/empty mbarriers.
-//  * Warp 9 (fetcher) fills the missed rows of the same unit and stage that
-//    RESOLVE flagged for it (all misses in fetch mode 0; in mode 2 those RESOLVE
-//    did not pull itself): it copies each from the mapped pinned host copy
-//    straight into its stage row with 16-byte cp.async, and the stage's full
-//    barrier also waits for those copies.  Host reads are thus issued at most `stages` units ahead of the
-//    consumers, so the host link serves them roughly in the order the CTAs
-//    consume them instead of in one burst at kernel start.
+// Design (sm_103a).  HBM-bound (each K/V byte is used by the h_q / h_kv query
+// heads of its group only):
+//  * Persistent grid, one CTA per SM, launched as a programmatic dependent of
+//    the select kernel and started on the SMs its scorers free.  Work items form
+//    one queue, taken with a global atomic counter: for each request, its chunks
+//    (64 selected rows, in selection order), and one request later its merge
+//    tasks (8 heads each).  Requests are published in about queue order, so a
+//    CTA rarely waits; a chunk waits (bounded) for its request's ready flag, a
+//    merge task for its request's chunk counter.  Every wait is on an item
+//    earlier in the queue, and every CTA runs its items in queue order, so the
+//    waits always end.
+//  * Warp 8 (loader) reads the slots of a unit (16 rows per warp slice) and
+//    copies every hit row (all kv heads: one contiguous hot slot) HBM -> shared
+//    memory with one 1-D bulk async copy into a row-padded layout (16 extra bytes
+//    per row put the 8 rows of an ldmatrix phase in 8 bank groups), and every
+//    missed row from the mapped pinned host copy with 16-byte cp.async (RESOLVE
+//    already started those rows moving into L2); up to 3 stages, full/empty
+//    mbarriers, a descriptor per stage.
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
 //    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
-//    with the group's query heads as the 16 M rows (zero-padded): the tensor
-//    cores cut the instruction count per byte; K and V fragments come straight
-//    from shared memory with ldmatrix (.trans for V).  Online softmax in fp32
-//    (exp2, scale * log2(e) applied to the fp32 scores); P enters the second
-//    product as bf16.  Consumer warp 0 also writes each fetched row into its hot
-//    slot (bulk shared -> global copy), so later steps hit.
-//  * Every (CTA, request, slice) writes a partial (m, l, o) to scratch; a small
-//    merge kernel (launched as a programmatic dependent, so its CTAs are already
-//    resident beside the attention CTAs when those finish) combines each head's
-//    partials in part order and writes bf16.  Rows are visited in ascending
-//    selection order and the merge order is fixed, so the output is
-//    bit-identical for any B.
-//  * Launched as a programmatic dependent: barrier set-up overlaps the previous
-//    kernel's tail; everything else waits for it.
+//    with the group's query heads as the 16 M rows (zero-padded); K and V
+//    fragments come from shared memory with ldmatrix (.trans for V).  Online
+//    softmax in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P enters
+//    the second product as bf16.  Consumer warp 0 writes each fetched row into its
+//    hot slot (bulk shared -> global copy), so later steps hit.
+//  * Each (chunk, slice) writes a partial (m, l, o); a merge task combines its
+//    heads' partials in chunk order and writes bf16.  Rows are visited in
+//    ascending selection order and chunks depend only on k_eff, so the output is
+//    bit-identical for any B and any schedule.
+//  * Counters of the call reset themselves: the last merge task of a request
+//    clears its flags, the last CTA to leave clears the queue.  Each CTA waits
+//    for the select kernel to complete before it exits, so the next launch on the
+//    stream sees both kernels finished.
 #include <cuda_bf16.h>
 
 #include "hs_internal.cuh"
@@ -57,37 +55,50 @@ namespace {
 
 constexpr int D = 128;
 constexpr int NCONS = 8;                   // consumer warps
-constexpr int STAGER = NCONS;              // warp index of the stager
-constexpr int FETCHER = NCONS + 1;         // warp index of the host fetcher
-constexpr int THREADS = (NCONS + 2) * 32;
+constexpr int LOADER = NCONS;              // warp index of the loader
+constexpr int THREADS = (NCONS + 1) * 32;
 constexpr int MAX_STAGES = 3;
 constexpr int TILE_MAX = 128;   // rows of a unit at h_kv = 1 (8 slices of 16)
+constexpr int CHUNK_ROWS_MIN = 64;
+constexpr int MERGE_HEADS = 8;
+constexpr int BAR_CONS = 1;     // named barrier: the 256 consumer threads
+constexpr int BAR_VOTE = 2;     // named barrier: the consumers' vote on a failed wait
+
+enum { DESC_UNIT = 0, DESC_MERGE = 1, DESC_STOP = 2 };
+struct __align__(16) Desc {
+  int type, ri, c, row0, nr, first, last, pad;
+};
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+__host__ __device__ inline int att_tile(const Geometry& g) { return ATT_SUBTILE * (NCONS / g.h_kv); }
+__host__ __device__ inline int att_chunk_rows(const Geometry& g) {
+  const int t = att_tile(g);
+  return t >= CHUNK_ROWS_MIN ? t : (CHUNK_ROWS_MIN / t) * t;
+}
+__host__ __device__ inline int att_nchunk(const Geometry& g) {
+  return (g.top_k + att_chunk_rows(g) - 1) / att_chunk_rows(g);
+}
+
 struct AttLayout {
-  size_t bar, slot_tab, prefix, rowc, stage, stage_bytes, total;
+  size_t bar, desc, slot_tab, stage, stage_bytes, total;
 };
 
-constexpr int ROWCACHE = 2048;   // (slot, position) pairs of the CTA's rows kept in shared memory
-
-// Shared memory: barriers | per-stage hot slots of fetched rows | per-request
-// tables | row cache | stages.
+// Shared memory: barriers | per-stage descriptors | per-stage hot slots of
+// fetched rows | stages.
 __host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage) {
   AttLayout L;
-  const int nslice = NCONS / g.h_kv;
-  const int tile = ATT_SUBTILE * nslice;
+  const int tile = att_tile(g);
   const size_t row_stride = (size_t)g.row_bytes + ATT_ROW_PAD;
   size_t off = 0;
   L.bar = off;
   off += 8 * (2 * MAX_STAGES) + 16;   // full/empty barriers, abort flag
   off = align_up(off, 128);
+  L.desc = off;
+  off += sizeof(Desc) * MAX_STAGES;
   L.slot_tab = off;
   off += (size_t)MAX_STAGES * TILE_MAX * 4;   // hot slot of each fetched row (-1: none)
-  L.prefix = off;
-  off += align_up((size_t)(g.max_requests + 1) * 4 * 3, 128);   // unit prefix, k_eff, request id
-  L.rowc = off;
-  off += (size_t)ROWCACHE * 8;
+  off = align_up(off, 128);
   L.stage = off;
   L.stage_bytes = align_up((size_t)tile * row_stride, 128);
   off += (size_t)nstage * L.stage_bytes;
@@ -144,14 +155,14 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 
 // Bounded wait that also gives up once another warp has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              unsigned int* err) {
+                                              unsigned int* err, unsigned long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+      if (global_timer_ns() - t0 > limit) {
         *abort_flag = 1;
         set_error(err, HS_DEVERR_TIMEOUT);
         return false;
@@ -160,22 +171,47 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// CTA owning flattened unit u when U units are split over G CTAs as [c*U/G, (c+1)*U/G).
-__device__ __forceinline__ int owner_of(long long u, long long U, int G) {
-  return (int)(((u + 1) * G + U - 1) / U) - 1;
+// Work item i of the queue [chunks of r0][chunks of r1, merges of r0] ...
+// [chunks of r_{n-1}, merges of r_{n-2}][merges of r_{n-1}].
+struct Item {
+  int merge, ri, idx;
+};
+__device__ __forceinline__ Item decode_item(long long i, int n_req, int nchk, int nmt) {
+  Item it;
+  if (i < nchk) {
+    it.merge = 0;
+    it.ri = 0;
+    it.idx = (int)i;
+    return it;
+  }
+  const long long per = nchk + nmt;
+  const long long i2 = i - nchk;
+  const int b = 1 + (int)(i2 / per);
+  const int o = (int)(i2 % per);
+  if (b == n_req) {
+    it.merge = 1;
+    it.ri = n_req - 1;
+    it.idx = o;
+  } else if (o < nchk) {
+    it.merge = 0;
+    it.ri = b;
+    it.idx = o;
+  } else {
+    it.merge = 1;
+    it.ri = b - 1;
+    it.idx = o - nchk;
+  }
+  return it;
 }
 
 }  // namespace
 
 int attention_parts(const Geometry& g) {
   if (g.shared_kv) return mla_parts(g);
-  const int nslice = NCONS / g.h_kv;
-  const int tile = ATT_SUBTILE * nslice;
-  const int units = (g.top_k + tile - 1) / tile;
-  return (units + 1) * nslice;
+  return att_nchunk(g) * (NCONS / g.h_kv);
 }
 
-// Three stages where they fit (small request tables), else two.
+// Three stages where they fit, else two.
 static int attention_stages(const Geometry& g, size_t limit) {
   return att_layout(g, MAX_STAGES).total <= limit ? MAX_STAGES : 2;
 }
@@ -191,257 +227,178 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   constexpr int TILE = ATT_SUBTILE * NSLICE;
   constexpr int NJ = (TILE + 31) / 32;   // 32-row words of a unit
   constexpr int HQ = HKV * G;
+  constexpr int CR = TILE >= CHUNK_ROWS_MIN ? TILE : (CHUNK_ROWS_MIN / TILE) * TILE;   // rows per chunk
+  constexpr int HPT = HQ < MERGE_HEADS ? HQ : MERGE_HEADS;   // heads per merge task
+  constexpr int NMT = HQ / HPT;                              // merge tasks per request
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = g.top_k;
-  const int c = blockIdx.x;
+  const int NCHK = (K + CR - 1) / CR;
+  const int NPARTS = NCHK * NSLICE;
+  const long long total = (long long)p.n_req * (NCHK + NMT);
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const AttLayout L = att_layout(g, nstage);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
   uint64_t* empty = full + MAX_STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + MAX_STAGES);
+  Desc* desc = reinterpret_cast<Desc*>(smem_raw + L.desc);
   int* slot_tab = reinterpret_cast<int*>(smem_raw + L.slot_tab);   // [stage][TILE]: hot slot of a fetched row
-  int* prefix = reinterpret_cast<int*>(smem_raw + L.prefix);       // prefix[i] = first unit of request i
-  int* kk_s = prefix + (g.max_requests + 1);                        // k_eff of request i
-  int* req_s = kk_s + (g.max_requests + 1);                         // request id of request i
-  int2* rowc = reinterpret_cast<int2*>(smem_raw + L.rowc);   // [unit k][row i] -> (slot_of_sel, position)
   unsigned char* stage = smem_raw + L.stage;
   const int row_stride = g.row_bytes + ATT_ROW_PAD;
   const int rvec = g.row_bytes / 16;
-  __shared__ int scan_tmp[THREADS / 32 + 1];
   HS_TRACE(p, 2, 0);
 
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
-      mbar_init(&full[s], 2);   // the stager's expect-tx arrival and the fetcher's
+      mbar_init(&full[s], 1);      // the loader's arrival (with the hit bytes and its lanes' cp.async)
       mbar_init(&empty[s], NCONS);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  griddep_wait();   // selection, slots, lengths and host rows come from the kernels before
+  // no griddepcontrol.wait here: everything the select kernel writes for a
+  // request is published through that request's ready flag
   griddep_launch_dependents();
-
-  // ---- flattened work list: units of every request (k_eff / TILE, rounded up) ----
-  int carry = 0;
-  for (int base = 0; base < p.n_req; base += THREADS) {
-    const int i = base + tid;
-    int units = 0;
-    if (i < p.n_req) {
-      const int req = p.req_ids ? p.req_ids[i] : i;
-      int kk = 0;
-      if (req >= 0 && req < g.max_requests) kk = min(K, p.s.length[(long long)req * g.n_layers + p.layer]);
-      units = (kk + TILE - 1) / TILE;
-      kk_s[i] = kk;
-      req_s[i] = req;
-      if (kk == 0 && i % (int)gridDim.x == c) {   // nothing selected: the output is defined as 0
-        uint16_t* out = p.out + (long long)i * HQ * D;
-        for (int e = 0; e < HQ * D; ++e) out[e] = 0;
-        if (req >= 0 && req < g.max_requests) set_error(p.s.dev_error, HS_DEVERR_EMPTY);
-      }
-    }
-    int tot;
-    const int ex = block_exclusive_scan<THREADS>(units, scan_tmp, &tot);
-    if (i < p.n_req) prefix[i] = carry + ex;
-    carry += tot;
-  }
-  if (tid == 0) prefix[p.n_req] = carry;
   __syncthreads();
   HS_TRACE(p, 2, 1);
-  const long long U = carry;
-  // Only the first min(grid, U) CTAs take part, so every one taking part owns at
-  // least one unit.
-  const int Gc = (int)max(1LL, min((long long)gridDim.x, U));
-  if (c == 0)   // partials of each request, for the merge kernel
-    for (int i = tid; i < p.n_req; i += THREADS)
-      p.s.att_nparts[i] = prefix[i + 1] > prefix[i]
-                              ? (owner_of(prefix[i + 1] - 1, U, Gc) - owner_of(prefix[i], U, Gc) + 1) * NSLICE
-                              : 0;
-  if (U == 0) return;
-  if (c >= Gc) return;
-  const long long u0 = (long long)c * U / Gc, u1 = (long long)(c + 1) * U / Gc;
 
-  // first request with units at or after u0
-  int ri = 0;
-  {
-    int lo = 0, hi = p.n_req - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= u0) lo = mid;
-      else hi = mid - 1;
-    }
-    ri = lo;
-    while (prefix[ri + 1] <= u0) ++ri;
-  }
-
-  // Slot ids and positions of this CTA's rows, read once: in the loop below the
-  // stager and the fetcher then issue no global loads, which would otherwise
-  // queue behind the fetcher's slow host-memory requests.
-  const int ncache = (int)min((long long)ROWCACHE / TILE, u1 - u0);   // units whose rows are cached
-  for (int e0 = tid; e0 < ncache * TILE; e0 += 4 * THREADS) {   // all loads in flight together
-    int2 v[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int e = e0 + q * THREADS;
-      v[q] = make_int2(0, 0);
-      if (e < ncache * TILE) {
-        const long long u = u0 + e / TILE;
-        int lo = ri, hi = p.n_req - 1;   // request of unit u: last r with prefix[r] <= u
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (prefix[mid] <= u) lo = mid;
-          else hi = mid - 1;
-        }
-        const int row = (int)(u - prefix[lo]) * TILE + e % TILE;
-        if (row < kk_s[lo]) {
-          const long long gi = (long long)lo * K + row;
-          v[q] = make_int2(p.s.slot_of_sel[gi], p.s.sel[gi]);
-        }
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (e0 + q * THREADS < ncache * TILE) rowc[e0 + q * THREADS] = v[q];
-  }
-  __syncthreads();
-  HS_TRACE(p, 2, 2);
-  // (slot_of_sel, position) of row i of unit u (request r, first row row0)
-  auto row_info = [&](long long u, int r, int row0, int i) -> int2 {
-    const long long k = u - u0;
-    if (k < ncache) return rowc[k * TILE + i];
-    const long long gi = (long long)r * K + row0 + i;
-    return make_int2(p.s.slot_of_sel[gi], p.s.sel[gi]);
-  };
-
-  if (warp == STAGER) {
-    // ============================ stager warp ============================
-    // Hit rows of each unit by bulk copy; unit u+1's slots are read while the
-    // stager waits for a free stage.
-    int r = ri;
-    int slots[NJ];
-    int cur_r = -1, cur_nr = 0;
-    auto load_unit = [&](long long u, int (&sl)[NJ], int& ur, int& unr) {
-      while (prefix[r + 1] <= u) ++r;
-      ur = r;
-      const int urow0 = (int)(u - prefix[r]) * TILE;
-      unr = min(TILE, kk_s[r] - urow0);
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int i = lane + 32 * j;
-        sl[j] = i < unr ? row_info(u, r, urow0, i).x : 0;
-      }
-    };
-    load_unit(u0, slots, cur_r, cur_nr);
+  if (warp == LOADER) {
+    // ============================ loader warp ============================
     const uint64_t stream_policy = l2_evict_first_policy();   // hit rows are read once per call
     int s = 0;
     long long it = 0;
-    for (long long u = u0; u < u1; ++u, ++it) {
-      int nslots[NJ];
-      int n_r = cur_r, n_nr = 0;
-      if (u + 1 < u1) load_unit(u + 1, nslots, n_r, n_nr);
-      if (it >= nstage &&
-          !__all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
-                                               p.s.dev_error)))
-        break;
-      const int nr = cur_nr;
-      const long long rl = (long long)req_s[cur_r] * g.n_layers + p.layer;
-      unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+    unsigned nxt = 0;
+    if (lane == 0) nxt = atomicAdd(&p.s.sync[2], 1u);
+    bool dead = false;
+    auto take_stage = [&]() -> bool {   // wait until stage s may be refilled
+      if (it < nstage) return true;
+      return __all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
+                                                 p.s.dev_error, 4 * WAIT_LIMIT_NS));
+    };
+    while (!dead) {
+      const long long item = (long long)__shfl_sync(FULL_MASK, nxt, 0);
+      if (item >= total) break;
+      if (lane == 0) nxt = atomicAdd(&p.s.sync[2], 1u);   // the next item, while this one loads
+      const Item itm = decode_item(item, p.n_req, NCHK, NMT);
+      const int r = itm.ri;
+      if (itm.merge) {
+        if (!take_stage()) break;
+        if (lane == 0) {
+          desc[s] = Desc{DESC_MERGE, r, itm.idx, 0, 0, 0, 0, 0};
+          mbar_arrive(&full[s]);
+        }
+        __syncwarp();
+        s = (s + 1 == nstage) ? 0 : s + 1;
+        ++it;
+        continue;
+      }
+      // a chunk: wait for the request's publication
+      int kk = 0;
+      if (lane == 0) {
+        if (wait_counter(p.s.ready + r, 1u)) {
+          kk = __ldcg(p.s.kk_pub + r);
+        } else {
+          set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+        }
+      }
+      kk = __shfl_sync(FULL_MASK, kk, 0);
+      const int row0 = itm.idx * CR;
+      const int nrows = max(0, min(CR, kk - row0));
+      if (nrows == 0) {   // past k_eff: nothing to attend, the chunk is done
+        __syncwarp();
+        if (lane == 0) red_release_add(p.s.chunk_done + r, 1u);
+        continue;
+      }
+      const int req = p.req_ids ? p.req_ids[r] : r;
+      const long long rl = (long long)req * g.n_layers + p.layer;
       const unsigned char* hot =
           reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
-      int hit_rows = 0;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int i = lane + 32 * j;
-        hit_rows += __popc(__ballot_sync(FULL_MASK, i < nr && (slots[j] & HS_SLOT_MISS_FLAG) == 0));
-      }
-      // rows past the end of a request: zero them so their masked (weight-0)
-      // values stay finite
-      if (nr < TILE) {
-        for (int e = lane; e < (TILE - nr) * rvec; e += 32) {
-          const int i = nr + e / rvec;
-          *reinterpret_cast<int4*>(st_s + (size_t)i * row_stride + (e % rvec) * 16) = make_int4(0, 0, 0, 0);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(hit_rows * g.row_bytes));
-      }
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int i = lane + 32 * j;
-        if (i < nr && (slots[j] & HS_SLOT_MISS_FLAG) == 0) {
-          int slot = slots[j];
-          if (slot < 0 || slot >= g.hot_slots) {   // never expected: keep the copy in bounds
-            set_error(p.s.dev_error, HS_DEVERR_METADATA);
-            slot = 0;
-          }
-          bulk_g2s_hint(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
-                        &full[s], stream_policy);
-        }
-      }
-      HS_TRACE_IF(p, 2, 3, lane == 0 && it == 0);
-      s = (s + 1 == nstage) ? 0 : s + 1;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) slots[j] = nslots[j];
-      cur_r = n_r;
-      cur_nr = n_nr;
-    }
-    HS_TRACE_IF(p, 2, 4, lane == 0);
-  } else if (warp == FETCHER) {
-    // ============================ fetcher warp ============================
-    // Missed rows of each unit, from the mapped host copy straight into their
-    // stage rows; the stage's full barrier completes when these copies land.
-    int r = ri;
-    int s = 0;
-    long long it = 0;
-    for (long long u = u0; u < u1; ++u, ++it) {
-      while (prefix[r + 1] <= u) ++r;
-      const int row0 = (int)(u - prefix[r]) * TILE;
-      const int nr = min(TILE, kk_s[r] - row0);
-      const long long rl = (long long)req_s[r] * g.n_layers + p.layer;
       const unsigned char* host =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
-      int2 info[NJ];
+      const int32_t* sos = p.s.slot_of_sel + (long long)r * K;
+      const int32_t* selr = p.s.sel + (long long)r * K;
+      const int nunits = (nrows + TILE - 1) / TILE;
+      for (int u = 0; u < nunits; ++u) {
+        const int ur0 = row0 + u * TILE;
+        const int unr = min(TILE, nrows - u * TILE);
+        int slots[NJ], pos[NJ];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int i = lane + 32 * j;
-        info[j] = i < nr ? row_info(u, r, row0, i) : make_int2(0, 0);
-      }
-      if (it >= nstage &&
-          !__all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
-                                               p.s.dev_error)))
-        break;
-      unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
-      int* tab = slot_tab + s * TILE_MAX;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int i = lane + 32 * j;
-        const bool miss = i < nr && (info[j].x & HS_SLOT_MISS_FLAG) != 0;
-        if (i < TILE) tab[i] = miss ? (info[j].x & ~HS_SLOT_MISS_FLAG) : -1;
-        unsigned bits = __ballot_sync(FULL_MASK, miss);
-        while (bits) {
-          const int b0 = __ffs(bits) - 1;
-          bits &= bits - 1;
-          const int pos = __shfl_sync(FULL_MASK, info[j].y, b0);
-          const unsigned char* src = host + (size_t)pos * g.row_bytes;
-          unsigned char* dst = st_s + (size_t)(32 * j + b0) * row_stride;
-          for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+        for (int j = 0; j < NJ; ++j) {
+          const int i = lane + 32 * j;
+          slots[j] = i < unr ? __ldcg(sos + ur0 + i) : 0;
+          pos[j] = i < unr ? __ldcg(selr + ur0 + i) : 0;
         }
+        if (!take_stage()) {
+          dead = true;
+          break;
+        }
+        unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+        int* tab = slot_tab + s * TILE_MAX;
+        // rows past the end of the chunk: zero them so their masked (weight-0)
+        // values stay finite
+        if (unr < TILE) {
+          for (int e = lane; e < (TILE - unr) * rvec; e += 32) {
+            const int i = unr + e / rvec;
+            *reinterpret_cast<int4*>(st_s + (size_t)i * row_stride + (e % rvec) * 16) = make_int4(0, 0, 0, 0);
+          }
+        }
+        int hit_rows = 0;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int i = lane + 32 * j;
+          const bool valid = i < unr;
+          const bool miss = valid && (slots[j] & HS_SLOT_MISS_FLAG) != 0;
+          if (i < TILE) tab[i] = miss ? (slots[j] & ~HS_SLOT_MISS_FLAG) : -1;
+          hit_rows += __popc(__ballot_sync(FULL_MASK, valid && !miss));
+          // missed rows: host copy -> stage row, 16 bytes per lane per step
+          unsigned bits = __ballot_sync(FULL_MASK, miss);
+          while (bits) {
+            const int b0 = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int pp = __shfl_sync(FULL_MASK, pos[j], b0);
+            const unsigned char* src = host + (size_t)pp * g.row_bytes;
+            unsigned char* dst = st_s + (size_t)(32 * j + b0) * row_stride;
+            for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+          }
+        }
+        cp_async_mbar_arrive(&full[s]);   // the phase also waits for this lane's copies
+        __syncwarp();
+        if (lane == 0) {
+          desc[s] = Desc{DESC_UNIT, r, itm.idx, ur0 - row0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, 0};
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(hit_rows * g.row_bytes));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int i = lane + 32 * j;
+          if (i < unr && (slots[j] & HS_SLOT_MISS_FLAG) == 0) {
+            int slot = slots[j];
+            if (slot < 0 || slot >= g.hot_slots) {   // never expected: keep the copy in bounds
+              set_error(p.s.dev_error, HS_DEVERR_METADATA);
+              slot = 0;
+            }
+            bulk_g2s_hint(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
+                          &full[s], stream_policy);
+          }
+        }
+        HS_TRACE_IF(p, 2, 2, lane == 0 && it == 0);
+        s = (s + 1 == nstage) ? 0 : s + 1;
+        ++it;
       }
-      HS_TRACE_IF(p, 2, 5, lane == 0 && it == 0);
-      cp_async_mbar_arrive(&full[s]);   // balanced: completes when this lane's copies land
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
-      s = (s + 1 == nstage) ? 0 : s + 1;
     }
-    HS_TRACE_IF(p, 2, 6, lane == 0);
+    // no more work: tell the consumers
+    if (!dead && take_stage() && lane == 0) {
+      desc[s] = Desc{DESC_STOP, 0, 0, 0, 0, 0, 0, 0};
+      mbar_arrive(&full[s]);
+    }
+    __syncwarp();
+    HS_TRACE_IF(p, 2, 3, lane == 0);
     cp_async_wait_all();
-    HS_TRACE_IF(p, 2, 7, lane == 0);
   } else {
     // ============================ consumer warps ============================
+    const int ct = tid;   // 0..255
     const int kvh = warp % HKV;
     const int slice = warp / HKV;
     const int gq = lane >> 2, tq = lane & 3;
@@ -449,63 +406,95 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     uint32_t qa[8][4];
     float o[16][4];
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
-    int r = -1;
-    int s = 0;
+    int q_r = -1;
 
-    auto flush = [&](int req_i) {   // partial (m, l, o) of this (CTA, request, slice)
-      float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
-      ll += __shfl_xor_sync(FULL_MASK, ll, 2);
-      float lh = l_hi + __shfl_xor_sync(FULL_MASK, l_hi, 1);
-      lh += __shfl_xor_sync(FULL_MASK, lh, 2);
-      const int c_first = owner_of(prefix[req_i], U, Gc);
-      const int part = (c - c_first) * NSLICE + slice;
-      float* po = p.s.part_o + ((long long)req_i * p.att_parts + part) * HQ * D;
-      float* pml = p.s.part_ml + ((long long)req_i * p.att_parts + part) * HQ * 2;
-      const int h_lo = kvh * G + gq, h_hi = kvh * G + gq + 8;
-      if (gq < G) {
+    for (long long it = 0;; ++it) {
+      const int s = (int)(it % nstage);
+      const bool ok = wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
+                                    4 * WAIT_LIMIT_NS);
+      if (named_sync_or(BAR_VOTE, NCONS * 32, !ok)) break;   // the consumers leave together
+      const Desc dsc = desc[s];
+      if (dsc.type == DESC_STOP) break;
+      if (dsc.type == DESC_MERGE) {
+        if (lane == 0) mbar_arrive(&empty[s]);
+        // ---- merge task: heads [idx*HPT, (idx+1)*HPT) of request ri, chunk order ----
+        const int r = dsc.ri;
+        if (ct == 0 && !wait_counter(p.s.chunk_done + r, (unsigned)NCHK)) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+        named_sync(BAR_CONS, NCONS * 32);
+        const int kk = __ldcg(p.s.kk_pub + r);
+        const int nparts = ((kk + CR - 1) / CR) * NSLICE;
+        const int hl = ct >> 5, d4 = ct & 31;
+        if (hl < HPT) {
+          const int head = dsc.c * HPT + hl;
+          const float2* pml = reinterpret_cast<const float2*>(p.s.part_ml) + (long long)r * NPARTS * HQ;
+          const float4* po = reinterpret_cast<const float4*>(p.s.part_o) + (long long)r * NPARTS * HQ * (D / 4);
+          float M = -INFINITY;
+          for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(pml + (long long)q * HQ + head).x);
+          float Ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          constexpr int UQ = 4;
+          for (int q0 = 0; q0 < nparts; q0 += UQ) {
+            float2 ml[UQ];
+            float4 v[UQ];
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-          *reinterpret_cast<float2*>(po + (long long)h_lo * D + 8 * t + 2 * tq) = make_float2(o[t][0], o[t][1]);
-        if (tq == 0) *reinterpret_cast<float2*>(pml + h_lo * 2) = make_float2(m_lo, ll);
+            for (int u = 0; u < UQ; ++u) {
+              const int q = q0 + u;
+              ml[u] = q < nparts ? __ldcg(pml + (long long)q * HQ + head) : make_float2(-INFINITY, 0.f);
+              v[u] = q < nparts ? __ldcg(po + ((long long)q * HQ + head) * (D / 4) + d4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < UQ; ++u)
+              if (q0 + u < nparts) {
+                const float w = exp2f(ml[u].x - M);
+                Ls = fmaf(ml[u].y, w, Ls);
+                acc.x = fmaf(v[u].x, w, acc.x);
+                acc.y = fmaf(v[u].y, w, acc.y);
+                acc.z = fmaf(v[u].z, w, acc.z);
+                acc.w = fmaf(v[u].w, w, acc.w);
+              }
+          }
+          uint2 pk = make_uint2(0u, 0u);
+          if (nparts > 0) {
+            const float inv = 1.f / Ls;
+            pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+          }
+          *reinterpret_cast<uint2*>(p.out + ((long long)r * HQ + head) * D + 4 * d4) = pk;
+        }
+        if (ct == 0) {
+          const unsigned prev = atom_acq_rel_add(p.s.merge_done + r, 1u);
+          if (prev + 1 == (unsigned)NMT) {   // the request's last merge task: clear its flags
+            p.s.ready[r] = 0;
+            p.s.chunk_done[r] = 0;
+            p.s.merge_done[r] = 0;
+          }
+        }
+        continue;
       }
-      if (gq + 8 < G) {
+      // ---- a unit of a chunk ----
+      const int r = dsc.ri;
+      if (dsc.first) {
+        if (r != q_r) {
+          q_r = r;
+          // the group's query heads as the mma A operand (rows >= G are zero)
+          const uint16_t* qg = p.q + ((long long)r * HQ + kvh * G) * D;
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-          *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
-        if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
-      }
-    };
-
-    long long it = 0;
-    for (long long u = u0; u < u1; ++u, ++it) {
-      int rn = r < 0 ? ri : r;
-      while (prefix[rn + 1] <= u) ++rn;
-      if (rn != r) {
-        if (r >= 0) flush(r);
-        r = rn;
-        // the group's query heads as the mma A operand (rows >= G are zero)
-        const uint16_t* qg = p.q + ((long long)r * HQ + kvh * G) * D;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int d0 = ks * 16 + 2 * tq;
-          qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qg + gq * D + d0) : 0u;
-          qa[ks][1] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (gq + 8) * D + d0) : 0u;
-          qa[ks][2] = gq < G ? *reinterpret_cast<const uint32_t*>(qg + gq * D + d0 + 8) : 0u;
-          qa[ks][3] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (gq + 8) * D + d0 + 8) : 0u;
+          for (int ks = 0; ks < 8; ++ks) {
+            const int d0 = ks * 16 + 2 * tq;
+            qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qg + gq * D + d0) : 0u;
+            qa[ks][1] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (gq + 8) * D + d0) : 0u;
+            qa[ks][2] = gq < G ? *reinterpret_cast<const uint32_t*>(qg + gq * D + d0 + 8) : 0u;
+            qa[ks][3] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (gq + 8) * D + d0 + 8) : 0u;
+          }
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
         m_lo = m_hi = -INFINITY;
         l_lo = l_hi = 0.f;
       }
-      const int kk = kk_s[r];
-      const int row0 = (int)(u - prefix[r]) * TILE;
-      const int nv = max(0, min(ATT_SUBTILE, kk - row0 - slice * ATT_SUBTILE));
-
-      if (!__all_sync(FULL_MASK, wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag,
-                                               p.s.dev_error)))
-        break;
-      HS_TRACE_IF(p, 2, 8, tid == 0 && it == 0);
+      const int nv = max(0, min(ATT_SUBTILE, dsc.nr - slice * ATT_SUBTILE));
+      HS_TRACE_IF(p, 2, 4, tid == 0 && it == 0);
       const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
       if (nv > 0) {
         const int rbase = slice * ATT_SUBTILE;
@@ -582,7 +571,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       // consumer warp 0 writes the rows fetched for this unit into their hot slots
       if (warp == 0) {
         const int* tab = slot_tab + s * TILE_MAX;
-        const long long rl = (long long)req_s[r] * g.n_layers + p.layer;
+        const int req = p.req_ids ? p.req_ids[r] : r;
+        const long long rl = (long long)req * g.n_layers + p.layer;
         unsigned char* hotw = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
         bool any = false;
         for (int i = lane; i < TILE; i += 32) {
@@ -600,11 +590,32 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      s = (s + 1 == nstage) ? 0 : s + 1;
+      if (dsc.last) {   // the chunk's partial (m, l, o) for this slice
+        float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
+        ll += __shfl_xor_sync(FULL_MASK, ll, 2);
+        float lh = l_hi + __shfl_xor_sync(FULL_MASK, l_hi, 1);
+        lh += __shfl_xor_sync(FULL_MASK, lh, 2);
+        const int part = dsc.c * NSLICE + slice;
+        float* po = p.s.part_o + ((long long)r * NPARTS + part) * HQ * D;
+        float* pml = p.s.part_ml + ((long long)r * NPARTS + part) * HQ * 2;
+        const int h_lo = kvh * G + gq, h_hi = kvh * G + gq + 8;
+        if (gq < G) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            *reinterpret_cast<float2*>(po + (long long)h_lo * D + 8 * t + 2 * tq) = make_float2(o[t][0], o[t][1]);
+          if (tq == 0) *reinterpret_cast<float2*>(pml + h_lo * 2) = make_float2(m_lo, ll);
+        }
+        if (gq + 8 < G) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
+          if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
+        }
+        named_sync(BAR_CONS, NCONS * 32);
+        if (ct == 0) red_release_add(p.s.chunk_done + r, 1u);
+      }
     }
-    HS_TRACE_IF(p, 2, 9, tid == 0);
-    HS_TRACE_IF(p, 2, 10, tid == 32 * (NCONS - 1));
-    if (r >= 0 && !*abort_flag) flush(r);
+    HS_TRACE_IF(p, 2, 5, tid == 0);
   }
 
   __syncthreads();
@@ -617,10 +628,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
     }
     __syncthreads();
-    return;
   }
-
-  HS_TRACE(p, 2, 14);
+  // the last CTA to leave resets the queue (every CTA has taken its last item)
+  if (tid == 0) {
+    const unsigned prev = atom_acq_rel_add(&p.s.sync[3], 1u);
+    if (prev + 1 == gridDim.x) {
+      p.s.sync[2] = 0;
+      p.s.sync[3] = 0;
+    }
+  }
+  HS_TRACE(p, 2, 6);
+  // complete only after the select kernel has: the next launch on the stream
+  // then sees both kernels finished
+  griddep_wait();
 }
 
 // Combines the partials of each (request, head) in part order: grid (heads /
@@ -747,9 +767,7 @@ static cudaError_t run_gqa(const DecodeParams* p, size_t smem, cudaStream_t st) 
   if (p == nullptr)   // prepare: allow the shared memory this shape needs
     return allow_smem(kern, smem);
   const int ns = attention_stages(p->g, 227 * 1024);
-  cudaError_t e = launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);
-  if (e != cudaSuccess) return e;
-  return launch_merge(*p, st);
+  return launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);
 }
 
 template <int HKV>

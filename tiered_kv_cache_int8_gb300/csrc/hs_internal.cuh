@@ -21,7 +21,14 @@ constexpr int IDX_TILE_BYTES = 32768;  // index keys per bulk copy (one tile)
 constexpr int IDX_BINS = 4096;       // radix digit: 12 bits, two levels cover 24-bit keys
 constexpr int IDX_KEY_BIAS = 1 << 22;  // |score| <= 128*128*256 = 2^22 for d_idx <= 256
 
-constexpr int RES_THREADS = 1024;    // top-k + RESOLVE CTA (one per request)
+constexpr int RES_THREADS = 1024;    // top-k CTA of the static (no-allocation) entry point
+
+// The select kernel (scores, top-k and RESOLVE in one persistent launch): every
+// CTA has SEL_THREADS threads; a scorer CTA runs two independent 256-thread
+// scoring groups, a resolver CTA runs the top-k + RESOLVE chain of its requests.
+constexpr int SEL_THREADS = 512;
+constexpr int SEL_GROUP = 256;       // threads of one scoring group
+constexpr int SEL_MAX_RESOLVERS = 16;
 
 // slot_of_sel entries of rows RESOLVE left for the attention kernel to fetch
 constexpr int HS_SLOT_MISS_FLAG = 0x40000000;
@@ -71,6 +78,16 @@ struct DeviceState {
   int32_t* att_nparts;     // [R][8] partial results of each (request, head group) of the current call
   int32_t* call_n;         // [R] positions of request i in the current call (with its appended token)
   unsigned int* app_counter;   // [R]
+  // cross-CTA progress of one decode call (all zero between calls: every counter
+  // is reset by the last party that reads it)
+  unsigned int* tiles_done;    // [R] score tiles of request i finished (select kernel)
+  unsigned int* ready;         // [R] 1: request i's selection and slots are published
+  int32_t* kk_pub;             // [R] k_eff of request i (valid once ready)
+  unsigned int* chunk_done;    // [R] attention chunks of request i finished
+  unsigned int* merge_done;    // [R] merge tasks of request i finished
+  unsigned int* sync;          // [4]: 0 = CTAs of the select kernel past their set-up,
+                               //      1 = resolvers finished, 2 = next attention work item,
+                               //      3 = attention CTAs finished
 };
 
 struct AppendParams {
@@ -101,6 +118,10 @@ struct DecodeParams {
   int fetch_mode;          // 0: attention kernel fetches misses, 1: RESOLVE does
   int replacement;         // HS_REPLACE_LRU / _FIFO / _RANDOM
   unsigned int replacement_seed;
+  int sel_grid;            // select kernel CTAs (one per SM)
+  int n_resolvers;         // of them, resolver CTAs (the rest score)
+  int publish;             // 1: resolvers publish each request (the chunked attention kernel waits on it)
+  int fault;               // test hook: 1 = the resolver never publishes request 0 (a wait runs out)
 #ifdef HS_WITH_TRACE
   unsigned long long* trace;   // [2][3][1024][64]: clock64 and %globaltimer per (kernel, CTA, point)
 #endif
@@ -119,7 +140,8 @@ struct hs_handle {
   float scale_log2 = 0.f;
   int num_sms = 0;
   long long score_stride = 0;
-  size_t idx_smem = 0, res_smem = 0, att_smem = 0;
+  size_t sel_smem = 0, att_smem = 0;
+  int fault = 0;                       // HS_FAULT_INJECT=noready at create (test hook)
   int att_parts = 0;
   size_t host_bytes = 0, hot_bytes = 0, index_bytes = 0, meta_bytes = 0;
   uint64_t decode_calls = 0, append_calls = 0;
@@ -140,7 +162,9 @@ namespace hs {
 // launchers (one per kernel translation unit); return a CUDA error code
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
-cudaError_t launch_resolve(const DecodeParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st);
+size_t select_smem_bytes(const Geometry& g);
+cudaError_t prepare_select(const Geometry& g, size_t smem);
 cudaError_t launch_attention(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_init_order(int32_t* order, long long n_lists, int B, cudaStream_t st);
 // records a message for hs_last_error(NULL) and returns `code`
@@ -148,11 +172,9 @@ int set_static_error(int code, const char* msg);
 
 // shared-memory needs, checked against the device limit at create time
 size_t score_smem_bytes(const Geometry& g);
-size_t resolve_smem_bytes(const Geometry& g);
 size_t attention_smem_bytes(const Geometry& g);
 int attention_parts(const Geometry& g);
 cudaError_t prepare_score(const Geometry& g, size_t smem);
-cudaError_t prepare_resolve(size_t smem);
 cudaError_t prepare_attention(const Geometry& g, size_t smem);
 // attention over shared latent rows (hs_attention_mla.cu) and the partial merge
 int mla_parts(const Geometry& g);
@@ -327,6 +349,49 @@ __device__ __forceinline__ int4 ld_nc_v4(const void* p) {
 }
 
 __device__ __forceinline__ void set_error(unsigned int* word, unsigned int bit) { atomicOr(word, bit); }
+
+// GPU-scope release add / store and acquire load: the publication of one CTA's
+// writes to CTAs of the same or a concurrently running kernel.
+__device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int atom_acq_rel_add(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Spins until *p >= target (acquire); gives up after WAIT_LIMIT_NS and returns false.
+__device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int target) {
+  if (ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire(p) >= target) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+// Named barrier over `n` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 // Fire-and-forget 64-bit add (no value returned, so the issuing thread never waits).
 __device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {

@@ -1,0 +1,1090 @@
+// The select kernel: indexer scores, exact top-k and RESOLVE of one decode
+// layer-step for every request, in ONE persistent launch, so that a request's
+// selection and cache update start as soon as its own scores exist instead of
+// after every request has been scored.
+//
+// Method.  "10月14日学习笔记" (zgchen.com), "HiSparse / 动机": an indexer scores
+// the context and attention runs over the top-k positions (ties here: the lower
+// position; output ascending).  The score is an int8 query dotted with each
+// position's int8 index key, summed exactly in int32 with dp4a.
+// "KV卸载上主机:HiSparse、PDD与DDR4回收", "论文1：HiSparse": a page table plus
+// LRU metadata drive replacement of the B hot slots of each (request, layer);
+// hit detection, LRU replacement, metadata update and the host fetch are
+// resolved in one kernel per layer.  "10月14日学习笔记", "方法" 1: adjacent
+// steps overlap, so LRU fits.
+//
+// Replacement rule: slots holding a selected position (hits) are pinned; the m
+// misses, in ascending position order, go to the m unpinned slots with the
+// smallest (stamp, slot), in that order; every used slot's stamp (LRU), or only
+// every filled slot's (FIFO, a comparison policy of the pages), becomes the
+// (request, layer) step counter, which then grows by one.  Random replacement
+// (the other comparison policy) takes the m unpinned slots with the smallest
+// counter-based hash keys instead, in ascending slot order, and stamps as LRU.
+//
+// Design (sm_103a).  Grid = one 512-thread CTA per SM.  CTAs 0..n_resolvers-1
+// are resolvers, the rest score:
+//  * Scoring is HBM-bound (d_idx bytes per position).  The positions of every
+//    request that needs a selection (more positions than k) are flattened in
+//    request order and cut into warp tiles (two sub-tiles of 8 x 16-byte loads
+//    per lane); scorer warp w takes tiles w, w + W, w + 2W, ... so all warps
+//    sweep the requests in order and request r is complete early.  Loads are
+//    coalesced 16-byte streaming loads (the 8 lanes of a position read its
+//    8 chunks side by side), one sub-tile in flight while the other is scored;
+//    dp4a partial sums are combined with lane shuffles.  Each key
+//    (score + 2^22, order-preserving, 24 bits) goes to a scratch row; keys at or
+//    above the request's candidate threshold (left by the previous call) are
+//    also listed with their positions (one atomic per warp sub-tile).  After a
+//    tile its warp adds 1 to the request's tile counter with release order.
+//  * A resolver takes requests j, j + n_resolvers, ...: it first prefetches
+//    what does not depend on the scores (LRU list, reverse map, the appended
+//    row), waits (bounded) until the request's tiles are all counted, then runs
+//    the latency-bound chain:
+//     - exact top-k: when the previous call's threshold listed between k and 2k
+//       keys, the k largest (ties included) are all in the list, so a two-digit
+//       radix select over the list alone finds them; otherwise a histogram pass
+//       and one pass that turns "digit above the threshold digit" into a
+//       position bitmap (the few keys with the threshold digit go to per-warp
+//       lists in position order) over the scratch keys.  Either way the
+//       selection is emitted ascending from bitmaps.
+//     - RESOLVE: hit test through the page table (independent gathers, every
+//       missed host row prefetched into L2 line by line the moment it misses),
+//       miss compaction with block scans, victims from an explicit LRU list kept
+//       sorted by (stamp, slot) — a call moves exactly the slots it used to the
+//       most recent end, so two stable compactions maintain it: no sort, no heap.
+//     - publication: selection, slot of every selected row (misses flagged for
+//       the attention kernel, which copies them host -> stage -> slot) and k_eff,
+//       then the request's ready flag (release).  The attention kernel, launched
+//       as a programmatic dependent, starts on the requests that are ready while
+//       later ones are still being scored or resolved.
+//     - after publication: stamps, the new LRU list, counters, step + 1 and the
+//       appended token (its key to the HBM store, its row to the pinned host
+//       copy, length + 1).  Lengths and thresholds are written only once every
+//       CTA of the launch has read them (a grid-wide counter).
+//  * fetch_mode 1 (and latent rows, which every head group reads) pulls the
+//    missed rows into their slots inside the resolver before publication.
+#include "hs_internal.cuh"
+
+namespace hs {
+
+namespace {
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int NT = SEL_THREADS;
+constexpr int NWARP = NT / 32;
+constexpr int FAST_MAX_N = 256 * 1024;   // one-pass top-k: contexts up to this many positions
+constexpr int WCAP = 256;                // threshold-digit keys a warp lists in the one-pass top-k
+constexpr int CAND_MAX_N_PER_K = 20;     // candidate listing only for contexts up to 20 k positions
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+
+// Per-request tables of the launch (scorers) and the resolver's layout share the
+// dynamic shared memory: a CTA is one or the other.
+struct SelLayout {
+  // scorer tables
+  size_t t_prefix, t_req, t_n, t_thr, t_total;
+  // resolver
+  size_t hist, sel, slot, miss_i, victim, ord, rev, used, bitmap, lists, newrow, r_total;
+  bool rev_smem, fast;
+  size_t total;
+};
+
+__host__ __device__ inline SelLayout sel_layout(const Geometry& g) {
+  const int B = g.hot_slots, K = g.top_k;
+  SelLayout L;
+  size_t off = 0;
+  L.t_prefix = off;   // int [n+1]: first warp tile of request i
+  off += align_up((size_t)(g.max_requests + 1) * 4, 16);
+  L.t_req = off;      // int [n]: request id (-1: nothing to score)
+  off += align_up((size_t)g.max_requests * 4, 16);
+  L.t_n = off;        // int [n]: positions this call (with the appended token)
+  off += align_up((size_t)g.max_requests * 4, 16);
+  L.t_thr = off;      // u32 [n]: candidate threshold
+  off += align_up((size_t)g.max_requests * 4, 16);
+  L.t_total = off;
+
+  off = 0;
+  L.hist = off;
+  off += IDX_BINS * 4;
+  L.sel = off;
+  off += align_up((size_t)K * 4, 16);
+  L.slot = off;
+  off += align_up((size_t)K * 4, 16);
+  L.miss_i = off;
+  off += align_up((size_t)K * 4, 16);
+  L.victim = off;
+  off += align_up((size_t)K * 4, 16);
+  L.ord = off;
+  off += (size_t)B * 4;
+  L.used = off;
+  off += align_up((size_t)B, 16);
+  L.newrow = off;
+  off += align_up((size_t)g.row_bytes, 16) + align_up((size_t)g.d_idx, 16);
+  const size_t base = off;
+  // optional parts, in order of value: the one-pass top-k, then the reverse map
+  const size_t fast_bytes = (size_t)FAST_MAX_N / 8 + (size_t)WCAP * NWARP * 4;
+  L.fast = base + fast_bytes <= SMEM_LIMIT;
+  L.bitmap = off;
+  if (L.fast) off += (size_t)FAST_MAX_N / 8;
+  L.lists = off;
+  if (L.fast) off += (size_t)WCAP * NWARP * 4;
+  L.rev = off;
+  L.rev_smem = off + (size_t)B * 4 <= SMEM_LIMIT;
+  if (L.rev_smem) off += (size_t)B * 4;
+  L.r_total = off;
+  L.total = L.t_total > L.r_total ? L.t_total : L.r_total;
+  return L;
+}
+
+struct SelShared {
+  int scan[2 * (NWARP + 1)];
+  int b1, above1, b2, above2, bt, above_t;
+  int rb1, rabove1, rb2, rabove2;   // random replacement: digits of the m-th smallest key
+  int len, N, t_step, cnt, req, ok;
+  uint32_t thr, thr_next;
+};
+
+// Finds the digit holding the kneed-th largest key (bins scanned from the top)
+// and the number of keys in higher digits.  Leaves *out_b untouched when the
+// histogram holds fewer than kneed keys.
+__device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* scan, int* out_b, int* out_above) {
+  constexpr int PER = IDX_BINS / NT;   // bins per thread, descending
+  const int tid = threadIdx.x;
+  const int top = IDX_BINS - 1 - tid * PER;
+  int v = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) v += (int)h[top - j];
+  int tot;
+  const int ex = block_exclusive_scan<NT>(v, scan, &tot);
+  if (ex < kneed && kneed <= ex + v) {
+    int acc = ex;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int hv = (int)h[top - j];
+      if (acc < kneed && kneed <= acc + hv) {
+        *out_b = top - j;
+        *out_above = acc;
+      }
+      acc += hv;
+    }
+  }
+  __syncthreads();
+}
+
+// Random replacement's rank of an unpinned slot as a 24-bit value, larger =
+// evicted first (the digit selection scans from the top): never-filled slots
+// 0xFFFFFF (they go first, lowest slot first, as under LRU); a filled slot
+// 0x7FFFFF minus the top 23 bits of SplitMix64 (Steele, Lea and Flood, "Fast
+// splittable pseudorandom number generators", 2014; the finaliser constants of
+// Vigna's reference code) for draw number counter + 1 from state seed, with
+// counter = ((request * n_layers + layer) << 40) | ((step mod 2^24) << 16) | slot.
+__device__ __forceinline__ uint32_t random_ikey(unsigned long long seed, unsigned long long rl, int step, int slot,
+                                                bool empty) {
+  if (empty) return 0xFFFFFFu;
+  const unsigned long long ctr = (rl << 40) | ((unsigned long long)(step & 0xFFFFFF) << 16) | (unsigned)slot;
+  unsigned long long z = seed + (ctr + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return 0x7FFFFFu - (uint32_t)(z >> 41);
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Streaming 16-byte load (read once: evicted first from L1 and L2).
+__device__ __forceinline__ int4 ld_stream(const void* p) { return __ldcs(reinterpret_cast<const int4*>(p)); }
+
+// ---------------------------------------------------------------------------
+// scoring geometry for d_idx = 16 * NCH bytes
+// ---------------------------------------------------------------------------
+template <int NCH>
+struct ScoreGeom {
+  static constexpr int LPP = NCH < 8 ? NCH : 8;       // lanes per position
+  static constexpr int CPL = NCH / LPP;               // 16-byte chunks per lane per position (1 or 2)
+  static constexpr int PPI = 32 / LPP;                // positions covered by one load instruction
+  static constexpr int LD = 8;                        // loads per lane per sub-tile
+  static constexpr int NP = LD / CPL;                 // position groups per lane per sub-tile
+  static constexpr int SUB = NP * PPI;                // positions per sub-tile
+  static constexpr int TILE = 2 * SUB;                // positions per warp tile (two sub-tiles)
+  static constexpr int OWN = NP / LPP > 0 ? NP / LPP : 1;   // positions a lane owns per sub-tile
+};
+
+}  // namespace
+
+size_t select_smem_bytes(const Geometry& g) { return sel_layout(g).total; }
+
+// ===========================================================================
+// the kernel
+// ===========================================================================
+template <int NCH>
+__global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
+  using SG = ScoreGeom<NCH>;
+  constexpr int d = NCH * 16;
+  const Geometry& g = p.g;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = g.top_k;
+  const int B = g.hot_slots;
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const SelLayout L = sel_layout(g);
+  __shared__ SelShared sh;
+  HS_TRACE(p, 0, 0);
+
+  griddep_wait();   // lengths, keys, metadata and scratch of earlier stream work
+  griddep_launch_dependents();
+
+  const bool resolver = (int)blockIdx.x < p.n_resolvers;
+
+  // ======================= scorers =======================
+  if (!resolver) {
+    int* t_prefix = reinterpret_cast<int*>(smem_raw + L.t_prefix);
+    int* t_req = reinterpret_cast<int*>(smem_raw + L.t_req);
+    int* t_n = reinterpret_cast<int*>(smem_raw + L.t_n);
+    uint32_t* t_thr = reinterpret_cast<uint32_t*>(smem_raw + L.t_thr);
+    // warp tiles of every request that needs a selection
+    int carry = 0;
+    for (int base = 0; base < p.n_req; base += NT) {
+      const int i = base + tid;
+      int nt = 0;
+      if (i < p.n_req) {
+        const int req = p.req_ids ? p.req_ids[i] : i;
+        int N = 0;
+        uint32_t thr = 0;
+        if (req >= 0 && req < g.max_requests) {
+          const long long rl = (long long)req * g.n_layers + p.layer;
+          N = p.s.length[rl];
+          if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
+          thr = p.s.cand_thr[rl];
+        }
+        const bool scored = N > K;
+        nt = scored ? (N + SG::TILE - 1) / SG::TILE : 0;
+        t_req[i] = scored ? req : -1;
+        t_n[i] = N;
+        t_thr[i] = scored ? thr : 0u;
+      }
+      int tot;
+      const int ex = block_exclusive_scan<NT>(nt, sh.scan, &tot);
+      if (i < p.n_req) t_prefix[i] = carry + ex;
+      carry += tot;
+    }
+    if (tid == 0) t_prefix[p.n_req] = carry;
+    __syncthreads();
+    // this CTA has read every length and threshold it needs
+    if (tid == 0) red_release_add(&p.s.sync[0], 1u);
+    HS_TRACE(p, 0, 1);
+    const int total = carry;
+    const int W = (p.sel_grid - p.n_resolvers) * NWARP;
+    const int w0 = ((int)blockIdx.x - p.n_resolvers) * NWARP + warp;
+
+    // lane roles inside a load instruction
+    const int pg = lane / SG::LPP;            // position within the instruction
+    const int cl = lane % SG::LPP;            // chunk column of the lane
+    int4 q[SG::CPL];
+    int q_r = -1;
+
+    // request of warp tile t, searching forward from request `from`
+    auto req_of = [&](int t, int from) {
+      int x = from;
+      while (t_prefix[x + 1] <= t) ++x;
+      return x;
+    };
+    // loads of sub-tile `half` of tile t (request ri) into v (zeros past N)
+    auto load_sub = [&](int t, int ri, int half, int4 (&v)[SG::LD]) {
+      const int N = t_n[ri];
+      const int pos0 = (t - t_prefix[ri]) * SG::TILE + half * SG::SUB;
+      const long long rl = (long long)t_req[ri] * g.n_layers + p.layer;
+      const int8_t* base = p.s.idx_keys + rl * g.max_context * d;
+      const int newpos = p.new_kv ? N - 1 : -1;
+      const int8_t* nk = p.new_keys + (long long)ri * d;
+#pragma unroll
+      for (int u = 0; u < SG::LD; ++u) {
+        const int pos = pos0 + (u / SG::CPL) * SG::PPI + pg;
+        const int ch = cl * SG::CPL + (u % SG::CPL);
+        v[u] = make_int4(0, 0, 0, 0);
+        if (pos < N) v[u] = pos == newpos ? *reinterpret_cast<const int4*>(nk + ch * 16)
+                                          : ld_stream(base + (long long)pos * d + ch * 16);
+      }
+    };
+
+    int r_cur = 0;
+    int4 va[SG::LD], vb[SG::LD];
+    if (w0 < total) {
+      r_cur = req_of(w0, 0);
+      load_sub(w0, r_cur, 0, va);
+      load_sub(w0, r_cur, 1, vb);
+    }
+    for (int t = w0; t < total; t += W) {
+      const int ri = r_cur;
+      const int N = t_n[ri];
+      const int tile0 = (t - t_prefix[ri]) * SG::TILE;
+      const uint32_t thr = t_thr[ri];
+      if (ri != q_r) {
+        q_r = ri;
+        const int4* qs = reinterpret_cast<const int4*>(p.q_idx + (long long)ri * d);
+#pragma unroll
+        for (int c = 0; c < SG::CPL; ++c) q[c] = qs[cl * SG::CPL + c];
+      }
+      uint32_t* keys_out = p.s.scores + (long long)ri * p.score_stride;
+      const int tn = t + W;
+      const int rn = tn < total ? req_of(tn, ri) : ri;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        int4 (&v)[SG::LD] = half == 0 ? va : vb;
+        int acc[SG::NP];
+#pragma unroll
+        for (int j = 0; j < SG::NP; ++j) acc[j] = 0;
+#pragma unroll
+        for (int u = 0; u < SG::LD; ++u) {
+          const int j = u / SG::CPL;
+          const int4 qq = q[u % SG::CPL];
+          acc[j] = __dp4a(v[u].x, qq.x, acc[j]);
+          acc[j] = __dp4a(v[u].y, qq.y, acc[j]);
+          acc[j] = __dp4a(v[u].z, qq.z, acc[j]);
+          acc[j] = __dp4a(v[u].w, qq.w, acc[j]);
+        }
+        // the buffer is free: start the same half of this warp's next tile
+        if (tn < total) load_sub(tn, rn, half, v);
+#pragma unroll
+        for (int j = 0; j < SG::NP; ++j) {
+#pragma unroll
+          for (int o = 1; o < SG::LPP; o <<= 1) acc[j] += __shfl_xor_sync(FULL_MASK, acc[j], o);
+        }
+        // lane cl of a position group owns position groups j with j % LPP == cl
+        const int sub0 = tile0 + half * SG::SUB;
+        uint32_t ownk[SG::OWN];
+        int ownp[SG::OWN];
+#pragma unroll
+        for (int o = 0; o < SG::OWN; ++o) {
+          ownk[o] = 0;
+          ownp[o] = N;   // none
+        }
+#pragma unroll
+        for (int j = 0; j < SG::NP; ++j) {
+          if (j % SG::LPP == cl) {
+            const int o = j / SG::LPP;
+            ownp[o] = sub0 + j * SG::PPI + pg;
+            ownk[o] = (uint32_t)(acc[j] + IDX_KEY_BIAS);
+          }
+        }
+#pragma unroll
+        for (int o = 0; o < SG::OWN; ++o) {
+          const bool valid = ownp[o] < N;
+          if (valid) keys_out[ownp[o]] = ownk[o];
+          if (thr != 0u) {
+            const bool c = valid && ownk[o] >= thr;
+            const unsigned m = __ballot_sync(FULL_MASK, c);
+            if (m) {
+              unsigned base = 0;
+              if (lane == 0) base = atomicAdd(p.s.cand_cnt + ri, (unsigned)__popc(m));
+              base = __shfl_sync(FULL_MASK, base, 0);
+              const unsigned at = base + __popc(m & ((1u << lane) - 1u));
+              if (c && at < 2u * (unsigned)K)
+                p.s.cand[(long long)ri * 2 * K + at] = make_uint2((uint32_t)ownp[o], ownk[o]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) red_release_add(p.s.tiles_done + ri, 1u);
+      r_cur = rn;
+    }
+    HS_TRACE(p, 0, 2);
+    return;
+  }
+
+  // ======================= resolvers =======================
+  uint32_t* h = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
+  int32_t* sel = reinterpret_cast<int32_t*>(smem_raw + L.sel);
+  int32_t* slot_sel = reinterpret_cast<int32_t*>(smem_raw + L.slot);
+  int32_t* miss_i = reinterpret_cast<int32_t*>(smem_raw + L.miss_i);
+  int32_t* victim = reinterpret_cast<int32_t*>(smem_raw + L.victim);
+  int32_t* ord = reinterpret_cast<int32_t*>(smem_raw + L.ord);
+  int32_t* rev_s = reinterpret_cast<int32_t*>(smem_raw + L.rev);
+  uint8_t* used = smem_raw + L.used;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + L.bitmap);
+  uint32_t* lists = reinterpret_cast<uint32_t*>(smem_raw + L.lists);   // [warp][WCAP]
+  unsigned char* newrow = smem_raw + L.newrow;
+  unsigned char* newkey = newrow + align_up((size_t)g.row_bytes, 16);
+  static_assert(IDX_BINS % (4 * NT) == 0, "whole 16-byte histogram chunks per thread");
+
+  for (int ri = (int)blockIdx.x; ri < p.n_req; ri += p.n_resolvers) {
+    HS_TRACE_IF(p, 1, 0, tid == 0 && ri == (int)blockIdx.x);
+    int32_t* sel_out = p.sel_out ? p.sel_out + (long long)ri * K : nullptr;
+    const int req = p.req_ids ? p.req_ids[ri] : ri;
+    if (req < 0 || req >= g.max_requests) {
+      if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_REQ_RANGE);
+      if (sel_out)
+        for (int i = tid; i < K; i += NT) sel_out[i] = -1;
+      if (p.publish) {
+        __syncthreads();
+        if (tid == 0) {
+          p.s.kk_pub[ri] = 0;
+          __threadfence();
+          st_release(p.s.ready + ri, 1u);
+        }
+      }
+      __syncthreads();
+      continue;
+    }
+    const long long rl = (long long)req * g.n_layers + p.layer;
+    for (int j = tid; j < B; j += NT) used[j] = 0;
+
+    // ---- 0. every read that does not depend on the scores, issued together ----
+    const int32_t* order_g = p.s.order + rl * B;
+    for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(ord + 4 * c4, order_g + 4 * c4);
+    if (L.rev_smem) {
+      const int32_t* rev_g = p.s.reverse + rl * B;
+      for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(rev_s + 4 * c4, rev_g + 4 * c4);
+    }
+    if (p.new_kv) {
+      for (int v = tid; v < g.row_bytes / 16; v += NT)
+        cp_async_16(newrow + 16 * v,
+                    reinterpret_cast<const unsigned char*>(p.new_kv + (long long)ri * g.row_elems) + 16 * v);
+      if (tid < g.d_idx / 16) cp_async_16(newkey + 16 * tid, p.new_keys + (long long)ri * g.d_idx + 16 * tid);
+    }
+    if (tid == 0) {
+      const int len = p.s.length[rl];
+      sh.len = len;
+      sh.t_step = p.s.step[rl];
+      sh.thr = p.s.cand_thr[rl];
+      int N = len;
+      if (p.new_kv) {
+        if (len + 1 <= g.max_context) N = len + 1;
+        else set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
+      }
+      sh.N = N;
+      sh.ok = 1;
+      if (N == 0) set_error(p.s.dev_error, HS_DEVERR_EMPTY);   // nothing to attend: the output is 0
+      sh.thr_next = 0u;
+      if (N > K) {   // wait until every tile of this request is scored
+        const unsigned ntile = (unsigned)((N + SG::TILE - 1) / SG::TILE);
+        if (!wait_counter(p.s.tiles_done + ri, ntile)) {
+          set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+          sh.ok = 0;
+        }
+        p.s.tiles_done[ri] = 0;   // ready for the next call
+        sh.cnt = (int)min(__ldcg(p.s.cand_cnt + ri), 0x7fffffffu);
+        p.s.cand_cnt[ri] = 0;
+      } else {
+        sh.cnt = 0;
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    HS_TRACE_IF(p, 1, 1, tid == 0 && ri == (int)blockIdx.x);
+    const int len = sh.len, N = sh.N, t_step = sh.t_step;
+    const bool appended = N > len;
+    const int kk = sh.ok ? min(K, N) : 0;
+
+    // ======================= 1. top-k, ascending =======================
+    if (!sh.ok) {
+      // scores incomplete: nothing selected (the output of this request is 0)
+    } else if (N <= K) {
+      for (int i = tid; i < N; i += NT) sel[i] = i;
+    } else {
+      const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
+      const int cap = 2 * K;
+      // (the candidate path's tie bitmap lives in the per-warp lists)
+      const bool use_cand = L.fast && N <= FAST_MAX_N && (N + 31) / 32 <= WCAP * NWARP && sh.thr != 0u &&
+                            sh.cnt >= K && sh.cnt <= cap;
+      const bool fast = !use_cand && L.fast && N <= FAST_MAX_N;
+      const uint2* cl = p.s.cand + (long long)ri * cap;   // this call's candidates
+      const int32_t* page_rl = p.s.page + rl * g.max_context;
+      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      // first-digit histogram: of the listed keys, or of all keys
+      if (use_cand) {
+        for (int i = tid; i < sh.cnt; i += NT) {
+          const uint2 c = __ldcg(&cl[i]);
+          atomicAdd(&h[c.y >> 12], 1u);
+          // every selected position is a candidate: warm its page-table entry for the hit test
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(page_rl + c.x));
+        }
+      } else {
+        const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
+        const int n4 = N >> 2;
+        constexpr int UA = 8;
+        for (int i0 = tid; i0 < n4; i0 += UA * NT) {
+          uint4 v[UA];
+#pragma unroll
+          for (int u = 0; u < UA; ++u) {
+            const int i = i0 + u * NT;
+            v[u] = i < n4 ? __ldcg(k4 + i) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < UA; ++u)
+            if (i0 + u * NT < n4) {
+              atomicAdd(&h[v[u].x >> 12], 1u);
+              atomicAdd(&h[v[u].y >> 12], 1u);
+              atomicAdd(&h[v[u].z >> 12], 1u);
+              atomicAdd(&h[v[u].w >> 12], 1u);
+            }
+        }
+        for (int i = 4 * n4 + tid; i < N; i += NT) atomicAdd(&h[__ldcg(keys + i) >> 12], 1u);
+      }
+      __syncthreads();
+      // the digit of the k-th largest key, and the digit above which ~1.25 k keys
+      // lie: the next call lists keys from there on (exact whenever >= k clear it)
+      const int k_next = (int)min((long long)N, (long long)K + K / 4);
+      select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
+      const int listed = use_cand ? sh.cnt : N;
+      if (listed >= k_next) {
+        select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
+        if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
+      } else if (tid == 0) {
+        sh.thr_next = sh.thr;   // the list held fewer: keep the threshold that gave >= k
+      }
+      const int b1 = sh.b1, above1 = sh.above1;
+      // listing costs the scorers about as much per position as the full pass
+      // costs here, so it pays only while the context is short relative to k
+      if (tid == 0 && N > CAND_MAX_N_PER_K * K) sh.thr_next = 0u;
+      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      HS_TRACE_IF(p, 1, 2, tid == 0 && ri == (int)blockIdx.x);
+      // per-thread contiguous ranges (the rescan path)
+      const int per = ((N + NT - 1) / NT + 3) & ~3;
+      const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
+      // per-warp contiguous chunks of 128 positions (the one-pass path)
+      const int wid = warp;
+      const int NC = (N + 127) >> 7;
+      const int c0 = (int)((long long)wid * NC / NWARP), c1 = (int)((long long)(wid + 1) * NC / NWARP);
+      uint32_t* wl = lists + wid * WCAP;
+      int wcnt = 0;       // entries of this warp's list (warp-uniform)
+      int lane_gt = 0;    // keys above digit b1 seen by this lane
+      bool overflow = false;
+      uint32_t* tiebm = lists;                            // the candidate path's second bitmap
+      const int NWd = (N + 31) >> 5;
+      if (use_cand) {
+        for (int qq = tid; qq < NWd; qq += NT) {
+          bitmap[qq] = 0u;
+          tiebm[qq] = 0u;
+        }
+        for (int i = tid; i < sh.cnt; i += NT) {
+          const uint2 c = __ldcg(&cl[i]);
+          if ((int)(c.y >> 12) == b1) atomicAdd(&h[c.y & 4095u], 1u);
+        }
+      } else if (fast) {
+        const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+        constexpr int UC = 8;   // chunks in flight per lane
+        for (int cb = c0; cb < c1; cb += UC) {
+          uint4 v[UC];
+#pragma unroll
+          for (int u = 0; u < UC; ++u) {
+            const int pos = 128 * (cb + u) + 4 * lane;
+            v[u] = (cb + u < c1 && pos < N) ? __ldcg(k4 + (cb + u) * 32 + lane) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < UC; ++u) {
+            if (cb + u >= c1) break;   // warp-uniform
+            const int pos = 128 * (cb + u) + 4 * lane;
+            const uint32_t kv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t nib_gt = 0, nib_eq = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (pos + e < N) {
+                const int dg = (int)(kv[e] >> 12);
+                nib_gt |= (uint32_t)(dg > b1) << e;
+                if (dg == b1) {
+                  nib_eq |= 1u << e;
+                  atomicAdd(&h[kv[e] & 4095u], 1u);
+                }
+              }
+            }
+            lane_gt += __popc(nib_gt);
+            uint32_t word = nib_gt << (4 * (lane & 7));
+            word |= __shfl_xor_sync(FULL_MASK, word, 1);
+            word |= __shfl_xor_sync(FULL_MASK, word, 2);
+            word |= __shfl_xor_sync(FULL_MASK, word, 4);
+            if ((lane & 7) == 0) bitmap[4 * (cb + u) + (lane >> 3)] = word;
+            if (__any_sync(FULL_MASK, nib_eq != 0)) {   // list the digit-b1 keys in position order
+              const int cnt = __popc(nib_eq);
+              int incl = cnt;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(FULL_MASK, incl, o);
+                if (lane >= o) incl += n;
+              }
+              int at = wcnt + incl - cnt;
+              for (int e = 0; e < 4; ++e)
+                if ((nib_eq >> e) & 1u) {
+                  if (at < WCAP) wl[at] = ((uint32_t)(pos + e) << 12) | (kv[e] & 4095u);
+                  else overflow = true;
+                  ++at;
+                }
+              wcnt += __shfl_sync(FULL_MASK, incl, 31);
+            }
+          }
+        }
+      } else {   // second-digit histogram only; the counts and the emission rescan the keys
+        const int n4 = N >> 2;
+        const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+        constexpr int UA = 8;
+        for (int i0 = tid; i0 < n4; i0 += UA * NT) {
+          uint4 v[UA];
+#pragma unroll
+          for (int u = 0; u < UA; ++u) {
+            const int i = i0 + u * NT;
+            v[u] = i < n4 ? __ldcg(k4 + i) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < UA; ++u) {
+            if ((int)(v[u].x >> 12) == b1) atomicAdd(&h[v[u].x & 4095u], 1u);
+            if ((int)(v[u].y >> 12) == b1) atomicAdd(&h[v[u].y & 4095u], 1u);
+            if ((int)(v[u].z >> 12) == b1) atomicAdd(&h[v[u].z & 4095u], 1u);
+            if ((int)(v[u].w >> 12) == b1) atomicAdd(&h[v[u].w & 4095u], 1u);
+          }
+        }
+        for (int i = 4 * n4 + tid; i < N; i += NT) {
+          const uint32_t v = __ldcg(keys + i);
+          if ((int)(v >> 12) == b1) atomicAdd(&h[v & 4095u], 1u);
+        }
+      }
+      // the barrier is taken on every path (it orders the histogram atomics above
+      // before the digit select below), then decides whether the lists are usable
+      const bool any_overflow = __syncthreads_or(overflow);
+      const bool use_lists = fast && !any_overflow;
+      HS_TRACE_IF(p, 1, 3, tid == 0 && ri == (int)blockIdx.x);
+      select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
+      const int b2 = sh.b2;
+      const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)b2;
+      const int need_eq = K - (above1 + sh.above2);   // >= 1
+      if (use_cand) {
+        // mark the taken keys (> threshold) and the threshold ties in two bitmaps
+        for (int i = tid; i < sh.cnt; i += NT) {
+          const uint2 c = __ldcg(&cl[i]);
+          if (c.y > vstar) atomicOr(&bitmap[c.x >> 5], 1u << (c.x & 31));
+          else if (c.y == vstar) atomicOr(&tiebm[c.x >> 5], 1u << (c.x & 31));
+        }
+        __syncthreads();
+        const int q0w = (int)((long long)wid * NWd / NWARP), q1w = (int)((long long)(wid + 1) * NWd / NWARP);
+        int n_gt = 0, n_eq = 0;
+        for (int qq = q0w + lane; qq < q1w; qq += 32) {
+          n_gt += __popc(bitmap[qq]);
+          n_eq += __popc(tiebm[qq]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          n_gt += __shfl_xor_sync(FULL_MASK, n_gt, o);
+          n_eq += __shfl_xor_sync(FULL_MASK, n_eq, o);
+        }
+        const int2 wb =
+            block_exclusive_scan2<NT>(lane == 0 ? n_gt : 0, lane == 0 ? n_eq : 0, sh.scan, nullptr, nullptr);
+        const int gt_before = __shfl_sync(FULL_MASK, wb.x, 0), eq_before = __shfl_sync(FULL_MASK, wb.y, 0);
+        int out = gt_before + min(eq_before, need_eq);
+        int tie_run = eq_before;   // threshold ties before this group of words
+        for (int qg = q0w; qg < q1w; qg += 32) {
+          const int qq = qg + lane;
+          uint32_t m = qq < q1w ? bitmap[qq] : 0u;
+          uint32_t tb = qq < q1w ? tiebm[qq] : 0u;
+          const int nt = __popc(tb);
+          int tincl = nt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(FULL_MASK, tincl, o);
+            if (lane >= o) tincl += n;
+          }
+          int rank = tie_run + tincl - nt;   // ties take the lowest positions first
+          while (tb) {
+            const int bb = __ffs(tb) - 1;
+            tb &= tb - 1;
+            if (rank < need_eq) m |= 1u << bb;
+            ++rank;
+          }
+          tie_run += __shfl_sync(FULL_MASK, tincl, 31);
+          const int cnt = __popc(m);
+          int incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(FULL_MASK, incl, o);
+            if (lane >= o) incl += n;
+          }
+          int o = out + incl - cnt;
+          while (m) {
+            const int bb = __ffs(m) - 1;
+            m &= m - 1;
+            if (o < K) sel[o++] = 32 * qq + bb;
+          }
+          out += __shfl_sync(FULL_MASK, incl, 31);
+        }
+      } else if (use_lists) {
+        int n_gt = lane_gt, n_eq = 0;
+        for (int qq = lane; qq < wcnt; qq += 32) {
+          const int lo = (int)(wl[qq] & 4095u);
+          n_gt += lo > b2;
+          n_eq += lo == b2;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          n_gt += __shfl_xor_sync(FULL_MASK, n_gt, o);
+          n_eq += __shfl_xor_sync(FULL_MASK, n_eq, o);
+        }
+        const int2 wb =
+            block_exclusive_scan2<NT>(lane == 0 ? n_gt : 0, lane == 0 ? n_eq : 0, sh.scan, nullptr, nullptr);
+        const int gt_before = __shfl_sync(FULL_MASK, wb.x, 0), eq_before = __shfl_sync(FULL_MASK, wb.y, 0);
+        // emission: lane l owns bitmap word q0 + l of each group of 32 words
+        int out = gt_before + min(eq_before, need_eq);
+        int tie_run = eq_before;   // ties before the current list entry (position order)
+        int qe = 0;                // next list entry
+        const int w_end = 4 * c1;
+        for (int q0 = 4 * c0; q0 < w_end; q0 += 32) {
+          const int qq = q0 + lane;
+          uint32_t m = qq < w_end ? bitmap[qq] : 0u;
+          for (; qe < wcnt; ++qe) {   // list entries of this group of words, in order
+            const uint32_t e = wl[qe];
+            const int pos = (int)(e >> 12);
+            if ((pos >> 5) >= q0 + 32) break;
+            const int lo = (int)(e & 4095u);
+            const bool mine = (pos >> 5) == qq;
+            if (lo > b2) {
+              if (mine) m |= 1u << (pos & 31);
+            } else if (lo == b2) {
+              if (mine && tie_run < need_eq) m |= 1u << (pos & 31);
+              ++tie_run;
+            }
+          }
+          const int cnt = __popc(m);
+          int incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(FULL_MASK, incl, o);
+            if (lane >= o) incl += n;
+          }
+          int o = out + incl - cnt;
+          while (m) {
+            const int bb = __ffs(m) - 1;
+            m &= m - 1;
+            if (o < K) sel[o++] = 32 * qq + bb;
+          }
+          out += __shfl_sync(FULL_MASK, incl, 31);
+        }
+      } else {
+        int n_gt = 0, n_eq = 0;
+        for (int j = j0; j < j1; j += 4) {   // multiples of 4 in bounds (padded rows)
+          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(keys + j));
+          const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (j + e < j1) {
+              n_gt += kv[e] > vstar;
+              n_eq += kv[e] == vstar;
+            }
+        }
+        const int2 before = block_exclusive_scan2<NT>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+        int o = before.x + min(before.y, need_eq);
+        int eq_rank = before.y;
+        for (int j = j0; j < j1; j += 4) {
+          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(keys + j));
+          const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (j + e < j1) {
+              bool take = kv[e] > vstar;
+              if (kv[e] == vstar) {
+                take = eq_rank < need_eq;
+                ++eq_rank;
+              }
+              if (take && o < K) sel[o++] = j + e;
+            }
+        }
+      }
+    }
+    __syncthreads();
+    HS_TRACE_IF(p, 1, 4, tid == 0 && ri == (int)blockIdx.x);
+    int32_t* sel_g = p.s.sel + (long long)ri * K;
+    for (int i = tid; i < K; i += NT) {
+      const int v = i < kk ? sel[i] : -1;
+      if (i < kk) sel_g[i] = v;
+      if (sel_out) sel_out[i] = v;
+    }
+
+    // ======================= 2. RESOLVE metadata =======================
+    int32_t* page = p.s.page + rl * g.max_context;
+    int32_t* reverse = p.s.reverse + rl * B;
+    int32_t* stamp = p.s.stamp + rl * B;
+    int32_t* order = p.s.order + rl * B;
+    int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
+    const int t = t_step;
+    int m = 0;
+    const bool pull = p.fetch_mode == 1;   // else the attention kernel copies the missed rows
+    bool bad = false;
+    if (kk > 0) {
+      // hit test: independent page-table gathers, four in flight per thread
+      for (int i0 = tid; i0 < kk; i0 += 4 * NT) {
+        int pos[4], s4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * NT;
+          pos[u] = i < kk ? sel[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) s4[u] = (pos[u] >= 0 && pos[u] < N) ? page[pos[u]] : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * NT;
+          if (i < kk) {
+            if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
+            slot_sel[i] = s4[u];
+            if (s4[u] >= 0 && s4[u] < B) used[s4[u]] = 1;
+            // a miss: start moving its host row over the link into L2 now, line by
+            // line (the copy then reads it from L2); the row appended by this call
+            // comes from its input copy
+            if (s4[u] < 0 && pos[u] >= 0 && pos[u] < N && !(appended && pos[u] == len)) {
+              const unsigned char* src = reinterpret_cast<const unsigned char*>(p.s.host_kv) +
+                                         ((size_t)rl * g.max_context + pos[u]) * g.row_bytes;
+              for (int b = 0; b < g.row_bytes; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
+            }
+          }
+        }
+      }
+    }
+    if (__syncthreads_or(bad)) {
+      // inconsistent metadata: publish nothing usable for this request
+      if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
+      if (p.publish && tid == 0) {
+        p.s.kk_pub[ri] = 0;
+        __threadfence();
+        st_release(p.s.ready + ri, 1u);
+      }
+      __syncthreads();
+      continue;
+    }
+    HS_TRACE_IF(p, 1, 5, tid == 0 && ri == (int)blockIdx.x);
+    // misses in ascending selection order, and the unpinned entries of the LRU list
+    const int per_i = (kk + NT - 1) / NT;
+    const int i0 = min(kk, tid * per_i), i1 = min(kk, i0 + per_i);
+    const int per_j = (B + NT - 1) / NT;
+    const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
+    int nm = 0, nc = 0;
+    for (int i = i0; i < i1; ++i) nm += slot_sel[i] < 0;
+    for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
+    const int2 mc = block_exclusive_scan2<NT>(nm, nc, sh.scan, &m, nullptr);
+    int mb = mc.x;
+    for (int i = i0; i < i1; ++i)
+      if (slot_sel[i] < 0) miss_i[mb++] = i;
+    if (p.replacement == HS_REPLACE_RANDOM) {
+      // victims: the m unpinned slots ranked first (never-filled, then smallest
+      // (key, slot)), in ascending slot order.  Two 12-bit digit selections over
+      // the 24-bit ranks, then each thread takes its ranks above the threshold
+      // and, in slot order, the threshold ties still needed.  "Never filled" is
+      // read from the reverse map as it was before this call.
+      if (m > 0) {
+        const unsigned long long seed = p.replacement_seed;
+        auto rank_of = [&](int j) {
+          const int old = L.rev_smem ? rev_s[j] : reverse[j];
+          return random_ikey(seed, rl, t, j, old < 0);
+        };
+        for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) atomicAdd(&h[rank_of(j) >> 12], 1u);
+        __syncthreads();
+        select_digit(h, m, sh.scan, &sh.rb1, &sh.rabove1);
+        const int rb1 = sh.rb1, rab1 = sh.rabove1;
+        for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) {
+            const uint32_t k = rank_of(j);
+            if ((int)(k >> 12) == rb1) atomicAdd(&h[k & 4095u], 1u);
+          }
+        __syncthreads();
+        select_digit(h, m - rab1, sh.scan, &sh.rb2, &sh.rabove2);
+        const uint32_t vstar = ((uint32_t)rb1 << 12) | (uint32_t)sh.rb2;
+        const int need_eq = m - rab1 - sh.rabove2;   // >= 1
+        int n_gt = 0, n_eq = 0;
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) {
+            const uint32_t k = rank_of(j);
+            n_gt += k > vstar;
+            n_eq += k == vstar;
+          }
+        const int2 ex = block_exclusive_scan2<NT>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+        int eq_rank = ex.y;                        // threshold ties before this thread
+        int o = ex.x + min(ex.y, need_eq);         // victims before this thread
+        for (int j = j0; j < j1; ++j)
+          if (used[j] == 0) {
+            const uint32_t k = rank_of(j);
+            const bool take = k > vstar || (k == vstar && eq_rank++ < need_eq);
+            if (take) {
+              victim[o++] = j;
+              used[j] = 2;
+            }
+          }
+      }
+    } else {
+      // victims: the first m unpinned entries of the (stamp, slot)-sorted list
+      int cb = mc.y;
+      for (int j = j0; j < j1 && cb < m; ++j) {
+        const int sl = ord[j];
+        if (used[sl] == 0) {
+          victim[cb++] = sl;
+          used[sl] = 2;
+        }
+      }
+    }
+    __syncthreads();
+    HS_TRACE_IF(p, 1, 6, tid == 0 && ri == (int)blockIdx.x);
+    // evict, then record the new residents (stores only); slot of every selected
+    // row, misses flagged when the attention kernel copies them
+    for (int qq = tid; qq < m; qq += NT) {
+      const int v = victim[qq];
+      const int i = miss_i[qq];
+      const int pnew = sel[i];
+      const int old = L.rev_smem ? rev_s[v] : reverse[v];
+      if (old >= 0 && old < g.max_context) page[old] = -1;
+      reverse[v] = pnew;
+      page[pnew] = v;
+      slot_sel[i] = v;
+      // the appended token's row is in shared memory: it goes to its slot here
+      miss_i[qq] = (pull || (appended && pnew == len)) ? i : (i | HS_SLOT_MISS_FLAG);
+    }
+    __syncthreads();
+    for (int i = tid; i < kk; i += NT) sos[i] = slot_sel[i];
+    __syncthreads();
+    for (int qq = tid; qq < m; qq += NT)
+      if (miss_i[qq] & HS_SLOT_MISS_FLAG) sos[miss_i[qq] & ~HS_SLOT_MISS_FLAG] = victim[qq] | HS_SLOT_MISS_FLAG;
+
+    // ======================= 3. rows this kernel copies into their slots =======================
+    // fetch mode 1: every missed row from the host copy; otherwise only the
+    // appended token's (from its input copy)
+    {
+      const int rvec = g.row_bytes / 16;
+      const unsigned char* src_base =
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
+      unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * B * g.row_bytes;
+      if (pull) {
+        const long long total = (long long)m * rvec;
+        constexpr int U = 8;   // host reads in flight per thread
+        for (long long e0 = tid; e0 < total; e0 += (long long)U * NT) {
+          int4 v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const long long e = e0 + (long long)u * NT;
+            if (e < total) {
+              const int qq = (int)(e / rvec);
+              const int cidx = (int)(e - (long long)qq * rvec);
+              const int pos = sel[miss_i[qq]];
+              v[u] = (appended && pos == len)
+                         ? reinterpret_cast<const int4*>(newrow)[cidx]
+                         : *reinterpret_cast<const int4*>(src_base + (size_t)pos * g.row_bytes + cidx * 16);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const long long e = e0 + (long long)u * NT;
+            if (e < total) {
+              const int qq = (int)(e / rvec);
+              const int cidx = (int)(e - (long long)qq * rvec);
+              *reinterpret_cast<int4*>(dst_base + (size_t)victim[qq] * g.row_bytes + cidx * 16) = v[u];
+            }
+          }
+        }
+      } else if (appended && m > 0 && sel[miss_i[m - 1] & ~HS_SLOT_MISS_FLAG] == len) {
+        // the appended token is the highest position: if it missed, it is the last miss
+        for (int v = tid; v < rvec; v += NT)
+          *reinterpret_cast<int4*>(dst_base + (size_t)victim[m - 1] * g.row_bytes + v * 16) =
+              reinterpret_cast<const int4*>(newrow)[v];
+      }
+      fence_proxy_async_global();   // generic-proxy slot writes, read by bulk copies
+    }
+    // ======================= 4. publication =======================
+    __syncthreads();
+    HS_TRACE_IF(p, 1, 7, tid == 0 && ri == (int)blockIdx.x);
+    if (p.publish && tid == 0) {
+      p.s.kk_pub[ri] = kk;
+      __threadfence();
+      if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, 1u);
+    }
+
+    // ======================= 5. metadata after publication =======================
+    // LRU and random: every used slot is refreshed; FIFO: only the filled ones (used == 2)
+    const bool fifo = p.replacement == HS_REPLACE_FIFO;
+    auto refreshed = [&](uint8_t u) { return fifo ? u == 2 : u != 0; };
+    if (kk > 0) {
+      for (int i = tid; i < kk; i += NT) {
+        const int sl = slot_sel[i];
+        if (refreshed(used[sl])) stamp[sl] = t;
+      }
+      // new list: slots not refreshed keep their order, refreshed slots (all with
+      // the newest stamp) go last by slot
+      int nu = 0, nus = 0;
+      for (int j = j0; j < j1; ++j) nu += !refreshed(used[ord[j]]);
+      for (int sl = j0; sl < j1; ++sl) nus += refreshed(used[sl]);
+      int n_unused;
+      const int2 un = block_exclusive_scan2<NT>(nu, nus, sh.scan, &n_unused, nullptr);
+      int ub = un.x;
+      for (int j = j0; j < j1; ++j) {
+        const int sl = ord[j];
+        if (!refreshed(used[sl])) order[ub++] = sl;
+      }
+      int sb = n_unused + un.y;
+      for (int sl = j0; sl < j1; ++sl)
+        if (refreshed(used[sl])) order[sb++] = sl;
+      if (tid == 0) {
+        p.s.step[rl] = t + 1;
+        red_add_u64(&p.s.hits[rl], (unsigned long long)(kk - m));
+        red_add_u64(&p.s.misses[rl], (unsigned long long)m);
+        red_add_u64(&p.s.glob[0], (unsigned long long)m * g.row_bytes);
+      }
+    }
+    // the appended token: key to the HBM store, row to the pinned host copy
+    if (appended) {
+      const int rvec = g.row_bytes / 16;
+      int4* dst = reinterpret_cast<int4*>(p.s.host_kv + (rl * g.max_context + len) * g.row_elems);
+      for (int v = tid; v < rvec; v += NT) dst[v] = reinterpret_cast<const int4*>(newrow)[v];
+      if (tid < g.d_idx / 16)
+        reinterpret_cast<int4*>(p.s.idx_keys + (rl * g.max_context + len) * g.d_idx)[tid] =
+            reinterpret_cast<const int4*>(newkey)[tid];
+    }
+    // lengths and thresholds: only once every CTA of the launch has read them
+    if (tid == 0) {
+      if (!wait_counter(&p.s.sync[0], (unsigned)(p.sel_grid - p.n_resolvers))) {
+        set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+      } else {
+        if (appended) {
+          p.s.length[rl] = N;
+          red_add_u64(&p.s.glob[1], (unsigned long long)g.row_bytes);
+        }
+        if (sh.ok) p.s.cand_thr[rl] = sh.thr_next;
+      }
+    }
+    __syncthreads();
+    HS_TRACE_IF(p, 1, 8, tid == 0 && ri == (int)blockIdx.x);
+  }
+  // the last resolver to finish resets the launch's shared counters (once every
+  // scorer CTA has counted itself in)
+  if (tid == 0) {
+    const unsigned prev = atom_acq_rel_add(&p.s.sync[1], 1u);
+    if (prev + 1 == (unsigned)p.n_resolvers) {
+      if (!wait_counter(&p.s.sync[0], (unsigned)(p.sel_grid - p.n_resolvers)))
+        set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+      p.s.sync[0] = 0;
+      p.s.sync[1] = 0;
+    }
+  }
+}
+
+template <int NCH>
+static cudaError_t run_select(const DecodeParams* p, size_t smem, cudaStream_t st) {
+  auto kern = select_kernel<NCH>;
+  if (p == nullptr) return allow_smem(kern, smem);
+  return launch_pdl(kern, dim3(p->sel_grid), dim3(NT), smem, st, *p);
+}
+
+static cudaError_t dispatch_select(int d_idx, const DecodeParams* p, size_t smem, cudaStream_t st) {
+  switch (d_idx) {
+    case 16: return run_select<1>(p, smem, st);
+    case 32: return run_select<2>(p, smem, st);
+    case 64: return run_select<4>(p, smem, st);
+    case 128: return run_select<8>(p, smem, st);
+    case 256: return run_select<16>(p, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t prepare_select(const Geometry& g, size_t smem) { return dispatch_select(g.d_idx, nullptr, smem, 0); }
+
+cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st) {
+  return dispatch_select(p.g.d_idx, &p, smem, st);
+}
+
+}  // namespace hs

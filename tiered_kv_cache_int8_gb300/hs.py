@@ -27,13 +27,13 @@ HS_DEVERR_EMPTY = 0x4
 HS_DEVERR_TIMEOUT = 0x8
 HS_DEVERR_METADATA = 0x10
 
-HS_K_APPEND, HS_K_INDEXER, HS_K_TOPK_RESOLVE, HS_K_ATTENTION, HS_K_COUNT = 0, 1, 2, 3, 4
+HS_K_APPEND, HS_K_SELECT, HS_K_ATTENTION, HS_K_COUNT = 0, 1, 2, 3
 
 HS_REPLACE_LRU = 0
 HS_REPLACE_FIFO = 1
 HS_REPLACE_RANDOM = 2
 REPLACEMENT = {"lru": HS_REPLACE_LRU, "fifo": HS_REPLACE_FIFO, "random": HS_REPLACE_RANDOM}
-KERNEL_NAMES = ("append", "indexer", "topk_resolve", "attention")
+KERNEL_NAMES = ("append", "select", "attention")
 
 # the symbols include/hs.h declares
 EXPORTED = ("hs_create", "hs_destroy", "hs_append", "hs_decode_layer", "hs_stats", "hs_snapshot",
