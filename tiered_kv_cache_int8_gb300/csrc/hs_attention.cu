@@ -1,8 +1,8 @@
 // Sparse attention over the selected rows (GQA, head dim 128), fused with the
 // host fetch of the missed rows RESOLVE left to it and with the merge of its
 // split partials: a persistent, warp-specialised flash-decode kernel that works
-// through a queue of chunks and merge tasks while the select kernel is still
-// resolving later requests.  (The merge kernel further down serves latent rows.)
+// through a queue of chunks while the select kernel is still resolving later
+// requests.  (The merge kernel further down serves latent rows.)
 //
 // Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
 // for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
@@ -15,21 +15,20 @@
 // Design (sm_103a).  HBM-bound (each K/V byte is used by the h_q / h_kv query
 // heads of its group only):
 //  * Persistent grid, one CTA per SM, launched as a programmatic dependent of
-//    the select kernel and started on the SMs its scorers free.  Work items form
-//    one queue, taken with a global atomic counter: for each request, its chunks
-//    (64 selected rows, in selection order), and one request later its merge
-//    tasks (8 heads each).  Requests are published in about queue order, so a
-//    CTA rarely waits; a chunk waits (bounded) for its request's ready flag, a
-//    merge task for its request's chunk counter.  Every wait is on an item
-//    earlier in the queue, and every CTA runs its items in queue order, so the
-//    waits always end.
-//  * Warp 8 (loader) reads the slots of a unit (16 rows per warp slice) and
-//    copies every hit row (all kv heads: one contiguous hot slot) HBM -> shared
-//    memory with one 1-D bulk async copy into a row-padded layout (16 extra bytes
-//    per row put the 8 rows of an ldmatrix phase in 8 bank groups), and every
-//    missed row from the mapped pinned host copy with 16-byte cp.async (RESOLVE
-//    already started those rows moving into L2); up to 3 stages, full/empty
-//    mbarriers, a descriptor per stage.
+//    the select kernel and started on the SMs its scorers free.  The work is a
+//    queue of chunks (64 selected rows of one request, in selection order),
+//    request after request, taken with a global atomic counter.  A chunk waits
+//    (bounded) for its request's ready flag; requests are published in about
+//    queue order, so a CTA rarely waits.
+//  * Warp 8 (loader) reads the slots of a whole chunk at once, then per unit
+//    (16 rows per warp slice) copies every hit row (all kv heads: one
+//    contiguous hot slot) HBM -> shared memory with one 1-D bulk async copy into
+//    a row-padded layout (16 extra bytes per row put the 8 rows of an ldmatrix
+//    phase in 8 bank groups).  Warp 9 (fetcher) copies the unit's missed rows
+//    from the mapped pinned host copy with 16-byte cp.async (RESOLVE already
+//    started those rows moving into L2), so slow host reads never hold up the
+//    loader's own loads.  Up to 3 stages, full/empty mbarriers, a descriptor
+//    per stage.
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
 //    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
 //    with the group's query heads as the 16 M rows (zero-padded); K and V
@@ -37,12 +36,13 @@
 //    softmax in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P enters
 //    the second product as bf16.  Consumer warp 0 writes each fetched row into its
 //    hot slot (bulk shared -> global copy), so later steps hit.
-//  * Each (chunk, slice) writes a partial (m, l, o); a merge task combines its
-//    heads' partials in chunk order and writes bf16.  Rows are visited in
-//    ascending selection order and chunks depend only on k_eff, so the output is
-//    bit-identical for any B and any schedule.
-//  * Counters of the call reset themselves: the last merge task of a request
-//    clears its flags, the last CTA to leave clears the queue.  Each CTA waits
+//  * Each (chunk, slice) writes a partial (m, l, o) and counts the chunk done;
+//    the CTA that completes a request's last chunk merges all its partials in
+//    chunk order and writes bf16 — no CTA ever waits for another's chunk.  Rows
+//    are visited in ascending selection order and chunks depend only on k_eff,
+//    so the output is bit-identical for any B and any schedule.
+//  * Counters of the call reset themselves: the merging CTA clears its
+//    request's flags, the last CTA to leave clears the queue.  Each CTA waits
 //    for the select kernel to complete before it exits, so the next launch on the
 //    stream sees both kernels finished.
 #include <cuda_bf16.h>
@@ -56,15 +56,16 @@ namespace {
 constexpr int D = 128;
 constexpr int NCONS = 8;                   // consumer warps
 constexpr int LOADER = NCONS;              // warp index of the loader
-constexpr int THREADS = (NCONS + 1) * 32;
+constexpr int FETCHER = NCONS + 1;         // warp index of the host fetcher
+constexpr int THREADS = (NCONS + 2) * 32;
 constexpr int MAX_STAGES = 3;
 constexpr int TILE_MAX = 128;   // rows of a unit at h_kv = 1 (8 slices of 16)
 constexpr int CHUNK_ROWS_MIN = 64;
-constexpr int MERGE_HEADS = 8;
+constexpr int MERGE_HEADS = 8;  // heads merged per pass (one warp each)
 constexpr int BAR_CONS = 1;     // named barrier: the 256 consumer threads
 constexpr int BAR_VOTE = 2;     // named barrier: the consumers' vote on a failed wait
 
-enum { DESC_UNIT = 0, DESC_MERGE = 1, DESC_STOP = 2 };
+enum { DESC_UNIT = 0, DESC_STOP = 2 };
 struct __align__(16) Desc {
   int type, ri, c, row0, nr, first, last, pad;
 };
@@ -81,23 +82,25 @@ __host__ __device__ inline int att_nchunk(const Geometry& g) {
 }
 
 struct AttLayout {
-  size_t bar, desc, slot_tab, stage, stage_bytes, total;
+  size_t bar, desc, slot_tab, mpos, stage, stage_bytes, total;
 };
 
-// Shared memory: barriers | per-stage descriptors | per-stage hot slots of
-// fetched rows | stages.
+// Shared memory: barriers | per-stage descriptors | per-stage hot slots and host
+// positions of fetched rows | stages.
 __host__ __device__ inline AttLayout att_layout(const Geometry& g, int nstage) {
   AttLayout L;
   const int tile = att_tile(g);
   const size_t row_stride = (size_t)g.row_bytes + ATT_ROW_PAD;
   size_t off = 0;
   L.bar = off;
-  off += 8 * (2 * MAX_STAGES) + 16;   // full/empty barriers, abort flag
+  off += 8 * (3 * MAX_STAGES) + 16;   // full/empty/descriptor barriers, flags
   off = align_up(off, 128);
   L.desc = off;
   off += sizeof(Desc) * MAX_STAGES;
   L.slot_tab = off;
   off += (size_t)MAX_STAGES * TILE_MAX * 4;   // hot slot of each fetched row (-1: none)
+  L.mpos = off;
+  off += (size_t)MAX_STAGES * TILE_MAX * 4;   // host position of each fetched row (-1: none)
   off = align_up(off, 128);
   L.stage = off;
   L.stage_bytes = align_up((size_t)tile * row_stride, 128);
@@ -171,39 +174,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// Work item i of the queue [chunks of r0][chunks of r1, merges of r0] ...
-// [chunks of r_{n-1}, merges of r_{n-2}][merges of r_{n-1}].
-struct Item {
-  int merge, ri, idx;
-};
-__device__ __forceinline__ Item decode_item(long long i, int n_req, int nchk, int nmt) {
-  Item it;
-  if (i < nchk) {
-    it.merge = 0;
-    it.ri = 0;
-    it.idx = (int)i;
-    return it;
-  }
-  const long long per = nchk + nmt;
-  const long long i2 = i - nchk;
-  const int b = 1 + (int)(i2 / per);
-  const int o = (int)(i2 % per);
-  if (b == n_req) {
-    it.merge = 1;
-    it.ri = n_req - 1;
-    it.idx = o;
-  } else if (o < nchk) {
-    it.merge = 0;
-    it.ri = b;
-    it.idx = o;
-  } else {
-    it.merge = 1;
-    it.ri = b - 1;
-    it.idx = o - nchk;
-  }
-  return it;
-}
-
 }  // namespace
 
 int attention_parts(const Geometry& g) {
@@ -225,25 +195,27 @@ template <int G, int HKV>
 __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, int nstage) {
   constexpr int NSLICE = NCONS / HKV;
   constexpr int TILE = ATT_SUBTILE * NSLICE;
-  constexpr int NJ = (TILE + 31) / 32;   // 32-row words of a unit
   constexpr int HQ = HKV * G;
   constexpr int CR = TILE >= CHUNK_ROWS_MIN ? TILE : (CHUNK_ROWS_MIN / TILE) * TILE;   // rows per chunk
-  constexpr int HPT = HQ < MERGE_HEADS ? HQ : MERGE_HEADS;   // heads per merge task
-  constexpr int NMT = HQ / HPT;                              // merge tasks per request
+  constexpr int NJC = CR / 32;                                                          // rows per lane per chunk
+  constexpr int NJU = (TILE + 31) / 32;                                                 // rows per lane per unit
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = g.top_k;
   const int NCHK = (K + CR - 1) / CR;
   const int NPARTS = NCHK * NSLICE;
-  const long long total = (long long)p.n_req * (NCHK + NMT);
+  const long long total = (long long)p.n_req * NCHK;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const AttLayout L = att_layout(g, nstage);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
   uint64_t* empty = full + MAX_STAGES;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + MAX_STAGES);
+  uint64_t* dready = empty + MAX_STAGES;   // the loader's descriptor of a stage is written
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + MAX_STAGES);
+  volatile int* merge_flag = abort_flag + 1;
   Desc* desc = reinterpret_cast<Desc*>(smem_raw + L.desc);
   int* slot_tab = reinterpret_cast<int*>(smem_raw + L.slot_tab);   // [stage][TILE]: hot slot of a fetched row
+  int* mpos = reinterpret_cast<int*>(smem_raw + L.mpos);           // [stage][TILE]: its host position
   unsigned char* stage = smem_raw + L.stage;
   const int row_stride = g.row_bytes + ATT_ROW_PAD;
   const int rvec = g.row_bytes / 16;
@@ -251,10 +223,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
 
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
-      mbar_init(&full[s], 1);      // the loader's arrival (with the hit bytes and its lanes' cp.async)
+      mbar_init(&full[s], 2);      // the loader's arrival (with the hit bytes) and the fetcher's
       mbar_init(&empty[s], NCONS);
+      mbar_init(&dready[s], 1);
     }
     *abort_flag = 0;
+    *merge_flag = 0;
     fence_mbar_init();
   }
   // no griddepcontrol.wait here: everything the select kernel writes for a
@@ -280,20 +254,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       const long long item = (long long)__shfl_sync(FULL_MASK, nxt, 0);
       if (item >= total) break;
       if (lane == 0) nxt = atomicAdd(&p.s.sync[2], 1u);   // the next item, while this one loads
-      const Item itm = decode_item(item, p.n_req, NCHK, NMT);
-      const int r = itm.ri;
-      if (itm.merge) {
-        if (!take_stage()) break;
-        if (lane == 0) {
-          desc[s] = Desc{DESC_MERGE, r, itm.idx, 0, 0, 0, 0, 0};
-          mbar_arrive(&full[s]);
-        }
-        __syncwarp();
-        s = (s + 1 == nstage) ? 0 : s + 1;
-        ++it;
-        continue;
-      }
-      // a chunk: wait for the request's publication
+      const int r = (int)(item / NCHK);
+      const int c = (int)(item % NCHK);
+      // wait for the request's publication
       int kk = 0;
       if (lane == 0) {
         if (wait_counter(p.s.ready + r, 1u)) {
@@ -303,38 +266,34 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         }
       }
       kk = __shfl_sync(FULL_MASK, kk, 0);
-      const int row0 = itm.idx * CR;
+      const int row0 = c * CR;
       const int nrows = max(0, min(CR, kk - row0));
-      if (nrows == 0) {   // past k_eff: nothing to attend, the chunk is done
-        __syncwarp();
-        if (lane == 0) red_release_add(p.s.chunk_done + r, 1u);
-        continue;
+      // slots and positions of the whole chunk, one batch of loads
+      const int32_t* sos = p.s.slot_of_sel + (long long)r * K + row0;
+      const int32_t* selr = p.s.sel + (long long)r * K + row0;
+      int cslot[NJC], cpos[NJC];
+#pragma unroll
+      for (int j = 0; j < NJC; ++j) {
+        const int i = lane + 32 * j;
+        cslot[j] = i < nrows ? __ldcg(sos + i) : 0;
+        cpos[j] = i < nrows ? __ldcg(selr + i) : 0;
       }
       const int req = p.req_ids ? p.req_ids[r] : r;
       const long long rl = (long long)req * g.n_layers + p.layer;
       const unsigned char* hot =
           reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
-      const unsigned char* host =
-          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
-      const int32_t* sos = p.s.slot_of_sel + (long long)r * K;
-      const int32_t* selr = p.s.sel + (long long)r * K;
-      const int nunits = (nrows + TILE - 1) / TILE;
+      // a chunk past k_eff still goes through the consumers (it counts as done)
+      const int nunits = nrows > 0 ? (nrows + TILE - 1) / TILE : 1;
       for (int u = 0; u < nunits; ++u) {
-        const int ur0 = row0 + u * TILE;
-        const int unr = min(TILE, nrows - u * TILE);
-        int slots[NJ], pos[NJ];
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const int i = lane + 32 * j;
-          slots[j] = i < unr ? __ldcg(sos + ur0 + i) : 0;
-          pos[j] = i < unr ? __ldcg(selr + ur0 + i) : 0;
-        }
+        const int ur0 = u * TILE;   // first row of the unit within the chunk
+        const int unr = max(0, min(TILE, nrows - ur0));
         if (!take_stage()) {
           dead = true;
           break;
         }
         unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
         int* tab = slot_tab + s * TILE_MAX;
+        int* mp = mpos + s * TILE_MAX;
         // rows past the end of the chunk: zero them so their masked (weight-0)
         // values stay finite
         if (unr < TILE) {
@@ -343,58 +302,99 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
             *reinterpret_cast<int4*>(st_s + (size_t)i * row_stride + (e % rvec) * 16) = make_int4(0, 0, 0, 0);
           }
         }
+        // the unit's rows: lane l takes rows l, l + 32, ... of the unit; row i of
+        // the unit is row ur0 + i of the chunk, held by lane (ur0 + i) % 32 in
+        // word (ur0 + i) / 32 of the chunk's batch (every lane joins every shuffle)
+        int usl[NJU];
         int hit_rows = 0;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const int i = lane + 32 * j;
-          const bool valid = i < unr;
-          const bool miss = valid && (slots[j] & HS_SLOT_MISS_FLAG) != 0;
-          if (i < TILE) tab[i] = miss ? (slots[j] & ~HS_SLOT_MISS_FLAG) : -1;
-          hit_rows += __popc(__ballot_sync(FULL_MASK, valid && !miss));
-          // missed rows: host copy -> stage row, 16 bytes per lane per step
-          unsigned bits = __ballot_sync(FULL_MASK, miss);
-          while (bits) {
-            const int b0 = __ffs(bits) - 1;
-            bits &= bits - 1;
-            const int pp = __shfl_sync(FULL_MASK, pos[j], b0);
-            const unsigned char* src = host + (size_t)pp * g.row_bytes;
-            unsigned char* dst = st_s + (size_t)(32 * j + b0) * row_stride;
-            for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+        for (int m = 0; m < NJU; ++m) {
+          const int i = lane + 32 * m;
+          const int cr = ur0 + i;
+          int sl = 0, ps = 0;
+#pragma unroll
+          for (int j = 0; j < NJC; ++j) {
+            const int a = __shfl_sync(FULL_MASK, cslot[j], cr & 31);
+            const int b = __shfl_sync(FULL_MASK, cpos[j], cr & 31);
+            if (j == (cr >> 5)) {
+              sl = a;
+              ps = b;
+            }
           }
+          const bool valid = i < unr;
+          const bool miss = valid && (sl & HS_SLOT_MISS_FLAG) != 0;
+          if (i < TILE) {
+            tab[i] = miss ? (sl & ~HS_SLOT_MISS_FLAG) : -1;
+            mp[i] = miss ? ps : -1;
+          }
+          usl[m] = (valid && !miss) ? sl : -1;
+          hit_rows += __popc(__ballot_sync(FULL_MASK, valid && !miss));
         }
-        cp_async_mbar_arrive(&full[s]);   // the phase also waits for this lane's copies
         __syncwarp();
         if (lane == 0) {
-          desc[s] = Desc{DESC_UNIT, r, itm.idx, ur0 - row0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, 0};
+          desc[s] = Desc{DESC_UNIT, r, c, ur0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, 0};
+          mbar_arrive(&dready[s]);   // the fetcher may read the descriptor and tables now
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&full[s], (uint32_t)(hit_rows * g.row_bytes));
         }
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const int i = lane + 32 * j;
-          if (i < unr && (slots[j] & HS_SLOT_MISS_FLAG) == 0) {
-            int slot = slots[j];
-            if (slot < 0 || slot >= g.hot_slots) {   // never expected: keep the copy in bounds
-              set_error(p.s.dev_error, HS_DEVERR_METADATA);
-              slot = 0;
-            }
-            bulk_g2s_hint(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
-                          &full[s], stream_policy);
+        for (int m = 0; m < NJU; ++m) {   // hit rows: one bulk copy each
+          const int i = lane + 32 * m;
+          int slot = usl[m];
+          if (slot < 0) continue;
+          if (slot >= g.hot_slots) {   // never expected: keep the copy in bounds
+            set_error(p.s.dev_error, HS_DEVERR_METADATA);
+            slot = 0;
           }
+          bulk_g2s_hint(st_s + (size_t)i * row_stride, hot + (size_t)slot * g.row_bytes, (uint32_t)g.row_bytes,
+                        &full[s], stream_policy);
         }
         HS_TRACE_IF(p, 2, 2, lane == 0 && it == 0);
         s = (s + 1 == nstage) ? 0 : s + 1;
         ++it;
       }
     }
-    // no more work: tell the consumers
+    // no more work: tell the fetcher and the consumers
     if (!dead && take_stage() && lane == 0) {
       desc[s] = Desc{DESC_STOP, 0, 0, 0, 0, 0, 0, 0};
+      mbar_arrive(&dready[s]);
       mbar_arrive(&full[s]);
     }
     __syncwarp();
     HS_TRACE_IF(p, 2, 3, lane == 0);
+  } else if (warp == FETCHER) {
+    // ============================ fetcher warp ============================
+    // Missed rows of each unit, from the mapped host copy straight into their
+    // stage rows; the stage's full barrier completes when these copies land.
+    for (long long it = 0;; ++it) {
+      const int s = (int)(it % nstage);
+      if (!__all_sync(FULL_MASK, wait_or_abort(&dready[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
+                                               4 * WAIT_LIMIT_NS)))
+        break;
+      const Desc dsc = desc[s];
+      if (dsc.type == DESC_STOP) {
+        if (lane == 0) mbar_arrive(&full[s]);
+        break;
+      }
+      const int r = dsc.ri;
+      const int req = p.req_ids ? p.req_ids[r] : r;
+      const long long rl = (long long)req * g.n_layers + p.layer;
+      const unsigned char* host =
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
+      unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
+      const int* mp = mpos + s * TILE_MAX;
+      for (int i = 0; i < dsc.nr; ++i) {
+        const int ps = mp[i];
+        if (ps < 0) continue;
+        const unsigned char* src = host + (size_t)ps * g.row_bytes;
+        unsigned char* dst = st_s + (size_t)i * row_stride;
+        for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+      }
+      cp_async_mbar_arrive(&full[s]);   // balanced: completes when this lane's copies land
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+    }
     cp_async_wait_all();
   } else {
     // ============================ consumer warps ============================
@@ -415,64 +415,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       if (named_sync_or(BAR_VOTE, NCONS * 32, !ok)) break;   // the consumers leave together
       const Desc dsc = desc[s];
       if (dsc.type == DESC_STOP) break;
-      if (dsc.type == DESC_MERGE) {
-        if (lane == 0) mbar_arrive(&empty[s]);
-        // ---- merge task: heads [idx*HPT, (idx+1)*HPT) of request ri, chunk order ----
-        const int r = dsc.ri;
-        if (ct == 0 && !wait_counter(p.s.chunk_done + r, (unsigned)NCHK)) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
-        named_sync(BAR_CONS, NCONS * 32);
-        const int kk = __ldcg(p.s.kk_pub + r);
-        const int nparts = ((kk + CR - 1) / CR) * NSLICE;
-        const int hl = ct >> 5, d4 = ct & 31;
-        if (hl < HPT) {
-          const int head = dsc.c * HPT + hl;
-          const float2* pml = reinterpret_cast<const float2*>(p.s.part_ml) + (long long)r * NPARTS * HQ;
-          const float4* po = reinterpret_cast<const float4*>(p.s.part_o) + (long long)r * NPARTS * HQ * (D / 4);
-          float M = -INFINITY;
-          for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(pml + (long long)q * HQ + head).x);
-          float Ls = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          constexpr int UQ = 4;
-          for (int q0 = 0; q0 < nparts; q0 += UQ) {
-            float2 ml[UQ];
-            float4 v[UQ];
-#pragma unroll
-            for (int u = 0; u < UQ; ++u) {
-              const int q = q0 + u;
-              ml[u] = q < nparts ? __ldcg(pml + (long long)q * HQ + head) : make_float2(-INFINITY, 0.f);
-              v[u] = q < nparts ? __ldcg(po + ((long long)q * HQ + head) * (D / 4) + d4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < UQ; ++u)
-              if (q0 + u < nparts) {
-                const float w = exp2f(ml[u].x - M);
-                Ls = fmaf(ml[u].y, w, Ls);
-                acc.x = fmaf(v[u].x, w, acc.x);
-                acc.y = fmaf(v[u].y, w, acc.y);
-                acc.z = fmaf(v[u].z, w, acc.z);
-                acc.w = fmaf(v[u].w, w, acc.w);
-              }
-          }
-          uint2 pk = make_uint2(0u, 0u);
-          if (nparts > 0) {
-            const float inv = 1.f / Ls;
-            pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-            pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-          }
-          *reinterpret_cast<uint2*>(p.out + ((long long)r * HQ + head) * D + 4 * d4) = pk;
-        }
-        if (ct == 0) {
-          const unsigned prev = atom_acq_rel_add(p.s.merge_done + r, 1u);
-          if (prev + 1 == (unsigned)NMT) {   // the request's last merge task: clear its flags
-            p.s.ready[r] = 0;
-            p.s.chunk_done[r] = 0;
-            p.s.merge_done[r] = 0;
-          }
-        }
-        continue;
-      }
-      // ---- a unit of a chunk ----
       const int r = dsc.ri;
       if (dsc.first) {
         if (r != q_r) {
@@ -590,7 +532,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (dsc.last) {   // the chunk's partial (m, l, o) for this slice
+      if (!dsc.last) continue;
+      // ---- the chunk's partial (m, l, o) for this slice, then count the chunk ----
+      {
         float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
         ll += __shfl_xor_sync(FULL_MASK, ll, 2);
         float lh = l_hi + __shfl_xor_sync(FULL_MASK, l_hi, 1);
@@ -611,8 +555,60 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
             *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
           if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
         }
-        named_sync(BAR_CONS, NCONS * 32);
-        if (ct == 0) red_release_add(p.s.chunk_done + r, 1u);
+      }
+      named_sync(BAR_CONS, NCONS * 32);
+      if (ct == 0) {
+        const unsigned prev = atom_acq_rel_add(p.s.chunk_done + r, 1u);
+        *merge_flag = prev + 1 == (unsigned)NCHK;   // this CTA completed the request's last chunk
+      }
+      named_sync(BAR_CONS, NCONS * 32);
+      if (!*merge_flag) continue;
+      // ---- merge: every head of request r, partials in chunk order ----
+      {
+        const int kk = __ldcg(p.s.kk_pub + r);
+        const int nparts = ((kk + CR - 1) / CR) * NSLICE;
+        const float2* pml = reinterpret_cast<const float2*>(p.s.part_ml) + (long long)r * NPARTS * HQ;
+        const float4* po = reinterpret_cast<const float4*>(p.s.part_o) + (long long)r * NPARTS * HQ * (D / 4);
+        const int d4 = ct & 31;
+        for (int head = ct >> 5; head < HQ; head += MERGE_HEADS) {
+          float M = -INFINITY;
+          for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(pml + (long long)q * HQ + head).x);
+          float Ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          constexpr int UQ = 4;
+          for (int q0 = 0; q0 < nparts; q0 += UQ) {
+            float2 ml[UQ];
+            float4 v[UQ];
+#pragma unroll
+            for (int u = 0; u < UQ; ++u) {
+              const int q = q0 + u;
+              ml[u] = q < nparts ? __ldcg(pml + (long long)q * HQ + head) : make_float2(-INFINITY, 0.f);
+              v[u] = q < nparts ? __ldcg(po + ((long long)q * HQ + head) * (D / 4) + d4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < UQ; ++u)
+              if (q0 + u < nparts) {
+                const float w = exp2f(ml[u].x - M);
+                Ls = fmaf(ml[u].y, w, Ls);
+                acc.x = fmaf(v[u].x, w, acc.x);
+                acc.y = fmaf(v[u].y, w, acc.y);
+                acc.z = fmaf(v[u].z, w, acc.z);
+                acc.w = fmaf(v[u].w, w, acc.w);
+              }
+          }
+          uint2 pk = make_uint2(0u, 0u);
+          if (nparts > 0) {
+            const float inv = 1.f / Ls;
+            pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+          }
+          *reinterpret_cast<uint2*>(p.out + ((long long)r * HQ + head) * D + 4 * d4) = pk;
+        }
+        if (ct == 0) {   // the request is done: clear its flags for the next call
+          p.s.ready[r] = 0;
+          p.s.chunk_done[r] = 0;
+        }
       }
     }
     HS_TRACE_IF(p, 2, 5, tid == 0);

@@ -75,6 +75,8 @@ constexpr int NWARP = NT / 32;
 constexpr int FAST_MAX_N = 256 * 1024;   // one-pass top-k: contexts up to this many positions
 constexpr int WCAP = 256;                // threshold-digit keys a warp lists in the one-pass top-k
 constexpr int CAND_MAX_N_PER_K = 20;     // candidate listing only for contexts up to 20 k positions
+constexpr int CAND_REG = 8;              // listed candidates a resolver thread holds in registers
+constexpr int CAND_WORDS = 2048;         // candidate path: contexts up to 32 * CAND_WORDS positions
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 // Per-request tables of the launch (scorers) and the resolver's layout share the
@@ -476,30 +478,122 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     const int kk = sh.ok ? min(K, N) : 0;
 
     // ======================= 1. top-k, ascending =======================
+    // The previous call's threshold listed between k and min(2k, 4096) keys: the k
+    // largest (ties included) are all in the list, held in registers here.
+    const bool use_cand = sh.ok && N > K && L.fast && (N + 31) / 32 <= CAND_WORDS && sh.thr != 0u &&
+                          sh.cnt >= K && sh.cnt <= min(2 * K, CAND_REG * NT);
+    bool slots_known = false;   // the candidate path reads each selected position's page entry itself
+    const int k_next = (int)min((long long)N, (long long)K + K / 4);
     if (!sh.ok) {
       // scores incomplete: nothing selected (the output of this request is 0)
     } else if (N <= K) {
       for (int i = tid; i < N; i += NT) sel[i] = i;
-    } else {
-      const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
-      const int cap = 2 * K;
-      // (the candidate path's tie bitmap lives in the per-warp lists)
-      const bool use_cand = L.fast && N <= FAST_MAX_N && (N + 31) / 32 <= WCAP * NWARP && sh.thr != 0u &&
-                            sh.cnt >= K && sh.cnt <= cap;
-      const bool fast = !use_cand && L.fast && N <= FAST_MAX_N;
-      const uint2* cl = p.s.cand + (long long)ri * cap;   // this call's candidates
+    } else if (use_cand) {
+      const int cnt = sh.cnt;
+      const uint2* cl = p.s.cand + (long long)ri * 2 * K;
       const int32_t* page_rl = p.s.page + rl * g.max_context;
+      const int NWd = (N + 31) >> 5;
+      uint32_t* gtw = bitmap;                         // [NWd] positions whose key is above the k-th
+      uint32_t* tiw = bitmap + CAND_WORDS;            // [NWd] positions whose key equals it
+      int* gpre = reinterpret_cast<int*>(lists);      // [NWd] above-threshold positions before each word
+      int* epre = gpre + CAND_WORDS;                  // [NWd] ties before each word
+      uint2 cv[CAND_REG];
+      int cpg[CAND_REG];
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j) {
+        const int i = tid + j * NT;
+        cv[j] = i < cnt ? __ldcg(cl + i) : make_uint2(0u, 0u);
+      }
+      // every selected position is a candidate: its page entry is the hit test
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j) cpg[j] = tid + j * NT < cnt ? page_rl[cv[j].x] : -1;
+      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+      for (int w = tid; w < NWd; w += NT) {
+        gtw[w] = 0u;
+        tiw[w] = 0u;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j)
+        if (tid + j * NT < cnt) atomicAdd(&h[cv[j].y >> 12], 1u);
+      __syncthreads();
+      select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
+      if (cnt >= k_next) {
+        select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
+        if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
+      } else if (tid == 0) {
+        sh.thr_next = sh.thr;   // the list held fewer: keep the threshold that gave >= k
+      }
+      if (tid == 0 && N > CAND_MAX_N_PER_K * K) sh.thr_next = 0u;
+      const int b1 = sh.b1, above1 = sh.above1;
       for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
       __syncthreads();
-      // first-digit histogram: of the listed keys, or of all keys
-      if (use_cand) {
-        for (int i = tid; i < sh.cnt; i += NT) {
-          const uint2 c = __ldcg(&cl[i]);
-          atomicAdd(&h[c.y >> 12], 1u);
-          // every selected position is a candidate: warm its page-table entry for the hit test
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(page_rl + c.x));
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j)
+        if (tid + j * NT < cnt && (int)(cv[j].y >> 12) == b1) atomicAdd(&h[cv[j].y & 4095u], 1u);
+      __syncthreads();
+      HS_TRACE_IF(p, 1, 2, tid == 0 && ri == (int)blockIdx.x);
+      select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
+      const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)sh.b2;
+      const int need_eq = K - (above1 + sh.above2);   // >= 1
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j)
+        if (tid + j * NT < cnt) {
+          const uint32_t pp = cv[j].x;
+          if (cv[j].y > vstar) atomicOr(&gtw[pp >> 5], 1u << (pp & 31));
+          else if (cv[j].y == vstar) atomicOr(&tiw[pp >> 5], 1u << (pp & 31));
         }
-      } else {
+      __syncthreads();
+      // per-word prefix counts of the taken-above and tie positions
+      constexpr int WPT = CAND_WORDS / NT;
+      int ng = 0, ne = 0;
+#pragma unroll
+      for (int k = 0; k < WPT; ++k) {
+        const int w = tid * WPT + k;
+        if (w < NWd) {
+          ng += __popc(gtw[w]);
+          ne += __popc(tiw[w]);
+        }
+      }
+      const int2 ex = block_exclusive_scan2<NT>(ng, ne, sh.scan, nullptr, nullptr);
+      int rg = ex.x, re = ex.y;
+#pragma unroll
+      for (int k = 0; k < WPT; ++k) {
+        const int w = tid * WPT + k;
+        if (w < NWd) {
+          gpre[w] = rg;
+          epre[w] = re;
+          rg += __popc(gtw[w]);
+          re += __popc(tiw[w]);
+        }
+      }
+      __syncthreads();
+      HS_TRACE_IF(p, 1, 3, tid == 0 && ri == (int)blockIdx.x);
+      // each taken candidate's place in the ascending output: the taken positions
+      // before it (all above-threshold ones, ties only up to need_eq)
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j)
+        if (tid + j * NT < cnt) {
+          const uint32_t pp = cv[j].x;
+          const int w = (int)(pp >> 5);
+          const uint32_t lm = (1u << (pp & 31)) - 1u;
+          const int gb = gpre[w] + __popc(gtw[w] & lm);
+          const int eb = epre[w] + __popc(tiw[w] & lm);
+          const bool taken = cv[j].y > vstar || (cv[j].y == vstar && eb < need_eq);
+          if (taken) {
+            const int idx = gb + min(eb, need_eq);
+            sel[idx] = (int)pp;
+            slot_sel[idx] = cpg[j];
+          }
+        }
+      slots_known = true;
+    } else {
+      const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
+      const bool fast = L.fast && N <= FAST_MAX_N;
+      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      // first-digit histogram of all keys
+      {
         const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
         const int n4 = N >> 2;
         constexpr int UA = 8;
@@ -524,22 +618,15 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       __syncthreads();
       // the digit of the k-th largest key, and the digit above which ~1.25 k keys
       // lie: the next call lists keys from there on (exact whenever >= k clear it)
-      const int k_next = (int)min((long long)N, (long long)K + K / 4);
       select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
-      const int listed = use_cand ? sh.cnt : N;
-      if (listed >= k_next) {
-        select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
-        if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
-      } else if (tid == 0) {
-        sh.thr_next = sh.thr;   // the list held fewer: keep the threshold that gave >= k
-      }
+      select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
+      if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
       const int b1 = sh.b1, above1 = sh.above1;
       // listing costs the scorers about as much per position as the full pass
       // costs here, so it pays only while the context is short relative to k
       if (tid == 0 && N > CAND_MAX_N_PER_K * K) sh.thr_next = 0u;
       for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
       __syncthreads();
-      HS_TRACE_IF(p, 1, 2, tid == 0 && ri == (int)blockIdx.x);
       // per-thread contiguous ranges (the rescan path)
       const int per = ((N + NT - 1) / NT + 3) & ~3;
       const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
@@ -551,18 +638,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       int wcnt = 0;       // entries of this warp's list (warp-uniform)
       int lane_gt = 0;    // keys above digit b1 seen by this lane
       bool overflow = false;
-      uint32_t* tiebm = lists;                            // the candidate path's second bitmap
-      const int NWd = (N + 31) >> 5;
-      if (use_cand) {
-        for (int qq = tid; qq < NWd; qq += NT) {
-          bitmap[qq] = 0u;
-          tiebm[qq] = 0u;
-        }
-        for (int i = tid; i < sh.cnt; i += NT) {
-          const uint2 c = __ldcg(&cl[i]);
-          if ((int)(c.y >> 12) == b1) atomicAdd(&h[c.y & 4095u], 1u);
-        }
-      } else if (fast) {
+      if (fast) {
         const uint4* k4 = reinterpret_cast<const uint4*>(keys);
         constexpr int UC = 8;   // chunks in flight per lane
         for (int cb = c0; cb < c1; cb += UC) {
@@ -642,70 +718,11 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       // before the digit select below), then decides whether the lists are usable
       const bool any_overflow = __syncthreads_or(overflow);
       const bool use_lists = fast && !any_overflow;
-      HS_TRACE_IF(p, 1, 3, tid == 0 && ri == (int)blockIdx.x);
       select_digit(h, K - above1, sh.scan, &sh.b2, &sh.above2);
       const int b2 = sh.b2;
       const uint32_t vstar = ((uint32_t)b1 << 12) | (uint32_t)b2;
       const int need_eq = K - (above1 + sh.above2);   // >= 1
-      if (use_cand) {
-        // mark the taken keys (> threshold) and the threshold ties in two bitmaps
-        for (int i = tid; i < sh.cnt; i += NT) {
-          const uint2 c = __ldcg(&cl[i]);
-          if (c.y > vstar) atomicOr(&bitmap[c.x >> 5], 1u << (c.x & 31));
-          else if (c.y == vstar) atomicOr(&tiebm[c.x >> 5], 1u << (c.x & 31));
-        }
-        __syncthreads();
-        const int q0w = (int)((long long)wid * NWd / NWARP), q1w = (int)((long long)(wid + 1) * NWd / NWARP);
-        int n_gt = 0, n_eq = 0;
-        for (int qq = q0w + lane; qq < q1w; qq += 32) {
-          n_gt += __popc(bitmap[qq]);
-          n_eq += __popc(tiebm[qq]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          n_gt += __shfl_xor_sync(FULL_MASK, n_gt, o);
-          n_eq += __shfl_xor_sync(FULL_MASK, n_eq, o);
-        }
-        const int2 wb =
-            block_exclusive_scan2<NT>(lane == 0 ? n_gt : 0, lane == 0 ? n_eq : 0, sh.scan, nullptr, nullptr);
-        const int gt_before = __shfl_sync(FULL_MASK, wb.x, 0), eq_before = __shfl_sync(FULL_MASK, wb.y, 0);
-        int out = gt_before + min(eq_before, need_eq);
-        int tie_run = eq_before;   // threshold ties before this group of words
-        for (int qg = q0w; qg < q1w; qg += 32) {
-          const int qq = qg + lane;
-          uint32_t m = qq < q1w ? bitmap[qq] : 0u;
-          uint32_t tb = qq < q1w ? tiebm[qq] : 0u;
-          const int nt = __popc(tb);
-          int tincl = nt;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(FULL_MASK, tincl, o);
-            if (lane >= o) tincl += n;
-          }
-          int rank = tie_run + tincl - nt;   // ties take the lowest positions first
-          while (tb) {
-            const int bb = __ffs(tb) - 1;
-            tb &= tb - 1;
-            if (rank < need_eq) m |= 1u << bb;
-            ++rank;
-          }
-          tie_run += __shfl_sync(FULL_MASK, tincl, 31);
-          const int cnt = __popc(m);
-          int incl = cnt;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(FULL_MASK, incl, o);
-            if (lane >= o) incl += n;
-          }
-          int o = out + incl - cnt;
-          while (m) {
-            const int bb = __ffs(m) - 1;
-            m &= m - 1;
-            if (o < K) sel[o++] = 32 * qq + bb;
-          }
-          out += __shfl_sync(FULL_MASK, incl, 31);
-        }
-      } else if (use_lists) {
+      if (use_lists) {
         int n_gt = lane_gt, n_eq = 0;
         for (int qq = lane; qq < wcnt; qq += 32) {
           const int lo = (int)(wl[qq] & 4095u);
@@ -806,7 +823,18 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     int m = 0;
     const bool pull = p.fetch_mode == 1;   // else the attention kernel copies the missed rows
     bool bad = false;
-    if (kk > 0) {
+    if (kk > 0 && slots_known) {
+      for (int i = tid; i < kk; i += NT) {
+        const int pos = sel[i], s4 = slot_sel[i];
+        if (s4 >= B) bad = true;
+        if (s4 >= 0 && s4 < B) used[s4] = 1;
+        if (s4 < 0 && !(appended && pos == len)) {   // a miss: its host row starts moving into L2 now
+          const unsigned char* src = reinterpret_cast<const unsigned char*>(p.s.host_kv) +
+                                     ((size_t)rl * g.max_context + pos) * g.row_bytes;
+          for (int b = 0; b < g.row_bytes; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
+        }
+      }
+    } else if (kk > 0) {
       // hit test: independent page-table gathers, four in flight per thread
       for (int i0 = tid; i0 < kk; i0 += 4 * NT) {
         int pos[4], s4[4];
