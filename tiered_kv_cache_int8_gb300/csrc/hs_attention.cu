@@ -1,8 +1,8 @@
 // Sparse attention over the selected rows (GQA, head dim 128), fused with the
-// host fetch of the missed rows RESOLVE left to it and with the merge of its
-// split partials: a persistent, warp-specialised flash-decode kernel that works
-// through a queue of chunks while the select kernel is still resolving later
-// requests.  (The merge kernel further down serves latent rows.)
+// host fetch of the missed rows RESOLVE left to it: a persistent,
+// warp-specialised flash-decode kernel that works through a queue of chunks
+// while the select kernel is still resolving later requests, and the merge
+// kernel (further down) that combines its partials.
 //
 // Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
 // for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
@@ -36,13 +36,14 @@
 //    softmax in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P enters
 //    the second product as bf16.  Consumer warp 0 writes each fetched row into its
 //    hot slot (bulk shared -> global copy), so later steps hit.
-//  * Each (chunk, slice) writes a partial (m, l, o) and counts the chunk done;
-//    the CTA that completes a request's last chunk merges all its partials in
-//    chunk order and writes bf16 — no CTA ever waits for another's chunk.  Rows
-//    are visited in ascending selection order and chunks depend only on k_eff,
-//    so the output is bit-identical for any B and any schedule.
-//  * Counters of the call reset themselves: the merging CTA clears its
-//    request's flags, the last CTA to leave clears the queue.  Each CTA waits
+//  * Each (chunk, slice) writes a partial (m, l, o); the merge kernel, launched
+//    after this one, combines each head's partials in chunk order over many
+//    CTAs at once and writes bf16 (one CTA merging a whole request alone is a
+//    chain of dependent L2 round trips).  Rows are visited in ascending selection
+//    order and chunks depend only on k_eff, so the output is bit-identical for
+//    any B and any schedule.
+//  * Counters of the call reset themselves: the last CTA to leave clears the
+//    queue, the merge kernel clears each request's ready flag.  Each CTA waits
 //    for the select kernel to complete before it exits, so the next launch on the
 //    stream sees both kernels finished.
 #include <cuda_bf16.h>
@@ -61,8 +62,6 @@ constexpr int THREADS = (NCONS + 2) * 32;
 constexpr int MAX_STAGES = 3;
 constexpr int TILE_MAX = 128;   // rows of a unit at h_kv = 1 (8 slices of 16)
 constexpr int CHUNK_ROWS_MIN = 64;
-constexpr int MERGE_HEADS = 8;  // heads merged per pass (one warp each)
-constexpr int BAR_CONS = 1;     // named barrier: the 256 consumer threads
 constexpr int BAR_VOTE = 2;     // named barrier: the consumers' vote on a failed wait
 
 enum { DESC_UNIT = 0, DESC_STOP = 2 };
@@ -212,7 +211,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* dready = empty + MAX_STAGES;   // the loader's descriptor of a stage is written
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + MAX_STAGES);
-  volatile int* merge_flag = abort_flag + 1;
   Desc* desc = reinterpret_cast<Desc*>(smem_raw + L.desc);
   int* slot_tab = reinterpret_cast<int*>(smem_raw + L.slot_tab);   // [stage][TILE]: hot slot of a fetched row
   int* mpos = reinterpret_cast<int*>(smem_raw + L.mpos);           // [stage][TILE]: its host position
@@ -228,7 +226,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       mbar_init(&dready[s], 1);
     }
     *abort_flag = 0;
-    *merge_flag = 0;
     fence_mbar_init();
   }
   // no griddepcontrol.wait here: everything the select kernel writes for a
@@ -268,6 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       kk = __shfl_sync(FULL_MASK, kk, 0);
       const int row0 = c * CR;
       const int nrows = max(0, min(CR, kk - row0));
+      if (c == 0 && lane == 0) p.s.att_nparts[r] = ((kk + CR - 1) / CR) * NSLICE;   // for the merge kernel
       // slots and positions of the whole chunk, one batch of loads
       const int32_t* sos = p.s.slot_of_sel + (long long)r * K + row0;
       const int32_t* selr = p.s.sel + (long long)r * K + row0;
@@ -398,7 +396,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     cp_async_wait_all();
   } else {
     // ============================ consumer warps ============================
-    const int ct = tid;   // 0..255
     const int kvh = warp % HKV;
     const int slice = warp / HKV;
     const int gq = lane >> 2, tq = lane & 3;
@@ -532,9 +529,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (!dsc.last) continue;
-      // ---- the chunk's partial (m, l, o) for this slice, then count the chunk ----
-      {
+      if (dsc.last) {   // the chunk's partial (m, l, o) for this slice
         float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
         ll += __shfl_xor_sync(FULL_MASK, ll, 2);
         float lh = l_hi + __shfl_xor_sync(FULL_MASK, l_hi, 1);
@@ -554,60 +549,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
           for (int t = 0; t < 16; ++t)
             *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
           if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
-        }
-      }
-      named_sync(BAR_CONS, NCONS * 32);
-      if (ct == 0) {
-        const unsigned prev = atom_acq_rel_add(p.s.chunk_done + r, 1u);
-        *merge_flag = prev + 1 == (unsigned)NCHK;   // this CTA completed the request's last chunk
-      }
-      named_sync(BAR_CONS, NCONS * 32);
-      if (!*merge_flag) continue;
-      // ---- merge: every head of request r, partials in chunk order ----
-      {
-        const int kk = __ldcg(p.s.kk_pub + r);
-        const int nparts = ((kk + CR - 1) / CR) * NSLICE;
-        const float2* pml = reinterpret_cast<const float2*>(p.s.part_ml) + (long long)r * NPARTS * HQ;
-        const float4* po = reinterpret_cast<const float4*>(p.s.part_o) + (long long)r * NPARTS * HQ * (D / 4);
-        const int d4 = ct & 31;
-        for (int head = ct >> 5; head < HQ; head += MERGE_HEADS) {
-          float M = -INFINITY;
-          for (int q = 0; q < nparts; ++q) M = fmaxf(M, __ldcg(pml + (long long)q * HQ + head).x);
-          float Ls = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          constexpr int UQ = 4;
-          for (int q0 = 0; q0 < nparts; q0 += UQ) {
-            float2 ml[UQ];
-            float4 v[UQ];
-#pragma unroll
-            for (int u = 0; u < UQ; ++u) {
-              const int q = q0 + u;
-              ml[u] = q < nparts ? __ldcg(pml + (long long)q * HQ + head) : make_float2(-INFINITY, 0.f);
-              v[u] = q < nparts ? __ldcg(po + ((long long)q * HQ + head) * (D / 4) + d4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < UQ; ++u)
-              if (q0 + u < nparts) {
-                const float w = exp2f(ml[u].x - M);
-                Ls = fmaf(ml[u].y, w, Ls);
-                acc.x = fmaf(v[u].x, w, acc.x);
-                acc.y = fmaf(v[u].y, w, acc.y);
-                acc.z = fmaf(v[u].z, w, acc.z);
-                acc.w = fmaf(v[u].w, w, acc.w);
-              }
-          }
-          uint2 pk = make_uint2(0u, 0u);
-          if (nparts > 0) {
-            const float inv = 1.f / Ls;
-            pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-            pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-          }
-          *reinterpret_cast<uint2*>(p.out + ((long long)r * HQ + head) * D + 4 * d4) = pk;
-        }
-        if (ct == 0) {   // the request is done: clear its flags for the next call
-          p.s.ready[r] = 0;
-          p.s.chunk_done[r] = 0;
         }
       }
     }
@@ -658,7 +599,12 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(DecodeParams p) {
   griddep_wait();   // the attention kernel's partials
   griddep_launch_dependents();
   const int nparts = p.s.att_nparts[(long long)ri * (HQ / GH) + h0 / GH];
-  if (nparts <= 0) return;   // no units: the attention kernel wrote zeros
+  if (!p.g.shared_kv && blockIdx.x == 0 && tid == 0) p.s.ready[ri] = 0;   // this call is done with the request
+  if (nparts <= 0) {   // nothing selected: the output is defined as 0
+    if (!p.g.shared_kv)
+      for (int e = tid; e < HPC * DV; e += blockDim.x) p.out[((long long)ri * HQ + h0) * DV + e] = 0;
+    return;
+  }
   if (nparts > MERGE_MAX_PARTS) {   // not reachable with the shapes hs_create accepts
     if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
     return;
@@ -763,7 +709,9 @@ static cudaError_t run_gqa(const DecodeParams* p, size_t smem, cudaStream_t st) 
   if (p == nullptr)   // prepare: allow the shared memory this shape needs
     return allow_smem(kern, smem);
   const int ns = attention_stages(p->g, 227 * 1024);
-  return launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);
+  cudaError_t e = launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);
+  if (e != cudaSuccess) return e;
+  return launch_merge(*p, st);
 }
 
 template <int HKV>

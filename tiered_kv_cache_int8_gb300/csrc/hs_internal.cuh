@@ -83,8 +83,6 @@ struct DeviceState {
   unsigned int* tiles_done;    // [R] score tiles of request i finished (select kernel)
   unsigned int* ready;         // [R] 1: request i's selection and slots are published
   int32_t* kk_pub;             // [R] k_eff of request i (valid once ready)
-  unsigned int* chunk_done;    // [R] attention chunks of request i finished
-  unsigned int* merge_done;    // [R] merge tasks of request i finished
   unsigned int* sync;          // [4]: 0 = CTAs of the select kernel past their set-up,
                                //      1 = resolvers finished, 2 = next attention work item,
                                //      3 = attention CTAs finished

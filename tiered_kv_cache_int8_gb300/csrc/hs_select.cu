@@ -46,8 +46,8 @@
 //       position bitmap (the few keys with the threshold digit go to per-warp
 //       lists in position order) over the scratch keys.  Either way the
 //       selection is emitted ascending from bitmaps.
-//     - RESOLVE: hit test through the page table (independent gathers, every
-//       missed host row prefetched into L2 line by line the moment it misses),
+//     - RESOLVE: hit test through the page table (on the candidate path the page
+//       entries come with the candidates; else independent gathers),
 //       miss compaction with block scans, victims from an explicit LRU list kept
 //       sorted by (stamp, slot) — a call moves exactly the slots it used to the
 //       most recent end, so two stable compactions maintain it: no sort, no heap.
@@ -56,7 +56,9 @@
 //       then the request's ready flag (release).  The attention kernel, launched
 //       as a programmatic dependent, starts on the requests that are ready while
 //       later ones are still being scored or resolved.
-//     - after publication: stamps, the new LRU list, counters, step + 1 and the
+//     - after publication: the L2 prefetch of every missed host row (the
+//       attention kernel's copies then read them from L2), stamps, the new LRU
+//       list, counters, step + 1 and the
 //       appended token (its key to the HBM store, its row to the pinned host
 //       copy, length + 1).  Lengths and thresholds are written only once every
 //       CTA of the launch has read them (a grid-wide counter).
@@ -825,14 +827,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     bool bad = false;
     if (kk > 0 && slots_known) {
       for (int i = tid; i < kk; i += NT) {
-        const int pos = sel[i], s4 = slot_sel[i];
+        const int s4 = slot_sel[i];
         if (s4 >= B) bad = true;
         if (s4 >= 0 && s4 < B) used[s4] = 1;
-        if (s4 < 0 && !(appended && pos == len)) {   // a miss: its host row starts moving into L2 now
-          const unsigned char* src = reinterpret_cast<const unsigned char*>(p.s.host_kv) +
-                                     ((size_t)rl * g.max_context + pos) * g.row_bytes;
-          for (int b = 0; b < g.row_bytes; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
-        }
       }
     } else if (kk > 0) {
       // hit test: independent page-table gathers, four in flight per thread
@@ -852,14 +849,6 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
             if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
             slot_sel[i] = s4[u];
             if (s4[u] >= 0 && s4[u] < B) used[s4[u]] = 1;
-            // a miss: start moving its host row over the link into L2 now, line by
-            // line (the copy then reads it from L2); the row appended by this call
-            // comes from its input copy
-            if (s4[u] < 0 && pos[u] >= 0 && pos[u] < N && !(appended && pos[u] == len)) {
-              const unsigned char* src = reinterpret_cast<const unsigned char*>(p.s.host_kv) +
-                                         ((size_t)rl * g.max_context + pos[u]) * g.row_bytes;
-              for (int b = 0; b < g.row_bytes; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
-            }
           }
         }
       }
@@ -1021,6 +1010,21 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       p.s.kk_pub[ri] = kk;
       __threadfence();
       if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, 1u);
+    }
+
+    // the missed rows the attention kernel will copy start moving over the link
+    // into L2 now, line by line, spread over the whole CTA (its later chunks then
+    // read them from L2)
+    if (!pull && m > 0) {
+      const int lines = g.row_bytes / 128;
+      const unsigned char* src_base =
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
+      for (int e = tid; e < m * lines; e += NT) {
+        const int qq = e / lines;
+        if (!(miss_i[qq] & HS_SLOT_MISS_FLAG)) continue;   // the appended token: already in its slot
+        const int pos = sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG];
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src_base + (size_t)pos * g.row_bytes + (e - qq * lines) * 128));
+      }
     }
 
     // ======================= 5. metadata after publication =======================
