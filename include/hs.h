@@ -119,6 +119,15 @@ typedef struct hs_config {
                                 for LRU.
                             The attention result does not depend on it. */
   uint32_t replacement_seed;  /* seed of HS_REPLACE_RANDOM (ignored otherwise) */
+  int32_t write_allocate;     /* 0 (write-around, the default): an appended token enters the hot
+                                 cache only when a later step selects it.  1: the token a
+                                 hs_decode_layer call appends (new_kv_rows) counts as used by that
+                                 call: when its selection does not take it, it is filled from its
+                                 input row into one more victim slot (the last, after the
+                                 selection's misses) and stamped like the rest; hits and misses
+                                 still count the selected positions only.  Requires
+                                 top_k < hot_slots.  Tokens appended by hs_append are never
+                                 allocated.  The attention result does not depend on it. */
 } hs_config_t;
 
 #define HS_REPLACE_LRU 0

@@ -28,7 +28,9 @@ candidates = every position < N including the token just appended;
 k_eff = min(k, N); ties broken by lower position; selection reported in
 ascending position order; LRU victims = unpinned slots with the smallest
 (last-use stamp, slot); misses filled in ascending position order; appends do
-not enter the hot cache; q head h reads kv head floor(h * H_kv / H_q);
+not enter the hot cache (write-around), or, under the write-allocate variant,
+the token a decode call appends counts as used by that call; q head h reads kv
+head floor(h * H_kv / H_q);
 softmax scale 1/sqrt(d_qk) unless given.
 
 Floating point is fp64 throughout; integer work is exact int64.
@@ -132,13 +134,24 @@ class LRUHotCache:
         self.page: dict[int, int] = {}
         self.step_no = 0
 
-    def step(self, sel) -> dict:
+    def step(self, sel, allocate: int | None = None) -> dict:
+        """One decode call.  ``allocate``: under write-allocate, the position this
+        call appended (the highest so far); the cache then treats it as used at
+        this step even when the selection does not take it — the update runs over
+        sel + [allocate], so an unselected new token is filled into the last
+        victim and stamped like the rest.  Hits and misses count the selected
+        positions only; such a fill is counted in "allocs" (its row comes with
+        the append, not over the host link)."""
         sel = [int(p) for p in sel]
-        assert len(sel) <= self.B, "every selected row must fit in the hot cache"
         assert all(a < b for a, b in zip(sel, sel[1:])), "selection must be ascending and unique"
+        used = sel
+        if allocate is not None and int(allocate) not in sel:
+            assert not sel or int(allocate) > sel[-1], "the appended position is the highest"
+            used = sel + [int(allocate)]
+        assert len(used) <= self.B, "every selected row (and an allocated one) must fit in the hot cache"
         t = self.step_no
-        hit_slots = {self.page[p] for p in sel if p in self.page}
-        misses = [p for p in sel if p not in self.page]
+        hit_slots = {self.page[p] for p in used if p in self.page}
+        misses = [p for p in used if p not in self.page]
         victims = self._victims(t, hit_slots, len(misses))
         fills = []
         for p, v in zip(misses, victims):
@@ -150,14 +163,16 @@ class LRUHotCache:
             fills.append((p, v))
         slot_of_sel = [self.page[p] for p in sel]
         filled = {v for _, v in fills}
-        for s in slot_of_sel:
+        for s in [self.page[p] for p in used]:
             if self.refresh_hits or s in filled:
                 self.slot_stamp[s] = t
         self.step_no = t + 1
+        allocs = len(used) - len(sel)
         return {
             "slot_of_sel": np.asarray(slot_of_sel, dtype=np.int64),
-            "hits": len(sel) - len(misses),
-            "misses": len(misses),
+            "hits": len(sel) - (len(misses) - allocs),
+            "misses": len(misses) - allocs,
+            "allocs": allocs,
             "fills": fills,
         }
 

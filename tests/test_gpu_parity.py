@@ -33,8 +33,9 @@ def oracle_cache(w, r, l, n_slots, replacement="lru", seed=0):
     return {"lru": LRUHotCache, "fifo": FIFOHotCache}[replacement](n_slots)
 
 
-def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru", seed=0):
-    """Per step: (sel, step result, snapshot) from the oracle."""
+def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru", seed=0, write_allocate=False):
+    """Per step: (sel, step result, snapshot) from the oracle (with write_allocate,
+    the position each step appends counts as used by that step)."""
     keys = wl.idx_keys_upto(w, r, l, steps)
     walk = wl.query_walk(w, r, l, steps)
     scores = indexer_scores_many(keys, walk)
@@ -44,7 +45,7 @@ def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru", seed=0):
     for t in range(steps):
         n = n0 + t + 1
         sel = topk_select(scores[:n, t], w.top_k)
-        st = cache.step(sel)
+        st = cache.step(sel, allocate=n - 1 if write_allocate else None)
         out.append((sel, st, cache.snapshot(n)))
     return out
 
@@ -60,8 +61,10 @@ def check_order(order, stamp):
     assert order.tolist() == keys
 
 
-def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement="lru", seed=0):
-    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode, replacement=replacement, replacement_seed=seed)
+def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement="lru", seed=0,
+                write_allocate=False):
+    cache = make_cache(w, steps, hot_slots, fetch_mode=fetch_mode, replacement=replacement, replacement_seed=seed,
+                       write_allocate=write_allocate)
     prefill(cache, w)
     inp = StepInputs(w, steps)
     got = run_steps(cache, w, inp, steps, collect_meta=True, fused=fused)
@@ -70,7 +73,8 @@ def full_parity(w, steps, hot_slots=None, fetch_mode=2, fused=False, replacement
     for l in range(w.n_layers):
         for r in range(w.n_requests):
             prev_h = prev_m = 0
-            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B, replacement, seed)):
+            for t, (sel, st, snap) in enumerate(oracle_steps(w, r, l, steps, B, replacement, seed,
+                                                             write_allocate)):
                 k_eff = sel.size
                 g_sel = got["sel"][l, t][r]
                 assert np.array_equal(g_sel[:k_eff], sel), f"selection r{r} l{l} t{t}"
@@ -489,3 +493,35 @@ def test_largest_hot_cache_keeps_the_reverse_map_in_global_memory(replacement):
     w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=40000, top_k=2048,
                          hot_slots=16384, steps=4, sigma=0.3)
     full_parity(w, 4, replacement=replacement, seed=3)
+
+
+@pytest.mark.parametrize("fetch_mode,replacement", [(0, "lru"), (1, "lru"), (2, "fifo"), (2, "random")])
+def test_write_allocate_matches_the_oracle(fetch_mode, replacement):
+    # the token each call appends counts as used by the call (the oracle's
+    # write-allocate variant); page table, reverse map, stamps, order and
+    # counters bit-exact after every step, attention within tolerance
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=3000, top_k=256, hot_slots=320,
+                         steps=8, sigma=0.3)
+    full_parity(w, 8, fetch_mode=fetch_mode, fused=True, replacement=replacement, write_allocate=True)
+
+
+def test_write_allocate_changes_placement_not_the_result():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=2500, top_k=128, hot_slots=200,
+                         steps=6, sigma=0.2)
+    outs = []
+    for wa in (False, True):
+        cache = make_cache(w, 6, write_allocate=wa)
+        prefill(cache, w)
+        outs.append(run_steps(cache, w, StepInputs(w, 6), 6, fused=True))
+        cache.close()
+    for t in range(6):
+        assert np.array_equal(outs[0]["sel"][0, t], outs[1]["sel"][0, t])
+        assert np.array_equal(outs[0]["out"][0, t], outs[1]["out"][0, t])
+
+
+def test_write_allocate_needs_a_free_slot():
+    from tiered_kv_cache_int8_gb300 import hs
+    w = wl.make_workload("batch16_32k", n_requests=1, n_layers=1, context=300, top_k=128, hot_slots=128, steps=1)
+    with pytest.raises(hs.HsError) as e:
+        make_cache(w, 1, write_allocate=True)
+    assert e.value.status == hs.HS_ERR_CONFIG

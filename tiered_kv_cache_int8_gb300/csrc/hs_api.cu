@@ -43,6 +43,9 @@ std::string check_config(const hs_config_t& c) {
   if (c.fetch_mode < 0 || c.fetch_mode > 2) return "fetch_mode must be 0, 1 or 2";
   if (c.replacement != HS_REPLACE_LRU && c.replacement != HS_REPLACE_FIFO && c.replacement != HS_REPLACE_RANDOM)
     return "replacement must be HS_REPLACE_LRU (0), HS_REPLACE_FIFO (1) or HS_REPLACE_RANDOM (2)";
+  if (c.write_allocate != 0 && c.write_allocate != 1) return "write_allocate must be 0 or 1";
+  if (c.write_allocate && c.top_k >= c.hot_slots)
+    return "write_allocate needs top_k < hot_slots (the appended token needs a slot of its own)";
   if (c.shared_kv == 0) {
     if (c.d_qk != 128 || c.d_v != 128) return "GQA rows: d_qk = d_v = 128 required";
     if (!is_pow2_in(c.h_kv, 1, 8)) return "GQA rows: h_kv must be one of 1, 2, 4, 8";
@@ -456,6 +459,7 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.n_resolvers = std::min(std::min(n_req, hs::SEL_MAX_RESOLVERS), h->num_sms - 1);
   p.publish = h->cfg.shared_kv ? 0 : 1;   // the chunked GQA kernel starts on published requests
   p.fault = h->fault;
+  p.write_allocate = h->cfg.write_allocate;
 #ifdef HS_WITH_TRACE
   p.trace = h->trace;
 #endif

@@ -120,6 +120,7 @@ struct DecodeParams {
   int n_resolvers;         // of them, resolver CTAs (the rest score)
   int publish;             // 1: resolvers publish each request (the chunked attention kernel waits on it)
   int fault;               // test hook: 1 = the resolver never publishes request 0 (a wait runs out)
+  int write_allocate;      // 1: the token this call appends counts as used (filled if not selected)
 #ifdef HS_WITH_TRACE
   unsigned long long* trace;   // [2][3][1024][64]: clock64 and %globaltimer per (kernel, CTA, point)
 #endif

@@ -64,6 +64,10 @@
 //       CTA of the launch has read them (a grid-wide counter).
 //  * fetch_mode 1 (and latent rows, which every head group reads) pulls the
 //    missed rows into their slots inside the resolver before publication.
+//  * Write-allocate (a variant; the pages leave open whether a new token enters
+//    the hot cache): the token a call appends counts as used by the call — when
+//    the selection does not take it, it is one more miss after the selection,
+//    filled from its input row into the last victim and stamped like the rest.
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -110,13 +114,13 @@ __host__ __device__ inline SelLayout sel_layout(const Geometry& g) {
   L.hist = off;
   off += IDX_BINS * 4;
   L.sel = off;
-  off += align_up((size_t)K * 4, 16);
+  off += align_up((size_t)(K + 1) * 4, 16);
   L.slot = off;
-  off += align_up((size_t)K * 4, 16);
+  off += align_up((size_t)(K + 1) * 4, 16);
   L.miss_i = off;
-  off += align_up((size_t)K * 4, 16);
+  off += align_up((size_t)(K + 1) * 4, 16);
   L.victim = off;
-  off += align_up((size_t)K * 4, 16);
+  off += align_up((size_t)(K + 1) * 4, 16);
   L.ord = off;
   off += (size_t)B * 4;
   L.used = off;
@@ -853,6 +857,15 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         }
       }
     }
+    // write-allocate: the token this call appends counts as used even when the
+    // selection does not take it (one extra entry after the selection: a new
+    // position, so never resident)
+    const int extra = (p.write_allocate && appended && sh.ok && !(kk > 0 && sel[kk - 1] == len)) ? 1 : 0;
+    const int kx = kk + extra;
+    if (extra && tid == 0) {
+      sel[kk] = len;
+      slot_sel[kk] = -1;
+    }
     if (__syncthreads_or(bad)) {
       // inconsistent metadata: publish nothing usable for this request
       if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
@@ -866,8 +879,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     }
     HS_TRACE_IF(p, 1, 5, tid == 0 && ri == (int)blockIdx.x);
     // misses in ascending selection order, and the unpinned entries of the LRU list
-    const int per_i = (kk + NT - 1) / NT;
-    const int i0 = min(kk, tid * per_i), i1 = min(kk, i0 + per_i);
+    const int per_i = (kx + NT - 1) / NT;
+    const int i0 = min(kx, tid * per_i), i1 = min(kx, i0 + per_i);
     const int per_j = (B + NT - 1) / NT;
     const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
     int nm = 0, nc = 0;
@@ -1031,8 +1044,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // LRU and random: every used slot is refreshed; FIFO: only the filled ones (used == 2)
     const bool fifo = p.replacement == HS_REPLACE_FIFO;
     auto refreshed = [&](uint8_t u) { return fifo ? u == 2 : u != 0; };
-    if (kk > 0) {
-      for (int i = tid; i < kk; i += NT) {
+    if (kx > 0) {
+      for (int i = tid; i < kx; i += NT) {
         const int sl = slot_sel[i];
         if (refreshed(used[sl])) stamp[sl] = t;
       }
@@ -1053,9 +1066,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         if (refreshed(used[sl])) order[sb++] = sl;
       if (tid == 0) {
         p.s.step[rl] = t + 1;
-        red_add_u64(&p.s.hits[rl], (unsigned long long)(kk - m));
-        red_add_u64(&p.s.misses[rl], (unsigned long long)m);
-        red_add_u64(&p.s.glob[0], (unsigned long long)m * g.row_bytes);
+        // counters of the selected positions (an allocated new token is neither)
+        red_add_u64(&p.s.hits[rl], (unsigned long long)(kk - (m - extra)));
+        red_add_u64(&p.s.misses[rl], (unsigned long long)(m - extra));
+        red_add_u64(&p.s.glob[0], (unsigned long long)(m - extra) * g.row_bytes);
       }
     }
     // the appended token: key to the HBM store, row to the pinned host copy

@@ -49,7 +49,7 @@ class HsConfig(ctypes.Structure):
                 ("d_idx", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hot_slots", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("device", ctypes.c_int32),
                 ("fetch_mode", ctypes.c_int32), ("replacement", ctypes.c_int32),
-                ("replacement_seed", ctypes.c_uint32)]
+                ("replacement_seed", ctypes.c_uint32), ("write_allocate", ctypes.c_int32)]
 
 
 class HsStats(ctypes.Structure):
@@ -161,12 +161,12 @@ class HiSparseCache:
     def __init__(self, *, n_layers: int, max_requests: int, max_context: int, h_q: int, h_kv: int,
                  d_qk: int, d_v: int, d_idx: int, top_k: int, hot_slots: int, shared_kv: bool = False,
                  softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 2,
-                 replacement: str = "lru", replacement_seed: int = 0):
+                 replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False):
         if replacement not in REPLACEMENT:
             raise ValueError(f"replacement must be one of {sorted(REPLACEMENT)}")
         self.cfg = HsConfig(n_layers, max_requests, max_context, h_q, h_kv, d_qk, d_v, int(shared_kv),
                             d_idx, top_k, hot_slots, softmax_scale, device, fetch_mode,
-                            REPLACEMENT[replacement], replacement_seed)
+                            REPLACEMENT[replacement], replacement_seed, int(write_allocate))
         self._h = ctypes.c_void_p()
         rc = lib().hs_create(ctypes.byref(self.cfg), ctypes.byref(self._h))
         if rc != HS_OK:
