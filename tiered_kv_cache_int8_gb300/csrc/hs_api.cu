@@ -315,7 +315,6 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.app_counter, R * 4, false},
       {(void**)&s.tiles_done, R * 4, false},
       {(void**)&s.ready, R * 4, false},
-      {(void**)&s.kk_pub, R * 4, false},
       {(void**)&s.sync, 16, false},
 #ifdef HS_WITH_TRACE
       {(void**)&h->trace, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8, false},
@@ -351,7 +350,6 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.tiles_done, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.ready, 0, R * 4) == cudaSuccess;
-  ok = ok && cudaMemset(s.kk_pub, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.sync, 0, 16) == cudaSuccess;
 #ifdef HS_WITH_TRACE
   ok = ok && cudaMemset(h->trace, 0, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8) ==

@@ -20,7 +20,9 @@
 //    request after request, taken with a global atomic counter.  A chunk waits
 //    (bounded) for its request's ready flag; requests are published in about
 //    queue order, so a CTA rarely waits.
-//  * Warp 8 (loader) reads the slots of a whole chunk at once, then per unit
+//  * Warp 8 (loader) reads the slots of a whole chunk at once (those of the next
+//    chunk already while it streams this one, when that request is published),
+//    then per unit
 //    (16 rows per warp slice) copies every hit row (all kv heads: one
 //    contiguous hot slot) HBM -> shared memory with one 1-D bulk async copy into
 //    a row-padded layout (16 extra bytes per row put the 8 rows of an ldmatrix
@@ -239,44 +241,65 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     const uint64_t stream_policy = l2_evict_first_policy();   // hit rows are read once per call
     int s = 0;
     long long it = 0;
-    unsigned nxt = 0;
-    if (lane == 0) nxt = atomicAdd(&p.s.sync[2], 1u);
     bool dead = false;
     auto take_stage = [&]() -> bool {   // wait until stage s may be refilled
       if (it < nstage) return true;
       return __all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
                                                  p.s.dev_error, 4 * WAIT_LIMIT_NS));
     };
-    while (!dead) {
-      const long long item = (long long)__shfl_sync(FULL_MASK, nxt, 0);
-      if (item >= total) break;
-      if (lane == 0) nxt = atomicAdd(&p.s.sync[2], 1u);   // the next item, while this one loads
-      const int r = (int)(item / NCHK);
-      const int c = (int)(item % NCHK);
-      // wait for the request's publication
-      int kk = 0;
-      if (lane == 0) {
-        if (wait_counter(p.s.ready + r, 1u)) {
-          kk = __ldcg(p.s.kk_pub + r);
-        } else {
-          set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
-        }
-      }
-      kk = __shfl_sync(FULL_MASK, kk, 0);
+    // a chunk's metadata: k_eff (the request's ready flag holds k_eff + 1), the
+    // request id, the slots and positions of its rows (one batch of loads)
+    struct Meta {
+      int kk, req;
+      int slot[NJC], pos[NJC];
+    };
+    auto load_rows = [&](Meta& m, int r, int c) {
       const int row0 = c * CR;
-      const int nrows = max(0, min(CR, kk - row0));
-      if (c == 0 && lane == 0) p.s.att_nparts[r] = ((kk + CR - 1) / CR) * NSLICE;   // for the merge kernel
-      // slots and positions of the whole chunk, one batch of loads
+      const int nrows = max(0, min(CR, m.kk - row0));
       const int32_t* sos = p.s.slot_of_sel + (long long)r * K + row0;
       const int32_t* selr = p.s.sel + (long long)r * K + row0;
-      int cslot[NJC], cpos[NJC];
 #pragma unroll
       for (int j = 0; j < NJC; ++j) {
         const int i = lane + 32 * j;
-        cslot[j] = i < nrows ? __ldcg(sos + i) : 0;
-        cpos[j] = i < nrows ? __ldcg(selr + i) : 0;
+        m.slot[j] = i < nrows ? __ldcg(sos + i) : 0;
+        m.pos[j] = i < nrows ? __ldcg(selr + i) : 0;
       }
-      const int req = p.req_ids ? p.req_ids[r] : r;
+      m.req = p.req_ids ? p.req_ids[r] : r;
+    };
+    unsigned nxt = 0;   // lane 0: the queue index after the current one
+    if (lane == 0) nxt = atomicAdd(&p.s.sync[2], 1u);
+    long long cur = (long long)__shfl_sync(FULL_MASK, nxt, 0);
+    if (lane == 0 && cur < total) nxt = atomicAdd(&p.s.sync[2], 1u);
+    Meta pf;                // metadata of the next chunk, when it was ready early
+    long long pf_item = -1;
+    while (!dead && cur < total) {
+      const long long item = cur;
+      const int r = (int)(item / NCHK);
+      const int c = (int)(item % NCHK);
+      Meta mt;
+      if (pf_item == item) {
+        mt = pf;
+      } else {   // wait for the request's publication
+        unsigned v = 0;
+        if (lane == 0) {
+          v = wait_counter(p.s.ready + r, 1u) ? ld_acquire(p.s.ready + r) : 0u;
+          if (v == 0u) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+        }
+        v = __shfl_sync(FULL_MASK, v, 0);
+        mt.kk = v ? (int)v - 1 : 0;
+        load_rows(mt, r, c);
+      }
+      const int kk = mt.kk;
+      const int req = mt.req;
+      const int row0 = c * CR;
+      const int nrows = max(0, min(CR, kk - row0));
+      if (c == 0 && lane == 0) p.s.att_nparts[r] = ((kk + CR - 1) / CR) * NSLICE;   // for the merge kernel
+      int cslot[NJC], cpos[NJC];
+#pragma unroll
+      for (int j = 0; j < NJC; ++j) {
+        cslot[j] = mt.slot[j];
+        cpos[j] = mt.pos[j];
+      }
       const long long rl = (long long)req * g.n_layers + p.layer;
       const unsigned char* hot =
           reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
@@ -351,7 +374,24 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         HS_TRACE_IF(p, 2, 2, lane == 0 && it == 0);
         s = (s + 1 == nstage) ? 0 : s + 1;
         ++it;
+        if (u == 0) {   // the next chunk's metadata now, if its request is already published
+          const long long nx = (long long)__shfl_sync(FULL_MASK, nxt, 0);
+          pf_item = -1;
+          if (nx < total) {
+            const int rn = (int)(nx / NCHK);
+            unsigned v = 0;
+            if (lane == 0) v = ld_acquire(p.s.ready + rn);
+            v = __shfl_sync(FULL_MASK, v, 0);
+            if (v != 0u) {
+              pf.kk = (int)v - 1;
+              load_rows(pf, rn, (int)(nx % NCHK));
+              pf_item = nx;
+            }
+          }
+        }
       }
+      cur = (long long)__shfl_sync(FULL_MASK, nxt, 0);
+      if (lane == 0 && cur < total) nxt = atomicAdd(&p.s.sync[2], 1u);
     }
     // no more work: tell the fetcher and the consumers
     if (!dead && take_stage() && lane == 0) {

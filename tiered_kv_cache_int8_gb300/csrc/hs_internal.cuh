@@ -81,8 +81,7 @@ struct DeviceState {
   // cross-CTA progress of one decode call (all zero between calls: every counter
   // is reset by the last party that reads it)
   unsigned int* tiles_done;    // [R] score tiles of request i finished (select kernel)
-  unsigned int* ready;         // [R] 1: request i's selection and slots are published
-  int32_t* kk_pub;             // [R] k_eff of request i (valid once ready)
+  unsigned int* ready;         // [R] k_eff + 1 once request i's selection and slots are published
   unsigned int* sync;          // [4]: 0 = CTAs of the select kernel past their set-up,
                                //      1 = resolvers finished, 2 = next attention work item,
                                //      3 = attention CTAs finished

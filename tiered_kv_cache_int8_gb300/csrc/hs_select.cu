@@ -52,8 +52,8 @@
 //       sorted by (stamp, slot) — a call moves exactly the slots it used to the
 //       most recent end, so two stable compactions maintain it: no sort, no heap.
 //     - publication: selection, slot of every selected row (misses flagged for
-//       the attention kernel, which copies them host -> stage -> slot) and k_eff,
-//       then the request's ready flag (release).  The attention kernel, launched
+//       the attention kernel, which copies them host -> stage -> slot), then the
+//       request's ready flag = k_eff + 1 (release).  The attention kernel, launched
 //       as a programmatic dependent, starts on the requests that are ready while
 //       later ones are still being scored or resolved.
 //     - after publication: the L2 prefetch of every missed host row (the
@@ -425,9 +425,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       if (p.publish) {
         __syncthreads();
         if (tid == 0) {
-          p.s.kk_pub[ri] = 0;
           __threadfence();
-          st_release(p.s.ready + ri, 1u);
+          st_release(p.s.ready + ri, 1u);   // k_eff + 1 = 1: nothing selected
         }
       }
       __syncthreads();
@@ -870,9 +869,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       // inconsistent metadata: publish nothing usable for this request
       if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
       if (p.publish && tid == 0) {
-        p.s.kk_pub[ri] = 0;
         __threadfence();
-        st_release(p.s.ready + ri, 1u);
+        st_release(p.s.ready + ri, 1u);   // k_eff + 1 = 1: nothing selected
       }
       __syncthreads();
       continue;
@@ -1020,9 +1018,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     __syncthreads();
     HS_TRACE_IF(p, 1, 7, tid == 0 && ri == (int)blockIdx.x);
     if (p.publish && tid == 0) {
-      p.s.kk_pub[ri] = kk;
       __threadfence();
-      if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, 1u);
+      if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, (unsigned)kk + 1u);   // k_eff + 1
     }
 
     // the missed rows the attention kernel will copy start moving over the link
