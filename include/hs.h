@@ -128,6 +128,14 @@ typedef struct hs_config {
                                  still count the selected positions only.  Requires
                                  top_k < hot_slots.  Tokens appended by hs_append are never
                                  allocated.  The attention result does not depend on it. */
+  int32_t idx_heads;          /* the indexer: 0 or 1 = one int8 query per request, score
+                                 s[p] = q . K_idx[p] (signed, exact int32); 2, 4 or 8 = the
+                                 multi-head ReLU-weighted variant (needs d_idx 64 or 128):
+                                 s[p] = sum_h w_h * max(0, q_h . K_idx[p]), exact in uint32, with
+                                 per-request query heads q_h and weights w_h in [0, 127]
+                                 (negative weights count as 0).  Selection, ties and the cache
+                                 rule are the same; the top-k then takes three digit passes over
+                                 the keys and no candidate list. */
 } hs_config_t;
 
 #define HS_REPLACE_LRU 0
@@ -206,7 +214,9 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
  * earlier and later stream work is the usual one.  At most 16 requests are
  * resolved at a time (one resolver CTA each); the rest of the GPU scores.
  *   req_ids     : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
- *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned)
+ *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned); with
+ *                 idx_heads = H > 1: [n_req][H * d_idx + 16], per request the H query
+ *                 heads, then the H weights (int8), then padding
  *   q           : dev bf16 [n_req][h_q][d_qk]   attention query
  *   out         : dev bf16 [n_req][h_q][d_v]    attention output (written)
  *   sel_out     : dev int32 [n_req][top_k] or NULL: selected positions, ascending;

@@ -7,6 +7,7 @@ from .hisparse_oracle import (  # noqa: F401
     bf16_to_f64,
     indexer_scores,
     indexer_scores_many,
+    indexer_scores_multihead,
     topk_select,
     LRUHotCache,
     FIFOHotCache,

@@ -84,6 +84,23 @@ def indexer_scores_many(idx_keys: np.ndarray, q_idx: np.ndarray) -> np.ndarray:
     return s.astype(np.int64)
 
 
+def indexer_scores_multihead(idx_keys: np.ndarray, q_heads: np.ndarray, weights: np.ndarray) -> np.ndarray:
+    """The multi-head ReLU-weighted indexer variant: s[p] = sum_h w_h *
+    max(0, q_h . K_idx[p]), exact int64.
+
+    "10月14日学习笔记", "HiSparse / 动机" names the indexer only and the pages
+    cite DeepSeek's sparse attention (DSA) without its formula; this reading
+    takes DSA's indexer shape: several query heads against one shared key per
+    position, each head's dot product through a ReLU, combined with per-head
+    non-negative weights.  q_heads: int8 [H, d_idx]; weights: int8 [H] in [0, 127]."""
+    k = np.asarray(idx_keys, dtype=np.int8).astype(np.int64)
+    q = np.asarray(q_heads, dtype=np.int8).astype(np.int64)
+    wts = np.asarray(weights, dtype=np.int8).astype(np.int64)
+    assert (wts >= 0).all(), "head weights are non-negative"
+    dots = k @ q.T                                   # [N, H]
+    return np.maximum(dots, 0) @ wts
+
+
 # ---------------------------------------------------------------------------
 # a2: top-k selection ("10月14日学习笔记", HiSparse / 动机: the indexer keeps
 # the top-k tokens).  Ties go to the lower position; output ascending.

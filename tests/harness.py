@@ -23,7 +23,17 @@ def make_cache(w: wl.Workload, steps: int, hot_slots: int | None = None, device:
                          h_q=w.h_q, h_kv=w.h_kv, d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k,
                          hot_slots=hot_slots or w.hot_slots, shared_kv=w.shared_kv, device=device,
                          fetch_mode=fetch_mode, replacement=replacement, replacement_seed=replacement_seed,
-                         write_allocate=write_allocate)
+                         write_allocate=write_allocate, idx_heads=w.idx_heads)
+
+
+def packed_q_idx(w: wl.Workload, heads: np.ndarray, weights: np.ndarray) -> np.ndarray:
+    """The multi-head indexer's query rows as the library takes them: per request
+    the heads [H, d_idx], then the H weights, then zero padding to 16 bytes."""
+    R, H, d = heads.shape
+    out = np.zeros((R, H * d + 16), np.int8)
+    out[:, :H * d] = heads.reshape(R, H * d)
+    out[:, H * d:H * d + H] = weights
+    return out
 
 
 def prefill(cache, w: wl.Workload, requests=None, layers=None):
@@ -54,13 +64,21 @@ class StepInputs:
         layers = range(w.n_layers) if layers is None else layers
         R = w.n_requests
         self.walk = {l: np.stack([wl.query_walk(w, r, l, steps) for r in range(R)]) for l in layers}
+        if w.idx_heads > 1:   # every head's walk [R, T, H, d] and the per-step weights [R, T, H]
+            self.heads = {l: np.stack([wl.query_walk_heads(w, r, l, steps) for r in range(R)]) for l in layers}
+            self.weights = {l: np.stack([np.stack([wl.step_idx_weights(w, r, l, t) for t in range(steps)])
+                                         for r in range(R)]) for l in layers}
         self.q_idx = {}
         self.q = {}
         self.kv = {}
         self.keys = {}
         for l in layers:
             for t in range(steps):
-                self.q_idx[l, t] = torch.from_numpy(np.ascontiguousarray(self.walk[l][:, t])).to(dev)
+                if w.idx_heads > 1:
+                    qi = packed_q_idx(w, self.heads[l][:, t], self.weights[l][:, t])
+                else:
+                    qi = np.ascontiguousarray(self.walk[l][:, t])
+                self.q_idx[l, t] = torch.from_numpy(qi).to(dev)
                 q = np.stack([wl.step_query(w, r, l, t) for r in range(R)])
                 self.q[l, t] = torch.from_numpy(q.view(np.int16)).to(dev)
                 kv = np.stack([wl.step_kv_row(w, r, l, t) for r in range(R)])[:, None, :]

@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 
 import workload as wl
-from oracle import FIFOHotCache, LRUHotCache, RandomHotCache, indexer_scores_many, sparse_attention, topk_select
+from oracle import (FIFOHotCache, LRUHotCache, RandomHotCache, indexer_scores_many, indexer_scores_multihead,
+                    sparse_attention, topk_select)
 from tests.harness import MAX_ABS, REL_L2, StepInputs, attention_error, make_cache, prefill, run_steps
 
 pytestmark = pytest.mark.gpu
@@ -37,8 +38,12 @@ def oracle_steps(w, r, l, steps, n_slots=None, replacement="lru", seed=0, write_
     """Per step: (sel, step result, snapshot) from the oracle (with write_allocate,
     the position each step appends counts as used by that step)."""
     keys = wl.idx_keys_upto(w, r, l, steps)
-    walk = wl.query_walk(w, r, l, steps)
-    scores = indexer_scores_many(keys, walk)
+    if w.idx_heads > 1:   # the multi-head ReLU-weighted indexer
+        heads = wl.query_walk_heads(w, r, l, steps)
+        scores = np.stack([indexer_scores_multihead(keys, heads[t], wl.step_idx_weights(w, r, l, t))
+                           for t in range(steps)], axis=1)
+    else:
+        scores = indexer_scores_many(keys, wl.query_walk(w, r, l, steps))
     cache = oracle_cache(w, r, l, n_slots or w.hot_slots, replacement, seed)
     n0 = int(w.contexts()[r])
     out = []
@@ -525,3 +530,30 @@ def test_write_allocate_needs_a_free_slot():
     with pytest.raises(hs.HsError) as e:
         make_cache(w, 1, write_allocate=True)
     assert e.value.status == hs.HS_ERR_CONFIG
+
+
+@pytest.mark.parametrize("d_idx,heads", [(128, 4), (64, 8), (128, 2)])
+def test_multihead_indexer_matches_the_oracle(d_idx, heads):
+    # s[p] = sum_h w_h * max(0, q_h . K[p]) with 32-bit keys: selection, cache
+    # state and attention against the oracle's multi-head scores
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=1, context=3001, top_k=256, hot_slots=512,
+                         steps=5, d_idx=d_idx, idx_heads=heads, sigma=0.2)
+    full_parity(w, 5, fused=True)
+
+
+def test_multihead_indexer_ties_and_short_contexts():
+    # all-zero weights: every score ties at 0, so the lowest positions win
+    import torch
+    from tiered_kv_cache_int8_gb300 import hs
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=700, top_k=256, hot_slots=512,
+                         steps=1, d_idx=64, idx_heads=4)
+    cache = make_cache(w, 1)
+    prefill(cache, w)
+    inp = StepInputs(w, 1)
+    qi = inp.q_idx[0, 0].clone()
+    qi[:, 4 * 64:4 * 64 + 4] = 0
+    sel = torch.full((2, 256), -7, dtype=torch.int32, device="cuda")
+    cache.decode_layer(0, qi, inp.q[0, 0], sel_out=sel, new_kv=inp.kv[0, 0], new_keys=inp.keys[0, 0])
+    assert np.array_equal(sel.cpu().numpy(), np.tile(np.arange(256, dtype=np.int32), (2, 1)))
+    assert cache.stats()["device_error"] == 0
+    cache.close()

@@ -44,6 +44,10 @@ std::string check_config(const hs_config_t& c) {
   if (c.replacement != HS_REPLACE_LRU && c.replacement != HS_REPLACE_FIFO && c.replacement != HS_REPLACE_RANDOM)
     return "replacement must be HS_REPLACE_LRU (0), HS_REPLACE_FIFO (1) or HS_REPLACE_RANDOM (2)";
   if (c.write_allocate != 0 && c.write_allocate != 1) return "write_allocate must be 0 or 1";
+  if (c.idx_heads < 0 || c.idx_heads > 8 || (c.idx_heads > 1 && (c.idx_heads & (c.idx_heads - 1))))
+    return "idx_heads must be 0, 1, 2, 4 or 8";
+  if (c.idx_heads > 1 && c.d_idx != 64 && c.d_idx != 128)
+    return "the multi-head indexer (idx_heads > 1) needs d_idx 64 or 128";
   if (c.write_allocate && c.top_k >= c.hot_slots)
     return "write_allocate needs top_k < hot_slots (the appended token needs a slot of its own)";
   if (c.shared_kv == 0) {
@@ -202,6 +206,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   g.row_elems = hs_row_elems(cfg);
   g.row_bytes = 2 * g.row_elems;
   g.v_off = cfg->shared_kv ? 0 : cfg->h_kv * cfg->d_qk;
+  g.idx_heads = cfg->idx_heads > 1 ? cfg->idx_heads : 1;
   const float scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / std::sqrt((float)cfg->d_qk);
   h->scale_log2 = scale * 1.4426950408889634f;
 

@@ -47,6 +47,7 @@ struct Geometry {
   int n_layers, max_requests, max_context;
   int h_q, h_kv, d_qk, d_v, shared_kv, d_idx, top_k, hot_slots;
   int row_elems, row_bytes, v_off;
+  int idx_heads;           // 1: one indexer query (signed score); 2/4/8: the multi-head ReLU-weighted indexer
 };
 
 struct DeviceState {

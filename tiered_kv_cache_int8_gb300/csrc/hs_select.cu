@@ -204,12 +204,12 @@ __device__ __forceinline__ int4 ld_stream(const void* p) { return __ldcs(reinter
 // ---------------------------------------------------------------------------
 // scoring geometry for d_idx = 16 * NCH bytes
 // ---------------------------------------------------------------------------
-template <int NCH>
+template <int NCH, int NH>
 struct ScoreGeom {
   static constexpr int LPP = NCH < 8 ? NCH : 8;       // lanes per position
   static constexpr int CPL = NCH / LPP;               // 16-byte chunks per lane per position (1 or 2)
   static constexpr int PPI = 32 / LPP;                // positions covered by one load instruction
-  static constexpr int LD = 8;                        // loads per lane per sub-tile
+  static constexpr int LD = NH > 1 ? 4 : 8;           // loads per lane per sub-tile (fewer with several heads)
   static constexpr int NP = LD / CPL;                 // position groups per lane per sub-tile
   static constexpr int SUB = NP * PPI;                // positions per sub-tile
   static constexpr int TILE = 2 * SUB;                // positions per warp tile (two sub-tiles)
@@ -223,9 +223,9 @@ size_t select_smem_bytes(const Geometry& g) { return sel_layout(g).total; }
 // ===========================================================================
 // the kernel
 // ===========================================================================
-template <int NCH>
+template <int NCH, int NH>
 __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
-  using SG = ScoreGeom<NCH>;
+  using SG = ScoreGeom<NCH, NH>;
   constexpr int d = NCH * 16;
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         nt = scored ? (N + SG::TILE - 1) / SG::TILE : 0;
         t_req[i] = scored ? req : -1;
         t_n[i] = N;
-        t_thr[i] = scored ? thr : 0u;
+        t_thr[i] = (scored && NH == 1) ? thr : 0u;   // candidate listing: single-head keys only
       }
       int tot;
       const int ex = block_exclusive_scan<NT>(nt, sh.scan, &tot);
@@ -286,8 +286,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // lane roles inside a load instruction
     const int pg = lane / SG::LPP;            // position within the instruction
     const int cl = lane % SG::LPP;            // chunk column of the lane
-    int4 q[SG::CPL];
+    int4 q[NH][SG::CPL];
+    int qw[NH];   // head weights (multi-head indexer)
     int q_r = -1;
+    const int qstride = NH > 1 ? NH * d + 16 : d;   // bytes of one request's indexer query
 
     // request of warp tile t, searching forward from request `from`
     auto req_of = [&](int t, int from) {
@@ -327,9 +329,14 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const uint32_t thr = t_thr[ri];
       if (ri != q_r) {
         q_r = ri;
-        const int4* qs = reinterpret_cast<const int4*>(p.q_idx + (long long)ri * d);
+        const int8_t* qrow = p.q_idx + (long long)ri * qstride;
 #pragma unroll
-        for (int c = 0; c < SG::CPL; ++c) q[c] = qs[cl * SG::CPL + c];
+        for (int h = 0; h < NH; ++h) {
+          const int4* qs = reinterpret_cast<const int4*>(qrow + h * d);
+#pragma unroll
+          for (int c = 0; c < SG::CPL; ++c) q[h][c] = qs[cl * SG::CPL + c];
+          qw[h] = NH > 1 ? max(0, (int)qrow[NH * d + h]) : 1;   // negative weights count as 0
+        }
       }
       uint32_t* keys_out = p.s.scores + (long long)ri * p.score_stride;
       const int tn = t + W;
@@ -337,24 +344,40 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         int4 (&v)[SG::LD] = half == 0 ? va : vb;
-        int acc[SG::NP];
+        int acc[SG::NP][NH];   // each head's partial dot product over this lane's chunks
 #pragma unroll
-        for (int j = 0; j < SG::NP; ++j) acc[j] = 0;
+        for (int j = 0; j < SG::NP; ++j)
+#pragma unroll
+          for (int h = 0; h < NH; ++h) acc[j][h] = 0;
 #pragma unroll
         for (int u = 0; u < SG::LD; ++u) {
           const int j = u / SG::CPL;
-          const int4 qq = q[u % SG::CPL];
-          acc[j] = __dp4a(v[u].x, qq.x, acc[j]);
-          acc[j] = __dp4a(v[u].y, qq.y, acc[j]);
-          acc[j] = __dp4a(v[u].z, qq.z, acc[j]);
-          acc[j] = __dp4a(v[u].w, qq.w, acc[j]);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const int4 qq = q[h][u % SG::CPL];
+            acc[j][h] = __dp4a(v[u].x, qq.x, acc[j][h]);
+            acc[j][h] = __dp4a(v[u].y, qq.y, acc[j][h]);
+            acc[j][h] = __dp4a(v[u].z, qq.z, acc[j][h]);
+            acc[j][h] = __dp4a(v[u].w, qq.w, acc[j][h]);
+          }
         }
         // the buffer is free: start the same half of this warp's next tile
         if (tn < total) load_sub(tn, rn, half, v);
+        // key of each position group: single head, score + 2^22 (24 bits); several
+        // heads, sum_h w_h * max(0, dot_h) (non-negative, below 2^32)
+        uint32_t key[SG::NP];
 #pragma unroll
         for (int j = 0; j < SG::NP; ++j) {
+          unsigned tot = 0;
 #pragma unroll
-          for (int o = 1; o < SG::LPP; o <<= 1) acc[j] += __shfl_xor_sync(FULL_MASK, acc[j], o);
+          for (int h = 0; h < NH; ++h) {
+            int dh = acc[j][h];
+#pragma unroll
+            for (int o = 1; o < SG::LPP; o <<= 1) dh += __shfl_xor_sync(FULL_MASK, dh, o);
+            if (NH == 1) tot = (unsigned)(dh + IDX_KEY_BIAS);
+            else tot += (unsigned)qw[h] * (unsigned)max(dh, 0);
+          }
+          key[j] = tot;
         }
         // lane cl of a position group owns position groups j with j % LPP == cl
         const int sub0 = tile0 + half * SG::SUB;
@@ -370,7 +393,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           if (j % SG::LPP == cl) {
             const int o = j / SG::LPP;
             ownp[o] = sub0 + j * SG::PPI + pg;
-            ownk[o] = (uint32_t)(acc[j] + IDX_KEY_BIAS);
+            ownk[o] = key[j];
           }
         }
 #pragma unroll
@@ -592,15 +615,26 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           }
         }
       slots_known = true;
-    } else {
+    } else if (NH > 1) {
+      // the multi-head indexer's 32-bit keys: three digits (12, 12 and 8 bits),
+      // each found by a histogram pass over the keys of the digits above it, then
+      // a counting pass and the ascending emission (ties to the lower position)
       const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
-      const bool fast = L.fast && N <= FAST_MAX_N;
-      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
-      __syncthreads();
-      // first-digit histogram of all keys
-      {
-        const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
-        const int n4 = N >> 2;
+      const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
+      const int n4 = N >> 2;
+      int above = 0;
+      uint32_t prefix = 0;   // the digits found so far
+      constexpr int SHIFT[3] = {20, 8, 0};
+      constexpr uint32_t MASK[3] = {4095u, 4095u, 255u};
+#pragma unroll 1
+      for (int dgt = 0; dgt < 3; ++dgt) {
+        for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        const int sh_d = SHIFT[dgt];
+        const int sh_p = dgt == 0 ? 32 : SHIFT[dgt - 1];   // keys whose higher digits match `prefix`
+        auto count = [&](uint32_t k) {
+          if (sh_p == 32 || (k >> sh_p) == prefix) atomicAdd(&h[(k >> sh_d) & MASK[dgt]], 1u);
+        };
         constexpr int UA = 8;
         for (int i0 = tid; i0 < n4; i0 += UA * NT) {
           uint4 v[UA];
@@ -612,20 +646,103 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
 #pragma unroll
           for (int u = 0; u < UA; ++u)
             if (i0 + u * NT < n4) {
-              atomicAdd(&h[v[u].x >> 12], 1u);
-              atomicAdd(&h[v[u].y >> 12], 1u);
-              atomicAdd(&h[v[u].z >> 12], 1u);
-              atomicAdd(&h[v[u].w >> 12], 1u);
+              count(v[u].x);
+              count(v[u].y);
+              count(v[u].z);
+              count(v[u].w);
             }
         }
-        for (int i = 4 * n4 + tid; i < N; i += NT) atomicAdd(&h[__ldcg(keys + i) >> 12], 1u);
+        for (int i = 4 * n4 + tid; i < N; i += NT) count(__ldcg(keys + i));
+        __syncthreads();
+        select_digit(h, K - above, sh.scan, &sh.b1, &sh.above1);
+        above += sh.above1;
+        prefix = (prefix << (dgt == 0 ? 0 : (SHIFT[dgt - 1] - SHIFT[dgt]))) | (uint32_t)sh.b1;
+        __syncthreads();
+      }
+      const uint32_t vstar = prefix;   // the k-th largest key
+      const int need_eq = K - above;   // >= 1
+      if (tid == 0) sh.thr_next = 0u;  // no candidate listing for these keys
+      const int per = ((N + NT - 1) / NT + 3) & ~3;
+      const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
+      int n_gt = 0, n_eq = 0;
+      for (int j = j0; j < j1; j += 4) {   // multiples of 4 in bounds (padded rows)
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(keys + j));
+        const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < j1) {
+            n_gt += kv[e] > vstar;
+            n_eq += kv[e] == vstar;
+          }
+      }
+      const int2 before = block_exclusive_scan2<NT>(n_gt, n_eq, sh.scan, nullptr, nullptr);
+      int o = before.x + min(before.y, need_eq);
+      int eq_rank = before.y;
+      for (int j = j0; j < j1; j += 4) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(keys + j));
+        const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < j1) {
+            bool take = kv[e] > vstar;
+            if (kv[e] == vstar) {
+              take = eq_rank < need_eq;
+              ++eq_rank;
+            }
+            if (take && o < K) sel[o++] = j + e;
+          }
+      }
+    } else {
+      const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
+      const bool fast = L.fast && N <= FAST_MAX_N;
+      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      // first-digit histogram: when the candidate list only overflowed, every one of
+      // the k largest keys clears the threshold, so only those keys are counted;
+      // else all keys.  Lanes adding to the same bin are combined first (the bins
+      // near the middle of the score distribution are hot).
+      {
+        const uint32_t floor_key = (sh.thr != 0u && sh.cnt >= K) ? sh.thr : 0u;
+        const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
+        const int n4 = N >> 2;
+        auto hadd = [&](uint32_t k, bool valid) {   // called by every lane of the warp
+          const unsigned bin = (valid && k >= floor_key) ? (k >> 12) : 0xFFFFFFFFu;
+          const unsigned peers = __match_any_sync(FULL_MASK, bin);
+          if (bin != 0xFFFFFFFFu && __ffs(peers) - 1 == lane) atomicAdd(&h[bin], (unsigned)__popc(peers));
+        };
+        constexpr int UA = 8;
+        for (int b0 = tid & ~31; b0 < n4; b0 += UA * NT) {   // warp-uniform trip count
+          uint4 v[UA];
+#pragma unroll
+          for (int u = 0; u < UA; ++u) {
+            const int i = b0 + lane + u * NT;
+            v[u] = i < n4 ? __ldcg(k4 + i) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < UA; ++u) {
+            const bool ok = b0 + lane + u * NT < n4;
+            hadd(v[u].x, ok);
+            hadd(v[u].y, ok);
+            hadd(v[u].z, ok);
+            hadd(v[u].w, ok);
+          }
+        }
+        for (int i = 4 * n4 + tid; i < N; i += NT) {
+          const uint32_t k = __ldcg(keys + i);
+          if (k >= floor_key) atomicAdd(&h[k >> 12], 1u);
+        }
       }
       __syncthreads();
       // the digit of the k-th largest key, and the digit above which ~1.25 k keys
       // lie: the next call lists keys from there on (exact whenever >= k clear it)
       select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
-      select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
-      if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
+      const int counted = (sh.thr != 0u && sh.cnt >= K) ? sh.cnt : N;   // keys the histogram holds
+      if (counted >= k_next) {
+        select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
+        if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
+      } else if (tid == 0) {
+        sh.thr_next = sh.thr;
+      }
       const int b1 = sh.b1, above1 = sh.above1;
       // listing costs the scorers about as much per position as the full pass
       // costs here, so it pays only while the context is short relative to k
@@ -1106,28 +1223,42 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
   }
 }
 
-template <int NCH>
+template <int NCH, int NH>
 static cudaError_t run_select(const DecodeParams* p, size_t smem, cudaStream_t st) {
-  auto kern = select_kernel<NCH>;
+  auto kern = select_kernel<NCH, NH>;
   if (p == nullptr) return allow_smem(kern, smem);
   return launch_pdl(kern, dim3(p->sel_grid), dim3(NT), smem, st, *p);
 }
 
-static cudaError_t dispatch_select(int d_idx, const DecodeParams* p, size_t smem, cudaStream_t st) {
-  switch (d_idx) {
-    case 16: return run_select<1>(p, smem, st);
-    case 32: return run_select<2>(p, smem, st);
-    case 64: return run_select<4>(p, smem, st);
-    case 128: return run_select<8>(p, smem, st);
-    case 256: return run_select<16>(p, smem, st);
+// single-head indexer: d_idx 16..256; the multi-head indexer: d_idx 64 or 128,
+// 2, 4 or 8 heads
+static cudaError_t dispatch_select(const Geometry& g, const DecodeParams* p, size_t smem, cudaStream_t st) {
+  if (g.idx_heads <= 1) {
+    switch (g.d_idx) {
+      case 16: return run_select<1, 1>(p, smem, st);
+      case 32: return run_select<2, 1>(p, smem, st);
+      case 64: return run_select<4, 1>(p, smem, st);
+      case 128: return run_select<8, 1>(p, smem, st);
+      case 256: return run_select<16, 1>(p, smem, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  const int key = g.d_idx * 16 + g.idx_heads;
+  switch (key) {
+    case 64 * 16 + 2: return run_select<4, 2>(p, smem, st);
+    case 64 * 16 + 4: return run_select<4, 4>(p, smem, st);
+    case 64 * 16 + 8: return run_select<4, 8>(p, smem, st);
+    case 128 * 16 + 2: return run_select<8, 2>(p, smem, st);
+    case 128 * 16 + 4: return run_select<8, 4>(p, smem, st);
+    case 128 * 16 + 8: return run_select<8, 8>(p, smem, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t prepare_select(const Geometry& g, size_t smem) { return dispatch_select(g.d_idx, nullptr, smem, 0); }
+cudaError_t prepare_select(const Geometry& g, size_t smem) { return dispatch_select(g, nullptr, smem, 0); }
 
 cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st) {
-  return dispatch_select(p.g.d_idx, &p, smem, st);
+  return dispatch_select(p.g, &p, smem, st);
 }
 
 }  // namespace hs

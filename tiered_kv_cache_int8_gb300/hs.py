@@ -49,7 +49,8 @@ class HsConfig(ctypes.Structure):
                 ("d_idx", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hot_slots", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("device", ctypes.c_int32),
                 ("fetch_mode", ctypes.c_int32), ("replacement", ctypes.c_int32),
-                ("replacement_seed", ctypes.c_uint32), ("write_allocate", ctypes.c_int32)]
+                ("replacement_seed", ctypes.c_uint32), ("write_allocate", ctypes.c_int32),
+                ("idx_heads", ctypes.c_int32)]
 
 
 class HsStats(ctypes.Structure):
@@ -161,12 +162,15 @@ class HiSparseCache:
     def __init__(self, *, n_layers: int, max_requests: int, max_context: int, h_q: int, h_kv: int,
                  d_qk: int, d_v: int, d_idx: int, top_k: int, hot_slots: int, shared_kv: bool = False,
                  softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 2,
-                 replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False):
+                 replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False,
+                 idx_heads: int = 1):
         if replacement not in REPLACEMENT:
             raise ValueError(f"replacement must be one of {sorted(REPLACEMENT)}")
         self.cfg = HsConfig(n_layers, max_requests, max_context, h_q, h_kv, d_qk, d_v, int(shared_kv),
                             d_idx, top_k, hot_slots, softmax_scale, device, fetch_mode,
-                            REPLACEMENT[replacement], replacement_seed, int(write_allocate))
+                            REPLACEMENT[replacement], replacement_seed, int(write_allocate), int(idx_heads))
+        # bytes of one request's indexer query (heads, then weights and padding)
+        self.q_idx_row = d_idx if idx_heads <= 1 else idx_heads * d_idx + 16
         self._h = ctypes.c_void_p()
         rc = lib().hs_create(ctypes.byref(self.cfg), ctypes.byref(self._h))
         if rc != HS_OK:
@@ -215,6 +219,7 @@ class HiSparseCache:
         import torch
         n_req = int(q_idx.shape[0])
         assert q_idx.is_cuda and q.is_cuda and q_idx.is_contiguous() and q.is_contiguous()
+        assert q_idx.element_size() == 1 and q_idx.numel() == n_req * self.q_idx_row
         assert tuple(q.shape) == (n_req, self.cfg.h_q, self.cfg.d_qk) and q.element_size() == 2
         if out is None:
             out = torch.empty((n_req, self.cfg.h_q, self.cfg.d_v), dtype=torch.bfloat16, device=q.device)

@@ -38,6 +38,7 @@ _S_QUERY = 3
 _S_STEP_KV = 4
 _S_STEP_IDX = 5
 _S_LENGTHS = 6
+_S_IDX_W = 7             # per-step indexer head weights (multi-head indexer)
 
 KV_CHUNK = 4096          # positions per prefill K/V stream
 IDX_CHUNK = 65536        # positions per prefill index-key stream
@@ -63,6 +64,7 @@ class Workload:
     context_range: tuple | None = None   # (lo, hi): per-request log-uniform lengths
     noise: str = "per_dim"       # "per_dim": eps ~ N(0, I/d_idx); "literal": eps ~ N(0, I)
     seed: int | None = None
+    idx_heads: int = 1           # > 1: the multi-head ReLU-weighted indexer (one walk per head)
 
     # ---- derived layout -------------------------------------------------
     @property
@@ -177,16 +179,25 @@ def prefill_idx_keys(w: Workload, req: int, layer: int) -> np.ndarray:
 
 # ---- per-step inputs ----------------------------------------------------------
 
-def query_walk(w: Workload, req: int, layer: int, steps: int | None = None) -> np.ndarray:
-    """Indexer queries for decode steps 0..T-1 of one (request, layer): int8 [T, d_idx].
-
-    u_0 = normalise(N(0, I)); u_t = normalise(u_{t-1} + sigma * eps_t);
-    q_t = round_half_even(127 * u_t / max|u_t|).  eps_t ~ N(0, I / d_idx) under
-    the per-dimension reading (drift of about sigma radians per step), N(0, I)
-    under the literal one."""
+def query_walk_heads(w: Workload, req: int, layer: int, steps: int | None = None) -> np.ndarray:
+    """Indexer queries of every head for steps 0..T-1: int8 [T, idx_heads, d_idx].
+    Head 0 is query_walk's walk; head h > 0 is an independent walk of its own
+    stream, with the same sigma."""
     T = w.steps if steps is None else steps
+    heads = [query_walk(w, req, layer, T)]
+    for h in range(1, w.idx_heads):
+        heads.append(_walk(w, _rng(w.base_seed, (req, layer, _S_WALK, h)), T))
+    return np.stack(heads, axis=1)
+
+
+def step_idx_weights(w: Workload, req: int, layer: int, t: int) -> np.ndarray:
+    """Per-head indexer weights of one (request, layer, step): int8 [idx_heads]
+    uniform in [0, 127] (the multi-head indexer's query-dependent weights)."""
+    return _rng(w.base_seed, (req, layer, _S_IDX_W, t)).integers(0, 128, size=w.idx_heads, dtype=np.int8)
+
+
+def _walk(w: Workload, g: np.random.Generator, T: int) -> np.ndarray:
     d = w.d_idx
-    g = _rng(w.base_seed, (req, layer, _S_WALK, 0))
     u = g.standard_normal(d)
     u /= np.linalg.norm(u)
     eps_scale = 1.0 / math.sqrt(d) if w.noise == "per_dim" else 1.0
@@ -198,6 +209,17 @@ def query_walk(w: Workload, req: int, layer: int, steps: int | None = None) -> n
         q = np.rint(127.0 * u / np.abs(u).max())
         out[t] = np.clip(q, -127, 127).astype(np.int8)
     return out
+
+
+def query_walk(w: Workload, req: int, layer: int, steps: int | None = None) -> np.ndarray:
+    """Indexer queries for decode steps 0..T-1 of one (request, layer): int8 [T, d_idx].
+
+    u_0 = normalise(N(0, I)); u_t = normalise(u_{t-1} + sigma * eps_t);
+    q_t = round_half_even(127 * u_t / max|u_t|).  eps_t ~ N(0, I / d_idx) under
+    the per-dimension reading (drift of about sigma radians per step), N(0, I)
+    under the literal one."""
+    T = w.steps if steps is None else steps
+    return _walk(w, _rng(w.base_seed, (req, layer, _S_WALK, 0)), T)
 
 
 def step_query(w: Workload, req: int, layer: int, t: int) -> np.ndarray:
