@@ -61,3 +61,14 @@ def test_sizes_of_the_full_workloads():
     assert abs(w2.host_bytes() / 1e9 - 8.6) < 0.1 and abs(w2.hot_bytes() / 1e9 - 1.07) < 0.01
     w5 = wl.WORKLOADS["stress_128k"]
     assert abs(w5.host_bytes() / 2 ** 30 - 64) < 0.1
+
+
+def test_multihead_queries_and_weights():
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=1, context=100, steps=6, idx_heads=4)
+    h = wl.query_walk_heads(w, 1, 0, 6)
+    assert h.shape == (6, 4, w.d_idx) and h.dtype == np.int8
+    assert np.array_equal(h[:, 0], wl.query_walk(w, 1, 0, 6))        # head 0 is the single-head walk
+    assert not np.array_equal(h[:, 1], h[:, 2])                        # independent heads
+    assert np.array_equal(h, wl.query_walk_heads(w, 1, 0, 6))          # deterministic
+    wt = wl.step_idx_weights(w, 1, 0, 3)
+    assert wt.shape == (4,) and wt.dtype == np.int8 and (wt >= 0).all()

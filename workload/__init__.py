@@ -14,6 +14,8 @@ from .synth import (  # noqa: F401
     prefill_kv,
     prefill_idx_keys,
     query_walk,
+    query_walk_heads,
+    step_idx_weights,
     step_query,
     step_kv_row,
     step_idx_key,
