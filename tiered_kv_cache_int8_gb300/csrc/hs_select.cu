@@ -84,18 +84,15 @@ constexpr int CAND_MAX_N_PER_K = 20;     // candidate listing only for contexts 
 constexpr int CAND_REG = 8;              // listed candidates a resolver thread holds in registers
 constexpr int CAND_WORDS = 2048;         // candidate path: contexts up to 32 * CAND_WORDS positions
 constexpr size_t SMEM_LIMIT = 227 * 1024;
-constexpr int SEL_RING = 3;              // sub-tile buffers per scorer warp (two in flight while one is scored)
-constexpr int SUB_BYTES = 8 * 32 * 16;   // one sub-tile: 8 16-byte chunks per lane
 
 // Per-request tables of the launch (scorers) and the resolver's layout share the
 // dynamic shared memory: a CTA is one or the other.
 struct SelLayout {
-  // scorer tables and load ring
-  size_t t_prefix, t_req, t_n, t_thr, s_ring, t_total;
+  // scorer tables
+  size_t t_prefix, t_req, t_n, t_thr, t_total;
   // resolver
   size_t hist, sel, slot, miss_i, victim, ord, rev, used, bitmap, lists, newrow, r_total;
   bool rev_smem, fast;
-  int score_warps;
   size_t total;
 };
 
@@ -111,14 +108,6 @@ __host__ __device__ inline SelLayout sel_layout(const Geometry& g) {
   off += align_up((size_t)g.max_requests * 4, 16);
   L.t_thr = off;      // u32 [n]: candidate threshold
   off += align_up((size_t)g.max_requests * 4, 16);
-  off = align_up(off, 128);
-  L.s_ring = off;     // per scoring warp: SEL_RING sub-tile buffers of 4 KB
-  // as many scoring warps as the ring space allows (all 16 unless the request
-  // tables are very large)
-  const size_t per_warp = (size_t)SEL_RING * SUB_BYTES;
-  const size_t room = SMEM_LIMIT > off ? (SMEM_LIMIT - off) / per_warp : 0;
-  L.score_warps = (int)(room < (size_t)NWARP ? room : (size_t)NWARP);
-  off += (size_t)L.score_warps * per_warp;
   L.t_total = off;
 
   off = 0;
@@ -209,19 +198,8 @@ __device__ __forceinline__ uint32_t random_ikey(unsigned long long seed, unsigne
 
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-// 16-byte asynchronous copy global -> shared, L2 only, with an L2 eviction
-// policy; src_bytes = 0 writes zeros (positions past the end).
-__device__ __forceinline__ void cp_async_16_zfill(void* smem_dst, const void* gsrc, uint32_t src_bytes,
-                                                  uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_addr(smem_dst)),
-               "l"(gsrc), "r"(src_bytes), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// Streaming 16-byte load (read once: evicted first from L1 and L2).
+__device__ __forceinline__ int4 ld_stream(const void* p) { return __ldcs(reinterpret_cast<const int4*>(p)); }
 
 // ---------------------------------------------------------------------------
 // scoring geometry for d_idx = 16 * NCH bytes
@@ -240,10 +218,7 @@ struct ScoreGeom {
 
 }  // namespace
 
-size_t select_smem_bytes(const Geometry& g) {
-  const SelLayout L = sel_layout(g);
-  return L.score_warps < 1 ? SMEM_LIMIT + 1 : L.total;   // no room to score: rejected at create
-}
+size_t select_smem_bytes(const Geometry& g) { return sel_layout(g).total; }
 
 // ===========================================================================
 // the kernel
@@ -305,10 +280,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     if (tid == 0) red_release_add(&p.s.sync[0], 1u);
     HS_TRACE(p, 0, 1);
     const int total = carry;
-    const int SW = L.score_warps;
-    if (warp >= SW) return;   // no ring space for this warp (very large request tables)
-    const int W = (p.sel_grid - p.n_resolvers) * SW;
-    const int w0 = ((int)blockIdx.x - p.n_resolvers) * SW + warp;
+    const int W = (p.sel_grid - p.n_resolvers) * NWARP;
+    const int w0 = ((int)blockIdx.x - p.n_resolvers) * NWARP + warp;
 
     // lane roles inside a load instruction
     const int pg = lane / SG::LPP;            // position within the instruction
@@ -324,47 +297,35 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       while (t_prefix[x + 1] <= t) ++x;
       return x;
     };
-    // Each warp streams its sub-tiles (SUB positions, 8 16-byte chunks per lane)
-    // through a ring of SEL_RING shared-memory buffers with cp.async: two are in
-    // flight while one is scored.  A lane reads back exactly the chunks it
-    // copied, so the wait needs no warp barrier.  Positions past N read zeros.
-    static_assert(SG::LD * 32 * 16 <= SUB_BYTES, "a sub-tile fits its buffer");
-    unsigned char* ring = smem_raw + L.s_ring + (size_t)warp * SEL_RING * SUB_BYTES + lane * 16;
-    const uint64_t stream_policy = l2_evict_first_policy();   // index keys are read once per call
-    int r_iss = 0;   // request cursor of the sub-tiles issued
-    auto issue_sub = [&](int k) {   // sub-tile k of this warp into slot k % SEL_RING (an empty group past the end)
-      const int t = w0 + (k >> 1) * W;
-      if (t < total) {
-        r_iss = req_of(t, r_iss);
-        const int ri = r_iss;
-        const int N = t_n[ri];
-        const int pos0 = (t - t_prefix[ri]) * SG::TILE + (k & 1) * SG::SUB;
-        const long long rl = (long long)t_req[ri] * g.n_layers + p.layer;
-        const int8_t* base = p.s.idx_keys + rl * g.max_context * d;
-        const int newpos = p.new_kv ? N - 1 : -1;
-        const int8_t* nk = p.new_keys + (long long)ri * d;
-        unsigned char* dst = ring + (k % SEL_RING) * SUB_BYTES;
+    // loads of sub-tile `half` of tile t (request ri) into v (zeros past N)
+    auto load_sub = [&](int t, int ri, int half, int4 (&v)[SG::LD]) {
+      const int N = t_n[ri];
+      const int pos0 = (t - t_prefix[ri]) * SG::TILE + half * SG::SUB;
+      const long long rl = (long long)t_req[ri] * g.n_layers + p.layer;
+      const int8_t* base = p.s.idx_keys + rl * g.max_context * d;
+      const int newpos = p.new_kv ? N - 1 : -1;
+      const int8_t* nk = p.new_keys + (long long)ri * d;
 #pragma unroll
-        for (int u = 0; u < SG::LD; ++u) {
-          const int pos = pos0 + (u / SG::CPL) * SG::PPI + pg;
-          const int ch = cl * SG::CPL + (u % SG::CPL);
-          const int8_t* src = pos == newpos ? nk + ch * 16 : base + (long long)min(pos, N - 1) * d + ch * 16;
-          cp_async_16_zfill(dst + u * 512, src, pos < N ? 16u : 0u, stream_policy);
-        }
+      for (int u = 0; u < SG::LD; ++u) {
+        const int pos = pos0 + (u / SG::CPL) * SG::PPI + pg;
+        const int ch = cl * SG::CPL + (u % SG::CPL);
+        v[u] = make_int4(0, 0, 0, 0);
+        if (pos < N) v[u] = pos == newpos ? *reinterpret_cast<const int4*>(nk + ch * 16)
+                                          : ld_stream(base + (long long)pos * d + ch * 16);
       }
-      cp_async_commit();
     };
 
     int r_cur = 0;
-    for (int k = 0; k < SEL_RING - 1; ++k) issue_sub(k);
-    for (int k = 0;; ++k) {
-      const int t = w0 + (k >> 1) * W;
-      if (t >= total) break;
-      const int half = k & 1;
-      r_cur = req_of(t, r_cur);
+    int4 va[SG::LD], vb[SG::LD];
+    if (w0 < total) {
+      r_cur = req_of(w0, 0);
+      load_sub(w0, r_cur, 0, va);
+      load_sub(w0, r_cur, 1, vb);
+    }
+    for (int t = w0; t < total; t += W) {
       const int ri = r_cur;
       const int N = t_n[ri];
-      const int sub0 = (t - t_prefix[ri]) * SG::TILE + half * SG::SUB;
+      const int tile0 = (t - t_prefix[ri]) * SG::TILE;
       const uint32_t thr = t_thr[ri];
       if (ri != q_r) {
         q_r = ri;
@@ -378,85 +339,85 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         }
       }
       uint32_t* keys_out = p.s.scores + (long long)ri * p.score_stride;
-      cp_async_wait_group<SEL_RING - 2>();   // sub-tile k has landed
-      int4 v[SG::LD];
-      const unsigned char* src = ring + (k % SEL_RING) * SUB_BYTES;
+      const int tn = t + W;
+      const int rn = tn < total ? req_of(tn, ri) : ri;
 #pragma unroll
-      for (int u = 0; u < SG::LD; ++u) v[u] = *reinterpret_cast<const int4*>(src + u * 512);
-      // refill the slot scored in the previous step (its values are long consumed)
-      issue_sub(k + SEL_RING - 1);
-      int acc[SG::NP][NH];   // each head's partial dot product over this lane's chunks
+      for (int half = 0; half < 2; ++half) {
+        int4 (&v)[SG::LD] = half == 0 ? va : vb;
+        int acc[SG::NP][NH];   // each head's partial dot product over this lane's chunks
 #pragma unroll
-      for (int j = 0; j < SG::NP; ++j)
+        for (int j = 0; j < SG::NP; ++j)
 #pragma unroll
-        for (int h = 0; h < NH; ++h) acc[j][h] = 0;
+          for (int h = 0; h < NH; ++h) acc[j][h] = 0;
 #pragma unroll
-      for (int u = 0; u < SG::LD; ++u) {
-        const int j = u / SG::CPL;
+        for (int u = 0; u < SG::LD; ++u) {
+          const int j = u / SG::CPL;
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int4 qq = q[h][u % SG::CPL];
-          acc[j][h] = __dp4a(v[u].x, qq.x, acc[j][h]);
-          acc[j][h] = __dp4a(v[u].y, qq.y, acc[j][h]);
-          acc[j][h] = __dp4a(v[u].z, qq.z, acc[j][h]);
-          acc[j][h] = __dp4a(v[u].w, qq.w, acc[j][h]);
+          for (int h = 0; h < NH; ++h) {
+            const int4 qq = q[h][u % SG::CPL];
+            acc[j][h] = __dp4a(v[u].x, qq.x, acc[j][h]);
+            acc[j][h] = __dp4a(v[u].y, qq.y, acc[j][h]);
+            acc[j][h] = __dp4a(v[u].z, qq.z, acc[j][h]);
+            acc[j][h] = __dp4a(v[u].w, qq.w, acc[j][h]);
+          }
         }
-      }
-      // key of each position group: single head, score + 2^22 (24 bits); several
-      // heads, sum_h w_h * max(0, dot_h) (non-negative, below 2^32)
-      uint32_t key[SG::NP];
+        // the buffer is free: start the same half of this warp's next tile
+        if (tn < total) load_sub(tn, rn, half, v);
+        // key of each position group: single head, score + 2^22 (24 bits); several
+        // heads, sum_h w_h * max(0, dot_h) (non-negative, below 2^32)
+        uint32_t key[SG::NP];
 #pragma unroll
-      for (int j = 0; j < SG::NP; ++j) {
-        unsigned tot = 0;
+        for (int j = 0; j < SG::NP; ++j) {
+          unsigned tot = 0;
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          int dh = acc[j][h];
+          for (int h = 0; h < NH; ++h) {
+            int dh = acc[j][h];
 #pragma unroll
-          for (int o = 1; o < SG::LPP; o <<= 1) dh += __shfl_xor_sync(FULL_MASK, dh, o);
-          if (NH == 1) tot = (unsigned)(dh + IDX_KEY_BIAS);
-          else tot += (unsigned)qw[h] * (unsigned)max(dh, 0);
+            for (int o = 1; o < SG::LPP; o <<= 1) dh += __shfl_xor_sync(FULL_MASK, dh, o);
+            if (NH == 1) tot = (unsigned)(dh + IDX_KEY_BIAS);
+            else tot += (unsigned)qw[h] * (unsigned)max(dh, 0);
+          }
+          key[j] = tot;
         }
-        key[j] = tot;
-      }
-      // lane cl of a position group owns position groups j with j % LPP == cl
-      uint32_t ownk[SG::OWN];
-      int ownp[SG::OWN];
+        // lane cl of a position group owns position groups j with j % LPP == cl
+        const int sub0 = tile0 + half * SG::SUB;
+        uint32_t ownk[SG::OWN];
+        int ownp[SG::OWN];
 #pragma unroll
-      for (int o = 0; o < SG::OWN; ++o) {
-        ownk[o] = 0;
-        ownp[o] = N;   // none
-      }
-#pragma unroll
-      for (int j = 0; j < SG::NP; ++j) {
-        if (j % SG::LPP == cl) {
-          const int o = j / SG::LPP;
-          ownp[o] = sub0 + j * SG::PPI + pg;
-          ownk[o] = key[j];
+        for (int o = 0; o < SG::OWN; ++o) {
+          ownk[o] = 0;
+          ownp[o] = N;   // none
         }
-      }
 #pragma unroll
-      for (int o = 0; o < SG::OWN; ++o) {
-        const bool valid = ownp[o] < N;
-        if (valid) keys_out[ownp[o]] = ownk[o];
-        if (thr != 0u) {
-          const bool c = valid && ownk[o] >= thr;
-          const unsigned m = __ballot_sync(FULL_MASK, c);
-          if (m) {
-            unsigned base = 0;
-            if (lane == 0) base = atomicAdd(p.s.cand_cnt + ri, (unsigned)__popc(m));
-            base = __shfl_sync(FULL_MASK, base, 0);
-            const unsigned at = base + __popc(m & ((1u << lane) - 1u));
-            if (c && at < 2u * (unsigned)K)
-              p.s.cand[(long long)ri * 2 * K + at] = make_uint2((uint32_t)ownp[o], ownk[o]);
+        for (int j = 0; j < SG::NP; ++j) {
+          if (j % SG::LPP == cl) {
+            const int o = j / SG::LPP;
+            ownp[o] = sub0 + j * SG::PPI + pg;
+            ownk[o] = key[j];
+          }
+        }
+#pragma unroll
+        for (int o = 0; o < SG::OWN; ++o) {
+          const bool valid = ownp[o] < N;
+          if (valid) keys_out[ownp[o]] = ownk[o];
+          if (thr != 0u) {
+            const bool c = valid && ownk[o] >= thr;
+            const unsigned m = __ballot_sync(FULL_MASK, c);
+            if (m) {
+              unsigned base = 0;
+              if (lane == 0) base = atomicAdd(p.s.cand_cnt + ri, (unsigned)__popc(m));
+              base = __shfl_sync(FULL_MASK, base, 0);
+              const unsigned at = base + __popc(m & ((1u << lane) - 1u));
+              if (c && at < 2u * (unsigned)K)
+                p.s.cand[(long long)ri * 2 * K + at] = make_uint2((uint32_t)ownp[o], ownk[o]);
+            }
           }
         }
       }
-      if (half == 1) {   // the warp tile is done
-        __syncwarp();
-        if (lane == 0) red_release_add(p.s.tiles_done + ri, 1u);
-      }
+      __syncwarp();
+      if (lane == 0) red_release_add(p.s.tiles_done + ri, 1u);
+      r_cur = rn;
     }
-    cp_async_wait_group<0>();
     HS_TRACE(p, 0, 2);
     return;
   }
