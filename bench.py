@@ -644,6 +644,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         "link_gbs": round(link_total / (ms_total * 1e-3) / 1e9, 2),
         "link_peak_gbs": round(peak_link, 1),
         "miss_rate": round(misses / max(1, hits + misses), 5),
+        "full_select_frac": round((st1["full_selects"] - st0["full_selects"]) / max(1, K * L * R), 4),
         "misses_per_layer_step": round(misses / (K * L), 1),
         "step_roofline": {"t_roof_ms": round(t_roof * 1e3 / K, 4), "t_meas_ms": round(ms_step, 4),
                           "frac": round(step_frac, 4), "hbm_bytes_per_step": int(hbm_total / K),

@@ -53,6 +53,8 @@ extern "C" {
 #define HS_DEVERR_EMPTY 0x4u      /* decode of a request with no positions: output set to 0 */
 #define HS_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel gave up */
 #define HS_DEVERR_METADATA 0x10u  /* page table / reverse map found inconsistent */
+#define HS_DEVERR_NO_LEAD 0x20u   /* a follower layer of a shared selection was decoded without
+                                     its group lead's selection of the same step: output 0 */
 
 /*
  * Configuration.  Positions and rows:
@@ -136,6 +138,18 @@ typedef struct hs_config {
                                  (negative weights count as 0).  Selection, ties and the cache
                                  rule are the same; the top-k then takes three digit passes over
                                  the keys and no candidate list. */
+  int32_t index_share;        /* layers per indexer group, G (0 or 1: every layer selects for itself).
+                                 With G > 1 (GQA rows only), layer l selects only when l % G == 0
+                                 (the group's lead); layers l+1 .. l+G-1 of the same step reuse its
+                                 selection, as a model that shares one indexer's choice across a
+                                 group of layers does.  Every call of such a handle must append its
+                                 token through new_kv_rows / new_idx_keys, and a step must call the
+                                 lead before its followers (else HS_DEVERR_NO_LEAD, output 0). */
+  int32_t share_prefetch;     /* with G > 1: 1 = the lead's call also resolves every follower layer
+                                 (page table, LRU, stamps) and pulls its missed rows into its slots
+                                 right away, so a follower's call only appends its token and attends
+                                 (the prefetch that a shared selection makes exact); 0 = each
+                                 follower resolves and pulls at its own call. */
 } hs_config_t;
 
 #define HS_REPLACE_LRU 0
@@ -155,6 +169,8 @@ typedef struct hs_stats {
   uint64_t hot_bytes;     /* size of the HBM hot cache */
   uint64_t index_bytes;   /* size of the HBM index-key store */
   uint64_t meta_bytes;    /* page table, reverse map, stamps, LRU order, counters */
+  uint64_t full_selects;  /* selections that scanned every key (no usable candidate list:
+                             first steps, a large drift, contexts above 20 k positions) */
   uint32_t device_error;  /* HS_DEVERR_* bits seen so far (sticky) */
   uint32_t _pad;
 } hs_stats_t;

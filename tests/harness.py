@@ -17,13 +17,13 @@ def torch_mod():
 
 
 def make_cache(w: wl.Workload, steps: int, hot_slots: int | None = None, device: int = 0, fetch_mode: int = 2,
-               replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False):
+               replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False, **extra):
     from tiered_kv_cache_int8_gb300 import HiSparseCache
     return HiSparseCache(n_layers=w.n_layers, max_requests=w.n_requests, max_context=w.max_context(steps),
                          h_q=w.h_q, h_kv=w.h_kv, d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k,
                          hot_slots=hot_slots or w.hot_slots, shared_kv=w.shared_kv, device=device,
                          fetch_mode=fetch_mode, replacement=replacement, replacement_seed=replacement_seed,
-                         write_allocate=write_allocate, idx_heads=w.idx_heads)
+                         write_allocate=write_allocate, idx_heads=w.idx_heads, **extra)
 
 
 def packed_q_idx(w: wl.Workload, heads: np.ndarray, weights: np.ndarray) -> np.ndarray:

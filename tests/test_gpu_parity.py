@@ -557,3 +557,73 @@ def test_multihead_indexer_ties_and_short_contexts():
     assert np.array_equal(sel.cpu().numpy(), np.tile(np.arange(256, dtype=np.int32), (2, 1)))
     assert cache.stats()["device_error"] == 0
     cache.close()
+
+
+def _shared_selection_oracle(w, steps, share, write_allocate=False):
+    """Per (request, layer, step): (sel, step result, snapshot) when every layer
+    reuses its group lead's selection of the same step (lead = layer - layer % share)."""
+    out = {}
+    for r in range(w.n_requests):
+        n0 = int(w.contexts()[r])
+        leads = {}
+        for lead in range(0, w.n_layers, share):
+            keys = wl.idx_keys_upto(w, r, lead, steps)
+            sc = indexer_scores_many(keys, wl.query_walk(w, r, lead, steps))
+            leads[lead] = [topk_select(sc[:n0 + t + 1, t], w.top_k) for t in range(steps)]
+        for l in range(w.n_layers):
+            cache = LRUHotCache(w.hot_slots)
+            for t in range(steps):
+                sel = leads[l - l % share][t]
+                st = cache.step(sel, allocate=n0 + t if write_allocate else None)
+                out[r, l, t] = (sel, st, cache.snapshot(n0 + t + 1))
+    return out
+
+
+@pytest.mark.parametrize("share,prefetch,fetch_mode,wa", [(2, True, 2, False), (4, True, 0, True),
+                                                           (2, False, 0, False), (4, False, 1, False)])
+def test_shared_selection_matches_the_oracle(share, prefetch, fetch_mode, wa):
+    # layers of a group reuse the lead's selection; with prefetch the lead's call
+    # resolves the followers and pulls their rows ahead, without it each follower
+    # resolves at its own call: same selections, cache state and outputs
+    steps = 6
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=4, context=3000, top_k=256, hot_slots=384,
+                         steps=steps, sigma=0.3)
+    cache = make_cache(w, steps, fetch_mode=fetch_mode, write_allocate=wa, index_share=share,
+                       share_prefetch=prefetch)
+    prefill(cache, w)
+    got = run_steps(cache, w, StepInputs(w, steps), steps, collect_meta=True, fused=True)
+    ref = _shared_selection_oracle(w, steps, share, wa)
+    for l in range(w.n_layers):
+        for r in range(w.n_requests):
+            prev_h = prev_m = 0
+            for t in range(steps):
+                sel, st, snap = ref[r, l, t]
+                g_sel = got["sel"][l, t][r]
+                assert np.array_equal(g_sel[:sel.size], sel), f"selection r{r} l{l} t{t}"
+                page, rev, stamp, order, (length, step, hits, misses) = got["meta"][l, t][r]
+                assert length == int(w.contexts()[r]) + t + 1 and step == t + 1
+                assert (hits - prev_h, misses - prev_m) == (st["hits"], st["misses"]), f"hit/miss r{r} l{l} t{t}"
+                prev_h, prev_m = hits, misses
+                assert np.array_equal(page, snap[0]) and np.array_equal(rev, snap[1])
+                assert np.array_equal(stamp, snap[2])
+                check_order(order, stamp)
+                o = oracle_attention(w, r, l, t, sel)
+                ma, rel = attention_error(got["out"][l, t][r], o)
+                assert ma <= MAX_ABS and rel <= REL_L2, f"attention r{r} l{l} t{t}: {ma} {rel}"
+    assert cache.stats()["device_error"] == 0
+    cache.close()
+
+
+def test_follower_without_its_lead_is_reported():
+    import torch
+    from tiered_kv_cache_int8_gb300 import hs
+    w = wl.make_workload("batch16_32k", n_requests=2, n_layers=2, context=1000, top_k=128, hot_slots=256,
+                         steps=1)
+    cache = make_cache(w, 1, index_share=2, share_prefetch=True)
+    prefill(cache, w)
+    inp = StepInputs(w, 1)
+    out = cache.decode_layer(1, inp.q_idx[1, 0], inp.q[1, 0], new_kv=inp.kv[1, 0], new_keys=inp.keys[1, 0])
+    torch.cuda.synchronize()
+    assert cache.stats()["device_error"] & hs.HS_DEVERR_NO_LEAD
+    assert not out.view(torch.int16).any()
+    cache.close()

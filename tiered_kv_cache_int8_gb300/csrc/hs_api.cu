@@ -44,6 +44,9 @@ std::string check_config(const hs_config_t& c) {
   if (c.replacement != HS_REPLACE_LRU && c.replacement != HS_REPLACE_FIFO && c.replacement != HS_REPLACE_RANDOM)
     return "replacement must be HS_REPLACE_LRU (0), HS_REPLACE_FIFO (1) or HS_REPLACE_RANDOM (2)";
   if (c.write_allocate != 0 && c.write_allocate != 1) return "write_allocate must be 0 or 1";
+  if (c.index_share < 0 || c.index_share > c.n_layers) return "index_share must be in [0, n_layers]";
+  if (c.share_prefetch != 0 && c.share_prefetch != 1) return "share_prefetch must be 0 or 1";
+  if (c.index_share > 1 && c.shared_kv) return "index_share > 1 is supported for GQA rows";
   if (c.idx_heads < 0 || c.idx_heads > 8 || (c.idx_heads > 1 && (c.idx_heads & (c.idx_heads - 1))))
     return "idx_heads must be 0, 1, 2, 4 or 8";
   if (c.idx_heads > 1 && c.d_idx != 64 && c.d_idx != 128)
@@ -321,6 +324,11 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.tiles_done, R * 4, false},
       {(void**)&s.ready, R * 4, false},
       {(void**)&s.sync, 16, false},
+      {(void**)&s.sh_sel, cfg->index_share > 1 ? R * Lr * K * 4 : 16, false},
+      {(void**)&s.sh_slots, cfg->index_share > 1 ? R * Lr * K * 4 : 16, false},
+      {(void**)&s.sh_kk, R * Lr * 4, false},
+      {(void**)&s.sh_pend, R * Lr * 4, false},
+      {(void**)&s.sh_armed, R * Lr * 4, false},
 #ifdef HS_WITH_TRACE
       {(void**)&h->trace, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8, false},
 #endif
@@ -356,6 +364,9 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.tiles_done, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.ready, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.sync, 0, 16) == cudaSuccess;
+  ok = ok && cudaMemset(s.sh_armed, 0, R * Lr * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.sh_kk, 0, R * Lr * 4) == cudaSuccess;
+  ok = ok && cudaMemset(s.sh_pend, 0xff, R * Lr * 4) == cudaSuccess;
 #ifdef HS_WITH_TRACE
   ok = ok && cudaMemset(h->trace, 0, 2 * (size_t)hs::TRACE_KERNELS * hs::TRACE_CTAS * hs::TRACE_POINTS * 8) ==
                  cudaSuccess;
@@ -436,6 +447,10 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
     return set_err(h, HS_ERR_INVALID, "hs_decode_layer: new_kv_rows and new_idx_keys go together");
   if (new_kv_rows && (!aligned16(new_kv_rows) || !aligned16(new_idx_keys)))
     return set_err(h, HS_ERR_INVALID, "hs_decode_layer: new_kv_rows and new_idx_keys must be 16-byte aligned");
+  const int G = h->cfg.index_share > 1 ? h->cfg.index_share : 1;
+  if (G > 1 && !new_kv_rows)
+    return set_err(h, HS_ERR_INVALID, "hs_decode_layer: with index_share > 1 every call appends its token "
+                                      "(new_kv_rows, new_idx_keys)");
   use_device(h);
   hs::DecodeParams p;
   p.g = h->g;
@@ -463,11 +478,19 @@ int hs_decode_layer(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t*
   p.publish = h->cfg.shared_kv ? 0 : 1;   // the chunked GQA kernel starts on published requests
   p.fault = h->fault;
   p.write_allocate = h->cfg.write_allocate;
+  const bool lead = layer % G == 0;
+  p.role = lead ? hs::ROLE_SELECT : hs::ROLE_GIVEN;
+  p.n_follow = lead ? std::min(G, h->cfg.n_layers - layer) - 1 : 0;
+  p.share_prefetch = h->cfg.share_prefetch;
 #ifdef HS_WITH_TRACE
   p.trace = h->trace;
 #endif
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = timed_launch(h, HS_K_SELECT, st, [&] { return hs::launch_select(p, h->sel_smem, st); });
+  // a follower of a prefetching group only appends its token and attends
+  const bool follow = !lead && p.share_prefetch;
+  cudaError_t e = timed_launch(h, HS_K_SELECT, st, [&] {
+    return follow ? hs::launch_follow(p, st) : hs::launch_select(p, h->sel_smem, st);
+  });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: select launch");
   e = timed_launch(h, HS_K_ATTENTION, st, [&] { return hs::launch_attention(p, h->att_smem, st); });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_decode_layer: attention launch");
@@ -502,6 +525,7 @@ int hs_stats(hs_handle_t* h, hs_stats_t* out) {
   out->hot_bytes = h->hot_bytes;
   out->index_bytes = h->index_bytes;
   out->meta_bytes = h->meta_bytes;
+  out->full_selects = glob[2];
   out->device_error = err;
   if (err) return set_err(h, HS_ERR_DEVICE, "hs_stats: device error word " + std::to_string(err));
   return HS_OK;
@@ -562,6 +586,7 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream) {
       (e = cudaMemsetAsync(h->s.hits + r * L, 0, L * 8, st)) != cudaSuccess ||
       (e = cudaMemsetAsync(h->s.misses + r * L, 0, L * 8, st)) != cudaSuccess ||
       (e = cudaMemsetAsync(h->s.cand_thr + r * L, 0, L * 4, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->s.sh_armed + r * L, 0, L * 4, st)) != cudaSuccess ||
       (e = hs::launch_init_order(h->s.order + r * L * B, (long long)L, (int)B, st)) != cudaSuccess)
     return cuda_fail(h, e, "hs_reset_request");
   return HS_OK;

@@ -29,6 +29,7 @@ constexpr int RES_THREADS = 1024;    // top-k CTA of the static (no-allocation) 
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_GROUP = 256;       // threads of one scoring group
 constexpr int SEL_MAX_RESOLVERS = 16;
+constexpr int ROLE_SELECT = 0, ROLE_GIVEN = 1;
 
 // slot_of_sel entries of rows RESOLVE left for the attention kernel to fetch
 constexpr int HS_SLOT_MISS_FLAG = 0x40000000;
@@ -62,7 +63,7 @@ struct DeviceState {
   int32_t* step;           // [R][L]
   unsigned long long* hits;    // [R][L]
   unsigned long long* misses;  // [R][L]
-  unsigned long long* glob;    // [0] h2d bytes, [1] d2h bytes
+  unsigned long long* glob;    // [0] h2d bytes, [1] d2h bytes, [2] selections over every key
   unsigned int* dev_error;     // sticky HS_DEVERR_* bits
   // scratch (one call in flight per handle)
   uint32_t* scores;        // [R][score_stride] 24-bit keys of the current call
@@ -83,6 +84,13 @@ struct DeviceState {
   // is reset by the last party that reads it)
   unsigned int* tiles_done;    // [R] score tiles of request i finished (select kernel)
   unsigned int* ready;         // [R] k_eff + 1 once request i's selection and slots are published
+  // a selection shared by a group of layers (index_share > 1): what the group's
+  // lead call leaves for each follower layer [R][L][...]
+  int32_t* sh_sel;             // [R][L][k] the shared selection (positions, ascending)
+  int32_t* sh_slots;           // [R][L][k] the follower's slot of each (resolved ahead)
+  int32_t* sh_kk;              // [R][L] k_eff
+  int32_t* sh_pend;            // [R][L] slot awaiting the follower's own appended row (-1: none)
+  int32_t* sh_armed;           // [R][L] 1: left by the lead of this step, not yet used
   unsigned int* sync;          // [4]: 0 = CTAs of the select kernel past their set-up,
                                //      1 = resolvers finished, 2 = next attention work item,
                                //      3 = attention CTAs finished
@@ -121,6 +129,11 @@ struct DecodeParams {
   int publish;             // 1: resolvers publish each request (the chunked attention kernel waits on it)
   int fault;               // test hook: 1 = the resolver never publishes request 0 (a wait runs out)
   int write_allocate;      // 1: the token this call appends counts as used (filled if not selected)
+  int role;                // ROLE_SELECT: this call selects; ROLE_GIVEN: it resolves the selection its
+                           // group's lead left (no scoring)
+  int n_follow;            // ROLE_SELECT with index_share: follower layers of the group after this one
+  int share_prefetch;      // 1: resolve the followers now (pulling their missed rows ahead); 0: leave
+                           // the selection for them to resolve at their own calls
 #ifdef HS_WITH_TRACE
   unsigned long long* trace;   // [2][3][1024][64]: clock64 and %globaltimer per (kernel, CTA, point)
 #endif
@@ -162,6 +175,7 @@ namespace hs {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_follow(const DecodeParams& p, cudaStream_t st);
 size_t select_smem_bytes(const Geometry& g);
 cudaError_t prepare_select(const Geometry& g, size_t smem);
 cudaError_t launch_attention(const DecodeParams& p, size_t smem, cudaStream_t st);

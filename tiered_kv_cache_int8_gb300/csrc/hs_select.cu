@@ -146,8 +146,10 @@ __host__ __device__ inline SelLayout sel_layout(const Geometry& g) {
 struct SelShared {
   int scan[2 * (NWARP + 1)];
   int b1, above1, b2, above2, bt, above_t;
+  int thr_src;   // where the next threshold's low digit is found: 0 none, 1 the candidate list, 2 all keys
   int rb1, rabove1, rb2, rabove2;   // random replacement: digits of the m-th smallest key
   int len, N, t_step, cnt, req, ok;
+  int t_step_f, len_f;   // a follower layer's step counter and length
   uint32_t thr, thr_next;
 };
 
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
           thr = p.s.cand_thr[rl];
         }
-        const bool scored = N > K;
+        const bool scored = N > K && p.role == ROLE_SELECT;
         nt = scored ? (N + SG::TILE - 1) / SG::TILE : 0;
         t_req[i] = scored ? req : -1;
         t_n[i] = N;
@@ -484,8 +486,16 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       sh.N = N;
       sh.ok = 1;
       if (N == 0) set_error(p.s.dev_error, HS_DEVERR_EMPTY);   // nothing to attend: the output is 0
+      if (p.role == ROLE_GIVEN) {   // the lead of this step must have left a selection of this length
+        const bool armed = p.s.sh_armed[rl] != 0 && p.s.sh_kk[rl] == min(K, N);
+        p.s.sh_armed[rl] = 0;
+        if (!armed) {
+          set_error(p.s.dev_error, HS_DEVERR_NO_LEAD);
+          sh.ok = 0;
+        }
+      }
       sh.thr_next = 0u;
-      if (N > K) {   // wait until every tile of this request is scored
+      if (N > K && p.role == ROLE_SELECT) {   // wait until every tile of this request is scored
         const unsigned ntile = (unsigned)((N + SG::TILE - 1) / SG::TILE);
         if (!wait_counter(p.s.tiles_done + ri, ntile)) {
           set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
@@ -503,7 +513,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     HS_TRACE_IF(p, 1, 1, tid == 0 && ri == (int)blockIdx.x);
     const int len = sh.len, N = sh.N, t_step = sh.t_step;
     const bool appended = N > len;
-    const int kk = sh.ok ? min(K, N) : 0;
+    const int kk = sh.ok ? min(K, N) : 0;   // (a given selection has the same k_eff: same N)
 
     // ======================= 1. top-k, ascending =======================
     // The previous call's threshold listed between k and min(2k, 4096) keys: the k
@@ -511,9 +521,16 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     const bool use_cand = sh.ok && N > K && L.fast && (N + 31) / 32 <= CAND_WORDS && sh.thr != 0u &&
                           sh.cnt >= K && sh.cnt <= min(2 * K, CAND_REG * NT);
     bool slots_known = false;   // the candidate path reads each selected position's page entry itself
-    const int k_next = (int)min((long long)N, (long long)K + K / 4);
+    // the next call lists keys at or above the exact key of rank 1.5 k (found after
+    // publication): about 1.5 k of them, half way between k and the list's room
+    const int k_next = (int)min((long long)N, (long long)K + K / 2);
+    if (tid == 0) sh.thr_src = 0;
     if (!sh.ok) {
       // scores incomplete: nothing selected (the output of this request is 0)
+    } else if (p.role == ROLE_GIVEN) {
+      // the selection this layer's group lead left for it (same step, same positions)
+      const int32_t* gsel = p.s.sh_sel + rl * K;
+      for (int i = tid; i < kk; i += NT) sel[i] = __ldcg(gsel + i);
     } else if (N <= K) {
       for (int i = tid; i < N; i += NT) sel[i] = i;
     } else if (use_cand) {
@@ -548,7 +565,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
       if (cnt >= k_next) {
         select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
-        if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
+        if (tid == 0) {
+          sh.thr_next = (uint32_t)sh.bt << 12;
+          sh.thr_src = 1;
+        }
       } else if (tid == 0) {
         sh.thr_next = sh.thr;   // the list held fewer: keep the threshold that gave >= k
       }
@@ -695,37 +715,35 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     } else {
       const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
       const bool fast = L.fast && N <= FAST_MAX_N;
+      if (tid == 0) red_add_u64(&p.s.glob[2], 1ull);   // a selection over every key
       for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
       __syncthreads();
       // first-digit histogram: when the candidate list only overflowed, every one of
       // the k largest keys clears the threshold, so only those keys are counted;
-      // else all keys.  Lanes adding to the same bin are combined first (the bins
-      // near the middle of the score distribution are hot).
+      // else all keys
       {
         const uint32_t floor_key = (sh.thr != 0u && sh.cnt >= K) ? sh.thr : 0u;
         const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // rows padded to a multiple of 4 keys
         const int n4 = N >> 2;
-        auto hadd = [&](uint32_t k, bool valid) {   // called by every lane of the warp
-          const unsigned bin = (valid && k >= floor_key) ? (k >> 12) : 0xFFFFFFFFu;
-          const unsigned peers = __match_any_sync(FULL_MASK, bin);
-          if (bin != 0xFFFFFFFFu && __ffs(peers) - 1 == lane) atomicAdd(&h[bin], (unsigned)__popc(peers));
+        auto hadd = [&](uint32_t k) {
+          if (k >= floor_key) atomicAdd(&h[k >> 12], 1u);
         };
         constexpr int UA = 8;
-        for (int b0 = tid & ~31; b0 < n4; b0 += UA * NT) {   // warp-uniform trip count
+        for (int i0 = tid; i0 < n4; i0 += UA * NT) {
           uint4 v[UA];
 #pragma unroll
           for (int u = 0; u < UA; ++u) {
-            const int i = b0 + lane + u * NT;
+            const int i = i0 + u * NT;
             v[u] = i < n4 ? __ldcg(k4 + i) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
-          for (int u = 0; u < UA; ++u) {
-            const bool ok = b0 + lane + u * NT < n4;
-            hadd(v[u].x, ok);
-            hadd(v[u].y, ok);
-            hadd(v[u].z, ok);
-            hadd(v[u].w, ok);
-          }
+          for (int u = 0; u < UA; ++u)
+            if (i0 + u * NT < n4) {
+              hadd(v[u].x);
+              hadd(v[u].y);
+              hadd(v[u].z);
+              hadd(v[u].w);
+            }
         }
         for (int i = 4 * n4 + tid; i < N; i += NT) {
           const uint32_t k = __ldcg(keys + i);
@@ -739,7 +757,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const int counted = (sh.thr != 0u && sh.cnt >= K) ? sh.cnt : N;   // keys the histogram holds
       if (counted >= k_next) {
         select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
-        if (tid == 0) sh.thr_next = (uint32_t)sh.bt << 12;
+        if (tid == 0) {
+          sh.thr_next = (uint32_t)sh.bt << 12;
+          sh.thr_src = 2;
+        }
       } else if (tid == 0) {
         sh.thr_next = sh.thr;
       }
@@ -936,16 +957,44 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     }
 
     // ======================= 2. RESOLVE metadata =======================
-    int32_t* page = p.s.page + rl * g.max_context;
-    int32_t* reverse = p.s.reverse + rl * B;
-    int32_t* stamp = p.s.stamp + rl * B;
-    int32_t* order = p.s.order + rl * B;
+    // pass 0: this call's layer.  Passes 1..n_follow: the follower layers of its
+    // group, which share this selection: each is resolved against its own page
+    // table and LRU list now, and its missed rows are pulled into its slots ahead
+    // of its own call (all but its appended token, whose row comes with that call).
+    bool skip_rest = false;
+    const int n_pass = 1 + ((p.role == ROLE_SELECT && p.share_prefetch && sh.ok) ? p.n_follow : 0);
+    for (int pass = 0; pass < n_pass; ++pass) {
+    const long long rlx = rl + pass;
+    if (pass > 0) {
+      __syncthreads();   // the previous pass is done with the shared arrays
+      for (int j = tid; j < B; j += NT) used[j] = 0;
+      const int32_t* order_f = p.s.order + rlx * B;
+      for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(ord + 4 * c4, order_f + 4 * c4);
+      if (L.rev_smem) {
+        const int32_t* rev_f = p.s.reverse + rlx * B;
+        for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(rev_s + 4 * c4, rev_f + 4 * c4);
+      }
+      if (tid == 0) {
+        sh.t_step_f = p.s.step[rlx];
+        sh.len_f = p.s.length[rlx];
+        if (sh.len_f != len) set_error(p.s.dev_error, HS_DEVERR_METADATA);   // layers must move in step
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      if (sh.len_f != len) continue;
+    }
+    int32_t* page = p.s.page + rlx * g.max_context;
+    int32_t* reverse = p.s.reverse + rlx * B;
+    int32_t* stamp = p.s.stamp + rlx * B;
+    int32_t* order = p.s.order + rlx * B;
     int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
-    const int t = t_step;
+    const int t = pass == 0 ? t_step : sh.t_step_f;
     int m = 0;
-    const bool pull = p.fetch_mode == 1;   // else the attention kernel copies the missed rows
+    // the lead copies its missed rows in fetch mode 1 (else the attention kernel
+    // does); a follower layer always gets its rows now: that is the prefetch
+    const bool pull = pass > 0 || p.fetch_mode == 1;
     bool bad = false;
-    if (kk > 0 && slots_known) {
+    if (kk > 0 && slots_known && pass == 0) {
       for (int i = tid; i < kk; i += NT) {
         const int s4 = slot_sel[i];
         if (s4 >= B) bad = true;
@@ -985,14 +1034,15 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     if (__syncthreads_or(bad)) {
       // inconsistent metadata: publish nothing usable for this request
       if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_METADATA);
-      if (p.publish && tid == 0) {
+      if (pass == 0 && p.publish && tid == 0) {
         __threadfence();
         st_release(p.s.ready + ri, 1u);   // k_eff + 1 = 1: nothing selected
       }
+      skip_rest = pass == 0;
       __syncthreads();
-      continue;
+      break;
     }
-    HS_TRACE_IF(p, 1, 5, tid == 0 && ri == (int)blockIdx.x);
+    HS_TRACE_IF(p, 1, 5, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     // misses in ascending selection order, and the unpinned entries of the LRU list
     const int per_i = (kx + NT - 1) / NT;
     const int i0 = min(kx, tid * per_i), i1 = min(kx, i0 + per_i);
@@ -1015,7 +1065,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         const unsigned long long seed = p.replacement_seed;
         auto rank_of = [&](int j) {
           const int old = L.rev_smem ? rev_s[j] : reverse[j];
-          return random_ikey(seed, rl, t, j, old < 0);
+          return random_ikey(seed, rlx, t, j, old < 0);
         };
         for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
         __syncthreads();
@@ -1067,7 +1117,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
     }
     __syncthreads();
-    HS_TRACE_IF(p, 1, 6, tid == 0 && ri == (int)blockIdx.x);
+    HS_TRACE_IF(p, 1, 6, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     // evict, then record the new residents (stores only); slot of every selected
     // row, misses flagged when the attention kernel copies them
     for (int qq = tid; qq < m; qq += NT) {
@@ -1079,14 +1129,31 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       reverse[v] = pnew;
       page[pnew] = v;
       slot_sel[i] = v;
-      // the appended token's row is in shared memory: it goes to its slot here
-      miss_i[qq] = (pull || (appended && pnew == len)) ? i : (i | HS_SLOT_MISS_FLAG);
+      // the lead's appended token: its row is in shared memory, it goes to its slot
+      // here; a follower's appended token: flagged, its row comes with its own call
+      if (pass == 0) miss_i[qq] = (pull || (appended && pnew == len)) ? i : (i | HS_SLOT_MISS_FLAG);
+      else miss_i[qq] = (appended && pnew == len) ? (i | HS_SLOT_MISS_FLAG) : i;
     }
     __syncthreads();
-    for (int i = tid; i < kk; i += NT) sos[i] = slot_sel[i];
-    __syncthreads();
-    for (int qq = tid; qq < m; qq += NT)
-      if (miss_i[qq] & HS_SLOT_MISS_FLAG) sos[miss_i[qq] & ~HS_SLOT_MISS_FLAG] = victim[qq] | HS_SLOT_MISS_FLAG;
+    if (pass == 0) {
+      for (int i = tid; i < kk; i += NT) sos[i] = slot_sel[i];
+      __syncthreads();
+      for (int qq = tid; qq < m; qq += NT)
+        if (miss_i[qq] & HS_SLOT_MISS_FLAG) sos[miss_i[qq] & ~HS_SLOT_MISS_FLAG] = victim[qq] | HS_SLOT_MISS_FLAG;
+    } else {   // what the follower's own call needs: selection, slots, k_eff, the pending slot
+      int32_t* fs = p.s.sh_slots + rlx * K;
+      int32_t* fp = p.s.sh_sel + rlx * K;
+      for (int i = tid; i < kk; i += NT) {
+        fs[i] = slot_sel[i];
+        fp[i] = sel[i];
+      }
+      if (tid == 0) {
+        int pend = -1;
+        if (m > 0 && (miss_i[m - 1] & HS_SLOT_MISS_FLAG)) pend = victim[m - 1];
+        p.s.sh_pend[rlx] = pend;
+        p.s.sh_kk[rlx] = kk;
+      }
+    }
 
     // ======================= 3. rows this kernel copies into their slots =======================
     // fetch mode 1: every missed row from the host copy; otherwise only the
@@ -1094,8 +1161,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     {
       const int rvec = g.row_bytes / 16;
       const unsigned char* src_base =
-          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
-      unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * B * g.row_bytes;
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
+      unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rlx * B * g.row_bytes;
       if (pull) {
         const long long total = (long long)m * rvec;
         constexpr int U = 8;   // host reads in flight per thread
@@ -1107,8 +1174,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
             if (e < total) {
               const int qq = (int)(e / rvec);
               const int cidx = (int)(e - (long long)qq * rvec);
+              if (miss_i[qq] & HS_SLOT_MISS_FLAG) continue;   // a follower's own new token
               const int pos = sel[miss_i[qq]];
-              v[u] = (appended && pos == len)
+              v[u] = (pass == 0 && appended && pos == len)
                          ? reinterpret_cast<const int4*>(newrow)[cidx]
                          : *reinterpret_cast<const int4*>(src_base + (size_t)pos * g.row_bytes + cidx * 16);
             }
@@ -1119,11 +1187,12 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
             if (e < total) {
               const int qq = (int)(e / rvec);
               const int cidx = (int)(e - (long long)qq * rvec);
+              if (miss_i[qq] & HS_SLOT_MISS_FLAG) continue;
               *reinterpret_cast<int4*>(dst_base + (size_t)victim[qq] * g.row_bytes + cidx * 16) = v[u];
             }
           }
         }
-      } else if (appended && m > 0 && sel[miss_i[m - 1] & ~HS_SLOT_MISS_FLAG] == len) {
+      } else if (pass == 0 && appended && m > 0 && sel[miss_i[m - 1] & ~HS_SLOT_MISS_FLAG] == len) {
         // the appended token is the highest position: if it missed, it is the last miss
         for (int v = tid; v < rvec; v += NT)
           *reinterpret_cast<int4*>(dst_base + (size_t)victim[m - 1] * g.row_bytes + v * 16) =
@@ -1133,8 +1202,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     }
     // ======================= 4. publication =======================
     __syncthreads();
-    HS_TRACE_IF(p, 1, 7, tid == 0 && ri == (int)blockIdx.x);
-    if (p.publish && tid == 0) {
+    HS_TRACE_IF(p, 1, 7, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
+    if (pass == 0 && p.publish && tid == 0) {
       __threadfence();
       if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, (unsigned)kk + 1u);   // k_eff + 1
     }
@@ -1142,16 +1211,43 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // the missed rows the attention kernel will copy start moving over the link
     // into L2 now, line by line, spread over the whole CTA (its later chunks then
     // read them from L2)
-    if (!pull && m > 0) {
+    if (pass == 0 && !pull && m > 0) {
       const int lines = g.row_bytes / 128;
       const unsigned char* src_base =
-          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
       for (int e = tid; e < m * lines; e += NT) {
         const int qq = e / lines;
         if (!(miss_i[qq] & HS_SLOT_MISS_FLAG)) continue;   // the appended token: already in its slot
         const int pos = sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG];
         asm volatile("prefetch.global.L2 [%0];" ::"l"(src_base + (size_t)pos * g.row_bytes + (e - qq * lines) * 128));
       }
+    }
+
+    // the next threshold to the exact key of rank k_next: the low digit of that
+    // key from a histogram of the keys with its high digit (the candidates when
+    // they hold every key that large, else all keys); off the critical path
+    if (pass == 0 && sh.thr_src != 0 && N <= CAND_MAX_N_PER_K * K) {
+      const int src = sh.thr_src;
+      const uint32_t bt = (uint32_t)sh.bt;
+      for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      if (src == 1) {
+        const uint2* cl = p.s.cand + (long long)ri * 2 * K;
+        const int cnt = min(sh.cnt, 2 * K);
+        for (int i = tid; i < cnt; i += NT) {
+          const uint32_t k = __ldcg(cl + i).y;
+          if ((k >> 12) == bt) atomicAdd(&h[k & 4095u], 1u);
+        }
+      } else {
+        const uint32_t* keys = p.s.scores + (long long)ri * p.score_stride;
+        for (int i = tid; i < N; i += NT) {
+          const uint32_t k = __ldcg(keys + i);
+          if ((k >> 12) == bt) atomicAdd(&h[k & 4095u], 1u);
+        }
+      }
+      __syncthreads();
+      select_digit(h, k_next - sh.above_t, sh.scan, &sh.b2, &sh.above2);
+      if (tid == 0) sh.thr_next = (bt << 12) | (uint32_t)sh.b2;
     }
 
     // ======================= 5. metadata after publication =======================
@@ -1179,13 +1275,31 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       for (int sl = j0; sl < j1; ++sl)
         if (refreshed(used[sl])) order[sb++] = sl;
       if (tid == 0) {
-        p.s.step[rl] = t + 1;
+        p.s.step[rlx] = t + 1;
         // counters of the selected positions (an allocated new token is neither)
-        red_add_u64(&p.s.hits[rl], (unsigned long long)(kk - (m - extra)));
-        red_add_u64(&p.s.misses[rl], (unsigned long long)(m - extra));
+        red_add_u64(&p.s.hits[rlx], (unsigned long long)(kk - (m - extra)));
+        red_add_u64(&p.s.misses[rlx], (unsigned long long)(m - extra));
         red_add_u64(&p.s.glob[0], (unsigned long long)(m - extra) * g.row_bytes);
       }
     }
+    if (pass > 0 && tid == 0) p.s.sh_armed[rlx] = 1;   // ready for the follower's call
+    }   // passes
+    if (skip_rest) {
+      __syncthreads();
+      continue;
+    }
+    // a group lead that does not prefetch leaves the selection for its followers
+    if (p.role == ROLE_SELECT && !p.share_prefetch && p.n_follow > 0 && sh.ok) {
+      for (int f = 1; f <= p.n_follow; ++f) {
+        int32_t* fp = p.s.sh_sel + (rl + f) * K;
+        for (int i = tid; i < kk; i += NT) fp[i] = sel[i];
+        if (tid == 0) {
+          p.s.sh_kk[rl + f] = kk;
+          p.s.sh_armed[rl + f] = 1;
+        }
+      }
+    }
+
     // the appended token: key to the HBM store, row to the pinned host copy
     if (appended) {
       const int rvec = g.row_bytes / 16;
@@ -1259,6 +1373,105 @@ cudaError_t prepare_select(const Geometry& g, size_t smem) { return dispatch_sel
 
 cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st) {
   return dispatch_select(p.g, &p, smem, st);
+}
+
+}  // namespace hs
+
+// ===========================================================================
+// A follower layer's call under a shared selection whose group lead already
+// resolved it (share_prefetch): no scoring, no top-k, no RESOLVE.  One CTA per
+// request appends this layer's token (key to the HBM store, row to the host
+// copy, length + 1), puts that row into its slot when the shared selection took
+// it (the lead could not: the row did not exist yet), and publishes the
+// prepared slots to the attention kernel launched after it.
+// ===========================================================================
+namespace hs {
+
+constexpr int FOL_THREADS = 256;
+
+__global__ void __launch_bounds__(FOL_THREADS) follow_kernel(DecodeParams p) {
+  const Geometry& g = p.g;
+  const int tid = threadIdx.x;
+  const int ri = blockIdx.x;
+  const int K = g.top_k;
+  __shared__ int s_kk, s_len, s_ok;
+  griddep_wait();   // the lead's slots, lengths and earlier appends
+  griddep_launch_dependents();
+  int32_t* sel_out = p.sel_out ? p.sel_out + (long long)ri * K : nullptr;
+  const int req = p.req_ids ? p.req_ids[ri] : ri;
+  if (req < 0 || req >= g.max_requests) {
+    if (tid == 0) {
+      set_error(p.s.dev_error, HS_DEVERR_REQ_RANGE);
+      __threadfence();
+      st_release(p.s.ready + ri, 1u);   // nothing selected
+    }
+    if (sel_out)
+      for (int i = tid; i < K; i += FOL_THREADS) sel_out[i] = -1;
+    return;
+  }
+  const long long rl = (long long)req * g.n_layers + p.layer;
+  if (tid == 0) {
+    const int len = p.s.length[rl];
+    int N = len;
+    if (p.new_kv) {
+      if (len + 1 <= g.max_context) N = len + 1;
+      else set_error(p.s.dev_error, HS_DEVERR_CAPACITY);
+    }
+    const int kk = p.s.sh_kk[rl];
+    const bool ok = p.s.sh_armed[rl] != 0 && kk == min(K, N);
+    if (!ok) set_error(p.s.dev_error, HS_DEVERR_NO_LEAD);
+    p.s.sh_armed[rl] = 0;
+    s_kk = ok ? kk : 0;
+    s_len = len;
+    s_ok = N > len;   // appended
+  }
+  __syncthreads();
+  const int kk = s_kk, len = s_len;
+  const bool appended = s_ok != 0;
+  const int rvec = g.row_bytes / 16;
+  // this layer's token: into its slot when the shared selection took it
+  const int pend = kk > 0 ? p.s.sh_pend[rl] : -1;
+  if (appended && pend >= 0 && pend < g.hot_slots) {
+    const int4* src = reinterpret_cast<const int4*>(p.new_kv + (long long)ri * g.row_elems);
+    int4* dst = reinterpret_cast<int4*>(p.s.hot + ((size_t)rl * g.hot_slots + pend) * g.row_elems);
+    for (int v = tid; v < rvec; v += FOL_THREADS) dst[v] = src[v];
+  }
+  // the prepared slots and the selection, for the attention kernel and sel_out
+  const int32_t* fs = p.s.sh_slots + rl * K;
+  const int32_t* fp = p.s.sh_sel + rl * K;
+  int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
+  int32_t* sel_g = p.s.sel + (long long)ri * K;
+  for (int i = tid; i < K; i += FOL_THREADS) {
+    const int pos = i < kk ? __ldcg(fp + i) : -1;
+    if (i < kk) {
+      sos[i] = __ldcg(fs + i);
+      sel_g[i] = pos;
+    }
+    if (sel_out) sel_out[i] = pos;
+  }
+  // the append itself: key to the HBM store, row to the pinned host copy
+  if (appended) {
+    const int4* src = reinterpret_cast<const int4*>(p.new_kv + (long long)ri * g.row_elems);
+    int4* dst = reinterpret_cast<int4*>(p.s.host_kv + ((size_t)rl * g.max_context + len) * g.row_elems);
+    for (int v = tid; v < rvec; v += FOL_THREADS) dst[v] = src[v];
+    if (tid < g.d_idx / 16)
+      reinterpret_cast<int4*>(p.s.idx_keys + ((size_t)rl * g.max_context + len) * g.d_idx)[tid] =
+          reinterpret_cast<const int4*>(p.new_keys + (long long)ri * g.d_idx)[tid];
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");   // slot writes, read by bulk copies
+  __syncthreads();
+  if (tid == 0) {
+    if (appended) {
+      p.s.length[rl] = len + 1;
+      red_add_u64(&p.s.glob[1], (unsigned long long)g.row_bytes);
+    }
+    __threadfence();
+    st_release(p.s.ready + ri, (unsigned)kk + 1u);   // k_eff + 1
+  }
+}
+
+cudaError_t launch_follow(const DecodeParams& p, cudaStream_t st) {
+  return launch_pdl(follow_kernel, dim3(p.n_req), dim3(FOL_THREADS), 0, st, p);
 }
 
 }  // namespace hs

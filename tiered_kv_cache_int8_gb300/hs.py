@@ -26,6 +26,7 @@ HS_DEVERR_CAPACITY = 0x2
 HS_DEVERR_EMPTY = 0x4
 HS_DEVERR_TIMEOUT = 0x8
 HS_DEVERR_METADATA = 0x10
+HS_DEVERR_NO_LEAD = 0x20
 
 HS_K_APPEND, HS_K_SELECT, HS_K_ATTENTION, HS_K_COUNT = 0, 1, 2, 3
 
@@ -50,13 +51,14 @@ class HsConfig(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float), ("device", ctypes.c_int32),
                 ("fetch_mode", ctypes.c_int32), ("replacement", ctypes.c_int32),
                 ("replacement_seed", ctypes.c_uint32), ("write_allocate", ctypes.c_int32),
-                ("idx_heads", ctypes.c_int32)]
+                ("idx_heads", ctypes.c_int32), ("index_share", ctypes.c_int32),
+                ("share_prefetch", ctypes.c_int32)]
 
 
 class HsStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "hits", "misses", "h2d_bytes", "d2h_bytes", "decode_calls", "append_calls",
-        "host_bytes", "hot_bytes", "index_bytes", "meta_bytes")] + [
+        "host_bytes", "hot_bytes", "index_bytes", "meta_bytes", "full_selects")] + [
         ("device_error", ctypes.c_uint32), ("_pad", ctypes.c_uint32)]
 
     def as_dict(self) -> dict:
@@ -163,12 +165,13 @@ class HiSparseCache:
                  d_qk: int, d_v: int, d_idx: int, top_k: int, hot_slots: int, shared_kv: bool = False,
                  softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 2,
                  replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False,
-                 idx_heads: int = 1):
+                 idx_heads: int = 1, index_share: int = 1, share_prefetch: bool = True):
         if replacement not in REPLACEMENT:
             raise ValueError(f"replacement must be one of {sorted(REPLACEMENT)}")
         self.cfg = HsConfig(n_layers, max_requests, max_context, h_q, h_kv, d_qk, d_v, int(shared_kv),
                             d_idx, top_k, hot_slots, softmax_scale, device, fetch_mode,
-                            REPLACEMENT[replacement], replacement_seed, int(write_allocate), int(idx_heads))
+                            REPLACEMENT[replacement], replacement_seed, int(write_allocate), int(idx_heads),
+                            int(index_share), int(share_prefetch))
         # bytes of one request's indexer query (heads, then weights and padding)
         self.q_idx_row = d_idx if idx_heads <= 1 else idx_heads * d_idx + 16
         self._h = ctypes.c_void_p()
