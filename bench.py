@@ -218,7 +218,8 @@ def ncu_traffic(kernel: str, workload: str, latent: bool = False):
 # algorithmic traffic of one layer of all R requests (per kernel)
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_pulls: bool = False) -> dict:
+def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_pulls: bool = False,
+                      selects: bool = True) -> dict:
     """HBM and host-link bytes the method itself moves for one layer-step of all
     requests, per kernel.  n_ctx: context length of each request at this step;
     misses: rows pulled from host memory in this layer-step (all requests);
@@ -229,13 +230,16 @@ def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_
     selection, slot and page-table reads/writes (16 B per selected position), the
     stamp/reverse scan (8 B per slot), 12 B of metadata per miss, and the appended
     token (its row read from HBM and written to the host copy, its key).
-    attention: every selected row, its slot, the queries and the outputs."""
+    attention: every selected row, its slot, the queries and the outputs.
+    selects=False: a layer that reuses its group lead's selection (index sharing)
+    scans no index keys; its selection, slot and metadata bytes still move (the
+    lead's call writes them for it)."""
     k_eff = np.minimum(w.top_k, n_ctx)
     R = w.n_requests
     row = w.row_bytes
     hbm = {
         "append": 0.0,
-        "select": float((n_ctx * w.d_idx).sum()) + R * w.d_idx
+        "select": (float((n_ctx * w.d_idx).sum()) + R * w.d_idx if selects else 0.0)
         + float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12
         + R * (w.row_bytes + 2 * w.d_idx + 4),
         "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2,
@@ -403,7 +407,8 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     cache = HiSparseCache(n_layers=L, max_requests=R, max_context=w.max_context(T), h_q=w.h_q, h_kv=w.h_kv,
                           d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k, hot_slots=w.hot_slots,
                           shared_kv=w.shared_kv, device=dev_index, fetch_mode=args.fetch_mode,
-                          replacement=args.replacement)
+                          replacement=args.replacement, index_share=args.index_share,
+                          share_prefetch=bool(args.share_prefetch))
 
     # ---- prefill: generate each (request, layer) context and append it -----------
     t_pre = time.time()
@@ -563,10 +568,11 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         m_ls = n_miss / (K * L)
         rp = resolve_pulls(args.fetch_mode, w.shared_kv)
         for t in range(t_begin, t_begin + K):
-            ab = algorithmic_bytes(w, n0 + t + 1, m_ls, rp)
-            for k in KERNEL_FILES:
-                hb[k] += ab["hbm"][k] * L
-                lb[k] += ab["link"][k] * L
+            for l in range(L):
+                ab = algorithmic_bytes(w, n0 + t + 1, m_ls, rp, selects=l % max(1, args.index_share) == 0)
+                for k in KERNEL_FILES:
+                    hb[k] += ab["hbm"][k]
+                    lb[k] += ab["link"][k]
         return hb, lb
 
     hb_a, lb_a = region_bytes(W, misses)
@@ -634,7 +640,9 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                    "timed": "one CUDA graph of the timed steps, uploaded beforehand, replayed once"
                    if uploaded and uploaded[0] else "one CUDA graph of the timed steps, replayed once (not "
                    "uploaded beforehand: this torch does not expose the executable graph)",
-                   "fetch_mode": args.fetch_mode, "replacement": args.replacement},
+                   "fetch_mode": args.fetch_mode, "replacement": args.replacement,
+                   **({"index_share": args.index_share, "share_prefetch": args.share_prefetch}
+                      if args.index_share > 1 else {})},
         "kernel_timing": {"mode": timing_mode, "steps": K, "ms_per_step": round(ms_total_b / K, 4),
                           "miss_rate": round(misses_b / max(1, hits_b + misses_b), 5),
                           "note": "the K steps after the headline's, each kernel bracketed by CUDA events "
@@ -684,6 +692,12 @@ def main():
                          "2 chosen per request (default)")
     ap.add_argument("--replacement", default="lru", choices=["lru", "fifo", "random"],
                     help="hot-cache replacement: lru (the method's), fifo or random (its comparison policies)")
+    ap.add_argument("--index-share", type=int, default=1,
+                    help="layers per indexer group: > 1 reuses the group lead's selection in the following "
+                         "layers (a variant; the workloads select per layer)")
+    ap.add_argument("--share-prefetch", type=int, default=1,
+                    help="with --index-share > 1: 1 = the lead's call resolves and pulls the followers ahead, "
+                         "0 = each follower resolves at its own call")
     ap.add_argument("--policy-floor", type=int, default=1,
                     help="1: also report the policy's misses against Belady's MIN on a cold 2-request trace "
                          "(untimed, after the measurement); 0: skip")

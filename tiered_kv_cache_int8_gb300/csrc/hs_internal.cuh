@@ -381,12 +381,15 @@ __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// Spins until *p >= target (acquire); gives up after WAIT_LIMIT_NS and returns false.
+// Spins until *p >= target (acquire), backing off from 32 ns to 512 ns between
+// polls (many CTAs may poll one flag); gives up after WAIT_LIMIT_NS and returns false.
 __device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int target) {
   if (ld_acquire(p) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
+  unsigned ns = 32;
   for (uint32_t it = 1;; ++it) {
-    __nanosleep(64);
+    __nanosleep(ns);
+    if (ns < 512) ns <<= 1;
     if (ld_acquire(p) >= target) return true;
     if ((it & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
   }

@@ -80,9 +80,8 @@ constexpr int NT = SEL_THREADS;
 constexpr int NWARP = NT / 32;
 constexpr int FAST_MAX_N = 256 * 1024;   // one-pass top-k: contexts up to this many positions
 constexpr int WCAP = 256;                // threshold-digit keys a warp lists in the one-pass top-k
-constexpr int CAND_MAX_N_PER_K = 20;     // candidate listing only for contexts up to 20 k positions
+constexpr int CAND_MAX_N_PER_K = 128;    // candidate listing for contexts up to 128 k positions
 constexpr int CAND_REG = 8;              // listed candidates a resolver thread holds in registers
-constexpr int CAND_WORDS = 2048;         // candidate path: contexts up to 32 * CAND_WORDS positions
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 // Per-request tables of the launch (scorers) and the resolver's layout share the
@@ -91,7 +90,7 @@ struct SelLayout {
   // scorer tables
   size_t t_prefix, t_req, t_n, t_thr, t_total;
   // resolver
-  size_t hist, sel, slot, miss_i, victim, ord, rev, used, bitmap, lists, newrow, r_total;
+  size_t hist, sel, slot, miss_i, victim, ord, rev, used, bitmap, lists, wpre, newrow, r_total;
   bool rev_smem, fast;
   size_t total;
 };
@@ -129,12 +128,15 @@ __host__ __device__ inline SelLayout sel_layout(const Geometry& g) {
   off += align_up((size_t)g.row_bytes, 16) + align_up((size_t)g.d_idx, 16);
   const size_t base = off;
   // optional parts, in order of value: the one-pass top-k, then the reverse map
-  const size_t fast_bytes = (size_t)FAST_MAX_N / 8 + (size_t)WCAP * NWARP * 4;
+  // two position bitmaps, the per-warp lists and 16-bit per-word prefix counts
+  const size_t fast_bytes = (size_t)FAST_MAX_N / 4 + (size_t)WCAP * NWARP * 4 + (size_t)FAST_MAX_N / 32 * 4;
   L.fast = base + fast_bytes <= SMEM_LIMIT;
   L.bitmap = off;
-  if (L.fast) off += (size_t)FAST_MAX_N / 8;
+  if (L.fast) off += (size_t)FAST_MAX_N / 4;
   L.lists = off;
   if (L.fast) off += (size_t)WCAP * NWARP * 4;
+  L.wpre = off;
+  if (L.fast) off += (size_t)FAST_MAX_N / 32 * 4;
   L.rev = off;
   L.rev_smem = off + (size_t)B * 4 <= SMEM_LIMIT;
   if (L.rev_smem) off += (size_t)B * 4;
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // ======================= 1. top-k, ascending =======================
     // The previous call's threshold listed between k and min(2k, 4096) keys: the k
     // largest (ties included) are all in the list, held in registers here.
-    const bool use_cand = sh.ok && N > K && L.fast && (N + 31) / 32 <= CAND_WORDS && sh.thr != 0u &&
+    const bool use_cand = sh.ok && N > K && L.fast && N <= FAST_MAX_N && sh.thr != 0u &&
                           sh.cnt >= K && sh.cnt <= min(2 * K, CAND_REG * NT);
     bool slots_known = false;   // the candidate path reads each selected position's page entry itself
     // the next call lists keys at or above the exact key of rank 1.5 k (found after
@@ -539,9 +541,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const int32_t* page_rl = p.s.page + rl * g.max_context;
       const int NWd = (N + 31) >> 5;
       uint32_t* gtw = bitmap;                         // [NWd] positions whose key is above the k-th
-      uint32_t* tiw = bitmap + CAND_WORDS;            // [NWd] positions whose key equals it
-      int* gpre = reinterpret_cast<int*>(lists);      // [NWd] above-threshold positions before each word
-      int* epre = gpre + CAND_WORDS;                  // [NWd] ties before each word
+      uint32_t* tiw = bitmap + FAST_MAX_N / 32;       // [NWd] positions whose key equals it
+      uint16_t* gpre = reinterpret_cast<uint16_t*>(smem_raw + L.wpre);   // [NWd] above-threshold positions before each word
+      uint16_t* epre = gpre + FAST_MAX_N / 32;                           // [NWd] ties before each word (all < 2^16)
       uint2 cv[CAND_REG];
       int cpg[CAND_REG];
 #pragma unroll
@@ -592,28 +594,22 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           else if (cv[j].y == vstar) atomicOr(&tiw[pp >> 5], 1u << (pp & 31));
         }
       __syncthreads();
-      // per-word prefix counts of the taken-above and tie positions
-      constexpr int WPT = CAND_WORDS / NT;
+      // per-word prefix counts of the taken-above and tie positions (each thread a
+      // contiguous range of words)
+      const int WPT = (NWd + NT - 1) / NT;
+      const int w0 = min(NWd, tid * WPT), w1 = min(NWd, w0 + WPT);
       int ng = 0, ne = 0;
-#pragma unroll
-      for (int k = 0; k < WPT; ++k) {
-        const int w = tid * WPT + k;
-        if (w < NWd) {
-          ng += __popc(gtw[w]);
-          ne += __popc(tiw[w]);
-        }
+      for (int w = w0; w < w1; ++w) {
+        ng += __popc(gtw[w]);
+        ne += __popc(tiw[w]);
       }
       const int2 ex = block_exclusive_scan2<NT>(ng, ne, sh.scan, nullptr, nullptr);
       int rg = ex.x, re = ex.y;
-#pragma unroll
-      for (int k = 0; k < WPT; ++k) {
-        const int w = tid * WPT + k;
-        if (w < NWd) {
-          gpre[w] = rg;
-          epre[w] = re;
-          rg += __popc(gtw[w]);
-          re += __popc(tiw[w]);
-        }
+      for (int w = w0; w < w1; ++w) {
+        gpre[w] = (uint16_t)rg;
+        epre[w] = (uint16_t)re;
+        rg += __popc(gtw[w]);
+        re += __popc(tiw[w]);
       }
       __syncthreads();
       HS_TRACE_IF(p, 1, 3, tid == 0 && ri == (int)blockIdx.x);
