@@ -9,6 +9,9 @@ from .hisparse_oracle import (  # noqa: F401
     indexer_scores_many,
     indexer_scores_multihead,
     topk_select,
+    page_bounds,
+    page_scores,
+    page_select,
     LRUHotCache,
     FIFOHotCache,
     RandomHotCache,

@@ -118,6 +118,50 @@ def topk_select(scores: np.ndarray, k: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Quest-style page-granular selection (the HiSparse summary reports its results for
+# Qwen3 with Quest page selection as well as for token-level top-k).  Quest is
+# named there without its formulas; the reading here: positions are grouped into
+# pages of P; a page keeps the element-wise minimum and maximum of its index
+# keys; its score is the upper bound of q . k over the page that those give; the
+# k // P best pages are selected (ties to the lower page) and every position of
+# them is attended.
+# ---------------------------------------------------------------------------
+
+
+def page_bounds(idx_keys: np.ndarray, page_size: int):
+    """Element-wise (min, max) of each page's index keys: two int8 [n_pages, d_idx]."""
+    k = np.asarray(idx_keys, dtype=np.int8)
+    n = k.shape[0]
+    n_pages = (n + page_size - 1) // page_size
+    kmin = np.empty((n_pages, k.shape[1]), np.int8)
+    kmax = np.empty((n_pages, k.shape[1]), np.int8)
+    for j in range(n_pages):
+        blk = k[j * page_size:min(n, (j + 1) * page_size)]
+        kmin[j] = blk.min(axis=0)
+        kmax[j] = blk.max(axis=0)
+    return kmin, kmax
+
+
+def page_scores(kmin: np.ndarray, kmax: np.ndarray, q_idx: np.ndarray) -> np.ndarray:
+    """U[j] = sum_d max(q_d * kmin[j, d], q_d * kmax[j, d]): the largest q . k any
+    key within the page's per-dimension bounds can reach (exact int64)."""
+    q = np.asarray(q_idx, dtype=np.int8).astype(np.int64)
+    lo = np.asarray(kmin, dtype=np.int8).astype(np.int64) * q
+    hi = np.asarray(kmax, dtype=np.int8).astype(np.int64) * q
+    return np.maximum(lo, hi).sum(axis=1)
+
+
+def page_select(idx_keys: np.ndarray, q_idx: np.ndarray, page_size: int, k: int):
+    """(pages, positions): the k // page_size pages with the largest bound (ties to
+    the lower page), ascending, and all their positions below N, ascending."""
+    kmin, kmax = page_bounds(idx_keys, page_size)
+    pages = topk_select(page_scores(kmin, kmax, q_idx), k // page_size)
+    n = np.asarray(idx_keys).shape[0]
+    pos = [p for j in pages for p in range(int(j) * page_size, min(n, (int(j) + 1) * page_size))]
+    return pages, np.asarray(pos, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
 # a3/a4: the hot cache with LRU replacement (HiSparse summary: fixed B slots per
 # request per layer, page table + LRU metadata; study notes "方法" item 1: LRU).
 # ---------------------------------------------------------------------------
