@@ -219,7 +219,7 @@ def ncu_traffic(kernel: str, workload: str, latent: bool = False):
 # ---------------------------------------------------------------------------
 
 def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_pulls: bool = False,
-                      selects: bool = True) -> dict:
+                      selects: bool = True, page_size: int = 1) -> dict:
     """HBM and host-link bytes the method itself moves for one layer-step of all
     requests, per kernel.  n_ctx: context length of each request at this step;
     misses: rows pulled from host memory in this layer-step (all requests);
@@ -233,15 +233,20 @@ def algorithmic_bytes(w: wl.Workload, n_ctx: np.ndarray, misses: float, resolve_
     attention: every selected row, its slot, the queries and the outputs.
     selects=False: a layer that reuses its group lead's selection (index sharing)
     scans no index keys; its selection, slot and metadata bytes still move (the
-    lead's call writes them for it)."""
+    lead's call writes them for it).
+    page_size P > 1 (page selection): the scan reads each page's bounds (2 d_idx
+    bytes per page) instead of every key, slot metadata is per page slot (B / P),
+    and the appended token also updates its page's bounds; misses count rows."""
     k_eff = np.minimum(w.top_k, n_ctx)
     R = w.n_requests
     row = w.row_bytes
+    P = max(1, int(page_size))
+    scan = (n_ctx * w.d_idx).sum() if P == 1 else (((n_ctx + P - 1) // P) * 2 * w.d_idx).sum()
     hbm = {
         "append": 0.0,
-        "select": (float((n_ctx * w.d_idx).sum()) + R * w.d_idx if selects else 0.0)
-        + float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * w.hot_slots * 8 + misses * 12
-        + R * (w.row_bytes + 2 * w.d_idx + 4),
+        "select": (float(scan) + R * w.d_idx if selects else 0.0)
+        + float(k_eff.sum()) * (4 + 4 + 4 + 4) + R * (w.hot_slots // P) * 8 + misses / P * 12
+        + R * (w.row_bytes + 2 * w.d_idx + 4) + (R * 4 * w.d_idx if P > 1 else 0),
         "attention": float(k_eff.sum()) * (row + 4) + R * w.h_q * (w.d_qk + w.d_v) * 2,
     }
     link = {"append": 0.0, "select": R * row, "attention": 0.0}
@@ -408,7 +413,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                           d_qk=w.d_qk, d_v=w.d_v, d_idx=w.d_idx, top_k=w.top_k, hot_slots=w.hot_slots,
                           shared_kv=w.shared_kv, device=dev_index, fetch_mode=args.fetch_mode,
                           replacement=args.replacement, index_share=args.index_share,
-                          share_prefetch=bool(args.share_prefetch))
+                          share_prefetch=bool(args.share_prefetch), page_size=args.page_size)
 
     # ---- prefill: generate each (request, layer) context and append it -----------
     t_pre = time.time()
@@ -565,11 +570,12 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
     def region_bytes(t_begin, n_miss):
         hb = {k: 0.0 for k in KERNEL_FILES}
         lb = {k: 0.0 for k in KERNEL_FILES}
-        m_ls = n_miss / (K * L)
+        m_ls = n_miss * max(1, args.page_size) / (K * L)   # rows (page mode: a missed page is P rows)
         rp = resolve_pulls(args.fetch_mode, w.shared_kv)
         for t in range(t_begin, t_begin + K):
             for l in range(L):
-                ab = algorithmic_bytes(w, n0 + t + 1, m_ls, rp, selects=l % max(1, args.index_share) == 0)
+                ab = algorithmic_bytes(w, n0 + t + 1, m_ls, rp, selects=l % max(1, args.index_share) == 0,
+                                       page_size=args.page_size)
                 for k in KERNEL_FILES:
                     hb[k] += ab["hbm"][k]
                     lb[k] += ab["link"][k]
@@ -642,7 +648,8 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
                    "uploaded beforehand: this torch does not expose the executable graph)",
                    "fetch_mode": args.fetch_mode, "replacement": args.replacement,
                    **({"index_share": args.index_share, "share_prefetch": args.share_prefetch}
-                      if args.index_share > 1 else {})},
+                      if args.index_share > 1 else {}),
+                   **({"page_size": args.page_size} if args.page_size > 1 else {})},
         "kernel_timing": {"mode": timing_mode, "steps": K, "ms_per_step": round(ms_total_b / K, 4),
                           "miss_rate": round(misses_b / max(1, hits_b + misses_b), 5),
                           "note": "the K steps after the headline's, each kernel bracketed by CUDA events "
@@ -669,7 +676,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         "device_error": dev_err,
     }
     cache.close()
-    if args.policy_floor and rank == 0:
+    if args.policy_floor and args.page_size <= 1 and rank == 0:   # the floor is token-level
         try:   # a report beside the measurement: it must never cost the bench line
             out["policy_floor"] = policy_floor(args, w, dev_index)
         except Exception as e:   # noqa: BLE001
@@ -698,6 +705,8 @@ def main():
     ap.add_argument("--share-prefetch", type=int, default=1,
                     help="with --index-share > 1: 1 = the lead's call resolves and pulls the followers ahead, "
                          "0 = each follower resolves at its own call")
+    ap.add_argument("--page-size", type=int, default=1,
+                    help="Quest-style page selection: pages of this many positions (1 = token-level top-k)")
     ap.add_argument("--policy-floor", type=int, default=1,
                     help="1: also report the policy's misses against Belady's MIN on a cold 2-request trace "
                          "(untimed, after the measurement); 0: skip")

@@ -150,6 +150,24 @@ typedef struct hs_config {
                                  right away, so a follower's call only appends its token and attends
                                  (the prefetch that a shared selection makes exact); 0 = each
                                  follower resolves and pulls at its own call. */
+  int32_t page_size;          /* 0 or 1: positions are selected and cached one by one.  P in
+                                 {2, 4, 8, 16, 32, 64}: Quest-style page selection (GQA rows only).
+                                 Positions form pages of P (page j = positions jP .. jP+P-1); each
+                                 page keeps the element-wise maximum and minimum of its index keys
+                                 (the page-bound store, [max_requests][n_layers][ceil(max_context/P)]
+                                 [2 * d_idx] int8: maxima then minima, kept current by hs_append and
+                                 by the appending decode call); a page scores
+                                 U = sum_d max(q_d * kmax_d, q_d * kmin_d), the largest q . k any key
+                                 within those bounds reaches (exact int32); the top_k / P pages with
+                                 the largest U (ties: the lower page) are selected and every position
+                                 of them below the length is attended (the selection output lists
+                                 those positions ascending, then -1).  The hot cache then holds
+                                 hot_slots / P page slots of P consecutive rows, and the page table,
+                                 reverse map, stamps, LRU order and the hit / miss counters are per
+                                 page and page slot (hs_snapshot: page[j] = page slot of page j;
+                                 reverse, stamp and order: their first hot_slots / P entries).
+                                 Requires top_k % P == 0, hot_slots % (4 P) == 0, d_idx 64 or 128,
+                                 idx_heads <= 1, index_share <= 1 and write_allocate = 0. */
 } hs_config_t;
 
 #define HS_REPLACE_LRU 0
@@ -159,15 +177,15 @@ typedef struct hs_config {
 typedef struct hs_handle hs_handle_t;
 
 typedef struct hs_stats {
-  uint64_t hits;          /* selected positions found in the hot cache, all calls */
-  uint64_t misses;        /* selected positions pulled from host memory */
+  uint64_t hits;          /* selected positions (pages, with page_size > 1) found in the hot cache */
+  uint64_t misses;        /* selected positions (pages) pulled from host memory */
   uint64_t h2d_bytes;     /* bytes pulled host -> HBM by RESOLVE */
   uint64_t d2h_bytes;     /* K/V bytes written to the host copy by appends */
   uint64_t decode_calls;  /* hs_decode_layer calls enqueued */
   uint64_t append_calls;  /* hs_append calls enqueued */
   uint64_t host_bytes;    /* size of the pinned host K/V store */
   uint64_t hot_bytes;     /* size of the HBM hot cache */
-  uint64_t index_bytes;   /* size of the HBM index-key store */
+  uint64_t index_bytes;   /* size of the HBM index-key store (with the page-bound store) */
   uint64_t meta_bytes;    /* page table, reverse map, stamps, LRU order, counters */
   uint64_t full_selects;  /* selections that scanned every key (no usable candidate list:
                              first steps, a large drift, contexts above 20 k positions) */
@@ -212,7 +230,11 @@ void hs_destroy(hs_handle_t* h);
  * For request r with current length L the tokens take positions L..L+n_tok-1:
  * their index keys go to the HBM key store, their K/V rows to the pinned host
  * copy (not to the hot cache: a new token enters the cache only when a later
- * step selects it), and the length becomes L+n_tok.  A request whose append
+ * step selects it), and the length becomes L+n_tok.  With page_size P > 1 the
+ * bounds of every page the tokens touch are recomputed from the key store, and
+ * a token whose page is resident in the hot cache also has its row written into
+ * that page's slot (a page can be cached before all of its positions exist).
+ * A request whose append
  * would pass max_context is skipped whole (HS_DEVERR_CAPACITY).
  * n_req = 0 or n_tok = 0 is a no-op.  HS_ERR_INVALID for layer out of range,
  * n_req > max_requests, n_tok > max_context or a null buffer.

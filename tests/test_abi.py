@@ -56,6 +56,14 @@ def cfg(**over):
     dict(softmax_scale=-1.0),
     dict(fetch_mode=3),
     dict(replacement=3),             # none of LRU, FIFO, random
+    dict(page_size=3),               # pages: a power of two up to 64
+    dict(page_size=128),
+    dict(page_size=16, top_k=264, hot_slots=512),   # k not a whole number of pages
+    dict(page_size=16, hot_slots=528),              # page slots not a multiple of 4
+    dict(page_size=16, d_idx=32),                   # bounds rows of 64 or 128 keys only
+    dict(page_size=16, idx_heads=4),
+    dict(page_size=16, write_allocate=1),
+    dict(page_size=16, shared_kv=1, h_kv=1, h_q=16, d_qk=576, d_v=512),
 ])
 def test_unsupported_configs_are_rejected_before_touching_the_gpu(L, over):
     from tiered_kv_cache_int8_gb300 import hs

@@ -53,6 +53,16 @@ std::string check_config(const hs_config_t& c) {
     return "the multi-head indexer (idx_heads > 1) needs d_idx 64 or 128";
   if (c.write_allocate && c.top_k >= c.hot_slots)
     return "write_allocate needs top_k < hot_slots (the appended token needs a slot of its own)";
+  if (c.page_size < 0 || c.page_size > 64 || (c.page_size > 1 && (c.page_size & (c.page_size - 1))))
+    return "page_size must be 0, 1, 2, 4, 8, 16, 32 or 64";
+  if (c.page_size > 1) {
+    if (c.shared_kv) return "page_size > 1 is supported for GQA rows";
+    if (c.d_idx != 64 && c.d_idx != 128) return "page_size > 1 needs d_idx 64 or 128";
+    if (c.idx_heads > 1 || c.index_share > 1 || c.write_allocate)
+      return "page_size > 1 excludes idx_heads > 1, index_share > 1 and write_allocate";
+    if (c.top_k % c.page_size != 0) return "page_size > 1 needs top_k % page_size == 0";
+    if (c.hot_slots % (4 * c.page_size) != 0) return "page_size > 1 needs hot_slots % (4 * page_size) == 0";
+  }
   if (c.shared_kv == 0) {
     if (c.d_qk != 128 || c.d_v != 128) return "GQA rows: d_qk = d_v = 128 required";
     if (!is_pow2_in(c.h_kv, 1, 8)) return "GQA rows: h_kv must be one of 1, 2, 4, 8";
@@ -210,6 +220,10 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   g.row_bytes = 2 * g.row_elems;
   g.v_off = cfg->shared_kv ? 0 : cfg->h_kv * cfg->d_qk;
   g.idx_heads = cfg->idx_heads > 1 ? cfg->idx_heads : 1;
+  g.page_size = cfg->page_size > 1 ? cfg->page_size : 1;
+  g.page_shift = 0;
+  while ((1 << g.page_shift) < g.page_size) ++g.page_shift;
+  g.max_pages = (cfg->max_context + g.page_size - 1) / g.page_size;
   const float scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / std::sqrt((float)cfg->d_qk);
   h->scale_log2 = scale * 1.4426950408889634f;
 
@@ -250,6 +264,8 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   h->host_bytes = R * Lr * N * (size_t)g.row_bytes;
   h->hot_bytes = R * Lr * B * (size_t)g.row_bytes;
   h->index_bytes = R * Lr * N * (size_t)g.d_idx;
+  const size_t pbound_bytes = g.page_size > 1 ? R * Lr * (size_t)g.max_pages * 2 * g.d_idx : 16;
+  if (g.page_size > 1) h->index_bytes += pbound_bytes;
 
   FaultInject fi;
   h->fault = fi.noready ? 1 : 0;
@@ -298,7 +314,8 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   };
   const A allocs[] = {
       {(void**)&s.hot, h->hot_bytes, false},
-      {(void**)&s.idx_keys, h->index_bytes, false},
+      {(void**)&s.idx_keys, R * Lr * N * (size_t)g.d_idx, false},
+      {(void**)&s.pbound, pbound_bytes, false},
       {(void**)&s.page, R * Lr * N * 4, true},
       {(void**)&s.reverse, R * Lr * B * 4, true},
       {(void**)&s.stamp, R * Lr * B * 4, true},
@@ -423,7 +440,11 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
   p.kv_rows = static_cast<const uint16_t*>(kv_rows);
   p.keys = idx_keys;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = timed_launch(h, HS_K_APPEND, st, [&] { return hs::launch_append(p, st); });
+  cudaError_t e = timed_launch(h, HS_K_APPEND, st, [&] {
+    cudaError_t r = hs::launch_append(p, st);
+    if (r == cudaSuccess && p.g.page_shift > 0) r = hs::launch_page_bounds(p, st);   // bounds of the touched pages
+    return r;
+  });
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_append: launch");
   ++h->append_calls;
   return HS_OK;

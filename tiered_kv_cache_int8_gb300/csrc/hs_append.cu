@@ -47,6 +47,20 @@ __global__ void __launch_bounds__(APP_THREADS) append_kernel(AppendParams p) {
       for (int u = 0; u < 4; ++u)
         if (e + u * APP_THREADS < total) rdst[e + u * APP_THREADS] = v[u];
     }
+    // page mode: a page can be resident before all of its positions exist; the
+    // rows appended to a resident page go to its slot as well (write-through)
+    if (g.page_shift > 0) {
+      const int psh = g.page_shift;
+      const int32_t* ptab = p.s.page + rl * g.max_context;
+      unsigned char* hot = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
+      for (int i = 0; i < nt; ++i) {
+        const int pos = len + t0 + i;
+        const int ps = ptab[pos >> psh];
+        if (ps < 0 || ps >= (g.hot_slots >> psh)) continue;
+        int4* hdst = reinterpret_cast<int4*>(hot + (size_t)((ps << psh) + (pos & ((1 << psh) - 1))) * g.row_bytes);
+        for (int e = threadIdx.x; e < rvec; e += APP_THREADS) hdst[e] = rsrc[i * rvec + e];
+      }
+    }
   }
 
   if (gridDim.x == 1) {   // one CTA per request (decode-time appends): no arrival counter
@@ -79,6 +93,41 @@ __global__ void __launch_bounds__(APP_THREADS) append_kernel(AppendParams p) {
   }
 }
 
+// Page mode: the element-wise maximum and minimum of the index keys of every page
+// an append touched, recomputed whole from the key store: pages
+// (len - n_tok) / P .. (len - 1) / P of the length after the append (the same
+// pages again when the append was rejected, which rewrites the same values).
+// grid (x, n_req); block APP_THREADS; one thread per 16-byte column chunk of a page
+__global__ void __launch_bounds__(APP_THREADS) page_bound_kernel(AppendParams p) {
+  const Geometry& g = p.g;
+  const int ri = blockIdx.y;
+  const int req = p.req_ids ? p.req_ids[ri] : ri;
+  if (req < 0 || req >= g.max_requests) return;
+  const long long rl = (long long)req * g.n_layers + p.layer;
+  const int len = p.s.length[rl];
+  if (len <= 0) return;
+  const int psh = g.page_shift, P = 1 << psh;
+  const int lo = max(0, len - p.n_tok) >> psh, hi = (len - 1) >> psh;
+  const int hc = g.d_idx / 16;
+  const int total = (hi - lo + 1) * hc;
+  const int8_t* keys = p.s.idx_keys + rl * g.max_context * g.d_idx;
+  int8_t* bound = p.s.pbound + rl * (long long)g.max_pages * 2 * g.d_idx;
+  for (int e = blockIdx.x * APP_THREADS + threadIdx.x; e < total; e += gridDim.x * APP_THREADS) {
+    const int pg = lo + e / hc, c = e % hc;
+    const int r0 = pg << psh, r1 = min(len, r0 + P);
+    int4 mx = *reinterpret_cast<const int4*>(keys + (long long)r0 * g.d_idx + c * 16);
+    int4 mn = mx;
+    for (int r = r0 + 1; r < r1; ++r) {
+      const int4 v = *reinterpret_cast<const int4*>(keys + (long long)r * g.d_idx + c * 16);
+      mx = vmax16(mx, v);
+      mn = vmin16(mn, v);
+    }
+    int4* dst = reinterpret_cast<int4*>(bound + (long long)pg * 2 * g.d_idx);
+    dst[c] = mx;
+    dst[hc + c] = mn;
+  }
+}
+
 __global__ void init_order_kernel(int32_t* order, long long n_lists, int B) {
   const long long total = n_lists * B;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -89,6 +138,14 @@ __global__ void init_order_kernel(int32_t* order, long long n_lists, int B) {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st) {
   dim3 grid((p.n_tok + APP_TOKENS_PER_CTA - 1) / APP_TOKENS_PER_CTA, p.n_req);
   append_kernel<<<grid, APP_THREADS, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_page_bounds(const AppendParams& p, cudaStream_t st) {
+  const int pages = (p.n_tok >> p.g.page_shift) + 2;   // the most pages an append of n_tok touches
+  const int work = pages * (p.g.d_idx / 16);
+  dim3 grid(std::min((work + APP_THREADS - 1) / APP_THREADS, 1024), p.n_req);
+  page_bound_kernel<<<grid, APP_THREADS, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -242,10 +242,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     int s = 0;
     long long it = 0;
     bool dead = false;
+    unsigned long long tw_ready = 0, tw_empty = 0;   // summed waits (trace builds only)
+    int n_items = 0;
     auto take_stage = [&]() -> bool {   // wait until stage s may be refilled
       if (it < nstage) return true;
-      return __all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
-                                                 p.s.dev_error, 4 * WAIT_LIMIT_NS));
+      const unsigned long long t0 = HS_TNOW();
+      const bool ok = __all_sync(FULL_MASK, wait_or_abort(&empty[s], (uint32_t)(((it / nstage) + 1) & 1), abort_flag,
+                                                          p.s.dev_error, 4 * WAIT_LIMIT_NS));
+      tw_empty += HS_TNOW() - t0;
+      return ok;
     };
     // a chunk's metadata: k_eff (the request's ready flag holds k_eff + 1), the
     // request id, the slots and positions of its rows (one batch of loads)
@@ -281,10 +286,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         mt = pf;
       } else {   // wait for the request's publication
         unsigned v = 0;
+        const unsigned long long t0 = HS_TNOW();
         if (lane == 0) {
           v = wait_counter(p.s.ready + r, 1u) ? ld_acquire(p.s.ready + r) : 0u;
           if (v == 0u) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
         }
+        tw_ready += HS_TNOW() - t0;
         v = __shfl_sync(FULL_MASK, v, 0);
         mt.kk = v ? (int)v - 1 : 0;
         load_rows(mt, r, c);
@@ -392,6 +399,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
       cur = (long long)__shfl_sync(FULL_MASK, nxt, 0);
       if (lane == 0 && cur < total) nxt = atomicAdd(&p.s.sync[2], 1u);
+      ++n_items;
     }
     // no more work: tell the fetcher and the consumers
     if (!dead && take_stage() && lane == 0) {
@@ -401,10 +409,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     }
     __syncwarp();
     HS_TRACE_IF(p, 2, 3, lane == 0);
+    if (lane == 0) {
+      HS_TRACE_VAL(p, 2, 10, tw_ready);
+      HS_TRACE_VAL(p, 2, 11, tw_empty);
+      HS_TRACE_VAL(p, 2, 12, (unsigned long long)n_items);
+    }
   } else if (warp == FETCHER) {
     // ============================ fetcher warp ============================
     // Missed rows of each unit, from the mapped host copy straight into their
     // stage rows; the stage's full barrier completes when these copies land.
+    unsigned long long n_fetched = 0;
     for (long long it = 0;; ++it) {
       const int s = (int)(it % nstage);
       if (!__all_sync(FULL_MASK, wait_or_abort(&dready[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
@@ -428,12 +442,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         const unsigned char* src = host + (size_t)ps * g.row_bytes;
         unsigned char* dst = st_s + (size_t)i * row_stride;
         for (int v = lane; v < rvec; v += 32) cp_async_16(dst + v * 16, src + v * 16);
+        ++n_fetched;
       }
       cp_async_mbar_arrive(&full[s]);   // balanced: completes when this lane's copies land
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
     }
     cp_async_wait_all();
+    if (lane == 0) HS_TRACE_VAL(p, 2, 14, n_fetched);
   } else {
     // ============================ consumer warps ============================
     const int kvh = warp % HKV;
@@ -445,10 +461,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
     int q_r = -1;
 
+    unsigned long long tw_full = 0;   // summed waits (trace builds only)
     for (long long it = 0;; ++it) {
       const int s = (int)(it % nstage);
+      const unsigned long long t0 = HS_TNOW();
       const bool ok = wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
                                     4 * WAIT_LIMIT_NS);
+      tw_full += HS_TNOW() - t0;
       if (named_sync_or(BAR_VOTE, NCONS * 32, !ok)) break;   // the consumers leave together
       const Desc dsc = desc[s];
       if (dsc.type == DESC_STOP) break;
@@ -593,6 +612,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
     }
     HS_TRACE_IF(p, 2, 5, tid == 0);
+    if (tid == 0) HS_TRACE_VAL(p, 2, 13, tw_full);
   }
 
   __syncthreads();

@@ -49,12 +49,16 @@ struct Geometry {
   int h_q, h_kv, d_qk, d_v, shared_kv, d_idx, top_k, hot_slots;
   int row_elems, row_bytes, v_off;
   int idx_heads;           // 1: one indexer query (signed score); 2/4/8: the multi-head ReLU-weighted indexer
+  int page_size;           // 1: positions are selected and cached one by one; P > 1: pages of P positions
+  int page_shift;          // log2(page_size)
+  int max_pages;           // pages per (request, layer): ceil(max_context / page_size)
 };
 
 struct DeviceState {
   uint16_t* host_kv;       // device alias of the pinned host store [R][L][Nmax][row]
   uint16_t* hot;           // [R][L][B][row]
   int8_t* idx_keys;        // [R][L][Nmax][d_idx]
+  int8_t* pbound;          // [R][L][max_pages][2 * d_idx] page mode: per page [max | min] of its keys
   int32_t* page;           // [R][L][Nmax]
   int32_t* reverse;        // [R][L][B]
   int32_t* stamp;          // [R][L][B]
@@ -173,6 +177,7 @@ namespace hs {
 
 // launchers (one per kernel translation unit); return a CUDA error code
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+cudaError_t launch_page_bounds(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_follow(const DecodeParams& p, cudaStream_t st);
@@ -272,10 +277,24 @@ constexpr int TRACE_KERNELS = 3, TRACE_CTAS = 1024, TRACE_POINTS = 64;
       (p).trace[(size_t)TRACE_KERNELS * TRACE_CTAS * TRACE_POINTS + i_] = global_timer_ns();     \
     }                                                                                             \
   } while (0)
+// a measured quantity (a summed wait in ns, a count) in place of a timestamp
+#define HS_TRACE_VAL(p, k, pt, val)                                                               \
+  do {                                                                                            \
+    if ((p).trace && blockIdx.x < TRACE_CTAS) {                                                   \
+      const size_t i_ = ((size_t)(k) * TRACE_CTAS + blockIdx.x) * TRACE_POINTS + (pt);            \
+      (p).trace[i_] = 0;                                                                          \
+      (p).trace[(size_t)TRACE_KERNELS * TRACE_CTAS * TRACE_POINTS + i_] = (val);                 \
+    }                                                                                             \
+  } while (0)
+#define HS_TNOW() global_timer_ns()
 #else
 #define HS_TRACE_IF(p, k, pt, cond) \
   do {                              \
   } while (0)
+#define HS_TRACE_VAL(p, k, pt, val) \
+  do {                              \
+  } while (0)
+#define HS_TNOW() 0ull
 #endif
 #define HS_TRACE(p, k, pt) HS_TRACE_IF(p, k, pt, threadIdx.x == 0)
 
@@ -362,6 +381,14 @@ __device__ __forceinline__ int4 ld_nc_v4(const void* p) {
 }
 
 __device__ __forceinline__ void set_error(unsigned int* word, unsigned int bit) { atomicOr(word, bit); }
+
+// byte-wise signed maximum / minimum of 16 int8 values (page key bounds)
+__device__ __forceinline__ int4 vmax16(int4 a, int4 b) {
+  return make_int4(__vmaxs4(a.x, b.x), __vmaxs4(a.y, b.y), __vmaxs4(a.z, b.z), __vmaxs4(a.w, b.w));
+}
+__device__ __forceinline__ int4 vmin16(int4 a, int4 b) {
+  return make_int4(__vmins4(a.x, b.x), __vmins4(a.y, b.y), __vmins4(a.z, b.z), __vmins4(a.w, b.w));
+}
 
 // GPU-scope release add / store and acquire load: the publication of one CTA's
 // writes to CTAs of the same or a concurrently running kernel.

@@ -227,14 +227,18 @@ size_t select_smem_bytes(const Geometry& g) { return sel_layout(g).total; }
 // ===========================================================================
 // the kernel
 // ===========================================================================
-template <int NCH, int NH>
+template <int NCH, int NH, bool PG>
 __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
   using SG = ScoreGeom<NCH, NH>;
   constexpr int d = NCH * 16;
   const Geometry& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = g.top_k;
-  const int B = g.hot_slots;
+  const int KR = g.top_k;       // rows attended per request at most (the stride of per-request rows)
+  const int BR = g.hot_slots;   // slot rows per (request, layer)
+  // page mode: units (what is scored, selected and cached) are pages of PS
+  // positions; otherwise PS = 1 and a unit is a position
+  constexpr bool paged = PG;
+  const int psh = PG ? g.page_shift : 0, PS = 1 << psh;
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const SelLayout L = sel_layout(g);
@@ -267,8 +271,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
           thr = p.s.cand_thr[rl];
         }
-        const bool scored = N > K && p.role == ROLE_SELECT;
-        nt = scored ? (N + SG::TILE - 1) / SG::TILE : 0;
+        const int NU = (N + PS - 1) >> psh;
+        const bool scored = NU > (KR >> psh) && p.role == ROLE_SELECT;
+        nt = scored ? (NU + SG::TILE - 1) / SG::TILE : 0;
         t_req[i] = scored ? req : -1;
         t_n[i] = N;
         t_thr[i] = (scored && NH == 1) ? thr : 0u;   // candidate listing: single-head keys only
@@ -293,7 +298,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     int4 q[NH][SG::CPL];
     int qw[NH];   // head weights (multi-head indexer)
     int q_r = -1;
-    const int qstride = NH > 1 ? NH * d + 16 : d;   // bytes of one request's indexer query
+    const int qstride = NH > 1 ? NH * d + 16 : g.d_idx;   // bytes of one request's indexer query
+    const int hc = g.d_idx / 16;   // page mode: a unit row is [key maxima | key minima], 2 * hc chunks
 
     // request of warp tile t, searching forward from request `from`
     auto req_of = [&](int t, int from) {
@@ -301,21 +307,40 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       while (t_prefix[x + 1] <= t) ++x;
       return x;
     };
-    // loads of sub-tile `half` of tile t (request ri) into v (zeros past N)
+    // loads of sub-tile `half` of tile t (request ri) into v (zeros past the last
+    // unit).  Unit rows: index keys, or in page mode the stored [max | min] bounds
+    // of each page; the unit holding this call's appended token combines its key
+    // (a page it opens has that key as both bounds).
     auto load_sub = [&](int t, int ri, int half, int4 (&v)[SG::LD]) {
       const int N = t_n[ri];
+      const int NU = (N + PS - 1) >> psh;
       const int pos0 = (t - t_prefix[ri]) * SG::TILE + half * SG::SUB;
       const long long rl = (long long)t_req[ri] * g.n_layers + p.layer;
-      const int8_t* base = p.s.idx_keys + rl * g.max_context * d;
-      const int newpos = p.new_kv ? N - 1 : -1;
-      const int8_t* nk = p.new_keys + (long long)ri * d;
+      const int8_t* base = paged ? p.s.pbound + rl * (long long)g.max_pages * d : p.s.idx_keys + rl * g.max_context * d;
+      const int newu = p.new_kv ? (N - 1) >> psh : -1;
+      const bool fresh = ((N - 1) & (PS - 1)) == 0;   // the appended token opens its page
+      const int8_t* nk = p.new_keys + (long long)ri * g.d_idx;
 #pragma unroll
       for (int u = 0; u < SG::LD; ++u) {
         const int pos = pos0 + (u / SG::CPL) * SG::PPI + pg;
         const int ch = cl * SG::CPL + (u % SG::CPL);
         v[u] = make_int4(0, 0, 0, 0);
-        if (pos < N) v[u] = pos == newpos ? *reinterpret_cast<const int4*>(nk + ch * 16)
-                                          : ld_stream(base + (long long)pos * d + ch * 16);
+        if (pos < NU) {
+          if (pos != newu) {
+            v[u] = ld_stream(base + (long long)pos * d + ch * 16);
+          } else if (!paged) {
+            v[u] = *reinterpret_cast<const int4*>(nk + ch * 16);
+          } else {
+            const bool hi = ch < hc;
+            const int4 kn = *reinterpret_cast<const int4*>(nk + (hi ? ch : ch - hc) * 16);
+            if (fresh) {
+              v[u] = kn;
+            } else {
+              const int4 old = ld_stream(base + (long long)pos * d + ch * 16);
+              v[u] = hi ? vmax16(old, kn) : vmin16(old, kn);
+            }
+          }
+        }
       }
     };
 
@@ -328,7 +353,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     }
     for (int t = w0; t < total; t += W) {
       const int ri = r_cur;
-      const int N = t_n[ri];
+      const int N = (t_n[ri] + PS - 1) >> psh;   // units of this request
       const int tile0 = (t - t_prefix[ri]) * SG::TILE;
       const uint32_t thr = t_thr[ri];
       if (ri != q_r) {
@@ -338,7 +363,17 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         for (int h = 0; h < NH; ++h) {
           const int4* qs = reinterpret_cast<const int4*>(qrow + h * d);
 #pragma unroll
-          for (int c = 0; c < SG::CPL; ++c) q[h][c] = qs[cl * SG::CPL + c];
+          for (int c = 0; c < SG::CPL; ++c) {
+            const int cc = cl * SG::CPL + c;
+            if (!paged) {
+              q[h][c] = qs[cc];
+            } else {
+              // [max(q, 0) | min(q, 0)] against [maxima | minima]: per dimension the
+              // larger of q * kmax and q * kmin
+              const int4 z = make_int4(0, 0, 0, 0);
+              q[h][c] = cc < hc ? vmax16(qs[cc], z) : vmin16(qs[cc - hc], z);
+            }
+          }
           qw[h] = NH > 1 ? max(0, (int)qrow[NH * d + h]) : 1;   // negative weights count as 0
         }
       }
@@ -412,14 +447,16 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
               if (lane == 0) base = atomicAdd(p.s.cand_cnt + ri, (unsigned)__popc(m));
               base = __shfl_sync(FULL_MASK, base, 0);
               const unsigned at = base + __popc(m & ((1u << lane) - 1u));
-              if (c && at < 2u * (unsigned)K)
-                p.s.cand[(long long)ri * 2 * K + at] = make_uint2((uint32_t)ownp[o], ownk[o]);
+              if (c && at < 2u * (unsigned)KR)
+                p.s.cand[(long long)ri * 2 * KR + at] = make_uint2((uint32_t)ownp[o], ownk[o]);
             }
           }
         }
       }
       __syncwarp();
       if (lane == 0) red_release_add(p.s.tiles_done + ri, 1u);
+      HS_TRACE_IF(p, 0, 3, tid == 0 && t == w0);
+      HS_TRACE_IF(p, 0, 4, tid == 0 && t == w0 + W);
       r_cur = rn;
     }
     HS_TRACE(p, 0, 2);
@@ -427,6 +464,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
   }
 
   // ======================= resolvers =======================
+  // in units: k selected, B slots (page mode: pages and page slots of PS rows)
+  const int K = KR >> psh, B = BR >> psh;
   uint32_t* h = reinterpret_cast<uint32_t*>(smem_raw + L.hist);
   int32_t* sel = reinterpret_cast<int32_t*>(smem_raw + L.sel);
   int32_t* slot_sel = reinterpret_cast<int32_t*>(smem_raw + L.slot);
@@ -443,12 +482,12 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
 
   for (int ri = (int)blockIdx.x; ri < p.n_req; ri += p.n_resolvers) {
     HS_TRACE_IF(p, 1, 0, tid == 0 && ri == (int)blockIdx.x);
-    int32_t* sel_out = p.sel_out ? p.sel_out + (long long)ri * K : nullptr;
+    int32_t* sel_out = p.sel_out ? p.sel_out + (long long)ri * KR : nullptr;
     const int req = p.req_ids ? p.req_ids[ri] : ri;
     if (req < 0 || req >= g.max_requests) {
       if (tid == 0) set_error(p.s.dev_error, HS_DEVERR_REQ_RANGE);
       if (sel_out)
-        for (int i = tid; i < K; i += NT) sel_out[i] = -1;
+        for (int i = tid; i < KR; i += NT) sel_out[i] = -1;
       if (p.publish) {
         __syncthreads();
         if (tid == 0) {
@@ -463,10 +502,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     for (int j = tid; j < B; j += NT) used[j] = 0;
 
     // ---- 0. every read that does not depend on the scores, issued together ----
-    const int32_t* order_g = p.s.order + rl * B;
+    const int32_t* order_g = p.s.order + rl * BR;
     for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(ord + 4 * c4, order_g + 4 * c4);
     if (L.rev_smem) {
-      const int32_t* rev_g = p.s.reverse + rl * B;
+      const int32_t* rev_g = p.s.reverse + rl * BR;
       for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(rev_s + 4 * c4, rev_g + 4 * c4);
     }
     if (p.new_kv) {
@@ -487,9 +526,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
       sh.N = N;
       sh.ok = 1;
+      const int NUt = (N + PS - 1) >> psh;
       if (N == 0) set_error(p.s.dev_error, HS_DEVERR_EMPTY);   // nothing to attend: the output is 0
       if (p.role == ROLE_GIVEN) {   // the lead of this step must have left a selection of this length
-        const bool armed = p.s.sh_armed[rl] != 0 && p.s.sh_kk[rl] == min(K, N);
+        const bool armed = p.s.sh_armed[rl] != 0 && p.s.sh_kk[rl] == min(K, NUt);
         p.s.sh_armed[rl] = 0;
         if (!armed) {
           set_error(p.s.dev_error, HS_DEVERR_NO_LEAD);
@@ -497,8 +537,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         }
       }
       sh.thr_next = 0u;
-      if (N > K && p.role == ROLE_SELECT) {   // wait until every tile of this request is scored
-        const unsigned ntile = (unsigned)((N + SG::TILE - 1) / SG::TILE);
+      if (NUt > K && p.role == ROLE_SELECT) {   // wait until every tile of this request is scored
+        const unsigned ntile = (unsigned)((NUt + SG::TILE - 1) / SG::TILE);
         if (!wait_counter(p.s.tiles_done + ri, ntile)) {
           set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
           sh.ok = 0;
@@ -513,8 +553,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     cp_async_wait_all();
     __syncthreads();
     HS_TRACE_IF(p, 1, 1, tid == 0 && ri == (int)blockIdx.x);
-    const int len = sh.len, N = sh.N, t_step = sh.t_step;
-    const bool appended = N > len;
+    const int len = sh.len, Np = sh.N, t_step = sh.t_step;   // Np positions with the appended token
+    const int N = (Np + PS - 1) >> psh;                        // units
+    const bool appended = Np > len;
     const int kk = sh.ok ? min(K, N) : 0;   // (a given selection has the same k_eff: same N)
 
     // ======================= 1. top-k, ascending =======================
@@ -531,13 +572,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       // scores incomplete: nothing selected (the output of this request is 0)
     } else if (p.role == ROLE_GIVEN) {
       // the selection this layer's group lead left for it (same step, same positions)
-      const int32_t* gsel = p.s.sh_sel + rl * K;
+      const int32_t* gsel = p.s.sh_sel + rl * KR;
       for (int i = tid; i < kk; i += NT) sel[i] = __ldcg(gsel + i);
     } else if (N <= K) {
       for (int i = tid; i < N; i += NT) sel[i] = i;
     } else if (use_cand) {
       const int cnt = sh.cnt;
-      const uint2* cl = p.s.cand + (long long)ri * 2 * K;
+      const uint2* cl = p.s.cand + (long long)ri * 2 * KR;
       const int32_t* page_rl = p.s.page + rl * g.max_context;
       const int NWd = (N + 31) >> 5;
       uint32_t* gtw = bitmap;                         // [NWd] positions whose key is above the k-th
@@ -560,10 +601,12 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         tiw[w] = 0u;
       }
       __syncthreads();
+      HS_TRACE_IF(p, 1, 10, tid == 0 && ri == (int)blockIdx.x);
 #pragma unroll
       for (int j = 0; j < CAND_REG; ++j)
         if (tid + j * NT < cnt) atomicAdd(&h[cv[j].y >> 12], 1u);
       __syncthreads();
+      HS_TRACE_IF(p, 1, 11, tid == 0 && ri == (int)blockIdx.x);
       select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
       if (cnt >= k_next) {
         select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
@@ -945,10 +988,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     }
     __syncthreads();
     HS_TRACE_IF(p, 1, 4, tid == 0 && ri == (int)blockIdx.x);
-    int32_t* sel_g = p.s.sel + (long long)ri * K;
-    for (int i = tid; i < K; i += NT) {
-      const int v = i < kk ? sel[i] : -1;
-      if (i < kk) sel_g[i] = v;
+    // rows attended: every position of the selected units below the length (only
+    // the last page can be partial; when selected it is the last selected unit)
+    const int kkr = !paged ? kk : (kk > 0 ? kk * PS - (sel[kk - 1] == N - 1 ? N * PS - Np : 0) : 0);
+    int32_t* sel_g = p.s.sel + (long long)ri * KR;
+    for (int i = tid; i < KR; i += NT) {
+      const int v = i < kkr ? (paged ? (sel[i >> psh] << psh) + (i & (PS - 1)) : sel[i]) : -1;
+      if (i < kkr) sel_g[i] = v;
       if (sel_out) sel_out[i] = v;
     }
 
@@ -964,10 +1010,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     if (pass > 0) {
       __syncthreads();   // the previous pass is done with the shared arrays
       for (int j = tid; j < B; j += NT) used[j] = 0;
-      const int32_t* order_f = p.s.order + rlx * B;
+      const int32_t* order_f = p.s.order + rlx * BR;
       for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(ord + 4 * c4, order_f + 4 * c4);
       if (L.rev_smem) {
-        const int32_t* rev_f = p.s.reverse + rlx * B;
+        const int32_t* rev_f = p.s.reverse + rlx * BR;
         for (int c4 = tid; c4 < B / 4; c4 += NT) cp_async_16(rev_s + 4 * c4, rev_f + 4 * c4);
       }
       if (tid == 0) {
@@ -980,10 +1026,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       if (sh.len_f != len) continue;
     }
     int32_t* page = p.s.page + rlx * g.max_context;
-    int32_t* reverse = p.s.reverse + rlx * B;
-    int32_t* stamp = p.s.stamp + rlx * B;
-    int32_t* order = p.s.order + rlx * B;
-    int32_t* sos = p.s.slot_of_sel + (long long)ri * K;
+    int32_t* reverse = p.s.reverse + rlx * BR;
+    int32_t* stamp = p.s.stamp + rlx * BR;
+    int32_t* order = p.s.order + rlx * BR;
+    int32_t* sos = p.s.slot_of_sel + (long long)ri * KR;
     const int t = pass == 0 ? t_step : sh.t_step_f;
     int m = 0;
     // the lead copies its missed rows in fetch mode 1 (else the attention kernel
@@ -1021,7 +1067,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // write-allocate: the token this call appends counts as used even when the
     // selection does not take it (one extra entry after the selection: a new
     // position, so never resident)
-    const int extra = (p.write_allocate && appended && sh.ok && !(kk > 0 && sel[kk - 1] == len)) ? 1 : 0;
+    const int extra = (p.write_allocate && !paged && appended && sh.ok && !(kk > 0 && sel[kk - 1] == len)) ? 1 : 0;
     const int kx = kk + extra;
     if (extra && tid == 0) {
       sel[kk] = len;
@@ -1126,19 +1172,31 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       page[pnew] = v;
       slot_sel[i] = v;
       // the lead's appended token: its row is in shared memory, it goes to its slot
-      // here; a follower's appended token: flagged, its row comes with its own call
-      if (pass == 0) miss_i[qq] = (pull || (appended && pnew == len)) ? i : (i | HS_SLOT_MISS_FLAG);
+      // here; a follower's appended token: flagged, its row comes with its own call.
+      // Page mode: a page is flagged whole; its appended row is left out below.
+      if (pass == 0) miss_i[qq] = (pull || (!paged && appended && pnew == len)) ? i : (i | HS_SLOT_MISS_FLAG);
       else miss_i[qq] = (appended && pnew == len) ? (i | HS_SLOT_MISS_FLAG) : i;
     }
     __syncthreads();
-    if (pass == 0) {
+    if (pass == 0 && !paged) {
       for (int i = tid; i < kk; i += NT) sos[i] = slot_sel[i];
       __syncthreads();
       for (int qq = tid; qq < m; qq += NT)
         if (miss_i[qq] & HS_SLOT_MISS_FLAG) sos[miss_i[qq] & ~HS_SLOT_MISS_FLAG] = victim[qq] | HS_SLOT_MISS_FLAG;
+    } else if (pass == 0) {
+      // page mode: row i of the expansion is row i % PS of page slot slot_sel[i / PS]
+      for (int i = tid; i < kkr; i += NT) sos[i] = (slot_sel[i >> psh] << psh) + (i & (PS - 1));
+      __syncthreads();
+      for (int e = tid; e < m * PS; e += NT) {
+        const int qq = e >> psh, o = e & (PS - 1);
+        if (!(miss_i[qq] & HS_SLOT_MISS_FLAG)) continue;
+        const int u = miss_i[qq] & ~HS_SLOT_MISS_FLAG;
+        const int i = (u << psh) + o;
+        if (i < kkr && !(appended && (sel[u] << psh) + o == len)) sos[i] |= HS_SLOT_MISS_FLAG;
+      }
     } else {   // what the follower's own call needs: selection, slots, k_eff, the pending slot
-      int32_t* fs = p.s.sh_slots + rlx * K;
-      int32_t* fp = p.s.sh_sel + rlx * K;
+      int32_t* fs = p.s.sh_slots + rlx * KR;
+      int32_t* fp = p.s.sh_sel + rlx * KR;
       for (int i = tid; i < kk; i += NT) {
         fs[i] = slot_sel[i];
         fp[i] = sel[i];
@@ -1158,8 +1216,51 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const int rvec = g.row_bytes / 16;
       const unsigned char* src_base =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
-      unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rlx * B * g.row_bytes;
-      if (pull) {
+      unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rlx * BR * g.row_bytes;
+      if (paged) {
+        // every row of a missed page below the length (fetch mode 1), then the
+        // appended row into its page's slot whenever that page is resident: a hit,
+        // a page filled by this call, or a resident page the selection passed over
+        if (pull) {
+          const long long total = (long long)m * PS * rvec;
+          constexpr int U = 8;
+          for (long long e0 = tid; e0 < total; e0 += (long long)U * NT) {
+            int4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const long long e = e0 + (long long)u * NT;
+              if (e < total) {
+                const int qo = (int)(e / rvec);
+                const int cidx = (int)(e - (long long)qo * rvec);
+                const int pos = (sel[miss_i[qo >> psh]] << psh) + (qo & (PS - 1));
+                if (pos >= Np) continue;
+                v[u] = (appended && pos == len)
+                           ? reinterpret_cast<const int4*>(newrow)[cidx]
+                           : *reinterpret_cast<const int4*>(src_base + (size_t)pos * g.row_bytes + cidx * 16);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const long long e = e0 + (long long)u * NT;
+              if (e < total) {
+                const int qo = (int)(e / rvec);
+                const int cidx = (int)(e - (long long)qo * rvec);
+                const int o = qo & (PS - 1);
+                if ((sel[miss_i[qo >> psh]] << psh) + o >= Np) continue;
+                *reinterpret_cast<int4*>(dst_base + (size_t)((victim[qo >> psh] << psh) + o) * g.row_bytes +
+                                         cidx * 16) = v[u];
+              }
+            }
+          }
+        }
+        if (appended) {
+          const int ps = page[len >> psh];
+          if (ps >= 0 && ps < B)
+            for (int v = tid; v < rvec; v += NT)
+              *reinterpret_cast<int4*>(dst_base + (size_t)((ps << psh) + (len & (PS - 1))) * g.row_bytes + v * 16) =
+                  reinterpret_cast<const int4*>(newrow)[v];
+        }
+      } else if (pull) {
         const long long total = (long long)m * rvec;
         constexpr int U = 8;   // host reads in flight per thread
         for (long long e0 = tid; e0 < total; e0 += (long long)U * NT) {
@@ -1201,7 +1302,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     HS_TRACE_IF(p, 1, 7, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     if (pass == 0 && p.publish && tid == 0) {
       __threadfence();
-      if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, (unsigned)kk + 1u);   // k_eff + 1
+      if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, (unsigned)kkr + 1u);   // rows + 1
     }
 
     // the missed rows the attention kernel will copy start moving over the link
@@ -1211,14 +1312,16 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const int lines = g.row_bytes / 128;
       const unsigned char* src_base =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
-      for (int e = tid; e < m * lines; e += NT) {
-        const int qq = e / lines;
+      for (int e = tid; e < m * PS * lines; e += NT) {
+        const int qo = e / lines, qq = qo >> psh;
         if (!(miss_i[qq] & HS_SLOT_MISS_FLAG)) continue;   // the appended token: already in its slot
-        const int pos = sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG];
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(src_base + (size_t)pos * g.row_bytes + (e - qq * lines) * 128));
+        const int pos = (sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG] << psh) + (qo & (PS - 1));
+        if (pos >= Np || (appended && pos == len)) continue;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src_base + (size_t)pos * g.row_bytes + (e - qo * lines) * 128));
       }
     }
 
+    HS_TRACE_IF(p, 1, 12, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     // the next threshold to the exact key of rank k_next: the low digit of that
     // key from a histogram of the keys with its high digit (the candidates when
     // they hold every key that large, else all keys); off the critical path
@@ -1228,8 +1331,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
       __syncthreads();
       if (src == 1) {
-        const uint2* cl = p.s.cand + (long long)ri * 2 * K;
-        const int cnt = min(sh.cnt, 2 * K);
+        const uint2* cl = p.s.cand + (long long)ri * 2 * KR;
+        const int cnt = min(sh.cnt, 2 * KR);
         for (int i = tid; i < cnt; i += NT) {
           const uint32_t k = __ldcg(cl + i).y;
           if ((k >> 12) == bt) atomicAdd(&h[k & 4095u], 1u);
@@ -1246,6 +1349,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       if (tid == 0) sh.thr_next = (bt << 12) | (uint32_t)sh.b2;
     }
 
+    HS_TRACE_IF(p, 1, 13, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     // ======================= 5. metadata after publication =======================
     // LRU and random: every used slot is refreshed; FIFO: only the filled ones (used == 2)
     const bool fifo = p.replacement == HS_REPLACE_FIFO;
@@ -1275,7 +1379,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         // counters of the selected positions (an allocated new token is neither)
         red_add_u64(&p.s.hits[rlx], (unsigned long long)(kk - (m - extra)));
         red_add_u64(&p.s.misses[rlx], (unsigned long long)(m - extra));
-        red_add_u64(&p.s.glob[0], (unsigned long long)(m - extra) * g.row_bytes);
+        // rows over the host link: page mode, every row of a missed page below the length
+        const int mrows = !paged ? m - extra
+                                 : m * PS - ((m > 0 && sel[miss_i[m - 1] & ~HS_SLOT_MISS_FLAG] == N - 1) ? N * PS - Np : 0);
+        red_add_u64(&p.s.glob[0], (unsigned long long)mrows * g.row_bytes);
       }
     }
     if (pass > 0 && tid == 0) p.s.sh_armed[rlx] = 1;   // ready for the follower's call
@@ -1287,7 +1394,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // a group lead that does not prefetch leaves the selection for its followers
     if (p.role == ROLE_SELECT && !p.share_prefetch && p.n_follow > 0 && sh.ok) {
       for (int f = 1; f <= p.n_follow; ++f) {
-        int32_t* fp = p.s.sh_sel + (rl + f) * K;
+        int32_t* fp = p.s.sh_sel + (rl + f) * KR;
         for (int i = tid; i < kk; i += NT) fp[i] = sel[i];
         if (tid == 0) {
           p.s.sh_kk[rl + f] = kk;
@@ -1296,6 +1403,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
     }
 
+    HS_TRACE_IF(p, 1, 14, tid == 0 && ri == (int)blockIdx.x);
     // the appended token: key to the HBM store, row to the pinned host copy
     if (appended) {
       const int rvec = g.row_bytes / 16;
@@ -1304,14 +1412,24 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       if (tid < g.d_idx / 16)
         reinterpret_cast<int4*>(p.s.idx_keys + (rl * g.max_context + len) * g.d_idx)[tid] =
             reinterpret_cast<const int4*>(newkey)[tid];
+      // page mode: its page's bounds take the new key (a page it opens: the key alone)
+      const int hk = g.d_idx / 16;
+      if (paged && tid < 2 * hk) {
+        int4* bd = reinterpret_cast<int4*>(p.s.pbound + (rl * g.max_pages + (len >> psh)) * 2 * g.d_idx);
+        const bool hi = tid < hk;
+        const int4 kn = reinterpret_cast<const int4*>(newkey)[hi ? tid : tid - hk];
+        if ((len & (PS - 1)) == 0) bd[tid] = kn;
+        else bd[tid] = hi ? vmax16(bd[tid], kn) : vmin16(bd[tid], kn);
+      }
     }
+    HS_TRACE_IF(p, 1, 15, tid == 0 && ri == (int)blockIdx.x);
     // lengths and thresholds: only once every CTA of the launch has read them
     if (tid == 0) {
       if (!wait_counter(&p.s.sync[0], (unsigned)(p.sel_grid - p.n_resolvers))) {
         set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
       } else {
         if (appended) {
-          p.s.length[rl] = N;
+          p.s.length[rl] = Np;
           red_add_u64(&p.s.glob[1], (unsigned long long)g.row_bytes);
         }
         if (sh.ok) p.s.cand_thr[rl] = sh.thr_next;
@@ -1333,16 +1451,23 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
   }
 }
 
-template <int NCH, int NH>
+template <int NCH, int NH, bool PG = false>
 static cudaError_t run_select(const DecodeParams* p, size_t smem, cudaStream_t st) {
-  auto kern = select_kernel<NCH, NH>;
+  auto kern = select_kernel<NCH, NH, PG>;
   if (p == nullptr) return allow_smem(kern, smem);
   return launch_pdl(kern, dim3(p->sel_grid), dim3(NT), smem, st, *p);
 }
 
 // single-head indexer: d_idx 16..256; the multi-head indexer: d_idx 64 or 128,
-// 2, 4 or 8 heads
+// 2, 4 or 8 heads; page mode: unit rows of 2 * d_idx bytes (d_idx 64 or 128)
 static cudaError_t dispatch_select(const Geometry& g, const DecodeParams* p, size_t smem, cudaStream_t st) {
+  if (g.page_shift > 0) {
+    switch (g.d_idx) {
+      case 64: return run_select<8, 1, true>(p, smem, st);
+      case 128: return run_select<16, 1, true>(p, smem, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (g.idx_heads <= 1) {
     switch (g.d_idx) {
       case 16: return run_select<1, 1>(p, smem, st);

@@ -52,7 +52,7 @@ class HsConfig(ctypes.Structure):
                 ("fetch_mode", ctypes.c_int32), ("replacement", ctypes.c_int32),
                 ("replacement_seed", ctypes.c_uint32), ("write_allocate", ctypes.c_int32),
                 ("idx_heads", ctypes.c_int32), ("index_share", ctypes.c_int32),
-                ("share_prefetch", ctypes.c_int32)]
+                ("share_prefetch", ctypes.c_int32), ("page_size", ctypes.c_int32)]
 
 
 class HsStats(ctypes.Structure):
@@ -165,13 +165,13 @@ class HiSparseCache:
                  d_qk: int, d_v: int, d_idx: int, top_k: int, hot_slots: int, shared_kv: bool = False,
                  softmax_scale: float = 0.0, device: int = 0, fetch_mode: int = 2,
                  replacement: str = "lru", replacement_seed: int = 0, write_allocate: bool = False,
-                 idx_heads: int = 1, index_share: int = 1, share_prefetch: bool = True):
+                 idx_heads: int = 1, index_share: int = 1, share_prefetch: bool = True, page_size: int = 1):
         if replacement not in REPLACEMENT:
             raise ValueError(f"replacement must be one of {sorted(REPLACEMENT)}")
         self.cfg = HsConfig(n_layers, max_requests, max_context, h_q, h_kv, d_qk, d_v, int(shared_kv),
                             d_idx, top_k, hot_slots, softmax_scale, device, fetch_mode,
                             REPLACEMENT[replacement], replacement_seed, int(write_allocate), int(idx_heads),
-                            int(index_share), int(share_prefetch))
+                            int(index_share), int(share_prefetch), int(page_size))
         # bytes of one request's indexer query (heads, then weights and padding)
         self.q_idx_row = d_idx if idx_heads <= 1 else idx_heads * d_idx + 16
         self._h = ctypes.c_void_p()
