@@ -187,6 +187,9 @@ typedef struct hs_stats {
   uint64_t hot_bytes;     /* size of the HBM hot cache */
   uint64_t index_bytes;   /* size of the HBM index-key store (with the page-bound store) */
   uint64_t meta_bytes;    /* page table, reverse map, stamps, LRU order, counters */
+  uint64_t host_huge_bytes;  /* bytes of the host store backed by transparent huge pages when it
+                                was created (random row reads over the link take about half as
+                                long on them as on base pages) */
   uint64_t full_selects;  /* selections that scanned every key (no usable candidate list:
                              first steps, a large drift, contexts above 20 k positions) */
   uint32_t device_error;  /* HS_DEVERR_* bits seen so far (sticky) */
@@ -196,10 +199,12 @@ typedef struct hs_stats {
 /*
  * hs_create — validate `cfg` and allocate every store (synchronous).
  *   host store  D1: [max_requests][n_layers][max_context][row] bf16, pinned and
- *                   mapped host memory: anonymous memory advised for transparent
- *                   huge pages and registered with cudaHostRegister (Mapped |
- *                   Portable), else cudaHostAlloc(Mapped | Portable): the
- *                   authoritative copy;
+ *                   mapped host memory: anonymous memory in whole transparent huge
+ *                   pages (advised, faulted in, and what the kernel backed with
+ *                   base pages collapsed with MADV_COLLAPSE; the coverage is in
+ *                   hs_stats.host_huge_bytes), registered with cudaHostRegister
+ *                   (Mapped | Portable), else cudaHostAlloc(Mapped | Portable):
+ *                   the authoritative copy;
  *   hot cache   D2: [max_requests][n_layers][hot_slots][row] bf16 in HBM;
  *   index keys  D3: [max_requests][n_layers][max_context][d_idx] int8 in HBM;
  *   page table  D4: [max_requests][n_layers][max_context] int32, -1 = not resident;

@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <sys/mman.h>
+#include <unistd.h>
 #include <new>
 #include <string>
 
@@ -29,6 +30,33 @@ int cuda_fail(hs_handle* h, cudaError_t e, const char* what) {
 }
 
 bool is_pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+#ifndef MADV_COLLAPSE
+#define MADV_COLLAPSE 25   // Linux 6.1+: synchronous collapse of a range into transparent huge pages
+#endif
+
+// Bytes backed by transparent huge pages in the anonymous mappings that overlap
+// [a, a + n), from /proc/self/smaps (0 where it cannot be read).
+size_t huge_bytes_in(const void* a, size_t n) {
+  FILE* f = std::fopen("/proc/self/smaps", "r");
+  if (!f) return 0;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(a), hi = lo + n;
+  char line[512];
+  bool in = false;
+  unsigned long long kb = 0;
+  while (std::fgets(line, sizeof line, f)) {
+    unsigned long s0 = 0, s1 = 0;
+    const char* dash = std::strchr(line, '-');
+    const char* space = std::strchr(line, ' ');
+    if (dash && space && dash < space && std::sscanf(line, "%lx-%lx", &s0, &s1) == 2) {
+      in = s0 < hi && s1 > lo;   // a mapping's header line
+    } else if (in && std::strncmp(line, "AnonHugePages:", 14) == 0) {
+      kb += std::strtoull(line + 14, nullptr, 10);
+    }
+  }
+  std::fclose(f);
+  return (size_t)std::min<unsigned long long>(kb * 1024ull, n);
+}
 
 // Returns "" when the configuration is one the kernels support, else the reason.
 std::string check_config(const hs_config_t& c) {
@@ -271,18 +299,27 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   h->fault = fi.noready ? 1 : 0;
   // D1: authoritative copy in pinned, mapped host memory
   if (fi.host) return fail_free(HS_ERR_OOM, "hs_create: pinned host allocation failed (injected)");
-  // Anonymous memory advised for transparent huge pages, then pinned and mapped:
-  // RESOLVE and the attention kernel read missed rows at random positions, and
-  // with large pages far fewer of those reads miss the GPU's TLB.  Falls back
-  // to cudaHostAlloc where the kernel offers no huge pages or registration fails.
+  // Anonymous memory in whole transparent huge pages, then pinned and mapped:
+  // the missed rows are read at random positions, and a read of a row on a huge
+  // page takes about half as long as one on base pages (a latency the attention
+  // kernel waits for).  The store is faulted in first; whatever the kernel backed
+  // with base pages is then collapsed synchronously (MADV_COLLAPSE, which
+  // compacts memory as needed); the coverage is reported by hs_stats.  Falls
+  // back to cudaHostAlloc where mapping or registration fails.
   void* hp = nullptr;
   {
-    const size_t align = (size_t)512 << 20;
-    const size_t len = h->host_bytes + align;
+    const size_t align = (size_t)512 << 20;   // the largest huge page (64 KB base pages); a multiple of the rest
+    const size_t span = (h->host_bytes + align - 1) / align * align;
+    const size_t len = span + align;
     void* raw = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
     if (raw != MAP_FAILED) {
       void* a = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(raw) + align - 1) & ~(uintptr_t)(align - 1));
-      (void)madvise(a, h->host_bytes, MADV_HUGEPAGE);
+      (void)madvise(a, span, MADV_HUGEPAGE);
+      const long pg = sysconf(_SC_PAGESIZE);
+      const size_t step = pg > 0 ? (size_t)pg : 4096;
+      for (size_t off = 0; off < span; off += step) static_cast<volatile unsigned char*>(a)[off] = 0;
+      if (huge_bytes_in(a, span) < span) (void)madvise(a, span, MADV_COLLAPSE);
+      h->host_huge_bytes = std::min(huge_bytes_in(a, span), h->host_bytes);
       if (cudaHostRegister(a, h->host_bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
         hp = a;
         h->host_map_base = raw;
@@ -389,6 +426,9 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
                  cudaSuccess;
 #endif
   ok = ok && hs::launch_init_order(s.order, (long long)(R * Lr), (int)B, 0) == cudaSuccess;
+  // the GPU reads every line of the host store once now, so that no decode step
+  // waits on a first read (those can take hundreds of microseconds)
+  ok = ok && hs::launch_touch_host(s.host_kv, h->host_bytes, h->num_sms, 0) == cudaSuccess;
   if (!ok) return fail_free(HS_ERR_CUDA, "hs_create: initialising the metadata failed");
   if ((e = hs::prepare_select(g, h->sel_smem)) != cudaSuccess ||
       (e = hs::prepare_attention(g, h->att_smem)) != cudaSuccess)
@@ -547,6 +587,7 @@ int hs_stats(hs_handle_t* h, hs_stats_t* out) {
   out->index_bytes = h->index_bytes;
   out->meta_bytes = h->meta_bytes;
   out->full_selects = glob[2];
+  out->host_huge_bytes = h->host_huge_bytes;
   out->device_error = err;
   if (err) return set_err(h, HS_ERR_DEVICE, "hs_stats: device error word " + std::to_string(err));
   return HS_OK;

@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     if (lane == 0 && cur < total) nxt = atomicAdd(&p.s.sync[2], 1u);
     Meta pf;                // metadata of the next chunk, when it was ready early
     long long pf_item = -1;
+    bool pf_warm = false;   // its hit rows were sent towards L2
     while (!dead && cur < total) {
       const long long item = cur;
       const int r = (int)(item / NCHK);
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         if (u == 0) {   // the next chunk's metadata now, if its request is already published
           const long long nx = (long long)__shfl_sync(FULL_MASK, nxt, 0);
           pf_item = -1;
+          pf_warm = false;
           if (nx < total) {
             const int rn = (int)(nx / NCHK);
             unsigned v = 0;
@@ -394,6 +396,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
               load_rows(pf, rn, (int)(nx % NCHK));
               pf_item = nx;
             }
+          }
+        }
+        if (pf_item >= 0 && !pf_warm && (u == 1 || u == nunits - 1)) {
+          // one unit later (its metadata has landed by now): the next chunk's hit
+          // rows start moving into L2, one bulk prefetch per row, so that its bulk
+          // copies read L2 and more bytes are in flight than the stages hold
+          pf_warm = true;
+          const int pr0 = (int)(pf_item % NCHK) * CR;
+          const int pnr = max(0, min(CR, pf.kk - pr0));
+          const long long rln = (long long)pf.req * g.n_layers + p.layer;
+          const unsigned char* hotn =
+              reinterpret_cast<const unsigned char*>(p.s.hot) + (size_t)rln * g.hot_slots * g.row_bytes;
+#pragma unroll
+          for (int j = 0; j < NJC; ++j) {
+            const int sl = pf.slot[j];
+            if (lane + 32 * j < pnr && !(sl & HS_SLOT_MISS_FLAG) && sl >= 0 && sl < g.hot_slots)
+              bulk_prefetch_l2(hotn + (size_t)sl * g.row_bytes, (uint32_t)g.row_bytes);
           }
         }
       }

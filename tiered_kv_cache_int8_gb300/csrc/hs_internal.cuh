@@ -153,6 +153,7 @@ struct hs_handle {
   uint16_t* host_kv_host = nullptr;   // host view of the pinned store
   void* host_map_base = nullptr;      // the store's mapping when it was registered (else cudaHostAlloc)
   size_t host_map_bytes = 0;
+  size_t host_huge_bytes = 0;        // of the store, backed by transparent huge pages at create
   float scale_log2 = 0.f;
   int num_sms = 0;
   long long score_stride = 0;
@@ -178,6 +179,7 @@ namespace hs {
 // launchers (one per kernel translation unit); return a CUDA error code
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_page_bounds(const AppendParams& p, cudaStream_t st);
+cudaError_t launch_touch_host(const void* p, size_t bytes, int num_sms, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_follow(const DecodeParams& p, cudaStream_t st);
@@ -365,6 +367,12 @@ __device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, 
           smem_addr(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// Starts bringing `bytes` (a multiple of 16) at a 16-byte aligned global address
+// into L2; a hint: no data returns and nothing waits on it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {

@@ -27,13 +27,16 @@
 //    request that needs a selection (more positions than k) are flattened in
 //    request order and cut into warp tiles (two sub-tiles of 8 x 16-byte loads
 //    per lane); scorer warp w takes tiles w, w + W, w + 2W, ... so all warps
-//    sweep the requests in order and request r is complete early.  Loads are
-//    coalesced 16-byte streaming loads (the 8 lanes of a position read its
-//    8 chunks side by side), one sub-tile in flight while the other is scored;
-//    dp4a partial sums are combined with lane shuffles.  Each key
+//    sweep the requests in order and request r is complete early.  The DRAM
+//    stream is driven by bulk L2 prefetches two rounds of tiles ahead (the
+//    first two rounds before the grid dependency resolves); the tile itself is
+//    read with coalesced 16-byte loads (the 8 lanes of a position read its
+//    8 chunks side by side) that then hit L2, issued only after the previous
+//    tile's release so that its fence does not wait for them; dp4a partial
+//    sums are combined with lane shuffles.  Each key
 //    (score + 2^22, order-preserving, 24 bits) goes to a scratch row; keys at or
 //    above the request's candidate threshold (left by the previous call) are
-//    also listed with their positions (one atomic per warp sub-tile).  After a
+//    also listed with their positions (one atomic per warp tile).  After a
 //    tile its warp adds 1 to the request's tile counter with release order.
 //  * A resolver takes requests j, j + n_resolvers, ...: it first prefetches
 //    what does not depend on the scores (LRU list, reverse map, the appended
@@ -156,9 +159,11 @@ struct SelShared {
 };
 
 // Finds the digit holding the kneed-th largest key (bins scanned from the top)
-// and the number of keys in higher digits.  Leaves *out_b untouched when the
-// histogram holds fewer than kneed keys.
-__device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* scan, int* out_b, int* out_above) {
+// and the number of keys in higher digits; with kneed2 > 0 the same for a second
+// rank in the same scan.  Leaves an output untouched when the histogram holds
+// fewer keys than its rank.
+__device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* scan, int* out_b, int* out_above,
+                                             int kneed2 = 0, int* out_b2 = nullptr, int* out_above2 = nullptr) {
   constexpr int PER = IDX_BINS / NT;   // bins per thread, descending
   const int tid = threadIdx.x;
   const int top = IDX_BINS - 1 - tid * PER;
@@ -167,18 +172,22 @@ __device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* 
   for (int j = 0; j < PER; ++j) v += (int)h[top - j];
   int tot;
   const int ex = block_exclusive_scan<NT>(v, scan, &tot);
-  if (ex < kneed && kneed <= ex + v) {
-    int acc = ex;
+  auto find = [&](int kn, int* ob, int* oa) {
+    if (ex < kn && kn <= ex + v) {
+      int acc = ex;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int hv = (int)h[top - j];
-      if (acc < kneed && kneed <= acc + hv) {
-        *out_b = top - j;
-        *out_above = acc;
+      for (int j = 0; j < PER; ++j) {
+        const int hv = (int)h[top - j];
+        if (acc < kn && kn <= acc + hv) {
+          *ob = top - j;
+          *oa = acc;
+        }
+        acc += hv;
       }
-      acc += hv;
     }
-  }
+  };
+  find(kneed, out_b, out_above);
+  if (kneed2 > 0) find(kneed2, out_b2, out_above2);
   __syncthreads();
 }
 
@@ -245,10 +254,11 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
   __shared__ SelShared sh;
   HS_TRACE(p, 0, 0);
 
-  griddep_wait();   // lengths, keys, metadata and scratch of earlier stream work
-  griddep_launch_dependents();
-
   const bool resolver = (int)blockIdx.x < p.n_resolvers;
+  if (resolver) {
+    griddep_wait();   // lengths, keys, metadata and scratch of earlier stream work
+    griddep_launch_dependents();
+  }
 
   // ======================= scorers =======================
   if (!resolver) {
@@ -256,41 +266,74 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     int* t_req = reinterpret_cast<int*>(smem_raw + L.t_req);
     int* t_n = reinterpret_cast<int*>(smem_raw + L.t_n);
     uint32_t* t_thr = reinterpret_cast<uint32_t*>(smem_raw + L.t_thr);
-    // warp tiles of every request that needs a selection
-    int carry = 0;
-    for (int base = 0; base < p.n_req; base += NT) {
-      const int i = base + tid;
-      int nt = 0;
-      if (i < p.n_req) {
-        const int req = p.req_ids ? p.req_ids[i] : i;
-        int N = 0;
-        uint32_t thr = 0;
-        if (req >= 0 && req < g.max_requests) {
-          const long long rl = (long long)req * g.n_layers + p.layer;
-          N = p.s.length[rl];
-          if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
-          thr = p.s.cand_thr[rl];
+    const int W = (p.sel_grid - p.n_resolvers) * NWARP;
+    const int w0 = ((int)blockIdx.x - p.n_resolvers) * NWARP + warp;
+    // request of warp tile t, searching forward from request `from`
+    auto req_of = [&](int t, int from) {
+      int x = from;
+      while (t_prefix[x + 1] <= t) ++x;
+      return x;
+    };
+    // the unit rows of warp tile t (request ri) start moving into L2 (one bulk
+    // prefetch by lane 0): the register loads of the tile then hit L2, so far more
+    // bytes are in flight per SM than the registers hold
+    auto prefetch_tile = [&](int t, int ri) {
+      const int NU = (t_n[ri] + PS - 1) >> psh;
+      const int u0 = (t - t_prefix[ri]) * SG::TILE;
+      const int nu = min(SG::TILE, NU - u0);
+      if (lane != 0 || nu <= 0) return;
+      const long long rl = (long long)t_req[ri] * g.n_layers + p.layer;
+      const int8_t* base = paged ? p.s.pbound + rl * (long long)g.max_pages * d : p.s.idx_keys + rl * g.max_context * d;
+      bulk_prefetch_l2(base + (long long)u0 * d, (uint32_t)(nu * d));
+    };
+    // warp tiles of every request that needs a selection; returns their number
+    auto build_tables = [&]() {
+      int carry = 0;
+      for (int base = 0; base < p.n_req; base += NT) {
+        const int i = base + tid;
+        int nt = 0;
+        if (i < p.n_req) {
+          const int req = p.req_ids ? p.req_ids[i] : i;
+          int N = 0;
+          uint32_t thr = 0;
+          if (req >= 0 && req < g.max_requests) {
+            const long long rl = (long long)req * g.n_layers + p.layer;
+            N = p.s.length[rl];
+            if (p.new_kv && N + 1 <= g.max_context) ++N;   // the token this call appends
+            thr = p.s.cand_thr[rl];
+          }
+          const int NU = (N + PS - 1) >> psh;
+          const bool scored = NU > (KR >> psh) && p.role == ROLE_SELECT;
+          nt = scored ? (NU + SG::TILE - 1) / SG::TILE : 0;
+          t_req[i] = scored ? req : -1;
+          t_n[i] = N;
+          t_thr[i] = (scored && NH == 1) ? thr : 0u;   // candidate listing: single-head keys only
         }
-        const int NU = (N + PS - 1) >> psh;
-        const bool scored = NU > (KR >> psh) && p.role == ROLE_SELECT;
-        nt = scored ? (NU + SG::TILE - 1) / SG::TILE : 0;
-        t_req[i] = scored ? req : -1;
-        t_n[i] = N;
-        t_thr[i] = (scored && NH == 1) ? thr : 0u;   // candidate listing: single-head keys only
+        int tot;
+        const int ex = block_exclusive_scan<NT>(nt, sh.scan, &tot);
+        if (i < p.n_req) t_prefix[i] = carry + ex;
+        carry += tot;
       }
-      int tot;
-      const int ex = block_exclusive_scan<NT>(nt, sh.scan, &tot);
-      if (i < p.n_req) t_prefix[i] = carry + ex;
-      carry += tot;
+      if (tid == 0) t_prefix[p.n_req] = carry;
+      __syncthreads();
+      return carry;
+    };
+    // Before the grid dependency resolves: the tile map from the state as it
+    // stands and the first two rounds of this CTA's tiles into L2, overlapping
+    // the previous kernel's tail.  Only prefetch hints come of it (every address
+    // stays inside the stores whatever it read); the map is rebuilt after the wait.
+    {
+      const int total0 = build_tables();
+      if (w0 < total0) prefetch_tile(w0, req_of(w0, 0));
+      if (w0 + W < total0) prefetch_tile(w0 + W, req_of(w0 + W, 0));
+      __syncthreads();   // the tables are rebuilt below
     }
-    if (tid == 0) t_prefix[p.n_req] = carry;
-    __syncthreads();
+    griddep_wait();   // lengths, keys, metadata and scratch of earlier stream work
+    griddep_launch_dependents();
+    const int total = build_tables();
     // this CTA has read every length and threshold it needs
     if (tid == 0) red_release_add(&p.s.sync[0], 1u);
     HS_TRACE(p, 0, 1);
-    const int total = carry;
-    const int W = (p.sel_grid - p.n_resolvers) * NWARP;
-    const int w0 = ((int)blockIdx.x - p.n_resolvers) * NWARP + warp;
 
     // lane roles inside a load instruction
     const int pg = lane / SG::LPP;            // position within the instruction
@@ -301,12 +344,6 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     const int qstride = NH > 1 ? NH * d + 16 : g.d_idx;   // bytes of one request's indexer query
     const int hc = g.d_idx / 16;   // page mode: a unit row is [key maxima | key minima], 2 * hc chunks
 
-    // request of warp tile t, searching forward from request `from`
-    auto req_of = [&](int t, int from) {
-      int x = from;
-      while (t_prefix[x + 1] <= t) ++x;
-      return x;
-    };
     // loads of sub-tile `half` of tile t (request ri) into v (zeros past the last
     // unit).  Unit rows: index keys, or in page mode the stored [max | min] bounds
     // of each page; the unit holding this call's appended token combines its key
@@ -380,9 +417,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       uint32_t* keys_out = p.s.scores + (long long)ri * p.score_stride;
       const int tn = t + W;
       const int rn = tn < total ? req_of(tn, ri) : ri;
+      // keys of both sub-tiles; lane cl of a position group owns the groups j with
+      // j % LPP == cl
+      uint32_t ownk[2][SG::OWN];
+      int ownp[2][SG::OWN];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        int4 (&v)[SG::LD] = half == 0 ? va : vb;
+        const int4 (&v)[SG::LD] = half == 0 ? va : vb;
         int acc[SG::NP][NH];   // each head's partial dot product over this lane's chunks
 #pragma unroll
         for (int j = 0; j < SG::NP; ++j)
@@ -400,8 +441,6 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
             acc[j][h] = __dp4a(v[u].w, qq.w, acc[j][h]);
           }
         }
-        // the buffer is free: start the same half of this warp's next tile
-        if (tn < total) load_sub(tn, rn, half, v);
         // key of each position group: single head, score + 2^22 (24 bits); several
         // heads, sum_h w_h * max(0, dot_h) (non-negative, below 2^32)
         uint32_t key[SG::NP];
@@ -418,43 +457,61 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           }
           key[j] = tot;
         }
-        // lane cl of a position group owns position groups j with j % LPP == cl
         const int sub0 = tile0 + half * SG::SUB;
-        uint32_t ownk[SG::OWN];
-        int ownp[SG::OWN];
 #pragma unroll
         for (int o = 0; o < SG::OWN; ++o) {
-          ownk[o] = 0;
-          ownp[o] = N;   // none
+          ownk[half][o] = 0;
+          ownp[half][o] = N;   // none
         }
 #pragma unroll
         for (int j = 0; j < SG::NP; ++j) {
           if (j % SG::LPP == cl) {
             const int o = j / SG::LPP;
-            ownp[o] = sub0 + j * SG::PPI + pg;
-            ownk[o] = key[j];
+            ownp[half][o] = sub0 + j * SG::PPI + pg;
+            ownk[half][o] = key[j];
           }
         }
 #pragma unroll
-        for (int o = 0; o < SG::OWN; ++o) {
-          const bool valid = ownp[o] < N;
-          if (valid) keys_out[ownp[o]] = ownk[o];
-          if (thr != 0u) {
-            const bool c = valid && ownk[o] >= thr;
-            const unsigned m = __ballot_sync(FULL_MASK, c);
-            if (m) {
-              unsigned base = 0;
-              if (lane == 0) base = atomicAdd(p.s.cand_cnt + ri, (unsigned)__popc(m));
-              base = __shfl_sync(FULL_MASK, base, 0);
-              const unsigned at = base + __popc(m & ((1u << lane) - 1u));
-              if (c && at < 2u * (unsigned)KR)
-                p.s.cand[(long long)ri * 2 * KR + at] = make_uint2((uint32_t)ownp[o], ownk[o]);
-            }
+        for (int o = 0; o < SG::OWN; ++o)
+          if (ownp[half][o] < N) keys_out[ownp[half][o]] = ownk[half][o];
+      }
+      // the tile's keys at or above the candidate threshold, listed with one atomic
+      if (thr != 0u) {
+        unsigned mk[2][SG::OWN];
+        int cnt = 0;
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int o = 0; o < SG::OWN; ++o) {
+            mk[half][o] = __ballot_sync(FULL_MASK, ownp[half][o] < N && ownk[half][o] >= thr);
+            cnt += __popc(mk[half][o]);
           }
+        if (cnt > 0) {   // warp-uniform
+          unsigned base = 0;
+          if (lane == 0) base = atomicAdd(p.s.cand_cnt + ri, (unsigned)cnt);
+          base = __shfl_sync(FULL_MASK, base, 0);
+          const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+#pragma unroll
+            for (int o = 0; o < SG::OWN; ++o) {
+              const unsigned at = base + __popc(mk[half][o] & below);
+              if (((mk[half][o] >> lane) & 1u) && at < 2u * (unsigned)KR)
+                p.s.cand[(long long)ri * 2 * KR + at] = make_uint2((uint32_t)ownp[half][o], ownk[half][o]);
+              base += __popc(mk[half][o]);
+            }
         }
       }
       __syncwarp();
       if (lane == 0) red_release_add(p.s.tiles_done + ri, 1u);
+      // then the next tile: its rows two rounds ahead towards L2, and the register
+      // loads of the next one (issued after the release, whose fence would
+      // otherwise wait for them to land)
+      if (tn + W < total) prefetch_tile(tn + W, req_of(tn + W, rn));
+      if (tn < total) {
+        load_sub(tn, rn, 0, va);
+        load_sub(tn, rn, 1, vb);
+      }
       HS_TRACE_IF(p, 0, 3, tid == 0 && t == w0);
       HS_TRACE_IF(p, 0, 4, tid == 0 && t == w0 + W);
       r_cur = rn;
@@ -544,11 +601,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           sh.ok = 0;
         }
         p.s.tiles_done[ri] = 0;   // ready for the next call
-        sh.cnt = (int)min(__ldcg(p.s.cand_cnt + ri), 0x7fffffffu);
-        p.s.cand_cnt[ri] = 0;
-      } else {
-        sh.cnt = 0;
       }
+      sh.cnt = 0;
     }
     cp_async_wait_all();
     __syncthreads();
@@ -557,6 +611,24 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     const int N = (Np + PS - 1) >> psh;                        // units
     const bool appended = Np > len;
     const int kk = sh.ok ? min(K, N) : 0;   // (a given selection has the same k_eff: same N)
+    // the candidate list (every entry it can hold: those past the count are
+    // ignored) and its count, in one round trip
+    uint2 cv[CAND_REG];
+    if (N > K && p.role == ROLE_SELECT) {   // CTA-uniform
+      const bool may_cand = sh.ok && L.fast && N <= FAST_MAX_N && sh.thr != 0u;
+      const uint2* cl = p.s.cand + (long long)ri * 2 * KR;
+      const int cap = min(2 * KR, CAND_REG * NT);
+#pragma unroll
+      for (int j = 0; j < CAND_REG; ++j) {
+        const int i = tid + j * NT;
+        cv[j] = (may_cand && i < cap) ? __ldcg(cl + i) : make_uint2(0u, 0u);
+      }
+      if (tid == 0) {
+        sh.cnt = (int)min(__ldcg(p.s.cand_cnt + ri), 0x7fffffffu);
+        p.s.cand_cnt[ri] = 0;
+      }
+      __syncthreads();
+    }
 
     // ======================= 1. top-k, ascending =======================
     // The previous call's threshold listed between k and min(2k, 4096) keys: the k
@@ -578,20 +650,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       for (int i = tid; i < N; i += NT) sel[i] = i;
     } else if (use_cand) {
       const int cnt = sh.cnt;
-      const uint2* cl = p.s.cand + (long long)ri * 2 * KR;
       const int32_t* page_rl = p.s.page + rl * g.max_context;
       const int NWd = (N + 31) >> 5;
       uint32_t* gtw = bitmap;                         // [NWd] positions whose key is above the k-th
       uint32_t* tiw = bitmap + FAST_MAX_N / 32;       // [NWd] positions whose key equals it
       uint16_t* gpre = reinterpret_cast<uint16_t*>(smem_raw + L.wpre);   // [NWd] above-threshold positions before each word
       uint16_t* epre = gpre + FAST_MAX_N / 32;                           // [NWd] ties before each word (all < 2^16)
-      uint2 cv[CAND_REG];
       int cpg[CAND_REG];
-#pragma unroll
-      for (int j = 0; j < CAND_REG; ++j) {
-        const int i = tid + j * NT;
-        cv[j] = i < cnt ? __ldcg(cl + i) : make_uint2(0u, 0u);
-      }
       // every selected position is a candidate: its page entry is the hit test
 #pragma unroll
       for (int j = 0; j < CAND_REG; ++j) cpg[j] = tid + j * NT < cnt ? page_rl[cv[j].x] : -1;
@@ -607,9 +672,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         if (tid + j * NT < cnt) atomicAdd(&h[cv[j].y >> 12], 1u);
       __syncthreads();
       HS_TRACE_IF(p, 1, 11, tid == 0 && ri == (int)blockIdx.x);
-      select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
+      select_digit(h, K, sh.scan, &sh.b1, &sh.above1, cnt >= k_next ? k_next : 0, &sh.bt, &sh.above_t);
       if (cnt >= k_next) {
-        select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
         if (tid == 0) {
           sh.thr_next = (uint32_t)sh.bt << 12;
           sh.thr_src = 1;
@@ -792,10 +856,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       __syncthreads();
       // the digit of the k-th largest key, and the digit above which ~1.25 k keys
       // lie: the next call lists keys from there on (exact whenever >= k clear it)
-      select_digit(h, K, sh.scan, &sh.b1, &sh.above1);
       const int counted = (sh.thr != 0u && sh.cnt >= K) ? sh.cnt : N;   // keys the histogram holds
+      select_digit(h, K, sh.scan, &sh.b1, &sh.above1, counted >= k_next ? k_next : 0, &sh.bt, &sh.above_t);
       if (counted >= k_next) {
-        select_digit(h, k_next, sh.scan, &sh.bt, &sh.above_t);
         if (tid == 0) {
           sh.thr_next = (uint32_t)sh.bt << 12;
           sh.thr_src = 2;
@@ -991,12 +1054,11 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // rows attended: every position of the selected units below the length (only
     // the last page can be partial; when selected it is the last selected unit)
     const int kkr = !paged ? kk : (kk > 0 ? kk * PS - (sel[kk - 1] == N - 1 ? N * PS - Np : 0) : 0);
+    // the selection for the attention kernel now; the caller's copy (sel_out)
+    // after publication
+    auto row_pos = [&](int i) { return paged ? (sel[i >> psh] << psh) + (i & (PS - 1)) : sel[i]; };
     int32_t* sel_g = p.s.sel + (long long)ri * KR;
-    for (int i = tid; i < KR; i += NT) {
-      const int v = i < kkr ? (paged ? (sel[i >> psh] << psh) + (i & (PS - 1)) : sel[i]) : -1;
-      if (i < kkr) sel_g[i] = v;
-      if (sel_out) sel_out[i] = v;
-    }
+    for (int i = tid; i < kkr; i += NT) sel_g[i] = row_pos(i);
 
     // ======================= 2. RESOLVE metadata =======================
     // pass 0: this call's layer.  Passes 1..n_follow: the follower layers of its
@@ -1217,11 +1279,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const unsigned char* src_base =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
       unsigned char* dst_base = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rlx * BR * g.row_bytes;
+      bool wrote = false;   // this call wrote slot rows (CTA-uniform)
       if (paged) {
         // every row of a missed page below the length (fetch mode 1), then the
         // appended row into its page's slot whenever that page is resident: a hit,
         // a page filled by this call, or a resident page the selection passed over
         if (pull) {
+          wrote = m > 0;
           const long long total = (long long)m * PS * rvec;
           constexpr int U = 8;
           for (long long e0 = tid; e0 < total; e0 += (long long)U * NT) {
@@ -1255,12 +1319,14 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         }
         if (appended) {
           const int ps = page[len >> psh];
+          if (ps >= 0 && ps < B) wrote = true;
           if (ps >= 0 && ps < B)
             for (int v = tid; v < rvec; v += NT)
               *reinterpret_cast<int4*>(dst_base + (size_t)((ps << psh) + (len & (PS - 1))) * g.row_bytes + v * 16) =
                   reinterpret_cast<const int4*>(newrow)[v];
         }
       } else if (pull) {
+        wrote = m > 0;
         const long long total = (long long)m * rvec;
         constexpr int U = 8;   // host reads in flight per thread
         for (long long e0 = tid; e0 < total; e0 += (long long)U * NT) {
@@ -1291,33 +1357,35 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         }
       } else if (pass == 0 && appended && m > 0 && sel[miss_i[m - 1] & ~HS_SLOT_MISS_FLAG] == len) {
         // the appended token is the highest position: if it missed, it is the last miss
+        wrote = true;
         for (int v = tid; v < rvec; v += NT)
           *reinterpret_cast<int4*>(dst_base + (size_t)victim[m - 1] * g.row_bytes + v * 16) =
               reinterpret_cast<const int4*>(newrow)[v];
       }
-      fence_proxy_async_global();   // generic-proxy slot writes, read by bulk copies
+      if (wrote) fence_proxy_async_global();   // generic-proxy slot writes, read by bulk copies
     }
     // ======================= 4. publication =======================
     __syncthreads();
     HS_TRACE_IF(p, 1, 7, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
+    // the barrier above orders every thread's writes for this request before
+    // thread 0's release store (release is cumulative), which the attention
+    // kernel's acquire load pairs with
     if (pass == 0 && p.publish && tid == 0) {
-      __threadfence();
       if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, (unsigned)kkr + 1u);   // rows + 1
     }
+    HS_TRACE_IF(p, 1, 16, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
 
     // the missed rows the attention kernel will copy start moving over the link
-    // into L2 now, line by line, spread over the whole CTA (its later chunks then
-    // read them from L2)
+    // into L2 now, one bulk prefetch per row (page mode: per page), spread over
+    // the CTA (its later chunks then read them from L2)
     if (pass == 0 && !pull && m > 0) {
-      const int lines = g.row_bytes / 128;
       const unsigned char* src_base =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
-      for (int e = tid; e < m * PS * lines; e += NT) {
-        const int qo = e / lines, qq = qo >> psh;
+      for (int qq = tid; qq < m; qq += NT) {
         if (!(miss_i[qq] & HS_SLOT_MISS_FLAG)) continue;   // the appended token: already in its slot
-        const int pos = (sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG] << psh) + (qo & (PS - 1));
-        if (pos >= Np || (appended && pos == len)) continue;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(src_base + (size_t)pos * g.row_bytes + (e - qo * lines) * 128));
+        const int pos0 = sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG] << psh;
+        const int nr = min(PS, len - pos0);   // rows already in the host copy
+        if (nr > 0) bulk_prefetch_l2(src_base + (size_t)pos0 * g.row_bytes, (uint32_t)(nr * g.row_bytes));
       }
     }
 
@@ -1387,6 +1455,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     }
     if (pass > 0 && tid == 0) p.s.sh_armed[rlx] = 1;   // ready for the follower's call
     }   // passes
+    if (sel_out)
+      for (int i = tid; i < KR; i += NT) sel_out[i] = i < kkr ? row_pos(i) : -1;
     if (skip_rest) {
       __syncthreads();
       continue;

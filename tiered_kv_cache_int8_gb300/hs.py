@@ -58,7 +58,7 @@ class HsConfig(ctypes.Structure):
 class HsStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "hits", "misses", "h2d_bytes", "d2h_bytes", "decode_calls", "append_calls",
-        "host_bytes", "hot_bytes", "index_bytes", "meta_bytes", "full_selects")] + [
+        "host_bytes", "hot_bytes", "index_bytes", "meta_bytes", "host_huge_bytes", "full_selects")] + [
         ("device_error", ctypes.c_uint32), ("_pad", ctypes.c_uint32)]
 
     def as_dict(self) -> dict:
