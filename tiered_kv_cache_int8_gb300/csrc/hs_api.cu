@@ -377,7 +377,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.app_counter, R * 4, false},
       {(void**)&s.tiles_done, R * 4, false},
       {(void**)&s.ready, R * 4, false},
-      {(void**)&s.sync, 16, false},
+      {(void**)&s.sync, 32, false},
       {(void**)&s.sh_sel, cfg->index_share > 1 ? R * Lr * K * 4 : 16, false},
       {(void**)&s.sh_slots, cfg->index_share > 1 ? R * Lr * K * 4 : 16, false},
       {(void**)&s.sh_kk, R * Lr * 4, false},
@@ -395,6 +395,11 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
                                        " bytes failed: " + cudaGetErrorName(e));
     }
     if (a.meta) meta += a.bytes;
+    // every allocation starts zeroed (the specific initial values follow)
+    if (cudaMemsetAsync(*a.p, 0, a.bytes, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail_free(HS_ERR_CUDA, "hs_create: clearing a device allocation failed");
+    }
   }
   h->meta_bytes = meta;
 
@@ -417,7 +422,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.app_counter, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.tiles_done, 0, R * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.ready, 0, R * 4) == cudaSuccess;
-  ok = ok && cudaMemset(s.sync, 0, 16) == cudaSuccess;
+  ok = ok && cudaMemset(s.sync, 0, 32) == cudaSuccess;
   ok = ok && cudaMemset(s.sh_armed, 0, R * Lr * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.sh_kk, 0, R * Lr * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.sh_pend, 0xff, R * Lr * 4) == cudaSuccess;
@@ -426,9 +431,6 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
                  cudaSuccess;
 #endif
   ok = ok && hs::launch_init_order(s.order, (long long)(R * Lr), (int)B, 0) == cudaSuccess;
-  // the GPU reads every line of the host store once now, so that no decode step
-  // waits on a first read (those can take hundreds of microseconds)
-  ok = ok && hs::launch_touch_host(s.host_kv, h->host_bytes, h->num_sms, 0) == cudaSuccess;
   if (!ok) return fail_free(HS_ERR_CUDA, "hs_create: initialising the metadata failed");
   if ((e = hs::prepare_select(g, h->sel_smem)) != cudaSuccess ||
       (e = hs::prepare_attention(g, h->att_smem)) != cudaSuccess)

@@ -149,21 +149,6 @@ cudaError_t launch_page_bounds(const AppendParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// One read of every 128-byte line of the mapped host store, at create: the GPU's
-// first reads of host memory it has not read before can take hundreds of
-// microseconds each, and a decode step must not wait on them.
-__global__ void touch_host_kernel(const int4* p, long long lines) {
-  int acc = 0;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < lines; i += (long long)gridDim.x * blockDim.x)
-    acc ^= __ldcg(p + i * 8).x;
-  if (acc == 0x5eed1e) asm volatile("" ::"r"(acc));   // keep the loads
-}
-
-cudaError_t launch_touch_host(const void* p, size_t bytes, int num_sms, cudaStream_t st) {
-  touch_host_kernel<<<num_sms * 8, 256, 0, st>>>(static_cast<const int4*>(p), (long long)(bytes / 128));
-  return cudaGetLastError();
-}
-
 cudaError_t launch_init_order(int32_t* order, long long n_lists, int B, cudaStream_t st) {
   const long long total = n_lists * B;
   int blocks = (int)std::min<long long>((total + 255) / 256, 4096);

@@ -27,10 +27,15 @@
 //    contiguous hot slot) HBM -> shared memory with one 1-D bulk async copy into
 //    a row-padded layout (16 extra bytes per row put the 8 rows of an ldmatrix
 //    phase in 8 bank groups).  Warp 9 (fetcher) copies the unit's missed rows
-//    from the mapped pinned host copy with 16-byte cp.async (RESOLVE already
-//    started those rows moving into L2), so slow host reads never hold up the
-//    loader's own loads.  Up to 3 stages, full/empty mbarriers, a descriptor
-//    per stage.
+//    from the mapped pinned host copy with 16-byte cp.async, so slow host reads
+//    never hold up the loader's own loads.  Up to 3 stages, full/empty
+//    mbarriers, a descriptor per stage.
+//  * Warp 10 (prefetcher) claims requests in order (a global counter) and, once
+//    a request is published, starts every missed row of it moving over the host
+//    link into L2 (one bulk prefetch per row): the link is the scarce resource,
+//    so its reads start as early as the misses are known, and the fetchers later
+//    read L2.  (A bulk prefetch of host memory can hold its issuing thread for
+//    microseconds, so it runs on a warp of its own.)
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
 //    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
 //    with the group's query heads as the 16 M rows (zero-padded); K and V
@@ -60,7 +65,8 @@ constexpr int D = 128;
 constexpr int NCONS = 8;                   // consumer warps
 constexpr int LOADER = NCONS;              // warp index of the loader
 constexpr int FETCHER = NCONS + 1;         // warp index of the host fetcher
-constexpr int THREADS = (NCONS + 2) * 32;
+constexpr int PREFETCHER = NCONS + 2;      // warp index of the host-row prefetcher
+constexpr int THREADS = (NCONS + 3) * 32;
 constexpr int MAX_STAGES = 3;
 constexpr int TILE_MAX = 128;   // rows of a unit at h_kv = 1 (8 slices of 16)
 constexpr int CHUNK_ROWS_MIN = 64;
@@ -433,6 +439,39 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       HS_TRACE_VAL(p, 2, 11, tw_empty);
       HS_TRACE_VAL(p, 2, 12, (unsigned long long)n_items);
     }
+  } else if (warp == PREFETCHER) {
+    // =========================== prefetcher warp ===========================
+    for (;;) {
+      unsigned r = 0;
+      if (lane == 0) r = atomicAdd(&p.s.sync[4], 1u);
+      r = __shfl_sync(FULL_MASK, r, 0);
+      if (r >= (unsigned)p.n_req) break;
+      unsigned v = 0;
+      if (lane == 0) v = wait_counter(p.s.ready + r, 1u) ? ld_acquire(p.s.ready + r) : 0u;
+      v = __shfl_sync(FULL_MASK, v, 0);
+      if (v == 0u || *abort_flag) break;   // a publication that never came: the loader reports it
+      const int kk = (int)v - 1;
+      const int req = p.req_ids ? p.req_ids[r] : (int)r;
+      if (req < 0 || req >= g.max_requests) continue;
+      const long long rl = (long long)req * g.n_layers + p.layer;
+      const unsigned char* host =
+          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
+      const int32_t* sos = p.s.slot_of_sel + (long long)r * K;
+      const int32_t* selr = p.s.sel + (long long)r * K;
+      constexpr int PB = 8;   // slot entries in flight per lane
+      for (int i0 = lane; i0 < kk; i0 += 32 * PB) {
+        int sl[PB];
+#pragma unroll
+        for (int u = 0; u < PB; ++u) sl[u] = i0 + 32 * u < kk ? __ldcg(sos + i0 + 32 * u) : 0;
+#pragma unroll
+        for (int u = 0; u < PB; ++u)
+          if (sl[u] & HS_SLOT_MISS_FLAG) {
+            const int pos = __ldcg(selr + i0 + 32 * u);
+            if (pos >= 0 && pos < g.max_context)
+              bulk_prefetch_l2(host + (size_t)pos * g.row_bytes, (uint32_t)g.row_bytes);
+          }
+      }
+    }
   } else if (warp == FETCHER) {
     // ============================ fetcher warp ============================
     // Missed rows of each unit, from the mapped host copy straight into their
@@ -651,6 +690,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     if (prev + 1 == gridDim.x) {
       p.s.sync[2] = 0;
       p.s.sync[3] = 0;
+      p.s.sync[4] = 0;
     }
   }
   HS_TRACE(p, 2, 6);

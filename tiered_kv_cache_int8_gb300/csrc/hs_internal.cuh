@@ -95,9 +95,10 @@ struct DeviceState {
   int32_t* sh_kk;              // [R][L] k_eff
   int32_t* sh_pend;            // [R][L] slot awaiting the follower's own appended row (-1: none)
   int32_t* sh_armed;           // [R][L] 1: left by the lead of this step, not yet used
-  unsigned int* sync;          // [4]: 0 = CTAs of the select kernel past their set-up,
+  unsigned int* sync;          // [8]: 0 = CTAs of the select kernel past their set-up,
                                //      1 = resolvers finished, 2 = next attention work item,
-                               //      3 = attention CTAs finished
+                               //      3 = attention CTAs finished, 4 = next request whose
+                               //      missed rows the attention kernel prefetches
 };
 
 struct AppendParams {
@@ -179,7 +180,6 @@ namespace hs {
 // launchers (one per kernel translation unit); return a CUDA error code
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_page_bounds(const AppendParams& p, cudaStream_t st);
-cudaError_t launch_touch_host(const void* p, size_t bytes, int num_sms, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_select(const DecodeParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_follow(const DecodeParams& p, cudaStream_t st);

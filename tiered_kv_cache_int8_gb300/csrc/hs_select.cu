@@ -59,9 +59,9 @@
 //       request's ready flag = k_eff + 1 (release).  The attention kernel, launched
 //       as a programmatic dependent, starts on the requests that are ready while
 //       later ones are still being scored or resolved.
-//     - after publication: the L2 prefetch of every missed host row (the
-//       attention kernel's copies then read them from L2), stamps, the new LRU
-//       list, counters, step + 1 and the
+//     - after publication (the attention kernel's prefetcher warp starts the
+//       missed host rows moving into L2): the next threshold, stamps, the new
+//       LRU list, counters, step + 1 and the
 //       appended token (its key to the HBM store, its row to the pinned host
 //       copy, length + 1).  Lengths and thresholds are written only once every
 //       CTA of the launch has read them (a grid-wide counter).
@@ -1367,27 +1367,15 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // ======================= 4. publication =======================
     __syncthreads();
     HS_TRACE_IF(p, 1, 7, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
-    // the barrier above orders every thread's writes for this request before
-    // thread 0's release store (release is cumulative), which the attention
-    // kernel's acquire load pairs with
+    // every thread's writes for this request (ordered before thread 0 by the
+    // barrier above) are made visible GPU-wide by a full fence before the release
+    // store that the attention kernel's acquire load pairs with (the release
+    // store alone measured far slower on some machines)
     if (pass == 0 && p.publish && tid == 0) {
+      __threadfence();
       if (!(p.fault == 1 && ri == 0)) st_release(p.s.ready + ri, (unsigned)kkr + 1u);   // rows + 1
     }
     HS_TRACE_IF(p, 1, 16, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
-
-    // the missed rows the attention kernel will copy start moving over the link
-    // into L2 now, one bulk prefetch per row (page mode: per page), spread over
-    // the CTA (its later chunks then read them from L2)
-    if (pass == 0 && !pull && m > 0) {
-      const unsigned char* src_base =
-          reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rlx * g.max_context * g.row_bytes;
-      for (int qq = tid; qq < m; qq += NT) {
-        if (!(miss_i[qq] & HS_SLOT_MISS_FLAG)) continue;   // the appended token: already in its slot
-        const int pos0 = sel[miss_i[qq] & ~HS_SLOT_MISS_FLAG] << psh;
-        const int nr = min(PS, len - pos0);   // rows already in the host copy
-        if (nr > 0) bulk_prefetch_l2(src_base + (size_t)pos0 * g.row_bytes, (uint32_t)(nr * g.row_bytes));
-      }
-    }
 
     HS_TRACE_IF(p, 1, 12, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     // the next threshold to the exact key of rank k_next: the low digit of that
