@@ -74,7 +74,7 @@ constexpr int BAR_VOTE = 2;     // named barrier: the consumers' vote on a faile
 
 enum { DESC_UNIT = 0, DESC_STOP = 2 };
 struct __align__(16) Desc {
-  int type, ri, c, row0, nr, first, last, pad;
+  int type, ri, c, row0, nr, first, last, nmiss;   // nmiss: rows of the unit the fetcher copies
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         // the unit is row ur0 + i of the chunk, held by lane (ur0 + i) % 32 in
         // word (ur0 + i) / 32 of the chunk's batch (every lane joins every shuffle)
         int usl[NJU];
-        int hit_rows = 0;
+        int hit_rows = 0, miss_rows = 0;
 #pragma unroll
         for (int m = 0; m < NJU; ++m) {
           const int i = lane + 32 * m;
@@ -364,10 +364,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
           }
           usl[m] = (valid && !miss) ? sl : -1;
           hit_rows += __popc(__ballot_sync(FULL_MASK, valid && !miss));
+          miss_rows += __popc(__ballot_sync(FULL_MASK, miss));
         }
         __syncwarp();
         if (lane == 0) {
-          desc[s] = Desc{DESC_UNIT, r, c, ur0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, 0};
+          desc[s] = Desc{DESC_UNIT, r, c, ur0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, miss_rows};
           mbar_arrive(&dready[s]);   // the fetcher may read the descriptor and tables now
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&full[s], (uint32_t)(hit_rows * g.row_bytes));
@@ -519,15 +520,20 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
     int q_r = -1;
 
-    unsigned long long tw_full = 0;   // summed waits (trace builds only)
+    unsigned long long tw_full = 0, tw_full_miss = 0, n_miss_units = 0;   // summed waits (trace builds only)
     for (long long it = 0;; ++it) {
       const int s = (int)(it % nstage);
       const unsigned long long t0 = HS_TNOW();
       const bool ok = wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
                                     4 * WAIT_LIMIT_NS);
-      tw_full += HS_TNOW() - t0;
+      const unsigned long long tw = HS_TNOW() - t0;
+      tw_full += tw;
       if (named_sync_or(BAR_VOTE, NCONS * 32, !ok)) break;   // the consumers leave together
       const Desc dsc = desc[s];
+      if (dsc.type == DESC_UNIT && dsc.nmiss > 0) {
+        tw_full_miss += tw;
+        ++n_miss_units;
+      }
       if (dsc.type == DESC_STOP) break;
       const int r = dsc.ri;
       if (dsc.first) {
@@ -670,7 +676,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       }
     }
     HS_TRACE_IF(p, 2, 5, tid == 0);
-    if (tid == 0) HS_TRACE_VAL(p, 2, 13, tw_full);
+    if (tid == 0) {
+      HS_TRACE_VAL(p, 2, 13, tw_full);
+      HS_TRACE_VAL(p, 2, 15, tw_full_miss);
+      HS_TRACE_VAL(p, 2, 16, n_miss_units);
+    }
   }
 
   __syncthreads();
