@@ -326,8 +326,9 @@ int hs_reset_request(hs_handle_t* h, int32_t req, void* stream);
 #define HS_K_APPEND 0     /* append kernel (hs_append) */
 #define HS_K_SELECT 1     /* the select kernel of hs_decode_layer: scores, exact top-k and RESOLVE
                              (and the host fetch when fetch_mode = 1 or rows are latent) */
-#define HS_K_ATTENTION 2  /* attention with the merge of its partials (and the host fetch when
-                             fetch_mode = 0 or 2); latent rows: attention + merge kernels */
+#define HS_K_ATTENTION 2  /* the attention kernel, which also merges its partials (and does the
+                             host fetch when fetch_mode = 0 or 2); latent rows: attention +
+                             merge kernels */
 #define HS_K_COUNT 3
 int hs_set_timing(hs_handle_t* h, int32_t enable);
 int hs_kernel_times(hs_handle_t* h, double* ms /*[HS_K_COUNT]*/, int64_t* launches /*[HS_K_COUNT]*/);

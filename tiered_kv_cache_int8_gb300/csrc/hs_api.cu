@@ -377,6 +377,9 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.app_counter, R * 4, false},
       {(void**)&s.tiles_done, R * 4, false},
       {(void**)&s.ready, R * 4, false},
+      {(void**)&s.miss_cnt, R * 4, false},
+      {(void**)&s.att_done, R * 4, false},
+      {(void**)&s.miss_pos, R * K * 4, false},
       {(void**)&s.sync, 32, false},
       {(void**)&s.sh_sel, cfg->index_share > 1 ? R * Lr * K * 4 : 16, false},
       {(void**)&s.sh_slots, cfg->index_share > 1 ? R * Lr * K * 4 : 16, false},

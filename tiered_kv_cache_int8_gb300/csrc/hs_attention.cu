@@ -1,8 +1,8 @@
 // Sparse attention over the selected rows (GQA, head dim 128), fused with the
-// host fetch of the missed rows RESOLVE left to it: a persistent,
-// warp-specialised flash-decode kernel that works through a queue of chunks
-// while the select kernel is still resolving later requests, and the merge
-// kernel (further down) that combines its partials.
+// host fetch of the missed rows RESOLVE left to it and with the merge of its
+// partials: a persistent, warp-specialised flash-decode kernel that works
+// through a queue of chunks while the select kernel is still resolving later
+// requests.  The merge kernel further down serves latent rows.
 //
 // Method: "Heterogeneous LLM Serving with General-Purpose Processing-Near-Memory
 // for Retrieval-Based Sparse Attention" (vsvnakers.github.io), "核心公式与算法",
@@ -30,11 +30,11 @@
 //    from the mapped pinned host copy with 16-byte cp.async, so slow host reads
 //    never hold up the loader's own loads.  Up to 3 stages, full/empty
 //    mbarriers, a descriptor per stage.
-//  * Warp 10 (prefetcher) claims requests in order (a global counter) and, once
-//    a request is published, starts every missed row of it moving over the host
-//    link into L2 (one bulk prefetch per row): the link is the scarce resource,
-//    so its reads start as early as the misses are known, and the fetchers later
-//    read L2.  (A bulk prefetch of host memory can hold its issuing thread for
+//  * Warp 10 (prefetcher) claims requests in order (a global counter) and, as
+//    soon as RESOLVE has listed a request's misses (before it publishes the
+//    request), starts every missed row moving over the host link into L2 (one
+//    bulk prefetch per row): the link is the scarce resource, so its reads start
+//    as early as the misses are known, and the fetchers later read L2.  (A bulk prefetch of host memory can hold its issuing thread for
 //    microseconds, so it runs on a warp of its own.)
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
 //    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
@@ -43,16 +43,17 @@
 //    softmax in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P enters
 //    the second product as bf16.  Consumer warp 0 writes each fetched row into its
 //    hot slot (bulk shared -> global copy), so later steps hit.
-//  * Each (chunk, slice) writes a partial (m, l, o); the merge kernel, launched
-//    after this one, combines each head's partials in chunk order over many
-//    CTAs at once and writes bf16 (one CTA merging a whole request alone is a
-//    chain of dependent L2 round trips).  Rows are visited in ascending selection
-//    order and chunks depend only on k_eff, so the output is bit-identical for
-//    any B and any schedule.
+//  * Each (chunk, slice) writes a partial (m, l, o) and counts its chunk done
+//    (release).  A CTA out of chunks merges: items (request, 8 heads) in request
+//    order, each once its request's chunks are all counted; per head one warp
+//    finds the weights, then each thread sums one float4 of a head's output over
+//    the partials in chunk order.  Rows are visited in ascending selection order
+//    and chunks depend only on k_eff, so the output is bit-identical for any B and
+//    any schedule.  (Latent rows use the separate merge kernel further down.)
 //  * Counters of the call reset themselves: the last CTA to leave clears the
-//    queue, the merge kernel clears each request's ready flag.  Each CTA waits
-//    for the select kernel to complete before it exits, so the next launch on the
-//    stream sees both kernels finished.
+//    queues, the ready flags and the chunk counters.  Each CTA waits for the
+//    select kernel to complete before it exits, so the next launch on the stream
+//    sees both kernels finished.
 #include <cuda_bf16.h>
 
 #include "hs_internal.cuh"
@@ -71,6 +72,8 @@ constexpr int MAX_STAGES = 3;
 constexpr int TILE_MAX = 128;   // rows of a unit at h_kv = 1 (8 slices of 16)
 constexpr int CHUNK_ROWS_MIN = 64;
 constexpr int BAR_VOTE = 2;     // named barrier: the consumers' vote on a failed wait
+constexpr int BAR_CHUNK = 3;    // named barrier: the consumers at the end of a chunk
+constexpr int MERGE_HEADS = 8;  // heads per merge item (32 threads per head of 128 dims)
 
 enum { DESC_UNIT = 0, DESC_STOP = 2 };
 struct __align__(16) Desc {
@@ -447,30 +450,41 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       if (lane == 0) r = atomicAdd(&p.s.sync[4], 1u);
       r = __shfl_sync(FULL_MASK, r, 0);
       if (r >= (unsigned)p.n_req) break;
-      unsigned v = 0;
-      if (lane == 0) v = wait_counter(p.s.ready + r, 1u) ? ld_acquire(p.s.ready + r) : 0u;
-      v = __shfl_sync(FULL_MASK, v, 0);
-      if (v == 0u || *abort_flag) break;   // a publication that never came: the loader reports it
-      const int kk = (int)v - 1;
+      // the resolver's miss list, which it writes before publication; a request
+      // published without one (fetch mode 1: RESOLVE pulled its rows) is skipped
+      unsigned mc = 0, rd = 0;
+      if (lane == 0) {
+        const unsigned long long t0 = global_timer_ns();
+        unsigned ns = 32;
+        for (uint32_t it = 1;; ++it) {
+          mc = *reinterpret_cast<volatile const unsigned*>(p.s.miss_cnt + r);
+          rd = ld_acquire(p.s.ready + r);
+          if (mc != 0u || rd != 0u) break;
+          __nanosleep(ns);
+          if (ns < 512) ns <<= 1;
+          if ((it & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
+        if (mc == 0u && rd != 0u) mc = *reinterpret_cast<volatile const unsigned*>(p.s.miss_cnt + r);
+      }
+      mc = __shfl_sync(FULL_MASK, mc, 0);
+      rd = __shfl_sync(FULL_MASK, rd, 0);
+      if ((mc == 0u && rd == 0u) || *abort_flag) break;   // a publication that never came: the loader reports it
+      if (mc == 0u) continue;
+      const int n = min((int)mc - 1, K);
       const int req = p.req_ids ? p.req_ids[r] : (int)r;
       if (req < 0 || req >= g.max_requests) continue;
       const long long rl = (long long)req * g.n_layers + p.layer;
       const unsigned char* host =
           reinterpret_cast<const unsigned char*>(p.s.host_kv) + (size_t)rl * g.max_context * g.row_bytes;
-      const int32_t* sos = p.s.slot_of_sel + (long long)r * K;
-      const int32_t* selr = p.s.sel + (long long)r * K;
-      constexpr int PB = 8;   // slot entries in flight per lane
-      for (int i0 = lane; i0 < kk; i0 += 32 * PB) {
-        int sl[PB];
-#pragma unroll
-        for (int u = 0; u < PB; ++u) sl[u] = i0 + 32 * u < kk ? __ldcg(sos + i0 + 32 * u) : 0;
-#pragma unroll
-        for (int u = 0; u < PB; ++u)
-          if (sl[u] & HS_SLOT_MISS_FLAG) {
-            const int pos = __ldcg(selr + i0 + 32 * u);
-            if (pos >= 0 && pos < g.max_context)
-              bulk_prefetch_l2(host + (size_t)pos * g.row_bytes, (uint32_t)g.row_bytes);
-          }
+      const int32_t* mp = p.s.miss_pos + (long long)r * K;
+      const int psh = g.page_shift;
+      for (int i = lane; i < n; i += 32) {
+        const int u = __ldcg(mp + i);   // a missed unit: a position, or a page of 2^psh
+        if (u < 0) continue;            // the appended token: its row is not in the host copy yet
+        const long long pos0 = (long long)u << psh;
+        if (pos0 >= g.max_context) continue;
+        const long long nr = min((long long)1 << psh, (long long)g.max_context - pos0);
+        bulk_prefetch_l2(host + pos0 * g.row_bytes, (uint32_t)(nr * g.row_bytes));
       }
     }
   } else if (warp == FETCHER) {
@@ -673,6 +687,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
             *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
           if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
         }
+        // every consumer warp has written its part of the chunk: count it done
+        named_sync(BAR_CHUNK, NCONS * 32);
+        if (tid == 0) {
+          __threadfence();
+          red_release_add(p.s.att_done + r, 1u);
+        }
       }
     }
     HS_TRACE_IF(p, 2, 5, tid == 0);
@@ -684,7 +704,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   }
 
   __syncthreads();
-  if (*abort_flag) {
+  const bool aborted = *abort_flag != 0;
+  if (aborted) {
     // drain copies that may still be in flight (bounded) before the buffers go away
     if (tid == 0) {
       for (int s2 = 0; s2 < nstage; ++s2) {
@@ -694,13 +715,108 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     }
     __syncthreads();
   }
-  // the last CTA to leave resets the queue (every CTA has taken its last item)
+
+  // ---- merge: (request, group of MERGE_HEADS heads) items in request order,
+  // each once every chunk of its request is written; the stage memory is free now
+  __shared__ int s_item, s_ok;
+  constexpr int HPM = HQ < MERGE_HEADS ? HQ : MERGE_HEADS;
+  constexpr int NHG = HQ / HPM;
+  float* wsm = reinterpret_cast<float*>(stage);   // [parts][HPM] merge weights
+  float* Ms = wsm + (size_t)NPARTS * HPM;          // [HPM]
+  float* Ls = Ms + HPM;                            // [HPM]
+  while (!aborted) {
+    if (tid == 0) s_item = (int)atomicAdd(&p.s.sync[5], 1u);
+    __syncthreads();
+    const int item = s_item;
+    if (item >= p.n_req * NHG) break;
+    const int r = item / NHG, h0 = (item % NHG) * HPM;
+    if (tid == 0) {
+      s_ok = wait_counter(p.s.att_done + r, (unsigned)NCHK) ? 1 : 0;
+      if (!s_ok) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
+    }
+    __syncthreads();
+    const int rdy = (int)__ldcg(p.s.ready + r);
+    const int kk = max(0, rdy - 1);
+    const int nparts = ((kk + CR - 1) / CR) * NSLICE;
+    uint16_t* outp = p.out + ((long long)r * HQ + h0) * D;
+    if (!s_ok || nparts == 0) {   // nothing selected (or never published): the output is defined as 0
+      for (int e = tid; e < HPM * D; e += THREADS) outp[e] = 0;
+      __syncthreads();
+      continue;
+    }
+    const float* pml = p.s.part_ml + (long long)r * NPARTS * HQ * 2;
+    const float* po = p.s.part_o + (long long)r * NPARTS * HQ * D;
+    // per head (one warp each): M = max_q m_q, w_q = 2^(m_q - M), L = sum_q w_q l_q
+    if (warp < HPM) {
+      const int h = h0 + warp;
+      float mx = -INFINITY;
+      for (int q = lane; q < nparts; q += 32) mx = fmaxf(mx, __ldcg(pml + ((long long)q * HQ + h) * 2));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+      float l = 0.f;
+      for (int q = lane; q < nparts; q += 32) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + (long long)q * HQ + h);
+        const float w = exp2f(ml.x - mx);
+        wsm[q * HPM + warp] = w;
+        l = fmaf(ml.y, w, l);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(FULL_MASK, l, o);
+      if (lane == 0) {
+        Ms[warp] = mx;
+        Ls[warp] = l;
+      }
+    }
+    __syncthreads();
+    // out = (sum_q w_q o_q) / L, parts in order, one float4 of a head's dims per thread
+    if (tid < HPM * (D / 4)) {
+      const int hh = tid / (D / 4), d4 = tid % (D / 4);
+      const float4* col = reinterpret_cast<const float4*>(po + (long long)(h0 + hh) * D) + d4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      constexpr int UQ = 8;   // parts in flight per thread
+      for (int q = 0; q < nparts; q += UQ) {
+        float4 v[UQ];
+#pragma unroll
+        for (int u = 0; u < UQ; ++u)
+          v[u] = q + u < nparts ? __ldcg(col + (long long)(q + u) * HQ * D / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < UQ; ++u)
+          if (q + u < nparts) {
+            const float w = wsm[(q + u) * HPM + hh];
+            acc.x = fmaf(w, v[u].x, acc.x);
+            acc.y = fmaf(w, v[u].y, acc.y);
+            acc.z = fmaf(w, v[u].z, acc.z);
+            acc.w = fmaf(w, v[u].w, acc.w);
+          }
+      }
+      const float inv = 1.f / Ls[hh];
+      uint2 packed;
+      packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(outp + (long long)hh * D + 4 * d4) = packed;
+    }
+    __syncthreads();   // wsm, Ms, Ls and s_item are reused
+  }
+
+  // the last CTA to leave resets the call's queues, counters and flags (every
+  // CTA has taken its last item and merged its last request by then)
+  __shared__ int s_last;
   if (tid == 0) {
     const unsigned prev = atom_acq_rel_add(&p.s.sync[3], 1u);
-    if (prev + 1 == gridDim.x) {
+    s_last = prev + 1 == gridDim.x;
+  }
+  __syncthreads();
+  if (s_last) {
+    for (int r = tid; r < p.n_req; r += THREADS) {
+      p.s.ready[r] = 0;
+      p.s.miss_cnt[r] = 0;
+      p.s.att_done[r] = 0;
+    }
+    if (tid == 0) {
       p.s.sync[2] = 0;
       p.s.sync[3] = 0;
       p.s.sync[4] = 0;
+      p.s.sync[5] = 0;
     }
   }
   HS_TRACE(p, 2, 6);
@@ -728,7 +844,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(DecodeParams p) {
   griddep_wait();   // the attention kernel's partials
   griddep_launch_dependents();
   const int nparts = p.s.att_nparts[(long long)ri * (HQ / GH) + h0 / GH];
-  if (!p.g.shared_kv && blockIdx.x == 0 && tid == 0) p.s.ready[ri] = 0;   // this call is done with the request
+  if (!p.g.shared_kv && blockIdx.x == 0 && tid == 0) {   // this call is done with the request
+    p.s.ready[ri] = 0;
+    p.s.miss_cnt[ri] = 0;
+  }
   if (nparts <= 0) {   // nothing selected: the output is defined as 0
     if (!p.g.shared_kv)
       for (int e = tid; e < HPC * DV; e += blockDim.x) p.out[((long long)ri * HQ + h0) * DV + e] = 0;
@@ -838,9 +957,7 @@ static cudaError_t run_gqa(const DecodeParams* p, size_t smem, cudaStream_t st) 
   if (p == nullptr)   // prepare: allow the shared memory this shape needs
     return allow_smem(kern, smem);
   const int ns = attention_stages(p->g, 227 * 1024);
-  cudaError_t e = launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);
-  if (e != cudaSuccess) return e;
-  return launch_merge(*p, st);
+  return launch_pdl(kern, dim3(p->att_grid), dim3(THREADS), smem, st, *p, ns);   // merges its own partials
 }
 
 template <int HKV>

@@ -88,6 +88,12 @@ struct DeviceState {
   // is reset by the last party that reads it)
   unsigned int* tiles_done;    // [R] score tiles of request i finished (select kernel)
   unsigned int* ready;         // [R] k_eff + 1 once request i's selection and slots are published
+  // the units request i misses this call, listed by RESOLVE as soon as they are
+  // known (before publication) for the attention kernel's host-row prefetch: a
+  // hint only (written and read without ordering; every entry is bounds-checked)
+  unsigned int* miss_cnt;      // [R] misses listed + 1 (0: not yet)
+  unsigned int* att_done;      // [R] chunks of request i whose partials the attention kernel has written
+  int32_t* miss_pos;           // [R][k] unit index of each listed miss
   // a selection shared by a group of layers (index_share > 1): what the group's
   // lead call leaves for each follower layer [R][L][...]
   int32_t* sh_sel;             // [R][L][k] the shared selection (positions, ascending)
@@ -98,7 +104,8 @@ struct DeviceState {
   unsigned int* sync;          // [8]: 0 = CTAs of the select kernel past their set-up,
                                //      1 = resolvers finished, 2 = next attention work item,
                                //      3 = attention CTAs finished, 4 = next request whose
-                               //      missed rows the attention kernel prefetches
+                               //      missed rows the attention kernel prefetches, 5 = next
+                               //      merge item of the attention kernel
 };
 
 struct AppendParams {

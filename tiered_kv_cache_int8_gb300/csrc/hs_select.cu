@@ -1157,8 +1157,14 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
     const int2 mc = block_exclusive_scan2<NT>(nm, nc, sh.scan, &m, nullptr);
     int mb = mc.x;
+    // the misses the attention kernel will fetch go to its prefetcher at once
+    const bool list_misses = pass == 0 && !pull && p.publish;
+    int32_t* mpos = p.s.miss_pos + (long long)ri * KR;
     for (int i = i0; i < i1; ++i)
-      if (slot_sel[i] < 0) miss_i[mb++] = i;
+      if (slot_sel[i] < 0) {
+        if (list_misses && i < kk) mpos[mb] = (!paged && appended && sel[i] == len) ? -1 : sel[i];
+        miss_i[mb++] = i;
+      }
     if (p.replacement == HS_REPLACE_RANDOM) {
       // victims: the m unpinned slots ranked first (never-filled, then smallest
       // (key, slot)), in ascending slot order.  Two 12-bit digit selections over
@@ -1221,6 +1227,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
     }
     __syncthreads();
+    if (list_misses && tid == 0) p.s.miss_cnt[ri] = (unsigned)(m - extra) + 1u;   // a hint: no ordering
     HS_TRACE_IF(p, 1, 6, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
     // evict, then record the new residents (stores only); slot of every selected
     // row, misses flagged when the attention kernel copies them
