@@ -627,18 +627,10 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "dtype_detail": "int8 indexer (int32 accumulate); bf16 K/V and q, fp32 softmax/accumulate",
         "data": "synthetic (seeded; N(0,1) bf16 K/V, uniform int8 index keys, random-walk int8 queries)",
-        "config": {"workload": w.name, "requests": R, "layers": L, "context": int(n0[0]) if w.context_range is None
-                   else [int(n0.min()), int(n0.max())], "h_q": w.h_q, "h_kv": w.h_kv, "d_qk": w.d_qk,
-                   "d_v": w.d_v, "d_idx": w.d_idx, "top_k": w.top_k, "hot_slots": w.hot_slots,
-                   "sigma": w.sigma, "parallelism": f"requests sharded, {world} independent cache(s)",
-                   "l2": f"inputs larger than L2: {hbm_total / K / 2**20:.0f} MiB read per step > 129 MiB",
-                   "timed": "one CUDA graph of the timed steps, uploaded beforehand, replayed once"
-                   if uploaded and uploaded[0] else "one CUDA graph of the timed steps, replayed once (not "
-                   "uploaded beforehand: this torch does not expose the executable graph)",
-                   "fetch_mode": args.fetch_mode, "replacement": args.replacement,
-                   **({"index_share": args.index_share, "share_prefetch": args.share_prefetch}
-                      if args.index_share > 1 else {}),
-                   **({"page_size": args.page_size} if args.page_size > 1 else {})},
+        "config": workload_config(w, args, world),
+        "timed": "one CUDA graph of the timed steps, uploaded beforehand, replayed once"
+        if uploaded and uploaded[0] else "one CUDA graph of the timed steps, replayed once (not "
+        "uploaded beforehand: this torch does not expose the executable graph)",
         "kernel_timing": {"mode": timing_mode, "steps": K, "ms_per_step": round(ms_total_b / K, 4),
                           "miss_rate": round(misses_b / max(1, hits_b + misses_b), 5),
                           "note": "the K steps after the headline's, each kernel bracketed by CUDA events "
@@ -745,6 +737,23 @@ def main():
         dist.destroy_process_group()
 
 
+def workload_config(w: wl.Workload, args, world: int) -> dict:
+    """The workload and method settings both arms report (the same dict)."""
+    n0 = w.contexts()
+    ab = algorithmic_bytes(w, n0, 0.0, page_size=args.page_size)   # one layer-step, no misses
+    step_mib = w.n_layers * sum(ab["hbm"].values()) / 2**20
+    return {"workload": w.name, "requests": w.n_requests, "layers": w.n_layers,
+            "context": int(n0[0]) if w.context_range is None else [int(n0.min()), int(n0.max())],
+            "h_q": w.h_q, "h_kv": w.h_kv, "d_qk": w.d_qk, "d_v": w.d_v, "d_idx": w.d_idx, "top_k": w.top_k,
+            "hot_slots": w.hot_slots, "sigma": w.sigma,
+            "parallelism": f"requests sharded, {world} independent cache(s)",
+            "l2": f"inputs larger than L2: at least {step_mib:.0f} MiB read per step > 129 MiB",
+            "fetch_mode": args.fetch_mode, "replacement": args.replacement,
+            **({"index_share": args.index_share, "share_prefetch": args.share_prefetch}
+               if args.index_share > 1 else {}),
+            **({"page_size": args.page_size} if args.page_size > 1 else {})}
+
+
 def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
     """The CPU oracle as the reference arm: each step runs the oracle on a
     bounded sample (sr requests x sl layers, one decode step each) and the rate
@@ -784,12 +793,13 @@ def run_reference(args, w: wl.Workload, sr: int, sl: int, ss: int) -> dict:
               f"scaled by {w.n_requests} requests per layer-step")
     # one step of this arm is the bounded sample (sr x sl request-layer-steps), so
     # ms_per_step is its measured time; value scales the rate to the whole batch
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 0,
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
             "steps": K, "warmup": W, "ms_per_step": round(per_unit * sr * sl * 1e3, 2),
             "step": f"a sample of {sr} request(s) x {sl} layer(s) of one decode step (value is scaled to "
                     f"{w.n_requests} requests per layer-step)",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": w.name},
+            "data": "synthetic (seeded)", "config": workload_config(w, args, args.gpus),
+            "timed": "the CPU oracle (numpy, fp64 / int64) on the host's cores, a bounded sample per step",
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -28,8 +28,9 @@
 //    request order and cut into warp tiles (two sub-tiles of 8 x 16-byte loads
 //    per lane); scorer warp w takes tiles w, w + W, w + 2W, ... so all warps
 //    sweep the requests in order and request r is complete early.  The DRAM
-//    stream is driven by bulk L2 prefetches two rounds of tiles ahead (the
-//    first two rounds before the grid dependency resolves); the tile itself is
+//    stream is driven by bulk L2 prefetches two rounds of tiles ahead (before
+//    the grid dependency resolves, each warp already loads its first tile and
+//    sends its second towards L2: the keys are the library's own); the tile is
 //    read with coalesced 16-byte loads (the 8 lanes of a position read its
 //    8 chunks side by side) that then hit L2, issued only after the previous
 //    tile's release so that its fence does not wait for them; dp4a partial
@@ -318,22 +319,6 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       __syncthreads();
       return carry;
     };
-    // Before the grid dependency resolves: the tile map from the state as it
-    // stands and the first two rounds of this CTA's tiles into L2, overlapping
-    // the previous kernel's tail.  Only prefetch hints come of it (every address
-    // stays inside the stores whatever it read); the map is rebuilt after the wait.
-    {
-      const int total0 = build_tables();
-      if (w0 < total0) prefetch_tile(w0, req_of(w0, 0));
-      if (w0 + W < total0) prefetch_tile(w0 + W, req_of(w0 + W, 0));
-      __syncthreads();   // the tables are rebuilt below
-    }
-    griddep_wait();   // lengths, keys, metadata and scratch of earlier stream work
-    griddep_launch_dependents();
-    const int total = build_tables();
-    // this CTA has read every length and threshold it needs
-    if (tid == 0) red_release_add(&p.s.sync[0], 1u);
-    HS_TRACE(p, 0, 1);
 
     // lane roles inside a load instruction
     const int pg = lane / SG::LPP;            // position within the instruction
@@ -381,12 +366,46 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
     };
 
-    int r_cur = 0;
+    // Before the grid dependency resolves: the tile map from the state as it
+    // stands (the library's own lengths and keys, which no kernel still running
+    // writes), this warp's first tile into registers and its second towards L2,
+    // overlapping the previous kernel's tail.  The map is rebuilt after the wait;
+    // the first tile is loaded again if its place in the map changed, and is
+    // loaded only then if it holds this call's appended token (whose key is the
+    // caller's input, which may come from the kernel just before).
     int4 va[SG::LD], vb[SG::LD];
+    int pre_req = -1, pre_n = -1, pre_off = -1;
+    {
+      const int total0 = build_tables();
+      if (w0 < total0) {
+        const int ri0 = req_of(w0, 0);
+        pre_n = t_n[ri0];
+        pre_off = (w0 - t_prefix[ri0]) * SG::TILE;
+        const int newu = p.new_kv ? (pre_n - 1) >> psh : -1;
+        if (newu < pre_off || newu >= pre_off + SG::TILE) {
+          pre_req = t_req[ri0];
+          load_sub(w0, ri0, 0, va);
+          load_sub(w0, ri0, 1, vb);
+        }
+      }
+      if (w0 + W < total0) prefetch_tile(w0 + W, req_of(w0 + W, 0));
+      __syncthreads();   // the tables are rebuilt below
+    }
+    griddep_wait();   // lengths, keys, metadata and scratch of earlier stream work
+    griddep_launch_dependents();
+    const int total = build_tables();
+    // this CTA has read every length and threshold it needs
+    if (tid == 0) red_release_add(&p.s.sync[0], 1u);
+    HS_TRACE(p, 0, 1);
+    int r_cur = 0;
     if (w0 < total) {
       r_cur = req_of(w0, 0);
-      load_sub(w0, r_cur, 0, va);
-      load_sub(w0, r_cur, 1, vb);
+      const bool same = pre_req >= 0 && t_req[r_cur] == pre_req && t_n[r_cur] == pre_n &&
+                        (w0 - t_prefix[r_cur]) * SG::TILE == pre_off;
+      if (!same) {
+        load_sub(w0, r_cur, 0, va);
+        load_sub(w0, r_cur, 1, vb);
+      }
     }
     for (int t = w0; t < total; t += W) {
       const int ri = r_cur;
