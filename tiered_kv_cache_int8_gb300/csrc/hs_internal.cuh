@@ -28,7 +28,7 @@ constexpr int RES_THREADS = 1024;    // top-k CTA of the static (no-allocation) 
 // scoring groups, a resolver CTA runs the top-k + RESOLVE chain of its requests.
 constexpr int SEL_THREADS = 512;
 constexpr int SEL_GROUP = 256;       // threads of one scoring group
-constexpr int SEL_MAX_RESOLVERS = 16;
+constexpr int SEL_MAX_RESOLVERS = 32;
 constexpr int ROLE_SELECT = 0, ROLE_GIVEN = 1;
 
 // slot_of_sel entries of rows RESOLVE left for the attention kernel to fetch
