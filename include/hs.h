@@ -254,7 +254,7 @@ int hs_append(hs_handle_t* h, int32_t layer, int32_t n_req, const int32_t* req_i
  * before it reads anything; the attention kernel is launched as its
  * programmatic dependent and starts on each request as soon as that request is
  * resolved, and completes only after the select kernel has.  So ordering against
- * earlier and later stream work is the usual one.  At most 16 requests are
+ * earlier and later stream work is the usual one.  At most 32 requests are
  * resolved at a time (one resolver CTA each); the rest of the GPU scores.
  *   req_ids     : dev int32 [n_req] distinct request ids, or NULL for 0..n_req-1
  *   q_idx       : dev int8 [n_req][d_idx]       indexer query (16-byte aligned); with
