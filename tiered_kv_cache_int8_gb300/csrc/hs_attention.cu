@@ -41,8 +41,9 @@
 //    with the group's query heads as the 16 M rows (zero-padded); K and V
 //    fragments come from shared memory with ldmatrix (.trans for V).  Online
 //    softmax in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P enters
-//    the second product as bf16.  Consumer warp 0 writes each fetched row into its
-//    hot slot (bulk shared -> global copy), so later steps hit.
+//    the second product as bf16.  Once a unit has landed, the fetcher writes the
+//    rows it fetched into their hot slots (bulk shared -> global copy), so later
+//    steps hit; a stage is released by the 8 consumers and the fetcher.
 //  * Each (chunk, slice) writes a partial (m, l, o) and counts its chunk done
 //    (release).  A CTA out of chunks merges: items (request, 8 heads) in request
 //    order, each once its request's chunks are all counted; per head one warp
@@ -78,6 +79,7 @@ constexpr int MERGE_HEADS = 8;  // heads per merge item (32 threads per head of 
 enum { DESC_UNIT = 0, DESC_STOP = 2 };
 struct __align__(16) Desc {
   int type, ri, c, row0, nr, first, last, nmiss;   // nmiss: rows of the unit the fetcher copies
+  int nxt, pad0, pad1, pad2;                       // nxt: the next chunk's request (last unit), or -1
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -144,6 +146,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// The transpose of an 8x8 b16 matrix held in the mma fragment layout (lane l:
+// row l / 4, columns 2 (l % 4) and +1), returned in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -162,6 +172,7 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* smem_src, uint3
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
       mbar_init(&full[s], 2);      // the loader's arrival (with the hit bytes) and the fetcher's
-      mbar_init(&empty[s], NCONS);
+      mbar_init(&empty[s], NCONS + 1);   // the consumers and the fetcher
       mbar_init(&dready[s], 1);
     }
     *abort_flag = 0;
@@ -371,7 +382,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
         }
         __syncwarp();
         if (lane == 0) {
-          desc[s] = Desc{DESC_UNIT, r, c, ur0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, miss_rows};
+          const int nxt = (u == nunits - 1 && pf_item >= 0) ? (int)(pf_item / NCHK) : -1;
+          desc[s] = Desc{DESC_UNIT, r, c, ur0, unr, u == 0 ? 1 : 0, u == nunits - 1 ? 1 : 0, miss_rows, nxt, 0, 0, 0};
           mbar_arrive(&dready[s]);   // the fetcher may read the descriptor and tables now
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&full[s], (uint32_t)(hit_rows * g.row_bytes));
@@ -432,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     }
     // no more work: tell the fetcher and the consumers
     if (!dead && take_stage() && lane == 0) {
-      desc[s] = Desc{DESC_STOP, 0, 0, 0, 0, 0, 0, 0};
+      desc[s] = Desc{DESC_STOP, 0, 0, 0, 0, 0, 0, 0, -1, 0, 0, 0};
       mbar_arrive(&dready[s]);
       mbar_arrive(&full[s]);
     }
@@ -520,8 +532,34 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       cp_async_mbar_arrive(&full[s]);   // balanced: completes when this lane's copies land
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
+      if (dsc.nmiss > 0) {
+        // once the unit has landed, the fetched rows go on into their hot slots
+        // (bulk shared -> global), so later steps hit; the stage is released only
+        // after these copies have read it
+        if (!__all_sync(FULL_MASK, wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag,
+                                                 p.s.dev_error, 4 * WAIT_LIMIT_NS)))
+          break;
+        const int* tab = slot_tab + s * TILE_MAX;
+        unsigned char* hotw = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
+        fence_proxy_async_smem();   // cp.async writes -> async-proxy reads
+        bool any = false;
+        for (int i = lane; i < TILE; i += 32) {
+          const int slot = tab[i];
+          if (slot >= 0 && slot < g.hot_slots) {
+            any = true;
+            bulk_s2g(hotw + (size_t)slot * g.row_bytes, st_s + (size_t)i * row_stride, (uint32_t)g.row_bytes);
+          }
+        }
+        if (any) {
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
     cp_async_wait_all();
+    bulk_wait_all();   // the hot-slot writes of the fetched rows are complete before the CTA goes on
     if (lane == 0) HS_TRACE_VAL(p, 2, 14, n_fetched);
   } else {
     // ============================ consumer warps ============================
@@ -529,18 +567,38 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     const int slice = warp / HKV;
     const int gq = lane >> 2, tq = lane & 3;
     const float sl2 = p.scale_log2;
-    uint32_t qa[8][4];
-    float o[16][4];
-    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;   // heads gq and gq + 8
+    // Transposed products, so that a unit's 16 rows are the mma's M and the
+    // group's query heads its N (8 per n-tile, NT tiles): S^T = K Q^T, then
+    // O^T = V^T P^T with P^T moved into the B layout by movmatrix.  With at most
+    // 8 heads per kv head that is half the tensor work of heads-as-M.
+    constexpr int NT = (G + 7) / 8;
+    uint32_t qb[NT][8][2], qn[NT][8][2];   // Q^T as the B operand; qn: the next chunk's, loaded ahead
+    int qn_r = -1;
+    auto load_q = [&](uint32_t (&qd)[NT][8][2], int r) {
+      const uint16_t* qg = p.q + ((long long)r * HQ + kvh * G) * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = nt * 8 + gq;   // head (B column) of this lane
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int d0 = ks * 16 + 2 * tq;
+          qd[nt][ks][0] = h < G ? *reinterpret_cast<const uint32_t*>(qg + h * D + d0) : 0u;
+          qd[nt][ks][1] = h < G ? *reinterpret_cast<const uint32_t*>(qg + h * D + d0 + 8) : 0u;
+        }
+      }
+    };
+    float ot[NT][8][4];   // O^T: dims 16m + gq (+8) x heads nt * 8 + 2tq (+1)
+    float mh[NT][2], lh[NT][2];   // per head 2tq, 2tq + 1 of each n-tile: running max, partial sum
     int q_r = -1;
 
-    unsigned long long tw_full = 0, tw_full_miss = 0, n_miss_units = 0;   // summed waits (trace builds only)
+    unsigned long long tw_full = 0, tw_full_miss = 0, n_miss_units = 0, t_busy = 0;   // trace builds only
     for (long long it = 0;; ++it) {
       const int s = (int)(it % nstage);
       const unsigned long long t0 = HS_TNOW();
       const bool ok = wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
                                     4 * WAIT_LIMIT_NS);
-      const unsigned long long tw = HS_TNOW() - t0;
+      const unsigned long long t1 = HS_TNOW();
+      const unsigned long long tw = t1 - t0;
       tw_full += tw;
       if (named_sync_or(BAR_VOTE, NCONS * 32, !ok)) break;   // the consumers leave together
       const Desc dsc = desc[s];
@@ -553,140 +611,136 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       if (dsc.first) {
         if (r != q_r) {
           q_r = r;
-          // the group's query heads as the mma A operand (rows >= G are zero)
-          const uint16_t* qg = p.q + ((long long)r * HQ + kvh * G) * D;
+          if (r == qn_r) {   // loaded during the previous chunk's last unit
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const int d0 = ks * 16 + 2 * tq;
-            qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qg + gq * D + d0) : 0u;
-            qa[ks][1] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (gq + 8) * D + d0) : 0u;
-            qa[ks][2] = gq < G ? *reinterpret_cast<const uint32_t*>(qg + gq * D + d0 + 8) : 0u;
-            qa[ks][3] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (gq + 8) * D + d0 + 8) : 0u;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                qb[nt][ks][0] = qn[nt][ks][0];
+                qb[nt][ks][1] = qn[nt][ks][1];
+              }
+          } else {
+            load_q(qb, r);
           }
         }
 #pragma unroll
-        for (int t = 0; t < 16; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-        m_lo = m_hi = -INFINITY;
-        l_lo = l_hi = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) ot[nt][m][0] = ot[nt][m][1] = ot[nt][m][2] = ot[nt][m][3] = 0.f;
+          mh[nt][0] = mh[nt][1] = -INFINITY;
+          lh[nt][0] = lh[nt][1] = 0.f;
+        }
       }
       const int nv = max(0, min(ATT_SUBTILE, dsc.nr - slice * ATT_SUBTILE));
       HS_TRACE_IF(p, 2, 4, tid == 0 && it == 0);
       const unsigned char* st_s = stage + (size_t)s * L.stage_bytes;
       if (nv > 0) {
         const int rbase = slice * ATT_SUBTILE;
-        // ---- S = Q K^T over the 16 rows (two n-tiles of 8 rows) ----
-        float sc[2][4];
+        // ---- S^T = K Q^T: A = the 16 rows' K (8 k-steps of 16 dims), loaded first ----
+        uint32_t fr[8][4];
+        {
+          const uint32_t rowa =
+              smem_addr(st_s + (size_t)(rbase + (lane & 7) + 8 * ((lane >> 3) & 1)) * row_stride);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-          const uint32_t rowa = smem_addr(st_s + (size_t)(rbase + 8 * j + (lane & 7)) * row_stride);
-#pragma unroll
-          for (int kp = 0; kp < 4; ++kp) {
-            // four 8x8 matrices: K rows 8j..8j+7, dims 32kp + 8*(lane/8) .. +7
-            uint32_t b[4];
-            ldsm_x4(b, rowa + (uint32_t)((kvh * D + 32 * kp + 8 * (lane >> 3)) * 2));
-            mma_bf16(sc[j], qa[2 * kp], b[0], b[1]);
-            mma_bf16(sc[j], qa[2 * kp + 1], b[2], b[3]);
-          }
+          for (int ks = 0; ks < 8; ++ks) ldsm_x4(fr[ks], rowa + (uint32_t)((kvh * D + 16 * ks + 8 * (lane >> 4)) * 2));
         }
-        // ---- online softmax; rows >= nv are masked out ----
-        float mx_lo = -INFINITY, mx_hi = -INFINITY;
+        float sc[NT][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int nt = 0; nt < NT; ++nt) {
+          float sx[4] = {0.f, 0.f, 0.f, 0.f};   // two accumulation chains
+          sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 8; ks += 2) {
+            mma_bf16(sc[nt], fr[ks], qb[nt][ks][0], qb[nt][ks][1]);
+            mma_bf16(sx, fr[ks + 1], qb[nt][ks + 1][0], qb[nt][ks + 1][1]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] += sx[e];
+        }
+        // ---- online softmax per head (a column: rows gq, gq + 8 of the 8 lanes with this tq);
+        // rows >= nv are masked out ----
+        const bool ok0 = gq < nv, ok1 = gq + 8 < nv;
+        uint32_t pt[NT][2];   // P^T as the B operand (rows 0-7 | 8-15 x head gq)
+        bool rescale = false;
+        float al[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float mx[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const bool okr = 8 * j + 2 * tq + e < nv;
-            sc[j][e] = okr ? sc[j][e] * sl2 : -INFINITY;
-            sc[j][2 + e] = okr ? sc[j][2 + e] * sl2 : -INFINITY;
-            mx_lo = fmaxf(mx_lo, sc[j][e]);
-            mx_hi = fmaxf(mx_hi, sc[j][2 + e]);
+            sc[nt][e] = ok0 ? sc[nt][e] * sl2 : -INFINITY;
+            sc[nt][2 + e] = ok1 ? sc[nt][2 + e] * sl2 : -INFINITY;
+            mx[e] = fmaxf(sc[nt][e], sc[nt][2 + e]);
+            mx[e] = fmaxf(mx[e], __shfl_xor_sync(FULL_MASK, mx[e], 4));
+            mx[e] = fmaxf(mx[e], __shfl_xor_sync(FULL_MASK, mx[e], 8));
+            mx[e] = fmaxf(mx[e], __shfl_xor_sync(FULL_MASK, mx[e], 16));
+            // padded heads (>= G) see all-zero scores, never -inf: every m stays finite
+            const float mn = fmaxf(mh[nt][e], mx[e]);
+            al[nt][e] = exp2f(mh[nt][e] - mn);   // -inf - x -> 0
+            mh[nt][e] = mn;
+            rescale |= al[nt][e] != 1.f;
           }
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL_MASK, mx_lo, 1));
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL_MASK, mx_lo, 2));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL_MASK, mx_hi, 1));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL_MASK, mx_hi, 2));
-        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        // padded heads (>= G) see all-zero scores, never -inf: every m stays finite
-        const float a_lo = exp2f(m_lo - mn_lo), a_hi = exp2f(m_hi - mn_hi);   // -inf - x -> 0
-        m_lo = mn_lo;
-        m_hi = mn_hi;
-        uint32_t pa[4];
-        float ps_lo = 0.f, ps_hi = 0.f;
+          const float p0 = exp2f(sc[nt][0] - mh[nt][0]), p1 = exp2f(sc[nt][1] - mh[nt][1]);
+          const float p2 = exp2f(sc[nt][2] - mh[nt][0]), p3 = exp2f(sc[nt][3] - mh[nt][1]);
+          lh[nt][0] = lh[nt][0] * al[nt][0] + (p0 + p2);
+          lh[nt][1] = lh[nt][1] * al[nt][1] + (p1 + p3);
+          pt[nt][0] = movmatrix_trans(pack_bf16(p0, p1));   // rows 0-7
+          pt[nt][1] = movmatrix_trans(pack_bf16(p2, p3));   // rows 8-15
+        }
+        if (__any_sync(FULL_MASK, rescale)) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float p0 = exp2f(sc[j][0] - mn_lo), p1 = exp2f(sc[j][1] - mn_lo);
-          const float p2 = exp2f(sc[j][2] - mn_hi), p3 = exp2f(sc[j][3] - mn_hi);
-          ps_lo += p0 + p1;
-          ps_hi += p2 + p3;
-          pa[2 * j + 0] = pack_bf16(p0, p1);
-          pa[2 * j + 1] = pack_bf16(p2, p3);
-        }
-        l_lo = l_lo * a_lo + ps_lo;
-        l_hi = l_hi * a_hi + ps_hi;
-        if (__any_sync(FULL_MASK, a_lo != 1.f || a_hi != 1.f)) {
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            o[t][0] *= a_lo;
-            o[t][1] *= a_lo;
-            o[t][2] *= a_hi;
-            o[t][3] *= a_hi;
-          }
+            for (int m = 0; m < 8; ++m) {
+              ot[nt][m][0] *= al[nt][0];
+              ot[nt][m][1] *= al[nt][1];
+              ot[nt][m][2] *= al[nt][0];
+              ot[nt][m][3] *= al[nt][1];
+            }
         }
-        // ---- O += P V: 16 n-tiles of 8 dims, k = the 16 rows ----
-        const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
-        const uint32_t rowv = smem_addr(st_s + (size_t)(rbase + (lane & 7) + 8 * ((lane >> 3) & 1)) * row_stride);
+        // ---- O^T += V^T P^T: A = V^T of 16 dims x the 16 rows (ldmatrix .trans), loaded first ----
+        {
+          const uint32_t rowv =
+              smem_addr(st_s + (size_t)(rbase + (lane & 7) + 8 * (lane >> 4)) * row_stride);
 #pragma unroll
-        for (int tp = 0; tp < 8; ++tp) {
-          // four 8x8 matrices: (rows 0-7 | 8-15) x (dims 16tp..+7 | 16tp+8..+15), transposed
-          uint32_t b[4];
-          ldsm_x4_t(b, rowv + (uint32_t)((g.v_off + kvh * D + 16 * tp + 8 * (lane >> 4)) * 2));
-          mma_bf16(o[2 * tp], pfrag, b[0], b[1]);
-          mma_bf16(o[2 * tp + 1], pfrag, b[2], b[3]);
+          for (int m = 0; m < 8; ++m)
+            ldsm_x4_t(fr[m], rowv + (uint32_t)((g.v_off + kvh * D + 16 * m + 8 * ((lane >> 3) & 1)) * 2));
         }
-      }
-      // consumer warp 0 writes the rows fetched for this unit into their hot slots
-      if (warp == 0) {
-        const int* tab = slot_tab + s * TILE_MAX;
-        const int req = p.req_ids ? p.req_ids[r] : r;
-        const long long rl = (long long)req * g.n_layers + p.layer;
-        unsigned char* hotw = reinterpret_cast<unsigned char*>(p.s.hot) + (size_t)rl * g.hot_slots * g.row_bytes;
-        bool any = false;
-        for (int i = lane; i < TILE; i += 32) {
-          const int slot = tab[i];
-          if (slot >= 0 && slot < g.hot_slots) {
-            if (!any) fence_proxy_async_smem();   // cp.async writes -> async-proxy reads
-            any = true;
-            bulk_s2g(hotw + (size_t)slot * g.row_bytes, st_s + (size_t)i * row_stride, (uint32_t)g.row_bytes);
-          }
-        }
-        if (any) {
-          bulk_commit();
-          bulk_wait_read_all();   // the stage may be refilled only after these reads
-        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int m = 0; m < 8; ++m) mma_bf16(ot[nt][m], fr[m], pt[nt][0], pt[nt][1]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      t_busy += HS_TNOW() - t1;
+      if (NT == 1 && dsc.last && dsc.nxt >= 0 && dsc.nxt != r && dsc.nxt != qn_r) {   // the next chunk's query, ahead
+        load_q(qn, dsc.nxt);
+        qn_r = dsc.nxt;
+      }
       if (dsc.last) {   // the chunk's partial (m, l, o) for this slice
-        float ll = l_lo + __shfl_xor_sync(FULL_MASK, l_lo, 1);
-        ll += __shfl_xor_sync(FULL_MASK, ll, 2);
-        float lh = l_hi + __shfl_xor_sync(FULL_MASK, l_hi, 1);
-        lh += __shfl_xor_sync(FULL_MASK, lh, 2);
         const int part = dsc.c * NSLICE + slice;
         float* po = p.s.part_o + ((long long)r * NPARTS + part) * HQ * D;
         float* pml = p.s.part_ml + ((long long)r * NPARTS + part) * HQ * 2;
-        const int h_lo = kvh * G + gq, h_hi = kvh * G + gq + 8;
-        if (gq < G) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            *reinterpret_cast<float2*>(po + (long long)h_lo * D + 8 * t + 2 * tq) = make_float2(o[t][0], o[t][1]);
-          if (tq == 0) *reinterpret_cast<float2*>(pml + h_lo * 2) = make_float2(m_lo, ll);
-        }
-        if (gq + 8 < G) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            *reinterpret_cast<float2*>(po + (long long)h_hi * D + 8 * t + 2 * tq) = make_float2(o[t][2], o[t][3]);
-          if (tq == 0) *reinterpret_cast<float2*>(pml + h_hi * 2) = make_float2(m_hi, lh);
-        }
+          for (int e = 0; e < 2; ++e) {
+            float l = lh[nt][e];   // the sum over all 16 rows: this lane holds rows gq, gq + 8
+            l += __shfl_xor_sync(FULL_MASK, l, 4);
+            l += __shfl_xor_sync(FULL_MASK, l, 8);
+            l += __shfl_xor_sync(FULL_MASK, l, 16);
+            const int hl = nt * 8 + 2 * tq + e;   // head within the group
+            if (hl < G) {
+              float* ph = po + (long long)(kvh * G + hl) * D;
+#pragma unroll
+              for (int m = 0; m < 8; ++m) {
+                ph[16 * m + gq] = ot[nt][m][e];
+                ph[16 * m + gq + 8] = ot[nt][m][2 + e];
+              }
+              if (gq == 0) *reinterpret_cast<float2*>(pml + (kvh * G + hl) * 2) = make_float2(mh[nt][e], l);
+            }
+          }
         // every consumer warp has written its part of the chunk: count it done
         named_sync(BAR_CHUNK, NCONS * 32);
         if (tid == 0) {
@@ -700,6 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       HS_TRACE_VAL(p, 2, 13, tw_full);
       HS_TRACE_VAL(p, 2, 15, tw_full_miss);
       HS_TRACE_VAL(p, 2, 16, n_miss_units);
+      HS_TRACE_VAL(p, 2, 17, t_busy);
     }
   }
 
