@@ -251,6 +251,29 @@ def resolve_pulls(fetch_mode: int, shared_kv: bool) -> bool:
     return shared_kv or fetch_mode == 1
 
 
+def attention_timeline(st0: dict, st1: dict, n_launch: int, n_cta: int):
+    """Host-link exposure and load balance of the GQA attention kernel between two
+    hs_stats snapshots (None for latent rows, which record nothing).  A consumer
+    warp per CTA times its wait for every stage of rows; a stage holding a row read
+    from host memory waits longer than one of HBM rows only, and that excess, summed
+    over a CTA's host stages, is the link time the CTA could not hide."""
+    d = {k: st1[k] - st0[k] for k in ("att_host_wait_ns", "att_host_stages", "att_hbm_wait_ns", "att_hbm_stages")}
+    if d["att_host_stages"] + d["att_hbm_stages"] == 0 or n_launch == 0:
+        return None
+    hbm_mean = d["att_hbm_wait_ns"] / max(1, d["att_hbm_stages"])
+    host_mean = d["att_host_wait_ns"] / max(1, d["att_host_stages"])
+    exposed = max(0.0, d["att_host_wait_ns"] - d["att_host_stages"] * hbm_mean)
+    span, med = st1["att_last_span_ns"], st1["att_last_median_ns"]
+    return {"host_stage_wait_us": round(host_mean / 1e3, 3), "hbm_stage_wait_us": round(hbm_mean / 1e3, 3),
+            "host_stages_per_cta_layer": round(d["att_host_stages"] / (n_launch * n_cta), 2),
+            "link_exposed_us_per_cta_layer": round(exposed / (n_launch * n_cta) / 1e3, 3),
+            "last_launch_span_us": round(span / 1e3, 2), "last_launch_median_cta_end_us": round(med / 1e3, 2),
+            "span_over_median": round(span / med, 3) if med else None,
+            "note": "consumer waits per stage of 16 rows, summed over CTAs; exposed = host-stage waits minus "
+                    "the mean HBM-stage wait per host stage; span and median CTA end from the first CTA's start "
+                    "of the timed region's last attention launch"}
+
+
 def graph_upload(g, stream) -> bool:
     """Uploads an instantiated CUDA graph to the device (cudaGraphUpload) so
     that the timed replay does not pay the first launch's upload; False when the
@@ -642,6 +665,7 @@ def run_hisparse(args, w: wl.Workload, rank: int, world: int, dev_index: int) ->
         "miss_rate": round(misses / max(1, hits + misses), 5),
         "full_select_frac": round((st1["full_selects"] - st0["full_selects"]) / max(1, K * L * R), 4),
         "misses_per_layer_step": round(misses / (K * L), 1),
+        "attention_timeline": attention_timeline(st0, st1, K * L, torch.cuda.get_device_properties(dev).multi_processor_count),
         "step_roofline": {"t_roof_ms": round(t_roof * 1e3 / K, 4), "t_meas_ms": round(ms_step, 4),
                           "frac": round(step_frac, 4), "hbm_bytes_per_step": int(hbm_total / K),
                           "link_bytes_per_step": int(link_total / K),

@@ -192,6 +192,19 @@ typedef struct hs_stats {
                                 long on them as on base pages) */
   uint64_t full_selects;  /* selections that scanned every key (no usable candidate list:
                              first steps, a large drift, contexts above 20 k positions) */
+  /* Timing of the GQA attention kernel, from the device's global timer (latent-row
+     calls add nothing).  One consumer warp per CTA times its waits for each stage
+     of rows: stages holding at least one row read from host memory count as
+     "host", the others as "hbm"; the difference of their mean waits is the host
+     link's exposed latency per host stage. */
+  uint64_t att_host_wait_ns;  /* summed over CTAs and calls: waits for host stages */
+  uint64_t att_host_stages;   /* host stages waited for */
+  uint64_t att_hbm_wait_ns;   /* summed over CTAs and calls: waits for hbm stages */
+  uint64_t att_hbm_stages;    /* hbm stages waited for */
+  uint64_t att_last_span_ns;  /* the latest GQA attention launch: its last CTA's end minus
+                                 its first CTA's start (0 before the first launch) */
+  uint64_t att_last_median_ns;  /* the same launch: the median CTA end minus the first
+                                   CTA's start (load balance: span / median) */
   uint32_t device_error;  /* HS_DEVERR_* bits seen so far (sticky) */
   uint32_t _pad;
 } hs_stats_t;

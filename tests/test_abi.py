@@ -122,3 +122,23 @@ def test_plain_c_caller(L, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert "abi_from_c: ok" in r.stdout
+
+
+def header_struct_fields(name):
+    """(type, field) pairs of `typedef struct <name> { ... }` in include/hs.h."""
+    text = open(os.path.join(ROOT, "include", "hs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    body = re.search(r"typedef struct " + name + r"\s*\{(.*?)\}\s*" + name + r"_t;", text, flags=re.S).group(1)
+    return re.findall(r"\b(int32_t|uint32_t|uint64_t|float)\s+(\w+)\s*;", body)
+
+
+@pytest.mark.parametrize("struct, cls", [("hs_config", "HsConfig"), ("hs_stats", "HsStats")])
+def test_binding_structs_follow_the_header(struct, cls):
+    # the ctypes mirrors must list the header's fields in order, with the same types
+    from tiered_kv_cache_int8_gb300 import hs
+    ctype = {"int32_t": ctypes.c_int32, "uint32_t": ctypes.c_uint32, "uint64_t": ctypes.c_uint64,
+             "float": ctypes.c_float}
+    want = [(f, ctype[t]) for t, f in header_struct_fields(struct)]
+    got = list(getattr(hs, cls)._fields_)
+    assert [f for f, _ in got] == [f for f, _ in want]
+    assert [t for _, t in got] == [t for _, t in want]

@@ -627,3 +627,30 @@ def test_follower_without_its_lead_is_reported():
     assert cache.stats()["device_error"] & hs.HS_DEVERR_NO_LEAD
     assert not out.view(torch.int16).any()
     cache.close()
+
+
+def test_attention_timeline_counters():
+    # the GQA attention kernel's stage waits and CTA timeline (hs_stats): the first
+    # step misses every selected row, so host stages are seen; latent rows record
+    # nothing
+    w = wl.make_workload("batch16_32k", n_requests=3, n_layers=2, context=5003, top_k=256, hot_slots=512,
+                         steps=4)
+    cache = make_cache(w, 4)
+    prefill(cache, w)
+    run_steps(cache, w, StepInputs(w, 4), 4)
+    st = cache.stats()
+    cache.close()
+    assert st["device_error"] == 0
+    assert st["att_host_stages"] > 0 and st["att_host_wait_ns"] > 0
+    assert st["att_hbm_stages"] > 0
+    # 3 requests x 256 rows in 16-row stages, 2 layers x 4 steps
+    assert st["att_host_stages"] + st["att_hbm_stages"] == 3 * 256 // 16 * 2 * 4
+    assert 0 < st["att_last_median_ns"] <= st["att_last_span_ns"] < 10**9
+    w = wl.make_workload("mla_128k", n_requests=2, n_layers=1, context=3000, h_q=16, top_k=256, hot_slots=256,
+                         steps=2)
+    cache = make_cache(w, 2)
+    prefill(cache, w)
+    run_steps(cache, w, StepInputs(w, 2), 2)
+    st = cache.stats()
+    cache.close()
+    assert st["att_host_stages"] + st["att_hbm_stages"] == 0 and st["att_last_span_ns"] == 0

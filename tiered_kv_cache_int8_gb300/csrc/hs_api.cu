@@ -361,13 +361,15 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
       {(void**)&s.step, R * Lr * 4, true},
       {(void**)&s.hits, R * Lr * 8, true},
       {(void**)&s.misses, R * Lr * 8, true},
-      {(void**)&s.glob, 4 * 8, true},
+      {(void**)&s.glob, 8 * 8, true},
+      {(void**)&s.att_cta, (size_t)h->num_sms * 16, false},
       {(void**)&s.dev_error, 16, true},
       {(void**)&s.scores, R * (size_t)h->score_stride * 4, false},
       {(void**)&s.hist, R * (size_t)hs::IDX_BINS * 4, false},
       {(void**)&s.cand_thr, R * Lr * 4, true},
       {(void**)&s.cand_cnt, R * 4, false},
       {(void**)&s.cand, R * 2 * K * 8, false},
+      {(void**)&s.cand_slot, R * 2 * K * 4, false},
       {(void**)&s.sel, R * K * 4, false},
       {(void**)&s.slot_of_sel, R * K * 4, false},
       {(void**)&s.part_o, R * (size_t)h->att_parts * g.h_q * g.d_v * 4, false},
@@ -414,7 +416,7 @@ int hs_create(const hs_config_t* cfg, hs_handle_t** out) {
   ok = ok && cudaMemset(s.step, 0, R * Lr * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.hits, 0, R * Lr * 8) == cudaSuccess;
   ok = ok && cudaMemset(s.misses, 0, R * Lr * 8) == cudaSuccess;
-  ok = ok && cudaMemset(s.glob, 0, 32) == cudaSuccess;
+  ok = ok && cudaMemset(s.glob, 0, 64) == cudaSuccess;
   ok = ok && cudaMemset(s.dev_error, 0, 16) == cudaSuccess;
   ok = ok && cudaMemset(s.slot_of_sel, 0, R * K * 4) == cudaSuccess;
   ok = ok && cudaMemset(s.att_nparts, 0, R * 8 * 4) == cudaSuccess;
@@ -571,11 +573,12 @@ int hs_stats(hs_handle_t* h, hs_stats_t* out) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(h, e, "hs_stats: synchronize");
   const size_t RL = (size_t)h->cfg.max_requests * h->cfg.n_layers;
-  std::vector<unsigned long long> hits(RL), misses(RL), glob(4);
+  std::vector<unsigned long long> hits(RL), misses(RL), glob(8), cta(2 * (size_t)h->num_sms);
   unsigned int err = 0;
   if ((e = cudaMemcpy(hits.data(), h->s.hits, RL * 8, cudaMemcpyDeviceToHost)) != cudaSuccess ||
       (e = cudaMemcpy(misses.data(), h->s.misses, RL * 8, cudaMemcpyDeviceToHost)) != cudaSuccess ||
-      (e = cudaMemcpy(glob.data(), h->s.glob, 32, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(glob.data(), h->s.glob, 64, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(cta.data(), h->s.att_cta, cta.size() * 8, cudaMemcpyDeviceToHost)) != cudaSuccess ||
       (e = cudaMemcpy(&err, h->s.dev_error, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(h, e, "hs_stats: copy");
   std::memset(out, 0, sizeof(*out));
@@ -592,6 +595,27 @@ int hs_stats(hs_handle_t* h, hs_stats_t* out) {
   out->index_bytes = h->index_bytes;
   out->meta_bytes = h->meta_bytes;
   out->full_selects = glob[2];
+  out->att_host_wait_ns = glob[4];
+  out->att_host_stages = glob[5];
+  out->att_hbm_wait_ns = glob[6];
+  out->att_hbm_stages = glob[7];
+  // the latest launch's CTA timeline (a CTA that has not run yet holds zeros)
+  {
+    std::vector<unsigned long long> ends;
+    unsigned long long first = ~0ull, last = 0;
+    for (int b = 0; b < h->num_sms; ++b) {
+      const unsigned long long t0 = cta[2 * b], t1 = cta[2 * b + 1];
+      if (t0 == 0 || t1 < t0) continue;
+      first = std::min(first, t0);
+      last = std::max(last, t1);
+      ends.push_back(t1);
+    }
+    if (!ends.empty()) {
+      std::sort(ends.begin(), ends.end());
+      out->att_last_span_ns = last - first;
+      out->att_last_median_ns = ends[ends.size() / 2] - first;
+    }
+  }
   out->host_huge_bytes = h->host_huge_bytes;
   out->device_error = err;
   if (err) return set_err(h, HS_ERR_DEVICE, "hs_stats: device error word " + std::to_string(err));

@@ -240,6 +240,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   const int row_stride = g.row_bytes + ATT_ROW_PAD;
   const int rvec = g.row_bytes / 16;
   HS_TRACE(p, 2, 0);
+  // this CTA's timeline and its consumers' stage waits (hs_stats): thread 0,
+  // a consumer, times them
+  __shared__ unsigned long long s_wait[5];   // host ns, host stages, hbm ns, hbm stages, CTA start
 
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
@@ -248,6 +251,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
       mbar_init(&dready[s], 1);
     }
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) s_wait[i] = 0;
+    s_wait[4] = global_timer_ns();
     fence_mbar_init();
   }
   // no griddepcontrol.wait here: everything the select kernel writes for a
@@ -591,20 +596,21 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     float mh[NT][2], lh[NT][2];   // per head 2tq, 2tq + 1 of each n-tile: running max, partial sum
     int q_r = -1;
 
-    unsigned long long tw_full = 0, tw_full_miss = 0, n_miss_units = 0, t_busy = 0;   // trace builds only
+    unsigned long long tw_full = 0, t_busy = 0;   // trace builds only
     for (long long it = 0;; ++it) {
       const int s = (int)(it % nstage);
-      const unsigned long long t0 = HS_TNOW();
+      const unsigned long long t0 = tid == 0 ? global_timer_ns() : 0ull;
       const bool ok = wait_or_abort(&full[s], (uint32_t)((it / nstage) & 1), abort_flag, p.s.dev_error,
                                     4 * WAIT_LIMIT_NS);
-      const unsigned long long t1 = HS_TNOW();
+      const unsigned long long t1 = tid == 0 ? global_timer_ns() : 0ull;
       const unsigned long long tw = t1 - t0;
       tw_full += tw;
       if (named_sync_or(BAR_VOTE, NCONS * 32, !ok)) break;   // the consumers leave together
       const Desc dsc = desc[s];
-      if (dsc.type == DESC_UNIT && dsc.nmiss > 0) {
-        tw_full_miss += tw;
-        ++n_miss_units;
+      if (tid == 0 && dsc.type == DESC_UNIT) {
+        const int k = dsc.nmiss > 0 ? 0 : 2;
+        s_wait[k] += tw;
+        s_wait[k + 1] += 1;
       }
       if (dsc.type == DESC_STOP) break;
       const int r = dsc.ri;
@@ -752,8 +758,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     HS_TRACE_IF(p, 2, 5, tid == 0);
     if (tid == 0) {
       HS_TRACE_VAL(p, 2, 13, tw_full);
-      HS_TRACE_VAL(p, 2, 15, tw_full_miss);
-      HS_TRACE_VAL(p, 2, 16, n_miss_units);
+      HS_TRACE_VAL(p, 2, 15, s_wait[0]);
+      HS_TRACE_VAL(p, 2, 16, s_wait[1]);
       HS_TRACE_VAL(p, 2, 17, t_busy);
     }
   }
@@ -857,6 +863,18 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
   // CTA has taken its last item and merged its last request by then)
   __shared__ int s_last;
   if (tid == 0) {
+    if (s_wait[1]) {
+      red_add_u64(&p.s.glob[4], s_wait[0]);
+      red_add_u64(&p.s.glob[5], s_wait[1]);
+    }
+    if (s_wait[3]) {
+      red_add_u64(&p.s.glob[6], s_wait[2]);
+      red_add_u64(&p.s.glob[7], s_wait[3]);
+    }
+    if ((int)blockIdx.x < p.att_grid) {
+      p.s.att_cta[2 * blockIdx.x] = s_wait[4];
+      p.s.att_cta[2 * blockIdx.x + 1] = global_timer_ns();
+    }
     const unsigned prev = atom_acq_rel_add(&p.s.sync[3], 1u);
     s_last = prev + 1 == gridDim.x;
   }

@@ -67,7 +67,9 @@ struct DeviceState {
   int32_t* step;           // [R][L]
   unsigned long long* hits;    // [R][L]
   unsigned long long* misses;  // [R][L]
-  unsigned long long* glob;    // [0] h2d bytes, [1] d2h bytes, [2] selections over every key
+  unsigned long long* glob;    // [0] h2d bytes, [1] d2h bytes, [2] selections over every key,
+                               // [4..7] attention stage waits: host ns, host stages, hbm ns, hbm stages
+  unsigned long long* att_cta;  // [att_grid][2] (start, end) global-timer ns of each attention CTA, latest launch
   unsigned int* dev_error;     // sticky HS_DEVERR_* bits
   // scratch (one call in flight per handle)
   uint32_t* scores;        // [R][score_stride] 24-bit keys of the current call
@@ -77,6 +79,7 @@ struct DeviceState {
   uint32_t* cand_thr;      // [R][L] threshold for the next call (0: none)
   uint32_t* cand_cnt;      // [R] keys listed in the current call (zero between calls)
   uint2* cand;             // [R][2k] (position, key), unordered
+  int32_t* cand_slot;      // [R][2k] page-table entry of each listed unit, read by the scorer that lists it
   int32_t* sel;            // [R][k]
   int32_t* slot_of_sel;    // [R][k]
   float* part_o;           // [R][parts][h_q][d_v]

@@ -366,6 +366,23 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
     };
 
+    // page-table entries of the units this lane owns in tile t (request ri), for
+    // the candidates it lists: the resolver then needs no page-table gathers on
+    // its critical path.  Read after the grid dependency only (the page table is
+    // earlier stream work's), and only for requests that list candidates.
+    auto load_pg = [&](int t, int ri, int (&pv)[2][SG::OWN]) {
+      const int NU = (t_n[ri] + PS - 1) >> psh;
+      const int u0 = (t - t_prefix[ri]) * SG::TILE;
+      const int32_t* page_rl = p.s.page + ((long long)t_req[ri] * g.n_layers + p.layer) * g.max_context;
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+#pragma unroll
+        for (int o = 0; o < SG::OWN; ++o) {
+          const int pos = u0 + half * SG::SUB + (o * SG::LPP + cl) * SG::PPI + pg;
+          pv[half][o] = (t_thr[ri] != 0u && pos < NU) ? __ldcg(page_rl + pos) : -1;
+        }
+    };
+
     // Before the grid dependency resolves: the tile map from the state as it
     // stands (the library's own lengths and keys, which no kernel still running
     // writes), this warp's first tile into registers and its second towards L2,
@@ -398,6 +415,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     if (tid == 0) red_release_add(&p.s.sync[0], 1u);
     HS_TRACE(p, 0, 1);
     int r_cur = 0;
+    int pgv[2][SG::OWN];   // page-table entries of this lane's units in the current tile
     if (w0 < total) {
       r_cur = req_of(w0, 0);
       const bool same = pre_req >= 0 && t_req[r_cur] == pre_req && t_n[r_cur] == pre_n &&
@@ -406,6 +424,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
         load_sub(w0, r_cur, 0, va);
         load_sub(w0, r_cur, 1, vb);
       }
+      load_pg(w0, r_cur, pgv);
     }
     for (int t = w0; t < total; t += W) {
       const int ri = r_cur;
@@ -515,8 +534,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
 #pragma unroll
             for (int o = 0; o < SG::OWN; ++o) {
               const unsigned at = base + __popc(mk[half][o] & below);
-              if (((mk[half][o] >> lane) & 1u) && at < 2u * (unsigned)KR)
+              if (((mk[half][o] >> lane) & 1u) && at < 2u * (unsigned)KR) {
                 p.s.cand[(long long)ri * 2 * KR + at] = make_uint2((uint32_t)ownp[half][o], ownk[half][o]);
+                p.s.cand_slot[(long long)ri * 2 * KR + at] = pgv[half][o];
+              }
               base += __popc(mk[half][o]);
             }
         }
@@ -530,6 +551,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       if (tn < total) {
         load_sub(tn, rn, 0, va);
         load_sub(tn, rn, 1, vb);
+        load_pg(tn, rn, pgv);
       }
       HS_TRACE_IF(p, 0, 3, tid == 0 && t == w0);
       HS_TRACE_IF(p, 0, 4, tid == 0 && t == w0 + W);
@@ -669,16 +691,17 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       for (int i = tid; i < N; i += NT) sel[i] = i;
     } else if (use_cand) {
       const int cnt = sh.cnt;
-      const int32_t* page_rl = p.s.page + rl * g.max_context;
       const int NWd = (N + 31) >> 5;
       uint32_t* gtw = bitmap;                         // [NWd] positions whose key is above the k-th
       uint32_t* tiw = bitmap + FAST_MAX_N / 32;       // [NWd] positions whose key equals it
       uint16_t* gpre = reinterpret_cast<uint16_t*>(smem_raw + L.wpre);   // [NWd] above-threshold positions before each word
       uint16_t* epre = gpre + FAST_MAX_N / 32;                           // [NWd] ties before each word (all < 2^16)
       int cpg[CAND_REG];
-      // every selected position is a candidate: its page entry is the hit test
+      // every selected position is a candidate: its page entry, listed with it by
+      // the scorer, is the hit test
+      const int32_t* csl = p.s.cand_slot + (long long)ri * 2 * KR;
 #pragma unroll
-      for (int j = 0; j < CAND_REG; ++j) cpg[j] = tid + j * NT < cnt ? page_rl[cv[j].x] : -1;
+      for (int j = 0; j < CAND_REG; ++j) cpg[j] = tid + j * NT < cnt ? __ldcg(csl + tid + j * NT) : -1;
       for (int c = tid; c < IDX_BINS / 4; c += NT) reinterpret_cast<uint4*>(h)[c] = make_uint4(0, 0, 0, 0);
       for (int w = tid; w < NWd; w += NT) {
         gtw[w] = 0u;

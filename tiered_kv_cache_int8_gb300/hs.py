@@ -58,7 +58,9 @@ class HsConfig(ctypes.Structure):
 class HsStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "hits", "misses", "h2d_bytes", "d2h_bytes", "decode_calls", "append_calls",
-        "host_bytes", "hot_bytes", "index_bytes", "meta_bytes", "host_huge_bytes", "full_selects")] + [
+        "host_bytes", "hot_bytes", "index_bytes", "meta_bytes", "host_huge_bytes", "full_selects",
+        "att_host_wait_ns", "att_host_stages", "att_hbm_wait_ns", "att_hbm_stages", "att_last_span_ns",
+        "att_last_median_ns")] + [
         ("device_error", ctypes.c_uint32), ("_pad", ctypes.c_uint32)]
 
     def as_dict(self) -> dict:
