@@ -381,6 +381,10 @@ __device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, 
 
 // Starts bringing `bytes` (a multiple of 16) at a 16-byte aligned global address
 // into L2; a hint: no data returns and nothing waits on it.
+// The 128-byte line holding `gsrc` towards L2 (no alignment needed).
+__device__ __forceinline__ void prefetch_line_l2(const void* gsrc) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(gsrc));
+}
 __device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }

@@ -166,11 +166,23 @@ struct SelShared {
 __device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* scan, int* out_b, int* out_above,
                                              int kneed2 = 0, int* out_b2 = nullptr, int* out_above2 = nullptr) {
   constexpr int PER = IDX_BINS / NT;   // bins per thread, descending
+  static_assert(PER % 4 == 0, "whole 16-byte groups of bins per thread");
   const int tid = threadIdx.x;
   const int top = IDX_BINS - 1 - tid * PER;
+  // the thread's bins top - PER + 1 .. top, read as 16-byte vectors (a lane
+  // stride of PER words would otherwise conflict on the shared-memory banks)
+  uint32_t hb[PER];
+#pragma unroll
+  for (int c = 0; c < PER / 4; ++c) {
+    const uint4 x = reinterpret_cast<const uint4*>(h + top - PER + 1)[c];
+    hb[4 * c] = x.x;
+    hb[4 * c + 1] = x.y;
+    hb[4 * c + 2] = x.z;
+    hb[4 * c + 3] = x.w;
+  }
   int v = 0;
 #pragma unroll
-  for (int j = 0; j < PER; ++j) v += (int)h[top - j];
+  for (int j = 0; j < PER; ++j) v += (int)hb[j];
   int tot;
   const int ex = block_exclusive_scan<NT>(v, scan, &tot);
   auto find = [&](int kn, int* ob, int* oa) {
@@ -178,7 +190,7 @@ __device__ __forceinline__ void select_digit(const uint32_t* h, int kneed, int* 
       int acc = ex;
 #pragma unroll
       for (int j = 0; j < PER; ++j) {
-        const int hv = (int)h[top - j];
+        const int hv = (int)hb[PER - 1 - j];   // bin top - j
         if (acc < kn && kn <= acc + hv) {
           *ob = top - j;
           *oa = acc;
@@ -282,10 +294,16 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       const int NU = (t_n[ri] + PS - 1) >> psh;
       const int u0 = (t - t_prefix[ri]) * SG::TILE;
       const int nu = min(SG::TILE, NU - u0);
-      if (lane != 0 || nu <= 0) return;
+      if (nu <= 0) return;
       const long long rl = (long long)t_req[ri] * g.n_layers + p.layer;
-      const int8_t* base = paged ? p.s.pbound + rl * (long long)g.max_pages * d : p.s.idx_keys + rl * g.max_context * d;
-      bulk_prefetch_l2(base + (long long)u0 * d, (uint32_t)(nu * d));
+      if (lane == 0) {
+        const int8_t* base =
+            paged ? p.s.pbound + rl * (long long)g.max_pages * d : p.s.idx_keys + rl * g.max_context * d;
+        bulk_prefetch_l2(base + (long long)u0 * d, (uint32_t)(nu * d));
+      } else if (t_thr[ri] != 0u && lane * 32 - 32 < nu) {
+        // the tile's page-table entries (read for the candidates it lists), 32 a line
+        prefetch_line_l2(p.s.page + rl * g.max_context + u0 + (lane * 32 - 32));
+      }
     };
     // warp tiles of every request that needs a selection; returns their number
     auto build_tables = [&]() {
@@ -1189,24 +1207,39 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       break;
     }
     HS_TRACE_IF(p, 1, 5, tid == 0 && pass == 0 && ri == (int)blockIdx.x);
-    // misses in ascending selection order, and the unpinned entries of the LRU list
-    const int per_i = (kx + NT - 1) / NT;
-    const int i0 = min(kx, tid * per_i), i1 = min(kx, i0 + per_i);
-    const int per_j = (B + NT - 1) / NT;
-    const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
+    // misses in ascending selection order, and the unpinned entries of the LRU
+    // list: warp w takes the w-th contiguous segment of each, counts it by ballots
+    // (lane-strided: no shared-memory bank conflicts), one block scan places the
+    // segments, and each warp emits its own in order
+    const unsigned lt = (1u << lane) - 1u;
+    const int segi = (kx + NT - 1) / NT * 32, segj = (B + NT - 1) / NT * 32;
+    const int wi0 = min(kx, warp * segi), wi1 = min(kx, wi0 + segi);
+    const int wj0 = min(B, warp * segj), wj1 = min(B, wj0 + segj);
+    const bool lru_list = p.replacement != HS_REPLACE_RANDOM;
     int nm = 0, nc = 0;
-    for (int i = i0; i < i1; ++i) nm += slot_sel[i] < 0;
-    for (int j = j0; j < j1; ++j) nc += used[ord[j]] == 0;
-    const int2 mc = block_exclusive_scan2<NT>(nm, nc, sh.scan, &m, nullptr);
-    int mb = mc.x;
+#pragma unroll 4
+    for (int i = wi0; i < wi1; i += 32) nm += __popc(__ballot_sync(FULL_MASK, i + lane < wi1 && slot_sel[i + lane] < 0));
+    if (lru_list) {
+#pragma unroll 4
+      for (int j = wj0; j < wj1; j += 32)
+        nc += __popc(__ballot_sync(FULL_MASK, j + lane < wj1 && used[ord[j + lane]] == 0));
+    }
+    const int2 mc = block_exclusive_scan2<NT>(lane == 0 ? nm : 0, lane == 0 ? nc : 0, sh.scan, &m, nullptr);
+    int mb = __shfl_sync(FULL_MASK, mc.x, 0);
     // the misses the attention kernel will fetch go to its prefetcher at once
     const bool list_misses = pass == 0 && !pull && p.publish;
     int32_t* mpos = p.s.miss_pos + (long long)ri * KR;
-    for (int i = i0; i < i1; ++i)
-      if (slot_sel[i] < 0) {
-        if (list_misses && i < kk) mpos[mb] = (!paged && appended && sel[i] == len) ? -1 : sel[i];
-        miss_i[mb++] = i;
+    for (int i = wi0; i < wi1; i += 32) {
+      const int ii = i + lane;
+      const bool miss = ii < wi1 && slot_sel[ii] < 0;
+      const unsigned bal = __ballot_sync(FULL_MASK, miss);
+      if (miss) {
+        const int at = mb + __popc(bal & lt);
+        if (list_misses && ii < kk) mpos[at] = (!paged && appended && sel[ii] == len) ? -1 : sel[ii];
+        miss_i[at] = ii;
       }
+      mb += __popc(bal);
+    }
     if (p.replacement == HS_REPLACE_RANDOM) {
       // victims: the m unpinned slots ranked first (never-filled, then smallest
       // (key, slot)), in ascending slot order.  Two 12-bit digit selections over
@@ -1214,6 +1247,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       // and, in slot order, the threshold ties still needed.  "Never filled" is
       // read from the reverse map as it was before this call.
       if (m > 0) {
+        const int per_j = (B + NT - 1) / NT;   // a contiguous range of slots per thread
+        const int j0 = min(B, tid * per_j), j1 = min(B, j0 + per_j);
         const unsigned long long seed = p.replacement_seed;
         auto rank_of = [&](int j) {
           const int old = L.rev_smem ? rev_s[j] : reverse[j];
@@ -1259,13 +1294,20 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
     } else {
       // victims: the first m unpinned entries of the (stamp, slot)-sorted list
-      int cb = mc.y;
-      for (int j = j0; j < j1 && cb < m; ++j) {
-        const int sl = ord[j];
-        if (used[sl] == 0) {
-          victim[cb++] = sl;
-          used[sl] = 2;
+      int cb = __shfl_sync(FULL_MASK, mc.y, 0);
+      for (int j = wj0; j < wj1 && cb < m; j += 32) {   // warp-uniform
+        const int jj = j + lane;
+        const int sl = jj < wj1 ? ord[jj] : 0;
+        const bool fr = jj < wj1 && used[sl] == 0;
+        const unsigned bal = __ballot_sync(FULL_MASK, fr);
+        if (fr) {
+          const int at = cb + __popc(bal & lt);
+          if (at < m) {
+            victim[at] = sl;
+            used[sl] = 2;
+          }
         }
+        cb += __popc(bal);
       }
     }
     __syncthreads();
@@ -1466,19 +1508,29 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       }
       // new list: slots not refreshed keep their order, refreshed slots (all with
       // the newest stamp) go last by slot
+      // (the same warp segments as above: the list's entries and the slots)
       int nu = 0, nus = 0;
-      for (int j = j0; j < j1; ++j) nu += !refreshed(used[ord[j]]);
-      for (int sl = j0; sl < j1; ++sl) nus += refreshed(used[sl]);
-      int n_unused;
-      const int2 un = block_exclusive_scan2<NT>(nu, nus, sh.scan, &n_unused, nullptr);
-      int ub = un.x;
-      for (int j = j0; j < j1; ++j) {
-        const int sl = ord[j];
-        if (!refreshed(used[sl])) order[ub++] = sl;
+      for (int j = wj0; j < wj1; j += 32) {
+        const int jj = j + lane;
+        nu += __popc(__ballot_sync(FULL_MASK, jj < wj1 && !refreshed(used[ord[jj]])));
+        nus += __popc(__ballot_sync(FULL_MASK, jj < wj1 && refreshed(used[jj])));
       }
-      int sb = n_unused + un.y;
-      for (int sl = j0; sl < j1; ++sl)
-        if (refreshed(used[sl])) order[sb++] = sl;
+      int n_unused;
+      const int2 un = block_exclusive_scan2<NT>(lane == 0 ? nu : 0, lane == 0 ? nus : 0, sh.scan, &n_unused, nullptr);
+      int ub = __shfl_sync(FULL_MASK, un.x, 0);
+      int sb = n_unused + __shfl_sync(FULL_MASK, un.y, 0);
+      for (int j = wj0; j < wj1; j += 32) {
+        const int jj = j + lane;
+        const int sl = jj < wj1 ? ord[jj] : 0;
+        const bool keep = jj < wj1 && !refreshed(used[sl]);
+        const unsigned bk = __ballot_sync(FULL_MASK, keep);
+        if (keep) order[ub + __popc(bk & lt)] = sl;
+        ub += __popc(bk);
+        const bool rf = jj < wj1 && refreshed(used[jj]);
+        const unsigned br = __ballot_sync(FULL_MASK, rf);
+        if (rf) order[sb + __popc(br & lt)] = jj;
+        sb += __popc(br);
+      }
       if (tid == 0) {
         p.s.step[rlx] = t + 1;
         // counters of the selected positions (an allocated new token is neither)
