@@ -792,7 +792,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_gqa_kernel(DecodeParams p, in
     if (item >= p.n_req * NHG) break;
     const int r = item / NHG, h0 = (item % NHG) * HPM;
     if (tid == 0) {
-      s_ok = wait_counter(p.s.att_done + r, (unsigned)NCHK) ? 1 : 0;
+      // a chunk of this request may sit behind a chunk whose own request was
+      // never published (its loader gives up after WAIT_LIMIT_NS and goes on), so
+      // this wait outlasts that one
+      s_ok = wait_counter(p.s.att_done + r, (unsigned)NCHK, 4 * WAIT_LIMIT_NS) ? 1 : 0;
       if (!s_ok) set_error(p.s.dev_error, HS_DEVERR_TIMEOUT);
     }
     __syncthreads();

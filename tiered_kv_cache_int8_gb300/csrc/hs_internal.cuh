@@ -431,8 +431,10 @@ __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
   return v;
 }
 // Spins until *p >= target (acquire), backing off from 32 ns to 512 ns between
-// polls (many CTAs may poll one flag); gives up after WAIT_LIMIT_NS and returns false.
-__device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int target) {
+// polls (many CTAs may poll one flag); gives up after limit_ns (WAIT_LIMIT_NS
+// unless given) and returns false.
+__device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int target,
+                                             unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (ld_acquire(p) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
   unsigned ns = 32;
@@ -440,7 +442,7 @@ __device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int
     __nanosleep(ns);
     if (ns < 512) ns <<= 1;
     if (ld_acquire(p) >= target) return true;
-    if ((it & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 // Named barrier over `n` threads (a multiple of 32) of the CTA.
