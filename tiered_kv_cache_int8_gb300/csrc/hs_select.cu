@@ -51,8 +51,9 @@
 //       lists in position order) over the scratch keys.  Either way the
 //       selection is emitted ascending from bitmaps.
 //     - RESOLVE: hit test through the page table (on the candidate path the page
-//       entries come with the candidates; else independent gathers),
-//       miss compaction with block scans, victims from an explicit LRU list kept
+//       entries come with the candidates, read by the scorers; else independent
+//       gathers), miss compaction by warp segments (ballots, one block scan),
+//       victims from an explicit LRU list kept
 //       sorted by (stamp, slot) — a call moves exactly the slots it used to the
 //       most recent end, so two stable compactions maintain it: no sort, no heap.
 //     - publication: selection, slot of every selected row (misses flagged for
