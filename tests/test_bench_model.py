@@ -1,8 +1,8 @@
 """bench.py's host logic on CPU: the algorithmic-traffic model (the missed rows'
 host reads and slot writes are charged to the kernel that copies them, totals do
 not depend on which one that is), the code hash that keys the committed ncu
-figures, the package's Belady MIN against the oracle's, and the reference arm's
-JSON line."""
+figures, the package's Belady MIN against the oracle's, the reference arm's
+JSON line, and the attention timeline derived from two hs_stats snapshots."""
 import os
 
 import numpy as np
@@ -133,3 +133,22 @@ def test_bench_names_resolve():
     local |= {f.name for f in ast.walk(tree) if isinstance(f, ast.FunctionDef)}
     missing = sorted(c for c in called if c not in defined and c not in local and not hasattr(builtins, c))
     assert not missing, missing
+
+
+def test_attention_timeline_from_two_snapshots():
+    # the exposed link time is the host stages' waits beyond the mean wait of an
+    # HBM-only stage; the balance figures come from the later snapshot; latent rows
+    # (no counts) report nothing
+    import bench
+    keys = ("att_host_wait_ns", "att_host_stages", "att_hbm_wait_ns", "att_hbm_stages", "att_last_span_ns",
+            "att_last_median_ns")
+    st0 = dict(zip(keys, (1000, 1, 500, 1, 7, 7)))
+    st1 = dict(zip(keys, (1000 + 4 * 3000, 1 + 4, 500 + 10 * 1000, 1 + 10, 60000, 50000)))
+    t = bench.attention_timeline(st0, st1, n_launch=2, n_cta=2)
+    assert t["host_stage_wait_us"] == 3.0 and t["hbm_stage_wait_us"] == 1.0
+    # 4 host stages waited 12 us where HBM-only stages would have taken 4 us: 8 us
+    # over 2 launches x 2 CTAs
+    assert t["link_exposed_us_per_cta_layer"] == 2.0
+    assert t["host_stages_per_cta_layer"] == 1.0
+    assert t["last_launch_span_us"] == 60.0 and t["span_over_median"] == 1.2
+    assert bench.attention_timeline(st1, st1, 2, 2) is None
