@@ -696,6 +696,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     const bool use_cand = sh.ok && N > K && L.fast && N <= FAST_MAX_N && sh.thr != 0u &&
                           sh.cnt >= K && sh.cnt <= min(2 * K, CAND_REG * NT);
     bool slots_known = false;   // the candidate path reads each selected position's page entry itself
+    // the candidate path (rows, not pages) also writes the selection, marks the
+    // hits used and writes their slots as it emits them: no later passes for those
+    bool emitted_out = false, bad_pre = false;
     // the next call lists keys at or above the exact key of rank 1.5 k (found after
     // publication): about 1.5 k of them, half way between k and the list's room
     const int k_next = (int)min((long long)N, (long long)K + K / 2);
@@ -796,9 +799,20 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
             const int idx = gb + min(eb, need_eq);
             sel[idx] = (int)pp;
             slot_sel[idx] = cpg[j];
+            if (!paged) {
+              p.s.sel[(long long)ri * KR + idx] = (int)pp;
+              const int s4 = cpg[j];
+              if (s4 >= B) {
+                bad_pre = true;
+              } else if (s4 >= 0) {
+                used[s4] = 1;
+                p.s.slot_of_sel[(long long)ri * KR + idx] = s4;
+              }
+            }
           }
         }
       slots_known = true;
+      emitted_out = !paged;
     } else if (NH > 1) {
       // the multi-head indexer's 32-bit keys: three digits (12, 12 and 8 bits),
       // each found by a histogram pass over the keys of the digits above it, then
@@ -1119,7 +1133,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     // after publication
     auto row_pos = [&](int i) { return paged ? (sel[i >> psh] << psh) + (i & (PS - 1)) : sel[i]; };
     int32_t* sel_g = p.s.sel + (long long)ri * KR;
-    for (int i = tid; i < kkr; i += NT) sel_g[i] = row_pos(i);
+    if (!emitted_out)
+      for (int i = tid; i < kkr; i += NT) sel_g[i] = row_pos(i);
 
     // ======================= 2. RESOLVE metadata =======================
     // pass 0: this call's layer.  Passes 1..n_follow: the follower layers of its
@@ -1160,11 +1175,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
     const bool pull = pass > 0 || p.fetch_mode == 1;
     bool bad = false;
     if (kk > 0 && slots_known && pass == 0) {
-      for (int i = tid; i < kk; i += NT) {
-        const int s4 = slot_sel[i];
-        if (s4 >= B) bad = true;
-        if (s4 >= 0 && s4 < B) used[s4] = 1;
-      }
+      bad = bad_pre;
+      if (!emitted_out)
+        for (int i = tid; i < kk; i += NT) {
+          const int s4 = slot_sel[i];
+          if (s4 >= B) bad = true;
+          if (s4 >= 0 && s4 < B) used[s4] = 1;
+        }
     } else if (kk > 0) {
       // hit test: independent page-table gathers, four in flight per thread
       for (int i0 = tid; i0 < kk; i0 += 4 * NT) {
@@ -1182,7 +1199,10 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
           if (i < kk) {
             if (pos[u] < 0 || pos[u] >= N || s4[u] >= B) bad = true;
             slot_sel[i] = s4[u];
-            if (s4[u] >= 0 && s4[u] < B) used[s4[u]] = 1;
+            if (s4[u] >= 0 && s4[u] < B) {
+              used[s4[u]] = 1;
+              if (pass == 0 && !paged) sos[i] = s4[u];   // a hit's slot (misses get theirs below)
+            }
           }
         }
       }
@@ -1330,13 +1350,13 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(DecodeParams p) {
       // Page mode: a page is flagged whole; its appended row is left out below.
       if (pass == 0) miss_i[qq] = (pull || (!paged && appended && pnew == len)) ? i : (i | HS_SLOT_MISS_FLAG);
       else miss_i[qq] = (appended && pnew == len) ? (i | HS_SLOT_MISS_FLAG) : i;
+      // a missed row's slot, flagged when the attention kernel copies it (the
+      // hits' slots were written with the hit test)
+      if (pass == 0 && !paged && i < kk) sos[i] = (miss_i[qq] & HS_SLOT_MISS_FLAG) ? (v | HS_SLOT_MISS_FLAG) : v;
     }
     __syncthreads();
     if (pass == 0 && !paged) {
-      for (int i = tid; i < kk; i += NT) sos[i] = slot_sel[i];
-      __syncthreads();
-      for (int qq = tid; qq < m; qq += NT)
-        if (miss_i[qq] & HS_SLOT_MISS_FLAG) sos[miss_i[qq] & ~HS_SLOT_MISS_FLAG] = victim[qq] | HS_SLOT_MISS_FLAG;
+      // every selected row's slot is written
     } else if (pass == 0) {
       // page mode: row i of the expansion is row i % PS of page slot slot_sel[i / PS]
       for (int i = tid; i < kkr; i += NT) sos[i] = (slot_sel[i >> psh] << psh) + (i & (PS - 1));
