@@ -37,11 +37,12 @@
 //    as early as the misses are known, and the fetchers later read L2.  (A bulk prefetch of host memory can hold its issuing thread for
 //    microseconds, so it runs on a warp of its own.)
 //  * Warps 0-7 consume: warp w serves kv head w % h_kv and row slice w / h_kv.
-//    S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate)
-//    with the group's query heads as the 16 M rows (zero-padded); K and V
-//    fragments come from shared memory with ldmatrix (.trans for V).  Online
-//    softmax in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P enters
-//    the second product as bf16.  Once a unit has landed, the fetcher writes the
+//    S^T = K Q^T and O^T += V^T P^T run on mma.sync m16n8k16 (bf16 in, fp32
+//    accumulate) with the unit's 16 rows as M and the group's query heads as N
+//    (8 per n-tile); K and V fragments come from shared memory with ldmatrix
+//    (.trans for V), P^T moves into the A layout by movmatrix.  Online softmax
+//    per head in fp32 (exp2, scale * log2(e) applied to the fp32 scores); P
+//    enters the second product as bf16.  Once a unit has landed, the fetcher writes the
 //    rows it fetched into their hot slots (bulk shared -> global copy), so later
 //    steps hit; a stage is released by the 8 consumers and the fetcher.
 //  * Each (chunk, slice) writes a partial (m, l, o) and counts its chunk done
